@@ -1,0 +1,65 @@
+"""DSA-style sparse decode and the Quest page bound (fp64).  Test only.
+
+Follows "Long context, KV eviction and sparse attention":
+  * DSA paragraph: a light indexer with few heads scores every past token;
+    each query then runs full attention over only its 2048 best-scored
+    tokens.  The indexer score read here is the ReLU-weighted dot
+    I[s] = sum_j w_j * ReLU(q^I_j . k^I_s) over the indexer heads j, with
+    one shared indexer key per token and one selected set per (sequence,
+    step) shared by every q head; bf16 inputs, not FP8.
+  * sparse-selection section: restricting a query to a selected set means
+    masking every other logit to -inf before the softmax; "exact top-k" keeps
+    each query's k largest logits; Quest bounds a page's logit by
+    sum_d max(q_d * kmin_d, q_d * kmax_d) and keeps the best pages.
+Ties in a top-k go to the lower position; the selected set is reported in
+ascending order; with S <= k every position is selected.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .attention import softmax
+from .h2o import topk_positions
+
+
+def indexer_scores(q_idx: np.ndarray, w: np.ndarray, k_idx: np.ndarray) -> np.ndarray:
+    """I[s] = sum_j w[j] * max(0, q_idx[j] . k_idx[s]).  q_idx [Hi][Di], k_idx [S][Di]."""
+    dots = k_idx @ q_idx.T                  # [S][Hi]
+    return np.maximum(dots, 0.0) @ w
+
+
+def select_topk(I: np.ndarray, k: int) -> np.ndarray:
+    return topk_positions(I, k)
+
+
+def masked_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, sel: np.ndarray, scale: float):
+    """Attention of every q head over the selected positions only.
+
+    q [Hq][d]; K, V [Hkv][S][d]; sel: ascending positions shared by all heads.
+    Returns o [Hq][d].
+    """
+    Hq, d = q.shape
+    Hkv = K.shape[0]
+    G = Hq // Hkv
+    o = np.zeros((Hq, d))
+    for h in range(Hq):
+        kvh = h // G
+        p = softmax((K[kvh, sel] @ q[h]) * scale)
+        o[h] = p @ V[kvh, sel]
+    return o
+
+
+def sparse_decode_step(q, K, V, q_idx, w, k_idx, top_k, scale):
+    """Indexer scores -> top-k -> attention over the selection.  Returns (o, sel, I)."""
+    I = indexer_scores(q_idx, w, k_idx)
+    sel = select_topk(I, top_k)
+    return masked_attention(q, K, V, sel, scale), sel, I
+
+
+def quest_page_bound(q: np.ndarray, K: np.ndarray, page: int = 16) -> np.ndarray:
+    """Upper bound of q.k over each full page of K [S][d]: sum_d max(q*kmin, q*kmax)."""
+    S, d = K.shape
+    n = S // page
+    pages = K[:n * page].reshape(n, page, d)
+    kmin, kmax = pages.min(axis=1), pages.max(axis=1)
+    return np.maximum(q[None, :] * kmin, q[None, :] * kmax).sum(axis=1)
