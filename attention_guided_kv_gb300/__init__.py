@@ -1,0 +1,229 @@
+"""Python binding of libkvsel.so (attention-guided KV selection on GB300).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+their dtype/device/contiguity, and hands raw device pointers and the current
+stream to the C ABI declared in ``include/kvsel.h``.  Every step of the path
+runs in the library's CUDA kernels; there is no CPU or PyTorch fallback.  If
+the shared library is missing this module raises instead of degrading.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvsel.so")
+
+KVSEL_OK = 0
+KVSEL_ERR_INVALID_ARG = 1
+KVSEL_ERR_UNSUPPORTED = 2
+KVSEL_ERR_CUDA = 3
+KVSEL_ERR_TIMEOUT = 4
+KVSEL_ERR_BAD_INDEX = 5
+KVSEL_BF16 = 0
+KVSEL_F32 = 1
+
+_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT", 5: "BAD_INDEX"}
+
+
+class KvselError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"kvsel status {_STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class PagedKV(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32)]
+
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_PKV = ctypes.POINTER(PagedKV)
+
+# name -> (restype, argtypes)
+_SIGS = {
+    "kvsel_last_error_string": (ctypes.c_char_p, []),
+    "kvsel_clear_status": (_i, [_vp, _vp]),
+    "kvsel_read_status": (_i, [_vp, _vp]),
+    "kvsel_trace_start": (_i, [ctypes.POINTER(ctypes.c_void_p), _i]),
+    "kvsel_trace_stop": (_i, [ctypes.POINTER(ctypes.c_char_p), _i]),
+    "kvsel_decode_attn_workspace": (_sz, [_PKV, _i, _i, _i]),
+    "kvsel_decode_attn": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _f, _vp, _i, _vp,
+                               _vp, _i, _i, _vp, _sz, _vp]),
+    "kvsel_h2o_evict_workspace": (_sz, [_PKV, _i, _i]),
+    "kvsel_h2o_evict": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp,
+                             _sz, _vp]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkvsel.so once (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(nvcc, sm_103a); there is no fallback path")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _check(code: int):
+    if code != KVSEL_OK:
+        raise KvselError(code, lib().kvsel_last_error_string().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, allow_none=False):
+    if t is None:
+        if allow_none:
+            return
+        raise ValueError(f"{name} is required")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def paged_kv(k_pool: torch.Tensor, v_pool: torch.Tensor, num_q_heads: int) -> PagedKV:
+    """Descriptor of bf16 pools shaped [num_pages][num_kv_heads][page_size][head_dim]."""
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(v_pool, torch.bfloat16, "v_pool")
+    if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
+        raise ValueError("k_pool and v_pool must share one [pages][Hkv][page][d] shape")
+    P, H, pg, d = k_pool.shape
+    return PagedKV(k_pool.data_ptr(), v_pool.data_ptr(), P, H, num_q_heads, d, pg)
+
+
+def clear_status(workspace: torch.Tensor, stream=None):
+    _check(lib().kvsel_clear_status(_ptr(workspace), _stream(stream)))
+
+
+def read_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise and return (and clear) the device status word of a workspace."""
+    return int(lib().kvsel_read_status(_ptr(workspace), _stream(stream)))
+
+
+class LaunchTrace:
+    """Record CUDA events around every library kernel launched by this thread.
+
+    with LaunchTrace(capacity) as tr: ...   then tr.durations() -> [(name, ms)].
+    """
+
+    def __init__(self, capacity: int):
+        self.capacity = capacity
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for e in self.events:
+            e.record()                       # materialise the cudaEvent_t handles
+        self._handles = (ctypes.c_void_p * (2 * capacity))(*[e.cuda_event for e in self.events])
+        self.names = []
+
+    def __enter__(self):
+        _check(lib().kvsel_trace_start(self._handles, self.capacity))
+        return self
+
+    def __exit__(self, *exc):
+        buf = (ctypes.c_char_p * self.capacity)()
+        n = lib().kvsel_trace_stop(buf, self.capacity)
+        self.names = [buf[i].decode() for i in range(min(n, self.capacity))]
+        return False
+
+    def durations(self):
+        torch.cuda.synchronize()
+        return [(nm, self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
+                for i, nm in enumerate(self.names)]
+
+
+# ----------------------------------------------------------------------------
+# decode attention
+# ----------------------------------------------------------------------------
+def kvsel_decode_attn_workspace(kv: PagedKV, batch: int, max_len: int, with_probs: bool) -> int:
+    return int(lib().kvsel_decode_attn_workspace(ctypes.byref(kv), batch, max_len, int(with_probs)))
+
+
+def kvsel_decode_attn(kv: PagedKV, block_table, seq_lens, q, out, workspace, *, k_new=None,
+                      v_new=None, pos_map=None, next_pos=None, scale=None, probs=None,
+                      h2o_cum=None, max_len=None, num_splits=0, stream=None):
+    """Append (optional) + decode attention + probabilities + H2O score update."""
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(q, torch.bfloat16, "q")
+    _need(k_new, torch.bfloat16, "k_new", True)
+    _need(v_new, torch.bfloat16, "v_new", True)
+    _need(pos_map, torch.int32, "pos_map", True)
+    _need(next_pos, torch.int32, "next_pos", True)
+    _need(probs, torch.float32, "probs", True)
+    _need(h2o_cum, torch.float32, "h2o_cum", True)
+    _need(workspace, workspace.dtype, "workspace")
+    if out.dtype not in (torch.bfloat16, torch.float32) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 or fp32 CUDA tensor")
+    batch = seq_lens.shape[0]
+    if max_len is None:
+        for t in (probs, h2o_cum, pos_map):
+            if t is not None:
+                max_len = t.shape[-1]
+                break
+        else:
+            max_len = block_table.shape[1] * kv.page_size
+    if scale is None:
+        scale = kv.head_dim ** -0.5
+    odt = KVSEL_F32 if out.dtype == torch.float32 else KVSEL_BF16
+    _check(lib().kvsel_decode_attn(
+        ctypes.byref(kv), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch, _ptr(q),
+        _ptr(k_new), _ptr(v_new), _ptr(pos_map), _ptr(next_pos), float(scale), _ptr(out), odt,
+        _ptr(probs), _ptr(h2o_cum), int(max_len), int(num_splits), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------
+# H2O select / evict
+# ----------------------------------------------------------------------------
+def kvsel_h2o_evict_workspace(kv: PagedKV, batch: int, budget: int) -> int:
+    return int(lib().kvsel_h2o_evict_workspace(ctypes.byref(kv), batch, budget))
+
+
+def kvsel_h2o_evict(kv: PagedKV, block_table, seq_lens, h2o_cum, workspace, *, budget, n_sink,
+                    window, compact=False, pos_map=None, keep_out=None, freed_pages=None,
+                    stream=None):
+    """H2O heavy hitters + StreamingLLM sinks/window; optional in-place compaction."""
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(h2o_cum, torch.float32, "h2o_cum")
+    _need(pos_map, torch.int32, "pos_map", True)
+    _need(keep_out, torch.int32, "keep_out", True)
+    _need(freed_pages, torch.int32, "freed_pages", True)
+    batch = seq_lens.shape[0]
+    _check(lib().kvsel_h2o_evict(
+        ctypes.byref(kv), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch,
+        _ptr(h2o_cum), _ptr(pos_map), h2o_cum.shape[-1], int(budget), int(n_sink), int(window),
+        int(bool(compact)), _ptr(keep_out), _ptr(freed_pages), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zeroed, 256-byte aligned workspace buffer (status word cleared)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)

@@ -1,0 +1,180 @@
+/*
+ * kvsel.h - attention-guided KV selection on one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libkvsel.so.  Every entry point validates its arguments on the
+ * host, then enqueues hand-written CUDA kernels on the caller's stream and
+ * returns without synchronising.  Conventions shared by all calls:
+ *
+ *  - Pointers are DEVICE pointers owned by the caller unless stated
+ *    otherwise.  The library allocates no device memory: scratch comes from
+ *    a caller-provided workspace whose size the matching *_workspace()
+ *    function returns.
+ *  - The first 256 bytes of every workspace hold a device status word.  It
+ *    must be zero when a workspace is first used (allocate it zeroed, or
+ *    call kvsel_clear_status).  Kernels that detect a problem on the device
+ *    (a block-table entry outside the pool, a bounded wait that ran out)
+ *    record a kvsel_status there and carry on without faulting;
+ *    kvsel_read_status() returns it.
+ *  - Host-detectable errors (NULL where a buffer is required, unsupported
+ *    head_dim / page_size / group size, a budget smaller than sinks +
+ *    window, a workspace that is too small) return immediately with no
+ *    launch, and kvsel_last_error_string() describes them.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *  - No C++ exception crosses this interface.
+ *
+ * Paged KV layout (the paged cache of "From sliding window to
+ * attention-guided eviction" §5, blocks of 16 tokens): K and V pools are
+ * separate bf16 arrays [num_pages][num_kv_heads][page_size][head_dim]; a
+ * sequence owns the pages listed in its row of an int32 block table
+ * [batch][max_pages]; token slot t of sequence b lives in page
+ * block_table[b][t / page_size], row t % page_size.  Supported here:
+ * head_dim = 128, page_size = 16, num_q_heads / num_kv_heads <= 8.
+ */
+#ifndef KVSEL_H
+#define KVSEL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVSEL_API __attribute__((visibility("default")))
+#else
+#define KVSEL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvsel_status {
+  KVSEL_OK = 0,
+  KVSEL_ERR_INVALID_ARG = 1, /* rejected on the host; nothing was launched       */
+  KVSEL_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement */
+  KVSEL_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, attribute)   */
+  KVSEL_ERR_TIMEOUT = 4,     /* device: a bounded wait ran out                   */
+  KVSEL_ERR_BAD_INDEX = 5    /* device: a block-table entry outside the pool     */
+} kvsel_status;
+
+typedef enum kvsel_dtype { KVSEL_BF16 = 0, KVSEL_F32 = 1 } kvsel_dtype;
+
+typedef struct kvsel_paged_kv {
+  void* k_pool;          /* bf16 [num_pages][num_kv_heads][page_size][head_dim] */
+  void* v_pool;          /* bf16, same layout                                   */
+  int32_t num_pages;
+  int32_t num_kv_heads;
+  int32_t num_q_heads;   /* q head h reads kv head h / (num_q_heads/num_kv_heads) */
+  int32_t head_dim;      /* 128                                                 */
+  int32_t page_size;     /* 16                                                  */
+} kvsel_paged_kv;
+
+/* Human-readable reason for the last non-OK status returned on this thread. */
+KVSEL_API const char* kvsel_last_error_string(void);
+
+/* Zero the status word of `workspace` (async on `stream`). */
+KVSEL_API kvsel_status kvsel_clear_status(void* workspace, void* stream);
+
+/* Synchronise `stream`, return the device status recorded in `workspace`
+ * since it was last cleared, and clear it. */
+KVSEL_API kvsel_status kvsel_read_status(void* workspace, void* stream);
+
+/* Launch tracing for profiling.  While tracing is on for the calling thread,
+ * every kernel the library launches from that thread records
+ * events[2i] just before and events[2i+1] just after launch i, on the launch
+ * stream.  `events` holds 2*capacity cudaEvent_t handles created by the
+ * caller; launches past `capacity` are not recorded. */
+KVSEL_API kvsel_status kvsel_trace_start(void* const* events, int capacity);
+/* Stop tracing.  Returns the number of launches recorded and, when `names`
+ * is non-NULL, stores up to `capacity` static kernel-name strings there. */
+KVSEL_API int kvsel_trace_stop(const char** names, int capacity);
+
+/* ---------------------------------------------------------------------------
+ * Score-emitting decode attention (append + split-K attention + H2O update).
+ *
+ * Defines ("From sliding window to attention-guided eviction" §3.1 and §4.2
+ * step 1; "Long context, KV eviction and sparse attention", sparse-selection
+ * section, for the d^-1/2 scale and the q-head -> kv-head grouping):
+ *   for each sequence b (live length S_b after the optional append) and
+ *   q head h with kv head g = h / G:
+ *     s_j  = scale * q_h . K_g[j]            for j < S_b
+ *     p_hj = exp(s_j - max s) / sum exp(s - max s)
+ *     o_h  = sum_j p_hj V_g[j]
+ *     cum[b][g][j] += sum_{h in group g} p_hj      (the H2O cumulative score)
+ *
+ * Arguments:
+ *   kv           paged pools (read; the appended token is written).
+ *   block_table  int32 [batch][max_pages], read only.
+ *   seq_lens     int32 [batch]: in, live length before the append; out, +1
+ *                when k_new/v_new are given (written by the last kernel).
+ *   q            bf16 [batch][num_q_heads][head_dim].
+ *   k_new,v_new  bf16 [batch][num_kv_heads][head_dim], or both NULL (no
+ *                append).  The new token goes to slot seq_lens[b] and is
+ *                attended in the same call.
+ *   pos_map      int32 [batch][num_kv_heads][max_len] or NULL: slot -> original
+ *                token position; the appended slot gets next_pos[b].
+ *   next_pos     int32 [batch] or NULL: original position of the next token;
+ *                incremented with the append.  Required if pos_map is given.
+ *   scale        logit scale (head_dim^-1/2 for standard attention).
+ *   out          [batch][num_q_heads][head_dim], bf16 or fp32 per out_dtype.
+ *   probs        fp32 [batch][num_q_heads][max_len] or NULL: p_hj at slot j;
+ *                entries j >= S_b are not written.
+ *   h2o_cum      fp32 [batch][num_kv_heads][max_len] or NULL: updated in
+ *                place; the appended slot starts from 0.
+ *   max_len      capacity in slots of probs / h2o_cum / pos_map rows; every
+ *                S_b (after the append) must be <= max_len and
+ *                <= max_pages * page_size.
+ *   num_splits   key splits per (sequence, kv head); 0 = choose from the SM
+ *                count.  Results do not depend on it beyond fp32 rounding.
+ *   workspace    >= kvsel_decode_attn_workspace(...) bytes, status word zeroed.
+ * Returns KVSEL_OK once the kernels are enqueued.
+ */
+KVSEL_API size_t kvsel_decode_attn_workspace(const kvsel_paged_kv* kv, int batch, int max_len,
+                                   int with_probs);
+KVSEL_API kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_t* block_table,
+                               int max_pages, int32_t* seq_lens, int batch, const void* q,
+                               const void* k_new, const void* v_new, int32_t* pos_map,
+                               int32_t* next_pos, float scale, void* out, int out_dtype,
+                               float* probs, float* h2o_cum, int max_len, int num_splits,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * H2O heavy-hitter selection with StreamingLLM sinks + window, optional
+ * in-place compaction.
+ *
+ * Defines ("From sliding window to attention-guided eviction" §4.1 and the
+ * §4.2 pseudocode; "Long context, KV eviction and sparse attention",
+ * StreamingLLM section): for each sequence b and kv head g with live length
+ * S = seq_lens[b]:
+ *   if S <= budget nothing is evicted; otherwise
+ *   keep = [0, n_sink) U HH U [S - window, S), where HH is the
+ *   (budget - n_sink - window) slots of [n_sink, S - window) with the
+ *   largest h2o_cum[b][g][.], ties to the lower slot.
+ * With budget = n_sink + window this is StreamingLLM; with n_sink = 0 as
+ * well it is the sliding window.
+ *
+ * Arguments:
+ *   kv, block_table  pools and table; modified only when compact != 0.
+ *   seq_lens     int32 [batch]; when compact != 0 set to min(S, budget).
+ *   h2o_cum      fp32 [batch][num_kv_heads][max_len] (read; compacted).
+ *   pos_map      int32 [batch][num_kv_heads][max_len] or NULL (compacted).
+ *   budget, n_sink, window   budget >= n_sink + window, n_sink,window >= 0.
+ *   compact      0: select only.  1: also move the kept K/V rows, scores and
+ *                positions to slots 0..n_keep-1 in order, set block-table
+ *                entries from ceil(n_keep/page_size) up to the old page count
+ *                to -1 and list those page ids in freed_pages.
+ *   keep_out     int32 [batch][num_kv_heads][budget] or NULL: kept original
+ *                positions (pos_map applied; slot indices if pos_map is
+ *                NULL), ascending, padded with -1.
+ *   freed_pages  int32 [batch][max_pages] or NULL: released page ids, -1 padded.
+ *   workspace    >= kvsel_h2o_evict_workspace(...) bytes, status word zeroed.
+ */
+KVSEL_API size_t kvsel_h2o_evict_workspace(const kvsel_paged_kv* kv, int batch, int budget);
+KVSEL_API kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block_table, int max_pages,
+                             int32_t* seq_lens, int batch, float* h2o_cum, int32_t* pos_map,
+                             int max_len, int budget, int n_sink, int window, int compact,
+                             int32_t* keep_out, int32_t* freed_pages, void* workspace,
+                             size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVSEL_H */

@@ -1,0 +1,93 @@
+"""Helpers shared by the GPU tests: upload seeded workloads, drive the C ABI.
+
+Nothing here computes the method: inputs come from ``workloads`` and
+expected values from ``oracle``.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import attention_guided_kv_gb300 as K
+import workloads
+
+
+def bf16(bits, dev="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def rel_l2(x, ref) -> float:
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    n = np.linalg.norm(ref)
+    return float(np.linalg.norm(x - ref) / (n if n > 0 else 1.0))
+
+
+class DecodeState:
+    """Device-side paged cache + bookkeeping for a DecodeWorkload."""
+
+    def __init__(self, wl: workloads.DecodeWorkload, with_probs=True, with_pos=True,
+                 out_f32=True, spare_pages=0, dev="cuda"):
+        self.wl = wl
+        self.dev = dev
+        npages = wl.num_pages + spare_pages
+        self.kpool = bf16(workloads.paged_pool(wl.K, wl.block_table, npages), dev)
+        self.vpool = bf16(workloads.paged_pool(wl.V, wl.block_table, npages), dev)
+        self.kv = K.paged_kv(self.kpool, self.vpool, wl.Hq)
+        self.bt_host = wl.block_table.copy()
+        self.bt = torch.from_numpy(self.bt_host).to(dev)
+        self.free = list(range(wl.num_pages, npages))
+        self.S = np.full(wl.B, wl.S0, dtype=np.int64)
+        self.seq = torch.from_numpy(self.S.astype(np.int32)).to(dev)
+        self.cum = torch.zeros(wl.B, wl.Hkv, wl.max_len, device=dev)
+        self.probs = torch.zeros(wl.B, wl.Hq, wl.max_len, device=dev) if with_probs else None
+        if with_pos:
+            pos = np.tile(np.arange(wl.max_len, dtype=np.int32), (wl.B, wl.Hkv, 1))
+            self.pos = torch.from_numpy(pos).to(dev)
+            self.next_pos = torch.full((wl.B,), wl.S0, dtype=torch.int32, device=dev)
+        else:
+            self.pos = self.next_pos = None
+        self.out = torch.zeros(wl.B, wl.Hq, wl.d, device=dev,
+                               dtype=torch.float32 if out_f32 else torch.bfloat16)
+        self.ws = K.workspace(K.kvsel_decode_attn_workspace(self.kv, wl.B, wl.max_len, with_probs))
+        self.ws_ev = K.workspace(K.kvsel_h2o_evict_workspace(self.kv, wl.B, wl.budget))
+        self.keep = torch.full((wl.B, wl.Hkv, wl.budget), -1, dtype=torch.int32, device=dev)
+        self.freed = torch.full((wl.B, self.bt_host.shape[1]), -1, dtype=torch.int32, device=dev)
+
+    def ensure_append_page(self):
+        """Give every sequence a page for its next slot (host-side allocator)."""
+        changed = False
+        for b in range(self.wl.B):
+            p = int(self.S[b]) // 16
+            if self.bt_host[b, p] < 0:
+                self.bt_host[b, p] = self.free.pop()
+                changed = True
+        if changed:
+            self.bt.copy_(torch.from_numpy(self.bt_host))
+
+    def decode(self, step, num_splits=0, append=True):
+        wl = self.wl
+        if append:
+            self.ensure_append_page()
+        K.kvsel_decode_attn(self.kv, self.bt, self.seq, bf16(wl.q[step], self.dev), self.out, self.ws,
+                            k_new=bf16(wl.k_new[step], self.dev) if append else None,
+                            v_new=bf16(wl.v_new[step], self.dev) if append else None,
+                            pos_map=self.pos, next_pos=self.next_pos, probs=self.probs,
+                            h2o_cum=self.cum, max_len=wl.max_len, num_splits=num_splits)
+        if append:
+            self.S += 1
+
+    def evict(self, compact=True):
+        wl = self.wl
+        K.kvsel_h2o_evict(self.kv, self.bt, self.seq, self.cum, self.ws_ev, budget=wl.budget,
+                          n_sink=wl.n_sink, window=wl.window, compact=compact, pos_map=self.pos,
+                          keep_out=self.keep, freed_pages=self.freed if compact else None)
+        if compact:
+            torch.cuda.synchronize()
+            self.bt_host = self.bt.cpu().numpy().copy()
+            fr = self.freed.cpu().numpy()
+            self.free.extend(int(x) for x in fr.ravel() if x >= 0)
+            self.S = np.minimum(self.S, wl.budget)
+
+    def status(self):
+        return K.read_status(self.ws), K.read_status(self.ws_ev)

@@ -1,0 +1,110 @@
+"""The C-ABI library builds, loads and exports every declared symbol (no GPU).
+
+Only host-side argument checks are exercised here: they return before any
+CUDA call, so they run on a machine without a GPU.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import attention_guided_kv_gb300 as K
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(K.LIB_PATH):
+        from attention_guided_kv_gb300 import _build
+        _build.build()
+    return K.lib()
+
+
+def declared_symbols():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"KVSEL_API\s+[\w\s\*]*?\b(kvsel_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(K.exported_symbols())
+
+
+def test_binding_does_not_import_the_oracle():
+    src = open(os.path.join(ROOT, "attention_guided_kv_gb300", "__init__.py")).read()
+    assert "oracle" not in re.sub(r'""".*?"""', "", src, flags=re.S)
+    for f in glob.glob(os.path.join(ROOT, "attention_guided_kv_gb300", "csrc", "*")):
+        assert "oracle" not in open(f).read(), f
+
+
+def _kv(**kw):
+    d = dict(k_pool=16, v_pool=16, num_pages=10, num_kv_heads=8, num_q_heads=64, head_dim=128,
+             page_size=16)
+    d.update(kw)
+    return K.PagedKV(**d)
+
+
+def test_workspace_sizes(lib):
+    kv = _kv()
+    a = K.kvsel_decode_attn_workspace(kv, 8, 32896, True)
+    b = K.kvsel_decode_attn_workspace(kv, 8, 32896, False)
+    assert a > 0 and b - a >= 8 * 64 * 32896 * 4           # logits scratch when probs are not kept
+    assert K.kvsel_h2o_evict_workspace(kv, 8, 6553) >= 8 * 8 * 6553 * 4
+    assert K.kvsel_decode_attn_workspace(_kv(num_q_heads=12), 1, 10, True) == 0
+
+
+def _decode_status(lib, kv, **over):
+    args = dict(block_table=16, max_pages=4, seq_lens=16, batch=1, q=16, k_new=None, v_new=None,
+                pos_map=None, next_pos=None, scale=0.1, out=16, out_dtype=0, probs=None, cum=None,
+                max_len=64, num_splits=0, ws=256, ws_bytes=1 << 30, stream=None)
+    args.update(over)
+    return lib.kvsel_decode_attn(ctypes.byref(kv), args["block_table"], args["max_pages"],
+                                 args["seq_lens"], args["batch"], args["q"], args["k_new"],
+                                 args["v_new"], args["pos_map"], args["next_pos"], args["scale"],
+                                 args["out"], args["out_dtype"], args["probs"], args["cum"],
+                                 args["max_len"], args["num_splits"], args["ws"], args["ws_bytes"],
+                                 args["stream"])
+
+
+def test_decode_host_validation(lib):
+    assert _decode_status(lib, _kv(k_pool=None)) == K.KVSEL_ERR_INVALID_ARG
+    assert _decode_status(lib, _kv(head_dim=64)) == K.KVSEL_ERR_UNSUPPORTED
+    assert _decode_status(lib, _kv(page_size=32)) == K.KVSEL_ERR_UNSUPPORTED
+    assert _decode_status(lib, _kv(num_q_heads=160, num_kv_heads=8)) == K.KVSEL_ERR_UNSUPPORTED
+    assert _decode_status(lib, _kv(num_q_heads=12)) == K.KVSEL_ERR_INVALID_ARG
+    assert _decode_status(lib, _kv(), k_new=16) == K.KVSEL_ERR_INVALID_ARG
+    assert _decode_status(lib, _kv(), pos_map=16) == K.KVSEL_ERR_INVALID_ARG
+    assert _decode_status(lib, _kv(), out_dtype=7) == K.KVSEL_ERR_INVALID_ARG
+    assert _decode_status(lib, _kv(), num_splits=65) == K.KVSEL_ERR_INVALID_ARG
+    assert _decode_status(lib, _kv(), q=8) == K.KVSEL_ERR_INVALID_ARG          # misaligned
+    assert _decode_status(lib, _kv(), ws_bytes=100) == K.KVSEL_ERR_INVALID_ARG
+    assert _decode_status(lib, _kv(), ws=None) == K.KVSEL_ERR_INVALID_ARG
+    assert b"workspace" in lib.kvsel_last_error_string()
+
+
+def test_evict_host_validation(lib):
+    kv = _kv()
+
+    def st(**over):
+        a = dict(bt=16, max_pages=4, seq=16, batch=1, cum=16, pos=None, max_len=64, budget=10,
+                 n_sink=4, window=4, compact=0, keep=None, freed=None, ws=256, ws_bytes=1 << 20)
+        a.update(over)
+        return lib.kvsel_h2o_evict(ctypes.byref(a.pop("kv", kv)), a["bt"], a["max_pages"], a["seq"],
+                                   a["batch"], a["cum"], a["pos"], a["max_len"], a["budget"],
+                                   a["n_sink"], a["window"], a["compact"], a["keep"], a["freed"],
+                                   a["ws"], a["ws_bytes"], None)
+    assert st(budget=7) == K.KVSEL_ERR_INVALID_ARG          # budget < sinks + window
+    assert st(n_sink=-1) == K.KVSEL_ERR_INVALID_ARG
+    assert st(cum=None) == K.KVSEL_ERR_INVALID_ARG
+    assert st(ws_bytes=8) == K.KVSEL_ERR_INVALID_ARG
+    assert st(kv=_kv(page_size=8)) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(compact=1, kv=_kv(k_pool=None)) == K.KVSEL_ERR_INVALID_ARG

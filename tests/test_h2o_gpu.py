@@ -1,0 +1,187 @@
+"""GPU parity of H2O selection and compaction against the oracle.
+
+Selection is bit-exact: the GPU and the oracle get the same fp32 score
+arrays and must return identical keep lists.  Compaction must move bytes
+exactly.  The end-to-end decode+evict loop (the small config, evicting every
+step) must keep identical sets except at near-ties (oracle score within
+1e-5 relative of the k-th score), after which the oracle continues from the
+GPU's keep-set.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle.attention import bf16_bits_to_f64
+from oracle.h2o import H2OSequence, h2o_keep
+from _harness import DecodeState, bf16, rel_l2
+
+import attention_guided_kv_gb300 as K
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+def _run_select(cum_np, S_list, budget, n_sink, window, max_len, pos=None):
+    B, Hkv, _ = cum_np.shape
+    dev = "cuda"
+    kpool = torch.zeros(1, Hkv, 16, 128, dtype=torch.bfloat16, device=dev)
+    kv = K.paged_kv(kpool, kpool, Hkv)
+    bt = torch.zeros(B, (max_len + 15) // 16, dtype=torch.int32, device=dev)
+    seq = torch.tensor(S_list, dtype=torch.int32, device=dev)
+    cum = torch.from_numpy(cum_np.astype(np.float32)).to(dev)
+    keep = torch.full((B, Hkv, budget), -7, dtype=torch.int32, device=dev)
+    ws = K.workspace(K.kvsel_h2o_evict_workspace(kv, B, budget))
+    K.kvsel_h2o_evict(kv, bt, seq, cum, ws, budget=budget, n_sink=n_sink, window=window,
+                      compact=False, keep_out=keep,
+                      pos_map=None if pos is None else torch.from_numpy(pos).to(dev))
+    assert K.read_status(ws) == 0
+    return keep.cpu().numpy()
+
+
+def _expect(cum_np, S_list, budget, n_sink, window, pos=None):
+    B, Hkv, _ = cum_np.shape
+    out = np.full((B, Hkv, budget), -1, dtype=np.int64)
+    for b in range(B):
+        for h in range(Hkv):
+            k = h2o_keep(cum_np[b, h].astype(np.float32), S_list[b], budget, n_sink, window)
+            out[b, h, :len(k)] = k if pos is None else pos[b, h, k]
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_select_bit_exact_with_ties(seed):
+    rng = np.random.default_rng(seed)
+    B, Hkv, max_len = 3, 4, 5000
+    S_list = [int(x) for x in rng.integers(1, max_len + 1, B)]
+    budget, n_sink, window = int(rng.integers(40, 900)), int(rng.integers(0, 5)), int(rng.integers(0, 40))
+    # coarse quantisation -> many exact ties at the threshold
+    cum = (rng.integers(0, 50, (B, Hkv, max_len)) * 0.125).astype(np.float32)
+    got = _run_select(cum, S_list, budget, n_sink, window, max_len)
+    np.testing.assert_array_equal(got, _expect(cum, S_list, budget, n_sink, window))
+
+
+def test_select_bit_exact_continuous_scores_and_positions():
+    rng = np.random.default_rng(17)
+    B, Hkv, max_len = 2, 8, 32896
+    S_list = [32769, 20000]
+    cum = rng.random((B, Hkv, max_len), dtype=np.float32) * np.float32(3.0)
+    pos = rng.permutation(B * Hkv * max_len).astype(np.int32).reshape(B, Hkv, max_len)
+    got = _run_select(cum, S_list, 6553, 4, 1024, max_len, pos=pos)
+    np.testing.assert_array_equal(got, _expect(cum, S_list, 6553, 4, 1024, pos=pos))
+
+
+def test_streaming_and_sliding_window_special_cases():
+    rng = np.random.default_rng(2)
+    cum = rng.random((1, 2, 400), dtype=np.float32)
+    got = _run_select(cum, [320], 256, 4, 252, 400)          # StreamingLLM: heavy = 0
+    want = list(range(4)) + list(range(68, 320))
+    assert got[0, 0].tolist() == want and got[0, 1].tolist() == want
+    got = _run_select(cum, [320], 256, 0, 256, 400)          # sliding window
+    assert got[0, 0].tolist() == list(range(64, 320))
+    got = _run_select(cum, [100], 256, 4, 16, 400)           # short: nothing evicted
+    assert got[0, 0].tolist() == list(range(100)) + [-1] * 156
+
+
+def test_all_equal_scores_keep_lowest_candidates():
+    cum = np.ones((1, 1, 64), dtype=np.float32)
+    got = _run_select(cum, [50], 20, 4, 6, 64)
+    assert got[0, 0].tolist() == list(range(14)) + list(range(44, 50))
+
+
+def test_compaction_moves_rows_exactly():
+    wl = workloads.decode_custom(seed=12, B=2, Hq=16, Hkv=8, d=128, S0=700, steps=1, budget=300,
+                                 n_sink=4, window=40, permute_pages=True)
+    st = DecodeState(wl, spare_pages=4)
+    rng = np.random.default_rng(3)
+    cum = rng.random((wl.B, wl.Hkv, wl.max_len), dtype=np.float32)
+    st.cum.copy_(torch.from_numpy(cum))
+    k_before = st.kpool.view(torch.int16).cpu().numpy().copy()
+    v_before = st.vpool.view(torch.int16).cpu().numpy().copy()
+    bt_before = st.bt_host.copy()
+    pos_before = st.pos.cpu().numpy().copy()
+    st.evict(compact=True)
+    assert st.status() == (0, 0)
+    kn = st.kpool.view(torch.int16).cpu().numpy()
+    vn = st.vpool.view(torch.int16).cpu().numpy()
+    cn = st.cum.cpu().numpy()
+    pn = st.pos.cpu().numpy()
+    keep_out = st.keep.cpu().numpy()
+    for b in range(wl.B):
+        for h in range(wl.Hkv):
+            keep = h2o_keep(cum[b, h], wl.S0, wl.budget, wl.n_sink, wl.window)
+            assert keep_out[b, h].tolist() == pos_before[b, h, keep].tolist()
+            for i, src in enumerate(keep):
+                ps, pd = bt_before[b, src // 16], st.bt_host[b, i // 16]
+                assert np.array_equal(kn[pd, h, i % 16], k_before[ps, h, src % 16])
+                assert np.array_equal(vn[pd, h, i % 16], v_before[ps, h, src % 16])
+            np.testing.assert_array_equal(cn[b, h, :wl.budget], cum[b, h, keep])
+            np.testing.assert_array_equal(pn[b, h, :wl.budget], pos_before[b, h, keep])
+    new_pages = (wl.budget + 15) // 16
+    old_pages = (wl.S0 + 15) // 16
+    assert (st.bt_host[:, new_pages:old_pages] == -1).all()
+    fr = st.freed.cpu().numpy()
+    for b in range(wl.B):
+        assert fr[b, :old_pages - new_pages].tolist() == bt_before[b, new_pages:old_pages].tolist()
+        assert (fr[b, old_pages - new_pages:] == -1).all()
+    assert st.seq.cpu().tolist() == [wl.budget] * wl.B
+
+
+def _run_mode_a(wl, steps):
+    """Evict-every-step loop on GPU and oracle with teacher forcing at near-ties."""
+    st = DecodeState(wl, spare_pages=8)
+    refs = [H2OSequence(bf16_bits_to_f64(wl.K[b]), bf16_bits_to_f64(wl.V[b])) for b in range(wl.B)]
+    swaps = 0
+    for t in range(steps):
+        st.decode(t)
+        torch.cuda.synchronize()
+        S = int(st.S[0])
+        probs = st.probs[:, :, :S].double().cpu().numpy()
+        outs = st.out.double().cpu().numpy()
+        cum_gpu = st.cum[:, :, :S].double().cpu().numpy()
+        for b, ref in enumerate(refs):
+            ref.append(bf16_bits_to_f64(wl.k_new[t, b]), bf16_bits_to_f64(wl.v_new[t, b]))
+            o, p = ref.attend(bf16_bits_to_f64(wl.q[t, b]), wl.scale)
+            assert ref.S == S
+            assert rel_l2(outs[b], o) < TOL, (t, b)
+            assert rel_l2(probs[b], p) < TOL, (t, b)
+            assert rel_l2(cum_gpu[b], ref.cum) < TOL, (t, b)
+        st.evict(compact=True)
+        torch.cuda.synchronize()
+        assert st.status() == (0, 0)
+        if S <= wl.budget:
+            continue
+        kept_pos = st.keep.cpu().numpy()
+        for b, ref in enumerate(refs):
+            want = ref.select(wl.budget, wl.n_sink, wl.window)
+            want_pos = np.stack([ref.pos[h, want[h]] for h in range(wl.Hkv)])
+            if not np.array_equal(kept_pos[b], want_pos):
+                for h in range(wl.Hkv):
+                    diff = set(kept_pos[b, h].tolist()) ^ set(want_pos[h].tolist())
+                    if not diff:
+                        continue
+                    k = wl.budget - wl.n_sink - wl.window
+                    mid = ref.cum[h, wl.n_sink:S - wl.window]
+                    kth = np.sort(mid)[::-1][k - 1]
+                    slot = {int(p): i for i, p in enumerate(ref.pos[h])}
+                    for p in diff:
+                        assert abs(ref.cum[h, slot[p]] - kth) <= 1e-5 * kth, (t, b, h, p)
+                    swaps += 1
+                gpu_slots = np.stack([[{int(p): i for i, p in enumerate(ref.pos[h])}[int(x)]
+                                       for x in kept_pos[b, h]] for h in range(wl.Hkv)])
+                ref.apply_keep(gpu_slots)
+            else:
+                ref.apply_keep(want)
+    return swaps
+
+
+def test_small_config_evict_every_step_end_to_end():
+    wl = workloads.decode_small()
+    swaps = _run_mode_a(wl, wl.steps)
+    assert swaps <= 4
+
+
+def test_custom_config_evict_every_step_permuted_pages():
+    wl = workloads.decode_custom(seed=77, B=3, Hq=64, Hkv=8, d=128, S0=500, steps=12, budget=200,
+                                 n_sink=4, window=33, permute_pages=True)
+    _run_mode_a(wl, wl.steps)
