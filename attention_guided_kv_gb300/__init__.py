@@ -167,7 +167,7 @@ def kvsel_decode_attn_workspace(kv: PagedKV, batch: int, max_len: int, with_prob
 
 def kvsel_decode_attn(kv: PagedKV, block_table, seq_lens, q, out, workspace, *, k_new=None,
                       v_new=None, pos_map=None, next_pos=None, scale=None, probs=None,
-                      h2o_cum=None, max_len=None, num_splits=0, stream=None):
+                      h2o_cum=None, max_len=None, num_ctas=0, stream=None):
     """Append (optional) + decode attention + probabilities + H2O score update."""
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
@@ -195,7 +195,7 @@ def kvsel_decode_attn(kv: PagedKV, block_table, seq_lens, q, out, workspace, *, 
     _check(lib().kvsel_decode_attn(
         ctypes.byref(kv), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch, _ptr(q),
         _ptr(k_new), _ptr(v_new), _ptr(pos_map), _ptr(next_pos), float(scale), _ptr(out), odt,
-        _ptr(probs), _ptr(h2o_cum), int(max_len), int(num_splits), _ptr(workspace),
+        _ptr(probs), _ptr(h2o_cum), int(max_len), int(num_ctas), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

@@ -28,8 +28,8 @@ namespace kvsel {
 constexpr int kHD = 128;
 constexpr int kPg = 16;
 constexpr int kSelThreads = 1024;
-constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kChunk = 64;
+constexpr int kItems = 32;
 
 struct SelectParams {
   const int32_t* seq_lens;
@@ -71,11 +71,16 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
   return res;
 }
 
+// Candidate keys are fetched either from registers (rows of at most
+// kSelThreads * kItems candidates: each thread keeps its contiguous run of
+// order keys in registers for every pass) or re-read from global memory.
+template <bool kInRegs>
 __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectParams P) {
-  __shared__ uint32_t hist[kSelWarps][256];
+  __shared__ uint32_t hist[256];
   __shared__ uint32_t scan_tmp[33];
   __shared__ uint32_t s_digit, s_above;
   __shared__ int s_first;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the scores come from the previous kernel
 
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -102,33 +107,63 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
 
   const int k = P.budget - P.n_sink - P.window;
   const int lo = P.n_sink, hi = S - P.window;
+  const int n_cand = hi - lo;
+  const int C = (n_cand + kSelThreads - 1) / kSelThreads;
+  const int j0 = lo + min(n_cand, tid * C);
+  const int cnt = min(n_cand, (tid + 1) * C) - min(n_cand, tid * C);
+  constexpr int kR = kInRegs ? kItems : 1;
+  uint32_t key[kR];
+  if constexpr (kInRegs) {
+#pragma unroll
+    for (int e = 0; e < kR; ++e) key[e] = e < cnt ? order_key(row[j0 + e]) : 0u;
+  }
+  // Visit this thread's valid candidates in slot order: BODY sees (e, u).
+#define KVSEL_FOR_ITEMS(BODY)                                              \
+  if constexpr (kInRegs) {                                                 \
+    _Pragma("unroll") for (int e = 0; e < kR; ++e) if (e < cnt) {          \
+      const uint32_t u = key[e];                                           \
+      BODY                                                                 \
+    }                                                                      \
+  } else {                                                                 \
+    for (int e = 0; e < cnt; ++e) {                                        \
+      const uint32_t u = order_key(row[j0 + e]);                           \
+      BODY                                                                 \
+    }                                                                      \
+  }
+
   uint32_t T = 0xFFFFFFFFu, need_eq = 0;
   if (k > 0) {
     uint32_t prefix = 0, mask = 0, krem = uint32_t(k);
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int i = tid; i < kSelWarps * 256; i += kSelThreads) (&hist[0][0])[i] = 0;
+      if (tid < 256) hist[tid] = 0;
       __syncthreads();
-      for (int j = lo + tid; j < hi; j += kSelThreads) {
-        const uint32_t u = order_key(row[j]);
-        if ((u & mask) == prefix) atomicAdd(&hist[warp][(u >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      if (tid < 256) {
-        uint32_t t = 0;
-#pragma unroll 8
-        for (int w = 0; w < kSelWarps; ++w) t += hist[w][tid];
-        hist[0][tid] = t;  // warp 0's row now holds the totals
+      // warp-aggregated histogram: one shared atomic per distinct digit per warp
+      // step.  Every lane runs the same trip count (kR or C) for the collectives.
+      auto add = [&](uint32_t u, bool valid) {
+        const bool v = valid && (u & mask) == prefix;
+        const unsigned active = __ballot_sync(0xffffffffu, v);
+        if (v) {
+          const uint32_t digit = (u >> shift) & 255u;
+          const unsigned same = __match_any_sync(active, digit);
+          if (lane == __ffs(same) - 1) atomicAdd(&hist[digit], uint32_t(__popc(same)));
+        }
+      };
+      if constexpr (kInRegs) {
+#pragma unroll
+        for (int e = 0; e < kR; ++e) add(key[e], e < cnt);
+      } else {
+        for (int e = 0; e < C; ++e) add(e < cnt ? order_key(row[j0 + e]) : 0u, e < cnt);
       }
       __syncthreads();
       if (warp == 0) {
-        // lane l owns bins [255 - 8l - 7, 255 - 8l]; find the digit holding the krem-th largest.
-        uint32_t c[8], lsum = 0;
+        // lane l owns bins 255-8l .. 255-8l-7; find the digit holding the krem-th largest
+        uint32_t cb[8], lsum = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          c[e] = hist[0][255 - 8 * lane - e];
-          lsum += c[e];
+          cb[e] = hist[255 - 8 * lane - e];
+          lsum += cb[e];
         }
         uint32_t incl = lsum;
 #pragma unroll
@@ -136,17 +171,17 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
           const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
-        const uint32_t excl = incl - lsum;  // count in bins above this lane's bins
+        const uint32_t excl = incl - lsum;
         if (excl < krem && krem <= incl) {
           uint32_t above = excl;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            if (above + c[e] >= krem) {
+            if (above + cb[e] >= krem) {
               s_digit = 255 - 8 * lane - e;
               s_above = above;
               break;
             }
-            above += c[e];
+            above += cb[e];
           }
         }
       }
@@ -154,37 +189,28 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
       krem -= s_above;
       prefix |= s_digit << shift;
       mask |= 0xFFu << shift;
-      __syncthreads();
     }
     T = prefix;
     need_eq = krem;
   }
 
   // ordered emission of the heavy hitters
-  const int n_cand = hi - lo;
-  const int C = (n_cand + kSelThreads - 1) / kSelThreads;
-  const int j0 = lo + min(n_cand, tid * C);
-  const int j1 = lo + min(n_cand, (tid + 1) * C);
   uint32_t gt = 0, eq = 0;
-  if (k > 0)
-    for (int j = j0; j < j1; ++j) {
-      const uint32_t u = order_key(row[j]);
-      gt += u > T;
-      eq += u == T;
-    }
+  if (k > 0) {
+    KVSEL_FOR_ITEMS(gt += u > T; eq += u == T;)
+  }
   uint32_t tot;
   const uint32_t eq_base = block_exclusive_scan(eq, scan_tmp, tot);
   const uint32_t take_eq = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
   const uint32_t out_base = block_exclusive_scan(gt + take_eq, scan_tmp, tot);
   if (k > 0 && gt + take_eq > 0) {
-    uint32_t w = P.n_sink + out_base, e = eq_base;
-    for (int j = j0; j < j1; ++j) {
-      const uint32_t u = order_key(row[j]);
-      const bool isq = u == T;
-      if ((u > T || (isq && e < need_eq)) && w < uint32_t(P.n_sink + k)) keep[w++] = j;
-      e += isq;
-    }
+    uint32_t w = P.n_sink + out_base, q = eq_base;
+    const uint32_t wend = uint32_t(P.n_sink + k);
+    KVSEL_FOR_ITEMS(const bool isq = u == T;
+                    if ((u > T || (isq && q < need_eq)) && w < wend) keep[w++] = j0 + e;
+                    q += isq;)
   }
+#undef KVSEL_FOR_ITEMS
   for (int i = tid; i < P.n_sink; i += kSelThreads) keep[i] = i;
   for (int i = tid; i < P.window; i += kSelThreads) keep[P.budget - P.window + i] = S - P.window + i;
   if (tid == 0) s_first = P.budget;
@@ -360,9 +386,19 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   P.budget = budget;
   P.n_sink = n_sink;
   P.window = window;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kv->num_kv_heads, batch);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const bool in_regs = (long long)max_len - n_sink - window <= (long long)kSelThreads * kItems;
   trace_before("h2o_select", st);
-  h2o_select_kernel<<<dim3(kv->num_kv_heads, batch), kSelThreads, 0, st>>>(P);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = in_regs ? cudaLaunchKernelEx(&cfg, h2o_select_kernel<true>, P)
+                          : cudaLaunchKernelEx(&cfg, h2o_select_kernel<false>, P);
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_h2o_evict (select launch)");
   if (!compact) return KVSEL_OK;

@@ -9,9 +9,10 @@
  *    otherwise.  The library allocates no device memory: scratch comes from
  *    a caller-provided workspace whose size the matching *_workspace()
  *    function returns.
- *  - The first 256 bytes of every workspace hold a device status word.  It
- *    must be zero when a workspace is first used (allocate it zeroed, or
- *    call kvsel_clear_status).  Kernels that detect a problem on the device
+ *  - The first 256 bytes of every workspace hold a device status word and
+ *    grid-barrier counters.  They must be zero when a workspace is first
+ *    used (allocate it zeroed); afterwards the library keeps them
+ *    consistent.  Kernels that detect a problem on the device
  *    (a block-table entry outside the pool, a bounded wait that ran out)
  *    record a kvsel_status there and carry on without faulting;
  *    kvsel_read_status() returns it.
@@ -70,7 +71,8 @@ typedef struct kvsel_paged_kv {
 /* Human-readable reason for the last non-OK status returned on this thread. */
 KVSEL_API const char* kvsel_last_error_string(void);
 
-/* Zero the status word of `workspace` (async on `stream`). */
+/* Zero the status word of `workspace` (async on `stream`); the barrier
+ * counters are left alone. */
 KVSEL_API kvsel_status kvsel_clear_status(void* workspace, void* stream);
 
 /* Synchronise `stream`, return the device status recorded in `workspace`
@@ -119,11 +121,16 @@ KVSEL_API int kvsel_trace_stop(const char** names, int capacity);
  *                entries j >= S_b are not written.
  *   h2o_cum      fp32 [batch][num_kv_heads][max_len] or NULL: updated in
  *                place; the appended slot starts from 0.
- *   max_len      capacity in slots of probs / h2o_cum / pos_map rows; every
- *                S_b (after the append) must be <= max_len and
- *                <= max_pages * page_size.
- *   num_splits   key splits per (sequence, kv head); 0 = choose from the SM
- *                count.  Results do not depend on it beyond fp32 rounding.
+ *   max_len      capacity in slots of probs / h2o_cum / pos_map rows;
+ *                every S_b (after the append) must be <= max_len and
+ *                <= max_pages * page_size, else KVSEL_ERR_BAD_INDEX is
+ *                recorded on the device and nothing is computed.
+ *   batch        at most 1024 sequences.
+ *   num_ctas     how many CTAs share the work: the pages of all (sequence,
+ *                kv head) pairs are cut into num_ctas equal contiguous ranges
+ *                (0 = every co-resident CTA slot, the fastest choice; at most
+ *                that many, and at most 1024).  Results do not depend on it
+ *                beyond fp32 rounding.
  *   workspace    >= kvsel_decode_attn_workspace(...) bytes, status word zeroed.
  * Returns KVSEL_OK once the kernels are enqueued.
  */
@@ -133,7 +140,7 @@ KVSEL_API kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_t
                                int max_pages, int32_t* seq_lens, int batch, const void* q,
                                const void* k_new, const void* v_new, int32_t* pos_map,
                                int32_t* next_pos, float scale, void* out, int out_dtype,
-                               float* probs, float* h2o_cum, int max_len, int num_splits,
+                               float* probs, float* h2o_cum, int max_len, int num_ctas,
                                void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------

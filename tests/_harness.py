@@ -65,7 +65,7 @@ class DecodeState:
         if changed:
             self.bt.copy_(torch.from_numpy(self.bt_host))
 
-    def decode(self, step, num_splits=0, append=True):
+    def decode(self, step, num_ctas=0, append=True):
         wl = self.wl
         if append:
             self.ensure_append_page()
@@ -73,7 +73,7 @@ class DecodeState:
                             k_new=bf16(wl.k_new[step], self.dev) if append else None,
                             v_new=bf16(wl.v_new[step], self.dev) if append else None,
                             pos_map=self.pos, next_pos=self.next_pos, probs=self.probs,
-                            h2o_cum=self.cum, max_len=wl.max_len, num_splits=num_splits)
+                            h2o_cum=self.cum, max_len=wl.max_len, num_ctas=num_ctas)
         if append:
             self.S += 1
 

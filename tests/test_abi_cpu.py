@@ -58,6 +58,7 @@ def test_workspace_sizes(lib):
     a = K.kvsel_decode_attn_workspace(kv, 8, 32896, True)
     b = K.kvsel_decode_attn_workspace(kv, 8, 32896, False)
     assert a > 0 and b - a >= 8 * 64 * 32896 * 4           # logits scratch when probs are not kept
+    assert K.kvsel_decode_attn_workspace(kv, 8, 32896, True) < 8 << 20
     assert K.kvsel_h2o_evict_workspace(kv, 8, 6553) >= 8 * 8 * 6553 * 4
     assert K.kvsel_decode_attn_workspace(_kv(num_q_heads=12), 1, 10, True) == 0
 
@@ -65,13 +66,13 @@ def test_workspace_sizes(lib):
 def _decode_status(lib, kv, **over):
     args = dict(block_table=16, max_pages=4, seq_lens=16, batch=1, q=16, k_new=None, v_new=None,
                 pos_map=None, next_pos=None, scale=0.1, out=16, out_dtype=0, probs=None, cum=None,
-                max_len=64, num_splits=0, ws=256, ws_bytes=1 << 30, stream=None)
+                max_len=64, num_ctas=0, ws=256, ws_bytes=1 << 30, stream=None)
     args.update(over)
     return lib.kvsel_decode_attn(ctypes.byref(kv), args["block_table"], args["max_pages"],
                                  args["seq_lens"], args["batch"], args["q"], args["k_new"],
                                  args["v_new"], args["pos_map"], args["next_pos"], args["scale"],
                                  args["out"], args["out_dtype"], args["probs"], args["cum"],
-                                 args["max_len"], args["num_splits"], args["ws"], args["ws_bytes"],
+                                 args["max_len"], args["num_ctas"], args["ws"], args["ws_bytes"],
                                  args["stream"])
 
 
@@ -84,7 +85,7 @@ def test_decode_host_validation(lib):
     assert _decode_status(lib, _kv(), k_new=16) == K.KVSEL_ERR_INVALID_ARG
     assert _decode_status(lib, _kv(), pos_map=16) == K.KVSEL_ERR_INVALID_ARG
     assert _decode_status(lib, _kv(), out_dtype=7) == K.KVSEL_ERR_INVALID_ARG
-    assert _decode_status(lib, _kv(), num_splits=65) == K.KVSEL_ERR_INVALID_ARG
+    assert _decode_status(lib, _kv(), num_ctas=1025) == K.KVSEL_ERR_INVALID_ARG
     assert _decode_status(lib, _kv(), q=8) == K.KVSEL_ERR_INVALID_ARG          # misaligned
     assert _decode_status(lib, _kv(), ws_bytes=100) == K.KVSEL_ERR_INVALID_ARG
     assert _decode_status(lib, _kv(), ws=None) == K.KVSEL_ERR_INVALID_ARG

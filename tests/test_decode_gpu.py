@@ -50,12 +50,12 @@ def test_decode_small_config_one_step():
     assert int(st.pos[0, 3, wl.S0]) == wl.S0 and int(st.next_pos[0]) == wl.S0 + 1
 
 
-@pytest.mark.parametrize("splits", [1, 2, 7, 16, 64])
-def test_split_count_invariance(splits):
+@pytest.mark.parametrize("ctas", [1, 2, 7, 16, 64, 151, 0])
+def test_work_split_invariance(ctas):
     wl = workloads.decode_custom(seed=31, B=2, Hq=32, Hkv=4, d=128, S0=999, steps=1, budget=512,
                                  n_sink=4, window=64, permute_pages=True)
     st = DecodeState(wl)
-    st.decode(0, num_splits=splits)
+    st.decode(0, num_ctas=ctas)
     torch.cuda.synchronize()
     assert st.status() == (0, 0)
     _check_step(st, wl)
@@ -76,7 +76,7 @@ def test_ragged_lengths_and_page_tails(S0):
     wl = workloads.decode_custom(seed=50 + S0, B=1, Hq=16, Hkv=8, d=128, S0=S0, steps=1, budget=8,
                                  n_sink=0, window=8, permute_pages=True)
     st = DecodeState(wl)
-    st.decode(0, num_splits=3)
+    st.decode(0, num_ctas=3)
     torch.cuda.synchronize()
     assert st.status() == (0, 0)
     _check_step(st, wl)
