@@ -50,6 +50,7 @@ constexpr int kMaxG = 8;
 constexpr int kMaxCtas = 1024;
 constexpr int kMaxBatch = 1024;
 constexpr int kPartFloats = kMaxG * (kD + 2);  // one partial slot: m[8], l[8], O[8][128]
+constexpr int kMaxOwners = kMaxCtas;           // CTAs sharing one (sequence, kv head) pair
 
 struct SmemLayout {
   static constexpr size_t ring = 0;
@@ -59,7 +60,8 @@ struct SmemLayout {
   static constexpr size_t seqS = bars + 2 * kStages * 8;                                 // [kMaxBatch] i32
   static constexpr size_t seqPref = seqS + size_t(kMaxBatch) * 4;                        // [kMaxBatch+1] i64
   static constexpr size_t stats = seqPref + size_t(kMaxBatch + 1) * 8;                   // [8][2] f32
-  static constexpr size_t total = stats + kMaxG * 2 * 4;
+  static constexpr size_t owners = stats + kMaxG * 2 * 4;                                // [kMaxOwners+1] i32
+  static constexpr size_t total = owners + (kMaxOwners + 1) * 4;
 };
 constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 
@@ -82,6 +84,7 @@ struct StepParams {
   int* status;
   int B, max_pages, Hq, Hkv, G, num_pages, max_len, out_f32;
   int vec_logits;  // logit rows are 8-byte aligned: store pairs as float2
+  int vec4;        // logit / score rows are 16-byte aligned: phase B moves float4
   float scale_log2;
 };
 
@@ -162,6 +165,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   int32_t* sS = reinterpret_cast<int32_t*>(smem + SmemLayout::seqS);
   long long* sPref = reinterpret_cast<long long*>(smem + SmemLayout::seqPref);
   float* sStat = reinterpret_cast<float*>(smem + SmemLayout::stats);
+  int* sOwn = reinterpret_cast<int*>(smem + SmemLayout::owners);  // [kMaxOwners] + count
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = gridDim.x, c = blockIdx.x;
@@ -235,36 +239,53 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 
   // ================= phase A =================
   if (warp == kConsumerWarps) {
-    if (lane == 0 && n > 0) {
+    // Producer warp.  Every lane resolves one page of a 32-page chunk (block
+    // table entry -> TMA row coordinate), two chunks ahead of use, so the
+    // dependent block-table loads never sit between two TMA issues.
+    if (n > 0) {
       const uint64_t pol = l2_policy_evict_first();
-      int b, kvh, pg;
-      loc.locate(u0, b, kvh, pg);
-      int np = loc.pages(b);
-#pragma unroll 1
-      for (int i = 0; i < n; ++i) {
-        const int s = i % kStages;
-        if (i >= kStages && !mbar_wait(smem_u32(&empty[s]), ((i / kStages) + 1) & 1, P.status)) break;
+      auto resolve = [&](int i) -> int {  // TMA row of CTA-local page i (or -1 past the end)
+        if (i >= n) return -1;
+        int b, kvh, pg;
+        loc.locate(u0 + i, b, kvh, pg);
         int phys = P.block_table[size_t(b) * P.max_pages + pg];
         if (unsigned(phys) >= unsigned(P.num_pages)) {
           report(P.status, KVSEL_ERR_BAD_INDEX);
           phys = 0;
         }
-        const int y = (phys * Hkv + kvh) * kPage;
-        const uint32_t dst = smem_u32(smem + SmemLayout::ring + s * kStageBytes);
-        const uint32_t bar = smem_u32(&full[s]);
-        mbar_expect_tx(bar, kStageBytes);
-        tma_load_2d(dst, &tmK, 0, y, bar, pol);
-        tma_load_2d(dst + 2048, &tmK, 64, y, bar, pol);
-        tma_load_2d(dst + 4096, &tmV, 0, y, bar, pol);
-        tma_load_2d(dst + 6144, &tmV, 64, y, bar, pol);
-        if (++pg == np) {  // next pair in unit order
-          pg = 0;
-          if (++kvh == Hkv) {
-            kvh = 0;
-            do { ++b; } while (b < P.B && loc.pages(b) == 0);
-            if (b < P.B) np = loc.pages(b);
+        return (phys * Hkv + kvh) * kPage;
+      };
+      int y_cur = resolve(lane);
+      int y_next = resolve(32 + lane);
+#pragma unroll 1
+      for (int i0 = 0; i0 < n; i0 += 32) {
+        const int y_after = resolve(i0 + 64 + lane);  // issued early; used two chunks later
+        bool stop = false;
+#pragma unroll 1
+        for (int k = 0; k < 32 && i0 + k < n; ++k) {
+          const int i = i0 + k;
+          const int y = __shfl_sync(0xffffffffu, y_cur, k);
+          const int s = i % kStages;
+          bool ok = true;
+          if (i >= kStages) ok = mbar_wait(smem_u32(&empty[s]), ((i / kStages) + 1) & 1, P.status);
+          if (!__all_sync(0xffffffffu, ok)) {
+            stop = true;
+            break;
           }
+          if (lane == 0) {
+            const uint32_t dst = smem_u32(smem + SmemLayout::ring + s * kStageBytes);
+            const uint32_t bar = smem_u32(&full[s]);
+            mbar_expect_tx(bar, kStageBytes);
+            tma_load_2d(dst, &tmK, 0, y, bar, pol);
+            tma_load_2d(dst + 2048, &tmK, 64, y, bar, pol);
+            tma_load_2d(dst + 4096, &tmV, 0, y, bar, pol);
+            tma_load_2d(dst + 6144, &tmV, 64, y, bar, pol);
+          }
+          __syncwarp();
         }
+        if (stop) break;
+        y_cur = y_next;
+        y_next = y_after;
       }
     }
   } else {
@@ -447,17 +468,23 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     const int cf = cta_of(pfirst, U, NC);
     // The CTAs owning units of this pair, in order: cf, then the owner of the
     // unit right after each owner's range, up to the pair's last unit.
-    auto next_owner = [&](int cc) -> int {
-      const long long nu = U * (cc + 1) / NC;
-      return nu > plast ? -1 : cta_of(nu, U, NC);
-    };
+    if (tid == 0) {
+      int no = 0;
+      for (int cc = cf; cc >= 0 && no < kMaxOwners; ++no) {
+        sOwn[no] = cc;
+        const long long nu = U * (cc + 1) / NC;
+        cc = nu > plast ? -1 : cta_of(nu, U, NC);
+      }
+      sOwn[kMaxOwners] = no;
+    }
+    __syncthreads();
+    const int nown = sOwn[kMaxOwners];
     if (tid < G) {
       float M = -INFINITY;
-      for (int cc = cf; cc >= 0; cc = next_owner(cc))
-        M = fmaxf(M, __ldcg(P.part + size_t(cc + pair) * kPartFloats + tid));
+      for (int k = 0; k < nown; ++k) M = fmaxf(M, __ldcg(P.part + size_t(sOwn[k] + pair) * kPartFloats + tid));
       float L = 0.f;
-      for (int cc = cf; cc >= 0; cc = next_owner(cc)) {
-        const float* sl = P.part + size_t(cc + pair) * kPartFloats;
+      for (int k = 0; k < nown; ++k) {
+        const float* sl = P.part + size_t(sOwn[k] + pair) * kPartFloats;
         const float m = __ldcg(sl + tid);
         if (m != -INFINITY) L += __ldcg(sl + kMaxG + tid) * exp2f(m - M);
       }
@@ -470,10 +497,12 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         const int gg = idx / kD, dd = idx % kD;
         const float M = sStat[gg * 2];
         float acc = 0.f;
-        for (int cc = cf; cc >= 0; cc = next_owner(cc)) {
-          const float* sl = P.part + size_t(cc + pair) * kPartFloats;
+#pragma unroll 4
+        for (int k = 0; k < nown; ++k) {
+          const float* sl = P.part + size_t(sOwn[k] + pair) * kPartFloats;
           const float m = __ldcg(sl + gg);
-          if (m != -INFINITY) acc += __ldcg(sl + 2 * kMaxG + gg * kD + dd) * exp2f(m - M);
+          const float v = __ldcg(sl + 2 * kMaxG + gg * kD + dd);
+          if (m != -INFINITY) acc += v * exp2f(m - M);
         }
         const float v = acc * sStat[gg * 2 + 1];
         const size_t oi = (size_t(b) * P.Hq + kvh * G + gg) * kD + dd;
@@ -486,17 +515,63 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       const int j1 = min(S, int(pg + (seg_end - u)) * kPage);
       const size_t row0 = (size_t(b) * P.Hq + kvh * G) * P.max_len;
       float* crow = P.cum ? P.cum + (size_t(b) * Hkv + kvh) * P.max_len : nullptr;
-      for (int j = j0 + tid; j < j1; j += kThreads) {
-        float sum = 0.f;
-        for (int gg = 0; gg < G; ++gg) {
-          const size_t li = row0 + size_t(gg) * P.max_len + j;
-          const float pj = exp2f(P.logits[li] - sStat[gg * 2]) * sStat[gg * 2 + 1];
-          if (P.probs) P.probs[li] = pj;
-          sum += pj;
+      float Mg[kMaxG], Ig[kMaxG];
+#pragma unroll
+      for (int gg = 0; gg < kMaxG; ++gg) {
+        Mg[gg] = gg < G ? sStat[gg * 2] : 0.f;
+        Ig[gg] = gg < G ? sStat[gg * 2 + 1] : 0.f;
+      }
+      if (P.vec4) {
+        // 4 keys x all heads per thread per step: up to 8 independent 16-byte loads in flight
+        for (int j = j0 + 4 * tid; j + 3 < j1; j += 4 * kThreads) {
+          float4 lg[kMaxG];
+#pragma unroll
+          for (int gg = 0; gg < kMaxG; ++gg)
+            if (gg < G)
+              lg[gg] = __ldcg(reinterpret_cast<const float4*>(P.logits + row0 + size_t(gg) * P.max_len + j));
+          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int gg = 0; gg < kMaxG; ++gg)
+            if (gg < G) {
+              float4 pj;
+              pj.x = exp2f(lg[gg].x - Mg[gg]) * Ig[gg];
+              pj.y = exp2f(lg[gg].y - Mg[gg]) * Ig[gg];
+              pj.z = exp2f(lg[gg].z - Mg[gg]) * Ig[gg];
+              pj.w = exp2f(lg[gg].w - Mg[gg]) * Ig[gg];
+              if (P.probs) __stcg(reinterpret_cast<float4*>(P.probs + row0 + size_t(gg) * P.max_len + j), pj);
+              sum.x += pj.x;
+              sum.y += pj.y;
+              sum.z += pj.z;
+              sum.w += pj.w;
+            }
+          if (crow) {
+            float4 old = __ldcg(reinterpret_cast<const float4*>(crow + j));
+            if (append && j + 3 >= S - 1) {  // the appended slot starts from zero
+              if (j == S - 1) old.x = 0.f;
+              if (j + 1 == S - 1) old.y = 0.f;
+              if (j + 2 == S - 1) old.z = 0.f;
+              if (j + 3 == S - 1) old.w = 0.f;
+            }
+            __stcg(reinterpret_cast<float4*>(crow + j),
+                   make_float4(old.x + sum.x, old.y + sum.y, old.z + sum.z, old.w + sum.w));
+          }
         }
+      }
+      // keys left over (the whole segment when rows are not 16-byte aligned), one per thread
+      const int jr = P.vec4 ? j0 + ((j1 - j0) & ~3) : j0;
+      for (int jj = jr + tid; jj < j1; jj += kThreads) {
+        float sum = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < kMaxG; ++gg)
+          if (gg < G) {
+            const size_t li = row0 + size_t(gg) * P.max_len + jj;
+            const float pj = exp2f(__ldcg(P.logits + li) - Mg[gg]) * Ig[gg];
+            if (P.probs) P.probs[li] = pj;
+            sum += pj;
+          }
         if (crow) {
-          const float old = (append && j == S - 1) ? 0.f : crow[j];
-          crow[j] = old + sum;
+          const float old = (append && jj == S - 1) ? 0.f : crow[jj];
+          crow[jj] = old + sum;
         }
       }
     }
@@ -636,6 +711,7 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   P.max_len = max_len;
   P.out_f32 = out_dtype == KVSEL_F32;
   P.vec_logits = (max_len % 2 == 0) && aligned(P.logits, 8);
+  P.vec4 = (max_len % 4 == 0) && aligned(P.logits, 16) && (!h2o_cum || aligned(h2o_cum, 16));
   P.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -8,9 +8,11 @@
 // slot), and [S - window, S); evict the rest.
 //
 // select kernel, one 1024-thread CTA per (sequence, kv head):
-//   radix select of the k-th largest score over the middle slots, 4 passes of
-//   8-bit digits on a monotone uint32 image of the fp32 score, with per-warp
-//   shared-memory histograms; then an ordered emission: each thread owns a
+//   finds the k-th largest score over the middle slots on a monotone uint32
+//   image of the fp32 score: a sorted sample brackets it, one counting pass
+//   gathers the keys inside the bracket, and a 4 x 8-bit radix select finishes
+//   exactly (a radix select over the whole row is the fallback); then an
+//   ordered emission: each thread owns a
 //   contiguous run of slots, two block-wide scans give every thread its share
 //   of the threshold ties (lowest slots first) and its output offset, so the
 //   kept list comes out in ascending slot order without a sort.
@@ -30,6 +32,7 @@ constexpr int kPg = 16;
 constexpr int kSelThreads = 1024;
 constexpr int kChunk = 64;
 constexpr int kItems = 32;
+constexpr int kBandMax = 8192;
 
 struct SelectParams {
   const int32_t* seq_lens;
@@ -71,19 +74,84 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* w
   return res;
 }
 
-// Candidate keys are fetched either from registers (rows of at most
-// kSelThreads * kItems candidates: each thread keeps its contiguous run of
-// order keys in registers for every pass) or re-read from global memory.
+// Radix select over `n` keys held in shared memory: finds the krem-th largest
+// key T and how many copies of T belong to the top krem.
+__device__ __forceinline__ void smem_radix_select(const uint32_t* keys, int n, uint32_t krem,
+                                                  uint32_t* hist, uint32_t* s_digit,
+                                                  uint32_t* s_above, uint32_t& T, uint32_t& need_eq) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t prefix = 0, mask = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += blockDim.x) {
+      const uint32_t u = keys[i];
+      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255-8l .. 255-8l-7; find the digit holding the krem-th largest
+      uint32_t cb[8], lsum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cb[e] = hist[255 - 8 * lane - e];
+        lsum += cb[e];
+      }
+      uint32_t incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - lsum;
+      if (excl < krem && krem <= incl) {
+        uint32_t above = excl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (above + cb[e] >= krem) {
+            *s_digit = 255 - 8 * lane - e;
+            *s_above = above;
+            break;
+          }
+          above += cb[e];
+        }
+      }
+    }
+    __syncthreads();
+    krem -= *s_above;
+    prefix |= *s_digit << shift;
+    mask |= 0xFFu << shift;
+    __syncthreads();
+  }
+  T = prefix;
+  need_eq = krem;
+}
+
+// Per (sequence, kv head) row: the threshold key T of the top-k middle slots
+// and how many slots equal to T are taken (lowest slots first), then the
+// ordered emission of the kept list.
+//
+// Register path (rows of at most kSelThreads * kItems candidates): every
+// thread holds its contiguous run of candidate keys.  A sample (the first key
+// of every run) is sorted; two sample quantiles bracket the k-th key with a
+// margin of four binomial standard deviations; one counting pass checks the
+// bracket and the keys inside it are gathered to shared memory, where an
+// exact radix select finishes.  If the bracket misses, or for longer rows, a
+// radix select runs over the whole row in global memory instead.
 template <bool kInRegs>
 __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectParams P) {
   __shared__ uint32_t hist[256];
   __shared__ uint32_t scan_tmp[33];
   __shared__ uint32_t s_digit, s_above;
   __shared__ int s_first;
+  __shared__ uint32_t sample[kInRegs ? kSelThreads : 1];
+  __shared__ uint32_t band[kInRegs ? kBandMax : 1];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the scores come from the previous kernel
 
   const int kvh = blockIdx.x, b = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int S = P.seq_lens[b];
   const size_t rowi = size_t(b) * P.Hkv + kvh;
   const float* row = P.cum + rowi * P.max_len;
@@ -117,48 +185,78 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
 #pragma unroll
     for (int e = 0; e < kR; ++e) key[e] = e < cnt ? order_key(row[j0 + e]) : 0u;
   }
-  // Visit this thread's valid candidates in slot order: BODY sees (e, u).
-#define KVSEL_FOR_ITEMS(BODY)                                              \
-  if constexpr (kInRegs) {                                                 \
-    _Pragma("unroll") for (int e = 0; e < kR; ++e) if (e < cnt) {          \
-      const uint32_t u = key[e];                                           \
-      BODY                                                                 \
-    }                                                                      \
-  } else {                                                                 \
-    for (int e = 0; e < cnt; ++e) {                                        \
-      const uint32_t u = order_key(row[j0 + e]);                           \
-      BODY                                                                 \
-    }                                                                      \
+  // Visit this thread's candidates in slot order: BODY sees (e, u).
+#define KVSEL_FOR_ITEMS(BODY)                                     \
+  if constexpr (kInRegs) {                                        \
+    _Pragma("unroll") for (int e = 0; e < kR; ++e) if (e < cnt) { \
+      const uint32_t u = key[e];                                  \
+      BODY                                                        \
+    }                                                             \
+  } else {                                                        \
+    for (int e = 0; e < cnt; ++e) {                               \
+      const uint32_t u = order_key(row[j0 + e]);                  \
+      BODY                                                        \
+    }                                                             \
   }
 
-  uint32_t T = 0xFFFFFFFFu, need_eq = 0;
-  if (k > 0) {
+  uint32_t T = 0xFFFFFFFFu, need_eq = 0, tot = 0;
+  bool done = false;
+  if constexpr (kInRegs) {
+    if (k > 0) {
+      // 1. sample = first key of each run (0 sorts below every real key), sorted descending
+      sample[tid] = cnt > 0 ? key[0] : 0u;
+      __syncthreads();
+      for (int kk = 2; kk <= kSelThreads; kk <<= 1)
+        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+          const int l = tid ^ jj;
+          if (l > tid) {
+            const uint32_t x = sample[tid], y = sample[l];
+            const bool desc = (tid & kk) == 0;
+            if (desc ? (x < y) : (x > y)) {
+              sample[tid] = y;
+              sample[l] = x;
+            }
+          }
+          __syncthreads();
+        }
+      // 2. bracket [t_lo, t_hi] around the estimated sample rank of the k-th key
+      const int ns = (n_cand + C - 1) / C;  // runs that hold a sample
+      const float p = float(k) / float(n_cand);
+      const int est = int((long long)k * ns / n_cand);
+      const int margin = 16 + int(4.0f * sqrtf(float(ns) * p * (1.f - p)));
+      const uint32_t t_hi = est - margin >= 0 ? sample[est - margin] : 0xFFFFFFFFu;
+      const uint32_t t_lo = est + margin < ns ? sample[est + margin] : 0u;
+      uint32_t c_gt = 0, c_band = 0;
+      KVSEL_FOR_ITEMS(c_gt += u > t_hi; c_band += (u >= t_lo) & (u <= t_hi);)
+      uint32_t gt_tot, band_tot;
+      block_exclusive_scan(c_gt, scan_tmp, gt_tot);
+      const uint32_t band_base = block_exclusive_scan(c_band, scan_tmp, band_tot);
+      if (gt_tot < uint32_t(k) && uint32_t(k) <= gt_tot + band_tot && band_tot <= uint32_t(kBandMax)) {
+        // 3. gather the band and select exactly inside it
+        uint32_t w = band_base;
+        KVSEL_FOR_ITEMS(if ((u >= t_lo) & (u <= t_hi)) band[w++] = u;)
+        __syncthreads();
+        smem_radix_select(band, int(band_tot), uint32_t(k) - gt_tot, hist, &s_digit, &s_above, T,
+                          need_eq);
+        done = true;
+      }
+    }
+  }
+  if (k > 0 && !done) {
+    // full radix select, re-reading the row from global memory
     uint32_t prefix = 0, mask = 0, krem = uint32_t(k);
+    const int warp = tid >> 5, lane = tid & 31;
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       if (tid < 256) hist[tid] = 0;
       __syncthreads();
-      // warp-aggregated histogram: one shared atomic per distinct digit per warp
-      // step.  Every lane runs the same trip count (kR or C) for the collectives.
-      auto add = [&](uint32_t u, bool valid) {
-        const bool v = valid && (u & mask) == prefix;
-        const unsigned active = __ballot_sync(0xffffffffu, v);
-        if (v) {
-          const uint32_t digit = (u >> shift) & 255u;
-          const unsigned same = __match_any_sync(active, digit);
-          if (lane == __ffs(same) - 1) atomicAdd(&hist[digit], uint32_t(__popc(same)));
-        }
-      };
-      if constexpr (kInRegs) {
-#pragma unroll
-        for (int e = 0; e < kR; ++e) add(key[e], e < cnt);
-      } else {
-        for (int e = 0; e < C; ++e) add(e < cnt ? order_key(row[j0 + e]) : 0u, e < cnt);
+      for (int j = lo + tid; j < hi; j += kSelThreads) {
+        const uint32_t u = order_key(row[j]);
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
       }
       __syncthreads();
       if (warp == 0) {
-        // lane l owns bins 255-8l .. 255-8l-7; find the digit holding the krem-th largest
         uint32_t cb[8], lsum = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -189,6 +287,7 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
       krem -= s_above;
       prefix |= s_digit << shift;
       mask |= 0xFFu << shift;
+      __syncthreads();
     }
     T = prefix;
     need_eq = krem;
@@ -199,7 +298,6 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
   if (k > 0) {
     KVSEL_FOR_ITEMS(gt += u > T; eq += u == T;)
   }
-  uint32_t tot;
   const uint32_t eq_base = block_exclusive_scan(eq, scan_tmp, tot);
   const uint32_t take_eq = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
   const uint32_t out_base = block_exclusive_scan(gt + take_eq, scan_tmp, tot);
