@@ -54,6 +54,8 @@ _SIGS = {
     "kvsel_decode_attn_workspace": (_sz, [_PKV, _i, _i, _i]),
     "kvsel_decode_attn": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _f, _vp, _i, _vp,
                                _vp, _i, _i, _vp, _sz, _vp]),
+    "kvsel_decode_attn_noalloc": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _f, _vp, _i,
+                                       _vp, _vp, _i, _i, _vp]),
     "kvsel_h2o_evict_workspace": (_sz, [_PKV, _i, _i]),
     "kvsel_h2o_evict": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                              _sz, _vp]),
@@ -197,6 +199,38 @@ def kvsel_decode_attn(kv: PagedKV, block_table, seq_lens, q, out, workspace, *, 
         _ptr(k_new), _ptr(v_new), _ptr(pos_map), _ptr(next_pos), float(scale), _ptr(out), odt,
         _ptr(probs), _ptr(h2o_cum), int(max_len), int(num_ctas), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kvsel_decode_attn_noalloc(kv: PagedKV, block_table, seq_lens, q, out, *, k_new=None,
+                              v_new=None, pos_map=None, next_pos=None, scale=None, probs=None,
+                              h2o_cum=None, max_len=None, num_ctas=0, stream=None):
+    """kvsel_decode_attn without a workspace, for callers that cannot allocate.
+
+    The library's built-in 8 MiB device array serves as scratch; calls that
+    need more are rejected, and calls that overlap on the GPU race.
+    """
+    for t, dt, nm, opt in ((block_table, torch.int32, "block_table", False),
+                           (seq_lens, torch.int32, "seq_lens", False), (q, torch.bfloat16, "q", False),
+                           (k_new, torch.bfloat16, "k_new", True), (v_new, torch.bfloat16, "v_new", True),
+                           (pos_map, torch.int32, "pos_map", True), (next_pos, torch.int32, "next_pos", True),
+                           (probs, torch.float32, "probs", True), (h2o_cum, torch.float32, "h2o_cum", True)):
+        _need(t, dt, nm, opt)
+    if out.dtype not in (torch.bfloat16, torch.float32) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 or fp32 CUDA tensor")
+    if max_len is None:
+        for t in (probs, h2o_cum, pos_map):
+            if t is not None:
+                max_len = t.shape[-1]
+                break
+        else:
+            max_len = block_table.shape[1] * kv.page_size
+    if scale is None:
+        scale = kv.head_dim ** -0.5
+    odt = KVSEL_F32 if out.dtype == torch.float32 else KVSEL_BF16
+    _check(lib().kvsel_decode_attn_noalloc(
+        ctypes.byref(kv), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), seq_lens.shape[0],
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(pos_map), _ptr(next_pos), float(scale), _ptr(out), odt,
+        _ptr(probs), _ptr(h2o_cum), int(max_len), int(num_ctas), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------

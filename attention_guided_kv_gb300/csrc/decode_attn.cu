@@ -36,6 +36,8 @@
 // The CTA that owns the page of a sequence's appended slot writes k_new /
 // v_new into the pool (and the slot's original position) before its
 // producer starts, fencing the generic-proxy stores against the TMA reads.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace kvsel {
@@ -730,4 +732,68 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_decode_attn (launch)");
   return KVSEL_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of kvsel_decode_attn.
+//
+// Some callers cannot allocate device memory at the point where they run a
+// decode step: an allocator-less runtime embedding this library, a plug-in
+// whose host owns every allocation, or code that must not touch the
+// allocator mid-step.  For them the scratch the decode kernel needs (status
+// and grid-barrier words, per-CTA partial results, and the logit buffer when
+// no probability buffer is given) lives in the fixed array below, which every
+// GPU that loads this library holds until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+}  // namespace
+
+extern "C" kvsel_status kvsel_decode_attn_noalloc(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                                  int max_pages, int32_t* seq_lens, int batch,
+                                                  const void* q, const void* k_new, const void* v_new,
+                                                  int32_t* pos_map, int32_t* next_pos, float scale,
+                                                  void* out, int out_dtype, float* probs, float* h2o_cum,
+                                                  int max_len, int num_ctas, void* stream) {
+  const std::string fn = "kvsel_decode_attn_noalloc: ";
+  if (!kv || batch < 1 || max_len < 1 || kv->num_kv_heads < 1 || kv->num_q_heads < 1 ||
+      kv->num_q_heads % kv->num_kv_heads != 0)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "kv descriptor, batch >= 1 and max_len >= 1 are required");
+  const size_t need = decode_ws_layout(batch, kv->num_kv_heads, kv->num_q_heads, max_len,
+                                       probs != nullptr).total;
+  if (need > kNoAllocScratchBytes)
+    return fail(KVSEL_ERR_INVALID_ARG,
+                fn + "this call needs " + std::to_string(need) + " bytes of scratch, more than the " +
+                    std::to_string(kNoAllocScratchBytes) +
+                    "-byte built-in array (pass a probs buffer, or use kvsel_decode_attn with a workspace)");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "kvsel_decode_attn_noalloc (cudaGetDevice)");
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "device ordinal above 63");
+  void* scratch = nullptr;
+  {
+    // Set-up, once per device, with that device current: the array's name is
+    // only a host-side stand-in; the kernel needs its device address.
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_fail(e, "kvsel_decode_attn_noalloc (cudaGetSymbolAddress)");
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // The status word and the grid-barrier counters must start at zero; the
+  // array keeps whatever the previous call left there.
+  e = cudaMemsetAsync(scratch, 0, kStatusBytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvsel_decode_attn_noalloc (clear)");
+  return kvsel_decode_attn(kv, block_table, max_pages, seq_lens, batch, q, k_new, v_new, pos_map,
+                           next_pos, scale, out, out_dtype, probs, h2o_cum, max_len, num_ctas, scratch,
+                           kNoAllocScratchBytes, stream);
 }

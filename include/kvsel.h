@@ -143,6 +143,33 @@ KVSEL_API kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_t
                                float* probs, float* h2o_cum, int max_len, int num_ctas,
                                void* workspace, size_t ws_bytes, void* stream);
 
+/* Allocation-free kvsel_decode_attn.  The pages have no counterpart: this is
+ * for callers that cannot allocate device memory (a runtime without a device
+ * allocator, a plug-in whose host owns all allocations, code that must not
+ * call the allocator in the middle of a step).  It takes the same arguments
+ * as kvsel_decode_attn minus the workspace and computes the same results;
+ * its scratch is a fixed 8 MiB array inside this library that every GPU
+ * loading the library keeps until the process exits.
+ *  - The first call on a device looks up that array's device address (with
+ *    the device current); make that first call before any stream capture.
+ *  - Calls that need more scratch than 8 MiB are rejected with
+ *    KVSEL_ERR_INVALID_ARG: about (1024 + batch * num_kv_heads) * 4160 bytes,
+ *    plus batch * num_q_heads * max_len * 4 bytes when h2o_cum is given
+ *    without probs.
+ *  - Every call uses the same array, so calls that overlap on the GPU (other
+ *    streams, other threads) race and corrupt each other; serialise them.
+ *    Each call clears the array's status and barrier words first.
+ *  - Device-side problems (a block-table entry outside the pool) are not
+ *    reported back: there is no workspace to read them from.
+ * Nothing here calls cudaMalloc, cudaFree or any allocating library routine. */
+KVSEL_API kvsel_status kvsel_decode_attn_noalloc(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                                 int max_pages, int32_t* seq_lens, int batch,
+                                                 const void* q, const void* k_new, const void* v_new,
+                                                 int32_t* pos_map, int32_t* next_pos, float scale,
+                                                 void* out, int out_dtype, float* probs,
+                                                 float* h2o_cum, int max_len, int num_ctas,
+                                                 void* stream);
+
 /* ---------------------------------------------------------------------------
  * H2O heavy-hitter selection with StreamingLLM sinks + window, optional
  * in-place compaction.
