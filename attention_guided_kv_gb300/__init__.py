@@ -24,6 +24,8 @@ KVSEL_ERR_TIMEOUT = 4
 KVSEL_ERR_BAD_INDEX = 5
 KVSEL_BF16 = 0
 KVSEL_F32 = 1
+KVSEL_AGG_MAX, KVSEL_AGG_MEAN, KVSEL_AGG_TOPP = 0, 1, 2
+KVSEL_NORM_NONE, KVSEL_NORM_PERCENTILE = 0, 1
 
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT", 5: "BAD_INDEX"}
 
@@ -59,6 +61,9 @@ _SIGS = {
     "kvsel_h2o_evict_workspace": (_sz, [_PKV, _i, _i]),
     "kvsel_h2o_evict": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                              _sz, _vp]),
+    "kvsel_block_priority_workspace": (_sz, [_i, ctypes.c_int64]),
+    "kvsel_block_priority": (_i, [_vp, _vp, _f, _vp, _i, _i, _i, _f, _i, _f, _vp, ctypes.c_int64, _vp,
+                                  ctypes.c_int64, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -261,3 +266,29 @@ def kvsel_h2o_evict(kv: PagedKV, block_table, seq_lens, h2o_cum, workspace, *, b
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
     """A zeroed, 256-byte aligned workspace buffer (status word cleared)."""
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------------------
+# block offload priority
+# ----------------------------------------------------------------------------
+def kvsel_block_priority_workspace(num_requests: int, max_total_blocks: int) -> int:
+    return int(lib().kvsel_block_priority_workspace(num_requests, max_total_blocks))
+
+
+def kvsel_block_priority(token_scores, req_offsets, order_out, n_out, workspace, *, block_size, agg,
+                         norm, evict_frac, increment=None, decay=1.0, top_p=0.1, block_score_out=None,
+                         max_total_blocks=None, stream=None):
+    """Decay update + token->block fold + per-request percentile + global evict order."""
+    _need(token_scores, torch.float32, "token_scores")
+    _need(increment, torch.float32, "increment", True)
+    _need(req_offsets, torch.int64, "req_offsets")
+    _need(order_out, torch.int64, "order_out")
+    _need(n_out, torch.int64, "n_out")
+    _need(block_score_out, torch.float32, "block_score_out", True)
+    if max_total_blocks is None:
+        max_total_blocks = block_score_out.numel() if block_score_out is not None else token_scores.numel()
+    _check(lib().kvsel_block_priority(
+        _ptr(token_scores), _ptr(increment), float(decay), _ptr(req_offsets), req_offsets.numel() - 1,
+        int(block_size), int(agg), float(top_p), int(norm), float(evict_frac), _ptr(block_score_out),
+        int(max_total_blocks), _ptr(order_out), order_out.numel(), _ptr(n_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))

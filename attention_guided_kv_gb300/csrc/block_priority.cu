@@ -1,0 +1,501 @@
+// Block offload priority from per-token attention scores (sm_103a).
+//
+// What it computes ("Sparse attention x KV-cache offloading: eight
+// questions" §2.1, §3.1, §3.2, §5.1): optionally age every token score by
+// exponential decay and add this step's attention (score <- decay * score +
+// increment), fold the tokens of each block into one block score (max, mean,
+// or the mean of the ceil(p * n) largest of the block's n valid tokens),
+// normalise per request (the block's percentile inside its own request,
+// fp32(2r + 1) / fp32(2n) for rank r by (score asc, block asc), or no
+// normalisation), and emit the global eviction order: every block of every
+// request sorted by (normalised score asc, request asc, block asc), the first
+// ceil(frac * N) of them, as (request << 32) | block.
+//
+// Kernels (one call, four launches on the caller's stream):
+//   bp_prefix_kernel  one CTA: blocks per request -> block offsets, N, the
+//                     evict count; checks every length against the limits.
+//   bp_fold_kernel    one warp per block (grid-stride): decay update of the
+//                     block's tokens (written back) and the fold.
+//   bp_rank_kernel    one CTA per request (percentile only): bitonic sort of
+//                     the request's (score, block) keys in shared memory; the
+//                     rank gives the percentile key of each block.
+//   bp_sort_kernel    cooperative: stable LSD radix sort of the N 32-bit keys
+//                     (4-bit digits, 8 passes, two bounded grid barriers per
+//                     pass).  The input is in (request, block) order and the
+//                     sort is stable, so equal keys keep (request, block)
+//                     order, which is the specified tie-break.  The first
+//                     ceil(frac * N) codes go to the output.
+#include "common.cuh"
+
+namespace kvsel {
+
+constexpr int kBpMaxBlockSize = 256;          // tokens per block: the pages' 16..256
+constexpr int kBpMaxReqBlocks = 16384;        // blocks per request (shared-memory rank sort)
+constexpr int kBpSortThreads = 256;
+constexpr int kBpMaxSortCtas = 256;
+
+struct BpParams {
+  float* tok;                // token scores (CSR by request), updated in place
+  const float* inc;          // increments or null
+  const int64_t* off;        // [R+1] token offsets
+  float* bscore_out;         // [max_blocks] or null
+  int64_t* order_out;        // [order_cap]
+  int64_t* n_out;            // [2]: evict count, total blocks
+  int64_t* blk_off;          // workspace [R+1]
+  float* bscore;             // workspace [max_blocks]
+  uint32_t* key[2];          // workspace [max_blocks] x 2
+  int64_t* val[2];           // workspace [max_blocks] x 2
+  int64_t* meta;             // workspace [2]: N (or -1), evict count
+  unsigned* hist;            // workspace [kBpMaxSortCtas][16]
+  unsigned* bar;             // grid-barrier words
+  int* status;
+  int64_t max_blocks, order_cap;
+  int R, bs, agg, norm;
+  float decay, top_p, frac;
+};
+
+__device__ __forceinline__ int bp_request_of(const int64_t* blk_off, int R, int64_t g) {
+  int lo = 0, hi = R - 1;  // last r with blk_off[r] <= g
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (blk_off[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(1024) bp_prefix_kernel(const BpParams P) {
+  __shared__ long long warp_tot[33];
+  __shared__ int bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  long long carry = 0;
+  for (int base = 0; base < P.R; base += 1024) {
+    const int r = base + tid;
+    long long nb = 0;
+    if (r < P.R) {
+      const long long len = P.off[r + 1] - P.off[r];
+      if (len < 0) bad = KVSEL_ERR_BAD_INDEX;
+      nb = len > 0 ? (len + P.bs - 1) / P.bs : 0;
+      if (nb > kBpMaxReqBlocks) bad = KVSEL_ERR_UNSUPPORTED;
+    }
+    long long x = nb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      const long long t = warp_tot[lane];
+      long long sc = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, sc, o);
+        if (lane >= o) sc += y;
+      }
+      warp_tot[lane] = sc - t;
+      if (lane == 31) warp_tot[32] = sc;
+    }
+    __syncthreads();
+    if (r < P.R) P.blk_off[r] = carry + warp_tot[warp] + x - nb;
+    carry += warp_tot[32];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    P.blk_off[P.R] = carry;
+    if (!bad && carry > P.max_blocks) bad = KVSEL_ERR_BAD_INDEX;
+    const long long n_evict = bad ? 0 : (long long)ceil((double)P.frac * (double)carry);
+    if (bad) report(P.status, bad);
+    P.meta[0] = bad ? -1 : carry;
+    P.meta[1] = n_evict;
+    P.n_out[0] = n_evict;
+    P.n_out[1] = bad ? -1 : carry;
+  }
+}
+
+__global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
+  const long long N = P.meta[0];
+  if (N <= 0) return;
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  constexpr int kPer = kBpMaxBlockSize / 32;
+  for (long long g = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < N; g += warps) {
+    const int r = bp_request_of(P.blk_off, P.R, g);
+    const long long t0 = P.off[r] + (g - P.blk_off[r]) * P.bs;
+    const int n = int(min((long long)P.bs, P.off[r + 1] - t0));
+    float v[kPer];
+    float sum = 0.f, mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int t = lane + 32 * e;
+      v[e] = -INFINITY;
+      if (t < n) {
+        float s = P.tok[t0 + t];
+        if (P.inc) {
+          s = fmaf(P.decay, s, P.inc[t0 + t]);
+          P.tok[t0 + t] = s;
+        }
+        v[e] = s;
+        sum += s;
+        mx = fmaxf(mx, s);
+      }
+    }
+    float result;
+    if (P.agg == 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      result = mx;
+    } else if (P.agg == 1) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      result = __fdiv_rn(sum, float(n));
+    } else {
+      // mean of the ceil(p * n) largest (p * n as an fp32 product): take the
+      // warp maximum k times, removing one copy each time
+      const int k = max(1, int(ceilf(__fmul_rn(P.top_p, float(n)))));
+      float acc = 0.f;
+      for (int it = 0; it < k; ++it) {
+        float lm = -INFINITY;
+        int le = 0;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+          if (v[e] > lm) {
+            lm = v[e];
+            le = e;
+          }
+        float wm = lm;
+        int wl = lane;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float om = __shfl_xor_sync(0xffffffffu, wm, o);
+          const int ol = __shfl_xor_sync(0xffffffffu, wl, o);
+          if (om > wm || (om == wm && ol < wl)) {
+            wm = om;
+            wl = ol;
+          }
+        }
+        acc += wm;
+        if (lane == wl) {
+#pragma unroll
+          for (int e = 0; e < kPer; ++e)
+            if (e == le) v[e] = -INFINITY;
+        }
+      }
+      result = __fdiv_rn(acc, float(k));
+    }
+    if (lane == 0) {
+      P.bscore[g] = result;
+      if (P.bscore_out) P.bscore_out[g] = result;
+      if (P.norm == 0) {  // no normalisation: sort directly on the block score
+        P.key[0][g] = order_key(result);
+        P.val[0][g] = ((long long)r << 32) | (g - P.blk_off[r]);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) bp_rank_kernel(const BpParams P) {
+  extern __shared__ unsigned long long skeys[];
+  if (P.meta[0] <= 0) return;
+  const int r = blockIdx.x;
+  const long long b0 = P.blk_off[r];
+  const int n = int(P.blk_off[r + 1] - b0);
+  if (n == 0) return;
+  int npow = 1;
+  while (npow < n) npow <<= 1;
+  for (int i = threadIdx.x; i < npow; i += blockDim.x)
+    skeys[i] = i < n ? ((unsigned long long)order_key(P.bscore[b0 + i]) << 32) | unsigned(i)
+                     : ~0ull;
+  __syncthreads();
+  for (int kk = 2; kk <= npow; kk <<= 1)
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+      for (int i = threadIdx.x; i < npow; i += blockDim.x) {
+        const int l = i ^ jj;
+        if (l > i) {
+          const unsigned long long x = skeys[i], y = skeys[l];
+          const bool up = (i & kk) == 0;
+          if (up ? (x > y) : (x < y)) {
+            skeys[i] = y;
+            skeys[l] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const unsigned blk = unsigned(skeys[i] & 0xffffffffu);
+    const float pct = __fdiv_rn(float(2 * i + 1), float(2 * n));  // correctly rounded
+    P.key[0][b0 + blk] = __float_as_uint(pct);                    // pct > 0: bits are monotone
+    P.val[0][b0 + blk] = ((long long)r << 32) | blk;
+  }
+}
+
+__device__ __forceinline__ void bp_grid_barrier(unsigned* bar, int* status) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned* gen = bar + 32;
+    const unsigned g = *gen;
+    __threadfence();
+    if (atomicAdd(bar, 1u) + 1u == gridDim.x) {
+      bar[0] = 0u;
+      __threadfence();
+      atomicAdd(bar + 32, 1u);
+    } else {
+      unsigned spins = 0;
+      while (*gen == g) {
+        __nanosleep(32);
+        if (++spins > (1u << 26)) {  // a few seconds
+          report(status, KVSEL_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams P) {
+  __shared__ unsigned cnt[16][kBpSortThreads];
+  __shared__ unsigned base[16];
+  __shared__ unsigned sTot[kBpSortThreads / 16][16], sBefore[kBpSortThreads / 16][16];
+  __shared__ unsigned warp_tot[kBpSortThreads / 32 + 1];
+  const long long N = P.meta[0];
+  if (N < 0) return;  // same for every CTA
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int NC = gridDim.x, c = blockIdx.x;
+  const long long c0 = N * c / NC, c1 = N * (c + 1) / NC;
+  const long long per = (c1 - c0 + kBpSortThreads - 1) / kBpSortThreads;
+  const long long t0 = min(c1, c0 + per * tid), t1 = min(c1, t0 + per);
+
+#pragma unroll 1
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 4 * pass;
+    const uint32_t* ik = P.key[pass & 1];
+    const int64_t* iv = P.val[pass & 1];
+    uint32_t* ok = P.key[(pass + 1) & 1];
+    int64_t* ov = P.val[(pass + 1) & 1];
+    for (int d = 0; d < 16; ++d) cnt[d][tid] = 0;
+    for (long long e = t0; e < t1; ++e) ++cnt[(ik[e] >> shift) & 15u][tid];
+    __syncthreads();
+    // per digit: exclusive scan over threads (thread order = input order)
+    for (int d = 0; d < 16; ++d) {
+      const unsigned v = cnt[d][tid];
+      unsigned x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) warp_tot[warp] = x;
+      __syncthreads();
+      if (warp == 0) {
+        const unsigned t = lane < kBpSortThreads / 32 ? warp_tot[lane] : 0u;
+        unsigned s = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_up_sync(0xffffffffu, s, o);
+          if (lane >= o) s += y;
+        }
+        if (lane < kBpSortThreads / 32) warp_tot[lane] = s - t;
+        if (lane == 31) warp_tot[kBpSortThreads / 32] = s;
+      }
+      __syncthreads();
+      cnt[d][tid] = warp_tot[warp] + x - v;  // exclusive offset inside this CTA
+      if (tid == 0) P.hist[c * 16 + d] = warp_tot[kBpSortThreads / 32];
+      __syncthreads();
+    }
+    bp_grid_barrier(P.bar, P.status);
+    {
+      // start of digit d for this CTA = all keys with a smaller digit + this
+      // digit's keys in earlier CTAs; 16 stripes of CTAs x 16 digits in parallel
+      const int d = tid & 15, stripe = tid >> 4;
+      unsigned tot = 0, before = 0;
+      for (int cc = stripe; cc < NC; cc += kBpSortThreads / 16) {
+        const unsigned h = __ldcg(P.hist + cc * 16 + d);
+        tot += h;
+        if (cc < c) before += h;
+      }
+      sTot[stripe][d] = tot;
+      sBefore[stripe][d] = before;
+      __syncthreads();
+      if (tid < 16) {
+        unsigned t = 0, b = 0;
+        for (int st = 0; st < kBpSortThreads / 16; ++st) {
+          t += sTot[st][tid];
+          b += sBefore[st][tid];
+        }
+        sTot[0][tid] = t;   // digit totals (read below by thread 0 only after the sync)
+        base[tid] = b;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        unsigned run = 0;
+        for (int dd = 0; dd < 16; ++dd) {
+          const unsigned t = sTot[0][dd];
+          base[dd] += run;
+          run += t;
+        }
+      }
+    }
+    __syncthreads();
+    for (long long e = t0; e < t1; ++e) {
+      const uint32_t k = ik[e];
+      const unsigned d = (k >> shift) & 15u;
+      const unsigned pos = base[d] + cnt[d][tid]++;
+      ok[pos] = k;
+      ov[pos] = iv[e];
+    }
+    bp_grid_barrier(P.bar, P.status);
+  }
+  // 8 passes: the sorted keys are back in buffer 0
+  const long long n_ev = min(P.meta[1], P.order_cap);
+  for (long long i = (long long)c * kBpSortThreads + tid; i < n_ev; i += (long long)NC * kBpSortThreads)
+    P.order_out[i] = __ldcg(P.val[0] + i);
+}
+
+}  // namespace kvsel
+
+using namespace kvsel;
+using namespace kvsel_host;
+
+namespace {
+struct BpWs {
+  size_t blk_off, bscore, key0, key1, val0, val1, meta, hist, total;
+};
+BpWs bp_ws_layout(int R, long long max_blocks) {
+  BpWs w;
+  size_t off = kStatusBytes;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  w.blk_off = take(size_t(R + 1) * 8);
+  w.bscore = take(size_t(max_blocks) * 4);
+  w.key0 = take(size_t(max_blocks) * 4);
+  w.key1 = take(size_t(max_blocks) * 4);
+  w.val0 = take(size_t(max_blocks) * 8);
+  w.val1 = take(size_t(max_blocks) * 8);
+  w.meta = take(16);
+  w.hist = take(size_t(kBpMaxSortCtas) * 16 * 4);
+  w.total = off;
+  return w;
+}
+}  // namespace
+
+extern "C" size_t kvsel_block_priority_workspace(int num_requests, int64_t max_total_blocks) {
+  if (num_requests < 1 || max_total_blocks < 1) return 0;
+  return bp_ws_layout(num_requests, max_total_blocks).total;
+}
+
+extern "C" kvsel_status kvsel_block_priority(float* token_scores, const float* increment, float decay,
+                                             const int64_t* req_offsets, int num_requests, int block_size,
+                                             int agg, float top_p, int norm, float evict_frac,
+                                             float* block_score_out, int64_t max_total_blocks,
+                                             int64_t* order_out, int64_t order_capacity, int64_t* n_out,
+                                             void* workspace, size_t ws_bytes, void* stream) {
+  const std::string fn = "kvsel_block_priority: ";
+  if (!token_scores || !req_offsets || !n_out || num_requests < 1 || max_total_blocks < 1)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "token_scores, req_offsets, n_out are required; num_requests, "
+                                            "max_total_blocks >= 1");
+  if (block_size < 1 || block_size > kBpMaxBlockSize)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "block_size must be in [1, 256]");
+  if (agg < KVSEL_AGG_MAX || agg > KVSEL_AGG_TOPP)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "agg must be KVSEL_AGG_MAX, _MEAN or _TOPP");
+  if (norm != KVSEL_NORM_NONE && norm != KVSEL_NORM_PERCENTILE)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "norm must be KVSEL_NORM_NONE or KVSEL_NORM_PERCENTILE");
+  if (agg == KVSEL_AGG_TOPP && !(top_p > 0.f && top_p <= 1.f))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "top_p must be in (0, 1]");
+  if (!(evict_frac >= 0.f && evict_frac <= 1.f))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "evict_frac must be in [0, 1]");
+  if (increment && !(decay == decay))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "decay must be a number");
+  if (order_capacity < 0 || (order_capacity > 0 && !order_out))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "order_out is required when order_capacity > 0");
+  if (max_total_blocks >= (1LL << 31))
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "at most 2^31 - 1 blocks");
+  if (!workspace || !aligned(workspace, 256))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "a 256-byte aligned workspace is required");
+  const BpWs L = bp_ws_layout(num_requests, max_total_blocks);
+  if (ws_bytes < L.total)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace too small: need " + std::to_string(L.total));
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BpParams P;
+  P.tok = token_scores;
+  P.inc = increment;
+  P.off = req_offsets;
+  P.bscore_out = block_score_out;
+  P.order_out = order_out;
+  P.n_out = n_out;
+  P.blk_off = reinterpret_cast<int64_t*>(ws + L.blk_off);
+  P.bscore = reinterpret_cast<float*>(ws + L.bscore);
+  P.key[0] = reinterpret_cast<uint32_t*>(ws + L.key0);
+  P.key[1] = reinterpret_cast<uint32_t*>(ws + L.key1);
+  P.val[0] = reinterpret_cast<int64_t*>(ws + L.val0);
+  P.val[1] = reinterpret_cast<int64_t*>(ws + L.val1);
+  P.meta = reinterpret_cast<int64_t*>(ws + L.meta);
+  P.hist = reinterpret_cast<unsigned*>(ws + L.hist);
+  P.bar = reinterpret_cast<unsigned*>(ws + 64);
+  P.status = reinterpret_cast<int*>(ws);
+  P.max_blocks = max_total_blocks;
+  P.order_cap = order_capacity;
+  P.R = num_requests;
+  P.bs = block_size;
+  P.agg = agg;
+  P.norm = norm;
+  P.decay = decay;
+  P.top_p = top_p;
+  P.frac = evict_frac;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  trace_before("bp_prefix", st);
+  bp_prefix_kernel<<<1, 1024, 0, st>>>(P);
+  e = cudaGetLastError();
+  trace_after(st);
+  if (e != cudaSuccess) return cuda_fail(e, "kvsel_block_priority (prefix launch)");
+
+  const int sms = sm_count();
+  trace_before("bp_fold", st);
+  bp_fold_kernel<<<sms * 8, 256, 0, st>>>(P);
+  e = cudaGetLastError();
+  trace_after(st);
+  if (e != cudaSuccess) return cuda_fail(e, "kvsel_block_priority (fold launch)");
+
+  if (norm == KVSEL_NORM_PERCENTILE) {
+    const size_t smem = size_t(kBpMaxReqBlocks) * 8;
+    static bool attr_set = false;
+    if (!attr_set) {
+      e = cudaFuncSetAttribute(bp_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+      if (e != cudaSuccess) return cuda_fail(e, "kvsel_block_priority (rank attribute)");
+      attr_set = true;
+    }
+    trace_before("bp_rank", st);
+    bp_rank_kernel<<<num_requests, 1024, smem, st>>>(P);
+    e = cudaGetLastError();
+    trace_after(st);
+    if (e != cudaSuccess) return cuda_fail(e, "kvsel_block_priority (rank launch)");
+  }
+
+  // cooperative sort: CTAs co-resident (<= one per SM here), ~2K keys per CTA
+  int nc = int(std::min<long long>((max_total_blocks + 2047) / 2048, (long long)sms));
+  nc = std::max(1, std::min(nc, kBpMaxSortCtas));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nc);
+  cfg.blockDim = dim3(kBpSortThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  trace_before("bp_sort", st);
+  e = cudaLaunchKernelEx(&cfg, bp_sort_kernel, P);
+  trace_after(st);
+  if (e != cudaSuccess) return cuda_fail(e, "kvsel_block_priority (sort launch)");
+  return KVSEL_OK;
+}

@@ -208,6 +208,52 @@ KVSEL_API kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block_
                              int32_t* keep_out, int32_t* freed_pages, void* workspace,
                              size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Block offload priority: decay aging, token -> block fold, per-request
+ * percentile, global eviction order.
+ *
+ * Defines ("Sparse attention x KV-cache offloading: eight questions" §2.1
+ * exponential decay, §3.1 token -> block aggregation, §3.2 per-request
+ * percentile normalisation, §5.1 fp32 score per block):
+ *   if increment: score[t] = fmaf(decay, score[t], increment[t]) (in place)
+ *   block i of request r covers tokens [i*block_size, (i+1)*block_size) of r,
+ *   valid ones only; its score is the max, the mean, or (TOPP) the mean of
+ *   the ceil(top_p * n) largest (top_p * n as an fp32 product) of its n
+ *   valid tokens;
+ *   PERCENTILE: rank q of the block in its request by (score asc, block asc),
+ *   key = fp32(2q + 1) / fp32(2n_r) (correctly rounded); NONE: key = score;
+ *   order = all blocks sorted by (key asc, request asc, block asc); the first
+ *   ceil(evict_frac * N) (evaluated in double) are written as
+ *   (request << 32) | block.
+ *
+ * Arguments (device pointers unless noted):
+ *   token_scores  fp32 [total tokens], requests laid out back to back (CSR).
+ *   increment     fp32, same layout, or NULL (no update).
+ *   req_offsets   int64 [num_requests + 1] token offsets, non-decreasing.
+ *   block_size    1..256 tokens; at most 16384 blocks per request.
+ *   agg           KVSEL_AGG_MAX / _MEAN / _TOPP;  norm  KVSEL_NORM_*.
+ *   block_score_out  fp32 [max_total_blocks] or NULL: block scores in
+ *                 (request, block) order.
+ *   max_total_blocks  host-side upper bound on the total block count N.
+ *   order_out     int64 [order_capacity]; entries past the evict count are
+ *                 not written.
+ *   n_out         int64 [2]: the evict count and N (-1 if the lengths were
+ *                 rejected on the device).
+ * Device-detected problems: N > max_total_blocks or a negative length ->
+ * KVSEL_ERR_BAD_INDEX; more than 16384 blocks in one request ->
+ * KVSEL_ERR_UNSUPPORTED; in both cases nothing else is computed.
+ */
+typedef enum kvsel_block_agg { KVSEL_AGG_MAX = 0, KVSEL_AGG_MEAN = 1, KVSEL_AGG_TOPP = 2 } kvsel_block_agg;
+typedef enum kvsel_block_norm { KVSEL_NORM_NONE = 0, KVSEL_NORM_PERCENTILE = 1 } kvsel_block_norm;
+KVSEL_API size_t kvsel_block_priority_workspace(int num_requests, int64_t max_total_blocks);
+KVSEL_API kvsel_status kvsel_block_priority(float* token_scores, const float* increment, float decay,
+                                            const int64_t* req_offsets, int num_requests,
+                                            int block_size, int agg, float top_p, int norm,
+                                            float evict_frac, float* block_score_out,
+                                            int64_t max_total_blocks, int64_t* order_out,
+                                            int64_t order_capacity, int64_t* n_out, void* workspace,
+                                            size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

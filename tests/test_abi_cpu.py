@@ -109,3 +109,23 @@ def test_evict_host_validation(lib):
     assert st(ws_bytes=8) == K.KVSEL_ERR_INVALID_ARG
     assert st(kv=_kv(page_size=8)) == K.KVSEL_ERR_UNSUPPORTED
     assert st(compact=1, kv=_kv(k_pool=None)) == K.KVSEL_ERR_INVALID_ARG
+
+
+def test_block_priority_host_validation(lib):
+    def st(**over):
+        a = dict(tok=16, inc=None, decay=0.98, off=16, R=4, bs=16, agg=0, top_p=0.1, norm=1,
+                 frac=0.25, bso=None, maxb=100, order=16, cap=25, n_out=16, ws=256, ws_bytes=1 << 20)
+        a.update(over)
+        return lib.kvsel_block_priority(a["tok"], a["inc"], a["decay"], a["off"], a["R"], a["bs"],
+                                        a["agg"], a["top_p"], a["norm"], a["frac"], a["bso"], a["maxb"],
+                                        a["order"], a["cap"], a["n_out"], a["ws"], a["ws_bytes"], None)
+    assert st(bs=0) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(bs=512) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(agg=3) == K.KVSEL_ERR_INVALID_ARG
+    assert st(norm=2) == K.KVSEL_ERR_INVALID_ARG
+    assert st(agg=2, top_p=0.0) == K.KVSEL_ERR_INVALID_ARG
+    assert st(frac=1.5) == K.KVSEL_ERR_INVALID_ARG
+    assert st(order=None) == K.KVSEL_ERR_INVALID_ARG
+    assert st(tok=None) == K.KVSEL_ERR_INVALID_ARG
+    assert st(ws_bytes=64) == K.KVSEL_ERR_INVALID_ARG
+    assert K.kvsel_block_priority_workspace(64, 150000) > 150000 * 28

@@ -1,0 +1,153 @@
+"""GPU parity of block offload priority against the oracle.
+
+* block scores (and the decayed token scores) within relative L2 2e-3 of the
+  fp64 oracle;
+* the eviction order bit-exact when the oracle's percentile / order routines
+  are fed the GPU's own fp32 block scores (the selection is compared on
+  identical inputs);
+* with max aggregation and no update the block scores are exact, so the
+  order must also equal the oracle's end to end.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import block_priority as BP
+from _harness import rel_l2
+
+import attention_guided_kv_gb300 as K
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+def _run(tok, offsets, bs, agg, norm, frac, inc=None, decay=1.0, top_p=0.1):
+    dev = "cuda"
+    R = len(offsets) - 1
+    nblk = sum(int(-(-int(offsets[r + 1] - offsets[r]) // bs)) for r in range(R))
+    maxb = max(nblk, 1)
+    t_tok = torch.from_numpy(np.asarray(tok, dtype=np.float32)).to(dev)
+    t_inc = None if inc is None else torch.from_numpy(np.asarray(inc, dtype=np.float32)).to(dev)
+    t_off = torch.from_numpy(np.asarray(offsets, dtype=np.int64)).to(dev)
+    bso = torch.full((maxb,), float("nan"), device=dev)
+    cap = max(1, math.ceil(frac * maxb))
+    order = torch.full((cap,), -7, dtype=torch.int64, device=dev)
+    n_out = torch.zeros(2, dtype=torch.int64, device=dev)
+    ws = K.workspace(K.kvsel_block_priority_workspace(R, maxb))
+    K.kvsel_block_priority(t_tok, t_off, order, n_out, ws, block_size=bs, agg=agg, norm=norm,
+                           evict_frac=frac, increment=t_inc, decay=decay, top_p=top_p,
+                           block_score_out=bso, max_total_blocks=maxb)
+    assert K.read_status(ws) == 0
+    n_ev, N = n_out.cpu().tolist()
+    assert N == nblk
+    return t_tok.cpu().numpy(), bso.cpu().numpy()[:nblk], order.cpu().numpy()[:n_ev], n_ev
+
+
+def _split(blk, offsets, bs):
+    out, g = [], 0
+    for r in range(len(offsets) - 1):
+        n = int(-(-int(offsets[r + 1] - offsets[r]) // bs))
+        out.append(blk[g:g + n])
+        g += n
+    return out
+
+
+def _expected_order(blocks_per_req, norm, frac):
+    if norm == BP.NORM_PERCENTILE:
+        keys = [BP.percentiles(b.astype(np.float64)).astype(np.float64) for b in blocks_per_req]
+    else:
+        keys = [b.astype(np.float64) for b in blocks_per_req]
+    return BP.evict_order(keys, float(np.float32(frac)))
+
+
+@pytest.mark.parametrize("bs", [16, 64, 256])
+@pytest.mark.parametrize("agg", [BP.AGG_MAX, BP.AGG_MEAN, BP.AGG_TOPP])
+def test_fold_and_order_small_workload(bs, agg):
+    wl = workloads.block_priority(seed=7, R=9, steps=3, min_len=300, max_len=9000)
+    off = wl.offsets
+    tok = wl.increments(0)
+    inc = wl.increments(1)
+    new_tok, blk, order, n_ev = _run(tok, off, bs, agg, BP.NORM_PERCENTILE, 0.25, inc=inc, decay=0.98)
+    want_tok = BP.decay_update(tok.astype(np.float64), inc.astype(np.float64), 0.98)
+    assert rel_l2(new_tok, want_tok) < 1e-6
+    want_blk = np.concatenate([BP.block_scores(want_tok[off[r]:off[r + 1]], bs, agg, 0.1)
+                               for r in range(wl.R)])
+    assert rel_l2(blk, want_blk) < TOL
+    # same fp32 block scores into the oracle's normalisation + order: bit-exact
+    want = _expected_order(_split(blk, off, bs), BP.NORM_PERCENTILE, 0.25)
+    assert n_ev == len(want) == math.ceil(0.25 * len(blk))
+    np.testing.assert_array_equal(order, want)
+
+
+@pytest.mark.parametrize("norm", [BP.NORM_PERCENTILE, BP.NORM_NONE])
+def test_max_aggregation_order_is_exact_end_to_end(norm):
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 3000, 13)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    tok = (rng.integers(0, 40, int(off[-1])) * 0.25).astype(np.float32)    # many ties
+    _, blk, order, _ = _run(tok, off, 16, BP.AGG_MAX, norm, 0.4)
+    blocks, normed, want = BP.priority_pass(tok.astype(np.float64), off, 16, BP.AGG_MAX, 0.1, norm, 0.4)
+    np.testing.assert_array_equal(blk, np.concatenate(blocks).astype(np.float32))
+    np.testing.assert_array_equal(order, want)
+
+
+def test_edge_cases():
+    # single-token requests, an empty request, frac 0 and 1
+    off = np.array([0, 1, 1, 5, 37], dtype=np.int64)
+    tok = np.linspace(1.0, 0.0, 37).astype(np.float32)
+    for frac in (0.0, 1.0):
+        _, blk, order, n_ev = _run(tok, off, 16, BP.AGG_MEAN, BP.NORM_PERCENTILE, frac)
+        want = _expected_order(_split(blk, off, 16), BP.NORM_PERCENTILE, frac)
+        assert n_ev == len(want)
+        np.testing.assert_array_equal(order, want)
+    _, blk, _, _ = _run(tok, off, 16, BP.AGG_TOPP, BP.NORM_NONE, 0.5, top_p=1.0)
+    want = np.concatenate([BP.block_scores(tok[off[r]:off[r + 1]].astype(np.float64), 16, BP.AGG_TOPP, 1.0)
+                           for r in range(4)])
+    assert rel_l2(blk, want) < 1e-6
+
+
+def test_dirichlet_decay_invariant_on_device():
+    # increments sum to one per request per step: after T steps each request's
+    # token scores sum to (1 - 0.98^T) / (1 - 0.98)
+    wl = workloads.block_priority(seed=3, R=6, steps=40, min_len=4096, max_len=20000)
+    off = wl.offsets
+    tok = np.zeros(wl.total_tokens, dtype=np.float32)
+    R = wl.R
+    t_tok = torch.from_numpy(tok).cuda()
+    t_off = torch.from_numpy(off).cuda()
+    nblk = int(sum(-(-int(x) // 64) for x in wl.lengths))
+    order = torch.zeros(nblk, dtype=torch.int64, device="cuda")
+    n_out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    ws = K.workspace(K.kvsel_block_priority_workspace(R, nblk))
+    for t in range(wl.steps):
+        inc = torch.from_numpy(wl.increments(t)).cuda()
+        K.kvsel_block_priority(t_tok, t_off, order, n_out, ws, block_size=64, agg=BP.AGG_MEAN,
+                               norm=BP.NORM_PERCENTILE, evict_frac=0.25, increment=inc, decay=0.98,
+                               max_total_blocks=nblk)
+    sums = np.add.reduceat(t_tok.double().cpu().numpy(), off[:-1])
+    np.testing.assert_allclose(sums, (1 - 0.98 ** 40) / (1 - 0.98), rtol=1e-4)
+    assert K.read_status(ws) == 0
+
+
+@pytest.mark.slow
+def test_full_size_64_requests_all_variants():
+    """64 requests, 4K..128K tokens: every block size / aggregation, order bit-exact."""
+    wl = workloads.block_priority()
+    off = wl.offsets
+    tok = wl.increments(0)
+    inc = wl.increments(1)
+    want_tok = BP.decay_update(tok.astype(np.float64), inc.astype(np.float64), 0.98)
+    for bs in (16, 64, 256):
+        for agg in (BP.AGG_MAX, BP.AGG_MEAN, BP.AGG_TOPP):
+            new_tok, blk, order, n_ev = _run(tok, off, bs, agg, BP.NORM_PERCENTILE, 0.25, inc=inc,
+                                             decay=0.98)
+            assert rel_l2(new_tok, want_tok) < 1e-6
+            if agg == BP.AGG_MAX:
+                want_blk = np.concatenate([BP.block_scores(new_tok[off[r]:off[r + 1]], bs, agg)
+                                           for r in range(wl.R)])
+                assert rel_l2(blk, want_blk) < TOL
+            want = _expected_order(_split(blk, off, bs), BP.NORM_PERCENTILE, 0.25)
+            np.testing.assert_array_equal(order, want)
