@@ -64,6 +64,9 @@ _SIGS = {
     "kvsel_block_priority_workspace": (_sz, [_i, ctypes.c_int64]),
     "kvsel_block_priority": (_i, [_vp, _vp, _f, _vp, _i, _i, _i, _f, _i, _f, _vp, ctypes.c_int64, _vp,
                                   ctypes.c_int64, _vp, _vp, _sz, _vp]),
+    "kvsel_sparse_decode_workspace": (_sz, [_PKV, _i, _i, _i, _i]),
+    "kvsel_sparse_decode": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                 _i, _f, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -291,4 +294,38 @@ def kvsel_block_priority(token_scores, req_offsets, order_out, n_out, workspace,
         _ptr(token_scores), _ptr(increment), float(decay), _ptr(req_offsets), req_offsets.numel() - 1,
         int(block_size), int(agg), float(top_p), int(norm), float(evict_frac), _ptr(block_score_out),
         int(max_total_blocks), _ptr(order_out), order_out.numel(), _ptr(n_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------
+# DSA-style sparse decode
+# ----------------------------------------------------------------------------
+def kvsel_sparse_decode_workspace(kv: PagedKV, batch: int, max_len: int, top_k: int,
+                                  with_scores_out: bool) -> int:
+    return int(lib().kvsel_sparse_decode_workspace(ctypes.byref(kv), batch, max_len, top_k,
+                                                   int(with_scores_out)))
+
+
+def kvsel_sparse_decode(kv: PagedKV, block_table, seq_lens, q, idx_q, idx_w, idx_k, out, workspace, *,
+                        top_k=2048, k_new=None, v_new=None, idx_k_new=None, scale=None, topk_out=None,
+                        scores_out=None, stream=None):
+    """Indexer scores -> top-k positions -> attention over the selected keys."""
+    for t, dt, nm, opt in ((block_table, torch.int32, "block_table", False),
+                           (seq_lens, torch.int32, "seq_lens", False), (q, torch.bfloat16, "q", False),
+                           (idx_q, torch.bfloat16, "idx_q", False), (idx_w, torch.float32, "idx_w", False),
+                           (idx_k, torch.bfloat16, "idx_k", False), (k_new, torch.bfloat16, "k_new", True),
+                           (v_new, torch.bfloat16, "v_new", True), (idx_k_new, torch.bfloat16, "idx_k_new", True),
+                           (topk_out, torch.int32, "topk_out", True), (scores_out, torch.float32, "scores_out", True)):
+        _need(t, dt, nm, opt)
+    if out.dtype not in (torch.bfloat16, torch.float32) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 or fp32 CUDA tensor")
+    B, Hi, Di = idx_q.shape
+    max_len = idx_k.shape[1]
+    if scale is None:
+        scale = kv.head_dim ** -0.5
+    odt = KVSEL_F32 if out.dtype == torch.float32 else KVSEL_BF16
+    _check(lib().kvsel_sparse_decode(
+        ctypes.byref(kv), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, _ptr(q), _ptr(k_new),
+        _ptr(v_new), _ptr(idx_q), _ptr(idx_w), _ptr(idx_k), _ptr(idx_k_new), Hi, Di, max_len, int(top_k),
+        float(scale), _ptr(out), odt, _ptr(topk_out), _ptr(scores_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))

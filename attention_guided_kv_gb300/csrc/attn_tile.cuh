@@ -1,0 +1,104 @@
+// One 16-key attention tile for the GQA decode kernels (sm_103a, mma.sync).
+//
+// A tile holds 16 keys of one kv head in shared memory: K and V each as two
+// 64-column halves of 16 rows x 128 bytes, with the 128-byte swizzle (16-byte
+// unit u of row r stored at unit u ^ (r & 7)), the layout a TMA box with
+// CU_TENSOR_MAP_SWIZZLE_128B produces and the gather kernels reproduce.
+//
+// The group's q rows (at most 8) are the A operand of S = Q K^T (rows 8..15
+// zero); P is split into bf16(p) (A rows 0..7) and bf16(p - bf16(p)) (rows
+// 8..15) for O += P V, so the probabilities keep ~16 mantissa bits at no
+// extra MMA.  Each lane of a warp owns head g = lane / 4 and keys
+// {2q, 2q+1, 8+2q, 9+2q} (q = lane % 4) of the tile.
+#pragma once
+
+#include "common.cuh"
+
+namespace kvsel {
+
+__device__ __forceinline__ uint32_t tile_unit_off(int key, int u) {
+  return (u >> 3) * 2048 + key * 128 + ((((u & 7) ^ (key & 7))) << 4);
+}
+__device__ __forceinline__ uint32_t tile_keep_keys(uint32_t v, int k0, int valid) {
+  return v & ((k0 < valid ? 0x0000FFFFu : 0u) | (k0 + 1 < valid ? 0xFFFF0000u : 0u));
+}
+
+struct TileState {
+  float m = -INFINITY, l = 0.f;  // running max (log2 domain) and this lane's partial sum
+  float o[16][4];                // O accumulators: [n-tile of 8 dims][hi row pair, lo row pair]
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  }
+};
+
+// Load the A fragments of the group's q rows: qa[kt][0..1] for k-tile kt.
+__device__ __forceinline__ void load_q_frags(const __nv_bfloat16* qrow, bool head_ok, int qd,
+                                             uint32_t (&qa)[8][2]) {
+  const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow);
+#pragma unroll
+  for (int kt = 0; kt < 8; ++kt) {
+    qa[kt][0] = head_ok ? q32[(16 * kt + 2 * qd) >> 1] : 0u;
+    qa[kt][1] = head_ok ? q32[(16 * kt + 8 + 2 * qd) >> 1] : 0u;
+  }
+}
+
+// Process one tile of `valid` (1..16) keys at shared addresses kb / vb.
+// Returns the lane's four scaled log2 logits (-inf for keys >= valid).
+__device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb, const uint32_t (&qa)[8][2],
+                                            int valid, float scale_log2, TileState& st, float& x0,
+                                            float& x1, float& x2, float& x3) {
+  const int lane = threadIdx.x & 31, qd = lane & 3, mi = lane >> 3, r8 = lane & 7;
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kt = 0; kt < 8; ++kt) {
+    const int key = (mi >> 1) * 8 + r8;
+    const int uu = 2 * kt + (mi & 1);
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4(kb + tile_unit_off(key, uu), b0, b1, b2, b3);
+    mma_bf16_16816(s0, qa[kt][0], 0u, qa[kt][1], 0u, b0, b1);
+    mma_bf16_16816(s1, qa[kt][0], 0u, qa[kt][1], 0u, b2, b3);
+  }
+  const int k0 = 2 * qd, k2 = 8 + 2 * qd;
+  x0 = k0 < valid ? s0[0] * scale_log2 : -INFINITY;
+  x1 = k0 + 1 < valid ? s0[1] * scale_log2 : -INFINITY;
+  x2 = k2 < valid ? s1[0] * scale_log2 : -INFINITY;
+  x3 = k2 + 1 < valid ? s1[1] * scale_log2 : -INFINITY;
+  float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const float m_new = fmaxf(st.m, mx);
+  const float alpha = exp2f(st.m - m_new);
+  const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
+  const float p2 = exp2f(x2 - m_new), p3 = exp2f(x3 - m_new);
+  st.l = st.l * alpha + ((p0 + p1) + (p2 + p3));
+  st.m = m_new;
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    st.o[nt][0] *= alpha;
+    st.o[nt][1] *= alpha;
+    st.o[nt][2] *= alpha;
+    st.o[nt][3] *= alpha;
+  }
+  const uint32_t hi01 = pack_bf16x2(p0, p1);
+  const uint32_t hi23 = pack_bf16x2(p2, p3);
+  const uint32_t lo01 = pack_bf16x2(p0 - bf16lo_to_f32(hi01), p1 - bf16hi_to_f32(hi01));
+  const uint32_t lo23 = pack_bf16x2(p2 - bf16lo_to_f32(hi23), p3 - bf16hi_to_f32(hi23));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int key = (mi & 1) * 8 + r8;
+    const int uu = 2 * j + (mi >> 1);
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(vb + tile_unit_off(key, uu), b0, b1, b2, b3);
+    if (valid < 16) {  // rows past the valid keys may hold anything
+      b0 = tile_keep_keys(b0, 2 * qd, valid);
+      b1 = tile_keep_keys(b1, 8 + 2 * qd, valid);
+      b2 = tile_keep_keys(b2, 2 * qd, valid);
+      b3 = tile_keep_keys(b3, 8 + 2 * qd, valid);
+    }
+    mma_bf16_16816(st.o[2 * j], hi01, lo01, hi23, lo23, b0, b1);
+    mma_bf16_16816(st.o[2 * j + 1], hi01, lo01, hi23, lo23, b2, b3);
+  }
+}
+
+}  // namespace kvsel

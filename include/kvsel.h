@@ -254,6 +254,48 @@ KVSEL_API kvsel_status kvsel_block_priority(float* token_scores, const float* in
                                             int64_t order_capacity, int64_t* n_out, void* workspace,
                                             size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * DSA-style sparse decode: indexer scores, top-k, attention over the
+ * selected keys.
+ *
+ * Defines ("Long context, KV eviction and sparse attention": the DSA
+ * paragraph and the sparse-selection section's masked softmax), with S_b the
+ * live length after the optional append:
+ *   I[b][s]  = sum_j idx_w[b][j] * max(0, idx_q[b][j] . idx_k[b][s]),  s < S_b
+ *   sel_b    = the top_k positions by I (ties to the lower position; all of
+ *              them when S_b <= top_k), ascending
+ *   out[b][h]= softmax_{s in sel_b}(scale * q[b][h] . K_{h/G}[s]) V_{h/G}[s]
+ * One selected set per sequence, shared by every q head.
+ *
+ * Arguments (device pointers):
+ *   kv, block_table, max_pages, seq_lens, batch, q, k_new, v_new  as for
+ *                 kvsel_decode_attn (seq_lens += 1 when appending).
+ *   idx_q         bf16 [batch][num_idx_heads][idx_dim];  idx_w fp32
+ *                 [batch][num_idx_heads].
+ *   idx_k         bf16 [batch][max_len][idx_dim]: one indexer key per token;
+ *                 the appended token's key (idx_k_new, bf16 [batch][idx_dim])
+ *                 is written at slot seq_lens[b].  k_new, v_new, idx_k_new are
+ *                 all given or all NULL.
+ *   num_idx_heads 1..8;  idx_dim 64.
+ *   top_k         >= 1; ceil(max_len / 16384) <= 63 and
+ *                 ceil(max_len / 16384) * min(top_k, 16384) <= 32768.
+ *   out           [batch][num_q_heads][128], bf16 or fp32 (out_dtype).
+ *   topk_out      int32 [batch][top_k] or NULL: sel_b, padded with -1.
+ *   scores_out    fp32 [batch][max_len] or NULL: I (entries >= S_b untouched).
+ *   workspace     >= kvsel_sparse_decode_workspace(kv, batch, max_len, top_k,
+ *                 scores_out != NULL) bytes, status word zeroed.
+ */
+KVSEL_API size_t kvsel_sparse_decode_workspace(const kvsel_paged_kv* kv, int batch, int max_len,
+                                               int top_k, int with_scores_out);
+KVSEL_API kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                           int max_pages, int32_t* seq_lens, int batch, const void* q,
+                                           const void* k_new, const void* v_new, const void* idx_q,
+                                           const float* idx_w, void* idx_k, const void* idx_k_new,
+                                           int num_idx_heads, int idx_dim, int max_len, int top_k,
+                                           float scale, void* out, int out_dtype, int32_t* topk_out,
+                                           float* scores_out, void* workspace, size_t ws_bytes,
+                                           void* stream);
+
 #ifdef __cplusplus
 }
 #endif

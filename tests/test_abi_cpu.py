@@ -129,3 +129,26 @@ def test_block_priority_host_validation(lib):
     assert st(tok=None) == K.KVSEL_ERR_INVALID_ARG
     assert st(ws_bytes=64) == K.KVSEL_ERR_INVALID_ARG
     assert K.kvsel_block_priority_workspace(64, 150000) > 150000 * 28
+
+
+def test_sparse_decode_host_validation(lib):
+    kv = _kv()
+
+    def st(**over):
+        a = dict(bt=16, max_pages=8200, seq=16, batch=4, q=16, kn=None, vn=None, iq=16, iw=16, ik=16,
+                 ikn=None, Hi=4, Di=64, max_len=131136, top_k=2048, scale=0.1, out=16, odt=0,
+                 topk=None, scores=None, ws=256, ws_bytes=1 << 30)
+        a.update(over)
+        return lib.kvsel_sparse_decode(ctypes.byref(a.pop("kv", kv)), a["bt"], a["max_pages"], a["seq"],
+                                       a["batch"], a["q"], a["kn"], a["vn"], a["iq"], a["iw"], a["ik"],
+                                       a["ikn"], a["Hi"], a["Di"], a["max_len"], a["top_k"], a["scale"],
+                                       a["out"], a["odt"], a["topk"], a["scores"], a["ws"], a["ws_bytes"],
+                                       None)
+    assert st(Di=128) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(Hi=9) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(kn=16) == K.KVSEL_ERR_INVALID_ARG          # k_new without v_new / idx_k_new
+    assert st(top_k=0) == K.KVSEL_ERR_INVALID_ARG
+    assert st(max_len=64 * 16384) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(top_k=4096, max_len=20 * 16384) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(ws_bytes=100) == K.KVSEL_ERR_INVALID_ARG
+    assert st(kv=_kv(num_q_heads=128)) == K.KVSEL_ERR_UNSUPPORTED
