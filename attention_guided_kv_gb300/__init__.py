@@ -67,6 +67,8 @@ _SIGS = {
     "kvsel_sparse_decode_workspace": (_sz, [_PKV, _i, _i, _i, _i]),
     "kvsel_sparse_decode": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i,
                                  _i, _f, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
+    "kvsel_snapkv_select_workspace": (_sz, [_PKV, _i, _i, _i, _i]),
+    "kvsel_snapkv_select": (_i, [_PKV, _vp, _i, _i, _i, _vp, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -328,4 +330,29 @@ def kvsel_sparse_decode(kv: PagedKV, block_table, seq_lens, q, idx_q, idx_w, idx
         ctypes.byref(kv), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, _ptr(q), _ptr(k_new),
         _ptr(v_new), _ptr(idx_q), _ptr(idx_w), _ptr(idx_k), _ptr(idx_k_new), Hi, Di, max_len, int(top_k),
         float(scale), _ptr(out), odt, _ptr(topk_out), _ptr(scores_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------
+# SnapKV prefill selection
+# ----------------------------------------------------------------------------
+def kvsel_snapkv_select_workspace(kv: PagedKV, num_layers: int, seq_len: int, obs_window: int,
+                                  with_vote_out: bool) -> int:
+    return int(lib().kvsel_snapkv_select_workspace(ctypes.byref(kv), num_layers, seq_len, obs_window,
+                                                   int(with_vote_out)))
+
+
+def kvsel_snapkv_select(kv: PagedKV, block_table, q_obs, keep_out, workspace, *, seq_len, keep_k,
+                        pool_kernel=7, scale=None, vote_out=None, stream=None):
+    """Observation-window votes, max-pool and top-k keep per layer and kv head."""
+    _need(block_table, torch.int32, "block_table")
+    _need(q_obs, torch.bfloat16, "q_obs")
+    _need(keep_out, torch.int32, "keep_out")
+    _need(vote_out, torch.float32, "vote_out", True)
+    L, Hq, W, d = q_obs.shape
+    if scale is None:
+        scale = kv.head_dim ** -0.5
+    _check(lib().kvsel_snapkv_select(
+        ctypes.byref(kv), _ptr(block_table), block_table.shape[-1], L, int(seq_len), _ptr(q_obs), W,
+        float(scale), int(pool_kernel), int(keep_k), _ptr(keep_out), _ptr(vote_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))

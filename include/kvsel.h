@@ -296,6 +296,38 @@ KVSEL_API kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int32
                                            float* scores_out, void* workspace, size_t ws_bytes,
                                            void* stream);
 
+/* ---------------------------------------------------------------------------
+ * SnapKV prefill selection, all layers of one prompt in one call.
+ *
+ * Defines ("From sliding window to attention-guided eviction" §4.3 steps
+ * 2-5): per layer and kv head, the G*W observation rows (the last W prompt
+ * queries of each of the kv head's G q heads; window query i is at position
+ * S - W + i and attends causally to keys 0..S-W+i) vote for every prefix
+ * key j < S - W with the sum of their softmax weights (scale * q . k logits);
+ * the votes are max-pooled with a stride-1 window of pool_kernel positions
+ * clipped to the prefix; keep = the keep_k best pooled positions (ties to
+ * the lower position) followed by the window S-W..S-1, ascending.
+ *
+ * Arguments (device pointers):
+ *   kv            K pool (V is not read); num_q_heads / num_kv_heads = G.
+ *   block_table   int32 [num_layers][max_pages]: layer l's prompt pages.
+ *   seq_len       prompt length S (host value), obs_window W <= S.
+ *   q_obs         bf16 [num_layers][num_q_heads][W][128].
+ *   pool_kernel   odd, 1..33 (7 in SnapKV).
+ *   keep_out      int32 [num_layers][num_kv_heads][keep_k + W]; when
+ *                 S - W <= keep_k every position 0..S-1 is kept, -1 padded.
+ *   vote_out      fp32 [num_layers][num_kv_heads][S - W] or NULL (raw votes).
+ * Limits: G * W <= 256, S - W <= 32768.
+ */
+KVSEL_API size_t kvsel_snapkv_select_workspace(const kvsel_paged_kv* kv, int num_layers, int seq_len,
+                                               int obs_window, int with_vote_out);
+KVSEL_API kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                           int max_pages, int num_layers, int seq_len,
+                                           const void* q_obs, int obs_window, float scale,
+                                           int pool_kernel, int keep_k, int32_t* keep_out,
+                                           float* vote_out, void* workspace, size_t ws_bytes,
+                                           void* stream);
+
 #ifdef __cplusplus
 }
 #endif
