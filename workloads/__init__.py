@@ -215,10 +215,12 @@ class SnapKVWorkload:
         V = normal_bf16(rng, (Hkv, S, d))
         q_obs = normal_bf16(rng, (Hq, W, d))
         qf = _bits_as_f32(q_obs)
-        planted = np.empty((Hkv, self.n_planted), dtype=np.int64)
-        cells = (S - W) // 16
+        cells = max(0, (S - W) // 16)
+        n_pl = min(self.n_planted, cells)          # a short prefix holds fewer planted keys
+        planted = np.empty((Hkv, n_pl), dtype=np.int64)
         for kvh in range(Hkv):
-            pos = 16 * rng.choice(cells, self.n_planted, replace=False) + rng.integers(0, 8, self.n_planted)
+            pos = 16 * rng.choice(cells, n_pl, replace=False) + rng.integers(0, 8, n_pl) if n_pl else \
+                np.zeros(0, dtype=np.int64)
             pos.sort()
             planted[kvh] = pos
             u = _unit(qf[kvh * G:(kvh + 1) * G].reshape(-1, d).mean(0)).astype(np.float32)
