@@ -112,4 +112,4 @@ def test_full_size_qwen7b_sampled_layers():
     assert (np.diff(keep, axis=-1) > 0).all()
     kept = sum(len(set(lay.planted[h].tolist()) & set(keep[i, h].tolist()))
                for i, lay in enumerate(layers) for h in range(wl.Hkv))
-    assert kept >= 0.9 * 28 * 4 * 64, kept
+    assert kept >= 0.99 * 28 * 4 * 64, kept

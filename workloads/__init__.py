@@ -229,8 +229,13 @@ class SnapKVWorkload:
 
 
 def snapkv_qwen7b(seed: int = 2, L: int = 28, S: int = 32768) -> SnapKVWorkload:
+    """Qwen2.5-7B shape; 64 planted keys per kv head pushed +16 along the unit mean query.
+
+    (+16 gives each window query a logit boost of about 1.1 on average, so the
+    planted keys collect about three times the background vote.)
+    """
     return SnapKVWorkload("snapkv_qwen7b", L=L, Hq=28, Hkv=4, d=128, S=S, W=32,
-                          keep_k=2048, pool_kernel=7, n_planted=64, seed=seed)
+                          keep_k=2048, pool_kernel=7, n_planted=64, seed=seed, plant_amp=16.0)
 
 
 def snapkv_custom(seed, L, Hq, Hkv, d, S, W, keep_k, pool_kernel=7, n_planted=8, plant_amp=4.0):
