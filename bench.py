@@ -382,6 +382,448 @@ def cuda_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# the other hot-path workloads (one JSON line each)
+# ---------------------------------------------------------------------------
+WORKLOADS = {
+    "decode_70b": None,
+    "decode_small": ("decode steps/s with H2O evict + compaction every step",
+                     "single seq, 16 q / 8 kv heads, d=128, prompt 1600, 64 decode steps, H2O budget "
+                     "256 = 4 sinks + 64 window + 188 heavy hitters, evict and compact every step",
+                     "steps/s"),
+    "snapkv": ("SnapKV prefill selects/s (all 28 layers)",
+               "SnapKV prefill select, Qwen2.5-7B shape (28 layers, 28 q / 4 kv heads, d=128), prompt "
+               "32K, obs window 32, sum vote, maxpool 7, keep 2048 per kv head", "selects/s"),
+    "block_priority": ("block offload priority passes/s",
+                       "block offload priority: 64 requests, lengths log-uniform 4K-128K, Dirichlet "
+                       "increments with decay 0.98, 16-token blocks, max aggregation, per-request "
+                       "percentile, evict order for 25% of blocks", "passes/s"),
+    "sparse_decode": ("sparse decode steps/s",
+                      "DSA-style sparse decode, 70B shape (64 q / 8 kv heads, d=128), batch 4, 128K "
+                      "context, indexer 4 x 64, top-2048", "steps/s"),
+}
+
+
+def _dev_bf16(bits, dev):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _setup_decode_small(dev):
+    """Evict-every-step loop: append + attention + probabilities + H2O update, then select +
+    compaction; the caller's allocator hands the page released at index 16 back for the
+    next append (budget 256 = 16 full pages)."""
+    import numpy as np
+    import torch
+    import attention_guided_kv_gb300 as K
+    import workloads
+    wl = workloads.decode_small()
+    kpool = _dev_bf16(workloads.paged_pool(wl.K, wl.block_table, wl.num_pages), dev)
+    vpool = _dev_bf16(workloads.paged_pool(wl.V, wl.block_table, wl.num_pages), dev)
+    kv = K.paged_kv(kpool, vpool, wl.Hq)
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    seq = torch.full((1,), wl.S0, dtype=torch.int32, device=dev)
+    cum = torch.zeros(1, wl.Hkv, wl.max_len, device=dev)
+    probs = torch.zeros(1, wl.Hq, wl.max_len, device=dev)
+    pos = torch.from_numpy(np.tile(np.arange(wl.max_len, dtype=np.int32), (1, wl.Hkv, 1))).to(dev)
+    nxt = torch.full((1,), wl.S0, dtype=torch.int32, device=dev)
+    out = torch.zeros(1, wl.Hq, wl.d, device=dev, dtype=torch.bfloat16)
+    keep = torch.zeros(1, wl.Hkv, wl.budget, dtype=torch.int32, device=dev)
+    freed = torch.zeros(1, wl.max_pages, dtype=torch.int32, device=dev)
+    ws = K.workspace(K.kvsel_decode_attn_workspace(kv, 1, wl.max_len, True))
+    ws2 = K.workspace(K.kvsel_h2o_evict_workspace(kv, 1, wl.budget))
+    q, kn, vn = _dev_bf16(wl.q, dev), _dev_bf16(wl.k_new, dev), _dev_bf16(wl.v_new, dev)
+    page = wl.budget // 16
+
+    def run(i, qi, kni, vni):
+        K.kvsel_decode_attn(kv, bt, seq, qi, out, ws, k_new=kni, v_new=vni, pos_map=pos, next_pos=nxt,
+                            probs=probs, h2o_cum=cum, max_len=wl.max_len)
+        K.kvsel_h2o_evict(kv, bt, seq, cum, ws2, budget=wl.budget, n_sink=wl.n_sink, window=wl.window,
+                          compact=True, pos_map=pos, keep_out=keep, freed_pages=freed)
+        bt[:, page].copy_(freed[:, 0])
+
+    def step(i):
+        t = i % wl.steps
+        run(i, q[t], kn[t], vn[t])
+
+    host_in = [("q", q), ("k_new", kn), ("v_new", vn)]
+    outs = [out, keep]
+    # bytes of the dominant kernel (decode_step) per launch at the steady length 257
+    S = wl.budget + 1
+    byts = {"decode_step": S * wl.Hkv * 512 + S * wl.Hq * 4 + S * wl.Hkv * 8 + wl.Hq * wl.d * 4}
+    return dict(step=step, run=run, host_in=host_in, outs=outs, bytes=byts, flops={},
+                ws=[ws, ws2], per_step_launches=4, config={"batch": 1, "context": wl.S0,
+                "q_heads": wl.Hq, "kv_heads": wl.Hkv, "budget": wl.budget, "steps_cycle": wl.steps,
+                "l2": "working set (~1 MB) fits in L2: latency-bound"})
+
+
+def _setup_snapkv(dev):
+    import numpy as np
+    import torch
+    import attention_guided_kv_gb300 as K
+    import workloads
+    wl = workloads.snapkv_qwen7b()
+    P = wl.pages
+    pool = np.zeros((wl.L * P, wl.Hkv, 16, wl.d), dtype=np.uint16)
+    bts = np.zeros((wl.L, P), dtype=np.int32)
+    qo = np.zeros((wl.L, wl.Hq, wl.W, wl.d), dtype=np.uint16)
+    for l in range(wl.L):
+        lay = wl.layer(l)
+        pool[l * P:(l + 1) * P] = workloads.paged_pool(lay.K[None], lay.block_table[None], P)
+        bts[l] = lay.block_table + l * P
+        qo[l] = lay.q_obs
+    kpool = _dev_bf16(pool, dev)
+    del pool
+    kv = K.paged_kv(kpool, kpool, wl.Hq)
+    bt = torch.from_numpy(bts).to(dev)
+    q = _dev_bf16(qo, dev)
+    keep = torch.zeros(wl.L, wl.Hkv, wl.keep_k + wl.W, dtype=torch.int32, device=dev)
+    vote = torch.zeros(wl.L, wl.Hkv, wl.S - wl.W, device=dev)
+    ws = K.workspace(K.kvsel_snapkv_select_workspace(kv, wl.L, wl.S, wl.W, True))
+
+    def run(i, qi):
+        K.kvsel_snapkv_select(kv, bt, qi, keep, ws, seq_len=wl.S, keep_k=wl.keep_k,
+                              pool_kernel=wl.pool_kernel, vote_out=vote)
+
+    def step(i):
+        run(i, q)
+
+    pairs = wl.L * wl.Hkv
+    rows = wl.G * wl.W
+    qk_flops = 2.0 * rows * wl.S * wl.d * pairs
+    kbytes = wl.S * wl.d * 2 * pairs
+    return dict(step=step, run=run, host_in=[("q_obs", q[None])], outs=[keep], ws=[ws],
+                bytes={"snap_stats": kbytes, "snap_vote": kbytes}, flops={"snap_stats": qk_flops,
+                "snap_vote": 2.0 * rows * (wl.S - wl.W) * wl.d * pairs}, per_step_launches=3,
+                config={"layers": wl.L, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "prompt": wl.S,
+                        "obs_window": wl.W, "keep": wl.keep_k, "pool_kernel": wl.pool_kernel,
+                        "l2": "inputs larger than L2 (940 MB of K per pass)"})
+
+
+def _setup_block_priority(dev):
+    import numpy as np
+    import torch
+    import attention_guided_kv_gb300 as K
+    import workloads
+    wl = workloads.block_priority()
+    off = torch.from_numpy(wl.offsets).to(dev)
+    tok = torch.from_numpy(wl.increments(0)).to(dev)
+    incs = [torch.from_numpy(wl.increments(t)).to(dev) for t in range(1, 5)]
+    nblk = int(sum(-(-int(L) // 16) for L in wl.lengths))
+    order = torch.zeros(-(-nblk // 4), dtype=torch.int64, device=dev)
+    n_out = torch.zeros(2, dtype=torch.int64, device=dev)
+    maxb = int(sum(-(-int(L) // 1) for L in wl.lengths))      # bound for every block size
+    ws = K.workspace(K.kvsel_block_priority_workspace(wl.R, maxb))
+    variant = dict(block_size=16, agg=K.KVSEL_AGG_MAX, norm=K.KVSEL_NORM_PERCENTILE)
+
+    def run(i, inc, **v):
+        opts = dict(variant)
+        opts.update(v)
+        K.kvsel_block_priority(tok, off, order, n_out, ws, evict_frac=0.25, increment=inc, decay=0.98,
+                               top_p=0.1, max_total_blocks=maxb, **opts)
+
+    def step(i):
+        run(i, incs[i % 4])
+
+    T = wl.total_tokens
+    byts = {"bp_fold": T * 12 + nblk * 4, "bp_rank": nblk * 12, "bp_sort": nblk * 12 * 2 * 8,
+            "bp_prefix": wl.R * 16}
+    return dict(step=step, run=run, host_in=[("increment", incs[0][None])], outs=[order, n_out], ws=[ws],
+                bytes=byts, flops={}, per_step_launches=4, extra_variants=True, nblk=nblk,
+                config={"requests": wl.R, "tokens": T, "blocks": nblk, "block_size": 16, "agg": "max",
+                        "norm": "percentile", "evict_frac": 0.25,
+                        "l2": "~9 MB of token scores per pass (fits in L2): latency-bound"})
+
+
+def _setup_sparse_decode(dev):
+    import numpy as np
+    import torch
+    import attention_guided_kv_gb300 as K
+    import workloads
+    wl = workloads.sparse_decode()
+    kpool = _dev_bf16(workloads.paged_pool(wl.K, wl.block_table, wl.num_pages), dev)
+    vpool = _dev_bf16(workloads.paged_pool(wl.V, wl.block_table, wl.num_pages), dev)
+    wl.K = wl.V = None
+    kv = K.paged_kv(kpool, vpool, wl.Hq)
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    seq0 = torch.full((wl.B,), wl.S0, dtype=torch.int32, device=dev)
+    seq = seq0.clone()
+    idx = np.zeros((wl.B, wl.max_len, wl.Di), dtype=np.uint16)
+    idx[:, :wl.S0] = wl.k_idx
+    idx_k = _dev_bf16(idx, dev)
+    del idx
+    q, kn, vn = _dev_bf16(wl.q, dev), _dev_bf16(wl.k_new, dev), _dev_bf16(wl.v_new, dev)
+    qi, kin = _dev_bf16(wl.q_idx, dev), _dev_bf16(wl.k_idx_new, dev)
+    wi = torch.from_numpy(wl.w_idx).to(dev)
+    out = torch.zeros(wl.B, wl.Hq, wl.d, device=dev, dtype=torch.bfloat16)
+    topk = torch.zeros(wl.B, wl.top_k, dtype=torch.int32, device=dev)
+    ws = K.workspace(K.kvsel_sparse_decode_workspace(kv, wl.B, wl.max_len, wl.top_k, False))
+
+    def run(i, q_, qi_, wi_, kn_, vn_, kin_):
+        if i % wl.steps == 0 and i > 0:
+            seq.copy_(seq0)                 # replay the 64-step window from 128K again
+        K.kvsel_sparse_decode(kv, bt, seq, q_, qi_, wi_, idx_k, out, ws, top_k=wl.top_k, k_new=kn_,
+                              v_new=vn_, idx_k_new=kin_, topk_out=topk)
+
+    def step(i):
+        t = i % wl.steps
+        run(i, q[t], qi[t], wi[t], kn[t], vn[t], kin[t])
+
+    S = wl.S0 + wl.steps // 2
+    byts = {"sd_index": wl.B * S * (wl.Di * 2 + 4), "sd_attn": wl.B * wl.top_k * wl.Hkv * 512,
+            "sd_topk_chunk": wl.B * S * 4, "sd_topk_final": wl.B * 9 * wl.top_k * 8, "sd_merge": 0}
+    host_in = [("q", q), ("q_idx", qi), ("w_idx", wi), ("k_new", kn), ("v_new", vn), ("k_idx_new", kin)]
+    return dict(step=step, run=run, host_in=host_in, outs=[out, topk], ws=[ws], bytes=byts, flops={},
+                per_step_launches=5, steps_cycle=wl.steps,
+                config={"batch": wl.B, "context": wl.S0, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
+                        "indexer": f"{wl.Hi} x {wl.Di}", "top_k": wl.top_k,
+                        "l2": "inputs larger than L2 (67 MB indexer keys + 33.5 MB gathered K/V per step)"})
+
+
+SETUPS = {"decode_small": _setup_decode_small, "snapkv": _setup_snapkv,
+          "block_priority": _setup_block_priority, "sparse_decode": _setup_sparse_decode}
+
+
+def _oracle_decode_small():
+    import numpy as np
+    import workloads
+    from oracle.attention import bf16_bits_to_f64
+    from oracle.h2o import H2OSequence
+    wl = workloads.decode_small()
+    seq = H2OSequence(bf16_bits_to_f64(wl.K[0]), bf16_bits_to_f64(wl.V[0]))
+    args = [(bf16_bits_to_f64(wl.q[t, 0]), bf16_bits_to_f64(wl.k_new[t, 0]), bf16_bits_to_f64(wl.v_new[t, 0]))
+            for t in range(wl.steps)]
+    seq.step(*args[0], wl.scale, wl.budget, wl.n_sink, wl.window)       # first step from 1600
+    t0 = time.perf_counter()
+    for a in args[1:]:
+        seq.step(*a, wl.scale, wl.budget, wl.n_sink, wl.window)
+    dt = (time.perf_counter() - t0) / (wl.steps - 1)
+    return {"seconds_per_unit": dt, "sample": f"{wl.steps - 1} steady-state steps (append, attention, "
+            f"H2O update, select, compaction; fp64 numpy)", "scale": 1}
+
+
+def _oracle_snapkv():
+    import workloads
+    from oracle import snapkv
+    from oracle.attention import bf16_bits_to_f64
+    wl = workloads.snapkv_qwen7b()
+    lay = wl.layer(0)
+    G = wl.G
+    t0 = time.perf_counter()
+    v = snapkv.snapkv_vote(bf16_bits_to_f64(lay.q_obs[:G]), bf16_bits_to_f64(lay.K[:1]), wl.scale)
+    pooled = snapkv.maxpool1d(v, wl.pool_kernel)
+    snapkv.snapkv_keep(pooled[0], wl.S, wl.W, wl.keep_k)
+    dt = time.perf_counter() - t0
+    pairs = wl.L * wl.Hkv
+    return {"seconds_per_unit": dt * pairs, "sample": f"one (layer, kv head) of {pairs} (vote, max-pool, "
+            f"keep; fp64 numpy), scaled x{pairs}", "scale": pairs}
+
+
+def _oracle_block_priority():
+    import numpy as np
+    import workloads
+    from oracle import block_priority as BP
+    wl = workloads.block_priority()
+    tok = wl.increments(0).astype(np.float64)
+    inc = wl.increments(1).astype(np.float64)
+    t0 = time.perf_counter()
+    tok = BP.decay_update(tok, inc, 0.98)
+    BP.priority_pass(tok, wl.offsets, 16, BP.AGG_MAX, 0.1, BP.NORM_PERCENTILE, 0.25)
+    dt = time.perf_counter() - t0
+    return {"seconds_per_unit": dt, "sample": "one full pass (decay update, fold, percentile, global "
+            "order) over all 64 requests (fp64 numpy)", "scale": 1}
+
+
+def _oracle_sparse_decode():
+    import numpy as np
+    import workloads
+    from oracle import dsa
+    from oracle.attention import bf16_bits_to_f64
+    wl = workloads.sparse_decode(B=1, steps=1)
+    Kb, Vb = bf16_bits_to_f64(wl.K[0]), bf16_bits_to_f64(wl.V[0])
+    ki = bf16_bits_to_f64(wl.k_idx[0])
+    t0 = time.perf_counter()
+    dsa.sparse_decode_step(bf16_bits_to_f64(wl.q[0, 0]), Kb, Vb, bf16_bits_to_f64(wl.q_idx[0, 0]),
+                           wl.w_idx[0, 0].astype(np.float64), ki, wl.top_k, wl.scale)
+    dt = time.perf_counter() - t0
+    return {"seconds_per_unit": dt * 4, "sample": "one sequence of the batch of 4 (indexer over 128K "
+            "keys, top-2048, attention over the selection; fp64 numpy), scaled x4", "scale": 4}
+
+
+ORACLE_SAMPLES = {"decode_small": _oracle_decode_small, "snapkv": _oracle_snapkv,
+                  "block_priority": _oracle_block_priority, "sparse_decode": _oracle_sparse_decode}
+
+
+def _oracle_subprocess(name):
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", name],
+                       capture_output=True, text=True, env=env, timeout=1200)
+    line = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    if r.returncode != 0 or not line:
+        return None, cores
+    return json.loads(line[-1]), cores
+
+
+def other_reference(args, world):
+    metric, cfg, unit = WORKLOADS[args.workload]
+    ts = []
+    for i in range(args.warmup + args.steps):
+        res = ORACLE_SAMPLES[args.workload]()
+        if i >= args.warmup:
+            ts.append(res["seconds_per_unit"])
+    mean = sum(ts) / len(ts)
+    cores = len(os.sched_getaffinity(0))
+    line = {"metric": metric, "value": 1.0 / mean, "unit": unit, "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg},
+            "cpu_baseline": {"value": 1.0 / mean, "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": res["sample"]},
+            "e2e": {"value": 1.0 / mean, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def other_workload(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    import attention_guided_kv_gb300 as K
+    metric, cfg_name, unit = WORKLOADS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    K.lib()
+    S = SETUPS[args.workload](dev)
+    stream = torch.cuda.current_stream()
+    steps = args.steps
+    for i in range(args.warmup):
+        S["step"](i)
+    torch.cuda.synchronize()
+    for w in S["ws"]:
+        st = K.read_status(w)
+        if st:
+            raise RuntimeError(f"device status after warm-up: {st}")
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    clocks = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid)
+    clocks.start()
+    time.sleep(0.3)
+    trace = K.LaunchTrace(S["per_step_launches"] * steps + 8)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tw0 = time.time()
+    with trace:
+        e0.record(stream)
+        for i in range(args.warmup, args.warmup + steps):
+            S["step"](i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    durs = trace.durations()
+    per = {}
+    for nm, d in durs:
+        per.setdefault(nm, []).append(d)
+    kern_ms = {k: sum(v) / len(v) for k, v in per.items()}
+    dominant = max(kern_ms, key=lambda k: kern_ms[k] * len(per[k]))
+
+    # end to end: every step copies its inputs from pinned host memory and its results back
+    hin = [(n, t.cpu().pin_memory()) for n, t in S["host_in"]]
+    dins = [torch.empty_like(t[0]) for _, t in S["host_in"]]
+    houts = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in S["outs"]]
+    h2d = sum(t[0].numel() * t.element_size() for _, t in hin)
+    d2h = sum(o.numel() * o.element_size() for o in S["outs"])
+    base = args.warmup + steps
+    cyc = S.get("steps_cycle", None)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(base, base + steps):
+        for (n, h), d in zip(hin, dins):
+            d.copy_(h[i % h.shape[0]], non_blocking=True)
+        if args.workload == "decode_small":
+            S["run"](i, *dins)
+        elif args.workload == "snapkv":
+            S["run"](i, dins[0])
+        elif args.workload == "block_priority":
+            S["run"](i, dins[0])
+        else:
+            S["run"](i, *dins)
+        for ho, o in zip(houts, S["outs"]):
+            ho.copy_(o, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    variants = None
+    if S.get("extra_variants"):
+        variants = {}
+        for bs in (16, 64, 256):
+            for agg, an in ((K.KVSEL_AGG_MAX, "max"), (K.KVSEL_AGG_MEAN, "mean"), (K.KVSEL_AGG_TOPP, "top10%")):
+                torch.cuda.synchronize()
+                a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for i in range(20):
+                    S["run"](i, None, block_size=bs, agg=agg)
+                b2.record(stream)
+                torch.cuda.synchronize()
+                variants[f"bs{bs}_{an}"] = a.elapsed_time(b2) / 20 * 1e3
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(20):
+            S["step"](i)
+        b2.record(stream)
+        torch.cuda.synchronize()
+        variants["bs16_max_with_decay_update"] = a.elapsed_time(b2) / 20 * 1e3
+    clocks.stop()
+    for w in S["ws"]:
+        st = K.read_status(w)
+        if st:
+            raise RuntimeError(f"device status after the timed region: {st}")
+    if rank != 0:
+        return
+    hbm, peak_kind = peaks()
+    kms = kern_ms[dominant]
+    if dominant in S["flops"] and S["flops"][dominant]:
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                tf = float(json.load(f)["bf16_tflops"])
+            tk = "measured"
+        except Exception:
+            tf, tk = 1900.0, "fallback"
+        ach = S["flops"][dominant] / (kms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dominant, "achieved": ach, "peak": tf, "peak_kind": tk,
+                "unit": "TFLOP/s", "frac": ach / tf, "traffic": None,
+                "hbm_achieved_gbs": S["bytes"][dominant] / (kms / 1e3) / 1e9}
+    else:
+        ach = S["bytes"].get(dominant, 0) / (kms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": hbm, "peak_kind": peak_kind,
+                "unit": "GB/s", "frac": ach / hbm, "traffic": None}
+    line = {"metric": metric, "value": world * steps / (ms / 1e3), "unit": unit, "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if args.workload != "block_priority" else "f32",
+            "data": "synthetic", "config": dict({"workload": cfg_name}, **S["config"]),
+            "kernel_ms": kern_ms, "roofline": roof,
+            "e2e": {"value": world * steps / (e2e_ms / 1e3), "unit": unit, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": len(durs), "clocks": clocks.summary(tw0, tw1)}
+    if variants:
+        line["variants_us_per_pass"] = variants
+    if not args.no_cpu_baseline:
+        res, cores = _oracle_subprocess(args.workload)
+        if res:
+            line["cpu_baseline"] = {"value": 1.0 / res["seconds_per_unit"], "unit": unit, "cores": cores,
+                                    "kind": "oracle", "sample": res["sample"]}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,13 +836,26 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=64)
     ap.add_argument("--cpu-worker", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--workload", default="decode_70b", choices=list(WORKLOADS),
+                    help="decode_70b (the headline) or one of the other hot-path workloads")
+    ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_worker is not None:
         cpu_worker_main(args.cpu_worker)
         return
+    if args.oracle_sample is not None:
+        print(json.dumps(ORACLE_SAMPLES[args.oracle_sample]()))
+        return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.workload != "decode_70b":
+        if args.impl == "reference":
+            if rank == 0:
+                other_reference(args, world)
+            return
+        other_workload(args, rank, world)
+        return
     if args.impl == "reference":
         reference_arm(args, rank, world)
         return
