@@ -410,7 +410,7 @@ def _dev_bf16(bits, dev):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
 
-def _setup_decode_small(dev):
+def _setup_decode_small(dev, small=False):
     """Evict-every-step loop: append + attention + probabilities + H2O update, then select +
     compaction; the caller's allocator hands the page released at index 16 back for the
     next append (budget 256 = 16 full pages)."""
@@ -458,12 +458,12 @@ def _setup_decode_small(dev):
                 "l2": "working set (~1 MB) fits in L2: latency-bound"})
 
 
-def _setup_snapkv(dev):
+def _setup_snapkv(dev, small=False):
     import numpy as np
     import torch
     import attention_guided_kv_gb300 as K
     import workloads
-    wl = workloads.snapkv_qwen7b()
+    wl = workloads.snapkv_qwen7b(L=4 if small else 28)
     P = wl.pages
     pool = np.zeros((wl.L * P, wl.Hkv, 16, wl.d), dtype=np.uint16)
     bts = np.zeros((wl.L, P), dtype=np.int32)
@@ -501,7 +501,7 @@ def _setup_snapkv(dev):
                         "l2": "inputs larger than L2 (940 MB of K per pass)"})
 
 
-def _setup_block_priority(dev):
+def _setup_block_priority(dev, small=False):
     import numpy as np
     import torch
     import attention_guided_kv_gb300 as K
@@ -536,12 +536,12 @@ def _setup_block_priority(dev):
                         "l2": "~9 MB of token scores per pass (fits in L2): latency-bound"})
 
 
-def _setup_sparse_decode(dev):
+def _setup_sparse_decode(dev, small=False):
     import numpy as np
     import torch
     import attention_guided_kv_gb300 as K
     import workloads
-    wl = workloads.sparse_decode()
+    wl = workloads.sparse_decode(B=1 if small else 4)
     kpool = _dev_bf16(workloads.paged_pool(wl.K, wl.block_table, wl.num_pages), dev)
     vpool = _dev_bf16(workloads.paged_pool(wl.V, wl.block_table, wl.num_pages), dev)
     wl.K = wl.V = None
@@ -696,7 +696,7 @@ def other_workload(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     K.lib()
-    S = SETUPS[args.workload](dev)
+    S = SETUPS[args.workload](dev, small=args.small)
     stream = torch.cuda.current_stream()
     steps = args.steps
     for i in range(args.warmup):
@@ -816,6 +816,8 @@ def other_workload(args, rank, world):
             "gpu_launches": len(durs), "clocks": clocks.summary(tw0, tw1)}
     if variants:
         line["variants_us_per_pass"] = variants
+    if args.small:
+        line["note"] = "--small profiling case, not the measured workload"
     if not args.no_cpu_baseline:
         res, cores = _oracle_subprocess(args.workload)
         if res:
@@ -839,6 +841,8 @@ def main():
     ap.add_argument("--workload", default="decode_70b", choices=list(WORKLOADS),
                     help="decode_70b (the headline) or one of the other hot-path workloads")
     ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--small", action="store_true",
+                    help="profiling case (fewer layers / sequences), not the measured workload")
     args = ap.parse_args()
     if args.cpu_worker is not None:
         cpu_worker_main(args.cpu_worker)
