@@ -524,13 +524,15 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         Ig[gg] = gg < G ? sStat[gg * 2 + 1] : 0.f;
       }
       if (P.vec4) {
-        // 4 keys x all heads per thread per step: up to 8 independent 16-byte loads in flight
-        for (int j = j0 + 4 * tid; j + 3 < j1; j += 4 * kThreads) {
-          float4 lg[kMaxG];
+        // 4 keys x all heads per thread, two such groups per iteration: up to 16
+        // independent 16-byte loads in flight per thread
+        auto group = [&](int j, float4 (&lg)[kMaxG]) {
 #pragma unroll
           for (int gg = 0; gg < kMaxG; ++gg)
             if (gg < G)
               lg[gg] = __ldcg(reinterpret_cast<const float4*>(P.logits + row0 + size_t(gg) * P.max_len + j));
+        };
+        auto finish = [&](int j, const float4 (&lg)[kMaxG], float4 old) {
           float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int gg = 0; gg < kMaxG; ++gg)
@@ -547,7 +549,6 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
               sum.w += pj.w;
             }
           if (crow) {
-            float4 old = __ldcg(reinterpret_cast<const float4*>(crow + j));
             if (append && j + 3 >= S - 1) {  // the appended slot starts from zero
               if (j == S - 1) old.x = 0.f;
               if (j + 1 == S - 1) old.y = 0.f;
@@ -557,6 +558,21 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             __stcg(reinterpret_cast<float4*>(crow + j),
                    make_float4(old.x + sum.x, old.y + sum.y, old.z + sum.z, old.w + sum.w));
           }
+        };
+        const int jend = j0 + ((j1 - j0) & ~3);
+        for (int j = j0 + 4 * tid; j < jend; j += 8 * kThreads) {
+          const int jb = j + 4 * kThreads;
+          const bool has_b = jb < jend;
+          float4 la[kMaxG], lb[kMaxG];
+          group(j, la);
+          if (has_b) group(jb, lb);
+          float4 oa = make_float4(0.f, 0.f, 0.f, 0.f), ob = oa;
+          if (crow) {
+            oa = __ldcg(reinterpret_cast<const float4*>(crow + j));
+            if (has_b) ob = __ldcg(reinterpret_cast<const float4*>(crow + jb));
+          }
+          finish(j, la, oa);
+          if (has_b) finish(jb, lb, ob);
         }
       }
       // keys left over (the whole segment when rows are not 16-byte aligned), one per thread

@@ -9,9 +9,11 @@
 //
 // select kernel, one 1024-thread CTA per (sequence, kv head):
 //   finds the k-th largest score over the middle slots on a monotone uint32
-//   image of the fp32 score: a sorted sample brackets it, one counting pass
-//   gathers the keys inside the bracket, and a 4 x 8-bit radix select finishes
-//   exactly (a radix select over the whole row is the fallback); then an
+//   image of the fp32 score.  The row's previous threshold (kept in the
+//   workspace) usually bounds a band of about k keys from below; otherwise a
+//   sorted sample brackets it; one counting pass gathers the keys inside the
+//   band, and a 4 x 8-bit radix select finishes exactly (a radix select over
+//   the whole row is the last fallback); then an
 //   ordered emission: each thread owns a
 //   contiguous run of slots, two block-wide scans give every thread its share
 //   of the threshold ties (lowest slots first) and its output offset, so the
@@ -41,6 +43,7 @@ struct SelectParams {
   int32_t* keep_slots;  // workspace [B][Hkv][budget]
   int32_t* keep_out;    // [B][Hkv][budget] or null
   int32_t* first_move;  // workspace [B][Hkv]
+  uint32_t* hint;       // workspace [B][Hkv]: last threshold key per row (0 = none)
   int* status;
   int Hkv, max_len, budget, n_sink, window;
 };
@@ -202,7 +205,24 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
   uint32_t T = 0xFFFFFFFFu, need_eq = 0, tot = 0;
   bool done = false;
   if constexpr (kInRegs) {
-    if (k > 0) {
+    // 0. the previous call's threshold for this row: the keys at or above it are
+    //    usually about k (scores only grow between calls), so they make a small
+    //    band holding the k-th key; any stale hint just fails the check below.
+    const uint32_t hint = k > 0 ? P.hint[rowi] : 0u;
+    if (hint != 0u) {
+      uint32_t c_band = 0;
+      KVSEL_FOR_ITEMS(c_band += u >= hint;)
+      uint32_t band_tot;
+      const uint32_t band_base = block_exclusive_scan(c_band, scan_tmp, band_tot);
+      if (uint32_t(k) <= band_tot && band_tot <= uint32_t(kBandMax)) {
+        uint32_t w = band_base;
+        KVSEL_FOR_ITEMS(if (u >= hint) band[w++] = u;)
+        __syncthreads();
+        smem_radix_select(band, int(band_tot), uint32_t(k), hist, &s_digit, &s_above, T, need_eq);
+        done = true;
+      }
+    }
+    if (k > 0 && !done) {
       // 1. sample = first key of each run (0 sorts below every real key), sorted descending
       sample[tid] = cnt > 0 ? key[0] : 0u;
       __syncthreads();
@@ -292,6 +312,8 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
     T = prefix;
     need_eq = krem;
   }
+
+  if (k > 0 && tid == 0) P.hint[rowi] = T;
 
   // ordered emission of the heavy hitters
   uint32_t gt = 0, eq = 0;
@@ -426,7 +448,7 @@ using namespace kvsel_host;
 
 namespace {
 struct EvictWs {
-  size_t keep_off, first_off, total;
+  size_t keep_off, first_off, hint_off, total;
 };
 EvictWs evict_ws_layout(int batch, int Hkv, int budget) {
   EvictWs w;
@@ -435,6 +457,8 @@ EvictWs evict_ws_layout(int batch, int Hkv, int budget) {
   off = align_up(off + size_t(batch) * Hkv * budget * sizeof(int32_t), 256);
   w.first_off = off;
   off = align_up(off + size_t(batch) * Hkv * sizeof(int32_t), 256);
+  w.hint_off = off;
+  off = align_up(off + size_t(batch) * Hkv * sizeof(uint32_t), 256);
   w.total = off;
   return w;
 }
@@ -478,6 +502,7 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   P.keep_slots = reinterpret_cast<int32_t*>(ws + L.keep_off);
   P.keep_out = keep_out;
   P.first_move = reinterpret_cast<int32_t*>(ws + L.first_off);
+  P.hint = reinterpret_cast<uint32_t*>(ws + L.hint_off);
   P.status = reinterpret_cast<int*>(ws);
   P.Hkv = kv->num_kv_heads;
   P.max_len = max_len;

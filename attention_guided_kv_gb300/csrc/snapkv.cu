@@ -279,6 +279,7 @@ snap_qk_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
 // max-pool of the votes + exact top-keep_k + the window, ascending
 __global__ void __launch_bounds__(kTopkThreads) snap_select_kernel(const SnapParams P) {
   __shared__ TopkSmem sm;
+  extern __shared__ float svote[];  // the row's votes (prefix length floats)
   const int pair = blockIdx.x, tid = threadIdx.x;
   const int Pfx = P.S - P.W;
   const int nk = P.keep_k + P.W;
@@ -288,6 +289,8 @@ __global__ void __launch_bounds__(kTopkThreads) snap_select_kernel(const SnapPar
     for (int i = tid; i < nk; i += kTopkThreads) keep[i] = i < P.S ? i : -1;
     return;
   }
+  for (int j = tid; j < Pfx; j += kTopkThreads) svote[j] = __ldcg(vrow + j);
+  __syncthreads();
   const int C = (Pfx + kTopkThreads - 1) / kTopkThreads;
   const int e0 = min(Pfx, tid * C), cnt = min(Pfx, (tid + 1) * C) - e0;
   uint32_t key[kSnSelItems];
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(kTopkThreads) snap_select_kernel(const SnapPar
     if (e < cnt) {
       const int j = e0 + e;
       float mx = -INFINITY;
-      for (int t = max(0, j - P.pool_half); t <= min(Pfx - 1, j + P.pool_half); ++t) mx = fmaxf(mx, __ldcg(vrow + t));
+      for (int t = max(0, j - P.pool_half); t <= min(Pfx - 1, j + P.pool_half); ++t) mx = fmaxf(mx, svote[t]);
       key[e] = order_key(mx);
     }
   }
@@ -421,7 +424,10 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
   if (!attr_set) {
     cudaError_t e1 = cudaFuncSetAttribute(snap_qk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSnSmem));
     cudaError_t e2 = cudaFuncSetAttribute(snap_qk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSnSmem));
-    if (e1 != cudaSuccess || e2 != cudaSuccess) return cuda_fail(e1 != cudaSuccess ? e1 : e2, "kvsel_snapkv_select (attribute)");
+    cudaError_t e3 = cudaFuncSetAttribute(snap_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          int(kSnSelItems * kTopkThreads * sizeof(float)));
+    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess)
+      return cuda_fail(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3), "kvsel_snapkv_select (attribute)");
     attr_set = true;
   }
   const dim3 grid(chunks, num_layers * Hkv);
@@ -439,7 +445,7 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
     if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (vote launch)");
   }
   trace_before("snap_select", st);
-  snap_select_kernel<<<num_layers * Hkv, kTopkThreads, 0, st>>>(P);
+  snap_select_kernel<<<num_layers * Hkv, kTopkThreads, size_t(std::max(seq_len - obs_window, 1)) * sizeof(float), st>>>(P);
   e = cudaGetLastError();
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (select launch)");

@@ -216,26 +216,16 @@ __global__ void __launch_bounds__(kTopkThreads) sd_topk_final_kernel(const SdPar
   __syncthreads();
   const int m = coff[nch];
   const int k = min(P.top_k, m);
+  const int kcf = min(P.top_k, kSdChunk);  // every chunk but the last holds exactly kcf candidates
   const int C = (m + kTopkThreads - 1) / kTopkThreads;
   const int e0 = min(m, tid * C), cnt = min(m, (tid + 1) * C) - e0;
+  auto cand = [&](int i) -> size_t {
+    const int c = i / kcf;
+    return (size_t(b) * P.nchunks + c) * P.top_k + (i - c * kcf);
+  };
   uint32_t key[kSdFinalItems];
-  int pos[kSdFinalItems];
-  {
-    int ch = 0;
-    while (ch + 1 < nch && coff[ch + 1] <= e0) ++ch;
 #pragma unroll
-    for (int e = 0; e < kSdFinalItems; ++e) {
-      key[e] = 0u;
-      pos[e] = -1;
-      if (e < cnt) {
-        const int i = e0 + e;
-        while (ch + 1 < nch && coff[ch + 1] <= i) ++ch;
-        const size_t ci = (size_t(b) * P.nchunks + ch) * P.top_k + (i - coff[ch]);
-        key[e] = __ldcg(P.cand_key + ci);
-        pos[e] = __ldcg(P.cand_pos + ci);
-      }
-    }
-  }
+  for (int e = 0; e < kSdFinalItems; ++e) key[e] = e < cnt ? __ldcg(P.cand_key + cand(e0 + e)) : 0u;
   uint32_t T = 0u, need_eq = 0xFFFFFFFFu;
   if (k < m) block_topk_threshold<kSdFinalItems>(key, cnt, m, k, sm, T, need_eq);
   uint32_t q;
@@ -246,7 +236,7 @@ __global__ void __launch_bounds__(kTopkThreads) sd_topk_final_kernel(const SdPar
     if (e < cnt) {
       const uint32_t u = key[e];
       const bool isq = u == T;
-      if ((u > T || (isq && q < need_eq)) && w < uint32_t(k)) sel[w++] = pos[e];
+      if ((u > T || (isq && q < need_eq)) && w < uint32_t(k)) sel[w++] = __ldcg(P.cand_pos + cand(e0 + e));
       q += isq;
     }
   if (tid == 0) P.nsel[b] = k;
@@ -368,34 +358,43 @@ __global__ void __launch_bounds__(256) sd_merge_kernel(const SdParams P) {
   const int kvh = blockIdx.x, b = blockIdx.y;
   int S;
   if (!sd_len_ok(P, b, S)) return;
+  __shared__ float sm[kSdMaxSplits][kSdMaxG], sl[kSdMaxSplits][kSdMaxG], sf[kSdMaxSplits][kSdMaxG];
   __shared__ float sM[kSdMaxG], sI[kSdMaxG];
   const size_t pbase = (size_t(b) * P.Hkv + kvh) * P.splits;
-  if (threadIdx.x < P.G) {
+  const int G = P.G;
+  for (int t = threadIdx.x; t < P.splits * G; t += blockDim.x) {  // every (split, head) at once
+    const int sp = t / G, gg = t % G;
+    const float* sl_ = P.part + (pbase + sp) * kSdPartFloats;
+    sm[sp][gg] = sl_[gg];
+    sl[sp][gg] = sl_[kSdMaxG + gg];
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
     const int gg = threadIdx.x;
     float M = -INFINITY;
-    for (int s = 0; s < P.splits; ++s) M = fmaxf(M, P.part[(pbase + s) * kSdPartFloats + gg]);
+    for (int sp = 0; sp < P.splits; ++sp) M = fmaxf(M, sm[sp][gg]);
     float L = 0.f;
     if (M != -INFINITY)
-      for (int s = 0; s < P.splits; ++s) {
-        const float* sl = P.part + (pbase + s) * kSdPartFloats;
-        if (sl[gg] != -INFINITY) L += sl[kSdMaxG + gg] * exp2f(sl[gg] - M);
-      }
+      for (int sp = 0; sp < P.splits; ++sp)
+        if (sm[sp][gg] != -INFINITY) L += sl[sp][gg] * exp2f(sm[sp][gg] - M);
     sM[gg] = M;
     sI[gg] = L > 0.f ? 1.f / L : 0.f;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < P.G * kSdD; idx += blockDim.x) {
+  for (int t = threadIdx.x; t < P.splits * G; t += blockDim.x) {
+    const int sp = t / G, gg = t % G;
+    sf[sp][gg] = (sM[gg] != -INFINITY && sm[sp][gg] != -INFINITY) ? exp2f(sm[sp][gg] - sM[gg]) * sI[gg] : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * kSdD; idx += blockDim.x) {
     const int gg = idx / kSdD, dd = idx % kSdD;
     float acc = 0.f;
-    if (sM[gg] != -INFINITY)
-      for (int s = 0; s < P.splits; ++s) {
-        const float* sl = P.part + (pbase + s) * kSdPartFloats;
-        if (sl[gg] != -INFINITY) acc += sl[2 * kSdMaxG + gg * kSdD + dd] * exp2f(sl[gg] - sM[gg]);
-      }
-    const float v = acc * sI[gg];
-    const size_t oi = (size_t(b) * P.Hq + kvh * P.G + gg) * kSdD + dd;
-    if (P.out_f32) static_cast<float*>(P.out)[oi] = v;
-    else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(v);
+#pragma unroll 8
+    for (int sp = 0; sp < P.splits; ++sp)
+      acc += sf[sp][gg] * P.part[(pbase + sp) * kSdPartFloats + 2 * kSdMaxG + gg * kSdD + dd];
+    const size_t oi = (size_t(b) * P.Hq + kvh * G + gg) * kSdD + dd;
+    if (P.out_f32) static_cast<float*>(P.out)[oi] = acc;
+    else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(acc);
   }
   if (kvh == 0 && threadIdx.x == 0) P.seq_lens[b] = S;
 }
