@@ -26,6 +26,7 @@
 // truncate kernel, one CTA per sequence: releases the pages past
 //   ceil(n_keep / page_size) and publishes the new length.
 #include "common.cuh"
+#include "topk_block.cuh"
 
 namespace kvsel {
 
@@ -34,7 +35,6 @@ constexpr int kPg = 16;
 constexpr int kSelThreads = 1024;
 constexpr int kChunk = 64;
 constexpr int kItems = 32;
-constexpr int kBandMax = 8192;
 
 struct SelectParams {
   const int32_t* seq_lens;
@@ -48,109 +48,18 @@ struct SelectParams {
   int Hkv, max_len, budget, n_sink, window;
 };
 
-// Exclusive block-wide scan of one value per thread (1024 threads).
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_tot, uint32_t& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_tot[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t t = warp_tot[lane];
-    uint32_t s = t;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    warp_tot[lane] = s - t;  // exclusive prefix of warp totals
-    if (lane == 31) warp_tot[32] = s;
-  }
-  __syncthreads();
-  const uint32_t res = warp_tot[warp] + x - v;
-  total = warp_tot[32];
-  __syncthreads();
-  return res;
-}
-
-// Radix select over `n` keys held in shared memory: finds the krem-th largest
-// key T and how many copies of T belong to the top krem.
-__device__ __forceinline__ void smem_radix_select(const uint32_t* keys, int n, uint32_t krem,
-                                                  uint32_t* hist, uint32_t* s_digit,
-                                                  uint32_t* s_above, uint32_t& T, uint32_t& need_eq) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint32_t prefix = 0, mask = 0;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (tid < 256) hist[tid] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += blockDim.x) {
-      const uint32_t u = keys[i];
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins 255-8l .. 255-8l-7; find the digit holding the krem-th largest
-      uint32_t cb[8], lsum = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        cb[e] = hist[255 - 8 * lane - e];
-        lsum += cb[e];
-      }
-      uint32_t incl = lsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t excl = incl - lsum;
-      if (excl < krem && krem <= incl) {
-        uint32_t above = excl;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (above + cb[e] >= krem) {
-            *s_digit = 255 - 8 * lane - e;
-            *s_above = above;
-            break;
-          }
-          above += cb[e];
-        }
-      }
-    }
-    __syncthreads();
-    krem -= *s_above;
-    prefix |= *s_digit << shift;
-    mask |= 0xFFu << shift;
-    __syncthreads();
-  }
-  T = prefix;
-  need_eq = krem;
-}
-
-// Per (sequence, kv head) row: the threshold key T of the top-k middle slots
-// and how many slots equal to T are taken (lowest slots first), then the
-// ordered emission of the kept list.
-//
-// Register path (rows of at most kSelThreads * kItems candidates): every
-// thread holds its contiguous run of candidate keys.  A sample (the first key
-// of every run) is sorted; two sample quantiles bracket the k-th key with a
-// margin of four binomial standard deviations; one counting pass checks the
-// bracket and the keys inside it are gathered to shared memory, where an
-// exact radix select finishes.  If the bracket misses, or for longer rows, a
-// radix select runs over the whole row in global memory instead.
+// Per (sequence, kv head) row: the k kept middle slots (ties to the lower
+// slot), ascending.  Register path (rows of at most kSelThreads * kItems
+// candidates): each thread holds its contiguous run of candidate keys; the
+// row's previous threshold (kept in the workspace), or else a sample
+// quantile, bounds the k-th key from below and block_topk_upper finishes on
+// the keys above that bound.  Last fallback (and longer rows): a radix select
+// over the whole row in global memory, then an ordered emission over it.
 template <bool kInRegs>
 __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectParams P) {
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t scan_tmp[33];
-  __shared__ uint32_t s_digit, s_above;
+  extern __shared__ __align__(16) uint8_t sel_smem[];
+  UpperSmem& up = *reinterpret_cast<UpperSmem*>(sel_smem);
   __shared__ int s_first;
-  __shared__ uint32_t sample[kInRegs ? kSelThreads : 1];
-  __shared__ uint32_t band[kInRegs ? kBandMax : 1];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the scores come from the previous kernel
 
   const int kvh = blockIdx.x, b = blockIdx.y;
@@ -182,155 +91,62 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
   const int C = (n_cand + kSelThreads - 1) / kSelThreads;
   const int j0 = lo + min(n_cand, tid * C);
   const int cnt = min(n_cand, (tid + 1) * C) - min(n_cand, tid * C);
-  constexpr int kR = kInRegs ? kItems : 1;
-  uint32_t key[kR];
-  if constexpr (kInRegs) {
-#pragma unroll
-    for (int e = 0; e < kR; ++e) key[e] = e < cnt ? order_key(row[j0 + e]) : 0u;
-  }
-  // Visit this thread's candidates in slot order: BODY sees (e, u).
-#define KVSEL_FOR_ITEMS(BODY)                                     \
-  if constexpr (kInRegs) {                                        \
-    _Pragma("unroll") for (int e = 0; e < kR; ++e) if (e < cnt) { \
-      const uint32_t u = key[e];                                  \
-      BODY                                                        \
-    }                                                             \
-  } else {                                                        \
-    for (int e = 0; e < cnt; ++e) {                               \
-      const uint32_t u = order_key(row[j0 + e]);                  \
-      BODY                                                        \
-    }                                                             \
-  }
-
-  uint32_t T = 0xFFFFFFFFu, need_eq = 0, tot = 0;
+  uint32_t T = 0xFFFFFFFFu, need_eq = 0;
   bool done = false;
   if constexpr (kInRegs) {
-    // 0. the previous call's threshold for this row: the keys at or above it are
-    //    usually about k (scores only grow between calls), so they make a small
-    //    band holding the k-th key; any stale hint just fails the check below.
-    const uint32_t hint = k > 0 ? P.hint[rowi] : 0u;
-    if (hint != 0u) {
-      uint32_t c_band = 0;
-      KVSEL_FOR_ITEMS(c_band += u >= hint;)
-      uint32_t band_tot;
-      const uint32_t band_base = block_exclusive_scan(c_band, scan_tmp, band_tot);
-      if (uint32_t(k) <= band_tot && band_tot <= uint32_t(kBandMax)) {
-        uint32_t w = band_base;
-        KVSEL_FOR_ITEMS(if (u >= hint) band[w++] = u;)
-        __syncthreads();
-        smem_radix_select(band, int(band_tot), uint32_t(k), hist, &s_digit, &s_above, T, need_eq);
-        done = true;
-      }
-    }
-    if (k > 0 && !done) {
-      // 1. sample = first key of each run (0 sorts below every real key), sorted descending
-      sample[tid] = cnt > 0 ? key[0] : 0u;
-      __syncthreads();
-      for (int kk = 2; kk <= kSelThreads; kk <<= 1)
-        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-          const int l = tid ^ jj;
-          if (l > tid) {
-            const uint32_t x = sample[tid], y = sample[l];
-            const bool desc = (tid & kk) == 0;
-            if (desc ? (x < y) : (x > y)) {
-              sample[tid] = y;
-              sample[l] = x;
-            }
-          }
-          __syncthreads();
-        }
-      // 2. bracket [t_lo, t_hi] around the estimated sample rank of the k-th key
-      const int ns = (n_cand + C - 1) / C;  // runs that hold a sample
-      const float p = float(k) / float(n_cand);
-      const int est = int((long long)k * ns / n_cand);
-      const int margin = 16 + int(4.0f * sqrtf(float(ns) * p * (1.f - p)));
-      const uint32_t t_hi = est - margin >= 0 ? sample[est - margin] : 0xFFFFFFFFu;
-      const uint32_t t_lo = est + margin < ns ? sample[est + margin] : 0u;
-      uint32_t c_gt = 0, c_band = 0;
-      KVSEL_FOR_ITEMS(c_gt += u > t_hi; c_band += (u >= t_lo) & (u <= t_hi);)
-      uint32_t gt_tot, band_tot;
-      block_exclusive_scan(c_gt, scan_tmp, gt_tot);
-      const uint32_t band_base = block_exclusive_scan(c_band, scan_tmp, band_tot);
-      if (gt_tot < uint32_t(k) && uint32_t(k) <= gt_tot + band_tot && band_tot <= uint32_t(kBandMax)) {
-        // 3. gather the band and select exactly inside it
-        uint32_t w = band_base;
-        KVSEL_FOR_ITEMS(if ((u >= t_lo) & (u <= t_hi)) band[w++] = u;)
-        __syncthreads();
-        smem_radix_select(band, int(band_tot), uint32_t(k) - gt_tot, hist, &s_digit, &s_above, T,
-                          need_eq);
-        done = true;
-      }
+    if (k > 0) {
+      uint32_t key[kItems];
+#pragma unroll
+      for (int e = 0; e < kItems; ++e) key[e] = e < cnt ? order_key(row[j0 + e]) : 0u;
+      auto pos_of = [&](int e) { return j0 + e; };
+      const uint32_t hint = P.hint[rowi];
+      done = block_topk_upper<kItems>(key, cnt, pos_of, n_cand, k, hint, up, keep + P.n_sink, T, need_eq);
+      if (!done && hint != 0u)
+        done = block_topk_upper<kItems>(key, cnt, pos_of, n_cand, k, 0u, up, keep + P.n_sink, T, need_eq);
     }
   }
   if (k > 0 && !done) {
-    // full radix select, re-reading the row from global memory
+    // whole-row radix select in global memory
     uint32_t prefix = 0, mask = 0, krem = uint32_t(k);
-    const int warp = tid >> 5, lane = tid & 31;
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      if (tid < 256) hist[tid] = 0;
+      if (tid < 256) up.base.hist[tid] = 0;
       __syncthreads();
       for (int j = lo + tid; j < hi; j += kSelThreads) {
         const uint32_t u = order_key(row[j]);
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        if ((u & mask) == prefix) atomicAdd(&up.base.hist[(u >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (warp == 0) {
-        uint32_t cb[8], lsum = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          cb[e] = hist[255 - 8 * lane - e];
-          lsum += cb[e];
-        }
-        uint32_t incl = lsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const uint32_t excl = incl - lsum;
-        if (excl < krem && krem <= incl) {
-          uint32_t above = excl;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if (above + cb[e] >= krem) {
-              s_digit = 255 - 8 * lane - e;
-              s_above = above;
-              break;
-            }
-            above += cb[e];
-          }
-        }
-      }
+      topk_pick_digit(up.base, krem);
       __syncthreads();
-      krem -= s_above;
-      prefix |= s_digit << shift;
+      krem -= up.base.above;
+      prefix |= up.base.digit << shift;
       mask |= 0xFFu << shift;
       __syncthreads();
     }
     T = prefix;
     need_eq = krem;
-  }
-
-  if (k > 0 && tid == 0) P.hint[rowi] = T;
-
-  // ordered emission of the heavy hitters
-  uint32_t gt = 0, eq = 0;
-  if (k > 0) {
-    KVSEL_FOR_ITEMS(gt += u > T; eq += u == T;)
-  }
-  const uint32_t eq_base = block_exclusive_scan(eq, scan_tmp, tot);
-  const uint32_t take_eq = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
-  const uint32_t out_base = block_exclusive_scan(gt + take_eq, scan_tmp, tot);
-  if (k > 0 && gt + take_eq > 0) {
-    uint32_t w = P.n_sink + out_base, q = eq_base;
+    // ordered emission over the whole row (contiguous runs per thread)
+    uint32_t gt = 0, eq = 0;
+    for (int e = 0; e < cnt; ++e) {
+      const uint32_t u = order_key(row[j0 + e]);
+      gt += u > T;
+      eq += u == T;
+    }
+    uint32_t tot;
+    const uint32_t eq_base = topk_block_scan(eq, up.base.scan, tot);
+    const uint32_t take_eq = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
+    uint32_t w = P.n_sink + topk_block_scan(gt + take_eq, up.base.scan, tot), q = eq_base;
     const uint32_t wend = uint32_t(P.n_sink + k);
-    KVSEL_FOR_ITEMS(const bool isq = u == T;
-                    if ((u > T || (isq && q < need_eq)) && w < wend) keep[w++] = j0 + e;
-                    q += isq;)
+    for (int e = 0; e < cnt; ++e) {
+      const uint32_t u = order_key(row[j0 + e]);
+      const bool isq = u == T;
+      if ((u > T || (isq && q < need_eq)) && w < wend) keep[w++] = j0 + e;
+      q += isq;
+    }
   }
-#undef KVSEL_FOR_ITEMS
+  if (k > 0 && tid == 0) P.hint[rowi] = T;
   for (int i = tid; i < P.n_sink; i += kSelThreads) keep[i] = i;
   for (int i = tid; i < P.window; i += kSelThreads) keep[P.budget - P.window + i] = S - P.window + i;
   if (tid == 0) s_first = P.budget;
@@ -512,6 +328,7 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kv->num_kv_heads, batch);
   cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = kTopkDynSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -519,6 +336,13 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool in_regs = (long long)max_len - n_sink - window <= (long long)kSelThreads * kItems;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t a1 = cudaFuncSetAttribute(h2o_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTopkDynSmem));
+    cudaError_t a2 = cudaFuncSetAttribute(h2o_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTopkDynSmem));
+    if (a1 != cudaSuccess || a2 != cudaSuccess) return cuda_fail(a1 != cudaSuccess ? a1 : a2, "kvsel_h2o_evict (attribute)");
+    attr_set = true;
+  }
   trace_before("h2o_select", st);
   cudaError_t e = in_regs ? cudaLaunchKernelEx(&cfg, h2o_select_kernel<true>, P)
                           : cudaLaunchKernelEx(&cfg, h2o_select_kernel<false>, P);

@@ -278,8 +278,9 @@ snap_qk_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
 
 // max-pool of the votes + exact top-keep_k + the window, ascending
 __global__ void __launch_bounds__(kTopkThreads) snap_select_kernel(const SnapParams P) {
-  __shared__ TopkSmem sm;
-  extern __shared__ float svote[];  // the row's votes (prefix length floats)
+  extern __shared__ __align__(16) uint8_t tk_smem[];
+  UpperSmem& up = *reinterpret_cast<UpperSmem*>(tk_smem);
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem);
   const int pair = blockIdx.x, tid = threadIdx.x;
   const int Pfx = P.S - P.W;
   const int nk = P.keep_k + P.W;
@@ -289,33 +290,36 @@ __global__ void __launch_bounds__(kTopkThreads) snap_select_kernel(const SnapPar
     for (int i = tid; i < nk; i += kTopkThreads) keep[i] = i < P.S ? i : -1;
     return;
   }
-  for (int j = tid; j < Pfx; j += kTopkThreads) svote[j] = __ldcg(vrow + j);
-  __syncthreads();
   const int C = (Pfx + kTopkThreads - 1) / kTopkThreads;
   const int e0 = min(Pfx, tid * C), cnt = min(Pfx, (tid + 1) * C) - e0;
   uint32_t key[kSnSelItems];
+  // stride-1 max-pool over the clamped window; the vote row is L2-resident
 #pragma unroll
   for (int e = 0; e < kSnSelItems; ++e) {
     key[e] = 0u;
     if (e < cnt) {
       const int j = e0 + e;
+      const int t1 = min(Pfx - 1, j + P.pool_half);
       float mx = -INFINITY;
-      for (int t = max(0, j - P.pool_half); t <= min(Pfx - 1, j + P.pool_half); ++t) mx = fmaxf(mx, svote[t]);
+      for (int t = max(0, j - P.pool_half); t <= t1; ++t) mx = fmaxf(mx, __ldcg(vrow + t));
       key[e] = order_key(mx);
     }
   }
   uint32_t T, need_eq;
-  block_topk_threshold<kSnSelItems>(key, cnt, Pfx, P.keep_k, sm, T, need_eq);
-  uint32_t q;
-  uint32_t w = block_topk_emit_offsets<kSnSelItems>(key, cnt, T, need_eq, sm, q);
+  auto pos_of = [&](int e) { return e0 + e; };
+  if (!block_topk_upper<kSnSelItems>(key, cnt, pos_of, Pfx, P.keep_k, 0u, up, keep, T, need_eq)) {
+    block_topk_threshold<kSnSelItems>(key, cnt, Pfx, P.keep_k, sm, T, need_eq);
+    uint32_t q;
+    uint32_t w = block_topk_emit_offsets<kSnSelItems>(key, cnt, T, need_eq, sm, q);
 #pragma unroll
-  for (int e = 0; e < kSnSelItems; ++e)
-    if (e < cnt) {
-      const uint32_t u = key[e];
-      const bool isq = u == T;
-      if ((u > T || (isq && q < need_eq)) && w < uint32_t(P.keep_k)) keep[w++] = e0 + e;
-      q += isq;
-    }
+    for (int e = 0; e < kSnSelItems; ++e)
+      if (e < cnt) {
+        const uint32_t u = key[e];
+        const bool isq = u == T;
+        if ((u > T || (isq && q < need_eq)) && w < uint32_t(P.keep_k)) keep[w++] = e0 + e;
+        q += isq;
+      }
+  }
   for (int i = tid; i < P.W; i += kTopkThreads) keep[P.keep_k + i] = Pfx + i;
 }
 
@@ -425,7 +429,7 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
     cudaError_t e1 = cudaFuncSetAttribute(snap_qk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSnSmem));
     cudaError_t e2 = cudaFuncSetAttribute(snap_qk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSnSmem));
     cudaError_t e3 = cudaFuncSetAttribute(snap_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          int(kSnSelItems * kTopkThreads * sizeof(float)));
+                                          int(kTopkDynSmem));
     if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess)
       return cuda_fail(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3), "kvsel_snapkv_select (attribute)");
     attr_set = true;
@@ -445,7 +449,7 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
     if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (vote launch)");
   }
   trace_before("snap_select", st);
-  snap_select_kernel<<<num_layers * Hkv, kTopkThreads, size_t(std::max(seq_len - obs_window, 1)) * sizeof(float), st>>>(P);
+  snap_select_kernel<<<num_layers * Hkv, kTopkThreads, kTopkDynSmem, st>>>(P);
   e = cudaGetLastError();
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (select launch)");

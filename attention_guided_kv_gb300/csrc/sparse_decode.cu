@@ -59,8 +59,7 @@ struct SdParams {
   __nv_bfloat16* idx_k;            // [B][max_len][64]
   const __nv_bfloat16* idx_k_new;  // [B][64] or null
   float* scores;                   // [B][max_len] (workspace or the caller's buffer)
-  uint32_t* cand_key;              // [B][nchunks][top_k]
-  int32_t* cand_pos;
+  int32_t* cand_pos;               // [B][nchunks][top_k]
   int32_t* cand_cnt;               // [B][nchunks]
   int32_t* sel;                    // [B][top_k]
   int32_t* nsel;                   // [B]
@@ -163,24 +162,32 @@ __global__ void __launch_bounds__(128) sd_index_kernel(const SdParams P) {
 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kTopkThreads) sd_topk_chunk_kernel(const SdParams P) {
-  __shared__ TopkSmem sm;
+  extern __shared__ __align__(16) uint8_t tk_smem[];
+  UpperSmem& up = *reinterpret_cast<UpperSmem*>(tk_smem);
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem);
   const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   int S;
   if (!sd_len_ok(P, b, S)) return;
   const int p0 = c * kSdChunk;
   const int n = max(0, min(kSdChunk, S - p0));
   const int kc = min(P.top_k, n);
-  const size_t cbase = (size_t(b) * P.nchunks + c) * P.top_k;
+  int32_t* cpos = P.cand_pos + (size_t(b) * P.nchunks + c) * P.top_k;
   if (tid == 0) P.cand_cnt[b * P.nchunks + c] = kc;
   if (n == 0) return;
+  if (kc == n) {  // the whole chunk is kept
+    for (int i = tid; i < n; i += kTopkThreads) cpos[i] = p0 + i;
+    return;
+  }
   const float* srow = P.scores + size_t(b) * P.max_len + p0;
   const int C = (n + kTopkThreads - 1) / kTopkThreads;
   const int e0 = min(n, tid * C), cnt = min(n, (tid + 1) * C) - e0;
   uint32_t key[kSdChunkItems];
 #pragma unroll
   for (int e = 0; e < kSdChunkItems; ++e) key[e] = e < cnt ? order_key(__ldcg(srow + e0 + e)) : 0u;
-  uint32_t T = 0u, need_eq = 0xFFFFFFFFu;  // keep everything when n <= top_k
-  if (kc < n) block_topk_threshold<kSdChunkItems>(key, cnt, n, kc, sm, T, need_eq);
+  uint32_t T, need_eq;
+  auto pos_of = [&](int e) { return p0 + e0 + e; };
+  if (block_topk_upper<kSdChunkItems>(key, cnt, pos_of, n, kc, 0u, up, cpos, T, need_eq)) return;
+  block_topk_threshold<kSdChunkItems>(key, cnt, n, kc, sm, T, need_eq);
   uint32_t q;
   uint32_t w = block_topk_emit_offsets<kSdChunkItems>(key, cnt, T, need_eq, sm, q);
 #pragma unroll
@@ -188,18 +195,16 @@ __global__ void __launch_bounds__(kTopkThreads) sd_topk_chunk_kernel(const SdPar
     if (e < cnt) {
       const uint32_t u = key[e];
       const bool isq = u == T;
-      if ((u > T || (isq && q < need_eq)) && w < uint32_t(kc)) {
-        P.cand_key[cbase + w] = u;
-        P.cand_pos[cbase + w] = p0 + e0 + e;
-        ++w;
-      }
+      if ((u > T || (isq && q < need_eq)) && w < uint32_t(kc)) cpos[w++] = p0 + e0 + e;
       q += isq;
     }
 }
 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kTopkThreads) sd_topk_final_kernel(const SdParams P) {
-  __shared__ TopkSmem sm;
+  extern __shared__ __align__(16) uint8_t tk_smem[];
+  UpperSmem& up = *reinterpret_cast<UpperSmem*>(tk_smem);
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem);
   __shared__ int coff[kSdMaxChunks + 1];
   const int b = blockIdx.x, tid = threadIdx.x;
   int S;
@@ -217,28 +222,37 @@ __global__ void __launch_bounds__(kTopkThreads) sd_topk_final_kernel(const SdPar
   const int m = coff[nch];
   const int k = min(P.top_k, m);
   const int kcf = min(P.top_k, kSdChunk);  // every chunk but the last holds exactly kcf candidates
-  const int C = (m + kTopkThreads - 1) / kTopkThreads;
-  const int e0 = min(m, tid * C), cnt = min(m, (tid + 1) * C) - e0;
   auto cand = [&](int i) -> size_t {
     const int c = i / kcf;
     return (size_t(b) * P.nchunks + c) * P.top_k + (i - c * kcf);
   };
-  uint32_t key[kSdFinalItems];
-#pragma unroll
-  for (int e = 0; e < kSdFinalItems; ++e) key[e] = e < cnt ? __ldcg(P.cand_key + cand(e0 + e)) : 0u;
-  uint32_t T = 0u, need_eq = 0xFFFFFFFFu;
-  if (k < m) block_topk_threshold<kSdFinalItems>(key, cnt, m, k, sm, T, need_eq);
-  uint32_t q;
-  uint32_t w = block_topk_emit_offsets<kSdFinalItems>(key, cnt, T, need_eq, sm, q);
   int32_t* sel = P.sel + size_t(b) * P.top_k;
+  if (k == m) {  // every candidate is kept; candidates are already in position order
+    for (int i = tid; i < m; i += kTopkThreads) sel[i] = __ldcg(P.cand_pos + cand(i));
+  } else {
+    const float* srow = P.scores + size_t(b) * P.max_len;
+    const int C = (m + kTopkThreads - 1) / kTopkThreads;
+    const int e0 = min(m, tid * C), cnt = min(m, (tid + 1) * C) - e0;
+    uint32_t key[kSdFinalItems];
 #pragma unroll
-  for (int e = 0; e < kSdFinalItems; ++e)
-    if (e < cnt) {
-      const uint32_t u = key[e];
-      const bool isq = u == T;
-      if ((u > T || (isq && q < need_eq)) && w < uint32_t(k)) sel[w++] = __ldcg(P.cand_pos + cand(e0 + e));
-      q += isq;
+    for (int e = 0; e < kSdFinalItems; ++e)
+      key[e] = e < cnt ? order_key(__ldcg(srow + __ldcg(P.cand_pos + cand(e0 + e)))) : 0u;
+    auto pos_of = [&](int e) { return __ldcg(P.cand_pos + cand(e0 + e)); };
+    uint32_t T, need_eq;
+    if (!block_topk_upper<kSdFinalItems>(key, cnt, pos_of, m, k, 0u, up, sel, T, need_eq)) {
+      block_topk_threshold<kSdFinalItems>(key, cnt, m, k, sm, T, need_eq);
+      uint32_t q;
+      uint32_t w = block_topk_emit_offsets<kSdFinalItems>(key, cnt, T, need_eq, sm, q);
+#pragma unroll
+      for (int e = 0; e < kSdFinalItems; ++e)
+        if (e < cnt) {
+          const uint32_t u = key[e];
+          const bool isq = u == T;
+          if ((u > T || (isq && q < need_eq)) && w < uint32_t(k)) sel[w++] = pos_of(e);
+          q += isq;
+        }
     }
+  }
   if (tid == 0) P.nsel[b] = k;
   __syncthreads();
   if (P.topk_out)
@@ -406,7 +420,7 @@ using namespace kvsel_host;
 
 namespace {
 struct SdWs {
-  size_t scores, ckey, cpos, ccnt, sel, nsel, part, total;
+  size_t scores, cpos, ccnt, sel, nsel, part, total;
   int nchunks;
 };
 SdWs sd_ws_layout(int batch, int Hkv, int max_len, int top_k, bool own_scores) {
@@ -419,7 +433,6 @@ SdWs sd_ws_layout(int batch, int Hkv, int max_len, int top_k, bool own_scores) {
     return o;
   };
   w.scores = own_scores ? take(size_t(batch) * max_len * 4) : 0;
-  w.ckey = take(size_t(batch) * w.nchunks * top_k * 4);
   w.cpos = take(size_t(batch) * w.nchunks * top_k * 4);
   w.ccnt = take(size_t(batch) * w.nchunks * 4);
   w.sel = take(size_t(batch) * top_k * 4);
@@ -496,7 +509,6 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   P.idx_k = static_cast<__nv_bfloat16*>(idx_k);
   P.idx_k_new = static_cast<const __nv_bfloat16*>(idx_k_new);
   P.scores = scores_out ? scores_out : reinterpret_cast<float*>(ws + L.scores);
-  P.cand_key = reinterpret_cast<uint32_t*>(ws + L.ckey);
   P.cand_pos = reinterpret_cast<int32_t*>(ws + L.cpos);
   P.cand_cnt = reinterpret_cast<int32_t*>(ws + L.ccnt);
   P.sel = reinterpret_cast<int32_t*>(ws + L.sel);
@@ -523,8 +535,12 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e0 = cudaFuncSetAttribute(sd_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                int(kSdAttnSmem));
+    cudaError_t e0 = cudaFuncSetAttribute(sd_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          int(kSdAttnSmem));
+    if (e0 == cudaSuccess)
+      e0 = cudaFuncSetAttribute(sd_topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTopkDynSmem));
+    if (e0 == cudaSuccess)
+      e0 = cudaFuncSetAttribute(sd_topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTopkDynSmem));
     if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_sparse_decode (attribute)");
     attr_set = true;
   }
@@ -536,8 +552,8 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   trace_after(st);                                                       \
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_sparse_decode (" name ")");
   KVSEL_SD_LAUNCH("sd_index", sd_index_kernel, dim3((max_len + 127) / 128, batch), 128, 0)
-  KVSEL_SD_LAUNCH("sd_topk_chunk", sd_topk_chunk_kernel, dim3(L.nchunks, batch), kTopkThreads, 0)
-  KVSEL_SD_LAUNCH("sd_topk_final", sd_topk_final_kernel, dim3(batch), kTopkThreads, 0)
+  KVSEL_SD_LAUNCH("sd_topk_chunk", sd_topk_chunk_kernel, dim3(L.nchunks, batch), kTopkThreads, kTopkDynSmem)
+  KVSEL_SD_LAUNCH("sd_topk_final", sd_topk_final_kernel, dim3(batch), kTopkThreads, kTopkDynSmem)
   KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem)
   KVSEL_SD_LAUNCH("sd_merge", sd_merge_kernel, dim3(Hkv, batch), 256, 0)
 #undef KVSEL_SD_LAUNCH
