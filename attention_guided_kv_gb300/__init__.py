@@ -55,10 +55,11 @@ _SIGS = {
     "kvsel_trace_stop": (_i, [ctypes.POINTER(ctypes.c_char_p), _i]),
     "kvsel_decode_attn_workspace": (_sz, [_PKV, _i, _i, _i]),
     "kvsel_decode_attn": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _f, _vp, _i, _vp,
-                               _vp, _i, _i, _vp, _sz, _vp]),
+                               _vp, _i, _i, _vp, _sz, _vp, _sz, _vp]),
     "kvsel_decode_attn_noalloc": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _f, _vp, _i,
                                        _vp, _vp, _i, _i, _vp]),
     "kvsel_h2o_evict_workspace": (_sz, [_PKV, _i, _i]),
+    "kvsel_h2o_link_bytes": (_sz, [_i, _i]),
     "kvsel_h2o_evict": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                              _sz, _vp]),
     "kvsel_block_priority_workspace": (_sz, [_i, ctypes.c_int64]),
@@ -179,8 +180,12 @@ def kvsel_decode_attn_workspace(kv: PagedKV, batch: int, max_len: int, with_prob
 
 def kvsel_decode_attn(kv: PagedKV, block_table, seq_lens, q, out, workspace, *, k_new=None,
                       v_new=None, pos_map=None, next_pos=None, scale=None, probs=None,
-                      h2o_cum=None, max_len=None, num_ctas=0, stream=None):
-    """Append (optional) + decode attention + probabilities + H2O score update."""
+                      h2o_cum=None, max_len=None, num_ctas=0, h2o_link=None, stream=None):
+    """Append (optional) + decode attention + probabilities + H2O score update.
+
+    h2o_link: the workspace of the kvsel_h2o_evict calls that follow (same
+    batch); the step then hands them its heavy-hitter candidates.
+    """
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
     _need(q, torch.bfloat16, "q")
@@ -208,7 +213,8 @@ def kvsel_decode_attn(kv: PagedKV, block_table, seq_lens, q, out, workspace, *, 
         ctypes.byref(kv), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch, _ptr(q),
         _ptr(k_new), _ptr(v_new), _ptr(pos_map), _ptr(next_pos), float(scale), _ptr(out), odt,
         _ptr(probs), _ptr(h2o_cum), int(max_len), int(num_ctas), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        workspace.numel() * workspace.element_size(), _ptr(h2o_link),
+        0 if h2o_link is None else h2o_link.numel() * h2o_link.element_size(), _stream(stream)))
 
 
 def kvsel_decode_attn_noalloc(kv: PagedKV, block_table, seq_lens, q, out, *, k_new=None,

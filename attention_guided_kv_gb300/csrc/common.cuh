@@ -149,6 +149,8 @@ kvsel_status fail(kvsel_status code, const std::string& msg);
 kvsel_status cuda_fail(cudaError_t err, const char* what);
 bool aligned(const void* p, size_t a);
 int sm_count();
+// Raise a kernel's dynamic shared memory limit to `bytes`, once per device.
+cudaError_t smem_limit_once(const void* fn, int bytes);
 // Encode a 2D bf16 tensor map with 128-byte swizzle over a [rows][inner] array.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);

@@ -39,6 +39,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "h2o_link.cuh"
 
 namespace kvsel {
 
@@ -63,8 +64,11 @@ struct SmemLayout {
   static constexpr size_t seqPref = seqS + size_t(kMaxBatch) * 4;                        // [kMaxBatch+1] i64
   static constexpr size_t stats = seqPref + size_t(kMaxBatch + 1) * 8;                   // [8][2] f32
   static constexpr size_t owners = stats + kMaxG * 2 * 4;                                // [kMaxOwners+1] i32
-  static constexpr size_t total = owners + (kMaxOwners + 1) * 4;
+  static constexpr size_t link = owners + (kMaxOwners + 1) * 4;                          // count, base u32
+  static constexpr size_t total = link + 2 * 4;
 };
+// Phase B stages a segment's H2O candidates in the (then idle) TMA ring.
+constexpr int kStageCands = kStages * kStageBytes / 8;  // (key u32, slot i32) pairs
 constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 
 struct StepParams {
@@ -80,6 +84,10 @@ struct StepParams {
   float* logits;   // log2-domain logits [B][Hq][max_len] (the probs buffer or workspace), or null
   float* probs;    // output probabilities or null (may alias logits)
   float* cum;      // H2O score [B][Hkv][max_len] or null
+  uint32_t* link_hint;   // H2O candidate hand-off (h2o_link.cuh), all null when not linked
+  uint32_t* link_count;
+  uint32_t* link_key;
+  int32_t* link_pos;
   void* out;
   float* part;     // [slots][kPartFloats]
   unsigned* bar;   // grid barrier words: [0] arrivals, [32] generation
@@ -154,6 +162,44 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int NC) {
   return int(((u + 1) * NC + U - 1) / U) - 1;
 }
 
+// Stages the slots j + c (c < n) whose new score key is >= hk in shared
+// memory (sk / sp, counter *scnt): one shared atomic per warp (any subset of
+// its lanes).  Entries past kStageCands are dropped; the caller sees the
+// overflow in the counter.
+template <int n>
+__device__ __forceinline__ void link_stage(uint32_t* sk, int32_t* sp, uint32_t* scnt, int j, float4 v,
+                                           uint32_t hk) {
+  const uint32_t key[4] = {order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w)};
+  bool hit[n];
+#pragma unroll
+  for (int c = 0; c < n; ++c) hit[c] = key[c] >= hk;
+  const uint32_t act = __activemask();
+  const int lane = threadIdx.x & 31;
+  uint32_t lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+  uint32_t tot = 0, pre = 0;
+#pragma unroll
+  for (int c = 0; c < n; ++c) {
+    const uint32_t b = __ballot_sync(act, hit[c]);
+    tot += __popc(b);
+    pre += __popc(b & lt);
+  }
+  if (tot == 0) return;
+  const int leader = __ffs(act) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(scnt, tot);
+  base = __shfl_sync(act, base, leader) + pre;
+#pragma unroll
+  for (int c = 0; c < n; ++c)
+    if (hit[c]) {
+      if (base < uint32_t(kStageCands)) {
+        sk[base] = key[c];
+        sp[base] = j + c;
+      }
+      ++base;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
 decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const StepParams P) {
@@ -208,6 +254,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   }
   const Locator loc{sS, sPref, P.B, Hkv};
   const long long u0 = U * c / NC, u1 = U * (c + 1) / NC;
+  if (P.link_count && c == 0)  // fresh candidate lists (phase B appends after the grid barrier)
+    for (int i = tid; i < P.B * Hkv; i += kThreads) P.link_count[i] = 0u;
 
   // ---- append the new tokens whose page falls in this CTA's range ----
   if (append && tid < 32) {
@@ -443,6 +491,9 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ================= phase B =================
+  uint32_t* sLink = reinterpret_cast<uint32_t*>(smem + SmemLayout::link);  // staged count, list base
+  uint32_t* stKey = reinterpret_cast<uint32_t*>(smem + SmemLayout::ring);  // the idle TMA ring
+  int32_t* stPos = reinterpret_cast<int32_t*>(smem + SmemLayout::ring + kStageCands * 4);
   if (c == 0) {
     if (tid == 0)
       for (int b = 0; b < P.B; ++b) {
@@ -478,6 +529,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         cc = nu > plast ? -1 : cta_of(nu, U, NC);
       }
       sOwn[kMaxOwners] = no;
+      sLink[0] = 0u;
     }
     __syncthreads();
     const int nown = sOwn[kMaxOwners];
@@ -517,6 +569,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       const int j1 = min(S, int(pg + (seg_end - u)) * kPage);
       const size_t row0 = (size_t(b) * P.Hq + kvh * G) * P.max_len;
       float* crow = P.cum ? P.cum + (size_t(b) * Hkv + kvh) * P.max_len : nullptr;
+      // the row's last H2O threshold: collect the slots at or above it (0: no list)
+      const uint32_t hk = (crow && P.link_hint) ? __ldcg(P.link_hint + pair) : 0u;
       float Mg[kMaxG], Ig[kMaxG];
 #pragma unroll
       for (int gg = 0; gg < kMaxG; ++gg) {
@@ -555,8 +609,9 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
               if (j + 2 == S - 1) old.z = 0.f;
               if (j + 3 == S - 1) old.w = 0.f;
             }
-            __stcg(reinterpret_cast<float4*>(crow + j),
-                   make_float4(old.x + sum.x, old.y + sum.y, old.z + sum.z, old.w + sum.w));
+            const float4 nv = make_float4(old.x + sum.x, old.y + sum.y, old.z + sum.z, old.w + sum.w);
+            __stcg(reinterpret_cast<float4*>(crow + j), nv);
+            if (hk) link_stage<4>(stKey, stPos, sLink, j, nv, hk);
           }
         };
         const int jend = j0 + ((j1 - j0) & ~3);
@@ -589,7 +644,25 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           }
         if (crow) {
           const float old = (append && jj == S - 1) ? 0.f : crow[jj];
-          crow[jj] = old + sum;
+          const float nv = old + sum;
+          crow[jj] = nv;
+          if (hk) link_stage<1>(stKey, stPos, sLink, jj, make_float4(nv, 0.f, 0.f, 0.f), hk);
+        }
+      }
+      if (hk) {  // hand this segment's candidates to the row's list: one global atomic
+        __syncthreads();
+        const uint32_t n = sLink[0];
+        if (tid == 0)  // an overflowing stage invalidates the row's list (count > capacity)
+          sLink[1] = atomicAdd(P.link_count + pair, n > uint32_t(kStageCands) ? uint32_t(kLinkCap) + 1u : n);
+        __syncthreads();
+        const uint32_t base = sLink[1];
+        if (n <= uint32_t(kStageCands)) {
+          uint32_t* gk = P.link_key + size_t(pair) * kLinkCap;
+          int32_t* gp = P.link_pos + size_t(pair) * kLinkCap;
+          for (uint32_t i = tid; i < n && base + i < uint32_t(kLinkCap); i += kThreads) {
+            gk[base + i] = stKey[i];
+            gp[base + i] = stPos[i];
+          }
         }
       }
     }
@@ -653,7 +726,8 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
                                           const void* k_new, const void* v_new, int32_t* pos_map,
                                           int32_t* next_pos, float scale, void* out, int out_dtype,
                                           float* probs, float* h2o_cum, int max_len, int num_ctas,
-                                          void* workspace, size_t ws_bytes, void* stream) {
+                                          void* workspace, size_t ws_bytes, void* h2o_link,
+                                          size_t h2o_link_bytes, void* stream) {
   const std::string fn = "kvsel_decode_attn: ";
   if (!kv || !kv->k_pool || !kv->v_pool)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "kv pools must be non-NULL");
@@ -687,6 +761,9 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
     return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace too small: need " + std::to_string(L.total));
   if (!aligned(workspace, 256))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace must be 256-byte aligned");
+  if (h2o_link && (!aligned(h2o_link, 256) || h2o_link_bytes < link_bytes(batch * Hkv)))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "h2o_link must be a 256-byte aligned H2O evict workspace of at least " +
+                                           std::to_string(link_bytes(batch * Hkv)) + " bytes");
 
   const int occ = ctas_per_sm();
   if (occ < 1) return fail(KVSEL_ERR_CUDA, fn + "cannot configure the decode kernel (occupancy 0)");
@@ -716,6 +793,15 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   P.logits = probs ? probs : (h2o_cum ? reinterpret_cast<float*>(ws + L.logit_off) : nullptr);
   P.probs = probs;
   P.cum = h2o_cum;
+  P.link_hint = P.link_count = P.link_key = nullptr;
+  P.link_pos = nullptr;
+  if (h2o_link && h2o_cum) {
+    const H2OLink L2 = link_layout(h2o_link, batch * Hkv);
+    P.link_hint = L2.hint;
+    P.link_count = L2.count;
+    P.link_key = L2.key;
+    P.link_pos = L2.pos;
+  }
   P.out = out;
   P.part = reinterpret_cast<float*>(ws + L.part_off);
   P.bar = reinterpret_cast<unsigned*>(ws + 64);
@@ -811,5 +897,5 @@ extern "C" kvsel_status kvsel_decode_attn_noalloc(const kvsel_paged_kv* kv, cons
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_decode_attn_noalloc (clear)");
   return kvsel_decode_attn(kv, block_table, max_pages, seq_lens, batch, q, k_new, v_new, pos_map,
                            next_pos, scale, out, out_dtype, probs, h2o_cum, max_len, num_ctas, scratch,
-                           kNoAllocScratchBytes, stream);
+                           kNoAllocScratchBytes, nullptr, 0, stream);
 }

@@ -7,17 +7,13 @@
 // [n_sink, S - window) with the largest cumulative score (ties to the lower
 // slot), and [S - window, S); evict the rest.
 //
-// select kernel, one 1024-thread CTA per (sequence, kv head):
-//   finds the k-th largest score over the middle slots on a monotone uint32
-//   image of the fp32 score.  The row's previous threshold (kept in the
-//   workspace) usually bounds a band of about k keys from below; otherwise a
-//   sorted sample brackets it; one counting pass gathers the keys inside the
-//   band, and a 4 x 8-bit radix select finishes exactly (a radix select over
-//   the whole row is the last fallback); then an
-//   ordered emission: each thread owns a
-//   contiguous run of slots, two block-wide scans give every thread its share
-//   of the threshold ties (lowest slots first) and its output offset, so the
-//   kept list comes out in ascending slot order without a sort.
+// select kernel, one 1024-thread CTA per (sequence, kv head): an exact
+//   top-k over a monotone uint32 image of the fp32 score (row_topk.cuh):
+//   coalesced float4 loads into registers, a lower bound on the k-th key
+//   (the row's previous threshold, kept in the workspace, else a sample
+//   quantile), a radix select over the keys above that bound only, and an
+//   ordered emission that writes the kept list in ascending slot order
+//   (lowest slots first among ties) without a sort.
 // compact kernel, one CTA per (sequence, kv head): moves kept rows to slots
 //   0..n_keep-1 in chunks of 64 slots.  Each chunk reads all of its sources
 //   into shared memory before writing any destination; a kept list is sorted
@@ -26,7 +22,8 @@
 // truncate kernel, one CTA per sequence: releases the pages past
 //   ceil(n_keep / page_size) and publishes the new length.
 #include "common.cuh"
-#include "topk_block.cuh"
+#include "h2o_link.cuh"
+#include "row_topk.cuh"
 
 namespace kvsel {
 
@@ -34,7 +31,7 @@ constexpr int kHD = 128;
 constexpr int kPg = 16;
 constexpr int kSelThreads = 1024;
 constexpr int kChunk = 64;
-constexpr int kItems = 32;
+constexpr int kSelGroups = 8;  // register-resident rows: up to 32 x 8 x 128 candidates
 
 struct SelectParams {
   const int32_t* seq_lens;
@@ -43,23 +40,147 @@ struct SelectParams {
   int32_t* keep_slots;  // workspace [B][Hkv][budget]
   int32_t* keep_out;    // [B][Hkv][budget] or null
   int32_t* first_move;  // workspace [B][Hkv]
-  uint32_t* hint;       // workspace [B][Hkv]: last threshold key per row (0 = none)
+  H2OLink link;         // workspace: thresholds and the decode step's candidate lists
   int* status;
   int Hkv, max_len, budget, n_sink, window;
 };
 
-// Per (sequence, kv head) row: the k kept middle slots (ties to the lower
-// slot), ascending.  Register path (rows of at most kSelThreads * kItems
-// candidates): each thread holds its contiguous run of candidate keys; the
-// row's previous threshold (kept in the workspace), or else a sample
-// quantile, bounds the k-th key from below and block_topk_upper finishes on
-// the keys above that bound.  Last fallback (and longer rows): a radix select
-// over the whole row in global memory, then an ordered emission over it.
-template <bool kInRegs>
+constexpr int kListWords = 1024;  // list path: rows of up to 32768 candidate slots
+
+struct SelSmem {
+  RowTopkSmem rk;
+  int32_t upos[kRkUpMax];           // listed slots (relative to n_sink)
+  uint32_t bits[2][kListWords];     // kept-above / tie bitmaps over the candidate slots
+  uint32_t m, minkey, bad;
+};
+static_assert(kRkUpMax >= kLinkCap, "every listed slot fits in shared memory");
+
+__device__ __forceinline__ uint32_t lowest_bits(uint32_t x, uint32_t n) {
+  uint32_t r = 0;
+  for (uint32_t t = 0; t < n && x; ++t) {
+    const uint32_t b = x & (0u - x);
+    r |= b;
+    x ^= b;
+  }
+  return r;
+}
+
+// Top-k of the middle slots [lo, hi) from the candidate list that the decode
+// step collected (every slot whose score is >= the row's last threshold).
+// Usable when the list is fresh and holds at least k slots of [lo, hi): the
+// k-th score is then >= the old threshold, so the list holds every slot the
+// top k can contain.  Freshness is checked on the first 1024 entries (their
+// listed score must still equal the row's score at that slot); any later
+// decode step changes every listed score, since each live slot gains a
+// positive probability.  Emits the kept slots through put(i, slot) in ascending
+// order and returns true, else returns false (block-uniform) having written
+// nothing.
+template <class Put>
+__device__ __forceinline__ bool select_from_list(const SelectParams& P, size_t rowi, const float* row,
+                                                 uint32_t cnt, int lo, int hi, int k, SelSmem& sm,
+                                                 uint32_t& T, Put put) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t* lk = P.link.key + rowi * kLinkCap;
+  const int32_t* lp = P.link.pos + rowi * kLinkCap;
+  const int nw = (hi - lo + 31) >> 5;
+  if (tid == 0) {
+    sm.m = 0;
+    sm.rk.maxkey = 0;
+    sm.minkey = 0xFFFFFFFFu;
+  }
+  for (int i = tid; i < nw; i += kSelThreads) sm.bits[0][i] = sm.bits[1][i] = 0u;
+  __syncthreads();
+  uint32_t lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+  uint32_t mx = 0, mn = 0xFFFFFFFFu, bad = 0;
+  const uint32_t cnt_r = (cnt + 31u) & ~31u;
+  for (uint32_t i = tid; i < cnt_r; i += kSelThreads) {
+    bool v = false;
+    uint32_t key = 0;
+    int pos = 0;
+    if (i < cnt) {
+      key = __ldcg(lk + i);
+      pos = __ldcg(lp + i);
+      if (pos < 0 || pos >= P.max_len) bad = 1;
+      else if (i < uint32_t(kSelThreads)) bad |= order_key(__ldcg(row + pos)) != key;  // stale list?
+      v = pos >= lo && pos < hi;
+    }
+    const uint32_t bal = __ballot_sync(0xffffffffu, v);
+    if (bal) {
+      uint32_t base = 0;
+      if (lane == 0) base = atomicAdd(&sm.m, uint32_t(__popc(bal)));
+      base = __shfl_sync(0xffffffffu, base, 0) + __popc(bal & lt);
+      if (v) {
+        sm.rk.ukey[base] = key;
+        sm.upos[base] = pos - lo;
+        mx = max(mx, key);
+        mn = min(mn, key);
+      }
+    }
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  if (lane == 0) {
+    if (mx) atomicMax(&sm.rk.maxkey, mx);
+    atomicMin(&sm.minkey, mn);
+  }
+  if (__syncthreads_or(bad)) return false;
+  const uint32_t m = sm.m;
+  if (m < uint32_t(k)) return false;
+  uint32_t need_eq;
+  const uint32_t lo_key = sm.minkey, hi_key = sm.rk.maxkey;
+  if (lo_key == hi_key) {
+    T = lo_key;
+    need_eq = uint32_t(k);
+  } else {
+    const uint32_t m_r = (m + 31u) & ~31u;
+    rk_radix(
+        [&](auto&& f) {
+          for (uint32_t i = tid; i < m_r; i += kSelThreads) {
+            const bool live = i < m;
+            f(live ? sm.rk.ukey[i] : 0u, live);
+          }
+        },
+        31 - __clz(lo_key ^ hi_key), lo_key, uint32_t(k), sm.rk, T, need_eq);
+  }
+  for (uint32_t i = tid; i < m; i += kSelThreads) {
+    const uint32_t u = sm.rk.ukey[i];
+    const int r = sm.upos[i];
+    if (u > T) atomicOr(&sm.bits[0][r >> 5], 1u << (r & 31));
+    else if (u == T) atomicOr(&sm.bits[1][r >> 5], 1u << (r & 31));
+  }
+  __syncthreads();
+  // ordered emission: thread t owns bitmap word t (32 slots)
+  const uint32_t wg = tid < nw ? sm.bits[0][tid] : 0u, we = tid < nw ? sm.bits[1][tid] : 0u;
+  uint32_t total;
+  const uint32_t ex = rk_block_excl_scan(uint32_t(__popc(wg)) | (uint32_t(__popc(we)) << 16), sm.rk.wtot[0], total);
+  const uint32_t g_before = ex & 0xFFFFu, e_before = ex >> 16;
+  const uint32_t take = need_eq > e_before ? min(uint32_t(__popc(we)), need_eq - e_before) : 0u;
+  uint32_t keepw = wg | lowest_bits(we, take);
+  uint32_t o = g_before + min(e_before, need_eq);
+  uint32_t* staged = sm.rk.ukey;
+  while (keepw) {
+    const int bit = __ffs(keepw) - 1;
+    keepw &= keepw - 1;
+    if (o < uint32_t(k)) staged[o] = uint32_t(tid * 32 + bit);
+    ++o;
+  }
+  __syncthreads();
+  for (int i = tid; i < k; i += kSelThreads) put(i, lo + int(staged[i]));
+  return true;
+}
+
+// Per (sequence, kv head) row: the sinks, the k heaviest middle slots
+// [n_sink, S - window) (ties to the lower slot) and the window, ascending.
+// row_topk selects the middle slots, trying the row's previous threshold
+// (kept in the workspace) as its first lower bound; the kept list, the
+// original positions and the first slot that moves are written as the
+// positions are emitted.
 __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectParams P) {
   extern __shared__ __align__(16) uint8_t sel_smem[];
-  UpperSmem& up = *reinterpret_cast<UpperSmem*>(sel_smem);
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_smem);
   __shared__ int s_first;
+  __shared__ uint32_t s_cnt;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the scores come from the previous kernel
 
   const int kvh = blockIdx.x, b = blockIdx.y;
@@ -75,91 +196,56 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
     if (tid == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
     return;
   }
+  if (tid == 0) s_cnt = P.link.count[rowi];
+  __syncthreads();
+  const uint32_t cnt = s_cnt;
   if (S <= P.budget) {
     for (int i = tid; i < P.budget; i += kSelThreads) {
       const int slot = i < S ? i : -1;
       keep[i] = slot;
       if (kout) kout[i] = slot < 0 ? -1 : (prow ? prow[slot] : slot);
     }
-    if (tid == 0) P.first_move[rowi] = S;
+    if (tid == 0) {
+      P.first_move[rowi] = S;
+      P.link.count[rowi] = 0u;  // a list is used at most once
+    }
     return;
   }
-
-  const int k = P.budget - P.n_sink - P.window;
-  const int lo = P.n_sink, hi = S - P.window;
-  const int n_cand = hi - lo;
-  const int C = (n_cand + kSelThreads - 1) / kSelThreads;
-  const int j0 = lo + min(n_cand, tid * C);
-  const int cnt = min(n_cand, (tid + 1) * C) - min(n_cand, tid * C);
-  uint32_t T = 0xFFFFFFFFu, need_eq = 0;
-  bool done = false;
-  if constexpr (kInRegs) {
-    if (k > 0) {
-      uint32_t key[kItems];
-#pragma unroll
-      for (int e = 0; e < kItems; ++e) key[e] = e < cnt ? order_key(row[j0 + e]) : 0u;
-      auto pos_of = [&](int e) { return j0 + e; };
-      const uint32_t hint = P.hint[rowi];
-      done = block_topk_upper<kItems>(key, cnt, pos_of, n_cand, k, hint, up, keep + P.n_sink, T, need_eq);
-      if (!done && hint != 0u)
-        done = block_topk_upper<kItems>(key, cnt, pos_of, n_cand, k, 0u, up, keep + P.n_sink, T, need_eq);
-    }
-  }
-  if (k > 0 && !done) {
-    // whole-row radix select in global memory
-    uint32_t prefix = 0, mask = 0, krem = uint32_t(k);
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      if (tid < 256) up.base.hist[tid] = 0;
-      __syncthreads();
-      for (int j = lo + tid; j < hi; j += kSelThreads) {
-        const uint32_t u = order_key(row[j]);
-        if ((u & mask) == prefix) atomicAdd(&up.base.hist[(u >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      topk_pick_digit(up.base, krem);
-      __syncthreads();
-      krem -= up.base.above;
-      prefix |= up.base.digit << shift;
-      mask |= 0xFFu << shift;
-      __syncthreads();
-    }
-    T = prefix;
-    need_eq = krem;
-    // ordered emission over the whole row (contiguous runs per thread)
-    uint32_t gt = 0, eq = 0;
-    for (int e = 0; e < cnt; ++e) {
-      const uint32_t u = order_key(row[j0 + e]);
-      gt += u > T;
-      eq += u == T;
-    }
-    uint32_t tot;
-    const uint32_t eq_base = topk_block_scan(eq, up.base.scan, tot);
-    const uint32_t take_eq = need_eq > eq_base ? min(eq, need_eq - eq_base) : 0u;
-    uint32_t w = P.n_sink + topk_block_scan(gt + take_eq, up.base.scan, tot), q = eq_base;
-    const uint32_t wend = uint32_t(P.n_sink + k);
-    for (int e = 0; e < cnt; ++e) {
-      const uint32_t u = order_key(row[j0 + e]);
-      const bool isq = u == T;
-      if ((u > T || (isq && q < need_eq)) && w < wend) keep[w++] = j0 + e;
-      q += isq;
-    }
-  }
-  if (k > 0 && tid == 0) P.hint[rowi] = T;
-  for (int i = tid; i < P.n_sink; i += kSelThreads) keep[i] = i;
-  for (int i = tid; i < P.window; i += kSelThreads) keep[P.budget - P.window + i] = S - P.window + i;
   if (tid == 0) s_first = P.budget;
   __syncthreads();
+
+  const int k = P.budget - P.n_sink - P.window;
   int first = P.budget;
-  for (int i = tid; i < P.budget; i += kSelThreads) {
-    const int slot = keep[i];
-    if (kout) kout[i] = prow ? prow[slot] : slot;
-    if (slot != i) first = min(first, i);
+  auto put = [&](int o, int slot) {
+    keep[o] = slot;
+    if (kout) kout[o] = prow ? prow[slot] : slot;
+    if (slot != o) first = min(first, o);
+  };
+  if (k > 0) {
+    const int lo = P.n_sink, hi = S - P.window;
+    const uint32_t hk = P.link.hint[rowi];
+    uint32_t T = 0;
+    bool done = false;
+    if (hk != 0u && cnt >= uint32_t(k) && cnt <= uint32_t(kLinkCap) && hi - lo <= 32 * kListWords)
+      done = select_from_list(P, rowi, row, cnt, lo, hi, k, sm, T,
+                              [&](int i, int slot) { put(P.n_sink + i, slot); });
+    if (!done) {
+      const int a = P.n_sink & ~3;  // float4-aligned start of the candidate run
+      const float* base = row + a;
+      const F32RowKeys src{base, P.n_sink - a, S - P.window - a,
+                           (reinterpret_cast<uintptr_t>(base) & 15u) == 0};
+      T = row_topk<kSelGroups>(src, k, hk, sm.rk, [&](int i, int rel) { put(P.n_sink + i, a + rel); });
+    }
+    if (tid == 0) P.link.hint[rowi] = T;
   }
-  atomicMin(&s_first, first);
+  for (int i = tid; i < P.n_sink; i += kSelThreads) put(i, i);
+  for (int i = tid; i < P.window; i += kSelThreads) put(P.budget - P.window + i, S - P.window + i);
+  if (first < P.budget) atomicMin(&s_first, first);
   __syncthreads();
-  if (tid == 0) P.first_move[rowi] = s_first;
+  if (tid == 0) {
+    P.first_move[rowi] = s_first;
+    P.link.count[rowi] = 0u;
+  }
 }
 
 struct CompactParams {
@@ -264,21 +350,24 @@ using namespace kvsel_host;
 
 namespace {
 struct EvictWs {
-  size_t keep_off, first_off, hint_off, total;
+  size_t keep_off, first_off, total;
 };
 EvictWs evict_ws_layout(int batch, int Hkv, int budget) {
   EvictWs w;
-  size_t off = kStatusBytes;
+  size_t off = link_bytes(batch * Hkv);  // status block + the decode hand-off (h2o_link.cuh)
   w.keep_off = off;
   off = align_up(off + size_t(batch) * Hkv * budget * sizeof(int32_t), 256);
   w.first_off = off;
   off = align_up(off + size_t(batch) * Hkv * sizeof(int32_t), 256);
-  w.hint_off = off;
-  off = align_up(off + size_t(batch) * Hkv * sizeof(uint32_t), 256);
   w.total = off;
   return w;
 }
 }  // namespace
+
+extern "C" size_t kvsel_h2o_link_bytes(int batch, int num_kv_heads) {
+  if (batch < 1 || num_kv_heads < 1) return 0;
+  return link_bytes(batch * num_kv_heads);
+}
 
 extern "C" size_t kvsel_h2o_evict_workspace(const kvsel_paged_kv* kv, int batch, int budget) {
   if (!kv || batch < 1 || budget < 1 || kv->num_kv_heads < 1) return 0;
@@ -318,7 +407,7 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   P.keep_slots = reinterpret_cast<int32_t*>(ws + L.keep_off);
   P.keep_out = keep_out;
   P.first_move = reinterpret_cast<int32_t*>(ws + L.first_off);
-  P.hint = reinterpret_cast<uint32_t*>(ws + L.hint_off);
+  P.link = link_layout(workspace, batch * kv->num_kv_heads);
   P.status = reinterpret_cast<int*>(ws);
   P.Hkv = kv->num_kv_heads;
   P.max_len = max_len;
@@ -328,24 +417,18 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kv->num_kv_heads, batch);
   cfg.blockDim = dim3(kSelThreads);
-  cfg.dynamicSmemBytes = kTopkDynSmem;
+  cfg.dynamicSmemBytes = sizeof(SelSmem);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const bool in_regs = (long long)max_len - n_sink - window <= (long long)kSelThreads * kItems;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t a1 = cudaFuncSetAttribute(h2o_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTopkDynSmem));
-    cudaError_t a2 = cudaFuncSetAttribute(h2o_select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTopkDynSmem));
-    if (a1 != cudaSuccess || a2 != cudaSuccess) return cuda_fail(a1 != cudaSuccess ? a1 : a2, "kvsel_h2o_evict (attribute)");
-    attr_set = true;
-  }
+  if (cudaError_t a = smem_limit_once(reinterpret_cast<const void*>(h2o_select_kernel), int(sizeof(SelSmem)));
+      a != cudaSuccess)
+    return cuda_fail(a, "kvsel_h2o_evict (attribute)");
   trace_before("h2o_select", st);
-  cudaError_t e = in_regs ? cudaLaunchKernelEx(&cfg, h2o_select_kernel<true>, P)
-                          : cudaLaunchKernelEx(&cfg, h2o_select_kernel<false>, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, h2o_select_kernel, P);
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_h2o_evict (select launch)");
   if (!compact) return KVSEL_OK;

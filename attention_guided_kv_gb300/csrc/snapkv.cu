@@ -9,7 +9,7 @@
 // prefix) and the top keep_k prefix positions (ties to the lower position)
 // plus the window itself are kept, in ascending order.
 //
-// Kernels (three launches per call, all layers at once):
+// Kernels (four launches per call, all layers at once):
 //   snap_qk_kernel<1>  row softmax statistics: every CTA streams a chunk of a
 //                      (layer, kv head)'s K pages (TMA, 8-stage ring) and 8
 //                      warps each run 32 window rows against every page with
@@ -19,10 +19,12 @@
 //                      L2 or HBM), weights exp2(s - M_row) / L_row from the
 //                      merged statistics, summed over the warp's rows with
 //                      shuffles and over the 8 warps in shared memory.
-//   snap_select_kernel max-pool of the votes and exact top-k (sample
-//                      bracket + band radix select), window appended.
+//   snap_pool_kernel   max-pool of the votes into order keys (tiles of 1024
+//                      positions staged in shared memory with their halo).
+//   snap_select_kernel exact top-keep_k of the pooled keys per (layer, kv
+//                      head) with row_topk, window appended.
 #include "common.cuh"
-#include "topk_block.cuh"
+#include "row_topk.cuh"
 
 namespace kvsel {
 
@@ -34,7 +36,8 @@ constexpr int kSnWarps = 8;               // consumer warps: 32 window rows each
 constexpr int kSnThreads = (kSnWarps + 1) * 32;
 constexpr int kSnMaxRows = kSnWarps * 32; // G * W <= 256
 constexpr int kSnMaxChunks = 64;
-constexpr int kSnSelItems = 32;           // prefix <= 32768 positions per row
+constexpr int kSnSelGroups = 8;           // register-resident rows: prefix <= 32768
+constexpr int kSnPoolTile = 1024;
 constexpr int kSnMaxHalf = 16;            // pool kernel <= 33
 
 struct SnapParams {
@@ -43,6 +46,8 @@ struct SnapParams {
   float* stats;                // [L*Hkv][chunks][rows][2]
   float* vote;                 // [L*Hkv][S - W]
   int32_t* keep_out;           // [L*Hkv][keep_k + W]
+  uint32_t* pool_key;          // [L*Hkv][pool_stride]: order keys of the pooled votes
+  int pool_stride;
   int* status;
   int L, Hq, Hkv, G, W, rows, S, max_pages, num_pages, chunks, keep_k, pool_half;
   float scale_log2;
@@ -276,51 +281,43 @@ snap_qk_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
   }
 }
 
-// max-pool of the votes + exact top-keep_k + the window, ascending
-__global__ void __launch_bounds__(kTopkThreads) snap_select_kernel(const SnapParams P) {
+// Stride-1 max-pool of the votes over [j - pool_half, j + pool_half] clipped
+// to the prefix, stored as order keys; one tile of 1024 positions per CTA.
+__global__ void __launch_bounds__(kSnPoolTile) snap_pool_kernel(const SnapParams P) {
+  __shared__ float tile[kSnPoolTile + 2 * kSnMaxHalf];
+  const int pair = blockIdx.y, tid = threadIdx.x;
+  const int Pfx = P.S - P.W, h = P.pool_half;
+  const int j0 = blockIdx.x * kSnPoolTile;
+  const float* vrow = P.vote + size_t(pair) * Pfx;
+  for (int i = tid; i < kSnPoolTile + 2 * h; i += kSnPoolTile) {
+    const int j = j0 - h + i;
+    tile[i] = (j >= 0 && j < Pfx) ? __ldcg(vrow + j) : -INFINITY;
+  }
+  __syncthreads();
+  const int j = j0 + tid;
+  if (j < Pfx) {
+    float mx = tile[tid];
+    for (int t = 1; t <= 2 * h; ++t) mx = fmaxf(mx, tile[tid + t]);
+    P.pool_key[size_t(pair) * P.pool_stride + j] = order_key(mx);
+  }
+}
+
+// Exact top-keep_k of the pooled votes, then the window, ascending.
+__global__ void __launch_bounds__(kRkThreads) snap_select_kernel(const SnapParams P) {
   extern __shared__ __align__(16) uint8_t tk_smem[];
-  UpperSmem& up = *reinterpret_cast<UpperSmem*>(tk_smem);
-  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem);
+  RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
   const int pair = blockIdx.x, tid = threadIdx.x;
   const int Pfx = P.S - P.W;
   const int nk = P.keep_k + P.W;
   int32_t* keep = P.keep_out + size_t(pair) * nk;
-  const float* vrow = P.vote + size_t(pair) * Pfx;
   if (Pfx <= P.keep_k) {  // nothing to evict: every position, then -1 padding
-    for (int i = tid; i < nk; i += kTopkThreads) keep[i] = i < P.S ? i : -1;
+    for (int i = tid; i < nk; i += kRkThreads) keep[i] = i < P.S ? i : -1;
     return;
   }
-  const int C = (Pfx + kTopkThreads - 1) / kTopkThreads;
-  const int e0 = min(Pfx, tid * C), cnt = min(Pfx, (tid + 1) * C) - e0;
-  uint32_t key[kSnSelItems];
-  // stride-1 max-pool over the clamped window; the vote row is L2-resident
-#pragma unroll
-  for (int e = 0; e < kSnSelItems; ++e) {
-    key[e] = 0u;
-    if (e < cnt) {
-      const int j = e0 + e;
-      const int t1 = min(Pfx - 1, j + P.pool_half);
-      float mx = -INFINITY;
-      for (int t = max(0, j - P.pool_half); t <= t1; ++t) mx = fmaxf(mx, __ldcg(vrow + t));
-      key[e] = order_key(mx);
-    }
-  }
-  uint32_t T, need_eq;
-  auto pos_of = [&](int e) { return e0 + e; };
-  if (!block_topk_upper<kSnSelItems>(key, cnt, pos_of, Pfx, P.keep_k, 0u, up, keep, T, need_eq)) {
-    block_topk_threshold<kSnSelItems>(key, cnt, Pfx, P.keep_k, sm, T, need_eq);
-    uint32_t q;
-    uint32_t w = block_topk_emit_offsets<kSnSelItems>(key, cnt, T, need_eq, sm, q);
-#pragma unroll
-    for (int e = 0; e < kSnSelItems; ++e)
-      if (e < cnt) {
-        const uint32_t u = key[e];
-        const bool isq = u == T;
-        if ((u > T || (isq && q < need_eq)) && w < uint32_t(P.keep_k)) keep[w++] = e0 + e;
-        q += isq;
-      }
-  }
-  for (int i = tid; i < P.W; i += kTopkThreads) keep[P.keep_k + i] = Pfx + i;
+  const uint32_t* krow = P.pool_key + size_t(pair) * P.pool_stride;
+  const U32RowKeys src{krow, 0, Pfx, (reinterpret_cast<uintptr_t>(krow) & 15u) == 0};
+  row_topk<kSnSelGroups>(src, P.keep_k, 0u, sm, [&](int i, int rel) { keep[i] = rel; });
+  for (int i = tid; i < P.W; i += kRkThreads) keep[P.keep_k + i] = Pfx + i;
 }
 
 }  // namespace kvsel
@@ -332,7 +329,8 @@ namespace {
 constexpr size_t kSnSmem = size_t(kSnStages) * kSnStageBytes + 1024 + 2 * kSnStages * 8 +
                            kSnStages * 16 * 4 + kSnStages * 4 + kSnMaxRows * 2 * 4;
 struct SnWs {
-  size_t stats, vote, total;
+  size_t stats, vote, pool, total;
+  int pool_stride;
 };
 SnWs sn_ws_layout(int L, int Hkv, int rows, int S, int W, int chunks, bool own_vote) {
   SnWs w;
@@ -341,6 +339,9 @@ SnWs sn_ws_layout(int L, int Hkv, int rows, int S, int W, int chunks, bool own_v
   off = align_up(off + size_t(L) * Hkv * chunks * rows * 2 * 4, 256);
   w.vote = off;
   if (own_vote) off = align_up(off + size_t(L) * Hkv * std::max(S - W, 1) * 4, 256);
+  w.pool = off;
+  w.pool_stride = int(align_up(size_t(std::max(S - W, 1)), 4));
+  off = align_up(off + size_t(L) * Hkv * w.pool_stride * 4, 256);
   w.total = off;
   return w;
 }
@@ -382,8 +383,8 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
   const int rows = G * obs_window;
   if (rows > kSnMaxRows)
     return fail(KVSEL_ERR_UNSUPPORTED, fn + "(q heads per kv head) * obs_window must be <= 256");
-  if (seq_len - obs_window > kSnSelItems * kTopkThreads)
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "the prefix (seq_len - obs_window) must be <= 32768");
+  if (seq_len >= (1 << 28))
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "seq_len must be < 2^28");
   if (pool_kernel < 1 || pool_kernel % 2 == 0 || pool_kernel / 2 > kSnMaxHalf)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "pool_kernel must be odd, 1..33");
   if ((seq_len + kSnPage - 1) / kSnPage > max_pages)
@@ -408,6 +409,8 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
   P.stats = reinterpret_cast<float*>(ws + L.stats);
   P.vote = vote_out ? vote_out : reinterpret_cast<float*>(ws + L.vote);
   P.keep_out = keep_out;
+  P.pool_key = reinterpret_cast<uint32_t*>(ws + L.pool);
+  P.pool_stride = L.pool_stride;
   P.status = reinterpret_cast<int*>(ws);
   P.L = num_layers;
   P.Hq = Hq;
@@ -424,15 +427,12 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
   P.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e1 = cudaFuncSetAttribute(snap_qk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSnSmem));
-    cudaError_t e2 = cudaFuncSetAttribute(snap_qk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSnSmem));
-    cudaError_t e3 = cudaFuncSetAttribute(snap_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          int(kTopkDynSmem));
-    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess)
-      return cuda_fail(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3), "kvsel_snapkv_select (attribute)");
-    attr_set = true;
+  {
+    cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(snap_qk_kernel<1>), int(kSnSmem));
+    if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(snap_qk_kernel<2>), int(kSnSmem));
+    if (e0 == cudaSuccess)
+      e0 = smem_limit_once(reinterpret_cast<const void*>(snap_select_kernel), int(sizeof(RowTopkSmem)));
+    if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_snapkv_select (attribute)");
   }
   const dim3 grid(chunks, num_layers * Hkv);
   cudaError_t e;
@@ -448,8 +448,16 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
     trace_after(st);
     if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (vote launch)");
   }
+  if (seq_len - obs_window > keep_k) {
+    trace_before("snap_pool", st);
+    snap_pool_kernel<<<dim3((seq_len - obs_window + kSnPoolTile - 1) / kSnPoolTile, num_layers * Hkv),
+                       kSnPoolTile, 0, st>>>(P);
+    e = cudaGetLastError();
+    trace_after(st);
+    if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (pool launch)");
+  }
   trace_before("snap_select", st);
-  snap_select_kernel<<<num_layers * Hkv, kTopkThreads, kTopkDynSmem, st>>>(P);
+  snap_select_kernel<<<num_layers * Hkv, kRkThreads, sizeof(RowTopkSmem), st>>>(P);
   e = cudaGetLastError();
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (select launch)");

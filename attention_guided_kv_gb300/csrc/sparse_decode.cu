@@ -17,17 +17,19 @@
 //                        dims permuted per lane so every lane reads 8-byte runs
 //                        of a key row); also writes the appended token's K, V
 //                        and indexer key.
-//   sd_topk_chunk_kernel exact top-k of every 16K-position chunk of a row
-//   sd_topk_final_kernel exact top-k of the row over the chunk candidates
-//                        (candidates stay in position order, so the kept
-//                        positions come out ascending)
+//   sd_topk_chunk_kernel exact top-k (row_topk) of every 16K-position chunk
+//                        of a row, many CTAs per row: the candidates (key and
+//                        position, in position order)
+//   sd_topk_final_kernel exact top-k of each row over its chunk candidates;
+//                        kept positions come out ascending.  (With top_k >=
+//                        16K a single sd_topk_kernel per row replaces both.)
 //   sd_attn_kernel       (splits, kv head, sequence): each warp gathers 16
 //                        selected rows of K and V with cp.async into the
 //                        swizzled tile layout (double-buffered) and runs the
 //                        shared mma.sync tile; the 4 warps merge per CTA
 //   sd_merge_kernel      merges the splits into O and publishes the lengths
 #include "attn_tile.cuh"
-#include "topk_block.cuh"
+#include "row_topk.cuh"
 
 namespace kvsel {
 
@@ -35,11 +37,10 @@ constexpr int kSdD = 128;
 constexpr int kSdPage = 16;
 constexpr int kSdDi = 64;
 constexpr int kSdMaxHi = 8;
-constexpr int kSdChunk = 16384;          // positions per first-stage top-k chunk
-constexpr int kSdChunkItems = kSdChunk / kTopkThreads;
-constexpr int kSdFinalItems = 32;        // candidates per thread in the second stage
+constexpr int kSdTopkGroups = 8;         // rows up to 32K stay in registers; longer rows are swept
+constexpr int kSdChunk = 16384;          // positions per first-stage top-k chunk (top_k < kSdChunk)
+constexpr int kSdMaxLen = 1 << 28;
 constexpr int kSdMaxSplits = 64;
-constexpr int kSdMaxChunks = 63;       // max_len <= 63 * 16384
 constexpr int kSdMaxG = 8;
 constexpr int kSdPartFloats = kSdMaxG * (kSdD + 2);
 constexpr int kSdAttnWarps = 4;
@@ -59,8 +60,8 @@ struct SdParams {
   __nv_bfloat16* idx_k;            // [B][max_len][64]
   const __nv_bfloat16* idx_k_new;  // [B][64] or null
   float* scores;                   // [B][max_len] (workspace or the caller's buffer)
+  uint32_t* cand_key;              // [B][nchunks][top_k]: first-stage candidates (two-stage only)
   int32_t* cand_pos;               // [B][nchunks][top_k]
-  int32_t* cand_cnt;               // [B][nchunks]
   int32_t* sel;                    // [B][top_k]
   int32_t* nsel;                   // [B]
   int32_t* topk_out;               // [B][top_k] or null
@@ -161,103 +162,91 @@ __global__ void __launch_bounds__(128) sd_index_kernel(const SdParams P) {
 }
 
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kTopkThreads) sd_topk_chunk_kernel(const SdParams P) {
+// First stage (top_k < kSdChunk): the top_k of every chunk of kSdChunk
+// positions (the whole chunk when it is shorter), keys and positions in
+// position order.  Every chunk but a row's last holds exactly top_k
+// candidates, so a row's candidates are contiguous.
+__global__ void __launch_bounds__(kRkThreads) sd_topk_chunk_kernel(const SdParams P) {
   extern __shared__ __align__(16) uint8_t tk_smem[];
-  UpperSmem& up = *reinterpret_cast<UpperSmem*>(tk_smem);
-  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem);
+  RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
   const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   int S;
   if (!sd_len_ok(P, b, S)) return;
   const int p0 = c * kSdChunk;
   const int n = max(0, min(kSdChunk, S - p0));
+  if (n == 0 || S <= P.top_k) return;
   const int kc = min(P.top_k, n);
+  const float* srow = P.scores + size_t(b) * P.max_len + p0;
+  uint32_t* ckey = P.cand_key + (size_t(b) * P.nchunks + c) * P.top_k;
   int32_t* cpos = P.cand_pos + (size_t(b) * P.nchunks + c) * P.top_k;
-  if (tid == 0) P.cand_cnt[b * P.nchunks + c] = kc;
-  if (n == 0) return;
-  if (kc == n) {  // the whole chunk is kept
-    for (int i = tid; i < n; i += kTopkThreads) cpos[i] = p0 + i;
+  auto put = [&](int i, int rel) {
+    ckey[i] = order_key(__ldcg(srow + rel));
+    cpos[i] = p0 + rel;
+  };
+  if (kc == n) {
+    for (int i = tid; i < n; i += kRkThreads) put(i, i);
     return;
   }
-  const float* srow = P.scores + size_t(b) * P.max_len + p0;
-  const int C = (n + kTopkThreads - 1) / kTopkThreads;
-  const int e0 = min(n, tid * C), cnt = min(n, (tid + 1) * C) - e0;
-  uint32_t key[kSdChunkItems];
-#pragma unroll
-  for (int e = 0; e < kSdChunkItems; ++e) key[e] = e < cnt ? order_key(__ldcg(srow + e0 + e)) : 0u;
-  uint32_t T, need_eq;
-  auto pos_of = [&](int e) { return p0 + e0 + e; };
-  if (block_topk_upper<kSdChunkItems>(key, cnt, pos_of, n, kc, 0u, up, cpos, T, need_eq)) return;
-  block_topk_threshold<kSdChunkItems>(key, cnt, n, kc, sm, T, need_eq);
-  uint32_t q;
-  uint32_t w = block_topk_emit_offsets<kSdChunkItems>(key, cnt, T, need_eq, sm, q);
-#pragma unroll
-  for (int e = 0; e < kSdChunkItems; ++e)
-    if (e < cnt) {
-      const uint32_t u = key[e];
-      const bool isq = u == T;
-      if ((u > T || (isq && q < need_eq)) && w < uint32_t(kc)) cpos[w++] = p0 + e0 + e;
-      q += isq;
-    }
+  const F32RowKeys src{srow, 0, n, (reinterpret_cast<uintptr_t>(srow) & 15u) == 0};
+  row_topk<kSdTopkGroups>(src, kc, 0u, sm, put);
 }
 
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kTopkThreads) sd_topk_final_kernel(const SdParams P) {
+// Second stage: the top_k of a row over its chunk candidates, ascending.
+__global__ void __launch_bounds__(kRkThreads) sd_topk_final_kernel(const SdParams P) {
   extern __shared__ __align__(16) uint8_t tk_smem[];
-  UpperSmem& up = *reinterpret_cast<UpperSmem*>(tk_smem);
-  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem);
-  __shared__ int coff[kSdMaxChunks + 1];
+  RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
   const int b = blockIdx.x, tid = threadIdx.x;
   int S;
   if (!sd_len_ok(P, b, S)) return;
-  const int nch = (S + kSdChunk - 1) / kSdChunk;
-  if (tid == 0) {
-    int acc = 0;
-    for (int c = 0; c < nch; ++c) {
-      coff[c] = acc;
-      acc += P.cand_cnt[b * P.nchunks + c];
-    }
-    coff[nch] = acc;
-  }
-  __syncthreads();
-  const int m = coff[nch];
-  const int k = min(P.top_k, m);
-  const int kcf = min(P.top_k, kSdChunk);  // every chunk but the last holds exactly kcf candidates
-  auto cand = [&](int i) -> size_t {
-    const int c = i / kcf;
-    return (size_t(b) * P.nchunks + c) * P.top_k + (i - c * kcf);
-  };
+  const int k = min(P.top_k, S);
   int32_t* sel = P.sel + size_t(b) * P.top_k;
-  if (k == m) {  // every candidate is kept; candidates are already in position order
-    for (int i = tid; i < m; i += kTopkThreads) sel[i] = __ldcg(P.cand_pos + cand(i));
+  int32_t* tko = P.topk_out ? P.topk_out + size_t(b) * P.top_k : nullptr;
+  auto put = [&](int i, int pos) {
+    sel[i] = pos;
+    if (tko) tko[i] = pos;
+  };
+  if (k == S) {
+    for (int i = tid; i < S; i += kRkThreads) put(i, i);
+  } else {
+    const int nch = (S + kSdChunk - 1) / kSdChunk;
+    const int m = (nch - 1) * P.top_k + min(P.top_k, S - (nch - 1) * kSdChunk);
+    const uint32_t* ck = P.cand_key + size_t(b) * P.nchunks * P.top_k;
+    const int32_t* cp = P.cand_pos + size_t(b) * P.nchunks * P.top_k;
+    const U32RowKeys src{ck, 0, m, (reinterpret_cast<uintptr_t>(ck) & 15u) == 0};
+    row_topk<kSdTopkGroups>(src, k, 0u, sm, [&](int i, int rel) { put(i, __ldcg(cp + rel)); });
+  }
+  if (tko)
+    for (int i = k + tid; i < P.top_k; i += kRkThreads) tko[i] = -1;
+  if (tid == 0) P.nsel[b] = k;
+}
+
+// ---------------------------------------------------------------------------
+// Single stage (top_k >= kSdChunk): top-k positions of every row by indexer score (ties to the lower position),
+// ascending; every position when S <= top_k.  Also the -1-padded copy for the
+// caller.
+__global__ void __launch_bounds__(kRkThreads) sd_topk_kernel(const SdParams P) {
+  extern __shared__ __align__(16) uint8_t tk_smem[];
+  RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
+  const int b = blockIdx.x, tid = threadIdx.x;
+  int S;
+  if (!sd_len_ok(P, b, S)) return;
+  const int k = min(P.top_k, S);
+  int32_t* sel = P.sel + size_t(b) * P.top_k;
+  int32_t* tko = P.topk_out ? P.topk_out + size_t(b) * P.top_k : nullptr;
+  auto put = [&](int i, int pos) {
+    sel[i] = pos;
+    if (tko) tko[i] = pos;
+  };
+  if (k == S) {
+    for (int i = tid; i < S; i += kRkThreads) put(i, i);
   } else {
     const float* srow = P.scores + size_t(b) * P.max_len;
-    const int C = (m + kTopkThreads - 1) / kTopkThreads;
-    const int e0 = min(m, tid * C), cnt = min(m, (tid + 1) * C) - e0;
-    uint32_t key[kSdFinalItems];
-#pragma unroll
-    for (int e = 0; e < kSdFinalItems; ++e)
-      key[e] = e < cnt ? order_key(__ldcg(srow + __ldcg(P.cand_pos + cand(e0 + e)))) : 0u;
-    auto pos_of = [&](int e) { return __ldcg(P.cand_pos + cand(e0 + e)); };
-    uint32_t T, need_eq;
-    if (!block_topk_upper<kSdFinalItems>(key, cnt, pos_of, m, k, 0u, up, sel, T, need_eq)) {
-      block_topk_threshold<kSdFinalItems>(key, cnt, m, k, sm, T, need_eq);
-      uint32_t q;
-      uint32_t w = block_topk_emit_offsets<kSdFinalItems>(key, cnt, T, need_eq, sm, q);
-#pragma unroll
-      for (int e = 0; e < kSdFinalItems; ++e)
-        if (e < cnt) {
-          const uint32_t u = key[e];
-          const bool isq = u == T;
-          if ((u > T || (isq && q < need_eq)) && w < uint32_t(k)) sel[w++] = pos_of(e);
-          q += isq;
-        }
-    }
+    const F32RowKeys src{srow, 0, S, (reinterpret_cast<uintptr_t>(srow) & 15u) == 0};
+    row_topk<kSdTopkGroups>(src, k, 0u, sm, put);
   }
+  if (tko)
+    for (int i = k + tid; i < P.top_k; i += kRkThreads) tko[i] = -1;
   if (tid == 0) P.nsel[b] = k;
-  __syncthreads();
-  if (P.topk_out)
-    for (int i = tid; i < P.top_k; i += kTopkThreads)
-      P.topk_out[size_t(b) * P.top_k + i] = i < k ? sel[i] : -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -420,12 +409,12 @@ using namespace kvsel_host;
 
 namespace {
 struct SdWs {
-  size_t scores, cpos, ccnt, sel, nsel, part, total;
-  int nchunks;
+  size_t scores, ckey, cpos, sel, nsel, part, total;
+  int nchunks;  // 0: single-stage top-k
 };
 SdWs sd_ws_layout(int batch, int Hkv, int max_len, int top_k, bool own_scores) {
   SdWs w;
-  w.nchunks = (max_len + kSdChunk - 1) / kSdChunk;
+  w.nchunks = top_k < kSdChunk ? (max_len + kSdChunk - 1) / kSdChunk : 0;
   size_t off = kStatusBytes;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -433,8 +422,8 @@ SdWs sd_ws_layout(int batch, int Hkv, int max_len, int top_k, bool own_scores) {
     return o;
   };
   w.scores = own_scores ? take(size_t(batch) * max_len * 4) : 0;
+  w.ckey = take(size_t(batch) * w.nchunks * top_k * 4);
   w.cpos = take(size_t(batch) * w.nchunks * top_k * 4);
-  w.ccnt = take(size_t(batch) * w.nchunks * 4);
   w.sel = take(size_t(batch) * top_k * 4);
   w.nsel = take(size_t(batch) * 4);
   w.part = take(size_t(batch) * Hkv * kSdMaxSplits * kSdPartFloats * 4);
@@ -477,10 +466,7 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   if (out_dtype != KVSEL_BF16 && out_dtype != KVSEL_F32)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "out_dtype must be KVSEL_BF16 or KVSEL_F32");
   const SdWs L = sd_ws_layout(batch, Hkv, max_len, top_k, scores_out == nullptr);
-  if (L.nchunks > kSdMaxChunks ||
-      (long long)L.nchunks * std::min(top_k, kSdChunk) > (long long)kSdFinalItems * kTopkThreads)
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "need max_len <= 63 * 16384 and "
-                                            "ceil(max_len / 16384) * min(top_k, 16384) <= 32768");
+  if (max_len > kSdMaxLen) return fail(KVSEL_ERR_UNSUPPORTED, fn + "max_len must be <= 2^28");
   if (!aligned(kv->k_pool, 16) || !aligned(kv->v_pool, 16) || !aligned(q, 16) || !aligned(idx_k, 16) ||
       !aligned(idx_q, 8) || (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(idx_k_new, 16))))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "pools, q, k_new, v_new, idx_k, idx_k_new must be 16-byte aligned");
@@ -509,8 +495,9 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   P.idx_k = static_cast<__nv_bfloat16*>(idx_k);
   P.idx_k_new = static_cast<const __nv_bfloat16*>(idx_k_new);
   P.scores = scores_out ? scores_out : reinterpret_cast<float*>(ws + L.scores);
+  P.cand_key = reinterpret_cast<uint32_t*>(ws + L.ckey);
   P.cand_pos = reinterpret_cast<int32_t*>(ws + L.cpos);
-  P.cand_cnt = reinterpret_cast<int32_t*>(ws + L.ccnt);
+  P.nchunks = L.nchunks;
   P.sel = reinterpret_cast<int32_t*>(ws + L.sel);
   P.nsel = reinterpret_cast<int32_t*>(ws + L.nsel);
   P.topk_out = topk_out;
@@ -526,23 +513,19 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   P.num_pages = kv->num_pages;
   P.max_len = max_len;
   P.top_k = top_k;
-  P.nchunks = L.nchunks;
   P.splits = splits;
   P.appended = k_new ? 1 : 0;
   P.out_f32 = out_dtype == KVSEL_F32;
   P.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e0 = cudaFuncSetAttribute(sd_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          int(kSdAttnSmem));
-    if (e0 == cudaSuccess)
-      e0 = cudaFuncSetAttribute(sd_topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTopkDynSmem));
-    if (e0 == cudaSuccess)
-      e0 = cudaFuncSetAttribute(sd_topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTopkDynSmem));
+  {
+    cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(sd_attn_kernel), int(kSdAttnSmem));
+    for (const void* f : {reinterpret_cast<const void*>(sd_topk_kernel),
+                          reinterpret_cast<const void*>(sd_topk_chunk_kernel),
+                          reinterpret_cast<const void*>(sd_topk_final_kernel)})
+      if (e0 == cudaSuccess) e0 = smem_limit_once(f, int(sizeof(RowTopkSmem)));
     if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_sparse_decode (attribute)");
-    attr_set = true;
   }
   cudaError_t e;
 #define KVSEL_SD_LAUNCH(name, kernel, grid, block, smem)                 \
@@ -552,8 +535,12 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   trace_after(st);                                                       \
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_sparse_decode (" name ")");
   KVSEL_SD_LAUNCH("sd_index", sd_index_kernel, dim3((max_len + 127) / 128, batch), 128, 0)
-  KVSEL_SD_LAUNCH("sd_topk_chunk", sd_topk_chunk_kernel, dim3(L.nchunks, batch), kTopkThreads, kTopkDynSmem)
-  KVSEL_SD_LAUNCH("sd_topk_final", sd_topk_final_kernel, dim3(batch), kTopkThreads, kTopkDynSmem)
+  if (L.nchunks > 0) {
+    KVSEL_SD_LAUNCH("sd_topk_chunk", sd_topk_chunk_kernel, dim3(L.nchunks, batch), kRkThreads, sizeof(RowTopkSmem))
+    KVSEL_SD_LAUNCH("sd_topk_final", sd_topk_final_kernel, dim3(batch), kRkThreads, sizeof(RowTopkSmem))
+  } else {
+    KVSEL_SD_LAUNCH("sd_topk", sd_topk_kernel, dim3(batch), kRkThreads, sizeof(RowTopkSmem))
+  }
   KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem)
   KVSEL_SD_LAUNCH("sd_merge", sd_merge_kernel, dim3(Hkv, batch), 256, 0)
 #undef KVSEL_SD_LAUNCH

@@ -41,6 +41,34 @@ CONFIG_NAME = ("paged GQA decode + H2O select, Llama-2-70B layer shape (64 q / 8
 PAGE = 16
 
 
+
+TRACE_EVERY = 8   # launch tracing on one timed step in eight: events between kernels cost time
+
+
+def timed_steps(step_fn, first, steps, stream, per_step_launches):
+    """Run `steps` steps between two events on `stream`; every TRACE_EVERY-th
+    step is bracketed by the library's launch trace (events around each of its
+    kernels).  Returns (ms, [(kernel, ms)], launches per step)."""
+    import attention_guided_kv_gb300 as K
+    import torch
+    sampled = [i for i in range(first, first + steps) if (i - first) % TRACE_EVERY == 0]
+    traces = {i: K.LaunchTrace(per_step_launches + 4) for i in sampled}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(first, first + steps):
+        tr = traces.get(i)
+        if tr is None:
+            step_fn(i)
+        else:
+            with tr:
+                step_fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    durs = [d for tr in traces.values() for d in tr.durations()]
+    per_step = max(len(tr.names) for tr in traces.values())
+    return e0.elapsed_time(e1), durs, per_step
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -249,7 +277,7 @@ def cuda_arm(args, rank, world):
         if i % T == 0 and i > 0:
             seq.copy_(seq0)            # replay the 128-step window from 32K again
         K.kvsel_decode_attn(kv, bt, seq, q, out, ws, k_new=kn, v_new=vn, probs=probs, h2o_cum=cum,
-                            max_len=max_len)
+                            max_len=max_len, h2o_link=ws_ev)
         K.kvsel_h2o_evict(kv, bt, seq, cum, ws_ev, budget=wl.budget, n_sink=wl.n_sink,
                           window=wl.window, compact=False, keep_out=keep)
 
@@ -275,27 +303,17 @@ def cuda_arm(args, rank, world):
     time.sleep(0.3)
 
     # ---- timed region (device-resident inputs) ----
-    n_launch_cap = 3 * args.steps + 8
-    trace = K.LaunchTrace(n_launch_cap)
     barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
-    with trace:
-        ev0.record(stream)
-        for i in range(args.warmup, args.warmup + args.steps):
-            dev_step(i)
-        ev1.record(stream)
-    torch.cuda.synchronize()
+    ms, durs, per_step_launches = timed_steps(dev_step, args.warmup, args.steps, stream, 3)
     barrier()
     t_wall1 = time.time()
-    ms = ev0.elapsed_time(ev1)
     if world > 1:
         tt = torch.tensor([ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
-    durs = trace.durations()
-    launches = len(durs)
+    launches = per_step_launches * args.steps
 
     # live step lengths in the timed region (after the append)
     S_steps = [S0 + ((i % T) + 1) for i in range(args.warmup, args.warmup + args.steps)]
@@ -438,7 +456,7 @@ def _setup_decode_small(dev, small=False):
 
     def run(i, qi, kni, vni):
         K.kvsel_decode_attn(kv, bt, seq, qi, out, ws, k_new=kni, v_new=vni, pos_map=pos, next_pos=nxt,
-                            probs=probs, h2o_cum=cum, max_len=wl.max_len)
+                            probs=probs, h2o_cum=cum, max_len=wl.max_len, h2o_link=ws2)
         K.kvsel_h2o_evict(kv, bt, seq, cum, ws2, budget=wl.budget, n_sink=wl.n_sink, window=wl.window,
                           compact=True, pos_map=pos, keep_out=keep, freed_pages=freed)
         bt[:, page].copy_(freed[:, 0])
@@ -495,7 +513,7 @@ def _setup_snapkv(dev, small=False):
     kbytes = wl.S * wl.d * 2 * pairs
     return dict(step=step, run=run, host_in=[("q_obs", q[None])], outs=[keep], ws=[ws],
                 bytes={"snap_stats": kbytes, "snap_vote": kbytes}, flops={"snap_stats": qk_flops,
-                "snap_vote": 2.0 * rows * (wl.S - wl.W) * wl.d * pairs}, per_step_launches=3,
+                "snap_vote": 2.0 * rows * (wl.S - wl.W) * wl.d * pairs}, per_step_launches=4,
                 config={"layers": wl.L, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "prompt": wl.S,
                         "obs_window": wl.W, "keep": wl.keep_k, "pool_kernel": wl.pool_kernel,
                         "l2": "inputs larger than L2 (940 MB of K per pass)"})
@@ -710,25 +728,16 @@ def other_workload(args, rank, world):
     clocks = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid)
     clocks.start()
     time.sleep(0.3)
-    trace = K.LaunchTrace(S["per_step_launches"] * steps + 8)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     tw0 = time.time()
-    with trace:
-        e0.record(stream)
-        for i in range(args.warmup, args.warmup + steps):
-            S["step"](i)
-        e1.record(stream)
-    torch.cuda.synchronize()
+    ms, durs, per_step_launches = timed_steps(S["step"], args.warmup, steps, stream, S["per_step_launches"])
     tw1 = time.time()
-    ms = e0.elapsed_time(e1)
     if world > 1:
         tt = torch.tensor([ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
-    durs = trace.durations()
     per = {}
     for nm, d in durs:
         per.setdefault(nm, []).append(d)
@@ -813,7 +822,7 @@ def other_workload(args, rank, world):
             "kernel_ms": kern_ms, "roofline": roof,
             "e2e": {"value": world * steps / (e2e_ms / 1e3), "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": len(durs), "clocks": clocks.summary(tw0, tw1)}
+            "gpu_launches": per_step_launches * steps, "clocks": clocks.summary(tw0, tw1)}
     if variants:
         line["variants_us_per_pass"] = variants
     if args.small:

@@ -132,6 +132,17 @@ KVSEL_API int kvsel_trace_stop(const char** names, int capacity);
  *                that many, and at most 1024).  Results do not depend on it
  *                beyond fp32 rounding.
  *   workspace    >= kvsel_decode_attn_workspace(...) bytes, status word zeroed.
+ *   h2o_link     NULL, or the workspace of the kvsel_h2o_evict call(s) that
+ *                follow this step for the same batch and kv heads, with
+ *                h2o_link_bytes its size (at least the part that
+ *                kvsel_h2o_link_bytes(batch, num_kv_heads) gives; else
+ *                KVSEL_ERR_INVALID_ARG).  Used only with h2o_cum: the step
+ *                then also lists, per (sequence, kv head), the slots whose new
+ *                score is at or above the threshold that the last evict call
+ *                found for that row, and the next evict call selects among
+ *                those alone when the list allows it.  Selections are
+ *                identical with or without it.  The list is valid until the
+ *                next call that changes the scores.
  * Returns KVSEL_OK once the kernels are enqueued.
  */
 KVSEL_API size_t kvsel_decode_attn_workspace(const kvsel_paged_kv* kv, int batch, int max_len,
@@ -141,13 +152,18 @@ KVSEL_API kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_t
                                const void* k_new, const void* v_new, int32_t* pos_map,
                                int32_t* next_pos, float scale, void* out, int out_dtype,
                                float* probs, float* h2o_cum, int max_len, int num_ctas,
-                               void* workspace, size_t ws_bytes, void* stream);
+                               void* workspace, size_t ws_bytes, void* h2o_link,
+                               size_t h2o_link_bytes, void* stream);
+/* Bytes at the start of an H2O evict workspace that kvsel_decode_attn uses as
+ * h2o_link (0 for invalid arguments). */
+KVSEL_API size_t kvsel_h2o_link_bytes(int batch, int num_kv_heads);
 
 /* Allocation-free kvsel_decode_attn.  The pages have no counterpart: this is
  * for callers that cannot allocate device memory (a runtime without a device
  * allocator, a plug-in whose host owns all allocations, code that must not
  * call the allocator in the middle of a step).  It takes the same arguments
- * as kvsel_decode_attn minus the workspace and computes the same results;
+ * as kvsel_decode_attn minus the workspace and the H2O link, and computes
+ * the same results;
  * its scratch is a fixed 8 MiB array inside this library that every GPU
  * loading the library keeps until the process exits.
  *  - The first call on a device looks up that array's device address (with
@@ -277,8 +293,7 @@ KVSEL_API kvsel_status kvsel_block_priority(float* token_scores, const float* in
  *                 is written at slot seq_lens[b].  k_new, v_new, idx_k_new are
  *                 all given or all NULL.
  *   num_idx_heads 1..8;  idx_dim 64.
- *   top_k         >= 1; ceil(max_len / 16384) <= 63 and
- *                 ceil(max_len / 16384) * min(top_k, 16384) <= 32768.
+ *   top_k         >= 1;  max_len <= 2^28 (UNSUPPORTED beyond).
  *   out           [batch][num_q_heads][128], bf16 or fp32 (out_dtype).
  *   topk_out      int32 [batch][top_k] or NULL: sel_b, padded with -1.
  *   scores_out    fp32 [batch][max_len] or NULL: I (entries >= S_b untouched).
@@ -317,7 +332,7 @@ KVSEL_API kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int32
  *   keep_out      int32 [num_layers][num_kv_heads][keep_k + W]; when
  *                 S - W <= keep_k every position 0..S-1 is kept, -1 padded.
  *   vote_out      fp32 [num_layers][num_kv_heads][S - W] or NULL (raw votes).
- * Limits: G * W <= 256, S - W <= 32768.
+ * Limits: G * W <= 256, S < 2^28 (UNSUPPORTED beyond).
  */
 KVSEL_API size_t kvsel_snapkv_select_workspace(const kvsel_paged_kv* kv, int num_layers, int seq_len,
                                                int obs_window, int with_vote_out);

@@ -27,8 +27,9 @@ class DecodeState:
     """Device-side paged cache + bookkeeping for a DecodeWorkload."""
 
     def __init__(self, wl: workloads.DecodeWorkload, with_probs=True, with_pos=True,
-                 out_f32=True, spare_pages=0, dev="cuda"):
+                 out_f32=True, spare_pages=0, link=False, dev="cuda"):
         self.wl = wl
+        self.link = link
         self.dev = dev
         npages = wl.num_pages + spare_pages
         self.kpool = bf16(workloads.paged_pool(wl.K, wl.block_table, npages), dev)
@@ -73,7 +74,8 @@ class DecodeState:
                             k_new=bf16(wl.k_new[step], self.dev) if append else None,
                             v_new=bf16(wl.v_new[step], self.dev) if append else None,
                             pos_map=self.pos, next_pos=self.next_pos, probs=self.probs,
-                            h2o_cum=self.cum, max_len=wl.max_len, num_ctas=num_ctas)
+                            h2o_cum=self.cum, max_len=wl.max_len, num_ctas=num_ctas,
+                            h2o_link=self.ws_ev if self.link else None)
         if append:
             self.S += 1
 
@@ -88,6 +90,12 @@ class DecodeState:
             fr = self.freed.cpu().numpy()
             self.free.extend(int(x) for x in fr.ravel() if x >= 0)
             self.S = np.minimum(self.S, wl.budget)
+
+    def link_counts(self):
+        """Candidate counts the decode step left for the select (white-box view)."""
+        rows = self.wl.B * self.wl.Hkv
+        off = 256 + (rows * 4 + 255) // 256 * 256
+        return self.ws_ev[off:off + rows * 4].view(torch.int32).cpu().numpy().copy()
 
     def status(self):
         return K.read_status(self.ws), K.read_status(self.ws_ev)

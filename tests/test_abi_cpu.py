@@ -60,20 +60,24 @@ def test_workspace_sizes(lib):
     assert a > 0 and b - a >= 8 * 64 * 32896 * 4           # logits scratch when probs are not kept
     assert K.kvsel_decode_attn_workspace(kv, 8, 32896, True) < 8 << 20
     assert K.kvsel_h2o_evict_workspace(kv, 8, 6553) >= 8 * 8 * 6553 * 4
+    # the decode hand-off sits at the start of every evict workspace
+    assert K.kvsel_h2o_evict_workspace(kv, 8, 6553) >= K.lib().kvsel_h2o_link_bytes(8, 8) + 8 * 8 * 6553 * 4
+    assert K.lib().kvsel_h2o_link_bytes(8, 8) >= 64 * 16384 * 8
+    assert K.lib().kvsel_h2o_link_bytes(0, 8) == 0
     assert K.kvsel_decode_attn_workspace(_kv(num_q_heads=12), 1, 10, True) == 0
 
 
 def _decode_status(lib, kv, **over):
     args = dict(block_table=16, max_pages=4, seq_lens=16, batch=1, q=16, k_new=None, v_new=None,
                 pos_map=None, next_pos=None, scale=0.1, out=16, out_dtype=0, probs=None, cum=None,
-                max_len=64, num_ctas=0, ws=256, ws_bytes=1 << 30, stream=None)
+                max_len=64, num_ctas=0, ws=256, ws_bytes=1 << 30, link=None, link_bytes=0, stream=None)
     args.update(over)
     return lib.kvsel_decode_attn(ctypes.byref(kv), args["block_table"], args["max_pages"],
                                  args["seq_lens"], args["batch"], args["q"], args["k_new"],
                                  args["v_new"], args["pos_map"], args["next_pos"], args["scale"],
                                  args["out"], args["out_dtype"], args["probs"], args["cum"],
                                  args["max_len"], args["num_ctas"], args["ws"], args["ws_bytes"],
-                                 args["stream"])
+                                 args["link"], args["link_bytes"], args["stream"])
 
 
 def test_decode_host_validation(lib):
@@ -90,6 +94,10 @@ def test_decode_host_validation(lib):
     assert _decode_status(lib, _kv(), ws_bytes=100) == K.KVSEL_ERR_INVALID_ARG
     assert _decode_status(lib, _kv(), ws=None) == K.KVSEL_ERR_INVALID_ARG
     assert b"workspace" in lib.kvsel_last_error_string()
+    need = K.lib().kvsel_h2o_link_bytes(1, 8)
+    assert _decode_status(lib, _kv(), link=512, link_bytes=need - 1) == K.KVSEL_ERR_INVALID_ARG
+    assert _decode_status(lib, _kv(), link=512 + 16, link_bytes=need) == K.KVSEL_ERR_INVALID_ARG  # misaligned
+    assert b"h2o_link" in lib.kvsel_last_error_string()
 
 
 def test_evict_host_validation(lib):
@@ -148,7 +156,6 @@ def test_sparse_decode_host_validation(lib):
     assert st(Hi=9) == K.KVSEL_ERR_UNSUPPORTED
     assert st(kn=16) == K.KVSEL_ERR_INVALID_ARG          # k_new without v_new / idx_k_new
     assert st(top_k=0) == K.KVSEL_ERR_INVALID_ARG
-    assert st(max_len=64 * 16384) == K.KVSEL_ERR_UNSUPPORTED
-    assert st(top_k=4096, max_len=20 * 16384) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(max_len=(1 << 28) + 1) == K.KVSEL_ERR_UNSUPPORTED
     assert st(ws_bytes=100) == K.KVSEL_ERR_INVALID_ARG
     assert st(kv=_kv(num_q_heads=128)) == K.KVSEL_ERR_UNSUPPORTED

@@ -71,6 +71,44 @@ def test_select_bit_exact_continuous_scores_and_positions():
     np.testing.assert_array_equal(got, _expect(cum, S_list, 6553, 4, 1024, pos=pos))
 
 
+@pytest.mark.parametrize("max_len,S_list,budget", [
+    (70001, [70001, 40000, 33000], 6553),   # rows longer than the register-resident size, odd stride
+    (4999, [4999, 3001, 4000], 1000),       # row starts not 16-byte aligned
+    (60000, [60000, 45000, 30000], 20000),  # k above the shared-memory upper-set capacity
+])
+def test_select_long_unaligned_and_large_k(max_len, S_list, budget):
+    rng = np.random.default_rng(max_len)
+    cum = rng.random((len(S_list), 2, max_len), dtype=np.float32)
+    cum[1] = np.round(cum[1] * 64) / 64           # second kv head: many exact ties
+    got = _run_select(cum, S_list, budget, 4, 256, max_len)
+    np.testing.assert_array_equal(got, _expect(cum, S_list, budget, 4, 256))
+
+
+def test_select_reuses_previous_threshold_across_calls():
+    """Calls on one workspace start from the previous threshold: exact whether
+    the scores grew (bound too low), shrank (bound too high) or were shuffled."""
+    rng = np.random.default_rng(23)
+    B, Hkv, max_len, budget = 2, 4, 32896, 6553
+    S_list = [32896, 30000]
+    dev = "cuda"
+    kpool = torch.zeros(1, Hkv, 16, 128, dtype=torch.bfloat16, device=dev)
+    kv = K.paged_kv(kpool, kpool, Hkv)
+    bt = torch.zeros(B, max_len // 16 + 1, dtype=torch.int32, device=dev)
+    seq = torch.tensor(S_list, dtype=torch.int32, device=dev)
+    keep = torch.zeros((B, Hkv, budget), dtype=torch.int32, device=dev)
+    ws = K.workspace(K.kvsel_h2o_evict_workspace(kv, B, budget))
+    base = rng.random((B, Hkv, max_len), dtype=np.float32)
+    variants = [base, base + np.float32(0.001) * rng.random(base.shape, dtype=np.float32),
+                base * np.float32(0.25), base + np.float32(10.0), rng.permutation(base.ravel()).reshape(base.shape),
+                np.round(base * 16) / 16]
+    for cum_np in variants:
+        cum_np = cum_np.astype(np.float32)
+        K.kvsel_h2o_evict(kv, bt, seq, torch.from_numpy(cum_np).to(dev), ws, budget=budget, n_sink=4,
+                          window=1024, keep_out=keep)
+        assert K.read_status(ws) == 0
+        np.testing.assert_array_equal(keep.cpu().numpy(), _expect(cum_np, S_list, budget, 4, 1024))
+
+
 def test_streaming_and_sliding_window_special_cases():
     rng = np.random.default_rng(2)
     cum = rng.random((1, 2, 400), dtype=np.float32)
@@ -127,9 +165,9 @@ def test_compaction_moves_rows_exactly():
     assert st.seq.cpu().tolist() == [wl.budget] * wl.B
 
 
-def _run_mode_a(wl, steps):
+def _run_mode_a(wl, steps, link=False):
     """Evict-every-step loop on GPU and oracle with teacher forcing at near-ties."""
-    st = DecodeState(wl, spare_pages=8)
+    st = DecodeState(wl, spare_pages=8, link=link)
     refs = [H2OSequence(bf16_bits_to_f64(wl.K[b]), bf16_bits_to_f64(wl.V[b])) for b in range(wl.B)]
     swaps = 0
     for t in range(steps):
@@ -181,7 +219,37 @@ def test_small_config_evict_every_step_end_to_end():
     assert swaps <= 4
 
 
-def test_custom_config_evict_every_step_permuted_pages():
+@pytest.mark.parametrize("link", [False, True])
+def test_custom_config_evict_every_step_permuted_pages(link):
     wl = workloads.decode_custom(seed=77, B=3, Hq=64, Hkv=8, d=128, S0=500, steps=12, budget=200,
                                  n_sink=4, window=33, permute_pages=True)
-    _run_mode_a(wl, wl.steps)
+    _run_mode_a(wl, wl.steps, link=link)
+
+
+def test_decode_hands_candidates_to_select():
+    """With the hand-off, the select keeps exactly the top-k of the GPU's own
+    scores (compacting on every other step), and each list is used once."""
+    wl = workloads.decode_custom(seed=5, B=2, Hq=16, Hkv=4, d=128, S0=3000, steps=8, budget=1000,
+                                 n_sink=4, window=64, permute_pages=True)
+    st = DecodeState(wl, spare_pages=16, link=True)
+    used = 0
+    for t in range(wl.steps):
+        st.decode(t)
+        torch.cuda.synchronize()
+        S = st.seq.cpu().numpy()
+        cum = st.cum.cpu().numpy().copy()
+        pos = st.pos.cpu().numpy().copy()
+        counts = st.link_counts()
+        if t > 0:   # a threshold exists from the previous select
+            assert (counts >= wl.budget - wl.n_sink - wl.window).all() and (counts <= 16384).all(), counts
+            used += 1
+        st.evict(compact=(t % 2 == 0))
+        torch.cuda.synchronize()
+        assert st.status() == (0, 0)
+        assert (st.link_counts() == 0).all()
+        keep = st.keep.cpu().numpy()
+        for b in range(wl.B):
+            for h in range(wl.Hkv):
+                want = h2o_keep(cum[b, h].astype(np.float32), int(S[b]), wl.budget, wl.n_sink, wl.window)
+                np.testing.assert_array_equal(keep[b, h, :len(want)], pos[b, h, want])
+    assert used == wl.steps - 1

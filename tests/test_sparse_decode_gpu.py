@@ -123,6 +123,14 @@ def test_ties_resolve_to_lower_positions():
     _check(st, 0)
 
 
+def test_large_top_k_single_stage():
+    """top_k >= 16384: one CTA per row sweeps the whole row (rows longer than 32K stream)."""
+    wl = workloads.sparse_decode(seed=19, B=2, S0=50001, steps=1, Hq=16, Hkv=2, top_k=20000)
+    st = SparseState(wl)
+    st.step(0)
+    _check(st, 0)
+
+
 @pytest.mark.parametrize("G", [1, 4, 8])
 def test_group_sizes_and_bf16_output(G):
     wl = workloads.sparse_decode(seed=17 + G, B=2, S0=5000, steps=1, Hq=8 * G, Hkv=8, top_k=1000)
