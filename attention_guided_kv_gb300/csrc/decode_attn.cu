@@ -51,6 +51,10 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStageBytes = 8192;  // K (2 x 2 KB swizzled halves) + V (same)
 constexpr int kMaxG = 8;
 constexpr int kMaxCtas = 1024;
+// Consumer warp w takes pages i with i % kConsumerWarps == w, so with a ring
+// depth that is a multiple of the warp count a stage is always used by the
+// same warp and its parity wait cannot pass on a later lap's phase.
+static_assert(kStages % kConsumerWarps == 0, "ring depth must be a multiple of the consumer warps");
 constexpr int kMaxBatch = 1024;
 constexpr int kPartFloats = kMaxG * (kD + 2);  // one partial slot: m[8], l[8], O[8][128]
 constexpr int kMaxOwners = kMaxCtas;           // CTAs sharing one (sequence, kv head) pair
@@ -69,6 +73,8 @@ struct SmemLayout {
 };
 // Phase B stages a segment's H2O candidates in the (then idle) TMA ring.
 constexpr int kStageCands = kStages * kStageBytes / 8;  // (key u32, slot i32) pairs
+// ... and, before that, every owner's partial (m, l) per head.
+static_assert(size_t(2) * kMaxOwners * kMaxG * 4 <= size_t(kStages) * kStageBytes, "owner stats fit in the ring");
 constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 
 struct StepParams {
@@ -533,30 +539,42 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     }
     __syncthreads();
     const int nown = sOwn[kMaxOwners];
+    // every owner's (m, l) per head, fetched in parallel into the idle TMA ring
+    float* sM = reinterpret_cast<float*>(smem + SmemLayout::ring);  // [kMaxOwners][kMaxG]
+    float* sL = sM + kMaxOwners * kMaxG;
+    for (int i = tid; i < nown * G; i += kThreads) {
+      const int k = i / G, g = i - k * G;
+      const float* sl = P.part + size_t(sOwn[k] + pair) * kPartFloats;
+      sM[k * kMaxG + g] = __ldcg(sl + g);
+      sL[k * kMaxG + g] = __ldcg(sl + kMaxG + g);
+    }
+    __syncthreads();
     if (tid < G) {
       float M = -INFINITY;
-      for (int k = 0; k < nown; ++k) M = fmaxf(M, __ldcg(P.part + size_t(sOwn[k] + pair) * kPartFloats + tid));
+      for (int k = 0; k < nown; ++k) M = fmaxf(M, sM[k * kMaxG + tid]);
       float L = 0.f;
       for (int k = 0; k < nown; ++k) {
-        const float* sl = P.part + size_t(sOwn[k] + pair) * kPartFloats;
-        const float m = __ldcg(sl + tid);
-        if (m != -INFINITY) L += __ldcg(sl + kMaxG + tid) * exp2f(m - M);
+        const float m = sM[k * kMaxG + tid];
+        if (m != -INFINITY) L += sL[k * kMaxG + tid] * exp2f(m - M);
       }
       sStat[tid * 2] = M;
       sStat[tid * 2 + 1] = L > 0.f ? 1.f / L : 0.f;
     }
     __syncthreads();
-    if (c == cf) {
-      for (int idx = tid; idx < G * kD; idx += kThreads) {
+    {  // O = the rescaled sum of the partials: each owner merges its share of the G x 128 outputs
+      int kme = 0;
+      while (kme < nown - 1 && sOwn[kme] != c) ++kme;
+      const int E = G * kD;
+      const int e1 = (kme + 1) * E / nown;
+      for (int idx = kme * E / nown + tid; idx < e1; idx += kThreads) {
         const int gg = idx / kD, dd = idx % kD;
         const float M = sStat[gg * 2];
         float acc = 0.f;
 #pragma unroll 4
         for (int k = 0; k < nown; ++k) {
-          const float* sl = P.part + size_t(sOwn[k] + pair) * kPartFloats;
-          const float m = __ldcg(sl + gg);
-          const float v = __ldcg(sl + 2 * kMaxG + gg * kD + dd);
-          if (m != -INFINITY) acc += v * exp2f(m - M);
+          const float m = sM[k * kMaxG + gg];
+          if (m != -INFINITY)
+            acc += __ldcg(P.part + size_t(sOwn[k] + pair) * kPartFloats + 2 * kMaxG + gg * kD + dd) * exp2f(m - M);
         }
         const float v = acc * sStat[gg * 2 + 1];
         const size_t oi = (size_t(b) * P.Hq + kvh * G + gg) * kD + dd;
@@ -564,6 +582,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(v);
       }
     }
+    __syncthreads();  // the ring is reused for the H2O candidate stage below
     if (P.logits) {
       const int j0 = pg * kPage;
       const int j1 = min(S, int(pg + (seg_end - u)) * kPage);
