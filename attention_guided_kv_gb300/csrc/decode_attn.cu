@@ -26,12 +26,15 @@
 //     mantissa bits at no extra MMA cost;
 //   * at each segment end the 4 warps merge and write (m, l, O) for the
 //     segment to a partial slot.
-// Grid barrier (bounded spin; the launch is cooperative so all CTAs are
-// co-resident).
+// No grid barrier: after phase A a CTA announces each pair it worked on (a
+// per-pair counter); phase B of a pair waits (bounded spin; the launch is
+// cooperative, so all CTAs are co-resident) only until every owner of that
+// pair has announced.
 // Phase B, per CTA, for each of its segments: merge the pair's partials into
-// (M, L), write O once per pair, and turn the segment's stored logits (still
-// in L2) into probabilities exp2(s - M) / L, adding the group sum into the
-// H2O score.  CTA 0 publishes the new lengths.
+// (M, L) (every owner's (m, l) fetched at once), write the owner's share of
+// O, and turn the segment's stored logits (still in L2) into probabilities
+// exp2(s - M) / L, adding the group sum into the H2O score.  The last CTA to
+// finish publishes the new lengths.
 //
 // The CTA that owns the page of a sequence's appended slot writes k_new /
 // v_new into the pool (and the slot's original position) before its
@@ -96,7 +99,9 @@ struct StepParams {
   int32_t* link_pos;
   void* out;
   float* part;     // [slots][kPartFloats]
-  unsigned* bar;   // grid barrier words: [0] arrivals, [32] generation
+  unsigned* fin;   // CTAs finished (status area); the last one publishes the lengths
+  unsigned* pair_cnt;   // [B*Hkv] owners whose phase A is done
+  unsigned* pair_pass;  // [B*Hkv] owners past the wait (the last resets both)
   int* status;
   int B, max_pages, Hq, Hkv, G, num_pages, max_len, out_f32;
   int vec_logits;  // logit rows are 8-byte aligned: store pairs as float2
@@ -114,33 +119,20 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-// Grid-wide barrier for a cooperative launch.  The spin is bounded: on expiry
-// it records KVSEL_ERR_TIMEOUT and lets the CTA continue (results are then
-// unspecified, but nothing hangs).
-__device__ __forceinline__ void grid_barrier(unsigned* bar, int* status) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    volatile unsigned* gen = bar + 32;
-    const unsigned g = *gen;
-    __threadfence();
-    const unsigned arrived = atomicAdd(bar, 1u) + 1u;
-    if (arrived == gridDim.x) {
-      bar[0] = 0u;
-      __threadfence();
-      atomicAdd(bar + 32, 1u);
-    } else {
-      unsigned spins = 0;
-      while (*gen == g) {
-        __nanosleep(64);
-        if (++spins > (1u << 25)) {  // a few seconds
-          report(status, KVSEL_ERR_TIMEOUT);
-          break;
-        }
-      }
+// Bounded spin of one thread until *word == target.  On expiry it records
+// KVSEL_ERR_TIMEOUT and returns false (results are then unspecified, but
+// nothing hangs).
+__device__ __forceinline__ bool wait_word(const unsigned* word, unsigned target, int* status) {
+  unsigned spins = 0;
+  while (*reinterpret_cast<const volatile unsigned*>(word) != target) {
+    __nanosleep(64);
+    if (++spins > (1u << 25)) {  // a few seconds
+      report(status, KVSEL_ERR_TIMEOUT);
+      return false;
     }
-    __threadfence();
   }
-  __syncthreads();
+  __threadfence();
+  return true;
 }
 
 struct Locator {
@@ -260,8 +252,6 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   }
   const Locator loc{sS, sPref, P.B, Hkv};
   const long long u0 = U * c / NC, u1 = U * (c + 1) / NC;
-  if (P.link_count && c == 0)  // fresh candidate lists (phase B appends after the grid barrier)
-    for (int i = tid; i < P.B * Hkv; i += kThreads) P.link_count[i] = 0u;
 
   // ---- append the new tokens whose page falls in this CTA's range ----
   if (append && tid < 32) {
@@ -493,19 +483,28 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     }
   }
 
-  grid_barrier(P.bar, P.status);
+  // ---- announce: this CTA's partials (and logits) for its pairs are written ----
+  // No grid barrier: phase B of a pair waits only for that pair's owners.
+  __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) {
+    for (long long u = u0; u < u1;) {
+      int b, kvh, pg;
+      loc.locate(u, b, kvh, pg);
+      const int pair = b * Hkv + kvh;
+      // the first owner gives the pair a fresh H2O candidate list before anyone can append
+      if (P.link_count && pg == 0) P.link_count[pair] = 0u;
+      __threadfence();
+      atomicAdd(P.pair_cnt + pair, 1u);
+      u = min(u1, u + (loc.pages(b) - pg));
+    }
+  }
 
   // ================= phase B =================
   uint32_t* sLink = reinterpret_cast<uint32_t*>(smem + SmemLayout::link);  // staged count, list base
   uint32_t* stKey = reinterpret_cast<uint32_t*>(smem + SmemLayout::ring);  // the idle TMA ring
   int32_t* stPos = reinterpret_cast<int32_t*>(smem + SmemLayout::ring + kStageCands * 4);
   if (c == 0) {
-    if (tid == 0)
-      for (int b = 0; b < P.B; ++b) {
-        P.seq_lens[b] = sS[b];
-        if (append && P.next_pos) P.next_pos[b] += 1;
-      }
     for (int b = 0; b < P.B; ++b)  // sequences without keys: O = 0
       if (sS[b] == 0)
         for (int idx = tid; idx < P.Hq * kD; idx += kThreads) {
@@ -536,6 +535,12 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       }
       sOwn[kMaxOwners] = no;
       sLink[0] = 0u;
+      // every owner of the pair has announced: its partials are complete
+      if (wait_word(P.pair_cnt + pair, unsigned(no), P.status) &&
+          atomicAdd(P.pair_pass + pair, 1u) + 1u == unsigned(no)) {
+        P.pair_cnt[pair] = 0u;  // every owner is past the wait: reset for the next launch
+        P.pair_pass[pair] = 0u;
+      }
     }
     __syncthreads();
     const int nown = sOwn[kMaxOwners];
@@ -688,6 +693,19 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     __syncthreads();
     u = seg_end;
   }
+  // The last CTA to finish publishes the new lengths: every CTA has read the
+  // old ones by then.
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(P.fin, 1u) + 1u == unsigned(NC)) {
+      *P.fin = 0u;
+      for (int b = 0; b < P.B; ++b) {
+        P.seq_lens[b] = sS[b];
+        if (append && P.next_pos) P.next_pos[b] += 1;
+      }
+      __threadfence();
+    }
+  }
 }
 
 }  // namespace kvsel
@@ -701,13 +719,16 @@ using namespace kvsel_host;
 namespace {
 
 struct DecodeWs {
-  size_t part_off, logit_off, total;
+  size_t pair_off, part_off, logit_off, total;
 };
 
-// The grid-barrier words live in the workspace's status area (bytes 64..255).
+// The finish counter lives in the workspace's status area (byte 64); the
+// per-pair readiness counters follow it.
 DecodeWs decode_ws_layout(int batch, int Hkv, int Hq, int max_len, bool with_probs) {
   DecodeWs w;
   size_t off = kStatusBytes;
+  w.pair_off = off;
+  off = align_up(off + size_t(batch) * Hkv * 2 * sizeof(unsigned), 256);
   w.part_off = off;
   off = align_up(off + (size_t(kMaxCtas) + size_t(batch) * Hkv) * kPartFloats * sizeof(float), 256);
   w.logit_off = off;
@@ -823,7 +844,9 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   }
   P.out = out;
   P.part = reinterpret_cast<float*>(ws + L.part_off);
-  P.bar = reinterpret_cast<unsigned*>(ws + 64);
+  P.fin = reinterpret_cast<unsigned*>(ws + 64);
+  P.pair_cnt = reinterpret_cast<unsigned*>(ws + L.pair_off);
+  P.pair_pass = P.pair_cnt + size_t(batch) * Hkv;
   P.status = reinterpret_cast<int*>(ws);
   P.B = batch;
   P.max_pages = max_pages;
@@ -862,7 +885,7 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
 // decode step: an allocator-less runtime embedding this library, a plug-in
 // whose host owns every allocation, or code that must not touch the
 // allocator mid-step.  For them the scratch the decode kernel needs (status
-// and grid-barrier words, per-CTA partial results, and the logit buffer when
+// and readiness counters, per-CTA partial results, and the logit buffer when
 // no probability buffer is given) lives in the fixed array below, which every
 // GPU that loads this library holds until the process exits.
 // ---------------------------------------------------------------------------
@@ -910,9 +933,11 @@ extern "C" kvsel_status kvsel_decode_attn_noalloc(const kvsel_paged_kv* kv, cons
     }
     scratch = g_noalloc_ptr[dev];
   }
-  // The status word and the grid-barrier counters must start at zero; the
-  // array keeps whatever the previous call left there.
-  e = cudaMemsetAsync(scratch, 0, kStatusBytes, static_cast<cudaStream_t>(stream));
+  // The status word and the finish / per-pair readiness counters must start at
+  // zero; the array keeps whatever the previous call left there.
+  const size_t counters = decode_ws_layout(batch, kv->num_kv_heads, kv->num_q_heads, max_len,
+                                           probs != nullptr).part_off;
+  e = cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_decode_attn_noalloc (clear)");
   return kvsel_decode_attn(kv, block_table, max_pages, seq_lens, batch, q, k_new, v_new, pos_map,
                            next_pos, scale, out, out_dtype, probs, h2o_cum, max_len, num_ctas, scratch,

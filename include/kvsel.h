@@ -9,10 +9,10 @@
  *    otherwise.  The library allocates no device memory: scratch comes from
  *    a caller-provided workspace whose size the matching *_workspace()
  *    function returns.
- *  - The first 256 bytes of every workspace hold a device status word and
- *    grid-barrier counters.  They must be zero when a workspace is first
- *    used (allocate it zeroed); afterwards the library keeps them
- *    consistent.  Kernels that detect a problem on the device
+ *  - Every workspace starts with a device status word and the counters the
+ *    kernels synchronise on.  A workspace must be zero when first used
+ *    (allocate it zeroed); afterwards the library keeps it consistent.
+ *    After a KVSEL_ERR_TIMEOUT status, zero the whole workspace again.  Kernels that detect a problem on the device
  *    (a block-table entry outside the pool, a bounded wait that ran out)
  *    record a kvsel_status there and carry on without faulting;
  *    kvsel_read_status() returns it.
@@ -71,8 +71,8 @@ typedef struct kvsel_paged_kv {
 /* Human-readable reason for the last non-OK status returned on this thread. */
 KVSEL_API const char* kvsel_last_error_string(void);
 
-/* Zero the status word of `workspace` (async on `stream`); the barrier
- * counters are left alone. */
+/* Zero the status word of `workspace` (async on `stream`); the
+ * synchronisation counters are left alone. */
 KVSEL_API kvsel_status kvsel_clear_status(void* workspace, void* stream);
 
 /* Synchronise `stream`, return the device status recorded in `workspace`
@@ -169,12 +169,12 @@ KVSEL_API size_t kvsel_h2o_link_bytes(int batch, int num_kv_heads);
  *  - The first call on a device looks up that array's device address (with
  *    the device current); make that first call before any stream capture.
  *  - Calls that need more scratch than 8 MiB are rejected with
- *    KVSEL_ERR_INVALID_ARG: about (1024 + batch * num_kv_heads) * 4160 bytes,
- *    plus batch * num_q_heads * max_len * 4 bytes when h2o_cum is given
- *    without probs.
+ *    KVSEL_ERR_INVALID_ARG: about (1024 + batch * num_kv_heads) * 4160 bytes
+ *    + batch * num_kv_heads * 8 bytes, plus batch * num_q_heads * max_len * 4
+ *    bytes when h2o_cum is given without probs.
  *  - Every call uses the same array, so calls that overlap on the GPU (other
  *    streams, other threads) race and corrupt each other; serialise them.
- *    Each call clears the array's status and barrier words first.
+ *    Each call clears the array's status word and counters first.
  *  - Device-side problems (a block-table entry outside the pool) are not
  *    reported back: there is no workspace to read them from.
  * Nothing here calls cudaMalloc, cudaFree or any allocating library routine. */
