@@ -25,16 +25,13 @@
 //                      head) with row_topk, window appended.
 #include "common.cuh"
 #include "row_topk.cuh"
+#include "umma.cuh"
 
 namespace kvsel {
 
 constexpr int kSnD = 128;
 constexpr int kSnPage = 16;
-constexpr int kSnStages = 8;
-constexpr int kSnStageBytes = 4096;       // one K page: two 2 KB swizzled halves
-constexpr int kSnWarps = 8;               // consumer warps: 32 window rows each
-constexpr int kSnThreads = (kSnWarps + 1) * 32;
-constexpr int kSnMaxRows = kSnWarps * 32; // G * W <= 256
+constexpr int kSnMaxRows = 256;          // G * W <= 256
 constexpr int kSnMaxChunks = 64;
 constexpr int kSnSelGroups = 8;           // register-resident rows: prefix <= 32768
 constexpr int kSnPoolTile = 1024;
@@ -53,231 +50,307 @@ struct SnapParams {
   float scale_log2;
 };
 
-__device__ __forceinline__ uint32_t sn_tile_off(int key, int u) {
-  return (u >> 3) * 2048 + key * 128 + ((((u & 7) ^ (key & 7))) << 4);
+// ---------------------------------------------------------------------------
+// The contraction on the 5th-generation tensor cores.  One CTA per (chunk of
+// keys, layer x kv head); warp 0 streams the chunk's K pages by TMA into a
+// ring of 128-key tiles, warp 1 issues tcgen05.mma (one elected thread) into
+// a double-buffered TMEM accumulator, warps 2..5 read the accumulator back
+// (tcgen05.ld) and do the softmax work.
+//   pass 1 (row statistics): D[rows x keys] = Q K^T, rows on the M side in
+//           one or two 128-row tiles; each epilogue thread owns one row and
+//           keeps its online (max, sum) in the log2 domain;
+//   pass 2 (votes): D[keys x rows] = K Q^T, keys on the M side; each
+//           epilogue thread owns one key and sums its weights over the rows
+//           directly, so the vote needs no cross-thread reduction.
+// ---------------------------------------------------------------------------
+constexpr int kTcKeys = 128;                          // keys per MMA tile (8 pages)
+constexpr int kTcStages = 4;                          // K tiles in flight
+constexpr int kTcTileBytes = 2 * kTcKeys * 128;       // two 64-column slabs
+constexpr int kTcQRows = 256;
+constexpr int kTcQBytes = 2 * kTcQRows * 128;
+constexpr int kTcEpiWarps = 8;                        // two per TMEM lane quarter
+constexpr int kTcThreads = (2 + kTcEpiWarps) * 32;    // producer, MMA issuer, epilogue
+constexpr uint32_t kTcCols = 512;                     // TMEM columns: 2 accumulators x 256
+struct TcLayout {
+  static constexpr size_t q = 0;
+  static constexpr size_t ring = q + kTcQBytes;
+  static constexpr size_t bars = ring + size_t(kTcStages) * kTcTileBytes;  // full, empty, acc_full, acc_empty
+  static constexpr size_t tmem = bars + (2 * kTcStages + 4) * 8;
+  static constexpr size_t stat = tmem + 16;        // [kTcQRows] f32: pass 2 row offsets C = M - log2(1/L)
+  static constexpr size_t xch = stat + size_t(kTcQRows) * 4;  // [2][4][32] f32: half-warp exchange
+  static constexpr size_t total = xch + 2 * 4 * 32 * 4 * 2;
+};
+constexpr size_t kTcSmem = TcLayout::total + 1024;
+static_assert(kSnMaxRows <= kTcQRows, "window rows fit in the Q tile");
+
+// 2^x on the special-function unit (ex2.approx, relative error ~2^-22; -inf -> 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <int kPass>
-__global__ void __launch_bounds__(kSnThreads, 1)
-snap_qk_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSnStages * kSnStageBytes);
-  uint64_t* empty = full + kSnStages;
-  float* vacc = reinterpret_cast<float*>(empty + kSnStages);  // [stages][16]
-  int* vcnt = reinterpret_cast<int*>(vacc + kSnStages * 16);  // [stages]
-  float* sStat = reinterpret_cast<float*>(vcnt + kSnStages);  // [rows][2] merged (pass 2)
+  uint8_t* sQ = smem + TcLayout::q;
+  uint8_t* sK = smem + TcLayout::ring;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcLayout::bars);
+  uint64_t* empty = full + kTcStages;
+  uint64_t* acc_full = empty + kTcStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_word = reinterpret_cast<uint32_t*>(smem + TcLayout::tmem);
+  float* sStat = reinterpret_cast<float*>(smem + TcLayout::stat);
 
   const int chunk = blockIdx.x, pair = blockIdx.y;
   const int layer = pair / P.Hkv, kvh = pair % P.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Pfx = P.S - P.W;                      // prefix length
-  const int span = kPass == 1 ? P.S : Pfx;        // keys this pass needs
+  const int R = P.rows;
+  const int Pfx = P.S - P.W;
+  const int span = kPass == 1 ? P.S : Pfx;  // keys this pass needs
   const int npages = (span + kSnPage - 1) / kSnPage;
   const int pb = int((long long)chunk * npages / P.chunks);
   const int pe = int((long long)(chunk + 1) * npages / P.chunks);
-  const int n = pe - pb;
+  const int key0 = pb * kSnPage, key1 = min(span, pe * kSnPage);
+  const int ntiles = (pe - pb + 7) / 8;
 
-  if (tid == 0) {
-    for (int s = 0; s < kSnStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), kSnWarps);
+  // ---- Q rows of this (layer, kv head), 128-byte swizzled K-major; zero padding ----
+  {
+    const __nv_bfloat16* qbase = P.q_obs + ((size_t(layer) * P.Hq + kvh * P.G) * P.W) * kSnD;
+    for (int idx = tid; idx < kTcQRows * 16; idx += kTcThreads) {
+      const int r = idx >> 4, ch = idx & 15, slab = ch >> 3, c = ch & 7;
+      const uint4 v = r < R ? reinterpret_cast<const uint4*>(qbase + size_t(r) * kSnD)[ch] : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sQ + slab * (kTcQRows * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
-    mbar_fence_init();
   }
-  for (int i = tid; i < kSnStages * 16; i += kSnThreads) vacc[i] = 0.f;
-  if (tid < kSnStages) vcnt[tid] = 0;
   if (kPass == 2) {
     // merged row statistics: M = max over chunks, 1/L with L = sum l * 2^(m - M)
-    const float* st = P.stats + size_t(pair) * P.chunks * P.rows * 2;
-    for (int r = tid; r < P.rows; r += kSnThreads) {
+    const float* st = P.stats + size_t(pair) * P.chunks * R * 2;
+    for (int r = tid; r < R; r += kTcThreads) {
       float M = -INFINITY;
-      for (int c = 0; c < P.chunks; ++c) M = fmaxf(M, st[(size_t(c) * P.rows + r) * 2]);
+      for (int c = 0; c < P.chunks; ++c) M = fmaxf(M, st[(size_t(c) * R + r) * 2]);
       float Lr = 0.f;
       if (M != -INFINITY)
         for (int c = 0; c < P.chunks; ++c) {
-          const float m = st[(size_t(c) * P.rows + r) * 2];
-          if (m != -INFINITY) Lr += st[(size_t(c) * P.rows + r) * 2 + 1] * exp2f(m - M);
+          const float m = st[(size_t(c) * R + r) * 2];
+          if (m != -INFINITY) Lr += st[(size_t(c) * R + r) * 2 + 1] * exp2f(m - M);
         }
-      sStat[r * 2] = M;
-      sStat[r * 2 + 1] = Lr > 0.f ? 1.f / Lr : 0.f;
+      // weight = 2^(s - M) / L = 2^(s - C) with C = M + log2(L); rows without keys weigh 0
+      sStat[r] = (M != -INFINITY && Lr > 0.f) ? M + __log2f(Lr) : INFINITY;
     }
+    for (int r = R + tid; r < kTcQRows; r += kTcThreads) sStat[r] = INFINITY;  // padding rows weigh 0
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), kTcEpiWarps * 32);
+    }
+    mbar_fence_init();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q stores -> tensor-core reads
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_word), kTcCols);
+    tmem_relinquish();
+    tc_fence_before();
   }
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_word;
 
-  if (warp == kSnWarps) {
-    // producer: one K page of this (layer, kv head) per stage
-    if (lane == 0 && n > 0) {
+  if (warp == 0) {
+    // ---- producer: up to 8 pages per tile, two 64-column boxes per page ----
+    if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       const int32_t* bt = P.block_table + size_t(layer) * P.max_pages;
 #pragma unroll 1
-      for (int i = 0; i < n; ++i) {
-        const int s = i % kSnStages;
-        if (i >= kSnStages && !mbar_wait(smem_u32(&empty[s]), ((i / kSnStages) + 1) & 1, P.status)) break;
-        int phys = bt[pb + i];
-        if (unsigned(phys) >= unsigned(P.num_pages)) {
-          report(P.status, KVSEL_ERR_BAD_INDEX);
-          phys = 0;
-        }
-        const int y = (phys * P.Hkv + kvh) * kSnPage;
-        const uint32_t dst = smem_u32(smem + s * kSnStageBytes);
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kTcStages;
+        if (t >= kTcStages && !mbar_wait(smem_u32(&empty[s]), ((t / kTcStages) + 1) & 1, P.status)) break;
+        const int p0 = pb + 8 * t, np = min(8, pe - p0);
+        const uint32_t dst = smem_u32(sK + s * kTcTileBytes);
         const uint32_t bar = smem_u32(&full[s]);
-        mbar_expect_tx(bar, kSnStageBytes);
-        tma_load_2d(dst, &tmK, 0, y, bar, pol);
-        tma_load_2d(dst + 2048, &tmK, 64, y, bar, pol);
+        mbar_expect_tx(bar, uint32_t(np) * 4096u);
+        for (int i = 0; i < np; ++i) {
+          int phys = bt[p0 + i];
+          if (unsigned(phys) >= unsigned(P.num_pages)) {
+            report(P.status, KVSEL_ERR_BAD_INDEX);
+            phys = 0;
+          }
+          const int y = (phys * P.Hkv + kvh) * kSnPage;
+          tma_load_2d(dst + i * 2048, &tmK, 0, y, bar, pol);
+          tma_load_2d(dst + kTcKeys * 128 + i * 2048, &tmK, 64, y, bar, pol);
+        }
       }
     }
-    return;
-  }
-
-  // ---- consumers: warp w owns rows [32w, 32w + 32) as two m16 tiles ----
-  const int g = lane >> 2, qd = lane & 3, mi = lane >> 3, r8 = lane & 7;
-  const bool active = warp * 32 < P.rows;
-  int rowid[4];                  // rows of this lane: [mt][g or g+8]
-  bool rowok[4];
-  int limit[4];                  // last visible key of the row (causal)
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    rowid[k] = warp * 32 + (k >> 1) * 16 + g + (k & 1) * 8;
-    rowok[k] = rowid[k] < P.rows;
-    limit[k] = Pfx + (rowid[k] % P.W);
-  }
-  uint32_t qa[2][8][4];
-  {
-    const __nv_bfloat16* qbase = P.q_obs + ((size_t(layer) * P.Hq + kvh * P.G) * P.W) * kSnD;
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const uint32_t* r0 = reinterpret_cast<const uint32_t*>(qbase + size_t(rowok[2 * mt] ? rowid[2 * mt] : 0) * kSnD);
-      const uint32_t* r1 = reinterpret_cast<const uint32_t*>(qbase + size_t(rowok[2 * mt + 1] ? rowid[2 * mt + 1] : 0) * kSnD);
-#pragma unroll
-      for (int kt = 0; kt < 8; ++kt) {
-        qa[mt][kt][0] = rowok[2 * mt] ? r0[(16 * kt + 2 * qd) >> 1] : 0u;
-        qa[mt][kt][1] = rowok[2 * mt + 1] ? r1[(16 * kt + 2 * qd) >> 1] : 0u;
-        qa[mt][kt][2] = rowok[2 * mt] ? r0[(16 * kt + 8 + 2 * qd) >> 1] : 0u;
-        qa[mt][kt][3] = rowok[2 * mt + 1] ? r1[(16 * kt + 8 + 2 * qd) >> 1] : 0u;
-      }
-    }
-  }
-  float m_run[4], l_run[4], Mr[4], Ir[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    m_run[k] = -INFINITY;
-    l_run[k] = 0.f;
-    Mr[k] = kPass == 2 && rowok[k] ? sStat[rowid[k] * 2] : 0.f;
-    Ir[k] = kPass == 2 && rowok[k] ? sStat[rowid[k] * 2 + 1] : 0.f;
-  }
-  float* vrow = P.vote + size_t(pair) * Pfx;
-
+  } else if (warp == 1) {
+    // ---- MMA issuer ----
+    if (lane == 0) {
+      const int nMt = (R + 127) / 128;
+      const int Npad = (R + 31) & ~31;  // zero-padded rows up to whole 32-column loads
+      const uint32_t idesc = kPass == 1 ? umma_idesc_bf16_f32(128, kTcKeys) : umma_idesc_bf16_f32(128, Npad);
 #pragma unroll 1
-  for (int i = 0; i < n; ++i) {
-    const int s = i % kSnStages;
-    if (!mbar_wait(smem_u32(&full[s]), (i / kSnStages) & 1, P.status)) break;
-    const int key0 = (pb + i) * kSnPage;
-    if (active) {
-      const uint32_t kb = smem_u32(smem + s * kSnStageBytes);
-      float acc[2][2][4];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
-#pragma unroll
-      for (int kt = 0; kt < 8; ++kt) {
-        const int key = (mi >> 1) * 8 + r8;
-        const int uu = 2 * kt + (mi & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + sn_tile_off(key, uu), b0, b1, b2, b3);
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          mma_bf16_16816(acc[mt][0], qa[mt][kt][0], qa[mt][kt][1], qa[mt][kt][2], qa[mt][kt][3], b0, b1);
-          mma_bf16_16816(acc[mt][1], qa[mt][kt][0], qa[mt][kt][1], qa[mt][kt][2], qa[mt][kt][3], b2, b3);
-        }
-      }
-      // acc[mt][nt][e]: row (mt, e >> 1), key key0 + 8 nt + 2 qd + (e & 1)
-      if (kPass == 1) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int mt = k >> 1, hr = k & 1;
-          float x[4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int key = key0 + 8 * nt + 2 * qd + e;
-              const bool vis = rowok[k] && key < P.S && key <= limit[k];
-              x[nt * 2 + e] = vis ? acc[mt][nt][hr * 2 + e] * P.scale_log2 : -INFINITY;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kTcStages, buf = t & 1;
+        if (!mbar_wait(smem_u32(&full[s]), (t / kTcStages) & 1, P.status)) break;
+        if (t >= 2 && !mbar_wait(smem_u32(&acc_empty[buf]), ((t >> 1) + 1) & 1, P.status)) break;
+        tc_fence_after();
+        const uint32_t kt = smem_u32(sK + s * kTcTileBytes);
+        const uint32_t qt = smem_u32(sQ);
+        if (kPass == 1) {
+          for (int mt = 0; mt < nMt; ++mt)
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t koff = uint32_t(k >> 2) * (kTcKeys * 128) + uint32_t(k & 3) * 32;
+              const uint32_t qoff = uint32_t(k >> 2) * (kTcQRows * 128) + uint32_t(mt) * (128 * 128) + uint32_t(k & 3) * 32;
+              umma_bf16(tbase + uint32_t(buf) * 256 + uint32_t(mt) * 128, umma_desc_sw128(qt + qoff),
+                        umma_desc_sw128(kt + koff), idesc, k > 0);
             }
-          float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float m_new = fmaxf(m_run[k], mx);
-          if (m_new != -INFINITY) {
-            l_run[k] = l_run[k] * exp2f(m_run[k] - m_new) + (exp2f(x[0] - m_new) + exp2f(x[1] - m_new)) +
-                       (exp2f(x[2] - m_new) + exp2f(x[3] - m_new));
-            m_run[k] = m_new;
+        } else {
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = uint32_t(k >> 2) * (kTcKeys * 128) + uint32_t(k & 3) * 32;
+            const uint32_t qoff = uint32_t(k >> 2) * (kTcQRows * 128) + uint32_t(k & 3) * 32;
+            umma_bf16(tbase + uint32_t(buf) * 256, umma_desc_sw128(kt + koff), umma_desc_sw128(qt + qoff), idesc,
+                      k > 0);
           }
         }
-      } else {
-        // weights of prefix keys, summed over this lane's 4 rows, then over the warp's rows
-        float v[4];  // keys: nt * 2 + e
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float sum = 0.f;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (rowok[k]) sum += exp2f(acc[k >> 1][nt][(k & 1) * 2 + e] * P.scale_log2 - Mr[k]) * Ir[k];
-            v[nt * 2 + e] = sum;
-          }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          v[j] += __shfl_xor_sync(0xffffffffu, v[j], 4);
-          v[j] += __shfl_xor_sync(0xffffffffu, v[j], 8);
-          v[j] += __shfl_xor_sync(0xffffffffu, v[j], 16);
-        }
-        if (g == 0) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) atomicAdd(&vacc[s * 16 + 8 * (j >> 1) + 2 * qd + (j & 1)], v[j]);
-        }
-      }
-    }
-    if (kPass == 2) {
-      // the last warp to finish this page publishes its 16 votes and resets the slot
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) {
-        __threadfence_block();
-        last = atomicAdd(&vcnt[s], 1) == kSnWarps - 1;
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence_block();
-        if (lane < 16) {
-          const int key = key0 + lane;
-          const float val = atomicExch(&vacc[s * 16 + lane], 0.f);
-          if (key < Pfx) vrow[key] = val;
-        }
-        if (lane == 0) vcnt[s] = 0;
-        __threadfence_block();
+        umma_commit(smem_u32(&empty[s]));     // the K tile may be overwritten once these MMAs are done
+        umma_commit(smem_u32(&acc_full[buf]));
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-  }
-
-  if (kPass == 1 && active) {
-    float* st = P.stats + (size_t(pair) * P.chunks + chunk) * P.rows * 2;
+  } else {
+    // ---- epilogue: warps w and w + 4 share TMEM lane quarter w & 3; half h of
+    // the columns each (pass 1: keys of a tile, pass 2: window rows) ----
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int tl = quarter * 32 + lane;
+    const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
+    const int nMt = (R + 127) / 128;
+    float* xch = reinterpret_cast<float*>(smem + TcLayout::xch);  // [2 tile parities][4 quarters][32]
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    int limit[2];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float l = l_run[k];
-      l += __shfl_xor_sync(0xffffffffu, l, 1);
-      l += __shfl_xor_sync(0xffffffffu, l, 2);
-      if (qd == 0 && rowok[k]) {
-        st[rowid[k] * 2] = m_run[k];
-        st[rowid[k] * 2 + 1] = l;
+    for (int mt = 0; mt < 2; ++mt) limit[mt] = Pfx + ((mt * 128 + tl) % P.W);
+    float* vrow = P.vote + size_t(pair) * Pfx;
+    const float sc = P.scale_log2;
+    bool dead = false;  // a wait ran out: keep the trip count (named barriers), skip the waits
+#pragma unroll 1
+    for (int t = 0; t < ntiles; ++t) {
+      const int buf = t & 1;
+      if (!dead) dead = !mbar_wait(smem_u32(&acc_full[buf]), (t >> 1) & 1, P.status);
+      tc_fence_after();
+      const int kt0 = (pb + 8 * t) * kSnPage;
+      const uint32_t acc = tbase + lane_addr + uint32_t(buf) * 256;
+      if (kPass == 1) {
+        // a tile wholly inside [key0, key1) and the prefix needs no mask
+        const bool plain = kt0 >= key0 && kt0 + kTcKeys <= key1 && kt0 + kTcKeys <= Pfx;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          if (mt >= nMt) break;
+#pragma unroll 1
+          for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
+            float v[32];
+            tmem_ld32(acc + uint32_t(mt) * 128 + uint32_t(c0), v);
+            float mx = -INFINITY;
+            if (plain) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                v[i] *= sc;
+                mx = fmaxf(mx, v[i]);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int key = kt0 + c0 + i;
+                v[i] = (key >= key0 && key < key1 && key <= limit[mt]) ? v[i] * sc : -INFINITY;
+                mx = fmaxf(mx, v[i]);
+              }
+            }
+            const float m_new = fmaxf(m_run[mt], mx);
+            if (m_new != -INFINITY) {
+              float sum = 0.f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) sum += fast_exp2(v[i] - m_new);
+              l_run[mt] = l_run[mt] * fast_exp2(m_run[mt] - m_new) + sum;
+              m_run[mt] = m_new;
+            }
+          }
+        }
+      } else {
+        const int nchunks = ((R + 31) & ~31) / 32;
+        const int cbeg = half == 0 ? 0 : (nchunks + 1) / 2, cend = half == 0 ? (nchunks + 1) / 2 : nchunks;
+        float vote = 0.f;
+#pragma unroll 1
+        for (int ci = cbeg; ci < cend; ++ci) {
+          const int c0 = ci * 32;
+          float v[32];
+          tmem_ld32(acc + uint32_t(c0), v);
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 C = *reinterpret_cast<const float4*>(sStat + c0 + i);  // +inf past the rows
+            vote += fast_exp2(fmaf(v[i], sc, -C.x)) + fast_exp2(fmaf(v[i + 1], sc, -C.y)) +
+                    fast_exp2(fmaf(v[i + 2], sc, -C.z)) + fast_exp2(fmaf(v[i + 3], sc, -C.w));
+          }
+        }
+        float* xb = xch + (buf * 4 + quarter) * 32;
+        if (half == 1) xb[lane] = vote;
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+        if (half == 0) {
+          const int key = kt0 + tl;
+          if (key >= key0 && key < key1) vrow[key] = vote + xb[lane];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&acc_empty[buf]));
+    }
+    if (kPass == 1) {
+      // merge the two halves' (m, l) per row, then write this chunk's statistics
+      float* xb = xch;  // [4 quarters][32] m, then [4][32] l
+      if (half == 1) {
+        xb[quarter * 32 + lane] = m_run[0];
+        xb[128 + quarter * 32 + lane] = l_run[0];
+      }
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+      if (half == 0) {
+        const float m2 = xb[quarter * 32 + lane], l2 = xb[128 + quarter * 32 + lane];
+        const float M = fmaxf(m_run[0], m2);
+        if (M != -INFINITY) {
+          l_run[0] = l_run[0] * fast_exp2(m_run[0] - M) + l2 * fast_exp2(m2 - M);
+          m_run[0] = M;
+        }
+      }
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+      if (half == 1) {
+        xb[quarter * 32 + lane] = m_run[1];
+        xb[128 + quarter * 32 + lane] = l_run[1];
+      }
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+      if (half == 0) {
+        const float m2 = xb[quarter * 32 + lane], l2 = xb[128 + quarter * 32 + lane];
+        const float M = fmaxf(m_run[1], m2);
+        if (M != -INFINITY) {
+          l_run[1] = l_run[1] * fast_exp2(m_run[1] - M) + l2 * fast_exp2(m2 - M);
+          m_run[1] = M;
+        }
+        float* st = P.stats + (size_t(pair) * P.chunks + chunk) * R * 2;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+          if (mt < nMt && mt * 128 + tl < R) {
+            st[(mt * 128 + tl) * 2] = m_run[mt];
+            st[(mt * 128 + tl) * 2 + 1] = l_run[mt];
+          }
       }
     }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTcCols);
   }
 }
 
@@ -326,8 +399,6 @@ using namespace kvsel;
 using namespace kvsel_host;
 
 namespace {
-constexpr size_t kSnSmem = size_t(kSnStages) * kSnStageBytes + 1024 + 2 * kSnStages * 8 +
-                           kSnStages * 16 * 4 + kSnStages * 4 + kSnMaxRows * 2 * 4;
 struct SnWs {
   size_t stats, vote, pool, total;
   int pool_stride;
@@ -345,12 +416,21 @@ SnWs sn_ws_layout(int L, int Hkv, int rows, int S, int W, int chunks, bool own_v
   w.total = off;
   return w;
 }
+// Key chunks per (layer, kv head): one CTA per SM, so pick the count that
+// minimises waves x 128-key tiles per CTA (fewer chunks on ties).
 int sn_chunks(int L, int Hkv, int S) {
-  const int pages = (S + kSnPage - 1) / kSnPage;
-  const int slots = sm_count();
-  int c = std::max(1, (3 * slots + L * Hkv - 1) / (L * Hkv));
-  c = std::min(c, std::max(1, pages / 16));
-  return std::min(c, kSnMaxChunks);
+  const int tiles = ((S + kSnPage - 1) / kSnPage + 7) / 8;
+  const long long pairs = (long long)L * Hkv, sms = sm_count();
+  int best = 1;
+  long long best_cost = -1;
+  for (int c = 1; c <= std::min(kSnMaxChunks, tiles); ++c) {
+    const long long cost = ((pairs * c + sms - 1) / sms) * ((tiles + c - 1) / c);
+    if (best_cost < 0 || cost < best_cost) {
+      best = c;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 }  // namespace
 
@@ -428,8 +508,8 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   {
-    cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(snap_qk_kernel<1>), int(kSnSmem));
-    if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(snap_qk_kernel<2>), int(kSnSmem));
+    cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(snap_tc_kernel<1>), int(kTcSmem));
+    if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(snap_tc_kernel<2>), int(kTcSmem));
     if (e0 == cudaSuccess)
       e0 = smem_limit_once(reinterpret_cast<const void*>(snap_select_kernel), int(sizeof(RowTopkSmem)));
     if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_snapkv_select (attribute)");
@@ -437,13 +517,13 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
   const dim3 grid(chunks, num_layers * Hkv);
   cudaError_t e;
   trace_before("snap_stats", st);
-  snap_qk_kernel<1><<<grid, kSnThreads, kSnSmem, st>>>(tmK, P);
+  snap_tc_kernel<1><<<grid, kTcThreads, kTcSmem, st>>>(tmK, P);
   e = cudaGetLastError();
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (stats launch)");
   if (seq_len > obs_window) {
     trace_before("snap_vote", st);
-    snap_qk_kernel<2><<<grid, kSnThreads, kSnSmem, st>>>(tmK, P);
+    snap_tc_kernel<2><<<grid, kTcThreads, kTcSmem, st>>>(tmK, P);
     e = cudaGetLastError();
     trace_after(st);
     if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (vote launch)");
