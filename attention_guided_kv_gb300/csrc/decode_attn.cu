@@ -603,7 +603,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       }
       if (P.vec4) {
         // 4 keys x all heads per thread, two such groups per iteration: up to 16
-        // independent 16-byte loads in flight per thread
+        // independent 16-byte loads in flight per thread (a third group would
+        // not fit the 168 registers that two CTAs per SM leave each thread)
         auto group = [&](int j, float4 (&lg)[kMaxG]) {
 #pragma unroll
           for (int gg = 0; gg < kMaxG; ++gg)

@@ -94,27 +94,45 @@ __device__ __forceinline__ bool select_from_list(const SelectParams& P, size_t r
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
   uint32_t mx = 0, mn = 0xFFFFFFFFu, bad = 0;
   const uint32_t cnt_r = (cnt + 31u) & ~31u;
-  for (uint32_t i = tid; i < cnt_r; i += kSelThreads) {
-    bool v = false;
-    uint32_t key = 0;
-    int pos = 0;
-    if (i < cnt) {
-      key = __ldcg(lk + i);
-      pos = __ldcg(lp + i);
-      if (pos < 0 || pos >= P.max_len) bad = 1;
-      else if (i < uint32_t(kSelThreads)) bad |= order_key(__ldcg(row + pos)) != key;  // stale list?
-      v = pos >= lo && pos < hi;
+  // four entries per thread in flight per batch (the loads of a batch overlap)
+#pragma unroll 1
+  for (uint32_t i0 = 0; i0 < cnt_r; i0 += 4 * kSelThreads) {
+    uint32_t key[4];
+    int pos[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t i = i0 + j * kSelThreads + tid;
+      key[j] = 0u;
+      pos[j] = -1;
+      if (i < cnt) {
+        key[j] = __ldcg(lk + i);
+        pos[j] = __ldcg(lp + i);
+      }
     }
-    const uint32_t bal = __ballot_sync(0xffffffffu, v);
-    if (bal) {
-      uint32_t base = 0;
-      if (lane == 0) base = atomicAdd(&sm.m, uint32_t(__popc(bal)));
-      base = __shfl_sync(0xffffffffu, base, 0) + __popc(bal & lt);
-      if (v) {
-        sm.rk.ukey[base] = key;
-        sm.upos[base] = pos - lo;
-        mx = max(mx, key);
-        mn = min(mn, key);
+    if (i0 == 0 && tid < cnt) {  // freshness: the listed score must still be the row's score
+      if (pos[0] < 0 || pos[0] >= P.max_len) bad = 1;
+      else bad |= order_key(__ldcg(row + pos[0])) != key[0];
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t i = i0 + j * kSelThreads + tid;
+      if (i0 + j * kSelThreads + uint32_t(tid & ~31) >= cnt_r) break;  // uniform over the warp
+      bool v = false;
+      if (i < cnt) {
+        if (pos[j] < 0 || pos[j] >= P.max_len) bad = 1;
+        v = pos[j] >= lo && pos[j] < hi;
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, v);
+      if (bal) {
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&sm.m, uint32_t(__popc(bal)));
+        base = __shfl_sync(0xffffffffu, base, 0) + __popc(bal & lt);
+        if (v) {
+          sm.rk.ukey[base] = key[j];
+          sm.upos[base] = pos[j] - lo;
+          mx = max(mx, key[j]);
+          mn = min(mn, key[j]);
+        }
       }
     }
   }
