@@ -42,6 +42,10 @@ PAGE = 16
 
 
 
+# DRAM bytes (read + write) of one decode_step launch at batch 8 x 32K, from one ncu full-set
+# capture of this kernel (summarised under profiles/); set to None whenever the kernel changes.
+DECODE_STEP_TRAFFIC = 1.084455e9 + 76.023040e6
+
 TRACE_EVERY = 8   # launch tracing on one timed step in eight: events between kernels cost time
 
 
@@ -388,7 +392,8 @@ def cuda_arm(args, rank, world):
         "kernel_ms": {"decode_step": dec_ms, "h2o_select": sum(sel) / max(1, len(sel))},
         "roofline": {"bound": "hbm", "kernel": "decode_step", "achieved": achieved, "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None},
+                     "traffic": DECODE_STEP_TRAFFIC if B == 8 else None,
+                     "algorithmic_bytes": dec_bytes},
         "e2e": {"value": world * e2e_steps / (e2e_ms / 1e3), "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
