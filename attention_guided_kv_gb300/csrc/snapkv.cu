@@ -68,7 +68,8 @@ constexpr int kTcStages = 4;                          // K tiles in flight
 constexpr int kTcTileBytes = 2 * kTcKeys * 128;       // two 64-column slabs
 constexpr int kTcQRows = 256;
 constexpr int kTcQBytes = 2 * kTcQRows * 128;
-constexpr int kTcEpiWarps = 8;                        // two per TMEM lane quarter
+constexpr int kTcEpiPerQ = 4;                         // epilogue warps per TMEM lane quarter
+constexpr int kTcEpiWarps = 4 * kTcEpiPerQ;
 constexpr int kTcThreads = (2 + kTcEpiWarps) * 32;    // producer, MMA issuer, epilogue
 constexpr uint32_t kTcCols = 512;                     // TMEM columns: 2 accumulators x 256
 struct TcLayout {
@@ -77,8 +78,8 @@ struct TcLayout {
   static constexpr size_t bars = ring + size_t(kTcStages) * kTcTileBytes;  // full, empty, acc_full, acc_empty
   static constexpr size_t tmem = bars + (2 * kTcStages + 4) * 8;
   static constexpr size_t stat = tmem + 16;        // [kTcQRows] f32: pass 2 row offsets C = M - log2(1/L)
-  static constexpr size_t xch = stat + size_t(kTcQRows) * 4;  // [2][4][32] f32: half-warp exchange
-  static constexpr size_t total = xch + 2 * 4 * 32 * 4 * 2;
+  static constexpr size_t xch = stat + size_t(kTcQRows) * 4;  // partial exchange between a quarter's warps
+  static constexpr size_t total = xch + size_t(2) * 2 * kTcEpiPerQ * 4 * 32 * 4;
 };
 constexpr size_t kTcSmem = TcLayout::total + 1024;
 static_assert(kSnMaxRows <= kTcQRows, "window rows fit in the Q tile");
@@ -88,6 +89,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 template <int kPass>
@@ -165,29 +171,50 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
   const uint32_t tbase = *tmem_word;
 
   if (warp == 0) {
-    // ---- producer: up to 8 pages per tile, two 64-column boxes per page ----
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      const int32_t* bt = P.block_table + size_t(layer) * P.max_pages;
+    // ---- producer: up to 8 pages per tile, two 64-column boxes per page.  The
+    // lanes resolve block-table entries 32 pages (4 tiles) at a time, one group
+    // ahead, so no dependent table load sits between two tiles' TMA issues ----
+    const uint64_t pol = l2_policy_evict_first();
+    const int32_t* bt = P.block_table + size_t(layer) * P.max_pages;
+    const int n = pe - pb;
+    auto resolve = [&](int i) -> int {  // TMA row of chunk-local page i (0 past the end)
+      if (i >= n) return 0;
+      int phys = bt[pb + i];
+      if (unsigned(phys) >= unsigned(P.num_pages)) {
+        report(P.status, KVSEL_ERR_BAD_INDEX);
+        phys = 0;
+      }
+      return (phys * P.Hkv + kvh) * kSnPage;
+    };
+    int y_cur = resolve(lane), y_next = resolve(32 + lane);
+    bool stop = false;
 #pragma unroll 1
-      for (int t = 0; t < ntiles; ++t) {
-        const int s = t % kTcStages;
-        if (t >= kTcStages && !mbar_wait(smem_u32(&empty[s]), ((t / kTcStages) + 1) & 1, P.status)) break;
-        const int p0 = pb + 8 * t, np = min(8, pe - p0);
+    for (int t = 0; t < ntiles && !stop; ++t) {
+      const int pl = 8 * t;  // chunk-local first page of the tile
+      if (t > 0 && (pl & 31) == 0) {
+        y_cur = y_next;
+        y_next = resolve(pl + 32 + lane);
+      }
+      int ys[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ys[i] = __shfl_sync(0xffffffffu, y_cur, (pl & 31) + i);
+      const int s = t % kTcStages;
+      bool ok = true;
+      if (lane == 0 && t >= kTcStages) ok = mbar_wait(smem_u32(&empty[s]), ((t / kTcStages) + 1) & 1, P.status);
+      stop = !__shfl_sync(0xffffffffu, ok, 0);
+      if (!stop && lane == 0) {
+        const int np = min(8, n - pl);
         const uint32_t dst = smem_u32(sK + s * kTcTileBytes);
         const uint32_t bar = smem_u32(&full[s]);
         mbar_expect_tx(bar, uint32_t(np) * 4096u);
-        for (int i = 0; i < np; ++i) {
-          int phys = bt[p0 + i];
-          if (unsigned(phys) >= unsigned(P.num_pages)) {
-            report(P.status, KVSEL_ERR_BAD_INDEX);
-            phys = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < np) {
+            tma_load_2d(dst + i * 2048, &tmK, 0, ys[i], bar, pol);
+            tma_load_2d(dst + kTcKeys * 128 + i * 2048, &tmK, 64, ys[i], bar, pol);
           }
-          const int y = (phys * P.Hkv + kvh) * kSnPage;
-          tma_load_2d(dst + i * 2048, &tmK, 0, y, bar, pol);
-          tma_load_2d(dst + kTcKeys * 128 + i * 2048, &tmK, 64, y, bar, pol);
-        }
       }
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ---- MMA issuer ----
@@ -225,13 +252,14 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
     }
     __syncwarp();
   } else {
-    // ---- epilogue: warps w and w + 4 share TMEM lane quarter w & 3; half h of
-    // the columns each (pass 1: keys of a tile, pass 2: window rows) ----
-    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    // ---- epilogue: kTcEpiPerQ warps share TMEM lane quarter w & 3, each a
+    // part of the columns (pass 1: keys of a tile, pass 2: window rows) ----
+    const int quarter = warp & 3, part = (warp - 2) >> 2;
     const int tl = quarter * 32 + lane;
     const uint32_t lane_addr = uint32_t(quarter * 32) << 16;
     const int nMt = (R + 127) / 128;
-    float* xch = reinterpret_cast<float*>(smem + TcLayout::xch);  // [2 tile parities][4 quarters][32]
+    float* xch = reinterpret_cast<float*>(smem + TcLayout::xch);
+    auto qsync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + quarter), "n"(32 * kTcEpiPerQ) : "memory"); };
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     int limit[2];
 #pragma unroll
@@ -249,33 +277,32 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
       if (kPass == 1) {
         // a tile wholly inside [key0, key1) and the prefix needs no mask
         const bool plain = kt0 >= key0 && kt0 + kTcKeys <= key1 && kt0 + kTcKeys <= Pfx;
+        constexpr int kCols = kTcKeys / kTcEpiPerQ;
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           if (mt >= nMt) break;
 #pragma unroll 1
-          for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
+          for (int c0 = part * kCols; c0 < (part + 1) * kCols; c0 += 32) {
             float v[32];
             tmem_ld32(acc + uint32_t(mt) * 128 + uint32_t(c0), v);
-            float mx = -INFINITY;
-            if (plain) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                v[i] *= sc;
-                mx = fmaxf(mx, v[i]);
-              }
-            } else {
+            if (!plain) {
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 const int key = kt0 + c0 + i;
-                v[i] = (key >= key0 && key < key1 && key <= limit[mt]) ? v[i] * sc : -INFINITY;
-                mx = fmaxf(mx, v[i]);
+                if (!(key >= key0 && key < key1 && key <= limit[mt])) v[i] = -INFINITY;
               }
             }
-            const float m_new = fmaxf(m_run[mt], mx);
+            float mx = -INFINITY;  // raw logits (the scale is positive)
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) mx = max3(mx, v[i], v[i + 1]);
+            const float m_new = fmaxf(m_run[mt], mx * sc);
             if (m_new != -INFINITY) {
               float sum = 0.f;
 #pragma unroll
-              for (int i = 0; i < 32; ++i) sum += fast_exp2(v[i] - m_new);
+              for (int i = 0; i < 32; i += 4) {
+                sum += fast_exp2(fmaf(v[i], sc, -m_new)) + fast_exp2(fmaf(v[i + 1], sc, -m_new)) +
+                       fast_exp2(fmaf(v[i + 2], sc, -m_new)) + fast_exp2(fmaf(v[i + 3], sc, -m_new));
+              }
               l_run[mt] = l_run[mt] * fast_exp2(m_run[mt] - m_new) + sum;
               m_run[mt] = m_new;
             }
@@ -283,7 +310,7 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
         }
       } else {
         const int nchunks = ((R + 31) & ~31) / 32;
-        const int cbeg = half == 0 ? 0 : (nchunks + 1) / 2, cend = half == 0 ? (nchunks + 1) / 2 : nchunks;
+        const int cbeg = nchunks * part / kTcEpiPerQ, cend = nchunks * (part + 1) / kTcEpiPerQ;
         float vote = 0.f;
 #pragma unroll 1
         for (int ci = cbeg; ci < cend; ++ci) {
@@ -297,53 +324,49 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
                     fast_exp2(fmaf(v[i + 2], sc, -C.z)) + fast_exp2(fmaf(v[i + 3], sc, -C.w));
           }
         }
-        float* xb = xch + (buf * 4 + quarter) * 32;
-        if (half == 1) xb[lane] = vote;
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
-        if (half == 0) {
+        float* xb = xch + ((buf * kTcEpiPerQ + part) * 4 + quarter) * 32;  // [parity][part][quarter][32]
+        xb[lane] = vote;
+        qsync();
+        if (part == 0) {
           const int key = kt0 + tl;
-          if (key >= key0 && key < key1) vrow[key] = vote + xb[lane];
+          float sum = 0.f;
+#pragma unroll
+          for (int q = 0; q < kTcEpiPerQ; ++q) sum += xch[((buf * kTcEpiPerQ + q) * 4 + quarter) * 32 + lane];
+          if (key >= key0 && key < key1) vrow[key] = sum;
         }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acc_empty[buf]));
     }
     if (kPass == 1) {
-      // merge the two halves' (m, l) per row, then write this chunk's statistics
-      float* xb = xch;  // [4 quarters][32] m, then [4][32] l
-      if (half == 1) {
-        xb[quarter * 32 + lane] = m_run[0];
-        xb[128 + quarter * 32 + lane] = l_run[0];
+      // merge the parts' (m, l) per row, then write this chunk's statistics
+      float* xm = xch;                                   // [2 mt][part][quarter][32]
+      float* xl = xch + 2 * kTcEpiPerQ * 4 * 32;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        xm[((mt * kTcEpiPerQ + part) * 4 + quarter) * 32 + lane] = m_run[mt];
+        xl[((mt * kTcEpiPerQ + part) * 4 + quarter) * 32 + lane] = l_run[mt];
       }
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
-      if (half == 0) {
-        const float m2 = xb[quarter * 32 + lane], l2 = xb[128 + quarter * 32 + lane];
-        const float M = fmaxf(m_run[0], m2);
-        if (M != -INFINITY) {
-          l_run[0] = l_run[0] * fast_exp2(m_run[0] - M) + l2 * fast_exp2(m2 - M);
-          m_run[0] = M;
-        }
-      }
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
-      if (half == 1) {
-        xb[quarter * 32 + lane] = m_run[1];
-        xb[128 + quarter * 32 + lane] = l_run[1];
-      }
-      asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
-      if (half == 0) {
-        const float m2 = xb[quarter * 32 + lane], l2 = xb[128 + quarter * 32 + lane];
-        const float M = fmaxf(m_run[1], m2);
-        if (M != -INFINITY) {
-          l_run[1] = l_run[1] * fast_exp2(m_run[1] - M) + l2 * fast_exp2(m2 - M);
-          m_run[1] = M;
-        }
+      qsync();
+      if (part == 0) {
         float* st = P.stats + (size_t(pair) * P.chunks + chunk) * R * 2;
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int mt = 0; mt < 2; ++mt) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < kTcEpiPerQ; ++q) M = fmaxf(M, xm[((mt * kTcEpiPerQ + q) * 4 + quarter) * 32 + lane]);
+          float Lr = 0.f;
+          if (M != -INFINITY)
+#pragma unroll
+            for (int q = 0; q < kTcEpiPerQ; ++q) {
+              const float m = xm[((mt * kTcEpiPerQ + q) * 4 + quarter) * 32 + lane];
+              if (m != -INFINITY) Lr += xl[((mt * kTcEpiPerQ + q) * 4 + quarter) * 32 + lane] * fast_exp2(m - M);
+            }
           if (mt < nMt && mt * 128 + tl < R) {
-            st[(mt * 128 + tl) * 2] = m_run[mt];
-            st[(mt * 128 + tl) * 2 + 1] = l_run[mt];
+            st[(mt * 128 + tl) * 2] = M;
+            st[(mt * 128 + tl) * 2 + 1] = Lr;
           }
+        }
       }
     }
   }
@@ -465,6 +488,8 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
     return fail(KVSEL_ERR_UNSUPPORTED, fn + "(q heads per kv head) * obs_window must be <= 256");
   if (seq_len >= (1 << 28))
     return fail(KVSEL_ERR_UNSUPPORTED, fn + "seq_len must be < 2^28");
+  if (!(scale > 0.f))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "scale must be positive");
   if (pool_kernel < 1 || pool_kernel % 2 == 0 || pool_kernel / 2 > kSnMaxHalf)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "pool_kernel must be odd, 1..33");
   if ((seq_len + kSnPage - 1) / kSnPage > max_pages)

@@ -328,6 +328,7 @@ KVSEL_API kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int32
  *   block_table   int32 [num_layers][max_pages]: layer l's prompt pages.
  *   seq_len       prompt length S (host value), obs_window W <= S.
  *   q_obs         bf16 [num_layers][num_q_heads][W][128].
+ *   scale         logit scale, > 0 (head_dim^-1/2); else KVSEL_ERR_INVALID_ARG.
  *   pool_kernel   odd, 1..33 (7 in SnapKV).
  *   keep_out      int32 [num_layers][num_kv_heads][keep_k + W]; when
  *                 S - W <= keep_k every position 0..S-1 is kept, -1 padded.
