@@ -11,7 +11,7 @@
 //   o[b, h] = softmax over s in sel_b of scale * q[b, h] . K_{h/G}[s], times V
 // One selected set per (sequence, step), shared by every q head.
 //
-// Kernels (five launches on the caller's stream):
+// Kernels (four launches on the caller's stream):
 //   sd_index_kernel      128 tokens per CTA; the indexer dot products run on
 //                        mma.sync (16 tokens x 16 dims x 8 heads per MMA, the
 //                        dims permuted per lane so every lane reads 8-byte runs
@@ -25,9 +25,11 @@
 //                        16K a single sd_topk_kernel per row replaces both.)
 //   sd_attn_kernel       (splits, kv head, sequence): each warp gathers 16
 //                        selected rows of K and V with cp.async into the
-//                        swizzled tile layout (double-buffered) and runs the
-//                        shared mma.sync tile; the 4 warps merge per CTA
-//   sd_merge_kernel      merges the splits into O and publishes the lengths
+//                        swizzled tile layout (double-buffered; the pages were
+//                        resolved by the top-k stage) and runs the shared
+//                        mma.sync tile; the 4 warps merge per CTA; the last
+//                        split of a (sequence, kv head) merges the splits
+//                        into O and the last kv head publishes the length
 #include "attn_tile.cuh"
 #include "row_topk.cuh"
 
@@ -63,6 +65,9 @@ struct SdParams {
   uint32_t* cand_key;              // [B][nchunks][top_k]: first-stage candidates (two-stage only)
   int32_t* cand_pos;               // [B][nchunks][top_k]
   int32_t* sel;                    // [B][top_k]
+  int32_t* sel_page;               // [B][top_k]: physical page of each selected position
+  unsigned* merge_cnt;             // [B][Hkv]: splits done (the last one merges)
+  unsigned* seq_cnt;               // [B]: kv heads merged (the last one publishes the length)
   int32_t* nsel;                   // [B]
   int32_t* topk_out;               // [B][top_k] or null
   float* part;                     // [B][Hkv][splits][kSdPartFloats]
@@ -201,8 +206,11 @@ __global__ void __launch_bounds__(kRkThreads) sd_topk_final_kernel(const SdParam
   const int k = min(P.top_k, S);
   int32_t* sel = P.sel + size_t(b) * P.top_k;
   int32_t* tko = P.topk_out ? P.topk_out + size_t(b) * P.top_k : nullptr;
+  int32_t* spage = P.sel_page + size_t(b) * P.top_k;
+  const int32_t* bt = P.block_table + size_t(b) * P.max_pages;
   auto put = [&](int i, int pos) {
     sel[i] = pos;
+    spage[i] = bt[pos / kSdPage];  // resolved once here for every kv head's gather
     if (tko) tko[i] = pos;
   };
   if (k == S) {
@@ -233,8 +241,11 @@ __global__ void __launch_bounds__(kRkThreads) sd_topk_kernel(const SdParams P) {
   const int k = min(P.top_k, S);
   int32_t* sel = P.sel + size_t(b) * P.top_k;
   int32_t* tko = P.topk_out ? P.topk_out + size_t(b) * P.top_k : nullptr;
+  int32_t* spage = P.sel_page + size_t(b) * P.top_k;
+  const int32_t* bt = P.block_table + size_t(b) * P.max_pages;
   auto put = [&](int i, int pos) {
     sel[i] = pos;
+    spage[i] = bt[pos / kSdPage];  // resolved once here for every kv head's gather
     if (tko) tko[i] = pos;
   };
   if (k == S) {
@@ -248,6 +259,8 @@ __global__ void __launch_bounds__(kRkThreads) sd_topk_kernel(const SdParams P) {
     for (int i = k + tid; i < P.top_k; i += kRkThreads) tko[i] = -1;
   if (tid == 0) P.nsel[b] = k;
 }
+
+__device__ void sd_merge_splits(const SdParams& P, int b, int kvh, float* scratch);
 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdParams P) {
@@ -265,7 +278,7 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
   const int G = P.G, g = lane >> 2, qd = lane & 3;
   const bool head_ok = g < G;
   const int32_t* sel = P.sel + size_t(b) * P.top_k;
-  const int32_t* bt = P.block_table + size_t(b) * P.max_pages;
+  const int32_t* spg = P.sel_page + size_t(b) * P.top_k;
   const uint32_t wbuf = smem_u32(smem + warp * 2 * 8192);
 
   uint32_t qa[8][2];
@@ -282,8 +295,8 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
       const int r16 = row & 15;
       const int tok = t * 16 + r16;
       const bool valid = tok < nsel;
-      int posi = valid ? sel[tok] : 0;
-      int phys = valid ? bt[posi / kSdPage] : 0;
+      const int posi = valid ? sel[tok] : 0;
+      int phys = valid ? spg[tok] : 0;
       if (valid && unsigned(phys) >= unsigned(P.num_pages)) {
         report(P.status, KVSEL_ERR_BAD_INDEX);
         phys = 0;
@@ -354,15 +367,42 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
       slot[kSdMaxG + gg] = L;
     }
   }
+  // The last split of (sequence, kv head) to finish merges all of them into O;
+  // the last kv head of a sequence to be merged publishes its length.
+  __shared__ int s_last;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned done = atomicAdd(P.merge_cnt + size_t(b) * P.Hkv + kvh, 1u) + 1u;
+    s_last = done == unsigned(P.splits);
+    if (s_last) {
+      P.merge_cnt[size_t(b) * P.Hkv + kvh] = 0u;  // every split has arrived: ready for the next call
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (s_last) {
+    sd_merge_splits(P, b, kvh, reinterpret_cast<float*>(smem));
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      if (atomicAdd(P.seq_cnt + b, 1u) + 1u == unsigned(P.Hkv)) {
+        P.seq_cnt[b] = 0u;
+        P.seq_lens[b] = S;  // every CTA of this sequence has read the old length
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) sd_merge_kernel(const SdParams P) {
-  const int kvh = blockIdx.x, b = blockIdx.y;
-  int S;
-  if (!sd_len_ok(P, b, S)) return;
-  __shared__ float sm[kSdMaxSplits][kSdMaxG], sl[kSdMaxSplits][kSdMaxG], sf[kSdMaxSplits][kSdMaxG];
-  __shared__ float sM[kSdMaxG], sI[kSdMaxG];
+// Merge of the splits of one (sequence, kv head) into O, by one CTA of
+// kSdAttnWarps warps; `scratch` holds 3 x kSdMaxSplits x kSdMaxG + 2 x kSdMaxG floats.
+__device__ void sd_merge_splits(const SdParams& P, int b, int kvh, float* scratch) {
+  float (*sm)[kSdMaxG] = reinterpret_cast<float (*)[kSdMaxG]>(scratch);
+  float (*sl)[kSdMaxG] = sm + kSdMaxSplits;
+  float (*sf)[kSdMaxG] = sl + kSdMaxSplits;
+  float* sM = &sf[kSdMaxSplits][0];
+  float* sI = sM + kSdMaxG;
   const size_t pbase = (size_t(b) * P.Hkv + kvh) * P.splits;
   const int G = P.G;
   for (int t = threadIdx.x; t < P.splits * G; t += blockDim.x) {  // every (split, head) at once
@@ -399,7 +439,6 @@ __global__ void __launch_bounds__(256) sd_merge_kernel(const SdParams P) {
     if (P.out_f32) static_cast<float*>(P.out)[oi] = acc;
     else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(acc);
   }
-  if (kvh == 0 && threadIdx.x == 0) P.seq_lens[b] = S;
 }
 
 }  // namespace kvsel
@@ -409,7 +448,7 @@ using namespace kvsel_host;
 
 namespace {
 struct SdWs {
-  size_t scores, ckey, cpos, sel, nsel, part, total;
+  size_t scores, ckey, cpos, sel, spage, nsel, cnt, part, total;
   int nchunks;  // 0: single-stage top-k
 };
 SdWs sd_ws_layout(int batch, int Hkv, int max_len, int top_k, bool own_scores) {
@@ -425,6 +464,8 @@ SdWs sd_ws_layout(int batch, int Hkv, int max_len, int top_k, bool own_scores) {
   w.ckey = take(size_t(batch) * w.nchunks * top_k * 4);
   w.cpos = take(size_t(batch) * w.nchunks * top_k * 4);
   w.sel = take(size_t(batch) * top_k * 4);
+  w.spage = take(size_t(batch) * top_k * 4);
+  w.cnt = take((size_t(batch) * Hkv + batch) * 4);
   w.nsel = take(size_t(batch) * 4);
   w.part = take(size_t(batch) * Hkv * kSdMaxSplits * kSdPartFloats * 4);
   w.total = off;
@@ -499,6 +540,9 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   P.cand_pos = reinterpret_cast<int32_t*>(ws + L.cpos);
   P.nchunks = L.nchunks;
   P.sel = reinterpret_cast<int32_t*>(ws + L.sel);
+  P.sel_page = reinterpret_cast<int32_t*>(ws + L.spage);
+  P.merge_cnt = reinterpret_cast<unsigned*>(ws + L.cnt);
+  P.seq_cnt = P.merge_cnt + size_t(batch) * Hkv;
   P.nsel = reinterpret_cast<int32_t*>(ws + L.nsel);
   P.topk_out = topk_out;
   P.part = reinterpret_cast<float*>(ws + L.part);
@@ -542,7 +586,6 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
     KVSEL_SD_LAUNCH("sd_topk", sd_topk_kernel, dim3(batch), kRkThreads, sizeof(RowTopkSmem))
   }
   KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem)
-  KVSEL_SD_LAUNCH("sd_merge", sd_merge_kernel, dim3(Hkv, batch), 256, 0)
 #undef KVSEL_SD_LAUNCH
   return KVSEL_OK;
 }

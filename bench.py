@@ -595,10 +595,10 @@ def _setup_sparse_decode(dev, small=False):
 
     S = wl.S0 + wl.steps // 2
     byts = {"sd_index": wl.B * S * (wl.Di * 2 + 4), "sd_attn": wl.B * wl.top_k * wl.Hkv * 512,
-            "sd_topk_chunk": wl.B * S * 4, "sd_topk_final": wl.B * 9 * wl.top_k * 8, "sd_merge": 0}
+            "sd_topk_chunk": wl.B * S * 4, "sd_topk_final": wl.B * 9 * wl.top_k * 8}
     host_in = [("q", q), ("q_idx", qi), ("w_idx", wi), ("k_new", kn), ("v_new", vn), ("k_idx_new", kin)]
     return dict(step=step, run=run, host_in=host_in, outs=[out, topk], ws=[ws], bytes=byts, flops={},
-                per_step_launches=5, steps_cycle=wl.steps,
+                per_step_launches=4, steps_cycle=wl.steps,
                 config={"batch": wl.B, "context": wl.S0, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
                         "indexer": f"{wl.Hi} x {wl.Di}", "top_k": wl.top_k,
                         "l2": "inputs larger than L2 (67 MB indexer keys + 33.5 MB gathered K/V per step)"})
