@@ -92,6 +92,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
+// 3D tiled load (see encode_bf16_row_pages): one instruction moves a whole
+// box of rows x 128 bf16 as two 64-column halves, 128-byte swizzled.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
 // Order this thread's earlier generic-proxy global writes before later
 // async-proxy (TMA) reads of the same memory.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -154,6 +164,12 @@ cudaError_t smem_limit_once(const void* fn, int bytes);
 // Encode a 2D bf16 tensor map with 128-byte swizzle over a [rows][inner] array.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+// The same [rows][128] bf16 array as a 3D tensor {64 columns, rows, 2 halves}
+// (strides 256 B and 128 B) with boxes of {64, box_rows, 2}: one TMA load puts
+// box_rows whole rows in shared memory as two [box_rows][128 B] halves, the
+// second 64 * box_rows * 2 bytes after the first -- the layout two 2D loads of
+// 64-column boxes would write, at half the instructions.
+bool encode_bf16_row_pages(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Launch tracing (see kvsel_trace_start): call around every kernel launch.
 void trace_before(const char* kernel, cudaStream_t st);

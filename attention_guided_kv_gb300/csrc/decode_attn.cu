@@ -16,8 +16,11 @@
 //
 // Phase A, per CTA (5 warps):
 //   * warp 4 lane 0 is the producer: it walks the range through the block
-//     table and TMA-loads each page's K and V rows of its kv head (2 x 2 KB
-//     boxes each, 128-byte swizzle) into an 8-stage ring, evict-first in L2;
+//     table and TMA-loads each page's K and V rows of its kv head (one 3D
+//     load of 4 KB each, two 128-byte-swizzled 64-column halves) into an
+//     8-stage ring, evict-first in L2.  The producer's issue loop, not HBM,
+//     bounds the stream when a stage takes more instructions, so each stage
+//     costs two TMA instructions;
 //   * warps 0..3 take pages round-robin: S = Q K^T with mma.sync m16n8k16
 //     (A = the group's q rows, at most 8 real; B = 16 keys via ldmatrix),
 //     online softmax in the log2 domain, the log2 logits stored to the
@@ -322,10 +325,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             const uint32_t dst = smem_u32(smem + SmemLayout::ring + s * kStageBytes);
             const uint32_t bar = smem_u32(&full[s]);
             mbar_expect_tx(bar, kStageBytes);
-            tma_load_2d(dst, &tmK, 0, y, bar, pol);
-            tma_load_2d(dst + 2048, &tmK, 64, y, bar, pol);
-            tma_load_2d(dst + 4096, &tmV, 0, y, bar, pol);
-            tma_load_2d(dst + 6144, &tmV, 64, y, bar, pol);
+            tma_load_3d(dst, &tmK, 0, y, 0, bar, pol);
+            tma_load_3d(dst + 4096, &tmV, 0, y, 0, bar, pol);
           }
           __syncwarp();
         }
@@ -816,8 +817,8 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
 
   CUtensorMap tmK, tmV;
   const uint64_t rows = uint64_t(kv->num_pages) * Hkv * kPage;
-  if (!encode_bf16_2d(&tmK, kv->k_pool, kD, rows, kD * 2, 64, kPage) ||
-      !encode_bf16_2d(&tmV, kv->v_pool, kD, rows, kD * 2, 64, kPage))
+  if (!encode_bf16_row_pages(&tmK, kv->k_pool, rows, kPage) ||
+      !encode_bf16_row_pages(&tmV, kv->v_pool, rows, kPage))
     return fail(KVSEL_ERR_CUDA, fn + "tensor-map encode failed");
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
