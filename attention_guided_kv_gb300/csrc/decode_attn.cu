@@ -14,30 +14,34 @@
 // co-resident CTAs finishes together).  A CTA's range covers one or a few
 // pairs; each covered piece of a pair is a "segment".
 //
-// Phase A, per CTA (5 warps):
-//   * warp 4 lane 0 is the producer: it walks the range through the block
-//     table and TMA-loads each page's K and V rows of its kv head (one 3D
-//     load of 4 KB each, two 128-byte-swizzled 64-column halves) into an
-//     8-stage ring, evict-first in L2.  The producer's issue loop, not HBM,
-//     bounds the stream when a stage takes more instructions, so each stage
-//     costs two TMA instructions;
-//   * warps 0..3 take pages round-robin: S = Q K^T with mma.sync m16n8k16
-//     (A = the group's q rows, at most 8 real; B = 16 keys via ldmatrix),
-//     online softmax in the log2 domain, the log2 logits stored to the
-//     probability buffer, then O += P V with P split into a bf16 high part
-//     (A rows 0..7) and its bf16 residual (rows 8..15), so P keeps ~16
-//     mantissa bits at no extra MMA cost;
-//   * at each segment end the 4 warps merge and write (m, l, O) for the
-//     segment to a partial slot.
-// No grid barrier: after phase A a CTA announces each pair it worked on (a
-// per-pair counter); phase B of a pair waits (bounded spin; the launch is
-// cooperative, so all CTAs are co-resident) only until every owner of that
-// pair has announced.
-// Phase B, per CTA, for each of its segments: merge the pair's partials into
-// (M, L) (every owner's (m, l) fetched at once), write the owner's share of
-// O, and turn the segment's stored logits (still in L2) into probabilities
-// exp2(s - M) / L, adding the group sum into the H2O score.  The last CTA to
-// finish publishes the new lengths.
+// Each CTA (5 warps) streams its range twice, K pages first, then V pages:
+// warp 4 is the producer, TMA-loading two pages of K (or of V) of its kv
+// head per 8 KB stage -- one 3D load per 4 KB page, two 128-byte-swizzled
+// 64-column halves -- into an 8-stage ring, evict-first in L2; warps 0..3
+// take the ring's stages round-robin.  (The producer's issue loop costs a
+// fixed few hundred cycles per stage, so stages of one page could not keep
+// up with HBM.)
+//   * K pass: S = Q K^T with mma.sync m16n8k16 (A = the group's q rows, at
+//     most 8 real; B = 16 keys via ldmatrix); the scaled log2-domain logits
+//     are stored to the probability buffer, marked evict-last so they are
+//     still in L2 for the V pass, and each lane keeps a running (max, sum of
+//     exp2) of its keys.  At a segment end the CTA writes the segment's
+//     (m, l) per head to a partial slot and announces the pair (a per-pair
+//     counter).
+//   * V pass: per segment, once every owner of the pair has announced
+//     (bounded spin; the launch is cooperative, so all CTAs are co-resident),
+//     the pair's exact (M, L) per head are merged from the owners' slots.
+//     Every page then turns its stored logits into final probabilities
+//     p = exp2(s - M) / L, writes them (evict-first), adds the group's sum
+//     into the H2O score (collecting the H2O candidates of the next
+//     selection), and
+//     accumulates O += P V with P split into a bf16 high part (A rows 0..7)
+//     and its bf16 residual (rows 8..15), so P keeps ~16 mantissa bits at no
+//     extra MMA cost.  The segment's O, already normalised, goes to the slot.
+// The normalisation work therefore overlaps the V stream instead of trailing
+// the kernel.  Last, once every owner's V pass is done, each owner writes its
+// share of O = the sum of the pair's partial O.  The last CTA to finish
+// publishes the new lengths.
 //
 // The CTA that owns the page of a sequence's appended slot writes k_new /
 // v_new into the pool (and the slot's original position) before its
@@ -51,36 +55,34 @@ namespace kvsel {
 
 constexpr int kD = 128;            // head_dim
 constexpr int kPage = 16;          // tokens per page
-constexpr int kStages = 8;         // TMA ring depth (pages)
+constexpr int kStages = 8;         // TMA ring depth (two pages of K or of V per stage)
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStageBytes = 8192;  // K (2 x 2 KB swizzled halves) + V (same)
+constexpr int kPageBytes = 4096;   // 16 rows x 128 bf16, as two 2 KB swizzled halves
+constexpr int kStageBytes = 2 * kPageBytes;
 constexpr int kMaxG = 8;
 constexpr int kMaxCtas = 1024;
-// Consumer warp w takes pages i with i % kConsumerWarps == w, so with a ring
-// depth that is a multiple of the warp count a stage is always used by the
-// same warp and its parity wait cannot pass on a later lap's phase.
+// Consumer warp w takes the stages t with t % kConsumerWarps == w, so with a
+// ring depth that is a multiple of the warp count a stage is always used by
+// the same warp and its parity wait cannot pass on a later lap's phase.
 static_assert(kStages % kConsumerWarps == 0, "ring depth must be a multiple of the consumer warps");
 constexpr int kMaxBatch = 1024;
 constexpr int kPartFloats = kMaxG * (kD + 2);  // one partial slot: m[8], l[8], O[8][128]
 constexpr int kMaxOwners = kMaxCtas;           // CTAs sharing one (sequence, kv head) pair
+constexpr int kWarpCands = 256;                // H2O candidates a consumer warp stages
 
 struct SmemLayout {
   static constexpr size_t ring = 0;
   static constexpr size_t merge_o = ring + size_t(kStages) * kStageBytes;                // [4][8][128] f32
   static constexpr size_t merge_ml = merge_o + size_t(kConsumerWarps) * kMaxG * kD * 4;  // [4][8][2] f32
-  static constexpr size_t bars = merge_ml + size_t(kConsumerWarps) * kMaxG * 2 * 4;     // 2 x kStages u64
+  static constexpr size_t cands = merge_ml + size_t(kConsumerWarps) * kMaxG * 2 * 4;    // [4][256] u32 + i32
+  static constexpr size_t bars = cands + size_t(kConsumerWarps) * kWarpCands * 8;        // 2 x kStages u64
   static constexpr size_t seqS = bars + 2 * kStages * 8;                                 // [kMaxBatch] i32
   static constexpr size_t seqPref = seqS + size_t(kMaxBatch) * 4;                        // [kMaxBatch+1] i64
   static constexpr size_t stats = seqPref + size_t(kMaxBatch + 1) * 8;                   // [8][2] f32
   static constexpr size_t owners = stats + kMaxG * 2 * 4;                                // [kMaxOwners+1] i32
-  static constexpr size_t link = owners + (kMaxOwners + 1) * 4;                          // count, base u32
-  static constexpr size_t total = link + 2 * 4;
+  static constexpr size_t total = owners + (kMaxOwners + 1) * 4;
 };
-// Phase B stages a segment's H2O candidates in the (then idle) TMA ring.
-constexpr int kStageCands = kStages * kStageBytes / 8;  // (key u32, slot i32) pairs
-// ... and, before that, every owner's partial (m, l) per head.
-static_assert(size_t(2) * kMaxOwners * kMaxG * 4 <= size_t(kStages) * kStageBytes, "owner stats fit in the ring");
 constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 
 struct StepParams {
@@ -93,8 +95,8 @@ struct StepParams {
   __nv_bfloat16* v_pool;
   int32_t* pos_map;
   int32_t* next_pos;
-  float* logits;   // log2-domain logits [B][Hq][max_len] (the probs buffer or workspace), or null
-  float* probs;    // output probabilities or null (may alias logits)
+  float* logits;   // log2-domain logits [B][Hq][max_len]: the probs buffer, else workspace
+  float* probs;    // output probabilities or null (aliases logits when given)
   float* cum;      // H2O score [B][Hkv][max_len] or null
   uint32_t* link_hint;   // H2O candidate hand-off (h2o_link.cuh), all null when not linked
   uint32_t* link_count;
@@ -103,12 +105,12 @@ struct StepParams {
   void* out;
   float* part;     // [slots][kPartFloats]
   unsigned* fin;   // CTAs finished (status area); the last one publishes the lengths
-  unsigned* pair_cnt;   // [B*Hkv] owners whose phase A is done
-  unsigned* pair_pass;  // [B*Hkv] owners past the wait (the last resets both)
+  unsigned* pair_k;     // [B*Hkv] owners whose K pass is done: their (m, l) are written
+  unsigned* pair_v;     // [B*Hkv] owners whose V pass is done: their O is written
+  unsigned* pair_done;  // [B*Hkv] owners past both waits (the last resets all three)
   int* status;
   int B, max_pages, Hq, Hkv, G, num_pages, max_len, out_f32;
-  int vec_logits;  // logit rows are 8-byte aligned: store pairs as float2
-  int vec4;        // logit / score rows are 16-byte aligned: phase B moves float4
+  int vec2;        // logit and score rows are 8-byte aligned: key pairs move as float2
   float scale_log2;
 };
 
@@ -163,42 +165,113 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int NC) {
   return int(((u + 1) * NC + U - 1) / U) - 1;
 }
 
-// Stages the slots j + c (c < n) whose new score key is >= hk in shared
-// memory (sk / sp, counter *scnt): one shared atomic per warp (any subset of
-// its lanes).  Entries past kStageCands are dropped; the caller sees the
-// overflow in the counter.
-template <int n>
-__device__ __forceinline__ void link_stage(uint32_t* sk, int32_t* sp, uint32_t* scnt, int j, float4 v,
-                                           uint32_t hk) {
-  const uint32_t key[4] = {order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w)};
-  bool hit[n];
-#pragma unroll
-  for (int c = 0; c < n; ++c) hit[c] = key[c] >= hk;
-  const uint32_t act = __activemask();
-  const int lane = threadIdx.x & 31;
-  uint32_t lt;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
-  uint32_t tot = 0, pre = 0;
-#pragma unroll
-  for (int c = 0; c < n; ++c) {
-    const uint32_t b = __ballot_sync(act, hit[c]);
-    tot += __popc(b);
-    pre += __popc(b & lt);
+// The CTAs owning units [pfirst, plast] of a pair, in order: the owner of
+// pfirst, then the owner of the unit right after each owner's range.  Written
+// to own[0..n-1], n to own[kMaxOwners]; one thread.
+__device__ __forceinline__ int list_owners(int* own, long long pfirst, long long plast, long long U, int NC) {
+  int no = 0;
+  for (int cc = cta_of(pfirst, U, NC); cc >= 0 && no < kMaxOwners; ++no) {
+    own[no] = cc;
+    const long long nu = U * (cc + 1) / NC;
+    cc = nu > plast ? -1 : cta_of(nu, U, NC);
   }
-  if (tot == 0) return;
-  const int leader = __ffs(act) - 1;
+  own[kMaxOwners] = no;
+  return no;
+}
+
+// Merge of two (max, sum of exp2) pairs.
+__device__ __forceinline__ void ml_merge(float& m, float& l, float mo, float lo) {
+  const float mn = fmaxf(m, mo);
+  l = mn == -INFINITY ? 0.f : l * exp2f(m - mn) + lo * exp2f(mo - mn);
+  m = mn;
+}
+
+// A consumer warp's H2O candidates (slots whose new score key is >= the
+// row's last threshold), staged in shared memory and handed to the row's
+// list with one global atomic per flush.
+struct WarpCands {
+  uint32_t* key;  // [kWarpCands]
+  int32_t* pos;   // [kWarpCands]
+  uint32_t n;     // staged entries (warp-uniform)
+};
+
+// Every lane offers slot j with new score v (where on).
+__device__ __forceinline__ void cands_stage(WarpCands& wc, bool on, int j, float v, uint32_t hk, int lane) {
+  const uint32_t k = order_key(v);
+  const bool h = on && k >= hk;
+  const uint32_t bal = __ballot_sync(0xffffffffu, h);
+  if (h) {
+    const uint32_t o = wc.n + __popc(bal & ((1u << lane) - 1u));
+    wc.key[o] = k;
+    wc.pos[o] = j;
+  }
+  wc.n += __popc(bal);
+}
+
+__device__ __forceinline__ void cands_flush(WarpCands& wc, const StepParams& P, int pair, int lane) {
+  if (wc.n == 0) return;
+  __syncwarp();
   uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(scnt, tot);
-  base = __shfl_sync(act, base, leader) + pre;
-#pragma unroll
-  for (int c = 0; c < n; ++c)
-    if (hit[c]) {
-      if (base < uint32_t(kStageCands)) {
-        sk[base] = key[c];
-        sp[base] = j + c;
-      }
-      ++base;
-    }
+  if (lane == 0) base = atomicAdd(P.link_count + pair, wc.n);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  uint32_t* gk = P.link_key + size_t(pair) * kLinkCap;
+  int32_t* gp = P.link_pos + size_t(pair) * kLinkCap;
+  for (uint32_t i = lane; i < wc.n && base + i < uint32_t(kLinkCap); i += 32) {
+    gk[base + i] = wc.key[i];
+    gp[base + i] = wc.pos[i];
+  }
+  __syncwarp();
+  wc.n = 0;
+}
+
+// Two key pairs of one row: keys k0, k0 + 1 and k2, k2 + 1 of a page starting
+// at row[key0]; entries at or past `valid` read as `fill`.
+__device__ __forceinline__ float4 load_keys(const float* row, int key0, int valid, int k0, int k2, bool vec2,
+                                            float fill) {
+  float4 r = make_float4(fill, fill, fill, fill);
+  const float* p = row + key0;
+  if (vec2 && valid >= kPage) {
+    const float2 a = __ldcg(reinterpret_cast<const float2*>(p + k0));
+    const float2 b = __ldcg(reinterpret_cast<const float2*>(p + k2));
+    r = make_float4(a.x, a.y, b.x, b.y);
+  } else {
+    if (k0 < valid) r.x = __ldcg(p + k0);
+    if (k0 + 1 < valid) r.y = __ldcg(p + k0 + 1);
+    if (k2 < valid) r.z = __ldcg(p + k2);
+    if (k2 + 1 < valid) r.w = __ldcg(p + k2 + 1);
+  }
+  return r;
+}
+__device__ __forceinline__ void st_hint(float* p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st2_hint(float* p, float a, float b, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(p), "f"(a), "f"(b), "l"(pol) : "memory");
+}
+// Stores key pairs like load_keys reads them, with L2 eviction policy pol.
+__device__ __forceinline__ void store_keys(float* row, int key0, int valid, int k0, int k2, bool vec2, float4 v,
+                                           uint64_t pol) {
+  float* p = row + key0;
+  if (vec2 && valid >= kPage) {
+    st2_hint(p + k0, v.x, v.y, pol);
+    st2_hint(p + k2, v.z, v.w, pol);
+  } else {
+    if (k0 < valid) st_hint(p + k0, v.x, pol);
+    if (k0 + 1 < valid) st_hint(p + k0 + 1, v.y, pol);
+    if (k2 < valid) st_hint(p + k2, v.z, pol);
+    if (k2 + 1 < valid) st_hint(p + k2 + 1, v.w, pol);
+  }
+}
+// 2^x by the hardware approximation (relative error ~2^-22; -inf gives 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -282,15 +355,28 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   }
   __syncthreads();
 
-  const int n = int(u1 - u0);
+  const int n = int(u1 - u0);       // pages of the range
+  const int nsk = (n + 1) >> 1;     // stages per pass
   const int g = lane >> 2, qd = lane & 3;
   const bool head_ok = g < G;
+  const bool vec2 = P.vec2 != 0;
+  const int k0 = 2 * qd, k2 = 8 + 2 * qd;  // this lane's keys in a page: k0, k0+1, k2, k2+1
 
-  // ================= phase A =================
+  // Stage t of a pass holds the pass's pages 2t and 2t + 1; the K pass uses
+  // ring stages 0 .. nsk-1, the V pass nsk .. 2 nsk - 1.  Ring stage r
+  // belongs to consumer warp r % 4.
+  auto first_page = [&](int i, int base) -> int {  // this warp's first page >= i
+    const int t = i >> 1;
+    const int tt = t + ((warp - (base + t) % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+    return tt == t ? i : 2 * tt;
+  };
+  auto next_page = [](int i) -> int { return (i & 1) ? i + 2 * kConsumerWarps - 1 : i + 1; };
+
   if (warp == kConsumerWarps) {
-    // Producer warp.  Every lane resolves one page of a 32-page chunk (block
-    // table entry -> TMA row coordinate), two chunks ahead of use, so the
-    // dependent block-table loads never sit between two TMA issues.
+    // ================= producer =================
+    // Every lane resolves one page of a 32-page chunk (block table entry ->
+    // TMA row coordinate), two chunks ahead of use, so the dependent
+    // block-table loads never sit between two TMA issues.
     if (n > 0) {
       const uint64_t pol = l2_policy_evict_first();
       auto resolve = [&](int i) -> int {  // TMA row of CTA-local page i (or -1 past the end)
@@ -304,42 +390,50 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         }
         return (phys * Hkv + kvh) * kPage;
       };
-      int y_cur = resolve(lane);
-      int y_next = resolve(32 + lane);
+      bool stop = false;
 #pragma unroll 1
-      for (int i0 = 0; i0 < n; i0 += 32) {
-        const int y_after = resolve(i0 + 64 + lane);  // issued early; used two chunks later
-        bool stop = false;
+      for (int pass = 0; pass < 2 && !stop; ++pass) {
+        const CUtensorMap* tm = pass ? &tmV : &tmK;
+        int y_cur = resolve(lane);
+        int y_next = resolve(32 + lane);
 #pragma unroll 1
-        for (int k = 0; k < 32 && i0 + k < n; ++k) {
-          const int i = i0 + k;
-          const int y = __shfl_sync(0xffffffffu, y_cur, k);
-          const int s = i % kStages;
-          bool ok = true;
-          if (i >= kStages) ok = mbar_wait(smem_u32(&empty[s]), ((i / kStages) + 1) & 1, P.status);
-          if (!__all_sync(0xffffffffu, ok)) {
-            stop = true;
-            break;
+        for (int i0 = 0; i0 < n && !stop; i0 += 32) {
+          const int y_after = resolve(i0 + 64 + lane);  // issued early; used two chunks later
+#pragma unroll 1
+          for (int k = 0; k < 32 && i0 + k < n; k += 2) {
+            const int t = pass * nsk + ((i0 + k) >> 1);
+            const int ya = __shfl_sync(0xffffffffu, y_cur, k);
+            const int yb = __shfl_sync(0xffffffffu, y_cur, k + 1);
+            const bool two = i0 + k + 1 < n;
+            const int s = t % kStages;
+            bool ok = true;
+            if (t >= kStages) ok = mbar_wait(smem_u32(&empty[s]), ((t / kStages) + 1) & 1, P.status);
+            if (!__all_sync(0xffffffffu, ok)) {
+              stop = true;
+              break;
+            }
+            if (lane == 0) {
+              const uint32_t dst = smem_u32(smem + SmemLayout::ring + s * kStageBytes);
+              const uint32_t bar = smem_u32(&full[s]);
+              mbar_expect_tx(bar, two ? kStageBytes : kPageBytes);
+              tma_load_3d(dst, tm, 0, ya, 0, bar, pol);
+              if (two) tma_load_3d(dst + kPageBytes, tm, 0, yb, 0, bar, pol);
+            }
+            __syncwarp();
           }
-          if (lane == 0) {
-            const uint32_t dst = smem_u32(smem + SmemLayout::ring + s * kStageBytes);
-            const uint32_t bar = smem_u32(&full[s]);
-            mbar_expect_tx(bar, kStageBytes);
-            tma_load_3d(dst, &tmK, 0, y, 0, bar, pol);
-            tma_load_3d(dst + 4096, &tmV, 0, y, 0, bar, pol);
-          }
-          __syncwarp();
+          y_cur = y_next;
+          y_next = y_after;
         }
-        if (stop) break;
-        y_cur = y_next;
-        y_next = y_after;
       }
     }
   } else {
     const int mi = lane >> 3, r8 = lane & 7;
-    long long u = u0;
+    bool alive = true;  // false once a ring wait ran out: the warp then leaves the ring alone
+    const uint64_t keep_l2 = l2_policy_evict_last(), drop_l2 = l2_policy_evict_first();
+
+    // ================= K pass =================
 #pragma unroll 1
-    while (u < u1) {
+    for (long long u = u0; u < u1;) {
       int b, kvh, pg;
       loc.locate(u, b, kvh, pg);
       const int S = sS[b];
@@ -357,24 +451,18 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           qa[kt][1] = head_ok ? qrow[(16 * kt + 8 + 2 * qd) >> 1] : 0u;
         }
       }
-      float* lrow = (P.logits && head_ok)
-                        ? P.logits + (size_t(b) * P.Hq + kvh * G + g) * P.max_len
-                        : nullptr;
-      float m_run = -INFINITY, l_run = 0.f;
-      float o[16][4];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      float* lrow = head_ok ? P.logits + (size_t(b) * P.Hq + kvh * G + g) * P.max_len : nullptr;
+      float m_l = -INFINITY, l_l = 0.f;  // this lane's keys of the segment
 
       const int i_begin = int(u - u0), i_end = int(seg_end - u0);
-      // first index >= i_begin that belongs to this warp (index % 4 == warp)
-      int i = i_begin + ((warp - i_begin) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
 #pragma unroll 1
-      for (; i < i_end; i += kConsumerWarps) {
-        const int s = i % kStages;
-        if (!mbar_wait(smem_u32(&full[s]), (i / kStages) & 1, P.status)) break;
-        const uint32_t kb = smem_u32(smem + SmemLayout::ring + s * kStageBytes);
-        const uint32_t vb = kb + 4096;
-
+      for (int i = first_page(i_begin, 0); i < i_end && alive; i = next_page(i)) {
+        const int t = i >> 1, s = t % kStages;
+        if (!mbar_wait(smem_u32(&full[s]), (t / kStages) & 1, P.status)) {
+          alive = false;
+          break;
+        }
+        const uint32_t kb = smem_u32(smem + SmemLayout::ring + s * kStageBytes + (i & 1) * kPageBytes);
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kt = 0; kt < 8; ++kt) {
@@ -385,41 +473,172 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           mma_bf16_16816(s0, qa[kt][0], 0u, qa[kt][1], 0u, b0, b1);
           mma_bf16_16816(s1, qa[kt][0], 0u, qa[kt][1], 0u, b2, b3);
         }
+        __syncwarp();
+        if ((i & 1) || i + 1 == n)  // the stage's last page: its K rows are in registers now
+          if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+
         const int key0 = (pg + (i - i_begin)) * kPage;
         const int valid = S - key0;  // >= 1
-        const int k0 = 2 * qd, k2 = 8 + 2 * qd;
-        const float x0 = k0 < valid ? s0[0] * P.scale_log2 : -INFINITY;
-        const float x1 = k0 + 1 < valid ? s0[1] * P.scale_log2 : -INFINITY;
-        const float x2 = k2 < valid ? s1[0] * P.scale_log2 : -INFINITY;
-        const float x3 = k2 + 1 < valid ? s1[1] * P.scale_log2 : -INFINITY;
-        if (lrow) {
-          float* dst = lrow + key0;
-          if (valid >= kPage && P.vec_logits) {
-            *reinterpret_cast<float2*>(dst + k0) = make_float2(x0, x1);
-            *reinterpret_cast<float2*>(dst + k2) = make_float2(x2, x3);
-          } else {
-            if (k0 < valid) dst[k0] = x0;
-            if (k0 + 1 < valid) dst[k0 + 1] = x1;
-            if (k2 < valid) dst[k2] = x2;
-            if (k2 + 1 < valid) dst[k2 + 1] = x3;
-          }
+        float4 x;
+        x.x = k0 < valid ? s0[0] * P.scale_log2 : -INFINITY;
+        x.y = k0 + 1 < valid ? s0[1] * P.scale_log2 : -INFINITY;
+        x.z = k2 < valid ? s1[0] * P.scale_log2 : -INFINITY;
+        x.w = k2 + 1 < valid ? s1[1] * P.scale_log2 : -INFINITY;
+        if (lrow) store_keys(lrow, key0, valid, k0, k2, vec2, x, keep_l2);  // read back by the V pass
+        const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+        if (mx != -INFINITY) {
+          const float m_new = fmaxf(m_l, mx);
+          l_l = l_l * ex2(m_l - m_new) + ((ex2(x.x - m_new) + ex2(x.y - m_new)) +
+                                          (ex2(x.z - m_new) + ex2(x.w - m_new)));
+          m_l = m_new;
         }
-        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = exp2f(m_run - m_new);
-        const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
-        const float p2 = exp2f(x2 - m_new), p3 = exp2f(x3 - m_new);
-        l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
-        m_run = m_new;
+      }
+
+      // ---- the segment's (m, l) per head: over the head's 4 lanes, then the 4 warps ----
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          o[nt][0] *= alpha;
-          o[nt][1] *= alpha;
-          o[nt][2] *= alpha;
-          o[nt][3] *= alpha;
+      for (int off = 1; off <= 2; off <<= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m_l, off);
+        const float lo = __shfl_xor_sync(0xffffffffu, l_l, off);
+        ml_merge(m_l, l_l, mo, lo);
+      }
+      if (qd == 0 && head_ok) {
+        wml[(warp * kMaxG + g) * 2 + 0] = m_l;
+        wml[(warp * kMaxG + g) * 2 + 1] = l_l;
+      }
+      consumer_sync();
+      if (tid < G) {
+        float M = -INFINITY, L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w)
+          ml_merge(M, L, wml[(w * kMaxG + tid) * 2], wml[(w * kMaxG + tid) * 2 + 1]);
+        float* slot = P.part + size_t(c + pair) * kPartFloats;
+        slot[tid] = M;
+        slot[kMaxG + tid] = L;
+      }
+      __threadfence();  // the slot and this segment's logits
+      consumer_sync();
+      if (tid == 0) {
+        // the first owner gives the pair a fresh H2O candidate list before anyone can append
+        if (P.link_count && pg == 0) P.link_count[pair] = 0u;
+        __threadfence();
+        atomicAdd(P.pair_k + pair, 1u);
+      }
+      u = seg_end;
+    }
+
+    // ================= V pass =================
+    WarpCands wc;
+    wc.key = reinterpret_cast<uint32_t*>(smem + SmemLayout::cands) + warp * kWarpCands;
+    wc.pos = reinterpret_cast<int32_t*>(smem + SmemLayout::cands + kConsumerWarps * kWarpCands * 4) +
+             warp * kWarpCands;
+    wc.n = 0;
+    // after the head sums below, lanes of even heads hold key kc of each page
+    const bool csum_lane = (g & 1) == 0;
+    const int kc = ((g & 4) ? k2 : k0) + ((g & 2) ? 1 : 0);
+#pragma unroll 1
+    for (long long u = u0; u < u1;) {
+      int b, kvh, pg;
+      loc.locate(u, b, kvh, pg);
+      const int S = sS[b];
+      const int np = loc.pages(b);
+      const long long seg_end = min(u1, u + (np - pg));
+      const int pair = b * Hkv + kvh;
+      const size_t hrow = (size_t(b) * P.Hq + kvh * G + g) * P.max_len;
+      const float* lrow = head_ok ? P.logits + hrow : nullptr;
+      float* prow = (head_ok && P.probs) ? P.probs + hrow : nullptr;
+      float* crow = P.cum ? P.cum + (size_t(b) * Hkv + kvh) * P.max_len : nullptr;
+      const bool cown = crow != nullptr && csum_lane;
+      // the row's last H2O threshold: collect the slots at or above it (0: no list)
+      const uint32_t hk = (crow && P.link_hint) ? __ldcg(P.link_hint + pair) : 0u;
+
+      const int i_begin = int(u - u0), i_end = int(seg_end - u0);
+      // the stored logits and old score of one of this warp's pages
+      auto fetch = [&](int ii, float4& lg, float& cs) {
+        lg = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        cs = 0.f;
+        if (ii < i_end) {
+          const int key0 = (pg + (ii - i_begin)) * kPage;
+          const int valid = S - key0;
+          if (lrow) lg = load_keys(lrow, key0, valid, k0, k2, vec2, -INFINITY);
+          if (cown && kc < valid) cs = __ldcg(crow + key0 + kc);
         }
+      };
+      int i = first_page(i_begin, nsk);
+      float4 lgA, lgB;
+      float csA, csB;
+      fetch(i, lgA, csA);  // two pages ahead: issued before the wait below
+      fetch(next_page(i), lgB, csB);
+      if (tid == 0) {
+        const long long pfirst = sPref[b] + (long long)kvh * np;
+        const int no = list_owners(sOwn, pfirst, pfirst + np - 1, U, NC);
+        wait_word(P.pair_k + pair, unsigned(no), P.status);  // every owner's (m, l) is written
+      }
+      consumer_sync();
+      const int nown = sOwn[kMaxOwners];
+      // the pair's (M, 1/L) per head: warp w merges heads w, w + 4 over the owners, a lane per owner
+      for (int gg = warp; gg < G; gg += kConsumerWarps) {
+        float m = -INFINITY, l = 0.f;
+        for (int k = lane; k < nown; k += 32) {
+          const float* sl = P.part + size_t(sOwn[k] + pair) * kPartFloats;
+          ml_merge(m, l, __ldcg(sl + gg), __ldcg(sl + kMaxG + gg));
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+          const float lo = __shfl_xor_sync(0xffffffffu, l, off);
+          ml_merge(m, l, mo, lo);
+        }
+        if (lane == 0) {
+          sStat[gg * 2] = m;
+          sStat[gg * 2 + 1] = l > 0.f ? 1.f / l : 0.f;
+        }
+      }
+      consumer_sync();
+      const float Mg = head_ok ? sStat[g * 2] : 0.f;
+      const float Ig = head_ok ? sStat[g * 2 + 1] : 0.f;
+
+      float o[16][4];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+#pragma unroll 1
+      for (; i < i_end && alive; i = next_page(i)) {
+        const float4 lg = lgA;
+        const float cs = csA;
+        lgA = lgB;
+        csA = csB;
+        fetch(next_page(next_page(i)), lgB, csB);
+        const int t = nsk + (i >> 1), s = t % kStages;
+        if (!mbar_wait(smem_u32(&full[s]), (t / kStages) & 1, P.status)) {
+          alive = false;
+          break;
+        }
+        const uint32_t vb = smem_u32(smem + SmemLayout::ring + s * kStageBytes + (i & 1) * kPageBytes);
+        const int key0 = (pg + (i - i_begin)) * kPage;
+        const int valid = S - key0;  // >= 1
+
+        // final probabilities (keys past the length hold -inf: p = 0)
+        const float p0 = ex2(lg.x - Mg) * Ig, p1 = ex2(lg.y - Mg) * Ig;
+        const float p2 = ex2(lg.z - Mg) * Ig, p3 = ex2(lg.w - Mg) * Ig;
+        if (prow) store_keys(prow, key0, valid, k0, k2, vec2, make_float4(p0, p1, p2, p3), drop_l2);
+        if (crow) {
+          // the group's probability per key, a transposing sum over the 8 head
+          // rows: lanes of heads with bit 2 set keep keys k2, k2 + 1, the others
+          // k0, k0 + 1; bit 1 then picks one of the two; bit 0 completes the sum
+          const bool hi4 = (g & 4) != 0, hi2 = (g & 2) != 0;
+          float a = hi4 ? p2 : p0, bb = hi4 ? p3 : p1;
+          a += __shfl_xor_sync(0xffffffffu, hi4 ? p0 : p2, 16);
+          bb += __shfl_xor_sync(0xffffffffu, hi4 ? p1 : p3, 16);
+          float x = hi2 ? bb : a;
+          x += __shfl_xor_sync(0xffffffffu, hi2 ? a : bb, 8);
+          x += __shfl_xor_sync(0xffffffffu, x, 4);
+          const bool on = cown && kc < valid;
+          const float nv = ((append && key0 + kc == S - 1) ? 0.f : cs) + x;  // the appended slot starts from zero
+          if (on) __stcg(crow + key0 + kc, nv);
+          if (hk) cands_stage(wc, on, key0 + kc, nv, hk, lane);
+        }
+
+        // O += P V, P as bf16 high part (rows 0..7) + bf16 residual (rows 8..15)
         const uint32_t hi01 = pack_bf16x2(p0, p1);
         const uint32_t hi23 = pack_bf16x2(p2, p3);
         const uint32_t lo01 = pack_bf16x2(p0 - bf16lo_to_f32(hi01), p1 - bf16hi_to_f32(hi01));
@@ -440,17 +659,14 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           mma_bf16_16816(o[2 * j + 1], hi01, lo01, hi23, lo23, b2, b3);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if ((i & 1) || i + 1 == n)
+          if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (hk && wc.n > uint32_t(kWarpCands - 16)) cands_flush(wc, P, pair, lane);
       }
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+      if (hk) cands_flush(wc, P, pair, lane);
 
-      // ---- merge the 4 warps' state of this segment into partial slot c + pair ----
+      // ---- the segment's O (already normalised): the 4 warps' sum into the partial slot ----
       if (head_ok) {
-        if (qd == 0) {
-          wml[(warp * kMaxG + g) * 2 + 0] = m_run;
-          wml[(warp * kMaxG + g) * 2 + 1] = l_run;
-        }
         float* dst = wo + (warp * kMaxG + g) * kD;
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt)
@@ -458,53 +674,21 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
               make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
       }
       consumer_sync();
-      float* slot = P.part + size_t(c + pair) * kPartFloats;
-      for (int idx = tid; idx < G * kD; idx += kConsumerWarps * 32) {
-        const int gg = idx / kD, dd = idx % kD;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wml[(w * kMaxG + gg) * 2]);
-        float L = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float f = exp2f(wml[(w * kMaxG + gg) * 2] - M);
-            L += wml[(w * kMaxG + gg) * 2 + 1] * f;
-            acc += wo[(w * kMaxG + gg) * kD + dd] * f;
-          }
-        }
-        slot[2 * kMaxG + gg * kD + dd] = acc;
-        if (dd == 0) {
-          slot[gg] = M;
-          slot[kMaxG + gg] = L;
-        }
+      {
+        float* slot = P.part + size_t(c + pair) * kPartFloats + 2 * kMaxG;
+        for (int idx = tid; idx < G * kD; idx += kConsumerWarps * 32)
+          slot[idx] = ((wo[idx] + wo[kMaxG * kD + idx]) + wo[2 * kMaxG * kD + idx]) + wo[3 * kMaxG * kD + idx];
+        __threadfence();
       }
       consumer_sync();
+      if (tid == 0) atomicAdd(P.pair_v + pair, 1u);
       u = seg_end;
     }
   }
 
-  // ---- announce: this CTA's partials (and logits) for its pairs are written ----
-  // No grid barrier: phase B of a pair waits only for that pair's owners.
+  // ================= O = the sum of the pair's partial O =================
   __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (tid == 0) {
-    for (long long u = u0; u < u1;) {
-      int b, kvh, pg;
-      loc.locate(u, b, kvh, pg);
-      const int pair = b * Hkv + kvh;
-      // the first owner gives the pair a fresh H2O candidate list before anyone can append
-      if (P.link_count && pg == 0) P.link_count[pair] = 0u;
-      __threadfence();
-      atomicAdd(P.pair_cnt + pair, 1u);
-      u = min(u1, u + (loc.pages(b) - pg));
-    }
-  }
-
-  // ================= phase B =================
-  uint32_t* sLink = reinterpret_cast<uint32_t*>(smem + SmemLayout::link);  // staged count, list base
-  uint32_t* stKey = reinterpret_cast<uint32_t*>(smem + SmemLayout::ring);  // the idle TMA ring
-  int32_t* stPos = reinterpret_cast<int32_t*>(smem + SmemLayout::ring + kStageCands * 4);
   if (c == 0) {
     for (int b = 0; b < P.B; ++b)  // sequences without keys: O = 0
       if (sS[b] == 0)
@@ -514,183 +698,38 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(0.f);
         }
   }
-  long long u = u0;
 #pragma unroll 1
-  while (u < u1) {
+  for (long long u = u0; u < u1;) {
     int b, kvh, pg;
     loc.locate(u, b, kvh, pg);
-    const int S = sS[b];
     const int np = loc.pages(b);
     const long long seg_end = min(u1, u + (np - pg));
     const int pair = b * Hkv + kvh;
-    const long long pfirst = sPref[b] + (long long)kvh * np, plast = pfirst + np - 1;
-    const int cf = cta_of(pfirst, U, NC);
-    // The CTAs owning units of this pair, in order: cf, then the owner of the
-    // unit right after each owner's range, up to the pair's last unit.
     if (tid == 0) {
-      int no = 0;
-      for (int cc = cf; cc >= 0 && no < kMaxOwners; ++no) {
-        sOwn[no] = cc;
-        const long long nu = U * (cc + 1) / NC;
-        cc = nu > plast ? -1 : cta_of(nu, U, NC);
-      }
-      sOwn[kMaxOwners] = no;
-      sLink[0] = 0u;
-      // every owner of the pair has announced: its partials are complete
-      if (wait_word(P.pair_cnt + pair, unsigned(no), P.status) &&
-          atomicAdd(P.pair_pass + pair, 1u) + 1u == unsigned(no)) {
-        P.pair_cnt[pair] = 0u;  // every owner is past the wait: reset for the next launch
-        P.pair_pass[pair] = 0u;
+      const long long pfirst = sPref[b] + (long long)kvh * np;
+      const int no = list_owners(sOwn, pfirst, pfirst + np - 1, U, NC);
+      // every owner's O is written; the last owner past the wait resets the pair's counters
+      if (wait_word(P.pair_v + pair, unsigned(no), P.status) &&
+          atomicAdd(P.pair_done + pair, 1u) + 1u == unsigned(no)) {
+        P.pair_k[pair] = 0u;
+        P.pair_v[pair] = 0u;
+        P.pair_done[pair] = 0u;
       }
     }
     __syncthreads();
     const int nown = sOwn[kMaxOwners];
-    // every owner's (m, l) per head, fetched in parallel into the idle TMA ring
-    float* sM = reinterpret_cast<float*>(smem + SmemLayout::ring);  // [kMaxOwners][kMaxG]
-    float* sL = sM + kMaxOwners * kMaxG;
-    for (int i = tid; i < nown * G; i += kThreads) {
-      const int k = i / G, g = i - k * G;
-      const float* sl = P.part + size_t(sOwn[k] + pair) * kPartFloats;
-      sM[k * kMaxG + g] = __ldcg(sl + g);
-      sL[k * kMaxG + g] = __ldcg(sl + kMaxG + g);
-    }
-    __syncthreads();
-    if (tid < G) {
-      float M = -INFINITY;
-      for (int k = 0; k < nown; ++k) M = fmaxf(M, sM[k * kMaxG + tid]);
-      float L = 0.f;
-      for (int k = 0; k < nown; ++k) {
-        const float m = sM[k * kMaxG + tid];
-        if (m != -INFINITY) L += sL[k * kMaxG + tid] * exp2f(m - M);
-      }
-      sStat[tid * 2] = M;
-      sStat[tid * 2 + 1] = L > 0.f ? 1.f / L : 0.f;
-    }
-    __syncthreads();
-    {  // O = the rescaled sum of the partials: each owner merges its share of the G x 128 outputs
-      int kme = 0;
-      while (kme < nown - 1 && sOwn[kme] != c) ++kme;
-      const int E = G * kD;
-      const int e1 = (kme + 1) * E / nown;
-      for (int idx = kme * E / nown + tid; idx < e1; idx += kThreads) {
-        const int gg = idx / kD, dd = idx % kD;
-        const float M = sStat[gg * 2];
-        float acc = 0.f;
+    int kme = 0;
+    while (kme < nown - 1 && sOwn[kme] != c) ++kme;
+    const int E = G * kD;
+    const int e1 = (kme + 1) * E / nown;
+    for (int idx = kme * E / nown + tid; idx < e1; idx += kThreads) {
+      float acc = 0.f;
 #pragma unroll 4
-        for (int k = 0; k < nown; ++k) {
-          const float m = sM[k * kMaxG + gg];
-          if (m != -INFINITY)
-            acc += __ldcg(P.part + size_t(sOwn[k] + pair) * kPartFloats + 2 * kMaxG + gg * kD + dd) * exp2f(m - M);
-        }
-        const float v = acc * sStat[gg * 2 + 1];
-        const size_t oi = (size_t(b) * P.Hq + kvh * G + gg) * kD + dd;
-        if (P.out_f32) static_cast<float*>(P.out)[oi] = v;
-        else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(v);
-      }
-    }
-    __syncthreads();  // the ring is reused for the H2O candidate stage below
-    if (P.logits) {
-      const int j0 = pg * kPage;
-      const int j1 = min(S, int(pg + (seg_end - u)) * kPage);
-      const size_t row0 = (size_t(b) * P.Hq + kvh * G) * P.max_len;
-      float* crow = P.cum ? P.cum + (size_t(b) * Hkv + kvh) * P.max_len : nullptr;
-      // the row's last H2O threshold: collect the slots at or above it (0: no list)
-      const uint32_t hk = (crow && P.link_hint) ? __ldcg(P.link_hint + pair) : 0u;
-      float Mg[kMaxG], Ig[kMaxG];
-#pragma unroll
-      for (int gg = 0; gg < kMaxG; ++gg) {
-        Mg[gg] = gg < G ? sStat[gg * 2] : 0.f;
-        Ig[gg] = gg < G ? sStat[gg * 2 + 1] : 0.f;
-      }
-      if (P.vec4) {
-        // 4 keys x all heads per thread, two such groups per iteration: up to 16
-        // independent 16-byte loads in flight per thread (a third group would
-        // not fit the 168 registers that two CTAs per SM leave each thread)
-        auto group = [&](int j, float4 (&lg)[kMaxG]) {
-#pragma unroll
-          for (int gg = 0; gg < kMaxG; ++gg)
-            if (gg < G)
-              lg[gg] = __ldcg(reinterpret_cast<const float4*>(P.logits + row0 + size_t(gg) * P.max_len + j));
-        };
-        auto finish = [&](int j, const float4 (&lg)[kMaxG], float4 old) {
-          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int gg = 0; gg < kMaxG; ++gg)
-            if (gg < G) {
-              float4 pj;
-              pj.x = exp2f(lg[gg].x - Mg[gg]) * Ig[gg];
-              pj.y = exp2f(lg[gg].y - Mg[gg]) * Ig[gg];
-              pj.z = exp2f(lg[gg].z - Mg[gg]) * Ig[gg];
-              pj.w = exp2f(lg[gg].w - Mg[gg]) * Ig[gg];
-              if (P.probs) __stcg(reinterpret_cast<float4*>(P.probs + row0 + size_t(gg) * P.max_len + j), pj);
-              sum.x += pj.x;
-              sum.y += pj.y;
-              sum.z += pj.z;
-              sum.w += pj.w;
-            }
-          if (crow) {
-            if (append && j + 3 >= S - 1) {  // the appended slot starts from zero
-              if (j == S - 1) old.x = 0.f;
-              if (j + 1 == S - 1) old.y = 0.f;
-              if (j + 2 == S - 1) old.z = 0.f;
-              if (j + 3 == S - 1) old.w = 0.f;
-            }
-            const float4 nv = make_float4(old.x + sum.x, old.y + sum.y, old.z + sum.z, old.w + sum.w);
-            __stcg(reinterpret_cast<float4*>(crow + j), nv);
-            if (hk) link_stage<4>(stKey, stPos, sLink, j, nv, hk);
-          }
-        };
-        const int jend = j0 + ((j1 - j0) & ~3);
-        for (int j = j0 + 4 * tid; j < jend; j += 8 * kThreads) {
-          const int jb = j + 4 * kThreads;
-          const bool has_b = jb < jend;
-          float4 la[kMaxG], lb[kMaxG];
-          group(j, la);
-          if (has_b) group(jb, lb);
-          float4 oa = make_float4(0.f, 0.f, 0.f, 0.f), ob = oa;
-          if (crow) {
-            oa = __ldcg(reinterpret_cast<const float4*>(crow + j));
-            if (has_b) ob = __ldcg(reinterpret_cast<const float4*>(crow + jb));
-          }
-          finish(j, la, oa);
-          if (has_b) finish(jb, lb, ob);
-        }
-      }
-      // keys left over (the whole segment when rows are not 16-byte aligned), one per thread
-      const int jr = P.vec4 ? j0 + ((j1 - j0) & ~3) : j0;
-      for (int jj = jr + tid; jj < j1; jj += kThreads) {
-        float sum = 0.f;
-#pragma unroll
-        for (int gg = 0; gg < kMaxG; ++gg)
-          if (gg < G) {
-            const size_t li = row0 + size_t(gg) * P.max_len + jj;
-            const float pj = exp2f(__ldcg(P.logits + li) - Mg[gg]) * Ig[gg];
-            if (P.probs) P.probs[li] = pj;
-            sum += pj;
-          }
-        if (crow) {
-          const float old = (append && jj == S - 1) ? 0.f : crow[jj];
-          const float nv = old + sum;
-          crow[jj] = nv;
-          if (hk) link_stage<1>(stKey, stPos, sLink, jj, make_float4(nv, 0.f, 0.f, 0.f), hk);
-        }
-      }
-      if (hk) {  // hand this segment's candidates to the row's list: one global atomic
-        __syncthreads();
-        const uint32_t n = sLink[0];
-        if (tid == 0)  // an overflowing stage invalidates the row's list (count > capacity)
-          sLink[1] = atomicAdd(P.link_count + pair, n > uint32_t(kStageCands) ? uint32_t(kLinkCap) + 1u : n);
-        __syncthreads();
-        const uint32_t base = sLink[1];
-        if (n <= uint32_t(kStageCands)) {
-          uint32_t* gk = P.link_key + size_t(pair) * kLinkCap;
-          int32_t* gp = P.link_pos + size_t(pair) * kLinkCap;
-          for (uint32_t i = tid; i < n && base + i < uint32_t(kLinkCap); i += kThreads) {
-            gk[base + i] = stKey[i];
-            gp[base + i] = stPos[i];
-          }
-        }
-      }
+      for (int k = 0; k < nown; ++k)
+        acc += __ldcg(P.part + size_t(sOwn[k] + pair) * kPartFloats + 2 * kMaxG + idx);
+      const size_t oi = (size_t(b) * P.Hq + kvh * G) * kD + idx;
+      if (P.out_f32) static_cast<float*>(P.out)[oi] = acc;
+      else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(acc);
     }
     __syncthreads();
     u = seg_end;
@@ -725,12 +764,12 @@ struct DecodeWs {
 };
 
 // The finish counter lives in the workspace's status area (byte 64); the
-// per-pair readiness counters follow it.
+// three per-pair readiness counters follow it.
 DecodeWs decode_ws_layout(int batch, int Hkv, int Hq, int max_len, bool with_probs) {
   DecodeWs w;
   size_t off = kStatusBytes;
   w.pair_off = off;
-  off = align_up(off + size_t(batch) * Hkv * 2 * sizeof(unsigned), 256);
+  off = align_up(off + size_t(batch) * Hkv * 3 * sizeof(unsigned), 256);
   w.part_off = off;
   off = align_up(off + (size_t(kMaxCtas) + size_t(batch) * Hkv) * kPartFloats * sizeof(float), 256);
   w.logit_off = off;
@@ -832,7 +871,7 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   P.v_pool = static_cast<__nv_bfloat16*>(kv->v_pool);
   P.pos_map = pos_map;
   P.next_pos = next_pos;
-  P.logits = probs ? probs : (h2o_cum ? reinterpret_cast<float*>(ws + L.logit_off) : nullptr);
+  P.logits = probs ? probs : reinterpret_cast<float*>(ws + L.logit_off);
   P.probs = probs;
   P.cum = h2o_cum;
   P.link_hint = P.link_count = P.link_key = nullptr;
@@ -847,8 +886,9 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   P.out = out;
   P.part = reinterpret_cast<float*>(ws + L.part_off);
   P.fin = reinterpret_cast<unsigned*>(ws + 64);
-  P.pair_cnt = reinterpret_cast<unsigned*>(ws + L.pair_off);
-  P.pair_pass = P.pair_cnt + size_t(batch) * Hkv;
+  P.pair_k = reinterpret_cast<unsigned*>(ws + L.pair_off);
+  P.pair_v = P.pair_k + size_t(batch) * Hkv;
+  P.pair_done = P.pair_v + size_t(batch) * Hkv;
   P.status = reinterpret_cast<int*>(ws);
   P.B = batch;
   P.max_pages = max_pages;
@@ -858,8 +898,7 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   P.num_pages = kv->num_pages;
   P.max_len = max_len;
   P.out_f32 = out_dtype == KVSEL_F32;
-  P.vec_logits = (max_len % 2 == 0) && aligned(P.logits, 8);
-  P.vec4 = (max_len % 4 == 0) && aligned(P.logits, 16) && (!h2o_cum || aligned(h2o_cum, 16));
+  P.vec2 = (max_len % 2 == 0) && aligned(P.logits, 8) && (!h2o_cum || aligned(h2o_cum, 8));
   P.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

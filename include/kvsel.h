@@ -170,8 +170,8 @@ KVSEL_API size_t kvsel_h2o_link_bytes(int batch, int num_kv_heads);
  *    the device current); make that first call before any stream capture.
  *  - Calls that need more scratch than 8 MiB are rejected with
  *    KVSEL_ERR_INVALID_ARG: about (1024 + batch * num_kv_heads) * 4160 bytes
- *    + batch * num_kv_heads * 8 bytes, plus batch * num_q_heads * max_len * 4
- *    bytes when h2o_cum is given without probs.
+ *    + batch * num_kv_heads * 12 bytes, plus batch * num_q_heads * max_len * 4
+ *    bytes when probs is not given (the kernel keeps its logits there).
  *  - Every call uses the same array, so calls that overlap on the GPU (other
  *    streams, other threads) race and corrupt each other; serialise them.
  *    Each call clears the array's status word and counters first.
