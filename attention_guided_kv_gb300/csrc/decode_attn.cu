@@ -29,7 +29,8 @@
 //     (m, l) per head to a partial slot and announces the pair (a per-pair
 //     counter).
 //   * V pass: per segment, once every owner of the pair has announced
-//     (bounded spin; the launch is cooperative, so all CTAs are co-resident),
+//     (bounded spin; the grid is at most the co-resident CTA count, and by
+//     the end of a K pass every CTA has started),
 //     the pair's exact (M, L) per head are merged from the owners' slots.
 //     Every page then turns its stored logits into final probabilities
 //     p = exp2(s - M) / L, writes them (evict-first), adds the group's sum
@@ -517,13 +518,26 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       }
       __threadfence();  // the slot and this segment's logits
       consumer_sync();
-      if (tid == 0) {
+      u = seg_end;
+    }
+
+    // The kernel before this one in the stream (an H2O select, when it lets
+    // this launch start early) reads the H2O scores and candidate lists that
+    // the V pass writes, and writes the thresholds it reads: only the K pass
+    // overlaps it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // announce: this CTA's (m, l) partials (and logits) for its pairs are written
+    if (tid == 0) {
+      for (long long u = u0; u < u1;) {
+        int b, kvh, pg;
+        loc.locate(u, b, kvh, pg);
+        const int pair = b * Hkv + kvh;
         // the first owner gives the pair a fresh H2O candidate list before anyone can append
         if (P.link_count && pg == 0) P.link_count[pair] = 0u;
         __threadfence();
         atomicAdd(P.pair_k + pair, 1u);
+        u = min(u1, u + (loc.pages(b) - pg));
       }
-      u = seg_end;
     }
 
     // ================= V pass =================
@@ -907,9 +921,14 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
+  // No cooperative attribute: that would hold the launch until the whole grid
+  // fits at once.  The grid is at most the co-resident CTA count, and its
+  // cross-CTA waits come after the K pass, when every CTA is resident.  The
+  // launch may start while the previous kernel runs if that kernel allows it
+  // (the H2O select does); the kernel waits for it before its V pass.
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   trace_before("decode_step", st);

@@ -49,11 +49,14 @@ constexpr int kListWords = 1024;  // list path: rows of up to 32768 candidate sl
 
 struct SelSmem {
   RowTopkSmem rk;
-  int32_t upos[kRkUpMax];           // listed slots (relative to n_sink)
+  int32_t upos[kRkUpMax];           // listed slots (then relative to the candidate range)
   uint32_t bits[2][kListWords];     // kept-above / tie bitmaps over the candidate slots
   uint32_t m, minkey, bad;
+  uint64_t bar;                     // completion of the list's bulk copy
 };
 static_assert(kRkUpMax >= kLinkCap, "every listed slot fits in shared memory");
+static_assert(offsetof(RowTopkSmem, ukey) % 16 == 0 && offsetof(SelSmem, upos) % 16 == 0,
+              "bulk copies land on 16-byte boundaries");
 
 __device__ __forceinline__ uint32_t lowest_bits(uint32_t x, uint32_t n) {
   uint32_t r = 0;
@@ -83,64 +86,54 @@ __device__ __forceinline__ bool select_from_list(const SelectParams& P, size_t r
   const uint32_t* lk = P.link.key + rowi * kLinkCap;
   const int32_t* lp = P.link.pos + rowi * kLinkCap;
   const int nw = (hi - lo + 31) >> 5;
+  const uint32_t bar = smem_u32(&sm.bar);
   if (tid == 0) {
     sm.m = 0;
     sm.rk.maxkey = 0;
     sm.minkey = 0xFFFFFFFFu;
+    mbar_init(bar, 1);
+    mbar_fence_init();
   }
   for (int i = tid; i < nw; i += kSelThreads) sm.bits[0][i] = sm.bits[1][i] = 0u;
   __syncthreads();
-  uint32_t lt;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
-  uint32_t mx = 0, mn = 0xFFFFFFFFu, bad = 0;
-  const uint32_t cnt_r = (cnt + 31u) & ~31u;
-  // four entries per thread in flight per batch (the loads of a batch overlap)
-#pragma unroll 1
-  for (uint32_t i0 = 0; i0 < cnt_r; i0 += 4 * kSelThreads) {
-    uint32_t key[4];
-    int pos[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t i = i0 + j * kSelThreads + tid;
-      key[j] = 0u;
-      pos[j] = -1;
-      if (i < cnt) {
-        key[j] = __ldcg(lk + i);
-        pos[j] = __ldcg(lp + i);
-      }
-    }
-    if (i0 == 0 && tid < cnt) {  // freshness: the listed score must still be the row's score
-      if (pos[0] < 0 || pos[0] >= P.max_len) bad = 1;
-      else bad |= order_key(__ldcg(row + pos[0])) != key[0];
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t i = i0 + j * kSelThreads + tid;
-      if (i0 + j * kSelThreads + uint32_t(tid & ~31) >= cnt_r) break;  // uniform over the warp
-      bool v = false;
-      if (i < cnt) {
-        if (pos[j] < 0 || pos[j] >= P.max_len) bad = 1;
-        v = pos[j] >= lo && pos[j] < hi;
-      }
-      const uint32_t bal = __ballot_sync(0xffffffffu, v);
-      if (bal) {
-        uint32_t base = 0;
-        if (lane == 0) base = atomicAdd(&sm.m, uint32_t(__popc(bal)));
-        base = __shfl_sync(0xffffffffu, base, 0) + __popc(bal & lt);
-        if (v) {
-          sm.rk.ukey[base] = key[j];
-          sm.upos[base] = pos[j] - lo;
-          mx = max(mx, key[j]);
-          mn = min(mn, key[j]);
-        }
-      }
+  if (tid == 0) {  // the whole list into shared memory: two bulk copies (rows are 64 KB apart)
+    const uint32_t bytes = (cnt * 4u + 15u) & ~15u;
+    mbar_expect_tx(bar, 2u * bytes);
+    bulk_load(smem_u32(sm.rk.ukey), lk, bytes, bar);
+    bulk_load(smem_u32(sm.upos), lp, bytes, bar);
+  }
+  // freshness, while the copies run: the first listed scores must still be the row's
+  uint32_t bad = 0;
+  if (uint32_t(tid) < cnt) {
+    const uint32_t key = __ldcg(lk + tid);
+    const int pos = __ldcg(lp + tid);
+    if (pos < 0 || pos >= P.max_len) bad = 1;
+    else bad |= order_key(__ldcg(row + pos)) != key;
+  }
+  if (!mbar_wait(bar, 0u, P.status)) bad = 1;
+  // one sweep: entries outside [lo, hi) get key 0 (skipped from here on), the
+  // others their slot relative to lo; count, smallest and largest key
+  uint32_t mx = 0, mn = 0xFFFFFFFFu, n_in = 0;
+  for (uint32_t i = tid; i < cnt; i += kSelThreads) {
+    const uint32_t key = sm.rk.ukey[i];
+    const int pos = sm.upos[i];
+    if (pos < 0 || pos >= P.max_len) bad = 1;
+    if (pos >= lo && pos < hi) {
+      sm.upos[i] = pos - lo;
+      mx = max(mx, key);
+      mn = min(mn, key);
+      ++n_in;
+    } else {
+      sm.rk.ukey[i] = 0u;
     }
   }
   mx = __reduce_max_sync(0xffffffffu, mx);
   mn = __reduce_min_sync(0xffffffffu, mn);
+  n_in = __reduce_add_sync(0xffffffffu, n_in);
   if (lane == 0) {
     if (mx) atomicMax(&sm.rk.maxkey, mx);
     atomicMin(&sm.minkey, mn);
+    atomicAdd(&sm.m, n_in);
   }
   if (__syncthreads_or(bad)) return false;
   const uint32_t m = sm.m;
@@ -151,18 +144,19 @@ __device__ __forceinline__ bool select_from_list(const SelectParams& P, size_t r
     T = lo_key;
     need_eq = uint32_t(k);
   } else {
-    const uint32_t m_r = (m + 31u) & ~31u;
+    const uint32_t c_r = (cnt + 31u) & ~31u;
     rk_radix(
         [&](auto&& f) {
-          for (uint32_t i = tid; i < m_r; i += kSelThreads) {
-            const bool live = i < m;
+          for (uint32_t i = tid; i < c_r; i += kSelThreads) {
+            const bool live = i < cnt;
             f(live ? sm.rk.ukey[i] : 0u, live);
           }
         },
         31 - __clz(lo_key ^ hi_key), lo_key, uint32_t(k), sm.rk, T, need_eq);
   }
-  for (uint32_t i = tid; i < m; i += kSelThreads) {
+  for (uint32_t i = tid; i < cnt; i += kSelThreads) {
     const uint32_t u = sm.rk.ukey[i];
+    if (u == 0u) continue;  // outside the candidate range
     const int r = sm.upos[i];
     if (u > T) atomicOr(&sm.bits[0][r >> 5], 1u << (r & 31));
     else if (u == T) atomicOr(&sm.bits[1][r >> 5], 1u << (r & 31));
@@ -200,6 +194,10 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
   __shared__ int s_first;
   __shared__ uint32_t s_cnt;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the scores come from the previous kernel
+  // A decode step launched after this kernel may start now: it touches the
+  // scores, the candidate lists and the thresholds only after waiting for
+  // this kernel to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x;
@@ -239,6 +237,9 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
     if (kout) kout[o] = prow ? prow[slot] : slot;
     if (slot != o) first = min(first, o);
   };
+  // the sinks and the window do not depend on the selection: written first
+  for (int i = tid; i < P.n_sink; i += kSelThreads) put(i, i);
+  for (int i = tid; i < P.window; i += kSelThreads) put(P.budget - P.window + i, S - P.window + i);
   if (k > 0) {
     const int lo = P.n_sink, hi = S - P.window;
     const uint32_t hk = P.link.hint[rowi];
@@ -256,8 +257,6 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
     }
     if (tid == 0) P.link.hint[rowi] = T;
   }
-  for (int i = tid; i < P.n_sink; i += kSelThreads) put(i, i);
-  for (int i = tid; i < P.window; i += kSelThreads) put(P.budget - P.window + i, S - P.window + i);
   if (first < P.budget) atomicMin(&s_first, first);
   __syncthreads();
   if (tid == 0) {
