@@ -296,7 +296,11 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   const int Hkv = P.Hkv, G = P.G;
 
   // ---- lengths, unit prefix, this CTA's range ----
-  for (int b = tid; b < P.B; b += kThreads) sS[b] = P.seq_lens[b] + (append ? 1 : 0);
+  // Lengths, positions and the block table are read before this kernel waits
+  // for the previous one (see the K pass end), so they are read from L2, which
+  // holds every completed kernel's writes (a compaction that precedes this
+  // launch lets it start only once it has completed).
+  for (int b = tid; b < P.B; b += kThreads) sS[b] = __ldcg(P.seq_lens + b) + (append ? 1 : 0);
   __syncthreads();
   if (tid == 0) {
     long long acc = 0;
@@ -338,7 +342,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       for (int kvh = 0; kvh < Hkv; ++kvh) {
         const long long ua = sPref[b] + (long long)kvh * np + S_old / kPage;
         if (ua < u0 || ua >= u1) continue;
-        const int phys = P.block_table[size_t(b) * P.max_pages + S_old / kPage];
+        const int phys = __ldcg(P.block_table + size_t(b) * P.max_pages + S_old / kPage);
         if (unsigned(phys) < unsigned(P.num_pages)) {
           const size_t row = (size_t(phys) * Hkv + kvh) * kPage + (S_old % kPage);
           const int t = tid & 15;
@@ -349,7 +353,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           report(P.status, KVSEL_ERR_BAD_INDEX);
         }
         if (tid == 0 && P.pos_map)
-          P.pos_map[(size_t(b) * Hkv + kvh) * P.max_len + S_old] = P.next_pos ? P.next_pos[b] : S_old;
+          P.pos_map[(size_t(b) * Hkv + kvh) * P.max_len + S_old] = P.next_pos ? __ldcg(P.next_pos + b) : S_old;
       }
     }
     fence_proxy_async_global();
@@ -384,7 +388,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (i >= n) return -1;
         int b, kvh, pg;
         loc.locate(u0 + i, b, kvh, pg);
-        int phys = P.block_table[size_t(b) * P.max_pages + pg];
+        int phys = __ldcg(P.block_table + size_t(b) * P.max_pages + pg);
         if (unsigned(phys) >= unsigned(P.num_pages)) {
           report(P.status, KVSEL_ERR_BAD_INDEX);
           phys = 0;

@@ -292,6 +292,9 @@ __global__ void __launch_bounds__(256) h2o_compact_kernel(const CompactParams P)
   __shared__ float sc[kChunk];
   __shared__ int32_t sp[kChunk];
   const int kvh = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  // launched early (programmatic serialization): the kept lists come from the select
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the truncation waits for this kernel
   const int S = P.seq_lens[b];
   if (S <= P.budget) return;
   if (S > P.max_len || S > P.max_pages * kPg) {
@@ -345,6 +348,10 @@ struct TruncateParams {
 
 __global__ void __launch_bounds__(256) h2o_truncate_kernel(const TruncateParams P) {
   const int b = blockIdx.x;
+  // launched early (programmatic serialization): runs once the compaction is
+  // done.  It does not let the next kernel start early: a decode step reads
+  // the lengths and block table written here.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int S = P.seq_lens[b];
   if (S > P.max_len) return;
   const int n_keep = S > P.budget ? P.budget : S;
@@ -466,8 +473,10 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   C.num_pages = kv->num_pages;
   C.budget = budget;
   trace_before("h2o_compact", st);
-  h2o_compact_kernel<<<dim3(kv->num_kv_heads, batch), 256, 0, st>>>(C);
-  e = cudaGetLastError();
+  cfg.gridDim = dim3(kv->num_kv_heads, batch);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, h2o_compact_kernel, C);  // programmatic serialization, like the select
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_h2o_evict (compact launch)");
 
@@ -479,8 +488,10 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   T.budget = budget;
   T.max_len = max_len;
   trace_before("h2o_truncate", st);
-  h2o_truncate_kernel<<<batch, 256, 0, st>>>(T);
-  e = cudaGetLastError();
+  cfg.gridDim = dim3(batch);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, h2o_truncate_kernel, T);
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_h2o_evict (truncate launch)");
   return KVSEL_OK;
