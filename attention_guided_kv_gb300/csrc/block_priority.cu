@@ -21,7 +21,7 @@
 //                     rank gives the percentile key of each block.
 //   bp_sort_kernel    cooperative: stable LSD radix sort of the N 32-bit keys
 //                     (4-bit digits, 8 passes, two bounded grid barriers per
-//                     pass).  The input is in (request, block) order and the
+//                     pass; the 16 digit offsets of a CTA are scanned at once).  The input is in (request, block) order and the
 //                     sort is stable, so equal keys keep (request, block)
 //                     order, which is the specified tie-break.  The first
 //                     ceil(frac * N) codes go to the output.
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
   __shared__ unsigned cnt[16][kBpSortThreads];
   __shared__ unsigned base[16];
   __shared__ unsigned sTot[kBpSortThreads / 16][16], sBefore[kBpSortThreads / 16][16];
-  __shared__ unsigned warp_tot[kBpSortThreads / 32 + 1];
+  __shared__ unsigned wtot[kBpSortThreads / 32][16];
   const long long N = P.meta[0];
   if (N < 0) return;  // same for every CTA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -277,36 +277,44 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
     const int64_t* iv = P.val[pass & 1];
     uint32_t* ok = P.key[(pass + 1) & 1];
     int64_t* ov = P.val[(pass + 1) & 1];
-    for (int d = 0; d < 16; ++d) cnt[d][tid] = 0;
-    for (long long e = t0; e < t1; ++e) ++cnt[(ik[e] >> shift) & 15u][tid];
-    __syncthreads();
-    // per digit: exclusive scan over threads (thread order = input order)
+    // this thread's digit counts (its keys are a contiguous run of the input)
+    unsigned v[16];
+#pragma unroll
+    for (int d = 0; d < 16; ++d) v[d] = 0u;
+    for (long long e = t0; e < t1; ++e) {
+      const unsigned dd = (ik[e] >> shift) & 15u;
+#pragma unroll
+      for (int d = 0; d < 16; ++d) v[d] += dd == unsigned(d) ? 1u : 0u;
+    }
+    // all 16 digits scanned at once: inclusive over the warp's lanes, then the
+    // 8 warp totals of each digit by one thread per digit
+    unsigned x[16];
+#pragma unroll
     for (int d = 0; d < 16; ++d) {
-      const unsigned v = cnt[d][tid];
-      unsigned x = v;
+      x[d] = v[d];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const unsigned y = __shfl_up_sync(0xffffffffu, x[d], o);
+        if (lane >= o) x[d] += y;
       }
-      if (lane == 31) warp_tot[warp] = x;
-      __syncthreads();
-      if (warp == 0) {
-        const unsigned t = lane < kBpSortThreads / 32 ? warp_tot[lane] : 0u;
-        unsigned s = t;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned y = __shfl_up_sync(0xffffffffu, s, o);
-          if (lane >= o) s += y;
-        }
-        if (lane < kBpSortThreads / 32) warp_tot[lane] = s - t;
-        if (lane == 31) warp_tot[kBpSortThreads / 32] = s;
-      }
-      __syncthreads();
-      cnt[d][tid] = warp_tot[warp] + x - v;  // exclusive offset inside this CTA
-      if (tid == 0) P.hist[c * 16 + d] = warp_tot[kBpSortThreads / 32];
-      __syncthreads();
     }
+    if (lane == 31) {
+#pragma unroll
+      for (int d = 0; d < 16; ++d) wtot[warp][d] = x[d];
+    }
+    __syncthreads();
+    if (tid < 16) {
+      unsigned run = 0;
+      for (int w = 0; w < kBpSortThreads / 32; ++w) {
+        const unsigned t = wtot[w][tid];
+        wtot[w][tid] = run;
+        run += t;
+      }
+      P.hist[c * 16 + tid] = run;  // this CTA's count of digit tid
+    }
+    __syncthreads();
+#pragma unroll
+    for (int d = 0; d < 16; ++d) cnt[d][tid] = wtot[warp][d] + x[d] - v[d];  // exclusive offset inside this CTA
     bp_grid_barrier(P.bar, P.status);
     {
       // start of digit d for this CTA = all keys with a smaller digit + this

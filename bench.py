@@ -738,6 +738,7 @@ def other_workload(args, rank, world):
     torch.cuda.synchronize()
     tw0 = time.time()
     ms, durs, per_step_launches = timed_steps(S["step"], args.warmup, steps, stream, S["per_step_launches"])
+    tw1 = time.time()
     eager_ms = None
     if S.get("graph_cycle") and not args.no_graph:
         # Launch-bound loop: the same K steps captured once in a CUDA graph and
