@@ -16,9 +16,10 @@
 //                     evict count; checks every length against the limits.
 //   bp_fold_kernel    one warp per block (grid-stride): decay update of the
 //                     block's tokens (written back) and the fold.
-//   bp_rank_kernel    one CTA per request (percentile only): bitonic sort of
-//                     the request's (score, block) keys in shared memory; the
-//                     rank gives the percentile key of each block.
+//   bp_rank_kernel    one CTA per request (percentile only): stable radix sort
+//                     of the request's scores with block indices (up to 8192
+//                     blocks; a register bitonic sort above that); the rank
+//                     gives the percentile key of each block.
 //   bp_sort_kernel    cooperative: stable LSD radix sort of the N 32-bit keys
 //                     (4-bit digits, 8 passes, two bounded grid barriers per
 //                     pass; the 16 digit offsets of a CTA are scanned at once).  The input is in (request, block) order and the
@@ -196,6 +197,189 @@ __global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
   }
 }
 
+// Bitonic sort of one request's (score key << 32 | block) keys, E per thread
+// in registers (element i = thread * E + e): compare-exchanges inside a
+// thread in registers, inside a warp through shuffles, and only those
+// between warps through shared memory (one barrier pair each), then each
+// block's percentile from its sorted position.
+template <int E>
+__device__ __forceinline__ void bp_rank_sort(unsigned long long* sk, int npow, int n, long long b0, int r,
+                                             const BpParams& P) {
+  const int tid = threadIdx.x;
+  const bool act = tid * E < npow;
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = tid * E + e;
+    v[e] = (act && i < n) ? ((unsigned long long)order_key(P.bscore[b0 + i]) << 32) | unsigned(i) : ~0ull;
+  }
+#pragma unroll 1
+  for (int kk = 2; kk <= npow; kk <<= 1) {
+#pragma unroll 1
+    for (int jj = kk >> 1; jj >= E; jj >>= 1) {
+      if (jj < 32 * E) {  // partner in another lane of this warp
+        const int lx = jj / E;
+        const bool lower = (tid & lx) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const unsigned long long p = __shfl_xor_sync(0xffffffffu, v[e], lx);
+          const bool up = ((tid * E + e) & kk) == 0;
+          v[e] = (up == lower) ? (v[e] < p ? v[e] : p) : (v[e] > p ? v[e] : p);
+        }
+      } else {  // partner in another warp
+        __syncthreads();
+        if (act) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) sk[tid * E + e] = v[e];
+        }
+        __syncthreads();
+        if (act) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int i = tid * E + e;
+            const unsigned long long p = sk[i ^ jj];
+            const bool up = (i & kk) == 0, lower = (i & jj) == 0;
+            v[e] = (up == lower) ? (v[e] < p ? v[e] : p) : (v[e] > p ? v[e] : p);
+          }
+        }
+      }
+    }
+    // partners in this thread: distances below E, unrolled so v stays in registers
+#pragma unroll
+    for (int jb = E / 2; jb >= 1; jb >>= 1) {
+      if (jb < kk) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int l = e ^ jb;
+          if (l > e) {
+            const bool up = ((tid * E + e) & kk) == 0;
+            const unsigned long long x = v[e], y = v[l];
+            const bool sw = up ? (x > y) : (x < y);
+            v[e] = sw ? y : x;
+            v[l] = sw ? x : y;
+          }
+        }
+      }
+    }
+  }
+  if (act) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = tid * E + e;
+      if (i < n) {
+        const unsigned blk = unsigned(v[e] & 0xffffffffu);
+        const float pct = __fdiv_rn(float(2 * i + 1), float(2 * n));  // correctly rounded
+        P.key[0][b0 + blk] = __float_as_uint(pct);                    // pct > 0: bits are monotone
+        P.val[0][b0 + blk] = ((long long)r << 32) | blk;
+      }
+    }
+  }
+}
+
+// Stable LSD radix sort of one request's score keys (n <= 8192, 8-bit digits,
+// 4 passes) with the block index as the value, then each block's percentile
+// from its sorted position.  Thread t of warp w holds keys w*256 + e*32 + lane
+// (e < 8), so a warp meets its keys in index order; per pass each warp ranks
+// its keys among equal digits with match_any into a warp-private histogram
+// column, one scan over (digit, warp) turns the columns into offsets, and the
+// keys are scattered.  Equal scores keep block order, the specified tie-break.
+constexpr int kRankRadixMax = 8192;
+struct RankRadixSmem {
+  uint32_t key[2][kRankRadixMax];
+  uint16_t idx[2][kRankRadixMax];
+  uint32_t hist[256 * 32];  // [digit][warp]
+  uint32_t wsum[32];
+};
+__device__ __forceinline__ void bp_rank_radix(RankRadixSmem& sm, int n, long long b0, int r, const BpParams& P) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+  uint32_t k[8];
+  uint16_t v[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int i = warp * 256 + e * 32 + lane;
+    k[e] = i < n ? order_key(P.bscore[b0 + i]) : 0xFFFFFFFFu;  // padding sorts last
+    v[e] = uint16_t(i);
+  }
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 8 * pass;
+    for (int j = tid; j < 256 * 32; j += 1024) sm.hist[j] = 0u;
+    __syncthreads();
+    uint32_t pos[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t d = (k[e] >> shift) & 255u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      const int leader = __ffs(peers) - 1;
+      uint32_t old = 0;
+      if (lane == leader) {
+        old = sm.hist[d * 32 + warp];
+        sm.hist[d * 32 + warp] = old + __popc(peers);
+      }
+      pos[e] = __shfl_sync(0xffffffffu, old, leader) + __popc(peers & lt);
+    }
+    __syncthreads();
+    {  // exclusive scan of the 8192 counts in (digit, warp) order: 8 per thread
+      uint32_t c[8], run = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sm.hist[tid * 8 + j];
+        run += c[j];
+      }
+      uint32_t incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) sm.wsum[warp] = incl;
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t t = sm.wsum[lane];
+        uint32_t x = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        sm.wsum[lane] = x - t;
+      }
+      __syncthreads();
+      uint32_t base = sm.wsum[warp] + incl - run;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sm.hist[tid * 8 + j] = base;
+        base += c[j];
+      }
+    }
+    __syncthreads();
+    const int ob = pass & 1;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t d = (k[e] >> shift) & 255u;
+      const uint32_t dst = sm.hist[d * 32 + warp] + pos[e];
+      sm.key[ob][dst] = k[e];
+      sm.idx[ob][dst] = v[e];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int i = warp * 256 + e * 32 + lane;
+      k[e] = sm.key[ob][i];
+      v[e] = sm.idx[ob][i];
+    }
+  }
+  // after 4 passes position i holds the block of rank i (buffer 1)
+  for (int i = tid; i < n; i += 1024) {
+    const unsigned blk = sm.idx[1][i];
+    const float pct = __fdiv_rn(float(2 * i + 1), float(2 * n));  // correctly rounded
+    P.key[0][b0 + blk] = __float_as_uint(pct);                    // pct > 0: bits are monotone
+    P.val[0][b0 + blk] = ((long long)r << 32) | blk;
+  }
+}
+
 __global__ void __launch_bounds__(1024) bp_rank_kernel(const BpParams P) {
   extern __shared__ unsigned long long skeys[];
   if (P.meta[0] <= 0) return;
@@ -203,32 +387,18 @@ __global__ void __launch_bounds__(1024) bp_rank_kernel(const BpParams P) {
   const long long b0 = P.blk_off[r];
   const int n = int(P.blk_off[r + 1] - b0);
   if (n == 0) return;
+  if (n <= kRankRadixMax) {
+    bp_rank_radix(*reinterpret_cast<RankRadixSmem*>(skeys), n, b0, r, P);
+    return;
+  }
   int npow = 1;
   while (npow < n) npow <<= 1;
-  for (int i = threadIdx.x; i < npow; i += blockDim.x)
-    skeys[i] = i < n ? ((unsigned long long)order_key(P.bscore[b0 + i]) << 32) | unsigned(i)
-                     : ~0ull;
-  __syncthreads();
-  for (int kk = 2; kk <= npow; kk <<= 1)
-    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-      for (int i = threadIdx.x; i < npow; i += blockDim.x) {
-        const int l = i ^ jj;
-        if (l > i) {
-          const unsigned long long x = skeys[i], y = skeys[l];
-          const bool up = (i & kk) == 0;
-          if (up ? (x > y) : (x < y)) {
-            skeys[i] = y;
-            skeys[l] = x;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const unsigned blk = unsigned(skeys[i] & 0xffffffffu);
-    const float pct = __fdiv_rn(float(2 * i + 1), float(2 * n));  // correctly rounded
-    P.key[0][b0 + blk] = __float_as_uint(pct);                    // pct > 0: bits are monotone
-    P.val[0][b0 + blk] = ((long long)r << 32) | blk;
+  switch (npow <= 1024 ? 1 : npow / 1024) {  // keys per thread (bitonic, requests above 8192 blocks)
+    case 1: bp_rank_sort<1>(skeys, npow, n, b0, r, P); break;
+    case 2: bp_rank_sort<2>(skeys, npow, n, b0, r, P); break;
+    case 4: bp_rank_sort<4>(skeys, npow, n, b0, r, P); break;
+    case 8: bp_rank_sort<8>(skeys, npow, n, b0, r, P); break;
+    default: bp_rank_sort<16>(skeys, npow, n, b0, r, P); break;
   }
 }
 
@@ -475,7 +645,7 @@ extern "C" kvsel_status kvsel_block_priority(float* token_scores, const float* i
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_block_priority (fold launch)");
 
   if (norm == KVSEL_NORM_PERCENTILE) {
-    const size_t smem = size_t(kBpMaxReqBlocks) * 8;
+    const size_t smem = std::max(size_t(kBpMaxReqBlocks) * 8, sizeof(RankRadixSmem));
     static bool attr_set = false;
     if (!attr_set) {
       e = cudaFuncSetAttribute(bp_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
