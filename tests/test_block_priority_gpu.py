@@ -94,6 +94,21 @@ def test_max_aggregation_order_is_exact_end_to_end(norm):
     np.testing.assert_array_equal(order, want)
 
 
+@pytest.mark.parametrize("nblocks", [8192, 8193, 12500, 16384])
+def test_percentile_ranks_at_and_above_8192_blocks(nblocks):
+    """Requests of up to 8192 blocks are ranked by the shared-memory radix sort,
+    larger ones by the register bitonic sort: both must give the oracle's order."""
+    rng = np.random.default_rng(nblocks)
+    lens = np.array([nblocks * 16 - 7, 300, nblocks * 16], dtype=np.int64)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    tok = (rng.integers(0, 500, int(off[-1])) * 0.125).astype(np.float32)   # ties across blocks
+    _, blk, order, _ = _run(tok, off, 16, BP.AGG_MAX, BP.NORM_PERCENTILE, 0.3)
+    blocks, normed, want = BP.priority_pass(tok.astype(np.float64), off, 16, BP.AGG_MAX, 0.1,
+                                            BP.NORM_PERCENTILE, 0.3)
+    np.testing.assert_array_equal(blk, np.concatenate(blocks).astype(np.float32))
+    np.testing.assert_array_equal(order, want)
+
+
 def test_edge_cases():
     # single-token requests, an empty request, frac 0 and 1
     off = np.array([0, 1, 1, 5, 37], dtype=np.int64)
