@@ -516,9 +516,11 @@ def _setup_snapkv(dev, small=False):
     rows = wl.G * wl.W
     qk_flops = 2.0 * rows * wl.S * wl.d * pairs
     kbytes = wl.S * wl.d * 2 * pairs
+    # one exp2 per (window row, key) in each pass: the special-function unit bounds both
+    ex2 = {"snap_stats": float(rows) * wl.S * pairs, "snap_vote": float(rows) * (wl.S - wl.W) * pairs}
     return dict(step=step, run=run, host_in=[("q_obs", q[None])], outs=[keep], ws=[ws],
                 bytes={"snap_stats": kbytes, "snap_vote": kbytes}, flops={"snap_stats": qk_flops,
-                "snap_vote": 2.0 * rows * (wl.S - wl.W) * wl.d * pairs}, per_step_launches=4,
+                "snap_vote": 2.0 * rows * (wl.S - wl.W) * wl.d * pairs}, ex2=ex2, per_step_launches=4,
                 config={"layers": wl.L, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "prompt": wl.S,
                         "obs_window": wl.W, "keep": wl.keep_k, "pool_kernel": wl.pool_kernel,
                         "l2": "inputs larger than L2 (940 MB of K per pass)"})
@@ -827,7 +829,23 @@ def other_workload(args, rank, world):
         return
     hbm, peak_kind = peaks()
     kms = kern_ms[dominant]
-    if dominant in S["flops"] and S["flops"][dominant]:
+    if dominant in S.get("ex2", {}):
+        # bound by the special-function unit: one exp2 per element, 16 per clock per SM
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                mp = json.load(f)
+            tf, clk, tk = float(mp["bf16_tflops"]), float(mp["sm_max_mhz"]), "measured"
+        except Exception:
+            tf, clk, tk = 1900.0, 2070.0, "fallback"
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mufu = sms * 16 * clk * 1e6 / 1e9  # G exp2 / s
+        ach = S["ex2"][dominant] / (kms / 1e3) / 1e9
+        tach = S["flops"][dominant] / (kms / 1e3) / 1e12
+        roof = {"bound": "alu", "kernel": dominant, "achieved": ach, "peak": mufu, "peak_kind":
+                f"derived: {sms} SMs x 16 exp2/clock x {clk:.0f} MHz", "unit": "Gexp2/s", "frac": ach / mufu,
+                "traffic": None, "tensor_achieved_tflops": tach, "tensor_frac_of_" + tk + "_bf16": tach / tf,
+                "hbm_achieved_gbs": S["bytes"][dominant] / (kms / 1e3) / 1e9}
+    elif dominant in S["flops"] and S["flops"][dominant]:
         try:
             with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
                 tf = float(json.load(f)["bf16_tflops"])
