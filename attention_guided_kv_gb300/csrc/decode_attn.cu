@@ -14,13 +14,13 @@
 // co-resident CTAs finishes together).  A CTA's range covers one or a few
 // pairs; each covered piece of a pair is a "segment".
 //
-// Each CTA (5 warps) streams its range twice, K pages first, then V pages:
-// warp 4 is the producer, TMA-loading two pages of K (or of V) of its kv
-// head per 8 KB stage -- one 3D load per 4 KB page, two 128-byte-swizzled
-// 64-column halves -- into an 8-stage ring, evict-first in L2; warps 0..3
-// take the ring's stages round-robin.  (The producer's issue loop costs a
-// fixed few hundred cycles per stage, so stages of one page could not keep
-// up with HBM.)
+// Each CTA (6 warps) streams its range twice, K pages first, then V pages:
+// warps 4 and 5 are producers, TMA-loading two pages of K (or of V) of its
+// kv head per 8 KB stage -- one 3D load per 4 KB page, two 128-byte-swizzled
+// 64-column halves -- into an 8-stage ring, evict-first in L2, alternating
+// stages; warps 0..3 take the ring's stages round-robin.  (A producer's
+// issue loop costs a fixed few hundred cycles per stage, so one-page stages
+// or a single producer warp could not keep up with HBM.)
 //   * K pass: S = Q K^T with mma.sync m16n8k16 (A = the group's q rows, at
 //     most 8 real; B = 16 keys via ldmatrix); the scaled log2-domain logits
 //     are stored to the probability buffer, marked evict-last so they are
@@ -58,7 +58,8 @@ constexpr int kD = 128;            // head_dim
 constexpr int kPage = 16;          // tokens per page
 constexpr int kStages = 8;         // TMA ring depth (two pages of K or of V per stage)
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarps = 2;  // alternate stages: the issue loop's fixed cost is halved per warp
+constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kPageBytes = 4096;   // 16 rows x 128 bf16, as two 2 KB swizzled halves
 constexpr int kStageBytes = 2 * kPageBytes;
 constexpr int kMaxG = 8;
@@ -67,6 +68,7 @@ constexpr int kMaxCtas = 1024;
 // ring depth that is a multiple of the warp count a stage is always used by
 // the same warp and its parity wait cannot pass on a later lap's phase.
 static_assert(kStages % kConsumerWarps == 0, "ring depth must be a multiple of the consumer warps");
+static_assert(kStages % kProducerWarps == 0, "a ring slot must always have the same producer");
 constexpr int kMaxBatch = 1024;
 constexpr int kPartFloats = kMaxG * (kD + 2);  // one partial slot: m[8], l[8], O[8][128]
 constexpr int kMaxOwners = kMaxCtas;           // CTAs sharing one (sequence, kv head) pair
@@ -377,11 +379,13 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   };
   auto next_page = [](int i) -> int { return (i & 1) ? i + 2 * kConsumerWarps - 1 : i + 1; };
 
-  if (warp == kConsumerWarps) {
-    // ================= producer =================
+  if (warp >= kConsumerWarps) {
+    // ================= producers =================
+    // Producer warp pw fills the stages t with t % kProducerWarps == pw.
     // Every lane resolves one page of a 32-page chunk (block table entry ->
     // TMA row coordinate), two chunks ahead of use, so the dependent
     // block-table loads never sit between two TMA issues.
+    const int pw = warp - kConsumerWarps;
     if (n > 0) {
       const uint64_t pol = l2_policy_evict_first();
       auto resolve = [&](int i) -> int {  // TMA row of CTA-local page i (or -1 past the end)
@@ -407,6 +411,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll 1
           for (int k = 0; k < 32 && i0 + k < n; k += 2) {
             const int t = pass * nsk + ((i0 + k) >> 1);
+            if (t % kProducerWarps != pw) continue;  // the other producer's stage
             const int ya = __shfl_sync(0xffffffffu, y_cur, k);
             const int yb = __shfl_sync(0xffffffffu, y_cur, k + 1);
             const bool two = i0 + k + 1 < n;
