@@ -24,8 +24,9 @@ KVSEL_ERR_TIMEOUT = 4
 KVSEL_ERR_BAD_INDEX = 5
 KVSEL_BF16 = 0
 KVSEL_F32 = 1
-KVSEL_AGG_MAX, KVSEL_AGG_MEAN, KVSEL_AGG_TOPP = 0, 1, 2
+KVSEL_AGG_MAX, KVSEL_AGG_MEAN, KVSEL_AGG_TOPP, KVSEL_AGG_FRAC_HOT, KVSEL_AGG_ALL_COLD = 0, 1, 2, 3, 4
 KVSEL_NORM_NONE, KVSEL_NORM_PERCENTILE = 0, 1
+KVSEL_UPDATE_DECAY, KVSEL_UPDATE_MAX, KVSEL_UPDATE_WINDOW = 0, 1, 2
 
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT", 5: "BAD_INDEX"}
 
@@ -41,6 +42,11 @@ class PagedKV(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("num_q_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_size", ctypes.c_int32)]
+
+
+class BpOptions(ctypes.Structure):
+    _fields_ = [("update", ctypes.c_int), ("history", ctypes.c_void_p), ("window", ctypes.c_int),
+                ("step", ctypes.c_int64), ("history_tokens", ctypes.c_int64), ("threshold", ctypes.c_float)]
 
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -65,6 +71,8 @@ _SIGS = {
     "kvsel_block_priority_workspace": (_sz, [_i, ctypes.c_int64]),
     "kvsel_block_priority": (_i, [_vp, _vp, _f, _vp, _i, _i, _i, _f, _i, _f, _vp, ctypes.c_int64, _vp,
                                   ctypes.c_int64, _vp, _vp, _sz, _vp]),
+    "kvsel_block_priority_ex": (_i, [_vp, _vp, _f, _vp, _i, _i, _i, _f, _i, _f, _vp, ctypes.c_int64, _vp,
+                                     ctypes.c_int64, _vp, _vp, _sz, ctypes.POINTER(BpOptions), _vp]),
     "kvsel_sparse_decode_workspace": (_sz, [_PKV, _i, _i, _i, _i]),
     "kvsel_sparse_decode": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i,
                                  _i, _f, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
@@ -288,21 +296,26 @@ def kvsel_block_priority_workspace(num_requests: int, max_total_blocks: int) -> 
 
 def kvsel_block_priority(token_scores, req_offsets, order_out, n_out, workspace, *, block_size, agg,
                          norm, evict_frac, increment=None, decay=1.0, top_p=0.1, block_score_out=None,
-                         max_total_blocks=None, stream=None):
-    """Decay update + token->block fold + per-request percentile + global evict order."""
+                         max_total_blocks=None, update=KVSEL_UPDATE_DECAY, history=None, window=1, step=0,
+                         threshold=0.0, stream=None):
+    """Score update (decay, max over steps or sliding-window sum) + token->block fold + per-request
+    percentile + global evict order (kvsel_block_priority_ex)."""
     _need(token_scores, torch.float32, "token_scores")
     _need(increment, torch.float32, "increment", True)
+    _need(history, torch.float32, "history", True)
     _need(req_offsets, torch.int64, "req_offsets")
     _need(order_out, torch.int64, "order_out")
     _need(n_out, torch.int64, "n_out")
     _need(block_score_out, torch.float32, "block_score_out", True)
     if max_total_blocks is None:
         max_total_blocks = block_score_out.numel() if block_score_out is not None else token_scores.numel()
-    _check(lib().kvsel_block_priority(
+    opt = BpOptions(int(update), _ptr(history), int(window), int(step),
+                    (history.numel() // max(1, int(window))) if history is not None else 0, float(threshold))
+    _check(lib().kvsel_block_priority_ex(
         _ptr(token_scores), _ptr(increment), float(decay), _ptr(req_offsets), req_offsets.numel() - 1,
         int(block_size), int(agg), float(top_p), int(norm), float(evict_frac), _ptr(block_score_out),
         int(max_total_blocks), _ptr(order_out), order_out.numel(), _ptr(n_out), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        workspace.numel() * workspace.element_size(), ctypes.byref(opt), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------

@@ -1,10 +1,14 @@
 // Block offload priority from per-token attention scores (sm_103a).
 //
 // What it computes ("Sparse attention x KV-cache offloading: eight
-// questions" §2.1, §3.1, §3.2, §5.1): optionally age every token score by
-// exponential decay and add this step's attention (score <- decay * score +
-// increment), fold the tokens of each block into one block score (max, mean,
-// or the mean of the ceil(p * n) largest of the block's n valid tokens),
+// questions" §2.1, §3.1, §3.2, §5.1; "From sliding window to attention-guided
+// eviction" §5.1): optionally update every token score with this step's
+// attention -- exponential decay (score <- decay * score + increment), max
+// over steps, or the exact sum over a sliding window of steps --, fold the
+// tokens of each block into one block score (max, mean, the mean of the
+// ceil(p * n) largest of the block's n valid tokens, the fraction of its
+// tokens at or above a hotness threshold, or the max with only all-cold
+// blocks evictable),
 // normalise per request (the block's percentile inside its own request,
 // fp32(2r + 1) / fp32(2n) for rank r by (score asc, block asc), or no
 // normalisation), and emit the global eviction order: every block of every
@@ -46,14 +50,20 @@ struct BpParams {
   float* bscore;             // workspace [max_blocks]
   uint32_t* key[2];          // workspace [max_blocks] x 2
   int64_t* val[2];           // workspace [max_blocks] x 2
-  int64_t* meta;             // workspace [2]: N (or -1), evict count
+  int64_t* meta;             // workspace [3]: N (or -1), evict count, evictable (all-cold) blocks
   unsigned* hist;            // workspace [kBpMaxSortCtas][16]
   unsigned* bar;             // grid-barrier words
   int* status;
   int64_t max_blocks, order_cap;
-  int R, bs, agg, norm;
-  float decay, top_p, frac;
+  float* whist;              // WINDOW update: [window][hist_tokens] past increments
+  long long step, hist_tokens;
+  int R, bs, agg, norm, update, window;
+  float decay, top_p, frac, threshold;
 };
+
+// aggregations (kvsel_block_agg; 2 = top-p mean) and updates (kvsel_score_update; 0 = decay)
+constexpr int kAggMax = 0, kAggMean = 1, kAggFracHot = 3, kAggAllCold = 4;
+constexpr int kUpdMax = 1, kUpdWindow = 2;
 
 __device__ __forceinline__ int bp_request_of(const int64_t* blk_off, int R, int64_t g) {
   int lo = 0, hi = R - 1;  // last r with blk_off[r] <= g
@@ -107,6 +117,8 @@ __global__ void __launch_bounds__(1024) bp_prefix_kernel(const BpParams P) {
   if (tid == 0) {
     P.blk_off[P.R] = carry;
     if (!bad && carry > P.max_blocks) bad = KVSEL_ERR_BAD_INDEX;
+    if (!bad && P.inc && P.update == kUpdWindow && P.off[P.R] > P.hist_tokens) bad = KVSEL_ERR_BAD_INDEX;
+    P.meta[2] = 0;
     const long long n_evict = bad ? 0 : (long long)ceil((double)P.frac * (double)carry);
     if (bad) report(P.status, bad);
     P.meta[0] = bad ? -1 : carry;
@@ -135,7 +147,16 @@ __global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
       if (t < n) {
         float s = P.tok[t0 + t];
         if (P.inc) {
-          s = fmaf(P.decay, s, P.inc[t0 + t]);
+          const float in = P.inc[t0 + t];
+          if (P.update == kUpdMax) {
+            s = fmaxf(s, in);
+          } else if (P.update == kUpdWindow) {  // the increment leaving the window is replaced
+            float* h = P.whist + (P.step % P.window) * P.hist_tokens + t0 + t;
+            s = s + (in - *h);
+            *h = in;
+          } else {
+            s = fmaf(P.decay, s, in);
+          }
           P.tok[t0 + t] = s;
         }
         v[e] = s;
@@ -144,11 +165,18 @@ __global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
       }
     }
     float result;
-    if (P.agg == 0) {
+    if (P.agg == kAggMax || P.agg == kAggAllCold) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       result = mx;
-    } else if (P.agg == 1) {
+    } else if (P.agg == kAggFracHot) {  // fraction of valid tokens at or above the threshold
+      int hot = 0;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) hot += (lane + 32 * e < n && v[e] >= P.threshold) ? 1 : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) hot += __shfl_xor_sync(0xffffffffu, hot, o);
+      result = __fdiv_rn(float(hot), float(n));
+    } else if (P.agg == kAggMean) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       result = __fdiv_rn(sum, float(n));
@@ -189,8 +217,10 @@ __global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
     if (lane == 0) {
       P.bscore[g] = result;
       if (P.bscore_out) P.bscore_out[g] = result;
+      const bool hot_block = P.agg == kAggAllCold && result >= P.threshold;  // never evicted
+      if (P.agg == kAggAllCold && !hot_block) atomicAdd(reinterpret_cast<unsigned long long*>(P.meta + 2), 1ull);
       if (P.norm == 0) {  // no normalisation: sort directly on the block score
-        P.key[0][g] = order_key(result);
+        P.key[0][g] = hot_block ? 0xFFFFFFFFu : order_key(result);
         P.val[0][g] = ((long long)r << 32) | (g - P.blk_off[r]);
       }
     }
@@ -269,7 +299,8 @@ __device__ __forceinline__ void bp_rank_sort(unsigned long long* sk, int npow, i
       if (i < n) {
         const unsigned blk = unsigned(v[e] & 0xffffffffu);
         const float pct = __fdiv_rn(float(2 * i + 1), float(2 * n));  // correctly rounded
-        P.key[0][b0 + blk] = __float_as_uint(pct);                    // pct > 0: bits are monotone
+        const bool hot_block = P.agg == kAggAllCold && P.bscore[b0 + blk] >= P.threshold;
+        P.key[0][b0 + blk] = hot_block ? 0xFFFFFFFFu : __float_as_uint(pct);  // pct > 0: bits are monotone
         P.val[0][b0 + blk] = ((long long)r << 32) | blk;
       }
     }
@@ -375,7 +406,8 @@ __device__ __forceinline__ void bp_rank_radix(RankRadixSmem& sm, int n, long lon
   for (int i = tid; i < n; i += 1024) {
     const unsigned blk = sm.idx[1][i];
     const float pct = __fdiv_rn(float(2 * i + 1), float(2 * n));  // correctly rounded
-    P.key[0][b0 + blk] = __float_as_uint(pct);                    // pct > 0: bits are monotone
+    const bool hot_block = P.agg == kAggAllCold && P.bscore[b0 + blk] >= P.threshold;
+    P.key[0][b0 + blk] = hot_block ? 0xFFFFFFFFu : __float_as_uint(pct);  // pct > 0: bits are monotone
     P.val[0][b0 + blk] = ((long long)r << 32) | blk;
   }
 }
@@ -529,7 +561,12 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
     bp_grid_barrier(P.bar, P.status);
   }
   // 8 passes: the sorted keys are back in buffer 0
-  const long long n_ev = min(P.meta[1], P.order_cap);
+  long long n_all = P.meta[1];
+  if (P.agg == kAggAllCold) {  // only the evictable blocks (they sort first)
+    n_all = min(n_all, (long long)P.meta[2]);
+    if (c == 0 && tid == 0) P.n_out[0] = n_all;
+  }
+  const long long n_ev = min(n_all, (long long)P.order_cap);
   for (long long i = (long long)c * kBpSortThreads + tid; i < n_ev; i += (long long)NC * kBpSortThreads)
     P.order_out[i] = __ldcg(P.val[0] + i);
 }
@@ -557,7 +594,7 @@ BpWs bp_ws_layout(int R, long long max_blocks) {
   w.key1 = take(size_t(max_blocks) * 4);
   w.val0 = take(size_t(max_blocks) * 8);
   w.val1 = take(size_t(max_blocks) * 8);
-  w.meta = take(16);
+  w.meta = take(24);
   w.hist = take(size_t(kBpMaxSortCtas) * 16 * 4);
   w.total = off;
   return w;
@@ -575,21 +612,46 @@ extern "C" kvsel_status kvsel_block_priority(float* token_scores, const float* i
                                              float* block_score_out, int64_t max_total_blocks,
                                              int64_t* order_out, int64_t order_capacity, int64_t* n_out,
                                              void* workspace, size_t ws_bytes, void* stream) {
+  if (agg == KVSEL_AGG_FRAC_HOT || agg == KVSEL_AGG_ALL_COLD)
+    return fail(KVSEL_ERR_INVALID_ARG, "kvsel_block_priority: the threshold aggregations need kvsel_block_priority_ex");
+  return kvsel_block_priority_ex(token_scores, increment, decay, req_offsets, num_requests, block_size, agg, top_p,
+                                 norm, evict_frac, block_score_out, max_total_blocks, order_out, order_capacity,
+                                 n_out, workspace, ws_bytes, nullptr, stream);
+}
+
+extern "C" kvsel_status kvsel_block_priority_ex(float* token_scores, const float* increment, float decay,
+                                                const int64_t* req_offsets, int num_requests, int block_size,
+                                                int agg, float top_p, int norm, float evict_frac,
+                                                float* block_score_out, int64_t max_total_blocks,
+                                                int64_t* order_out, int64_t order_capacity, int64_t* n_out,
+                                                void* workspace, size_t ws_bytes, const kvsel_bp_options* opt,
+                                                void* stream) {
   const std::string fn = "kvsel_block_priority: ";
+  kvsel_bp_options o = {};
+  o.update = KVSEL_UPDATE_DECAY;
+  if (opt) o = *opt;
+  if (o.update < KVSEL_UPDATE_DECAY || o.update > KVSEL_UPDATE_WINDOW)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "update must be KVSEL_UPDATE_DECAY, _MAX or _WINDOW");
+  if (increment && o.update == KVSEL_UPDATE_WINDOW &&
+      (!o.history || o.window < 1 || o.step < 0 || o.history_tokens < 1 || !aligned(o.history, 4)))
+    return fail(KVSEL_ERR_INVALID_ARG,
+                fn + "the window update needs history, window >= 1, step >= 0 and history_tokens >= 1");
+  if ((agg == KVSEL_AGG_FRAC_HOT || agg == KVSEL_AGG_ALL_COLD) && !(o.threshold == o.threshold))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "threshold must be a number");
   if (!token_scores || !req_offsets || !n_out || num_requests < 1 || max_total_blocks < 1)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "token_scores, req_offsets, n_out are required; num_requests, "
                                             "max_total_blocks >= 1");
   if (block_size < 1 || block_size > kBpMaxBlockSize)
     return fail(KVSEL_ERR_UNSUPPORTED, fn + "block_size must be in [1, 256]");
-  if (agg < KVSEL_AGG_MAX || agg > KVSEL_AGG_TOPP)
-    return fail(KVSEL_ERR_INVALID_ARG, fn + "agg must be KVSEL_AGG_MAX, _MEAN or _TOPP");
+  if (agg < KVSEL_AGG_MAX || agg > KVSEL_AGG_ALL_COLD)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "agg must be KVSEL_AGG_MAX, _MEAN, _TOPP, _FRAC_HOT or _ALL_COLD");
   if (norm != KVSEL_NORM_NONE && norm != KVSEL_NORM_PERCENTILE)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "norm must be KVSEL_NORM_NONE or KVSEL_NORM_PERCENTILE");
   if (agg == KVSEL_AGG_TOPP && !(top_p > 0.f && top_p <= 1.f))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "top_p must be in (0, 1]");
   if (!(evict_frac >= 0.f && evict_frac <= 1.f))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "evict_frac must be in [0, 1]");
-  if (increment && !(decay == decay))
+  if (increment && o.update == KVSEL_UPDATE_DECAY && !(decay == decay))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "decay must be a number");
   if (order_capacity < 0 || (order_capacity > 0 && !order_out))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "order_out is required when order_capacity > 0");
@@ -628,6 +690,12 @@ extern "C" kvsel_status kvsel_block_priority(float* token_scores, const float* i
   P.decay = decay;
   P.top_p = top_p;
   P.frac = evict_frac;
+  P.update = o.update;
+  P.whist = o.history;
+  P.window = o.window > 0 ? o.window : 1;
+  P.step = o.step;
+  P.hist_tokens = o.history_tokens;
+  P.threshold = o.threshold;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;

@@ -259,7 +259,13 @@ KVSEL_API kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block_
  * KVSEL_ERR_BAD_INDEX; more than 16384 blocks in one request ->
  * KVSEL_ERR_UNSUPPORTED; in both cases nothing else is computed.
  */
-typedef enum kvsel_block_agg { KVSEL_AGG_MAX = 0, KVSEL_AGG_MEAN = 1, KVSEL_AGG_TOPP = 2 } kvsel_block_agg;
+typedef enum kvsel_block_agg {
+  KVSEL_AGG_MAX = 0,
+  KVSEL_AGG_MEAN = 1,
+  KVSEL_AGG_TOPP = 2,
+  KVSEL_AGG_FRAC_HOT = 3, /* fraction of the block's valid tokens with score >= threshold */
+  KVSEL_AGG_ALL_COLD = 4  /* the max; only blocks whose max is < threshold may be evicted */
+} kvsel_block_agg;
 typedef enum kvsel_block_norm { KVSEL_NORM_NONE = 0, KVSEL_NORM_PERCENTILE = 1 } kvsel_block_norm;
 KVSEL_API size_t kvsel_block_priority_workspace(int num_requests, int64_t max_total_blocks);
 KVSEL_API kvsel_status kvsel_block_priority(float* token_scores, const float* increment, float decay,
@@ -269,6 +275,49 @@ KVSEL_API kvsel_status kvsel_block_priority(float* token_scores, const float* in
                                             int64_t max_total_blocks, int64_t* order_out,
                                             int64_t order_capacity, int64_t* n_out, void* workspace,
                                             size_t ws_bytes, void* stream);
+
+/* Temporal aggregation and block policies beyond kvsel_block_priority
+ * ("Sparse attention x KV-cache offloading: eight questions" §2.1: sliding-
+ * window average, exponential decay, max pooling over steps; "From sliding
+ * window to attention-guided eviction" §5.1: order blocks by their fraction
+ * of important tokens, or evict only blocks whose tokens are all cold).
+ * kvsel_block_priority_ex takes the arguments of kvsel_block_priority plus
+ * `opt` (host pointer; NULL = decay update, threshold unused):
+ *   update   KVSEL_UPDATE_DECAY: score[t] = fmaf(decay, score[t], increment[t]);
+ *            KVSEL_UPDATE_MAX:   score[t] = max(score[t], increment[t]);
+ *            KVSEL_UPDATE_WINDOW: the sum of the last `window` increments,
+ *            kept exactly: slot = step % window, score[t] += increment[t] -
+ *            history[slot][t], history[slot][t] = increment[t] (the window
+ *            average is score / window, which orders blocks the same way).
+ *            Every update mode needs `increment`; without it no update runs.
+ *   history  fp32 [window][history_tokens] (device), zero before step 0.
+ *   window   >= 1; step >= 0; history_tokens >= the total token count, else
+ *            KVSEL_ERR_BAD_INDEX is recorded on the device and nothing is
+ *            computed.
+ *   threshold  AGG_FRAC_HOT / AGG_ALL_COLD: a token is hot when its score is
+ *            >= threshold.  With AGG_ALL_COLD the order holds evictable
+ *            blocks only and n_out[0] = min(ceil(evict_frac * N), their
+ *            count); block_score_out holds the max. */
+typedef enum kvsel_score_update {
+  KVSEL_UPDATE_DECAY = 0,
+  KVSEL_UPDATE_MAX = 1,
+  KVSEL_UPDATE_WINDOW = 2
+} kvsel_score_update;
+typedef struct kvsel_bp_options {
+  int update;
+  float* history;
+  int window;
+  int64_t step;
+  int64_t history_tokens;
+  float threshold;
+} kvsel_bp_options;
+KVSEL_API kvsel_status kvsel_block_priority_ex(float* token_scores, const float* increment, float decay,
+                                               const int64_t* req_offsets, int num_requests,
+                                               int block_size, int agg, float top_p, int norm,
+                                               float evict_frac, float* block_score_out,
+                                               int64_t max_total_blocks, int64_t* order_out,
+                                               int64_t order_capacity, int64_t* n_out, void* workspace,
+                                               size_t ws_bytes, const kvsel_bp_options* opt, void* stream);
 
 /* ---------------------------------------------------------------------------
  * DSA-style sparse decode: indexer scores, top-k, attention over the

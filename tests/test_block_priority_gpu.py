@@ -166,3 +166,64 @@ def test_full_size_64_requests_all_variants():
                 assert rel_l2(blk, want_blk) < TOL
             want = _expected_order(_split(blk, off, bs), BP.NORM_PERCENTILE, 0.25)
             np.testing.assert_array_equal(order, want)
+
+
+# --- temporal aggregation variants and block policies -----------------------
+def _run_ex(tok_dev, off, bs, agg, norm, frac, **kw):
+    dev = "cuda"
+    R = len(off) - 1
+    nblk = sum(int(-(-int(off[r + 1] - off[r]) // bs)) for r in range(R))
+    t_off = torch.from_numpy(np.asarray(off, dtype=np.int64)).to(dev)
+    bso = torch.full((nblk,), float("nan"), device=dev)
+    order = torch.full((max(1, math.ceil(frac * nblk)),), -7, dtype=torch.int64, device=dev)
+    n_out = torch.zeros(2, dtype=torch.int64, device=dev)
+    ws = K.workspace(K.kvsel_block_priority_workspace(R, nblk))
+    K.kvsel_block_priority(tok_dev, t_off, order, n_out, ws, block_size=bs, agg=agg, norm=norm,
+                           evict_frac=frac, block_score_out=bso, max_total_blocks=nblk, **kw)
+    assert K.read_status(ws) == 0
+    n_ev, N = n_out.cpu().tolist()
+    assert N == nblk
+    return bso.cpu().numpy(), order.cpu().numpy()[:n_ev]
+
+
+@pytest.mark.parametrize("update", [K.KVSEL_UPDATE_MAX, K.KVSEL_UPDATE_WINDOW])
+def test_max_and_window_updates_over_steps(update):
+    rng = np.random.default_rng(11 + update)
+    lens = rng.integers(1, 900, 6)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T, W, steps = int(off[-1]), 3, 7
+    tok = torch.zeros(T, device="cuda")
+    hist = torch.zeros(W, T, device="cuda")
+    incs = [rng.dirichlet(np.full(T, 0.5)).astype(np.float32) for _ in range(steps)]
+    want = np.zeros(T)
+    for t, inc in enumerate(incs):
+        blk, order = _run_ex(tok, off, 16, BP.AGG_MAX, BP.NORM_PERCENTILE, 0.25,
+                             increment=torch.from_numpy(inc).cuda(), update=update, history=hist,
+                             window=W, step=t)
+        if update == K.KVSEL_UPDATE_MAX:
+            want = BP.max_update(want, inc)
+        got = tok.cpu().numpy()
+        if update == K.KVSEL_UPDATE_MAX:
+            np.testing.assert_array_equal(got, want.astype(np.float32))       # max is exact
+        else:
+            assert rel_l2(got, BP.window_sum(incs[:t + 1], W)) < 1e-6
+        # the order on the GPU's own scores is exact
+        blocks, _, exp = BP.priority_pass(got.astype(np.float64), off, 16, BP.AGG_MAX, 0.1,
+                                          BP.NORM_PERCENTILE, 0.25)
+        np.testing.assert_array_equal(blk, np.concatenate(blocks).astype(np.float32))
+        np.testing.assert_array_equal(order, exp)
+
+
+@pytest.mark.parametrize("agg", [K.KVSEL_AGG_FRAC_HOT, K.KVSEL_AGG_ALL_COLD])
+@pytest.mark.parametrize("norm", [BP.NORM_NONE, BP.NORM_PERCENTILE])
+@pytest.mark.parametrize("bs", [16, 64])
+def test_threshold_policies_exact(agg, norm, bs):
+    rng = np.random.default_rng(3 + agg + 10 * norm + bs)
+    lens = rng.integers(1, 4000, 9)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    tok = (rng.integers(0, 64, int(off[-1])) * 0.015625).astype(np.float32)  # ties, exact in fp32
+    thr = 0.75
+    blk, order = _run_ex(torch.from_numpy(tok).cuda(), off, bs, agg, norm, 0.4, threshold=thr)
+    blocks, _, want = BP.priority_pass(tok.astype(np.float64), off, bs, agg, 0.1, norm, 0.4, threshold=thr)
+    np.testing.assert_array_equal(blk, np.concatenate(blocks).astype(np.float32))
+    np.testing.assert_array_equal(order, want)

@@ -99,3 +99,72 @@ def test_priority_pass_shapes():
     N = sum(len(b) for b in blk)
     assert len(order) == math.ceil(0.25 * N)
     assert [len(b) for b in blk] == [int(-(-L // 16)) for L in wl.lengths]
+
+
+# --- temporal aggregation variants and block policies -----------------------
+
+
+def test_window_sum_closed_forms():
+    # constant attention c every step: the window holds min(steps, W) copies
+    for W in range(1, 5):
+        for steps in range(1, 9):
+            got = BP.window_sum([np.full(3, 0.25)] * steps, W)
+            np.testing.assert_array_equal(got, np.full(3, 0.25 * min(steps, W)))
+    # hand example: increments 1, 2, 3, 4 -> last two sum to 7; a window longer
+    # than the history sums everything
+    seq = [np.array([float(x)]) for x in (1, 2, 3, 4)]
+    assert BP.window_sum(seq, 2)[0] == 7.0
+    assert BP.window_sum(seq, 10)[0] == 10.0
+    assert BP.window_sum(seq, 1)[0] == 4.0
+
+
+def test_window_ring_recurrence_equals_window_sum_exactly():
+    # the kernel's update (score += inc - history[step % W]; history[...] = inc,
+    # history and score starting at zero) reproduces the window sum; checked in
+    # exact rational arithmetic on a random sequence
+    rng = np.random.default_rng(7)
+    W, steps = 3, 11
+    incs = [rng.integers(0, 100, 5) for _ in range(steps)]
+    score = [Fraction(0)] * 5
+    hist = [[Fraction(0)] * 5 for _ in range(W)]
+    for t, inc in enumerate(incs):
+        for j in range(5):
+            score[j] += Fraction(int(inc[j])) - hist[t % W][j]
+            hist[t % W][j] = Fraction(int(inc[j]))
+        want = BP.window_sum([x.astype(np.float64) for x in incs[:t + 1]], W)
+        assert [float(x) for x in score] == list(want)
+
+
+def test_max_update_keeps_the_peak():
+    s = np.zeros(3)
+    for inc in ([1.0, -2.0, 0.5], [5.0, -3.0, 0.25], [3.0, -1.0, 0.75]):
+        s = BP.max_update(s, np.array(inc))
+    np.testing.assert_array_equal(s, [5.0, 0.0, 0.75])   # the zero start stays the floor
+
+
+def test_fraction_of_hot_tokens():
+    blk = np.array([0.1, 0.5, 0.9, 0.5, 0.2])
+    # block size 4: [0.1 .5 .9 .5] has 3 of 4 at >= 0.5; the partial block [0.2] has none
+    np.testing.assert_array_equal(BP.block_scores(blk, 4, BP.AGG_FRAC_HOT, threshold=0.5), [0.75, 0.0])
+    np.testing.assert_array_equal(BP.block_scores(blk, 4, BP.AGG_FRAC_HOT, threshold=-1.0), [1.0, 1.0])
+    np.testing.assert_array_equal(BP.block_scores(blk, 4, BP.AGG_FRAC_HOT, threshold=2.0), [0.0, 0.0])
+    # 1 of 3 is an fp32 division
+    assert BP.block_scores(np.array([1.0, 0.0, 0.0]), 3, BP.AGG_FRAC_HOT, threshold=0.5)[0] == \
+        np.float64(np.float32(1) / np.float32(3))
+
+
+def test_all_cold_evicts_only_cold_blocks():
+    # request 0 blocks (block size 2): maxes 0.2, 0.9, 0.1; request 1: 0.4, 0.6
+    tok = np.array([0.2, 0.1, 0.9, 0.3, 0.0, 0.1, 0.4, 0.4, 0.6, 0.0])
+    off = np.array([0, 6, 10])
+    blocks, normed, order = BP.priority_pass(tok, off, 2, BP.AGG_ALL_COLD, 0.1, BP.NORM_NONE, 1.0,
+                                             threshold=0.5)
+    np.testing.assert_array_equal(blocks[0], [0.2, 0.9, 0.1])
+    # cold blocks only, by max ascending: (0, 2) 0.1, (0, 0) 0.2, (1, 0) 0.4
+    np.testing.assert_array_equal(order, [(0 << 32) | 2, (0 << 32) | 0, (1 << 32) | 0])
+    # evict_frac 0.2 of N = 5 blocks -> ceil(1.0) = 1: the coldest only
+    _, _, order = BP.priority_pass(tok, off, 2, BP.AGG_ALL_COLD, 0.1, BP.NORM_NONE, 0.2, threshold=0.5)
+    np.testing.assert_array_equal(order, [(0 << 32) | 2])
+    # a threshold below every score leaves nothing evictable
+    _, _, order = BP.priority_pass(tok, off, 2, BP.AGG_ALL_COLD, 0.1, BP.NORM_NONE, 1.0, threshold=-1.0)
+    assert order.shape == (0,)
