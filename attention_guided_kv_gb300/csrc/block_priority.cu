@@ -134,6 +134,8 @@ __global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   constexpr int kPer = kBpMaxBlockSize / 32;
+  // sliding-window update: this step's slot of the history ring
+  float* const hslot = P.update == kUpdWindow ? P.whist + (P.step % P.window) * P.hist_tokens : nullptr;
   for (long long g = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < N; g += warps) {
     const int r = bp_request_of(P.blk_off, P.R, g);
     const long long t0 = P.off[r] + (g - P.blk_off[r]) * P.bs;
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
           if (P.update == kUpdMax) {
             s = fmaxf(s, in);
           } else if (P.update == kUpdWindow) {  // the increment leaving the window is replaced
-            float* h = P.whist + (P.step % P.window) * P.hist_tokens + t0 + t;
+            float* h = hslot + t0 + t;
             s = s + (in - *h);
             *h = in;
           } else {

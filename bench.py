@@ -541,8 +541,11 @@ def _setup_block_priority(dev, small=False):
     maxb = int(sum(-(-int(L) // 1) for L in wl.lengths))      # bound for every block size
     ws = K.workspace(K.kvsel_block_priority_workspace(wl.R, maxb))
     variant = dict(block_size=16, agg=K.KVSEL_AGG_MAX, norm=K.KVSEL_NORM_PERCENTILE)
+    hist = torch.zeros(8, wl.total_tokens, device=dev)   # sliding-window update: 8 steps
 
     def run(i, inc, **v):
+        if v.get("update") == K.KVSEL_UPDATE_WINDOW:
+            v = dict(v, history=hist, window=8, step=i)
         opts = dict(variant)
         opts.update(v)
         K.kvsel_block_priority(tok, off, order, n_out, ws, evict_frac=0.25, increment=inc, decay=0.98,
@@ -555,7 +558,7 @@ def _setup_block_priority(dev, small=False):
     byts = {"bp_fold": T * 12 + nblk * 4, "bp_rank": nblk * 12, "bp_sort": nblk * 12 * 2 * 8,
             "bp_prefix": wl.R * 16}
     return dict(step=step, run=run, host_in=[("increment", incs[0][None])], outs=[order, n_out], ws=[ws],
-                bytes=byts, flops={}, per_step_launches=4, extra_variants=True, nblk=nblk,
+                bytes=byts, flops={}, per_step_launches=4, extra_variants=True, nblk=nblk, incs=incs,
                 config={"requests": wl.R, "tokens": T, "blocks": nblk, "block_size": 16, "agg": "max",
                         "norm": "percentile", "evict_frac": 0.25,
                         "l2": "~9 MB of token scores per pass (fits in L2): latency-bound"})
@@ -820,6 +823,20 @@ def other_workload(args, rank, world):
         b2.record(stream)
         torch.cuda.synchronize()
         variants["bs16_max_with_decay_update"] = a.elapsed_time(b2) / 20 * 1e3
+        # the other temporal aggregations and the threshold block policies
+        for name, kw in (("bs16_max_with_max_update", dict(update=K.KVSEL_UPDATE_MAX)),
+                         ("bs16_max_with_window8_update", dict(update=K.KVSEL_UPDATE_WINDOW)),
+                         ("bs16_frac_hot", dict(agg=K.KVSEL_AGG_FRAC_HOT, threshold=1e-5)),
+                         ("bs16_all_cold", dict(agg=K.KVSEL_AGG_ALL_COLD, threshold=1e-5))):
+            upd = "update" in kw
+            torch.cuda.synchronize()
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(20):
+                S["run"](i, S["incs"][i % 4] if upd else None, **kw)
+            b2.record(stream)
+            torch.cuda.synchronize()
+            variants[name] = a.elapsed_time(b2) / 20 * 1e3
     clocks.stop()
     for w in S["ws"]:
         st = K.read_status(w)
