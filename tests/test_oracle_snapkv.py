@@ -84,3 +84,109 @@ def test_short_prefix_keeps_everything():
     q = rng.standard_normal((2, 4, 8))
     keep, _, _ = snapkv.snapkv_select(q, K, 0.3, keep_k=64)
     assert keep[0].tolist() == list(range(20))
+
+
+# ---- cold-start seed ("prefill attention as the seed score") ----
+
+def test_seed_of_each_group_sums_to_its_rows():
+    # every observation row is one softmax over the keys it sees: G*W in total
+    rng = np.random.default_rng(12)
+    K = rng.standard_normal((2, 30, 8))
+    q = rng.standard_normal((6, 5, 8))
+    seed = snapkv.prefill_seed(q, K, 0.7)
+    np.testing.assert_allclose(seed.sum(axis=1), [3 * 5, 3 * 5], rtol=1e-12)
+
+
+def test_seed_with_zero_queries_is_harmonic():
+    # q = 0: row i spreads 1 / (P + i + 1) over keys 0..P+i, so key j collects
+    # G * sum_{i : P + i >= j} 1 / (P + i + 1)
+    G, W, P, d = 3, 4, 9, 8
+    S = P + W
+    rng = np.random.default_rng(2)
+    K = rng.standard_normal((1, S, d))
+    seed = snapkv.prefill_seed(np.zeros((G, W, d)), K, 1.0)[0]
+    want = [G * sum(1.0 / (P + i + 1) for i in range(W) if P + i >= j) for j in range(S)]
+    np.testing.assert_allclose(seed, want, rtol=1e-12)
+
+
+def test_seed_on_the_prefix_is_the_vote():
+    # the row-by-row vote and the masked-matrix seed are separate code paths
+    rng = np.random.default_rng(13)
+    K = rng.standard_normal((2, 50, 16))
+    q = rng.standard_normal((4, 7, 16))
+    seed = snapkv.prefill_seed(q, K, 0.25)
+    vote = snapkv.snapkv_vote(q, K, 0.25)
+    np.testing.assert_allclose(seed[:, :43], vote, rtol=1e-12, atol=1e-15)
+
+
+@pytest.mark.parametrize("t", [0, 2, 3])
+def test_seed_of_a_window_key_counts_only_later_rows(t):
+    # window key P+t is strongly attractive: rows i >= t put ~all their weight
+    # on it, rows i < t cannot see it; two q heads share the kv head
+    d, W, P = 8, 4, 16
+    S = P + W
+    u = np.zeros(d)
+    u[0] = 1.0
+    rng = np.random.default_rng(3)
+    K = np.zeros((1, S, d))
+    K[0, :P] = 0.05 * rng.standard_normal((P, d))
+    K[0, P:] = -60 * u
+    K[0, P + t] = 60 * u
+    q = np.tile(u, (2, W, 1))
+    seed = snapkv.prefill_seed(q, K, 1 / math.sqrt(d))[0]
+    assert abs(seed[P + t] - 2 * (W - t)) < 1e-6
+    assert abs(seed[:P].sum() - 2 * t) < 1e-6
+
+
+# ---- GQA union of per-head picks ----
+
+def test_per_head_votes_add_up_to_the_group_vote():
+    rng = np.random.default_rng(14)
+    K = rng.standard_normal((2, 40, 8))
+    q = rng.standard_normal((8, 6, 8))
+    vh = snapkv.snapkv_vote_per_head(q, K, 0.5)
+    vg = snapkv.snapkv_vote(q, K, 0.5)
+    np.testing.assert_allclose(vh.reshape(2, 4, -1).sum(axis=1), vg, rtol=1e-12)
+
+
+def test_union_keeps_every_heads_favourite():
+    # one kv head, two q heads: head 0 looks along e0 (key 3 answers), head 1
+    # along e1 (key 11 answers, more strongly).  One pick per head: the summed
+    # vote keeps only key 11, the union keeps both.
+    d, W, P = 8, 2, 16
+    S = P + W
+    e = np.eye(d)
+    K = np.zeros((1, S, d))
+    K[0, 3] = 30 * e[0]
+    K[0, 11] = 40 * e[1]
+    K[0, P:] = -60 * (e[0] + e[1])
+    q = np.stack([np.tile(e[0], (W, 1)), np.tile(e[1], (W, 1))])
+    keep, vote, _ = snapkv.snapkv_select_union(q, K, 1.0, keep_k=1, kernel=1)
+    assert keep[0].tolist() == [3, 11, P, P + 1]
+    assert vote[0].argmax() == 3 and vote[1].argmax() == 11
+    keep_sum, _, _ = snapkv.snapkv_select(q, K, 1.0, keep_k=1, kernel=1)
+    assert keep_sum[0].tolist() == [11, P, P + 1]
+
+
+def test_union_with_one_q_head_per_group_is_the_summed_selection():
+    rng = np.random.default_rng(15)
+    K = rng.standard_normal((3, 200, 16))
+    q = rng.standard_normal((3, 8, 16))
+    keep_u, _, _ = snapkv.snapkv_select_union(q, K, 0.4, keep_k=20)
+    keep_s, _, _ = snapkv.snapkv_select(q, K, 0.4, keep_k=20)
+    for h in range(3):
+        assert keep_u[h].tolist() == keep_s[h].tolist()
+
+
+def test_union_size_and_order():
+    rng = np.random.default_rng(16)
+    G, W, S, k = 4, 8, 300, 25
+    K = rng.standard_normal((1, S, 16))
+    q = rng.standard_normal((G, W, 16))
+    keep, _, pooled = snapkv.snapkv_select_union(q, K, 0.4, keep_k=k)
+    u = keep[0]
+    assert np.all(np.diff(u) > 0)
+    assert u[-W:].tolist() == list(range(S - W, S))
+    assert k <= len(u) - W <= G * k
+    for g in range(G):
+        assert set(np.argsort(-pooled[g], kind="stable")[:k].tolist()) <= set(u.tolist())
