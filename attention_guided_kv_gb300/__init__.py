@@ -27,6 +27,7 @@ KVSEL_F32 = 1
 KVSEL_AGG_MAX, KVSEL_AGG_MEAN, KVSEL_AGG_TOPP, KVSEL_AGG_FRAC_HOT, KVSEL_AGG_ALL_COLD = 0, 1, 2, 3, 4
 KVSEL_NORM_NONE, KVSEL_NORM_PERCENTILE = 0, 1
 KVSEL_UPDATE_DECAY, KVSEL_UPDATE_MAX, KVSEL_UPDATE_WINDOW = 0, 1, 2
+KVSEL_SNAP_GROUP_SUM, KVSEL_SNAP_HEAD_UNION = 0, 1
 
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT", 5: "BAD_INDEX"}
 
@@ -47,6 +48,11 @@ class PagedKV(ctypes.Structure):
 class BpOptions(ctypes.Structure):
     _fields_ = [("update", ctypes.c_int), ("history", ctypes.c_void_p), ("window", ctypes.c_int),
                 ("step", ctypes.c_int64), ("history_tokens", ctypes.c_int64), ("threshold", ctypes.c_float)]
+
+
+class SnapOptions(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("keep_count", ctypes.c_void_p), ("seed_out", ctypes.c_void_p),
+                ("seed_layer_stride", ctypes.c_int64), ("seed_head_stride", ctypes.c_int64)]
 
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -78,6 +84,9 @@ _SIGS = {
                                  _i, _f, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "kvsel_snapkv_select_workspace": (_sz, [_PKV, _i, _i, _i, _i]),
     "kvsel_snapkv_select": (_i, [_PKV, _vp, _i, _i, _i, _vp, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "kvsel_snapkv_select_ex_workspace": (_sz, [_PKV, _i, _i, _i, _i, _i]),
+    "kvsel_snapkv_select_ex": (_i, [_PKV, _vp, _i, _i, _i, _vp, _i, _f, _i, _i, ctypes.POINTER(SnapOptions), _vp,
+                                    _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -375,3 +384,38 @@ def kvsel_snapkv_select(kv: PagedKV, block_table, q_obs, keep_out, workspace, *,
         ctypes.byref(kv), _ptr(block_table), block_table.shape[-1], L, int(seq_len), _ptr(q_obs), W,
         float(scale), int(pool_kernel), int(keep_k), _ptr(keep_out), _ptr(vote_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kvsel_snapkv_select_ex_workspace(kv: PagedKV, num_layers: int, seq_len: int, obs_window: int,
+                                     with_vote_out: bool, mode: int = KVSEL_SNAP_GROUP_SUM) -> int:
+    return int(lib().kvsel_snapkv_select_ex_workspace(ctypes.byref(kv), num_layers, seq_len, obs_window,
+                                                      int(with_vote_out), int(mode)))
+
+
+def kvsel_snapkv_select_ex(kv: PagedKV, block_table, q_obs, keep_out, workspace, *, seq_len, keep_k,
+                           mode=KVSEL_SNAP_GROUP_SUM, pool_kernel=7, scale=None, vote_out=None,
+                           keep_count=None, seed_out=None, seed_layer_stride=0, seed_head_stride=0,
+                           stream=None):
+    """SnapKV selection with the union keep mode, keep counts and cold-start seeds.
+
+    seed_out is a float32 tensor (or a view into one) addressed with the given
+    element strides: entry i of (layer l, kv head h) at l * seed_layer_stride +
+    h * seed_head_stride + i from its first element.
+    """
+    _need(block_table, torch.int32, "block_table")
+    _need(q_obs, torch.bfloat16, "q_obs")
+    _need(keep_out, torch.int32, "keep_out")
+    _need(vote_out, torch.float32, "vote_out", True)
+    _need(keep_count, torch.int32, "keep_count", True)
+    if seed_out is not None and (seed_out.dtype != torch.float32 or seed_out.device.type != "cuda"):
+        raise ValueError("seed_out must be a CUDA float32 tensor")
+    L, Hq, W, d = q_obs.shape
+    if scale is None:
+        scale = kv.head_dim ** -0.5
+    opt = SnapOptions(int(mode), keep_count.data_ptr() if keep_count is not None else None,
+                      seed_out.data_ptr() if seed_out is not None else None,
+                      int(seed_layer_stride), int(seed_head_stride))
+    _check(lib().kvsel_snapkv_select_ex(
+        ctypes.byref(kv), _ptr(block_table), block_table.shape[-1], L, int(seq_len), _ptr(q_obs), W,
+        float(scale), int(pool_kernel), int(keep_k), ctypes.byref(opt), _ptr(keep_out), _ptr(vote_out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))

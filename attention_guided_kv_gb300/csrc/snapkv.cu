@@ -9,20 +9,31 @@
 // prefix) and the top keep_k prefix positions (ties to the lower position)
 // plus the window itself are kept, in ascending order.
 //
-// Kernels (four launches per call, all layers at once):
-//   snap_qk_kernel<1>  row softmax statistics: every CTA streams a chunk of a
-//                      (layer, kv head)'s K pages (TMA, 8-stage ring) and 8
-//                      warps each run 32 window rows against every page with
-//                      mma.sync (S = Q K^T), keeping an online (max, sum) per
-//                      row; partial statistics per chunk.
-//   snap_qk_kernel<2>  votes: the same contraction again (K comes back from
-//                      L2 or HBM), weights exp2(s - M_row) / L_row from the
-//                      merged statistics, summed over the warp's rows with
-//                      shuffles and over the 8 warps in shared memory.
+// Two variants of the same section: the GQA union (each q head picks its own
+// top-k from its own pooled vote; the kv head keeps the union of its heads'
+// picks, then the window) and the cold-start seed (for every kept key, the
+// attention the G*W window rows gave it, window keys included causally: the
+// accumulator H2O would hold had the last W prompt tokens been decoded one
+// at a time with the same queries).
+//
+// Kernels (four launches per call, all layers at once; five for the union):
+//   snap_tc_kernel<1>  row softmax statistics: every CTA streams a chunk of a
+//                      (layer, kv head)'s K pages by TMA into a 4-tile ring,
+//                      one thread issues tcgen05.mma (S = Q K^T into TMEM),
+//                      16 epilogue warps keep an online (max, sum) per row;
+//                      partial statistics per chunk.
+//   snap_tc_kernel<2>  votes: the same contraction again with keys on the M
+//                      side (K comes back from L2 or HBM), weights
+//                      exp2(s - M_row) / L_row from the merged statistics,
+//                      each epilogue thread summing one key's row weights.
+//   snap_tc_kernel<3>  the union variant's per-q-head votes instead of <2>.
 //   snap_pool_kernel   max-pool of the votes into order keys (tiles of 1024
 //                      positions staged in shared memory with their halo).
 //   snap_select_kernel exact top-keep_k of the pooled keys per (layer, kv
-//                      head) with row_topk, window appended.
+//                      head) with row_topk, window appended, seeds gathered;
+//                      per q head for the union variant.
+//   snap_union_kernel  union variant: bitmap of the group's picks, emitted in
+//                      ascending order with the window and the seeds.
 #include "common.cuh"
 #include "row_topk.cuh"
 #include "umma.cuh"
@@ -41,12 +52,19 @@ struct SnapParams {
   const int32_t* block_table;  // [L][max_pages]
   const __nv_bfloat16* q_obs;  // [L][Hq][W][128]
   float* stats;                // [L*Hkv][chunks][rows][2]
-  float* vote;                 // [L*Hkv][S - W]
-  int32_t* keep_out;           // [L*Hkv][keep_k + W]
+  float* vote;                 // [L*Hkv][S - W]; the union variant: [L*Hq][S - W]
+  float* wvote;                // window keys' attention (the seed of keys S-W..S-1), rows as vote x [W]
+  int32_t* keep_out;           // [L*Hkv][keep_cap]
+  int32_t* keep_count;         // [L*Hkv] or null
+  int32_t* head_keep;          // union variant: [L*Hq][keep_k] per-head picks
+  uint32_t* bitmap;            // union variant: [L*Hkv][nwords] marks of the group's picks
+  float* seed;                 // kept keys' seeds (null: none), at layer * seed_ls + kv head * seed_hs
+  long long seed_ls, seed_hs;
   uint32_t* pool_key;          // [L*Hkv][pool_stride]: order keys of the pooled votes
   int pool_stride;
   int* status;
   int L, Hq, Hkv, G, W, rows, S, max_pages, num_pages, chunks, keep_k, pool_half;
+  int union_mode, keep_cap, vote_span, nwords;  // vote_span: S with seeds (window keys too), else S - W
   float scale_log2;
 };
 
@@ -61,7 +79,12 @@ struct SnapParams {
 //           keeps its online (max, sum) in the log2 domain;
 //   pass 2 (votes): D[keys x rows] = K Q^T, keys on the M side; each
 //           epilogue thread owns one key and sums its weights over the rows
-//           directly, so the vote needs no cross-thread reduction.
+//           directly, so the vote needs no cross-thread reduction;
+//   pass 3 (per-head votes, union variant): the same product; the four
+//           epilogue warps of a lane quarter split the group's heads and sum
+//           each head's W columns apart.
+// With seeds the vote passes also cover the window keys, whose weights are
+// masked causally per (key, row).
 // ---------------------------------------------------------------------------
 constexpr int kTcKeys = 128;                          // keys per MMA tile (8 pages)
 constexpr int kTcStages = 4;                          // K tiles in flight
@@ -116,7 +139,7 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = P.rows;
   const int Pfx = P.S - P.W;
-  const int span = kPass == 1 ? P.S : Pfx;  // keys this pass needs
+  const int span = kPass == 1 ? P.S : P.vote_span;  // keys this pass needs
   const int npages = (span + kSnPage - 1) / kSnPage;
   const int pb = int((long long)chunk * npages / P.chunks);
   const int pe = int((long long)(chunk + 1) * npages / P.chunks);
@@ -132,7 +155,7 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
       *reinterpret_cast<uint4*>(sQ + slab * (kTcQRows * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
   }
-  if (kPass == 2) {
+  if (kPass >= 2) {
     // merged row statistics: M = max over chunks, 1/L with L = sum l * 2^(m - M)
     const float* st = P.stats + size_t(pair) * P.chunks * R * 2;
     for (int r = tid; r < R; r += kTcThreads) {
@@ -308,20 +331,33 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
             }
           }
         }
-      } else {
+      } else if (kPass == 2) {
         const int nchunks = ((R + 31) & ~31) / 32;
         const int cbeg = nchunks * part / kTcEpiPerQ, cend = nchunks * (part + 1) / kTcEpiPerQ;
+        // a tile reaching the window keys masks row r of window key Pfx + kw unless r % W >= kw
+        const bool wtile = kt0 + kTcKeys > Pfx;
+        const int kw = kt0 + tl - Pfx;
         float vote = 0.f;
 #pragma unroll 1
         for (int ci = cbeg; ci < cend; ++ci) {
           const int c0 = ci * 32;
           float v[32];
           tmem_ld32(acc + uint32_t(c0), v);
+          if (!wtile) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 C = *reinterpret_cast<const float4*>(sStat + c0 + i);  // +inf past the rows
-            vote += fast_exp2(fmaf(v[i], sc, -C.x)) + fast_exp2(fmaf(v[i + 1], sc, -C.y)) +
-                    fast_exp2(fmaf(v[i + 2], sc, -C.z)) + fast_exp2(fmaf(v[i + 3], sc, -C.w));
+            for (int i = 0; i < 32; i += 4) {
+              const float4 C = *reinterpret_cast<const float4*>(sStat + c0 + i);  // +inf past the rows
+              vote += fast_exp2(fmaf(v[i], sc, -C.x)) + fast_exp2(fmaf(v[i + 1], sc, -C.y)) +
+                      fast_exp2(fmaf(v[i + 2], sc, -C.z)) + fast_exp2(fmaf(v[i + 3], sc, -C.w));
+            }
+          } else {
+            int rw = c0 % P.W;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float C = rw >= kw ? sStat[c0 + i] : INFINITY;
+              vote += fast_exp2(fmaf(v[i], sc, -C));
+              rw = rw + 1 == P.W ? 0 : rw + 1;
+            }
           }
         }
         float* xb = xch + ((buf * kTcEpiPerQ + part) * 4 + quarter) * 32;  // [parity][part][quarter][32]
@@ -332,7 +368,46 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
           float sum = 0.f;
 #pragma unroll
           for (int q = 0; q < kTcEpiPerQ; ++q) sum += xch[((buf * kTcEpiPerQ + q) * 4 + quarter) * 32 + lane];
-          if (key >= key0 && key < key1) vrow[key] = sum;
+          if (key >= key0 && key < key1) {
+            if (key < Pfx) vrow[key] = sum;
+            else P.wvote[size_t(pair) * P.W + (key - Pfx)] = sum;
+          }
+        }
+      } else {
+        // per-q-head votes: this warp's heads g0..g1-1, W columns each, no exchange
+        const int g0 = P.G * part / kTcEpiPerQ, g1 = P.G * (part + 1) / kTcEpiPerQ;
+        const int key = kt0 + tl, kw = key - Pfx;
+        const bool wtile = kt0 + kTcKeys > Pfx;
+#pragma unroll 1
+        for (int g = g0; g < g1; ++g) {
+          const int lo = g * P.W, hi = lo + P.W;
+          const bool whole = !wtile && (lo & 31) == 0 && (P.W & 31) == 0;  // 32-column loads inside the head
+          float vote = 0.f;
+#pragma unroll 1
+          for (int c0 = lo & ~31; c0 < hi; c0 += 32) {
+            float v[32];
+            tmem_ld32(acc + uint32_t(c0), v);
+            if (whole) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                const float4 C = *reinterpret_cast<const float4*>(sStat + c0 + i);
+                vote += fast_exp2(fmaf(v[i], sc, -C.x)) + fast_exp2(fmaf(v[i + 1], sc, -C.y)) +
+                        fast_exp2(fmaf(v[i + 2], sc, -C.z)) + fast_exp2(fmaf(v[i + 3], sc, -C.w));
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int r = c0 + i;
+                const bool in = r >= lo && r < hi && r - lo >= kw;  // kw < 0 for prefix keys
+                vote += fast_exp2(fmaf(v[i], sc, in ? -sStat[r] : -INFINITY));
+              }
+            }
+          }
+          if (key >= key0 && key < key1) {
+            const size_t vr = size_t(layer) * P.Hq + size_t(kvh) * P.G + g;
+            if (key < Pfx) P.vote[vr * Pfx + key] = vote;
+            else P.wvote[vr * P.W + (key - Pfx)] = vote;
+          }
         }
       }
       tc_fence_before();
@@ -398,22 +473,131 @@ __global__ void __launch_bounds__(kSnPoolTile) snap_pool_kernel(const SnapParams
   }
 }
 
-// Exact top-keep_k of the pooled votes, then the window, ascending.
+// Seed of key j of vote row vr (j < S: the prefix from the votes, the window
+// from the window-key sums).
+__device__ __forceinline__ float snap_seed_of(const SnapParams& P, size_t vr, int Pfx, int j) {
+  return j < Pfx ? P.vote[vr * Pfx + j] : P.wvote[vr * P.W + (j - Pfx)];
+}
+
+// Exact top-keep_k of the pooled votes, then the window, ascending; the
+// union variant stores each q head's picks for snap_union_kernel instead.
 __global__ void __launch_bounds__(kRkThreads) snap_select_kernel(const SnapParams P) {
   extern __shared__ __align__(16) uint8_t tk_smem[];
   RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
-  const int pair = blockIdx.x, tid = threadIdx.x;
+  const int row = blockIdx.x, tid = threadIdx.x;
   const int Pfx = P.S - P.W;
-  const int nk = P.keep_k + P.W;
-  int32_t* keep = P.keep_out + size_t(pair) * nk;
-  if (Pfx <= P.keep_k) {  // nothing to evict: every position, then -1 padding
-    for (int i = tid; i < nk; i += kRkThreads) keep[i] = i < P.S ? i : -1;
+  const uint32_t* krow = P.pool_key + size_t(row) * P.pool_stride;
+  const U32RowKeys src{krow, 0, Pfx, (reinterpret_cast<uintptr_t>(krow) & 15u) == 0};
+  if (P.union_mode) {  // launched only when Pfx > keep_k
+    int32_t* hk = P.head_keep + size_t(row) * P.keep_k;
+    row_topk<kSnSelGroups>(src, P.keep_k, 0u, sm, [&](int i, int rel) { hk[i] = rel; });
     return;
   }
-  const uint32_t* krow = P.pool_key + size_t(pair) * P.pool_stride;
-  const U32RowKeys src{krow, 0, Pfx, (reinterpret_cast<uintptr_t>(krow) & 15u) == 0};
+  const int nk = P.keep_cap;
+  int32_t* keep = P.keep_out + size_t(row) * nk;
+  float* sd = P.seed ? P.seed + (row / P.Hkv) * P.seed_ls + (row % P.Hkv) * P.seed_hs : nullptr;
+  if (Pfx <= P.keep_k) {  // nothing to evict: every position, then -1 padding
+    for (int i = tid; i < nk; i += kRkThreads) {
+      keep[i] = i < P.S ? i : -1;
+      if (sd) sd[i] = i < P.S ? snap_seed_of(P, size_t(row), Pfx, i) : 0.f;
+    }
+    if (tid == 0 && P.keep_count) P.keep_count[row] = P.S;
+    return;
+  }
   row_topk<kSnSelGroups>(src, P.keep_k, 0u, sm, [&](int i, int rel) { keep[i] = rel; });
-  for (int i = tid; i < P.W; i += kRkThreads) keep[P.keep_k + i] = Pfx + i;
+  if (sd) {
+    __syncthreads();  // the picks are this block's own global stores
+    for (int i = tid; i < P.keep_k; i += kRkThreads) sd[i] = P.vote[size_t(row) * Pfx + keep[i]];
+  }
+  for (int i = tid; i < P.W; i += kRkThreads) {
+    keep[P.keep_k + i] = Pfx + i;
+    if (sd) sd[P.keep_k + i] = P.wvote[size_t(row) * P.W + i];
+  }
+  if (tid == 0 && P.keep_count) P.keep_count[row] = P.keep_k + P.W;
+}
+
+// Union variant, one CTA per (layer, kv head): mark the G heads' picks in a
+// bitmap, then emit the marked positions in ascending order (a block scan of
+// the words' popcounts per round of kUnThreads words), the window after them,
+// -1 padding up to keep_cap; seeds summed over the group's vote rows.
+constexpr int kUnThreads = 512;
+__global__ void __launch_bounds__(kUnThreads) snap_union_kernel(const SnapParams P) {
+  __shared__ int wsum[kUnThreads / 32];
+  __shared__ int s_base;
+  const int pair = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int layer = pair / P.Hkv, kvh = pair % P.Hkv;
+  const int Pfx = P.S - P.W, nk = P.keep_cap;
+  const size_t vr0 = size_t(layer) * P.Hq + size_t(kvh) * P.G;  // the group's first vote row
+  int32_t* keep = P.keep_out + size_t(pair) * nk;
+  float* sd = P.seed ? P.seed + layer * P.seed_ls + kvh * P.seed_hs : nullptr;
+  auto seed = [&](int j) {
+    float a = 0.f;
+    for (int g = 0; g < P.G; ++g) a += snap_seed_of(P, vr0 + g, Pfx, j);
+    return a;
+  };
+  int count;
+  if (Pfx <= P.keep_k) {  // every head keeps its whole prefix
+    count = Pfx;
+    for (int i = tid; i < Pfx; i += kUnThreads) {
+      keep[i] = i;
+      if (sd) sd[i] = seed(i);
+    }
+  } else {
+    uint32_t* bits = P.bitmap + size_t(pair) * P.nwords;
+    const int nw = (Pfx + 31) >> 5;
+    for (int w = tid; w < nw; w += kUnThreads) bits[w] = 0u;
+    __syncthreads();
+    const int32_t* hk = P.head_keep + vr0 * P.keep_k;
+    for (int i = tid; i < P.G * P.keep_k; i += kUnThreads) {
+      const int x = hk[i];
+      if (unsigned(x) < unsigned(Pfx)) atomicOr(bits + (x >> 5), 1u << (x & 31));
+      else report(P.status, KVSEL_ERR_BAD_INDEX);
+    }
+    __syncthreads();
+    if (tid == 0) s_base = 0;
+    for (int w0 = 0; w0 < nw; w0 += kUnThreads) {
+      const int w = w0 + tid;
+      uint32_t word = w < nw ? __ldcg(bits + w) : 0u;
+      const int c = __popc(word);
+      int incl = c;  // warp inclusive scan
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      if (warp == 0) {
+        int t = lane < kUnThreads / 32 ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, t, o);
+          if (lane >= o) t += y;
+        }
+        if (lane < kUnThreads / 32) wsum[lane] = t;  // inclusive totals per warp
+      }
+      __syncthreads();
+      int off = s_base + (warp > 0 ? wsum[warp - 1] : 0) + incl - c;
+      while (word) {
+        const int b = __ffs(word) - 1;
+        word &= word - 1;
+        const int j = w * 32 + b;
+        keep[off] = j;
+        if (sd) sd[off] = seed(j);
+        ++off;
+      }
+      __syncthreads();
+      if (tid == 0) s_base += wsum[kUnThreads / 32 - 1];
+      __syncthreads();
+    }
+    count = s_base;
+  }
+  for (int i = tid; i < nk - count; i += kUnThreads) {
+    const int o = count + i;
+    keep[o] = i < P.W ? Pfx + i : -1;
+    if (sd) sd[o] = i < P.W ? seed(Pfx + i) : 0.f;
+  }
+  if (tid == 0 && P.keep_count) P.keep_count[pair] = count + P.W;
 }
 
 }  // namespace kvsel
@@ -423,19 +607,29 @@ using namespace kvsel_host;
 
 namespace {
 struct SnWs {
-  size_t stats, vote, pool, total;
-  int pool_stride;
+  size_t stats, vote, pool, wvote, hkeep, bitmap, total;
+  int pool_stride, nwords;
 };
-SnWs sn_ws_layout(int L, int Hkv, int rows, int S, int W, int chunks, bool own_vote) {
+// vote rows: one per (layer, kv head), or per (layer, q head) for the union
+SnWs sn_ws_layout(int L, int Hkv, int Hq, int rows, int S, int W, int chunks, bool own_vote, bool union_mode) {
   SnWs w;
+  const size_t vrows = size_t(L) * (union_mode ? Hq : Hkv);
+  const size_t pfx = size_t(std::max(S - W, 1));
   size_t off = kStatusBytes;
   w.stats = off;
   off = align_up(off + size_t(L) * Hkv * chunks * rows * 2 * 4, 256);
   w.vote = off;
-  if (own_vote) off = align_up(off + size_t(L) * Hkv * std::max(S - W, 1) * 4, 256);
+  if (own_vote) off = align_up(off + vrows * pfx * 4, 256);
   w.pool = off;
-  w.pool_stride = int(align_up(size_t(std::max(S - W, 1)), 4));
-  off = align_up(off + size_t(L) * Hkv * w.pool_stride * 4, 256);
+  w.pool_stride = int(align_up(pfx, 4));
+  off = align_up(off + vrows * w.pool_stride * 4, 256);
+  w.wvote = off;
+  off = align_up(off + vrows * W * 4, 256);
+  w.hkeep = off;
+  if (union_mode) off = align_up(off + vrows * pfx * 4, 256);  // keep_k < S - W whenever it is used
+  w.bitmap = off;
+  w.nwords = int((pfx + 31) / 32);
+  if (union_mode) off = align_up(off + size_t(L) * Hkv * w.nwords * 4, 256);
   w.total = off;
   return w;
 }
@@ -457,14 +651,20 @@ int sn_chunks(int L, int Hkv, int S) {
 }
 }  // namespace
 
-extern "C" size_t kvsel_snapkv_select_workspace(const kvsel_paged_kv* kv, int num_layers, int seq_len,
-                                                int obs_window, int with_vote_out) {
+extern "C" size_t kvsel_snapkv_select_ex_workspace(const kvsel_paged_kv* kv, int num_layers, int seq_len,
+                                                   int obs_window, int with_vote_out, int mode) {
   if (!kv || num_layers < 1 || seq_len < 1 || obs_window < 1 || kv->num_kv_heads < 1 ||
-      kv->num_q_heads % kv->num_kv_heads != 0)
+      kv->num_q_heads % kv->num_kv_heads != 0 || (mode != KVSEL_SNAP_GROUP_SUM && mode != KVSEL_SNAP_HEAD_UNION))
     return 0;
   const int rows = kv->num_q_heads / kv->num_kv_heads * obs_window;
-  return sn_ws_layout(num_layers, kv->num_kv_heads, rows, seq_len, obs_window, kSnMaxChunks,
-                      with_vote_out == 0).total;
+  return sn_ws_layout(num_layers, kv->num_kv_heads, kv->num_q_heads, rows, seq_len, obs_window, kSnMaxChunks,
+                      with_vote_out == 0, mode == KVSEL_SNAP_HEAD_UNION).total;
+}
+
+extern "C" size_t kvsel_snapkv_select_workspace(const kvsel_paged_kv* kv, int num_layers, int seq_len,
+                                                int obs_window, int with_vote_out) {
+  return kvsel_snapkv_select_ex_workspace(kv, num_layers, seq_len, obs_window, with_vote_out,
+                                          KVSEL_SNAP_GROUP_SUM);
 }
 
 extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int32_t* block_table,
@@ -472,6 +672,16 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
                                             int obs_window, float scale, int pool_kernel, int keep_k,
                                             int32_t* keep_out, float* vote_out, void* workspace,
                                             size_t ws_bytes, void* stream) {
+  return kvsel_snapkv_select_ex(kv, block_table, max_pages, num_layers, seq_len, q_obs, obs_window, scale,
+                                pool_kernel, keep_k, nullptr, keep_out, vote_out, workspace, ws_bytes, stream);
+}
+
+extern "C" kvsel_status kvsel_snapkv_select_ex(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                               int max_pages, int num_layers, int seq_len, const void* q_obs,
+                                               int obs_window, float scale, int pool_kernel, int keep_k,
+                                               const kvsel_snap_options* opt, int32_t* keep_out,
+                                               float* vote_out, void* workspace, size_t ws_bytes,
+                                               void* stream) {
   const std::string fn = "kvsel_snapkv_select: ";
   if (!kv || !kv->k_pool) return fail(KVSEL_ERR_INVALID_ARG, fn + "the K pool is required");
   if (kv->head_dim != kSnD || kv->page_size != kSnPage)
@@ -498,8 +708,22 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
     return fail(KVSEL_ERR_INVALID_ARG, fn + "num_pages * num_kv_heads * 16 must be in [1, 2^31)");
   if (!aligned(kv->k_pool, 16) || !aligned(q_obs, 16))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "K pool and q_obs must be 16-byte aligned");
+  const int mode = opt ? opt->mode : KVSEL_SNAP_GROUP_SUM;
+  if (mode != KVSEL_SNAP_GROUP_SUM && mode != KVSEL_SNAP_HEAD_UNION)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "mode must be KVSEL_SNAP_GROUP_SUM or KVSEL_SNAP_HEAD_UNION");
+  const bool uni = mode == KVSEL_SNAP_HEAD_UNION;
+  const long long cap = (uni ? (long long)G * keep_k : (long long)keep_k) + obs_window;
+  if (cap >= (1LL << 31)) return fail(KVSEL_ERR_INVALID_ARG, fn + "keep capacity must be < 2^31");
+  float* seed = opt ? opt->seed_out : nullptr;
+  if (seed) {
+    const long long ls = opt->seed_layer_stride, hs = opt->seed_head_stride;
+    if (hs < cap || (num_layers > 1 && ls < hs * Hkv))
+      return fail(KVSEL_ERR_INVALID_ARG, fn + "seed strides must give every (layer, kv head) its own row of "
+                                              "the keep capacity");
+  }
   const int chunks = sn_chunks(num_layers, Hkv, seq_len);
-  const SnWs L = sn_ws_layout(num_layers, Hkv, rows, seq_len, obs_window, kSnMaxChunks, vote_out == nullptr);
+  const SnWs L = sn_ws_layout(num_layers, Hkv, Hq, rows, seq_len, obs_window, kSnMaxChunks, vote_out == nullptr,
+                              uni);
   if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace missing, misaligned or smaller than " +
                                            std::to_string(L.total));
@@ -530,11 +754,25 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
   P.keep_k = keep_k;
   P.pool_half = pool_kernel / 2;
   P.scale_log2 = scale * 1.4426950408889634f;
+  P.wvote = reinterpret_cast<float*>(ws + L.wvote);
+  P.keep_count = opt ? opt->keep_count : nullptr;
+  P.head_keep = reinterpret_cast<int32_t*>(ws + L.hkeep);
+  P.bitmap = reinterpret_cast<uint32_t*>(ws + L.bitmap);
+  P.seed = seed;
+  P.seed_ls = seed ? opt->seed_layer_stride : 0;
+  P.seed_hs = seed ? opt->seed_head_stride : 0;
+  P.union_mode = uni ? 1 : 0;
+  P.keep_cap = int(cap);
+  P.vote_span = seed ? seq_len : seq_len - obs_window;
+  P.nwords = L.nwords;
+  const int Pfx = seq_len - obs_window;
+  const int vrows = num_layers * (uni ? Hq : Hkv);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   {
     cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(snap_tc_kernel<1>), int(kTcSmem));
     if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(snap_tc_kernel<2>), int(kTcSmem));
+    if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(snap_tc_kernel<3>), int(kTcSmem));
     if (e0 == cudaSuccess)
       e0 = smem_limit_once(reinterpret_cast<const void*>(snap_select_kernel), int(sizeof(RowTopkSmem)));
     if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_snapkv_select (attribute)");
@@ -546,25 +784,34 @@ extern "C" kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int3
   e = cudaGetLastError();
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (stats launch)");
-  if (seq_len > obs_window) {
+  if (Pfx > 0 || seed) {  // votes (and the window keys' sums when seeding)
     trace_before("snap_vote", st);
-    snap_tc_kernel<2><<<grid, kTcThreads, kTcSmem, st>>>(tmK, P);
+    if (uni) snap_tc_kernel<3><<<grid, kTcThreads, kTcSmem, st>>>(tmK, P);
+    else snap_tc_kernel<2><<<grid, kTcThreads, kTcSmem, st>>>(tmK, P);
     e = cudaGetLastError();
     trace_after(st);
     if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (vote launch)");
   }
-  if (seq_len - obs_window > keep_k) {
+  if (Pfx > keep_k) {
     trace_before("snap_pool", st);
-    snap_pool_kernel<<<dim3((seq_len - obs_window + kSnPoolTile - 1) / kSnPoolTile, num_layers * Hkv),
-                       kSnPoolTile, 0, st>>>(P);
+    snap_pool_kernel<<<dim3((Pfx + kSnPoolTile - 1) / kSnPoolTile, vrows), kSnPoolTile, 0, st>>>(P);
     e = cudaGetLastError();
     trace_after(st);
     if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (pool launch)");
   }
-  trace_before("snap_select", st);
-  snap_select_kernel<<<num_layers * Hkv, kRkThreads, sizeof(RowTopkSmem), st>>>(P);
-  e = cudaGetLastError();
-  trace_after(st);
-  if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (select launch)");
+  if (!uni || Pfx > keep_k) {
+    trace_before("snap_select", st);
+    snap_select_kernel<<<vrows, kRkThreads, sizeof(RowTopkSmem), st>>>(P);
+    e = cudaGetLastError();
+    trace_after(st);
+    if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (select launch)");
+  }
+  if (uni) {
+    trace_before("snap_union", st);
+    snap_union_kernel<<<num_layers * Hkv, kUnThreads, 0, st>>>(P);
+    e = cudaGetLastError();
+    trace_after(st);
+    if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (union launch)");
+  }
   return KVSEL_OK;
 }

@@ -512,15 +512,33 @@ def _setup_snapkv(dev, small=False):
     def step(i):
         run(i, q)
 
+    # the GQA-union keep mode and the cold-start seeds (timed apart, same inputs)
+    cap_u = wl.G * wl.keep_k + wl.W
+    keep_u = torch.zeros(wl.L, wl.Hkv, cap_u, dtype=torch.int32, device=dev)
+    count = torch.zeros(wl.L, wl.Hkv, dtype=torch.int32, device=dev)
+    seed = torch.zeros(wl.L, wl.Hkv, cap_u, device=dev)
+    ws_u = K.workspace(K.kvsel_snapkv_select_ex_workspace(kv, wl.L, wl.S, wl.W, False, K.KVSEL_SNAP_HEAD_UNION))
+
+    def run_ex(mode, seeds):
+        cap = cap_u if mode == K.KVSEL_SNAP_HEAD_UNION else wl.keep_k + wl.W
+        so = dict(seed_out=seed, seed_layer_stride=wl.Hkv * cap, seed_head_stride=cap) if seeds else {}
+        return lambda i: K.kvsel_snapkv_select_ex(
+            kv, bt, q, keep_u if mode == K.KVSEL_SNAP_HEAD_UNION else keep, ws_u, seq_len=wl.S,
+            keep_k=wl.keep_k, mode=mode, pool_kernel=wl.pool_kernel, keep_count=count, **so)
+    variant_runs = [("group_sum_with_seeds", run_ex(K.KVSEL_SNAP_GROUP_SUM, True)),
+                    ("head_union", run_ex(K.KVSEL_SNAP_HEAD_UNION, False)),
+                    ("head_union_with_seeds", run_ex(K.KVSEL_SNAP_HEAD_UNION, True))]
+
     pairs = wl.L * wl.Hkv
     rows = wl.G * wl.W
     qk_flops = 2.0 * rows * wl.S * wl.d * pairs
     kbytes = wl.S * wl.d * 2 * pairs
     # one exp2 per (window row, key) in each pass: the special-function unit bounds both
     ex2 = {"snap_stats": float(rows) * wl.S * pairs, "snap_vote": float(rows) * (wl.S - wl.W) * pairs}
-    return dict(step=step, run=run, host_in=[("q_obs", q[None])], outs=[keep], ws=[ws],
+    return dict(step=step, run=run, host_in=[("q_obs", q[None])], outs=[keep], ws=[ws, ws_u],
                 bytes={"snap_stats": kbytes, "snap_vote": kbytes}, flops={"snap_stats": qk_flops,
                 "snap_vote": 2.0 * rows * (wl.S - wl.W) * wl.d * pairs}, ex2=ex2, per_step_launches=4,
+                variant_runs=variant_runs, variants_key="variants_us_per_select",
                 config={"layers": wl.L, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "prompt": wl.S,
                         "obs_window": wl.W, "keep": wl.keep_k, "pool_kernel": wl.pool_kernel,
                         "l2": "inputs larger than L2 (940 MB of K per pass)"})
@@ -804,6 +822,19 @@ def other_workload(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)
     variants = None
+    if S.get("variant_runs"):
+        variants = {}
+        for name, fn in S["variant_runs"]:
+            for i in range(3):
+                fn(i)
+            torch.cuda.synchronize()
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(10):
+                fn(i)
+            b2.record(stream)
+            torch.cuda.synchronize()
+            variants[name] = a.elapsed_time(b2) / 10 * 1e3
     if S.get("extra_variants"):
         variants = {}
         for bs in (16, 64, 256):
@@ -889,7 +920,7 @@ def other_workload(args, rank, world):
         line["config"]["launch"] = f"CUDA graph of the {steps} timed steps (captured, replayed once untimed, then timed)"
         line["config"]["eager_ms_per_step"] = eager_ms / steps
     if variants:
-        line["variants_us_per_pass"] = variants
+        line[S.get("variants_key", "variants_us_per_pass")] = variants
     if args.small:
         line["note"] = "--small profiling case, not the measured workload"
     if not args.no_cpu_baseline:

@@ -393,6 +393,65 @@ KVSEL_API kvsel_status kvsel_snapkv_select(const kvsel_paged_kv* kv, const int32
                                            float* vote_out, void* workspace, size_t ws_bytes,
                                            void* stream);
 
+/* ---------------------------------------------------------------------------
+ * SnapKV selection with the GQA-union keep mode and cold-start seeds.
+ *
+ * Defines (same section, "KV sharing under GQA", and §2.3 "cold start", the
+ * option of prefill attention as the seed score):
+ *   KVSEL_SNAP_GROUP_SUM   the selection above (one summed vote per kv head).
+ *   KVSEL_SNAP_HEAD_UNION  every q head h votes alone (the sum over its own W
+ *                          rows), pools its vote and picks its own keep_k;
+ *                          the kv head keeps the union of its G heads' picks
+ *                          (ascending), then the window S-W..S-1.
+ *   seed of key j (either mode) = the sum over the group's G*W window rows of
+ *                          their causal softmax weight on key j, for every
+ *                          j < S (window keys included: row i sees keys up to
+ *                          S-W+i).  It is the H2O accumulated score the kv
+ *                          head would hold had the last W prompt tokens been
+ *                          decoded one by one with the same queries, so it can
+ *                          initialise H2O's cum or block_priority's token
+ *                          scores for the kept cache.
+ *
+ * Arguments as for kvsel_snapkv_select, plus:
+ *   opt           NULL (group sum, no seeds, no counts) or:
+ *     mode        kvsel_snap_mode.
+ *     keep_count  int32 [num_layers][num_kv_heads] or NULL: valid entries of
+ *                 each keep row (keep_k + W, or S when S - W <= keep_k; the
+ *                 union's size + W).
+ *     seed_out    fp32 or NULL: entry i of (layer l, kv head h) at
+ *                 seed_out[l * seed_layer_stride + h * seed_head_stride + i]
+ *                 = the seed of position keep[l][h][i] for i < keep_count,
+ *                 0 for the padding up to the keep capacity.  The strides
+ *                 (elements) must give each row the keep capacity:
+ *                 head stride >= capacity, layer stride >= head stride *
+ *                 num_kv_heads when num_layers > 1 (else INVALID_ARG).
+ *                 Pointing it at a cum buffer seeds the compacted cache.
+ *   keep_out      int32 [num_layers][num_kv_heads][capacity], capacity =
+ *                 keep_k + W (group sum) or G * keep_k + W (union); -1 padded.
+ *   vote_out      group sum: fp32 [num_layers][num_kv_heads][S - W];
+ *                 union: fp32 [num_layers][num_q_heads][S - W] (per-head votes).
+ *   workspace     >= kvsel_snapkv_select_ex_workspace(kv, num_layers, seq_len,
+ *                 obs_window, vote_out != NULL, mode) bytes, status zeroed.
+ * Launches: statistics, votes (also the window keys when seeding), pool and
+ * select (per q head for the union), plus one union launch.
+ */
+typedef enum kvsel_snap_mode { KVSEL_SNAP_GROUP_SUM = 0, KVSEL_SNAP_HEAD_UNION = 1 } kvsel_snap_mode;
+typedef struct kvsel_snap_options {
+  int mode;
+  int32_t* keep_count;
+  float* seed_out;
+  int64_t seed_layer_stride;
+  int64_t seed_head_stride;
+} kvsel_snap_options;
+KVSEL_API size_t kvsel_snapkv_select_ex_workspace(const kvsel_paged_kv* kv, int num_layers, int seq_len,
+                                                  int obs_window, int with_vote_out, int mode);
+KVSEL_API kvsel_status kvsel_snapkv_select_ex(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                              int max_pages, int num_layers, int seq_len,
+                                              const void* q_obs, int obs_window, float scale,
+                                              int pool_kernel, int keep_k, const kvsel_snap_options* opt,
+                                              int32_t* keep_out, float* vote_out, void* workspace,
+                                              size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -159,3 +159,35 @@ def test_sparse_decode_host_validation(lib):
     assert st(max_len=(1 << 28) + 1) == K.KVSEL_ERR_UNSUPPORTED
     assert st(ws_bytes=100) == K.KVSEL_ERR_INVALID_ARG
     assert st(kv=_kv(num_q_heads=128)) == K.KVSEL_ERR_UNSUPPORTED
+
+
+def test_snapkv_ex_host_validation(lib):
+    kv = _kv(num_q_heads=32, num_kv_heads=4, num_pages=4096)   # G = 8
+
+    def st(opt=None, **over):
+        a = dict(bt=16, max_pages=4096, L=2, S=4096, q=16, W=32, scale=0.1, pool=7, keep_k=256,
+                 keep=16, vote=None, ws=256, ws_bytes=1 << 30)
+        a.update(over)
+        return lib.kvsel_snapkv_select_ex(ctypes.byref(kv), a["bt"], a["max_pages"], a["L"], a["S"], a["q"],
+                                          a["W"], a["scale"], a["pool"], a["keep_k"],
+                                          ctypes.byref(opt) if opt is not None else None, a["keep"],
+                                          a["vote"], a["ws"], a["ws_bytes"], None)
+    assert st(K.SnapOptions(mode=2)) == K.KVSEL_ERR_INVALID_ARG
+    # union capacity is G * keep_k + W = 2080: a seed row of 2079 elements is too short
+    assert st(K.SnapOptions(mode=1, seed_out=16, seed_layer_stride=4 * 2080,
+                            seed_head_stride=2079)) == K.KVSEL_ERR_INVALID_ARG
+    assert b"seed strides" in lib.kvsel_last_error_string()
+    # layers overlapping each other
+    assert st(K.SnapOptions(mode=1, seed_out=16, seed_layer_stride=3 * 2080,
+                            seed_head_stride=2080)) == K.KVSEL_ERR_INVALID_ARG
+    # group sum: capacity keep_k + W = 288
+    assert st(K.SnapOptions(mode=0, seed_out=16, seed_layer_stride=4 * 287,
+                            seed_head_stride=287)) == K.KVSEL_ERR_INVALID_ARG
+    need = K.kvsel_snapkv_select_ex_workspace(kv, 2, 4096, 32, False, K.KVSEL_SNAP_HEAD_UNION)
+    assert st(K.SnapOptions(mode=1), ws_bytes=need - 1) == K.KVSEL_ERR_INVALID_ARG
+    # the union keeps per-q-head votes, keys and picks: more workspace than the group sum
+    assert need > K.kvsel_snapkv_select_ex_workspace(kv, 2, 4096, 32, False, K.KVSEL_SNAP_GROUP_SUM)
+    assert need >= 3 * 2 * 32 * (4096 - 32) * 4
+    assert K.kvsel_snapkv_select_ex_workspace(kv, 2, 4096, 32, False, 5) == 0
+    assert (K.kvsel_snapkv_select_workspace(kv, 2, 4096, 32, True) ==
+            K.kvsel_snapkv_select_ex_workspace(kv, 2, 4096, 32, True, K.KVSEL_SNAP_GROUP_SUM))

@@ -113,3 +113,126 @@ def test_full_size_qwen7b_sampled_layers():
     kept = sum(len(set(lay.planted[h].tolist()) & set(keep[i, h].tolist()))
                for i, lay in enumerate(layers) for h in range(wl.Hkv))
     assert kept >= 0.99 * 28 * 4 * 64, kept
+
+
+# ---- the union keep mode and cold-start seeds (kvsel_snapkv_select_ex) ----
+
+def _run_ex(st, mode, head_pad=5, layer_pad=3):
+    """Run the extended entry point; seeds go to strided rows padded with NaN sentinels."""
+    wl = st.wl
+    L = len(st.layers)
+    G = wl.G if mode == K.KVSEL_SNAP_HEAD_UNION else 1
+    cap = G * wl.keep_k + wl.W
+    hs = cap + head_pad
+    ls = wl.Hkv * hs + layer_pad
+    seed = torch.full((L * ls,), float("nan"), device="cuda")
+    keep = torch.full((L, wl.Hkv, cap), -7, dtype=torch.int32, device="cuda")
+    count = torch.full((L, wl.Hkv), -7, dtype=torch.int32, device="cuda")
+    vrows = wl.Hq if mode == K.KVSEL_SNAP_HEAD_UNION else wl.Hkv
+    vote = torch.zeros(L, vrows, max(wl.S - wl.W, 1), device="cuda")
+    ws = K.workspace(K.kvsel_snapkv_select_ex_workspace(st.kv, L, wl.S, wl.W, True, mode))
+    K.kvsel_snapkv_select_ex(st.kv, st.bt, st.q, keep, ws, seq_len=wl.S, keep_k=wl.keep_k, mode=mode,
+                             pool_kernel=wl.pool_kernel, vote_out=vote, keep_count=count, seed_out=seed,
+                             seed_layer_stride=ls, seed_head_stride=hs)
+    torch.cuda.synchronize()
+    assert K.read_status(ws) == 0
+    seed = seed.cpu().numpy()
+    rows = np.stack([np.stack([seed[l * ls + h * hs:l * ls + h * hs + cap] for h in range(wl.Hkv)])
+                     for l in range(L)])
+    # nothing written between the rows
+    for l in range(L):
+        for h in range(wl.Hkv):
+            assert np.isnan(seed[l * ls + h * hs + cap:l * ls + (h + 1) * hs]).all()
+        assert np.isnan(seed[l * ls + wl.Hkv * hs:(l + 1) * ls]).all()
+    return keep.cpu().numpy(), count.cpu().numpy(), vote.cpu().numpy(), rows
+
+
+def _check_seeds(wl, lay, h, keep_row, n, seed_row):
+    want = snapkv.prefill_seed(bf16_bits_to_f64(lay.q_obs[h * wl.G:(h + 1) * wl.G]),
+                               bf16_bits_to_f64(lay.K[h:h + 1]), wl.scale)[0]
+    assert rel_l2(seed_row[:n], want[keep_row[:n]]) < TOL
+    assert (seed_row[n:] == 0).all()
+
+
+@pytest.mark.parametrize("S,W,keep_k,G", [(3000, 16, 256, 4), (1000, 32, 2048, 7), (40, 40, 16, 2),
+                                          (777, 5, 100, 1)])
+def test_group_sum_seeds_and_counts(S, W, keep_k, G):
+    wl = workloads.snapkv_custom(seed=S + 1, L=2, Hq=2 * G, Hkv=2, d=128, S=S, W=W, keep_k=keep_k,
+                                 n_planted=4)
+    st = SnapState(wl, [wl.layer(l) for l in range(wl.L)])
+    keep, count, vote, seed = _run_ex(st, K.KVSEL_SNAP_GROUP_SUM)
+    P = S - W
+    for i, lay in enumerate(st.layers):
+        for h in range(wl.Hkv):
+            if P > keep_k:
+                pooled = snapkv.maxpool1d(vote[i, h, :P].astype(np.float64), wl.pool_kernel)
+                want = snapkv.snapkv_keep(pooled, S, W, keep_k)
+            else:
+                want = np.arange(S)
+            n = len(want)
+            assert count[i, h] == n
+            np.testing.assert_array_equal(keep[i, h, :n], want)
+            assert (keep[i, h, n:] == -1).all()
+            _check_seeds(wl, lay, h, keep[i, h], n, seed[i, h])
+            # a kept prefix key's seed is its raw vote
+            pre = keep[i, h, :n] < P
+            np.testing.assert_array_equal(seed[i, h, :n][pre], vote[i, h, keep[i, h, :n][pre]])
+
+
+@pytest.mark.parametrize("S,W,keep_k,G", [(3000, 32, 128, 7), (4099, 5, 300, 2), (2000, 16, 64, 4),
+                                          (777, 8, 100, 1), (300, 16, 512, 3)])
+def test_union_of_per_head_picks(S, W, keep_k, G):
+    wl = workloads.snapkv_custom(seed=S + 2, L=1, Hq=4 * G, Hkv=4, d=128, S=S, W=W, keep_k=keep_k,
+                                 n_planted=4)
+    st = SnapState(wl, [wl.layer(0)])
+    keep, count, vote, seed = _run_ex(st, K.KVSEL_SNAP_HEAD_UNION)
+    lay = st.layers[0]
+    P = S - W
+    want_vote = snapkv.snapkv_vote_per_head(bf16_bits_to_f64(lay.q_obs), bf16_bits_to_f64(lay.K), wl.scale)
+    for qh in range(wl.Hq):
+        assert rel_l2(vote[0, qh, :P], want_vote[qh]) < TOL, qh
+    sizes = []
+    for h in range(wl.Hkv):
+        pooled = snapkv.maxpool1d(vote[0, h * G:(h + 1) * G, :P].astype(np.float64), wl.pool_kernel)
+        want = snapkv.snapkv_union_keep(pooled, S, W, keep_k)
+        n = len(want)
+        assert count[0, h] == n
+        np.testing.assert_array_equal(keep[0, h, :n], want)
+        assert (keep[0, h, n:] == -1).all()
+        _check_seeds(wl, lay, h, keep[0, h], n, seed[0, h])
+        sizes.append(n - W)
+    if P > keep_k and G > 1:
+        assert max(sizes) > keep_k           # the heads disagree somewhere
+
+
+@pytest.mark.slow
+def test_full_size_qwen7b_union_with_seeds_sampled():
+    """28 layers x 32K, 28 q / 4 kv heads, W=32, pool 7, keep 2048 per q head, union + seeds."""
+    wl = workloads.snapkv_qwen7b()
+    layers = [wl.layer(l) for l in range(wl.L)]
+    st = SnapState(wl, layers)
+    keep, count, vote, seed = _run_ex(st, K.KVSEL_SNAP_HEAD_UNION)
+    P = wl.S - wl.W
+    G = wl.G
+    for i in (0, 27):
+        lay = layers[i]
+        for h in (0, 3):
+            q = bf16_bits_to_f64(lay.q_obs[h * G:(h + 1) * G])
+            k = bf16_bits_to_f64(lay.K[h:h + 1])
+            want_vote = snapkv.snapkv_vote_per_head(q, k, wl.scale)
+            for g in range(G):
+                assert rel_l2(vote[i, h * G + g, :P], want_vote[g]) < TOL
+            pooled = snapkv.maxpool1d(vote[i, h * G:(h + 1) * G, :P].astype(np.float64), wl.pool_kernel)
+            want = snapkv.snapkv_union_keep(pooled, wl.S, wl.W, wl.keep_k)
+            n = len(want)
+            assert count[i, h] == n
+            np.testing.assert_array_equal(keep[i, h, :n], want)
+            _check_seeds(wl, lay, h, keep[i, h], n, seed[i, h])
+    assert (count >= wl.keep_k + wl.W).all() and (count <= G * wl.keep_k + wl.W).all()
+    kept = 0
+    for i, lay in enumerate(layers):
+        for h in range(wl.Hkv):
+            row = keep[i, h, :count[i, h]]
+            assert (np.diff(row) > 0).all()
+            kept += len(set(lay.planted[h].tolist()) & set(row.tolist()))
+    assert kept >= 0.99 * 28 * 4 * 64, kept
