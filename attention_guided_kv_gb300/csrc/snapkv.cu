@@ -16,7 +16,7 @@
 // accumulator H2O would hold had the last W prompt tokens been decoded one
 // at a time with the same queries).
 //
-// Kernels (four launches per call, all layers at once; five for the union):
+// Kernels (three launches per call, all layers at once; four for the union):
 //   snap_tc_kernel<1>  row softmax statistics: every CTA streams a chunk of a
 //                      (layer, kv head)'s K pages by TMA into a 4-tile ring,
 //                      one thread issues tcgen05.mma (S = Q K^T into TMEM),
@@ -27,11 +27,10 @@
 //                      exp2(s - M_row) / L_row from the merged statistics,
 //                      each epilogue thread summing one key's row weights.
 //   snap_tc_kernel<3>  the union variant's per-q-head votes instead of <2>.
-//   snap_pool_kernel   max-pool of the votes into order keys (tiles of 1024
-//                      positions staged in shared memory with their halo).
-//   snap_select_kernel exact top-keep_k of the pooled keys per (layer, kv
-//                      head) with row_topk, window appended, seeds gathered;
-//                      per q head for the union variant.
+//   snap_select_kernel exact top-keep_k of the max-pooled votes per (layer,
+//                      kv head) with row_topk, the pool taken as the row is
+//                      loaded; window appended, seeds gathered; per q head
+//                      for the union variant.
 //   snap_union_kernel  union variant: bitmap of the group's picks, emitted in
 //                      ascending order with the window and the seeds.
 #include "common.cuh"
@@ -45,7 +44,6 @@ constexpr int kSnPage = 16;
 constexpr int kSnMaxRows = 256;          // G * W <= 256
 constexpr int kSnMaxChunks = 64;
 constexpr int kSnSelGroups = 8;           // register-resident rows: prefix <= 32768
-constexpr int kSnPoolTile = 1024;
 constexpr int kSnMaxHalf = 16;            // pool kernel <= 33
 
 struct SnapParams {
@@ -60,8 +58,6 @@ struct SnapParams {
   uint32_t* bitmap;            // union variant: [L*Hkv][nwords] marks of the group's picks
   float* seed;                 // kept keys' seeds (null: none), at layer * seed_ls + kv head * seed_hs
   long long seed_ls, seed_hs;
-  uint32_t* pool_key;          // [L*Hkv][pool_stride]: order keys of the pooled votes
-  int pool_stride;
   int* status;
   int L, Hq, Hkv, G, W, rows, S, max_pages, num_pages, chunks, keep_k, pool_half;
   int union_mode, keep_cap, vote_span, nwords;  // vote_span: S with seeds (window keys too), else S - W
@@ -452,26 +448,63 @@ snap_tc_kernel(const __grid_constant__ CUtensorMap tmK, const SnapParams P) {
   }
 }
 
-// Stride-1 max-pool of the votes over [j - pool_half, j + pool_half] clipped
-// to the prefix, stored as order keys; one tile of 1024 positions per CTA.
-__global__ void __launch_bounds__(kSnPoolTile) snap_pool_kernel(const SnapParams P) {
-  __shared__ float tile[kSnPoolTile + 2 * kSnMaxHalf];
-  const int pair = blockIdx.y, tid = threadIdx.x;
-  const int Pfx = P.S - P.W, h = P.pool_half;
-  const int j0 = blockIdx.x * kSnPoolTile;
-  const float* vrow = P.vote + size_t(pair) * Pfx;
-  for (int i = tid; i < kSnPoolTile + 2 * h; i += kSnPoolTile) {
-    const int j = j0 - h + i;
-    tile[i] = (j >= 0 && j < Pfx) ? __ldcg(vrow + j) : -INFINITY;
+// Keys of the max-pooled votes of one row, pooled as they are loaded: key(j)
+// = order key of max(p[j - h .. j + h]) with the window clipped to the prefix
+// [0, n) (stride 1).  row_topk loads a row once when it fits its registers
+// (prefix <= 32768), so the pooled row is never stored.  load4 must be called
+// by all 32 lanes of a warp together (row_topk's sweep does): for h <= 4 a
+// lane loads its own four votes and takes the halo from the neighbouring
+// lanes' (lane i - 1 / i + 1 when they hold positions rel - 4 / rel + 4, else
+// it loads them itself).
+struct PooledVoteKeys {
+  const float* p;
+  int lo, n, h;
+  __device__ __forceinline__ float at(int j) const { return (j >= 0 && j < n) ? __ldcg(p + j) : -INFINITY; }
+  __device__ __forceinline__ uint32_t key(int j, float m) const { return (j >= lo && j < n) ? order_key(m) : 0u; }
+  __device__ __forceinline__ uint32_t load1(int rel) const {
+    if (rel < lo || rel >= n) return 0u;
+    float m = -INFINITY;
+#pragma unroll 8
+    for (int t = -h; t <= h; ++t) m = fmaxf(m, at(rel + t));
+    return order_key(m);
   }
-  __syncthreads();
-  const int j = j0 + tid;
-  if (j < Pfx) {
-    float mx = tile[tid];
-    for (int t = 1; t <= 2 * h; ++t) mx = fmaxf(mx, tile[tid + t]);
-    P.pool_key[size_t(pair) * P.pool_stride + j] = order_key(mx);
+  __device__ __forceinline__ uint4 load4(int rel) const {
+    float w[12];  // positions rel - 4 .. rel + 7
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[4 + i] = at(rel + i);
+    if (h <= 4) {
+      const int rl = __shfl_up_sync(0xffffffffu, rel, 1), rr = __shfl_down_sync(0xffffffffu, rel, 1);
+      const int lane = threadIdx.x & 31;
+      const bool left = lane > 0 && rl == rel - 4, right = lane < 31 && rr == rel + 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = __shfl_up_sync(0xffffffffu, w[4 + i], 1), b = __shfl_down_sync(0xffffffffu, w[4 + i], 1);
+        w[i] = left ? a : at(rel - 4 + i);
+        w[8 + i] = right ? b : at(rel + 4 + i);
+      }
+      float m[4];
+#pragma unroll
+      for (int o = 0; o < 4; ++o) {
+        m[o] = w[4 + o];
+#pragma unroll
+        for (int i = 0; i < 12; ++i) {
+          const int d = i - 4 - o;  // offset of position rel - 4 + i from output rel + o
+          if (d != 0 && d >= -4 && d <= 4 && (d < 0 ? -d : d) <= h) m[o] = fmaxf(m[o], w[i]);
+        }
+      }
+      return make_uint4(key(rel, m[0]), key(rel + 1, m[1]), key(rel + 2, m[2]), key(rel + 3, m[3]));
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+    for (int t = -h; t <= h + 3; ++t) {  // wide pools: position rel + t feeds outputs o with |t - o| <= h
+      const float x = at(rel + t);
+      if (t <= h) m0 = fmaxf(m0, x);
+      if (t >= 1 - h && t <= h + 1) m1 = fmaxf(m1, x);
+      if (t >= 2 - h && t <= h + 2) m2 = fmaxf(m2, x);
+      if (t >= 3 - h) m3 = fmaxf(m3, x);
+    }
+    return make_uint4(key(rel, m0), key(rel + 1, m1), key(rel + 2, m2), key(rel + 3, m3));
   }
-}
+};
 
 // Seed of key j of vote row vr (j < S: the prefix from the votes, the window
 // from the window-key sums).
@@ -486,8 +519,7 @@ __global__ void __launch_bounds__(kRkThreads) snap_select_kernel(const SnapParam
   RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
   const int row = blockIdx.x, tid = threadIdx.x;
   const int Pfx = P.S - P.W;
-  const uint32_t* krow = P.pool_key + size_t(row) * P.pool_stride;
-  const U32RowKeys src{krow, 0, Pfx, (reinterpret_cast<uintptr_t>(krow) & 15u) == 0};
+  const PooledVoteKeys src{P.vote + size_t(row) * Pfx, 0, Pfx, P.pool_half};
   if (P.union_mode) {  // launched only when Pfx > keep_k
     int32_t* hk = P.head_keep + size_t(row) * P.keep_k;
     row_topk<kSnSelGroups>(src, P.keep_k, 0u, sm, [&](int i, int rel) { hk[i] = rel; });
@@ -532,6 +564,7 @@ __global__ void __launch_bounds__(kUnThreads) snap_union_kernel(const SnapParams
   float* sd = P.seed ? P.seed + layer * P.seed_ls + kvh * P.seed_hs : nullptr;
   auto seed = [&](int j) {
     float a = 0.f;
+#pragma unroll 4
     for (int g = 0; g < P.G; ++g) a += snap_seed_of(P, vr0 + g, Pfx, j);
     return a;
   };
@@ -581,16 +614,32 @@ __global__ void __launch_bounds__(kUnThreads) snap_union_kernel(const SnapParams
       while (word) {
         const int b = __ffs(word) - 1;
         word &= word - 1;
-        const int j = w * 32 + b;
-        keep[off] = j;
-        if (sd) sd[off] = seed(j);
-        ++off;
+        keep[off++] = w * 32 + b;
       }
       __syncthreads();
       if (tid == 0) s_base += wsum[kUnThreads / 32 - 1];
       __syncthreads();
     }
     count = s_base;
+    if (sd) {  // seeds in a pass of their own, four entries per thread at a time (this block's own stores)
+      for (int o0 = tid; o0 < count; o0 += 4 * kUnThreads) {
+        int j[4];
+        float a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) j[u] = o0 + u * kUnThreads < count ? keep[o0 + u * kUnThreads] : -1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = 0.f;
+        for (int g = 0; g < P.G; ++g) {
+          const float* vg = P.vote + (vr0 + g) * Pfx;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (j[u] >= 0) a[u] += __ldcg(vg + j[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (j[u] >= 0) sd[o0 + u * kUnThreads] = a[u];
+      }
+    }
   }
   for (int i = tid; i < nk - count; i += kUnThreads) {
     const int o = count + i;
@@ -607,8 +656,8 @@ using namespace kvsel_host;
 
 namespace {
 struct SnWs {
-  size_t stats, vote, pool, wvote, hkeep, bitmap, total;
-  int pool_stride, nwords;
+  size_t stats, vote, wvote, hkeep, bitmap, total;
+  int nwords;
 };
 // vote rows: one per (layer, kv head), or per (layer, q head) for the union
 SnWs sn_ws_layout(int L, int Hkv, int Hq, int rows, int S, int W, int chunks, bool own_vote, bool union_mode) {
@@ -620,9 +669,6 @@ SnWs sn_ws_layout(int L, int Hkv, int Hq, int rows, int S, int W, int chunks, bo
   off = align_up(off + size_t(L) * Hkv * chunks * rows * 2 * 4, 256);
   w.vote = off;
   if (own_vote) off = align_up(off + vrows * pfx * 4, 256);
-  w.pool = off;
-  w.pool_stride = int(align_up(pfx, 4));
-  off = align_up(off + vrows * w.pool_stride * 4, 256);
   w.wvote = off;
   off = align_up(off + vrows * W * 4, 256);
   w.hkeep = off;
@@ -738,8 +784,6 @@ extern "C" kvsel_status kvsel_snapkv_select_ex(const kvsel_paged_kv* kv, const i
   P.stats = reinterpret_cast<float*>(ws + L.stats);
   P.vote = vote_out ? vote_out : reinterpret_cast<float*>(ws + L.vote);
   P.keep_out = keep_out;
-  P.pool_key = reinterpret_cast<uint32_t*>(ws + L.pool);
-  P.pool_stride = L.pool_stride;
   P.status = reinterpret_cast<int*>(ws);
   P.L = num_layers;
   P.Hq = Hq;
@@ -791,13 +835,6 @@ extern "C" kvsel_status kvsel_snapkv_select_ex(const kvsel_paged_kv* kv, const i
     e = cudaGetLastError();
     trace_after(st);
     if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (vote launch)");
-  }
-  if (Pfx > keep_k) {
-    trace_before("snap_pool", st);
-    snap_pool_kernel<<<dim3((Pfx + kSnPoolTile - 1) / kSnPoolTile, vrows), kSnPoolTile, 0, st>>>(P);
-    e = cudaGetLastError();
-    trace_after(st);
-    if (e != cudaSuccess) return cuda_fail(e, "kvsel_snapkv_select (pool launch)");
   }
   if (!uni || Pfx > keep_k) {
     trace_before("snap_select", st);

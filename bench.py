@@ -537,7 +537,7 @@ def _setup_snapkv(dev, small=False):
     ex2 = {"snap_stats": float(rows) * wl.S * pairs, "snap_vote": float(rows) * (wl.S - wl.W) * pairs}
     return dict(step=step, run=run, host_in=[("q_obs", q[None])], outs=[keep], ws=[ws, ws_u],
                 bytes={"snap_stats": kbytes, "snap_vote": kbytes}, flops={"snap_stats": qk_flops,
-                "snap_vote": 2.0 * rows * (wl.S - wl.W) * wl.d * pairs}, ex2=ex2, per_step_launches=4,
+                "snap_vote": 2.0 * rows * (wl.S - wl.W) * wl.d * pairs}, ex2=ex2, per_step_launches=3,
                 variant_runs=variant_runs, variants_key="variants_us_per_select",
                 config={"layers": wl.L, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "prompt": wl.S,
                         "obs_window": wl.W, "keep": wl.keep_k, "pool_kernel": wl.pool_kernel,

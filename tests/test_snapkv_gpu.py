@@ -236,3 +236,38 @@ def test_full_size_qwen7b_union_with_seeds_sampled():
             assert (np.diff(row) > 0).all()
             kept += len(set(lay.planted[h].tolist()) & set(row.tolist()))
     assert kept >= 0.99 * 28 * 4 * 64, kept
+
+
+@pytest.mark.parametrize("pool_kernel", [1, 3, 9, 13, 33])
+def test_pool_widths(pool_kernel):
+    # the pool is taken while the select loads the votes: lane shuffles up to
+    # a half-width of 4, a plain loop above
+    wl = workloads.snapkv_custom(seed=pool_kernel, L=1, Hq=8, Hkv=2, d=128, S=5000, W=16, keep_k=300,
+                                 pool_kernel=pool_kernel, n_planted=4)
+    st = SnapState(wl, [wl.layer(0)])
+    st.run()
+    _check(st)
+    keep, count, vote, _ = _run_ex(st, K.KVSEL_SNAP_HEAD_UNION)
+    P = wl.S - wl.W
+    for h in range(wl.Hkv):
+        pooled = snapkv.maxpool1d(vote[0, h * wl.G:(h + 1) * wl.G, :P].astype(np.float64), pool_kernel)
+        want = snapkv.snapkv_union_keep(pooled, wl.S, wl.W, wl.keep_k)
+        np.testing.assert_array_equal(keep[0, h, :count[0, h]], want)
+
+
+def test_prefix_longer_than_the_register_rows():
+    # prefix > 32768: the select sweeps the row in parts and re-reads (and re-pools) the votes
+    wl = workloads.snapkv_custom(seed=77, L=1, Hq=8, Hkv=2, d=128, S=40000, W=32, keep_k=1024, n_planted=8,
+                                 plant_amp=16.0)
+    st = SnapState(wl, [wl.layer(0)])
+    st.run()
+    _check(st)
+    keep, count, vote, seed = _run_ex(st, K.KVSEL_SNAP_HEAD_UNION)
+    P = wl.S - wl.W
+    lay = st.layers[0]
+    for h in range(wl.Hkv):
+        pooled = snapkv.maxpool1d(vote[0, h * wl.G:(h + 1) * wl.G, :P].astype(np.float64), wl.pool_kernel)
+        want = snapkv.snapkv_union_keep(pooled, wl.S, wl.W, wl.keep_k)
+        n = len(want)
+        np.testing.assert_array_equal(keep[0, h, :n], want)
+        _check_seeds(wl, lay, h, keep[0, h], n, seed[0, h])
