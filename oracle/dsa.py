@@ -13,6 +13,15 @@ Follows "Long context, KV eviction and sparse attention":
     sum_d max(q_d * kmin_d, q_d * kmax_d) and keeps the best pages.
 Ties in a top-k go to the lower position; the selected set is reported in
 ascending order; with S <= k every position is selected.
+
+Quest as a decode-time selector (the same section's listing, read for what it
+computes): per q head, every full page of its kv head gets the bound; the
+budget_pages pages with the largest bounds (ties to the lower page; every
+full page when there are no more than that) are attended, together with the
+trailing partial page, which is always attended; the query is the last
+token, so every page is causally visible.  Page minima and maxima are
+elementwise over the page's tokens (over its valid tokens for the partial
+page, whose bound is never used).
 """
 from __future__ import annotations
 
@@ -63,3 +72,46 @@ def quest_page_bound(q: np.ndarray, K: np.ndarray, page: int = 16) -> np.ndarray
     pages = K[:n * page].reshape(n, page, d)
     kmin, kmax = pages.min(axis=1), pages.max(axis=1)
     return np.maximum(q[None, :] * kmin, q[None, :] * kmax).sum(axis=1)
+
+
+def page_minmax(K: np.ndarray, page: int = 16):
+    """Elementwise min and max over each page of K [S][d] -> (kmin, kmax), [ceil(S/page)][d] each."""
+    S, d = K.shape
+    n = -(-S // page)
+    kmin = np.empty((n, d))
+    kmax = np.empty((n, d))
+    for p in range(n):
+        rows = K[p * page:min(S, (p + 1) * page)]
+        kmin[p] = rows.min(axis=0)
+        kmax[p] = rows.max(axis=0)
+    return kmin, kmax
+
+
+def quest_select_pages(bounds: np.ndarray, budget_pages: int) -> np.ndarray:
+    """Full pages attended by one q head: the budget_pages largest bounds, ascending."""
+    return topk_positions(bounds, budget_pages)
+
+
+def quest_decode_step(q, K, V, budget_pages, scale, page=16):
+    """One decode step with Quest page selection per q head.
+
+    q [Hq][d]; K, V [Hkv][S][d] (the new token included).  Returns (o [Hq][d],
+    chosen pages per q head (list of ascending arrays), bounds [Hq][S // page]).
+    """
+    Hq, d = q.shape
+    Hkv, S, _ = K.shape
+    G = Hq // Hkv
+    n_full = S // page
+    o = np.zeros((Hq, d))
+    chosen = []
+    bounds = np.zeros((Hq, n_full))
+    for h in range(Hq):
+        kvh = h // G
+        bounds[h] = quest_page_bound(q[h], K[kvh], page)
+        pages = quest_select_pages(bounds[h], budget_pages)
+        chosen.append(pages)
+        tokens = np.concatenate([np.arange(p * page, (p + 1) * page) for p in pages] +
+                                [np.arange(n_full * page, S)]).astype(np.int64)
+        w = softmax((K[kvh, tokens] @ q[h]) * scale)
+        o[h] = w @ V[kvh, tokens]
+    return o, chosen, bounds

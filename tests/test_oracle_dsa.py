@@ -2,6 +2,7 @@
 import math
 
 import numpy as np
+import pytest
 import torch
 
 from oracle import dsa
@@ -55,3 +56,66 @@ def test_quest_hand_worked_and_is_an_upper_bound(golden):
     ub = dsa.quest_page_bound(q, K, 16)
     true_max = (K @ q).reshape(10, 16).max(1)
     assert np.all(ub >= true_max - 1e-12)
+
+
+# ---- Quest page selection in a decode step ----
+
+def test_quest_decode_hand_worked(golden):
+    rows = {r[0]: [float(x) for x in r[1:]] for r in golden("quest_decode.txt")}
+    K = np.array(rows["k"]).reshape(1, 5, 2)
+    q = np.array([rows["q0"], rows["q1"]])
+    V = np.arange(10, dtype=np.float64).reshape(1, 5, 2)
+    o, chosen, bounds = dsa.quest_decode_step(q, K, V, budget_pages=1, scale=0.5, page=2)
+    assert bounds.tolist() == [rows["bounds0"], rows["bounds1"]]
+    assert [c.tolist() for c in chosen] == [[0], [1]]
+    for h in range(2):
+        toks = np.array(rows[f"tokens{h}"], dtype=np.int64)
+        w = np.exp(0.5 * (K[0, toks] @ q[h]))
+        np.testing.assert_allclose(o[h], (w / w.sum()) @ V[0, toks], rtol=1e-12)
+
+
+@pytest.mark.parametrize("S", [7, 16, 100, 160])
+def test_quest_with_every_page_in_budget_is_full_attention(S):
+    rng = np.random.default_rng(S)
+    q = rng.standard_normal((4, 32))
+    K, V = rng.standard_normal((2, S, 32)), rng.standard_normal((2, S, 32))
+    o, chosen, _ = dsa.quest_decode_step(q, K, V, budget_pages=S // 16 + 1, scale=0.2)
+    full, _ = decode_attention(q, K, V, 0.2)
+    np.testing.assert_allclose(o, full, rtol=1e-12, atol=1e-14)
+    assert all(c.tolist() == list(range(S // 16)) for c in chosen)
+
+
+def test_quest_bound_is_tight_on_a_constant_page():
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal(16)
+    K = np.tile(k, (32, 1))
+    K[16:] = rng.standard_normal((16, 16))
+    q = rng.standard_normal(16)
+    assert abs(dsa.quest_page_bound(q, K, 16)[0] - q @ k) < 1e-12
+
+
+def test_page_minmax_attained_per_dimension():
+    rng = np.random.default_rng(4)
+    K = rng.standard_normal((37, 8))                  # two full pages and 5 tokens
+    kmin, kmax = dsa.page_minmax(K, 16)
+    assert kmin.shape == (3, 8)
+    for p, (a, b) in enumerate([(0, 16), (16, 32), (32, 37)]):
+        rows = K[a:b]
+        assert np.all(rows >= kmin[p]) and np.all(rows <= kmax[p])
+        for d in range(8):
+            assert kmin[p, d] in rows[:, d] and kmax[p, d] in rows[:, d]
+
+
+def test_quest_heads_choose_alone_and_keep_the_partial_page():
+    # one kv head, two q heads looking along opposite directions: each keeps
+    # the page its own direction favours; both keep the partial page
+    d = 8
+    e = np.eye(d)
+    K = np.zeros((1, 16 * 4 + 3, d))
+    K[0, 16 * 1 + 5] = 10 * e[0]
+    K[0, 16 * 3 + 2] = -10 * e[0]
+    q = np.stack([e[0], -e[0]])
+    V = np.random.default_rng(5).standard_normal(K.shape)
+    _, chosen, bounds = dsa.quest_decode_step(q, K, V, budget_pages=1, scale=1.0)
+    assert chosen[0].tolist() == [1] and chosen[1].tolist() == [3]
+    assert bounds.shape == (2, 4)
