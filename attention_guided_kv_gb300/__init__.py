@@ -85,6 +85,10 @@ _SIGS = {
     "kvsel_snapkv_select_workspace": (_sz, [_PKV, _i, _i, _i, _i]),
     "kvsel_snapkv_select": (_i, [_PKV, _vp, _i, _i, _i, _vp, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "kvsel_snapkv_select_ex_workspace": (_sz, [_PKV, _i, _i, _i, _i, _i]),
+    "kvsel_quest_page_meta": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp]),
+    "kvsel_quest_decode_workspace": (_sz, [_PKV, _i, _i, _i, _i, _i]),
+    "kvsel_quest_decode": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _f, _vp, _i, _vp, _vp, _vp, _sz,
+                                _vp]),
     "kvsel_snapkv_select_ex": (_i, [_PKV, _vp, _i, _i, _i, _vp, _i, _f, _i, _i, ctypes.POINTER(SnapOptions), _vp,
                                     _vp, _vp, _sz, _vp]),
 }
@@ -418,4 +422,42 @@ def kvsel_snapkv_select_ex(kv: PagedKV, block_table, q_obs, keep_out, workspace,
     _check(lib().kvsel_snapkv_select_ex(
         ctypes.byref(kv), _ptr(block_table), block_table.shape[-1], L, int(seq_len), _ptr(q_obs), W,
         float(scale), int(pool_kernel), int(keep_k), ctypes.byref(opt), _ptr(keep_out), _ptr(vote_out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kvsel_quest_page_meta(kv: PagedKV, block_table, seq_lens, page_meta, workspace, stream=None):
+    """Per-page key min / max for every page of each sequence (status in the workspace's first word)."""
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(page_meta, torch.bfloat16, "page_meta")
+    _check(lib().kvsel_quest_page_meta(ctypes.byref(kv), _ptr(block_table), block_table.shape[-1],
+                                       _ptr(seq_lens), seq_lens.shape[0], _ptr(page_meta), _ptr(workspace),
+                                       _stream(stream)))
+
+
+def kvsel_quest_decode_workspace(kv: PagedKV, batch: int, max_pages: int, budget_pages: int,
+                                 with_bounds_out: bool = False, with_pages_out: bool = False) -> int:
+    return int(lib().kvsel_quest_decode_workspace(ctypes.byref(kv), batch, max_pages, budget_pages,
+                                                  int(with_bounds_out), int(with_pages_out)))
+
+
+def kvsel_quest_decode(kv: PagedKV, block_table, seq_lens, q, page_meta, out, workspace, *, budget_pages,
+                       k_new=None, v_new=None, scale=None, pages_out=None, bounds_out=None, stream=None):
+    """One decode step with Quest page selection per q head."""
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(q, torch.bfloat16, "q")
+    _need(page_meta, torch.bfloat16, "page_meta")
+    _need(k_new, torch.bfloat16, "k_new", True)
+    _need(v_new, torch.bfloat16, "v_new", True)
+    _need(pages_out, torch.int32, "pages_out", True)
+    _need(bounds_out, torch.float32, "bounds_out", True)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out must be bfloat16 or float32")
+    if scale is None:
+        scale = kv.head_dim ** -0.5
+    _check(lib().kvsel_quest_decode(
+        ctypes.byref(kv), _ptr(block_table), block_table.shape[-1], _ptr(seq_lens), seq_lens.shape[0], _ptr(q),
+        _ptr(k_new), _ptr(v_new), _ptr(page_meta), int(budget_pages), float(scale), _ptr(out),
+        KVSEL_F32 if out.dtype == torch.float32 else KVSEL_BF16, _ptr(pages_out), _ptr(bounds_out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -44,10 +44,12 @@ __device__ __forceinline__ void load_q_frags(const __nv_bfloat16* qrow, bool hea
 }
 
 // Process one tile of `valid` (1..16) keys at shared addresses kb / vb.
-// Returns the lane's four scaled log2 logits (-inf for keys >= valid).
+// Returns the lane's four scaled log2 logits (-inf for keys >= valid).  A
+// lane whose head is off for this tile (head_on false) sees every logit as
+// -inf; its state is unchanged, also while it has seen no key yet.
 __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb, const uint32_t (&qa)[8][2],
                                             int valid, float scale_log2, TileState& st, float& x0,
-                                            float& x1, float& x2, float& x3) {
+                                            float& x1, float& x2, float& x3, bool head_on = true) {
   const int lane = threadIdx.x & 31, qd = lane & 3, mi = lane >> 3, r8 = lane & 7;
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -60,17 +62,18 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb, const uint
     mma_bf16_16816(s1, qa[kt][0], 0u, qa[kt][1], 0u, b2, b3);
   }
   const int k0 = 2 * qd, k2 = 8 + 2 * qd;
-  x0 = k0 < valid ? s0[0] * scale_log2 : -INFINITY;
-  x1 = k0 + 1 < valid ? s0[1] * scale_log2 : -INFINITY;
-  x2 = k2 < valid ? s1[0] * scale_log2 : -INFINITY;
-  x3 = k2 + 1 < valid ? s1[1] * scale_log2 : -INFINITY;
+  x0 = head_on && k0 < valid ? s0[0] * scale_log2 : -INFINITY;
+  x1 = head_on && k0 + 1 < valid ? s0[1] * scale_log2 : -INFINITY;
+  x2 = head_on && k2 < valid ? s1[0] * scale_log2 : -INFINITY;
+  x3 = head_on && k2 + 1 < valid ? s1[1] * scale_log2 : -INFINITY;
   float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   const float m_new = fmaxf(st.m, mx);
-  const float alpha = exp2f(st.m - m_new);
-  const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
-  const float p2 = exp2f(x2 - m_new), p3 = exp2f(x3 - m_new);
+  const float m_ref = m_new == -INFINITY ? 0.f : m_new;  // nothing seen yet: alpha and p come out 0
+  const float alpha = exp2f(st.m - m_ref);
+  const float p0 = exp2f(x0 - m_ref), p1 = exp2f(x1 - m_ref);
+  const float p2 = exp2f(x2 - m_ref), p3 = exp2f(x3 - m_ref);
   st.l = st.l * alpha + ((p0 + p1) + (p2 + p3));
   st.m = m_new;
 #pragma unroll
@@ -98,6 +101,105 @@ __device__ __forceinline__ void attend_tile(uint32_t kb, uint32_t vb, const uint
     }
     mma_bf16_16816(st.o[2 * j], hi01, lo01, hi23, lo23, b0, b1);
     mma_bf16_16816(st.o[2 * j + 1], hi01, lo01, hi23, lo23, b2, b3);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-KV partial results of one (sequence, kv head): a slot per split holds
+// every head's running max M (log2 domain), sum L and unnormalised O.
+constexpr int kTileMaxG = 8;
+constexpr int kTileD = 128;
+constexpr int kTileMaxSplits = 64;
+constexpr int kPartFloats = kTileMaxG * (kTileD + 2);  // [M x 8][L x 8][O 8 x 128]
+
+// Merge the kWarps warps' tile states of one CTA into its split slot.  wo:
+// shared scratch of kWarps x kTileMaxG x (kTileD + 2) floats.  Every thread
+// of the CTA calls it (it synchronises the block).
+template <int kWarps>
+__device__ __forceinline__ void merge_warps_to_slot(const TileState& st, float* wo, float* slot, int G) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, qd = lane & 3;
+  float l = st.l;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  float* mine = wo + (warp * kTileMaxG + g) * (kTileD + 2);
+  if (g < G) {
+    if (qd == 0) {
+      mine[kTileD] = st.m;
+      mine[kTileD + 1] = l;
+    }
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      mine[8 * nt + 2 * qd] = st.o[nt][0] + st.o[nt][2];
+      mine[8 * nt + 2 * qd + 1] = st.o[nt][1] + st.o[nt][3];
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * kTileD; idx += kWarps * 32) {
+    const int gg = idx / kTileD, dd = idx % kTileD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wo[(w * kTileMaxG + gg) * (kTileD + 2) + kTileD]);
+    float L = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float* pw = wo + (w * kTileMaxG + gg) * (kTileD + 2);
+        const float f = pw[kTileD] == -INFINITY ? 0.f : exp2f(pw[kTileD] - M);
+        L += pw[kTileD + 1] * f;
+        acc += pw[dd] * f;
+      }
+    }
+    slot[2 * kTileMaxG + gg * kTileD + dd] = acc;
+    if (dd == 0) {
+      slot[gg] = M;
+      slot[kTileMaxG + gg] = L;
+    }
+  }
+}
+
+// Merge `splits` slots (consecutive, from `part`) into the G heads' outputs
+// out[(out_row0 + g) * 128 + d], fp32 or bf16.  scratch: 3 x kTileMaxSplits x
+// kTileMaxG + 2 x kTileMaxG floats of shared memory.  Every thread of the CTA
+// calls it.
+__device__ __forceinline__ void merge_split_slots(const float* part, int splits, int G, void* out, bool out_f32,
+                                                  size_t out_row0, float* scratch) {
+  float (*sm)[kTileMaxG] = reinterpret_cast<float (*)[kTileMaxG]>(scratch);
+  float (*sl)[kTileMaxG] = sm + kTileMaxSplits;
+  float (*sf)[kTileMaxG] = sl + kTileMaxSplits;
+  float* sM = &sf[kTileMaxSplits][0];
+  float* sI = sM + kTileMaxG;
+  for (int t = threadIdx.x; t < splits * G; t += blockDim.x) {  // every (split, head) at once
+    const int sp = t / G, gg = t % G;
+    const float* slot = part + size_t(sp) * kPartFloats;
+    sm[sp][gg] = slot[gg];
+    sl[sp][gg] = slot[kTileMaxG + gg];
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int gg = threadIdx.x;
+    float M = -INFINITY;
+    for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, sm[sp][gg]);
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int sp = 0; sp < splits; ++sp)
+        if (sm[sp][gg] != -INFINITY) L += sl[sp][gg] * exp2f(sm[sp][gg] - M);
+    sM[gg] = M;
+    sI[gg] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < splits * G; t += blockDim.x) {
+    const int sp = t / G, gg = t % G;
+    sf[sp][gg] = (sM[gg] != -INFINITY && sm[sp][gg] != -INFINITY) ? exp2f(sm[sp][gg] - sM[gg]) * sI[gg] : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * kTileD; idx += blockDim.x) {
+    const int gg = idx / kTileD, dd = idx % kTileD;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int sp = 0; sp < splits; ++sp) acc += sf[sp][gg] * part[size_t(sp) * kPartFloats + 2 * kTileMaxG + gg * kTileD + dd];
+    const size_t oi = (out_row0 + gg) * kTileD + dd;
+    if (out_f32) static_cast<float*>(out)[oi] = acc;
+    else static_cast<__nv_bfloat16*>(out)[oi] = __float2bfloat16_rn(acc);
   }
 }
 

@@ -1,0 +1,599 @@
+// Quest page selection for GQA decode (sm_103a).
+//
+// What it computes ("Long context, KV eviction and sparse attention", the
+// sparse-selection section: Quest bounds a page's attention logit by the
+// elementwise min and max of its keys and keeps the best pages).  For
+// sequence b (S_b keys once the new token is appended) and q head h of kv
+// head h / G:
+//   bound[b, h, p] = sum_d max(q_d * kmin[p]_d, q_d * kmax[p]_d)   for every
+//                    full page p < S_b / 16
+//   pages[b, h]    = the budget_pages largest bounds, ties to the lower page
+//                    (every full page when there are no more), ascending
+//   o[b, h]        = softmax(scale * q . k) V over the tokens of pages[b, h]
+//                    and of the trailing partial page, which is always kept
+// Each q head chooses alone; the kv head streams the union of its heads'
+// pages once and masks, per page, the heads that did not choose it.
+//
+// The bound uses max(q x, q y) = q (x + y) / 2 + |q| (y - x) / 2 for x <= y,
+// which is the same number with two FMAs per (dimension, head) instead of two
+// products, a max and an add.
+//
+// Kernels:
+//   qu_meta_kernel   builds the per-page min / max of a prompt's keys: one
+//                    warp per (page, kv head), a partial page over its valid
+//                    tokens.
+//   qu_bound_kernel  (page chunk, kv head, sequence), 8 warps: the CTA whose
+//                    chunk holds the new token's page appends it (K and V
+//                    rows, and the page's min / max) before its own bounds;
+//                    then one warp per full page (four pages in flight per
+//                    warp): lane l reads dimensions 4l..4l+3 of the page's
+//                    min and max rows (bf16, 512 bytes a page, coalesced),
+//                    holds the same dimensions of the G heads' q in
+//                    registers, and a transposing shuffle reduction (9
+//                    shuffles) leaves head (l / 4) % 8's bound on lane l.
+//   qu_topk_kernel   (q head, sequence): row_topk of the head's bounds, the
+//                    kept pages marked in the kv head's page mask; the last of
+//                    the G heads to finish lists the marked pages in ascending
+//                    order with their head masks (the partial page last, for
+//                    every head) and clears the mask.
+//   qu_attn_kernel   (split, kv head, sequence), 4 warps: one 16-key tile per
+//                    listed page (cp.async gather of its K and V rows into the
+//                    swizzled tile, three stages per warp: two pages in
+//                    flight while one is computed), attend_tile with the
+//                    page's head mask;
+//                    the last split of a (sequence, kv head) merges the
+//                    splits into O and the last kv head publishes the length.
+#include "attn_tile.cuh"
+#include "row_topk.cuh"
+
+namespace kvsel {
+
+constexpr int kQuD = 128;
+constexpr int kQuPage = 16;
+constexpr int kQuMaxG = kTileMaxG;
+constexpr int kQuBoundThreads = 256;
+constexpr int kQuBoundPagesPerCta = 256;
+constexpr int kQuTopkGroups = 8;          // rows up to 32K pages stay in registers
+constexpr int kQuAttnWarps = 4;
+constexpr int kQuAttnStages = 3;          // per warp
+// the warps' merge scratch reuses the ring once every warp is done with it
+constexpr size_t kQuAttnSmem = size_t(kQuAttnWarps) * kQuAttnStages * 8192 + 1024;
+static_assert(size_t(kQuAttnWarps) * kTileMaxG * (kTileD + 2) * 4 <= size_t(kQuAttnWarps) * kQuAttnStages * 8192,
+              "merge scratch fits in the ring");
+
+struct QuParams {
+  const int32_t* block_table;    // [B][max_pages]
+  int32_t* seq_lens;             // [B]
+  const __nv_bfloat16* q;        // [B][Hq][128]
+  const __nv_bfloat16* k_new;    // [B][Hkv][128] or null
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_pool;
+  __nv_bfloat16* v_pool;
+  __nv_bfloat16* meta;           // [num_pages][Hkv][2][128]: min row, max row
+  float* bounds;                 // [B][Hq][max_pages]
+  int32_t* sel;                  // [B][Hq][budget]
+  uint32_t* mask;                // [B][Hkv][max_pages]: heads that chose each page (zero between calls)
+  int32_t* ulist;                // [B][Hkv][max_pages]: listed pages, ascending
+  uint32_t* umask;               // [B][Hkv][max_pages]: their head masks
+  int32_t* ucount;               // [B][Hkv]
+  unsigned* topk_cnt;            // [B][Hkv]: heads done (the last one lists)
+  unsigned* merge_cnt;           // [B][Hkv]: splits done (the last one merges)
+  unsigned* seq_cnt;             // [B]: kv heads merged (the last one publishes the length)
+  float* part;                   // [B][Hkv][splits][kPartFloats]
+  void* out;
+  int* status;
+  int B, max_pages, Hq, Hkv, G, num_pages, budget, chunks, splits, appended, out_f32;
+  float scale_log2;
+};
+
+__device__ __forceinline__ bool qu_len_ok(const QuParams& P, int b, int& S) {
+  S = P.seq_lens[b] + P.appended;
+  return S >= 0 && (S + kQuPage - 1) / kQuPage <= P.max_pages;
+}
+
+__device__ __forceinline__ int qu_phys(const QuParams& P, int b, int page) {
+  int phys = P.block_table[size_t(b) * P.max_pages + page];
+  if (unsigned(phys) >= unsigned(P.num_pages)) {
+    report(P.status, KVSEL_ERR_BAD_INDEX);
+    phys = 0;
+  }
+  return phys;
+}
+
+__device__ __forceinline__ void qu_cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ float bf16_at(uint4 v, int i) {
+  const uint32_t w = (&v.x)[i >> 1];
+  return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// ---------------------------------------------------------------------------
+// Page min / max of a prompt: grid (ceil(max_pages / 4), Hkv, B), 4 warps, one
+// page each; lane l owns dimensions 4l .. 4l + 3.
+struct QuMetaParams {
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const __nv_bfloat16* k_pool;
+  __nv_bfloat16* meta;
+  int* status;
+  int max_pages, Hkv, num_pages;
+};
+__global__ void __launch_bounds__(128) qu_meta_kernel(const QuMetaParams P) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int page = blockIdx.x * 4 + warp, kvh = blockIdx.y, b = blockIdx.z;
+  const int S = P.seq_lens[b];
+  if (S < 0 || (S + kQuPage - 1) / kQuPage > P.max_pages) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
+    return;
+  }
+  if (page * kQuPage >= S) return;
+  const int n = min(kQuPage, S - page * kQuPage);
+  int phys = P.block_table[size_t(b) * P.max_pages + page];
+  if (unsigned(phys) >= unsigned(P.num_pages)) {
+    if (lane == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
+    return;
+  }
+  const __nv_bfloat16* rows = P.k_pool + (size_t(phys) * P.Hkv + kvh) * kQuPage * kQuD;
+  float mn[4], mx[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    mn[i] = INFINITY;
+    mx[i] = -INFINITY;
+  }
+  for (int r = 0; r < n; ++r) {
+    const uint2 v = *reinterpret_cast<const uint2*>(rows + size_t(r) * kQuD + 4 * lane);
+    const uint4 w = make_uint4(v.x, v.y, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float x = bf16_at(w, i);
+      mn[i] = fminf(mn[i], x);
+      mx[i] = fmaxf(mx[i], x);
+    }
+  }
+  // min / max of bf16 values are bf16 values: the conversion back is exact
+  __nv_bfloat16* m = P.meta + (size_t(phys) * P.Hkv + kvh) * 2 * kQuD;
+  *reinterpret_cast<uint2*>(m + 4 * lane) = make_uint2(pack_bf16x2(mn[0], mn[1]), pack_bf16x2(mn[2], mn[3]));
+  *reinterpret_cast<uint2*>(m + kQuD + 4 * lane) =
+      make_uint2(pack_bf16x2(mx[0], mx[1]), pack_bf16x2(mx[2], mx[3]));
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kQuBoundThreads) qu_bound_kernel(const QuParams P) {
+  const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  int S;
+  if (!qu_len_ok(P, b, S)) {
+    if (chunk == 0 && kvh == 0 && tid == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
+    return;
+  }
+  const int npg = (S + kQuPage - 1) / kQuPage, n_full = S / kQuPage;
+  const int p0 = int((long long)chunk * npg / P.chunks), p1 = int((long long)(chunk + 1) * npg / P.chunks);
+  const int G = P.G;
+  const int S_old = S - P.appended;
+  const int pa = S_old / kQuPage;
+  if (P.appended && pa >= p0 && pa < p1) {
+    // the new token: K and V rows, then the page's min / max (first token: itself)
+    const int phys = qu_phys(P, b, pa);
+    const size_t row = (size_t(phys) * P.Hkv + kvh) * kQuPage + (S_old % kQuPage);
+    const __nv_bfloat16* kn = P.k_new + (size_t(b) * P.Hkv + kvh) * kQuD;
+    const __nv_bfloat16* vn = P.v_new + (size_t(b) * P.Hkv + kvh) * kQuD;
+    if (tid < 16) reinterpret_cast<uint4*>(P.k_pool + row * kQuD)[tid] = reinterpret_cast<const uint4*>(kn)[tid];
+    else if (tid < 32) reinterpret_cast<uint4*>(P.v_pool + row * kQuD)[tid - 16] = reinterpret_cast<const uint4*>(vn)[tid - 16];
+    else if (tid < 48) {
+      const int u = tid - 32;  // 8 dimensions
+      __nv_bfloat16* m = P.meta + (size_t(phys) * P.Hkv + kvh) * 2 * kQuD;
+      const uint4 x = reinterpret_cast<const uint4*>(kn)[u];
+      uint4 lo = x, hi = x;
+      if (S_old % kQuPage != 0) {
+        const uint4 a = __ldcg(reinterpret_cast<const uint4*>(m) + u);
+        const uint4 c = __ldcg(reinterpret_cast<const uint4*>(m + kQuD) + u);
+        uint32_t* lw = &lo.x;
+        uint32_t* hw = &hi.x;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          lw[i] = pack_bf16x2(fminf(bf16_at(a, 2 * i), bf16_at(x, 2 * i)), fminf(bf16_at(a, 2 * i + 1), bf16_at(x, 2 * i + 1)));
+          hw[i] = pack_bf16x2(fmaxf(bf16_at(c, 2 * i), bf16_at(x, 2 * i)), fmaxf(bf16_at(c, 2 * i + 1), bf16_at(x, 2 * i + 1)));
+        }
+      }
+      reinterpret_cast<uint4*>(m)[u] = lo;
+      reinterpret_cast<uint4*>(m + kQuD)[u] = hi;
+    }
+  }
+  // lane l holds dimensions 4l .. 4l + 3 of the G heads' q (zero for heads >= G)
+  const int warp = tid >> 5, lane = tid & 31;
+  float qv[kQuMaxG][4], qa[kQuMaxG][4];
+#pragma unroll
+  for (int g = 0; g < kQuMaxG; ++g) {
+    uint2 w = make_uint2(0u, 0u);
+    if (g < G) w = *reinterpret_cast<const uint2*>(P.q + (size_t(b) * P.Hq + size_t(kvh) * G + g) * kQuD + 4 * lane);
+    const uint4 x = make_uint4(w.x, w.y, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      qv[g][i] = bf16_at(x, i);
+      qa[g][i] = fabsf(qv[g][i]);
+    }
+  }
+  __syncthreads();  // orders the append's min / max before the reads below
+  const int pe = min(p1, n_full);
+  float* bnd = P.bounds + (size_t(b) * P.Hq + size_t(kvh) * G) * P.max_pages;
+  const int hsel = (lane >> 2) & 7;  // the head whose sum this lane ends with
+  constexpr int kWarps = kQuBoundThreads / 32;
+  constexpr int kAhead = 4;          // pages per warp in flight
+#pragma unroll 1
+  for (int pb = p0 + warp * kAhead; pb < pe; pb += kWarps * kAhead) {
+    uint2 lo[kAhead], hi[kAhead];
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) {
+      lo[j] = hi[j] = make_uint2(0u, 0u);
+      if (pb + j < pe) {
+        const uint2* m = reinterpret_cast<const uint2*>(
+            P.meta + (size_t(qu_phys(P, b, pb + j)) * P.Hkv + kvh) * 2 * kQuD);
+        lo[j] = __ldcg(m + lane);
+        hi[j] = __ldcg(m + kQuD / 4 + lane);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) {
+      const uint4 a = make_uint4(lo[j].x, lo[j].y, 0u, 0u), z = make_uint4(hi[j].x, hi[j].y, 0u, 0u);
+      float mid[4], rad[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float l = bf16_at(a, i), h = bf16_at(z, i);
+        mid[i] = 0.5f * (l + h);
+        rad[i] = 0.5f * (h - l);
+      }
+      float u[kQuMaxG];
+#pragma unroll
+      for (int g = 0; g < kQuMaxG; ++g) {
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t = fmaf(qv[g][i], mid[i], fmaf(qa[g][i], rad[i], t));
+        u[g] = t;
+      }
+      // transposing reduction over the 32 lanes: 8 sums with 4 + 2 + 1 + 2 shuffles;
+      // lane l ends with head (l >> 2) & 7
+      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+      float v[4];
+#pragma unroll
+      for (int j2 = 0; j2 < 4; ++j2) {
+        const float send = b4 ? u[j2] : u[j2 + 4], keep = b4 ? u[j2 + 4] : u[j2];
+        v[j2] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+      float w2[2];
+#pragma unroll
+      for (int j2 = 0; j2 < 2; ++j2) {
+        const float send = b3 ? v[j2] : v[j2 + 2], keep = b3 ? v[j2 + 2] : v[j2];
+        w2[j2] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+      float x = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+      x += __shfl_xor_sync(0xffffffffu, x, 1);
+      x += __shfl_xor_sync(0xffffffffu, x, 2);
+      if ((lane & 3) == 0 && hsel < G && pb + j < pe) bnd[size_t(hsel) * P.max_pages + pb + j] = x;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
+  extern __shared__ __align__(16) uint8_t tk_smem[];
+  RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
+  __shared__ int s_last;
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int G = P.G, kvh = h / G, g = h % G;
+  int S;
+  if (!qu_len_ok(P, b, S)) return;
+  const int n_full = S / kQuPage, k = P.budget;
+  int32_t* sel = P.sel + (size_t(b) * P.Hq + h) * k;
+  uint32_t* msk = P.mask + (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  const uint32_t bit = 1u << g;
+  if (n_full <= k) {
+    for (int i = tid; i < k; i += kRkThreads) {
+      sel[i] = i < n_full ? i : -1;
+      if (i < n_full) atomicOr(msk + i, bit);
+    }
+  } else {
+    const float* row = P.bounds + (size_t(b) * P.Hq + h) * P.max_pages;
+    const F32RowKeys src{row, 0, n_full, (reinterpret_cast<uintptr_t>(row) & 15u) == 0};
+    row_topk<kQuTopkGroups>(src, k, 0u, sm, [&](int i, int p) {
+      sel[i] = p;
+      atomicOr(msk + p, bit);
+    });
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    unsigned* cnt = P.topk_cnt + size_t(b) * P.Hkv + kvh;
+    s_last = atomicAdd(cnt, 1u) + 1u == unsigned(G);
+    if (s_last) {
+      *cnt = 0u;  // every head has arrived: ready for the next call
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // list the marked pages in ascending order (block scan per round of 1024)
+  int32_t* ul = P.ulist + (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  uint32_t* um = P.umask + (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  uint32_t total_all = 0;
+  for (int r0 = 0; r0 < n_full; r0 += kRkThreads) {
+    const int i = r0 + tid;
+    const uint32_t m = i < n_full ? __ldcg(msk + i) : 0u;
+    uint32_t tot;
+    const uint32_t off = rk_block_excl_scan(m != 0u ? 1u : 0u, sm.wtot[0], tot);
+    if (m != 0u) {
+      ul[total_all + off] = i;
+      um[total_all + off] = m;
+      msk[i] = 0u;
+    }
+    total_all += tot;
+  }
+  if (tid == 0) {
+    int n = int(total_all);
+    if (S % kQuPage != 0) {  // the partial page, for every head
+      ul[n] = n_full;
+      um[n] = (G >= 32) ? 0xFFFFFFFFu : ((1u << G) - 1u);
+      ++n;
+    }
+    P.ucount[size_t(b) * P.Hkv + kvh] = n;
+  }
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kQuAttnWarps * 32) qu_attn_kernel(const QuParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* wo = reinterpret_cast<float*>(smem);  // after the page loop
+  __shared__ int s_last;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int S;
+  if (!qu_len_ok(P, b, S)) return;
+  const int n = P.ucount[size_t(b) * P.Hkv + kvh];
+  const int n_full = S / kQuPage, tail = S % kQuPage;
+  const int t0 = int((long long)split * n / P.splits), t1 = int((long long)(split + 1) * n / P.splits);
+  const int G = P.G, g = lane >> 2, qd = lane & 3;
+  const bool head_ok = g < G;
+  const int32_t* ul = P.ulist + (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  const uint32_t* um = P.umask + (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  const uint32_t wbuf = smem_u32(smem + warp * kQuAttnStages * 8192);
+
+  uint32_t qa[8][2];
+  load_q_frags(P.q + (size_t(b) * P.Hq + kvh * G + (head_ok ? g : 0)) * kQuD, head_ok, qd, qa);
+  TileState st;
+  st.init();
+
+  // page t of the list into stage s: its 16 K rows then 16 V rows (rows past a
+  // partial page's tokens are zero-filled)
+  auto gather = [&](int t, int s) {
+    const int page = ul[t];
+    const int valid = page == n_full ? tail : kQuPage;
+    const size_t base = ((size_t(qu_phys(P, b, page)) * P.Hkv + kvh) * kQuPage) * kQuD;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = lane + 32 * i;
+      const int row = c >> 4, u = c & 15;
+      const int r16 = row & 15;
+      const __nv_bfloat16* src = (row < 16 ? P.k_pool : P.v_pool) + base + size_t(r16) * kQuD + u * 8;
+      qu_cp_async16(wbuf + s * 8192 + (row < 16 ? 0 : 4096) + tile_unit_off(r16, u), src, r16 < valid);
+    }
+  };
+  auto commit = []() { asm volatile("cp.async.commit_group;" ::: "memory"); };
+
+  // every iteration commits one group (empty past the end), so the current
+  // page's group is always the third most recent
+  int t = t0 + warp;
+#pragma unroll
+  for (int k = 0; k < kQuAttnStages - 1; ++k) {
+    if (t + k * kQuAttnWarps < t1) gather(t + k * kQuAttnWarps, k);
+    commit();
+  }
+  int s = 0;
+#pragma unroll 1
+  for (; t < t1; t += kQuAttnWarps) {
+    const int tn = t + (kQuAttnStages - 1) * kQuAttnWarps;
+    if (tn < t1) gather(tn, s == 0 ? kQuAttnStages - 1 : s - 1);
+    commit();
+    asm volatile("cp.async.wait_group %0;" ::"n"(kQuAttnStages - 1) : "memory");
+    __syncwarp();
+    const int page = ul[t];
+    const bool on = head_ok && ((um[t] >> g) & 1u);
+    float x0, x1, x2, x3;
+    attend_tile(wbuf + s * 8192, wbuf + s * 8192 + 4096, qa, page == n_full ? tail : kQuPage, P.scale_log2, st,
+                x0, x1, x2, x3, on);
+    __syncwarp();
+    s = s + 1 == kQuAttnStages ? 0 : s + 1;
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();  // every warp is done with the ring: it becomes the merge scratch
+  float* slot = P.part + ((size_t(b) * P.Hkv + kvh) * P.splits + split) * kPartFloats;
+  merge_warps_to_slot<kQuAttnWarps>(st, wo, slot, G);
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    unsigned* cnt = P.merge_cnt + size_t(b) * P.Hkv + kvh;
+    s_last = atomicAdd(cnt, 1u) + 1u == unsigned(P.splits);
+    if (s_last) {
+      *cnt = 0u;
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (s_last) {
+    merge_split_slots(P.part + (size_t(b) * P.Hkv + kvh) * P.splits * kPartFloats, P.splits, G, P.out,
+                      P.out_f32 != 0, size_t(b) * P.Hq + size_t(kvh) * G, reinterpret_cast<float*>(smem));
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      if (atomicAdd(P.seq_cnt + b, 1u) + 1u == unsigned(P.Hkv)) {
+        P.seq_cnt[b] = 0u;
+        P.seq_lens[b] = S;  // every CTA of this sequence has read the old length
+      }
+    }
+  }
+}
+
+}  // namespace kvsel
+
+using namespace kvsel;
+using namespace kvsel_host;
+
+namespace {
+struct QuWs {
+  size_t cnt, bounds, sel, mask, ulist, umask, ucount, part, total;
+};
+QuWs qu_ws_layout(int batch, int Hq, int Hkv, int max_pages, int budget, bool own_bounds, bool own_sel) {
+  QuWs w;
+  size_t off = kStatusBytes;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  w.cnt = take((size_t(batch) * Hkv * 2 + batch) * 4);
+  w.bounds = own_bounds ? take(size_t(batch) * Hq * max_pages * 4) : 0;
+  w.sel = own_sel ? take(size_t(batch) * Hq * budget * 4) : 0;
+  w.mask = take(size_t(batch) * Hkv * max_pages * 4);
+  w.ulist = take(size_t(batch) * Hkv * max_pages * 4);
+  w.umask = take(size_t(batch) * Hkv * max_pages * 4);
+  w.ucount = take(size_t(batch) * Hkv * 4);
+  w.part = take(size_t(batch) * Hkv * kTileMaxSplits * kPartFloats * 4);
+  w.total = off;
+  return w;
+}
+}  // namespace
+
+extern "C" kvsel_status kvsel_quest_page_meta(const kvsel_paged_kv* kv, const int32_t* block_table, int max_pages,
+                                              const int32_t* seq_lens, int batch, void* page_meta,
+                                              void* status_word, void* stream) {
+  const std::string fn = "kvsel_quest_page_meta: ";
+  if (!kv || !kv->k_pool || !block_table || !seq_lens || !page_meta || !status_word || batch < 1 || max_pages < 1)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "kv, block_table, seq_lens, page_meta, status_word required; "
+                                            "batch, max_pages >= 1");
+  if (kv->head_dim != kQuD || kv->page_size != kQuPage)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16 are implemented");
+  if (kv->num_kv_heads < 1 || kv->num_pages < 1 || batch > 65535 || kv->num_kv_heads > 65535)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "num_kv_heads and num_pages >= 1; batch, num_kv_heads <= 65535");
+  if (!aligned(kv->k_pool, 16) || !aligned(page_meta, 16) || !aligned(status_word, 4))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "K pool and page_meta must be 16-byte aligned");
+  QuMetaParams P;
+  P.block_table = block_table;
+  P.seq_lens = seq_lens;
+  P.k_pool = static_cast<const __nv_bfloat16*>(kv->k_pool);
+  P.meta = static_cast<__nv_bfloat16*>(page_meta);
+  P.status = static_cast<int*>(status_word);
+  P.max_pages = max_pages;
+  P.Hkv = kv->num_kv_heads;
+  P.num_pages = kv->num_pages;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  trace_before("qu_meta", st);
+  qu_meta_kernel<<<dim3((max_pages + 3) / 4, P.Hkv, batch), 128, 0, st>>>(P);
+  const cudaError_t e = cudaGetLastError();
+  trace_after(st);
+  if (e != cudaSuccess) return cuda_fail(e, "kvsel_quest_page_meta (launch)");
+  return KVSEL_OK;
+}
+
+extern "C" size_t kvsel_quest_decode_workspace(const kvsel_paged_kv* kv, int batch, int max_pages, int budget_pages,
+                                               int with_bounds_out, int with_pages_out) {
+  if (!kv || batch < 1 || max_pages < 1 || budget_pages < 1 || kv->num_kv_heads < 1 ||
+      kv->num_q_heads % kv->num_kv_heads != 0)
+    return 0;
+  return qu_ws_layout(batch, kv->num_q_heads, kv->num_kv_heads, max_pages, budget_pages, with_bounds_out == 0,
+                      with_pages_out == 0).total;
+}
+
+extern "C" kvsel_status kvsel_quest_decode(const kvsel_paged_kv* kv, const int32_t* block_table, int max_pages,
+                                           int32_t* seq_lens, int batch, const void* q, const void* k_new,
+                                           const void* v_new, void* page_meta, int budget_pages, float scale,
+                                           void* out, int out_dtype, int32_t* pages_out, float* bounds_out,
+                                           void* workspace, size_t ws_bytes, void* stream) {
+  const std::string fn = "kvsel_quest_decode: ";
+  if (!kv || !kv->k_pool || !kv->v_pool) return fail(KVSEL_ERR_INVALID_ARG, fn + "kv pools must be non-NULL");
+  if (kv->head_dim != kQuD || kv->page_size != kQuPage)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16 are implemented");
+  if (kv->num_kv_heads < 1 || kv->num_q_heads < 1 || kv->num_q_heads % kv->num_kv_heads != 0)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "num_q_heads must be a positive multiple of num_kv_heads");
+  const int Hkv = kv->num_kv_heads, Hq = kv->num_q_heads, G = Hq / Hkv;
+  if (G > kQuMaxG) return fail(KVSEL_ERR_UNSUPPORTED, fn + "at most 8 q heads per kv head");
+  if (!block_table || !seq_lens || !q || !out || !page_meta || batch < 1 || max_pages < 1 || budget_pages < 1)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "block_table, seq_lens, q, out, page_meta are required; batch, "
+                                            "max_pages, budget_pages >= 1");
+  if ((k_new == nullptr) != (v_new == nullptr))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "k_new and v_new must both be given or both NULL");
+  if (out_dtype != KVSEL_BF16 && out_dtype != KVSEL_F32)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "out_dtype must be KVSEL_BF16 or KVSEL_F32");
+  if (batch > 65535 || Hq > 65535 || (long long)max_pages * kQuPage >= (1LL << 31) ||
+      (long long)kv->num_pages * Hkv * kQuPage >= (1LL << 31) || kv->num_pages < 1)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "batch, num_q_heads <= 65535; max_pages * 16 and num_pages * "
+                                            "num_kv_heads * 16 < 2^31");
+  if (!aligned(kv->k_pool, 16) || !aligned(kv->v_pool, 16) || !aligned(q, 16) || !aligned(page_meta, 16) ||
+      (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "pools, q, k_new, v_new and page_meta must be 16-byte aligned");
+  const QuWs L = qu_ws_layout(batch, Hq, Hkv, max_pages, budget_pages, bounds_out == nullptr, pages_out == nullptr);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace missing, misaligned or smaller than " +
+                                           std::to_string(L.total));
+
+  const int sms = sm_count();
+  const int list_max = std::min(max_pages, G * budget_pages + 1);
+  int splits = std::max(1, (sms * 2) / (batch * Hkv));  // one wave at two CTAs per SM
+  splits = std::min(splits, std::max(1, (list_max + 7) / 8));
+  splits = std::min(splits, kTileMaxSplits);
+  const int chunks = std::max(1, std::min(65535, (max_pages + kQuBoundPagesPerCta - 1) / kQuBoundPagesPerCta));
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  QuParams P;
+  P.block_table = block_table;
+  P.seq_lens = seq_lens;
+  P.q = static_cast<const __nv_bfloat16*>(q);
+  P.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  P.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  P.k_pool = static_cast<__nv_bfloat16*>(kv->k_pool);
+  P.v_pool = static_cast<__nv_bfloat16*>(kv->v_pool);
+  P.meta = static_cast<__nv_bfloat16*>(page_meta);
+  P.bounds = bounds_out ? bounds_out : reinterpret_cast<float*>(ws + L.bounds);
+  P.sel = pages_out ? pages_out : reinterpret_cast<int32_t*>(ws + L.sel);
+  P.mask = reinterpret_cast<uint32_t*>(ws + L.mask);
+  P.ulist = reinterpret_cast<int32_t*>(ws + L.ulist);
+  P.umask = reinterpret_cast<uint32_t*>(ws + L.umask);
+  P.ucount = reinterpret_cast<int32_t*>(ws + L.ucount);
+  P.topk_cnt = reinterpret_cast<unsigned*>(ws + L.cnt);
+  P.merge_cnt = P.topk_cnt + size_t(batch) * Hkv;
+  P.seq_cnt = P.merge_cnt + size_t(batch) * Hkv;
+  P.part = reinterpret_cast<float*>(ws + L.part);
+  P.out = out;
+  P.status = reinterpret_cast<int*>(ws);
+  P.B = batch;
+  P.max_pages = max_pages;
+  P.Hq = Hq;
+  P.Hkv = Hkv;
+  P.G = G;
+  P.num_pages = kv->num_pages;
+  P.budget = budget_pages;
+  P.chunks = chunks;
+  P.splits = splits;
+  P.appended = k_new ? 1 : 0;
+  P.out_f32 = out_dtype == KVSEL_F32;
+  P.scale_log2 = scale * 1.4426950408889634f;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  {
+    cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(qu_attn_kernel), int(kQuAttnSmem));
+    if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(qu_topk_kernel), int(sizeof(RowTopkSmem)));
+    if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_quest_decode (attribute)");
+  }
+  cudaError_t e;
+#define KVSEL_QU_LAUNCH(name, kernel, grid, block, smem)                 \
+  trace_before(name, st);                                                \
+  kernel<<<grid, block, smem, st>>>(P);                                  \
+  e = cudaGetLastError();                                                \
+  trace_after(st);                                                       \
+  if (e != cudaSuccess) return cuda_fail(e, "kvsel_quest_decode (" name ")");
+  KVSEL_QU_LAUNCH("qu_bound", qu_bound_kernel, dim3(chunks, Hkv, batch), kQuBoundThreads, 0)
+  KVSEL_QU_LAUNCH("qu_topk", qu_topk_kernel, dim3(Hq, batch), kRkThreads, sizeof(RowTopkSmem))
+  KVSEL_QU_LAUNCH("qu_attn", qu_attn_kernel, dim3(splits, Hkv, batch), kQuAttnWarps * 32, kQuAttnSmem)
+#undef KVSEL_QU_LAUNCH
+  return KVSEL_OK;
+}

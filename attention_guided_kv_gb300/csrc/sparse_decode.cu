@@ -42,9 +42,9 @@ constexpr int kSdMaxHi = 8;
 constexpr int kSdTopkGroups = 8;         // rows up to 32K stay in registers; longer rows are swept
 constexpr int kSdChunk = 16384;          // positions per first-stage top-k chunk (top_k < kSdChunk)
 constexpr int kSdMaxLen = 1 << 28;
-constexpr int kSdMaxSplits = 64;
-constexpr int kSdMaxG = 8;
-constexpr int kSdPartFloats = kSdMaxG * (kSdD + 2);
+constexpr int kSdMaxSplits = kTileMaxSplits;
+constexpr int kSdMaxG = kTileMaxG;
+constexpr int kSdPartFloats = kPartFloats;
 constexpr int kSdAttnWarps = 4;
 constexpr size_t kSdAttnSmem = size_t(kSdAttnWarps) * 2 * 8192 + 1024 +
                                size_t(kSdAttnWarps) * kSdMaxG * (kSdD + 2) * 4;
@@ -260,8 +260,6 @@ __global__ void __launch_bounds__(kRkThreads) sd_topk_kernel(const SdParams P) {
   if (tid == 0) P.nsel[b] = k;
 }
 
-__device__ void sd_merge_splits(const SdParams& P, int b, int kvh, float* scratch);
-
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -329,44 +327,8 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
     __syncwarp();
     s ^= 1;
   }
-  st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
-  st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
-  // merge the 4 warps
-  float* mine = wo + (warp * kSdMaxG + g) * (kSdD + 2);
-  if (head_ok) {
-    if (qd == 0) {
-      mine[kSdD] = st.m;
-      mine[kSdD + 1] = st.l;
-    }
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      mine[8 * nt + 2 * qd] = st.o[nt][0] + st.o[nt][2];
-      mine[8 * nt + 2 * qd + 1] = st.o[nt][1] + st.o[nt][3];
-    }
-  }
-  __syncthreads();
   float* slot = P.part + ((size_t(b) * P.Hkv + kvh) * P.splits + split) * kSdPartFloats;
-  for (int idx = tid; idx < G * kSdD; idx += blockDim.x) {
-    const int gg = idx / kSdD, dd = idx % kSdD;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kSdAttnWarps; ++w) M = fmaxf(M, wo[(w * kSdMaxG + gg) * (kSdD + 2) + kSdD]);
-    float L = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kSdAttnWarps; ++w) {
-        const float* pw = wo + (w * kSdMaxG + gg) * (kSdD + 2);
-        const float f = exp2f(pw[kSdD] - M);
-        L += pw[kSdD + 1] * f;
-        acc += pw[dd] * f;
-      }
-    }
-    slot[2 * kSdMaxG + gg * kSdD + dd] = acc;
-    if (dd == 0) {
-      slot[gg] = M;
-      slot[kSdMaxG + gg] = L;
-    }
-  }
+  merge_warps_to_slot<kSdAttnWarps>(st, wo, slot, G);
   // The last split of (sequence, kv head) to finish merges all of them into O;
   // the last kv head of a sequence to be merged publishes its length.
   __shared__ int s_last;
@@ -382,7 +344,8 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
   }
   __syncthreads();
   if (s_last) {
-    sd_merge_splits(P, b, kvh, reinterpret_cast<float*>(smem));
+    merge_split_slots(P.part + (size_t(b) * P.Hkv + kvh) * P.splits * kSdPartFloats, P.splits, G, P.out,
+                      P.out_f32 != 0, size_t(b) * P.Hq + size_t(kvh) * G, reinterpret_cast<float*>(smem));
     __syncthreads();
     if (tid == 0) {
       __threadfence();
@@ -391,53 +354,6 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
         P.seq_lens[b] = S;  // every CTA of this sequence has read the old length
       }
     }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Merge of the splits of one (sequence, kv head) into O, by one CTA of
-// kSdAttnWarps warps; `scratch` holds 3 x kSdMaxSplits x kSdMaxG + 2 x kSdMaxG floats.
-__device__ void sd_merge_splits(const SdParams& P, int b, int kvh, float* scratch) {
-  float (*sm)[kSdMaxG] = reinterpret_cast<float (*)[kSdMaxG]>(scratch);
-  float (*sl)[kSdMaxG] = sm + kSdMaxSplits;
-  float (*sf)[kSdMaxG] = sl + kSdMaxSplits;
-  float* sM = &sf[kSdMaxSplits][0];
-  float* sI = sM + kSdMaxG;
-  const size_t pbase = (size_t(b) * P.Hkv + kvh) * P.splits;
-  const int G = P.G;
-  for (int t = threadIdx.x; t < P.splits * G; t += blockDim.x) {  // every (split, head) at once
-    const int sp = t / G, gg = t % G;
-    const float* sl_ = P.part + (pbase + sp) * kSdPartFloats;
-    sm[sp][gg] = sl_[gg];
-    sl[sp][gg] = sl_[kSdMaxG + gg];
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
-    const int gg = threadIdx.x;
-    float M = -INFINITY;
-    for (int sp = 0; sp < P.splits; ++sp) M = fmaxf(M, sm[sp][gg]);
-    float L = 0.f;
-    if (M != -INFINITY)
-      for (int sp = 0; sp < P.splits; ++sp)
-        if (sm[sp][gg] != -INFINITY) L += sl[sp][gg] * exp2f(sm[sp][gg] - M);
-    sM[gg] = M;
-    sI[gg] = L > 0.f ? 1.f / L : 0.f;
-  }
-  __syncthreads();
-  for (int t = threadIdx.x; t < P.splits * G; t += blockDim.x) {
-    const int sp = t / G, gg = t % G;
-    sf[sp][gg] = (sM[gg] != -INFINITY && sm[sp][gg] != -INFINITY) ? exp2f(sm[sp][gg] - sM[gg]) * sI[gg] : 0.f;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * kSdD; idx += blockDim.x) {
-    const int gg = idx / kSdD, dd = idx % kSdD;
-    float acc = 0.f;
-#pragma unroll 8
-    for (int sp = 0; sp < P.splits; ++sp)
-      acc += sf[sp][gg] * P.part[(pbase + sp) * kSdPartFloats + 2 * kSdMaxG + gg * kSdD + dd];
-    const size_t oi = (size_t(b) * P.Hq + kvh * G + gg) * kSdD + dd;
-    if (P.out_f32) static_cast<float*>(P.out)[oi] = acc;
-    else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(acc);
   }
 }
 

@@ -616,12 +616,28 @@ def _setup_sparse_decode(dev, small=False):
         t = i % wl.steps
         run(i, q[t], qi[t], wi[t], kn[t], vn[t], kin[t])
 
+    # Quest page selection on the same cache: top_k / 16 pages (2048 tokens) per q head
+    budget_pages = wl.top_k // 16
+    meta = torch.zeros(wl.num_pages, wl.Hkv, 2, wl.d, dtype=torch.bfloat16, device=dev)
+    seq_q = seq0.clone()
+    ws_q = K.workspace(K.kvsel_quest_decode_workspace(kv, wl.B, wl.max_pages, budget_pages))
+    K.kvsel_quest_page_meta(kv, bt, seq_q, meta, ws_q)
+    out_q = torch.zeros_like(out)
+
+    def quest(i):
+        t = i % wl.steps
+        if t == 0 and i > 0:
+            seq_q.copy_(seq0)
+        K.kvsel_quest_decode(kv, bt, seq_q, q[t], meta, out_q, ws_q, budget_pages=budget_pages, k_new=kn[t],
+                             v_new=vn[t])
+
     S = wl.S0 + wl.steps // 2
     byts = {"sd_index": wl.B * S * (wl.Di * 2 + 4), "sd_attn": wl.B * wl.top_k * wl.Hkv * 512,
             "sd_topk_chunk": wl.B * S * 4, "sd_topk_final": wl.B * 9 * wl.top_k * 8}
     host_in = [("q", q), ("q_idx", qi), ("w_idx", wi), ("k_new", kn), ("v_new", vn), ("k_idx_new", kin)]
-    return dict(step=step, run=run, host_in=host_in, outs=[out, topk], ws=[ws], bytes=byts, flops={},
+    return dict(step=step, run=run, host_in=host_in, outs=[out, topk], ws=[ws, ws_q], bytes=byts, flops={},
                 per_step_launches=4, steps_cycle=wl.steps,
+                variant_runs=[(f"quest_{budget_pages}_pages_per_head", quest)], variants_key="variants_us_per_step",
                 config={"batch": wl.B, "context": wl.S0, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
                         "indexer": f"{wl.Hi} x {wl.Di}", "top_k": wl.top_k,
                         "l2": "inputs larger than L2 (67 MB indexer keys + 33.5 MB gathered K/V per step)"})

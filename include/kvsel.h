@@ -452,6 +452,63 @@ KVSEL_API kvsel_status kvsel_snapkv_select_ex(const kvsel_paged_kv* kv, const in
                                               int32_t* keep_out, float* vote_out, void* workspace,
                                               size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Quest page selection for decode ("Long context, KV eviction and sparse
+ * attention", sparse-selection section: a page's logit is bounded by the
+ * elementwise min and max of its keys, and the best-bounded pages are kept).
+ *
+ * Defines, for sequence b (S_b keys once the new token is appended) and q
+ * head h (kv head h / G):
+ *   bound[b][h][p] = sum_d max(q_d * kmin[p]_d, q_d * kmax[p]_d), for every
+ *                    full page p < S_b / 16 (kmin / kmax over its 16 keys)
+ *   pages[b][h]    = the budget_pages largest bounds, ties to the lower page
+ *                    (every full page when there are no more), ascending
+ *   out[b][h]      = softmax(scale * q . k) V over the tokens of pages[b][h]
+ *                    and those of the trailing partial page (always kept)
+ * Each q head chooses alone.
+ *
+ * Page metadata (both calls): page_meta bf16 [num_pages][num_kv_heads][2][128]
+ * indexed by PHYSICAL page: the min row, then the max row, of the page's keys
+ * (its valid keys for a partial page).  kvsel_quest_page_meta fills it for
+ * every page 0..ceil(seq_lens[b] / 16) - 1 of each sequence (after a prefill);
+ * kvsel_quest_decode keeps it current as it appends.
+ *
+ * kvsel_quest_page_meta arguments (device pointers): kv (K pool), block_table
+ * int32 [batch][max_pages], seq_lens int32 [batch] (not modified), page_meta,
+ * status_word: an int32 the kernel records KVSEL_ERR_BAD_INDEX in for a bad
+ * length or block-table entry (e.g. the start of a zeroed workspace).
+ *
+ * kvsel_quest_decode arguments (device pointers):
+ *   kv, block_table, max_pages, seq_lens, batch, q, k_new, v_new  as for
+ *                 kvsel_decode_attn (k_new / v_new both given or both NULL;
+ *                 seq_lens += 1 when appending, published at the end).
+ *   page_meta     as above; updated for the appended token's page.
+ *   budget_pages  >= 1 full pages per q head (budget / 16 tokens).
+ *   out           [batch][num_q_heads][128], bf16 or fp32 (out_dtype).
+ *   pages_out     int32 [batch][num_q_heads][budget_pages] or NULL: pages[b][h],
+ *                 -1 padded.
+ *   bounds_out    fp32 [batch][num_q_heads][max_pages] or NULL: bound[b][h][p]
+ *                 for p < S_b / 16 (the rest untouched).
+ *   workspace     >= kvsel_quest_decode_workspace(kv, batch, max_pages,
+ *                 budget_pages, bounds_out != NULL, pages_out != NULL) bytes,
+ *                 zeroed before its first use (it carries counters and page
+ *                 masks that every call leaves at zero).
+ * Limits: head_dim 128, page_size 16, G <= 8 (else UNSUPPORTED).
+ * Launches: bounds (+ append), per-head top-k (+ the kv head's page list),
+ * attention over the listed pages.
+ */
+KVSEL_API kvsel_status kvsel_quest_page_meta(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                             int max_pages, const int32_t* seq_lens, int batch,
+                                             void* page_meta, void* status_word, void* stream);
+KVSEL_API size_t kvsel_quest_decode_workspace(const kvsel_paged_kv* kv, int batch, int max_pages,
+                                              int budget_pages, int with_bounds_out, int with_pages_out);
+KVSEL_API kvsel_status kvsel_quest_decode(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                          int max_pages, int32_t* seq_lens, int batch, const void* q,
+                                          const void* k_new, const void* v_new, void* page_meta,
+                                          int budget_pages, float scale, void* out, int out_dtype,
+                                          int32_t* pages_out, float* bounds_out, void* workspace,
+                                          size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
