@@ -14,9 +14,8 @@
 // Each q head chooses alone; the kv head streams the union of its heads'
 // pages once and masks, per page, the heads that did not choose it.
 //
-// The bound uses max(q x, q y) = q (x + y) / 2 + |q| (y - x) / 2 for x <= y,
-// which is the same number with two FMAs per (dimension, head) instead of two
-// products, a max and an add.
+// The bound uses max(q x, q y) = q+ y + q- x for x <= y (q+ = max(q, 0), q- =
+// min(q, 0)): a plain dot product of bf16 values, run on the tensor cores.
 //
 // Kernels:
 //   qu_meta_kernel   builds the per-page min / max of a prompt's keys: one
@@ -25,12 +24,10 @@
 //   qu_bound_kernel  (page chunk, kv head, sequence), 8 warps: the CTA whose
 //                    chunk holds the new token's page appends it (K and V
 //                    rows, and the page's min / max) before its own bounds;
-//                    then one warp per full page (four pages in flight per
-//                    warp): lane l reads dimensions 4l..4l+3 of the page's
-//                    min and max rows (bf16, 512 bytes a page, coalesced),
-//                    holds the same dimensions of the G heads' q in
-//                    registers, and a transposing shuffle reduction (9
-//                    shuffles) leaves head (l / 4) % 8's bound on lane l.
+//                    then the bounds of 16 full pages x 8 heads per warp
+//                    tile on the tensor cores (mma.sync: the pages' [min |
+//                    max] rows, 512 bytes each, against the heads' [q- | q+],
+//                    see below).
 //   qu_topk_kernel   (q head, sequence): row_topk of the head's bounds, the
 //                    kept pages marked in the kv head's page mask; the last of
 //                    the G heads to finish lists the marked pages in ascending
@@ -74,6 +71,7 @@ struct QuParams {
   int32_t* sel;                  // [B][Hq][budget]
   uint32_t* mask;                // [B][Hkv][max_pages]: heads that chose each page (zero between calls)
   int32_t* ulist;                // [B][Hkv][max_pages]: listed pages, ascending
+  int32_t* uphys;                // [B][Hkv][max_pages]: their physical pages
   uint32_t* umask;               // [B][Hkv][max_pages]: their head masks
   int32_t* ucount;               // [B][Hkv]
   unsigned* topk_cnt;            // [B][Hkv]: heads done (the last one lists)
@@ -201,76 +199,75 @@ __global__ void __launch_bounds__(kQuBoundThreads) qu_bound_kernel(const QuParam
       reinterpret_cast<uint4*>(m + kQuD)[u] = hi;
     }
   }
-  // lane l holds dimensions 4l .. 4l + 3 of the G heads' q (zero for heads >= G)
-  const int warp = tid >> 5, lane = tid & 31;
-  float qv[kQuMaxG][4], qa[kQuMaxG][4];
+  // Bounds on the tensor cores: with x <= y, max(q x, q y) = q+ y + q- x (q+ = max(q, 0),
+  // q- = min(q, 0)), so bound[p][h] = sum over the 256 entries of page p's [min | max]
+  // row times head h's [q- | q+]: an M = 16 pages x N = 8 heads x K = 256 product per
+  // tile, every operand an exact bf16 value.  K is permuted so that each lane reads
+  // 16-byte runs: for 16-byte unit u (physical entries 32u + 8c .. + 7, c = lane % 4)
+  // k-step 2u + v takes entries 32u + 8c + 4v + {0, 1} as logical k {2c, 2c + 1} and
+  // + {2, 3} as {2c + 8, 2c + 9}, on A and B alike.
+  const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, cq = lane & 3;
+  uint32_t bfr[16][2];
+  {
+    uint4 qraw[4] = {};
+    if (gq < G) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(P.q + (size_t(b) * P.Hq + size_t(kvh) * G + gq) * kQuD);
 #pragma unroll
-  for (int g = 0; g < kQuMaxG; ++g) {
-    uint2 w = make_uint2(0u, 0u);
-    if (g < G) w = *reinterpret_cast<const uint2*>(P.q + (size_t(b) * P.Hq + size_t(kvh) * G + g) * kQuD + 4 * lane);
-    const uint4 x = make_uint4(w.x, w.y, 0u, 0u);
+      for (int u = 0; u < 4; ++u) qraw[u] = qrow[4 * u + cq];  // dims 32u + 8c .. + 7
+    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      qv[g][i] = bf16_at(x, i);
-      qa[g][i] = fabsf(qv[g][i]);
+    for (int u = 0; u < 8; ++u) {
+      const uint4 x = qraw[u & 3];
+      const bool plus = u >= 4;  // entries 128.. multiply the max row
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t v = (&x.x)[i];
+        uint32_t r = 0u;
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          const uint32_t e = (v >> (16 * hlf)) & 0xFFFFu;
+          const bool neg = (e & 0x8000u) != 0u;
+          r |= ((plus ? !neg : neg) ? e : 0u) << (16 * hlf);
+        }
+        w[i] = r;
+      }
+      bfr[2 * u][0] = w[0];
+      bfr[2 * u][1] = w[1];
+      bfr[2 * u + 1][0] = w[2];
+      bfr[2 * u + 1][1] = w[3];
     }
   }
   __syncthreads();  // orders the append's min / max before the reads below
   const int pe = min(p1, n_full);
   float* bnd = P.bounds + (size_t(b) * P.Hq + size_t(kvh) * G) * P.max_pages;
-  const int hsel = (lane >> 2) & 7;  // the head whose sum this lane ends with
   constexpr int kWarps = kQuBoundThreads / 32;
-  constexpr int kAhead = 4;          // pages per warp in flight
 #pragma unroll 1
-  for (int pb = p0 + warp * kAhead; pb < pe; pb += kWarps * kAhead) {
-    uint2 lo[kAhead], hi[kAhead];
+  for (int tp = p0 + warp * 16; tp < pe; tp += kWarps * 16) {
+    const int pg0 = tp + gq, pg1 = tp + gq + 8;
+    const uint4* r0 = pg0 < pe ? reinterpret_cast<const uint4*>(P.meta + (size_t(qu_phys(P, b, pg0)) * P.Hkv + kvh) * 2 * kQuD) : nullptr;
+    const uint4* r1 = pg1 < pe ? reinterpret_cast<const uint4*>(P.meta + (size_t(qu_phys(P, b, pg1)) * P.Hkv + kvh) * 2 * kQuD) : nullptr;
+    uint4 x0[8], x1[8];
 #pragma unroll
-    for (int j = 0; j < kAhead; ++j) {
-      lo[j] = hi[j] = make_uint2(0u, 0u);
-      if (pb + j < pe) {
-        const uint2* m = reinterpret_cast<const uint2*>(
-            P.meta + (size_t(qu_phys(P, b, pb + j)) * P.Hkv + kvh) * 2 * kQuD);
-        lo[j] = __ldcg(m + lane);
-        hi[j] = __ldcg(m + kQuD / 4 + lane);
-      }
+    for (int u = 0; u < 8; ++u) {
+      x0[u] = r0 ? __ldcg(r0 + 4 * u + cq) : make_uint4(0u, 0u, 0u, 0u);
+      x1[u] = r1 ? __ldcg(r1 + 4 * u + cq) : make_uint4(0u, 0u, 0u, 0u);
     }
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < kAhead; ++j) {
-      const uint4 a = make_uint4(lo[j].x, lo[j].y, 0u, 0u), z = make_uint4(hi[j].x, hi[j].y, 0u, 0u);
-      float mid[4], rad[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float l = bf16_at(a, i), h = bf16_at(z, i);
-        mid[i] = 0.5f * (l + h);
-        rad[i] = 0.5f * (h - l);
-      }
-      float u[kQuMaxG];
-#pragma unroll
-      for (int g = 0; g < kQuMaxG; ++g) {
-        float t = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) t = fmaf(qv[g][i], mid[i], fmaf(qa[g][i], rad[i], t));
-        u[g] = t;
-      }
-      // transposing reduction over the 32 lanes: 8 sums with 4 + 2 + 1 + 2 shuffles;
-      // lane l ends with head (l >> 2) & 7
-      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-      float v[4];
-#pragma unroll
-      for (int j2 = 0; j2 < 4; ++j2) {
-        const float send = b4 ? u[j2] : u[j2 + 4], keep = b4 ? u[j2 + 4] : u[j2];
-        v[j2] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-      }
-      float w2[2];
-#pragma unroll
-      for (int j2 = 0; j2 < 2; ++j2) {
-        const float send = b3 ? v[j2] : v[j2 + 2], keep = b3 ? v[j2 + 2] : v[j2];
-        w2[j2] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-      }
-      float x = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
-      x += __shfl_xor_sync(0xffffffffu, x, 1);
-      x += __shfl_xor_sync(0xffffffffu, x, 2);
-      if ((lane & 3) == 0 && hsel < G && pb + j < pe) bnd[size_t(hsel) * P.max_pages + pb + j] = x;
+    for (int u = 0; u < 8; ++u) {
+      mma_bf16_16816(c, x0[u].x, x1[u].x, x0[u].y, x1[u].y, bfr[2 * u][0], bfr[2 * u][1]);
+      mma_bf16_16816(c, x0[u].z, x1[u].z, x0[u].w, x1[u].w, bfr[2 * u + 1][0], bfr[2 * u + 1][1]);
+    }
+    // c: pages (gq, gq + 8) x heads (2 cq, 2 cq + 1)
+    const int h0 = 2 * cq, h1 = 2 * cq + 1;
+    if (pg0 < pe) {
+      if (h0 < G) bnd[size_t(h0) * P.max_pages + pg0] = c[0];
+      if (h1 < G) bnd[size_t(h1) * P.max_pages + pg0] = c[1];
+    }
+    if (pg1 < pe) {
+      if (h0 < G) bnd[size_t(h0) * P.max_pages + pg1] = c[2];
+      if (h1 < G) bnd[size_t(h1) * P.max_pages + pg1] = c[3];
     }
   }
 }
@@ -315,6 +312,7 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
   if (!s_last) return;
   // list the marked pages in ascending order (block scan per round of 1024)
   int32_t* ul = P.ulist + (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  int32_t* uph = P.uphys + (size_t(b) * P.Hkv + kvh) * P.max_pages;
   uint32_t* um = P.umask + (size_t(b) * P.Hkv + kvh) * P.max_pages;
   uint32_t total_all = 0;
   for (int r0 = 0; r0 < n_full; r0 += kRkThreads) {
@@ -324,6 +322,7 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
     const uint32_t off = rk_block_excl_scan(m != 0u ? 1u : 0u, sm.wtot[0], tot);
     if (m != 0u) {
       ul[total_all + off] = i;
+      uph[total_all + off] = qu_phys(P, b, i);
       um[total_all + off] = m;
       msk[i] = 0u;
     }
@@ -333,6 +332,7 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
     int n = int(total_all);
     if (S % kQuPage != 0) {  // the partial page, for every head
       ul[n] = n_full;
+      uph[n] = qu_phys(P, b, n_full);
       um[n] = (G >= 32) ? 0xFFFFFFFFu : ((1u << G) - 1u);
       ++n;
     }
@@ -355,8 +355,7 @@ __global__ void __launch_bounds__(kQuAttnWarps * 32) qu_attn_kernel(const QuPara
   const int t0 = int((long long)split * n / P.splits), t1 = int((long long)(split + 1) * n / P.splits);
   const int G = P.G, g = lane >> 2, qd = lane & 3;
   const bool head_ok = g < G;
-  const int32_t* ul = P.ulist + (size_t(b) * P.Hkv + kvh) * P.max_pages;
-  const uint32_t* um = P.umask + (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  const size_t lbase = (size_t(b) * P.Hkv + kvh) * P.max_pages;
   const uint32_t wbuf = smem_u32(smem + warp * kQuAttnStages * 8192);
 
   uint32_t qa[8][2];
@@ -364,15 +363,44 @@ __global__ void __launch_bounds__(kQuAttnWarps * 32) qu_attn_kernel(const QuPara
   TileState st;
   st.init();
 
-  // page t of the list into stage s: its 16 K rows then 16 V rows (rows past a
+  // this warp's list entries are t0 + warp + 4 i; lane j holds entry cbase + j of
+  // the current chunk of 32 (page, physical page, head mask), read ahead in one go
+  const int nw = t0 + warp < t1 ? (t1 - t0 - warp + kQuAttnWarps - 1) / kQuAttnWarps : 0;
+  int cbase = 0, c_page = 0, c_phys = 0;
+  uint32_t c_mask = 0u;
+  auto load_chunk = [&](int base) {
+    const int e = t0 + warp + kQuAttnWarps * (base + lane);
+    const bool ok = base + lane < nw;
+    c_page = ok ? P.ulist[lbase + e] : 0;
+    c_phys = ok ? P.uphys[lbase + e] : 0;
+    c_mask = ok ? P.umask[lbase + e] : 0u;
+  };
+  auto entry = [&](int i, int& page, int& phys, uint32_t& m) {  // called by the whole warp
+    if (i - cbase < 32) {
+      page = __shfl_sync(0xffffffffu, c_page, i - cbase);
+      phys = __shfl_sync(0xffffffffu, c_phys, i - cbase);
+      m = __shfl_sync(0xffffffffu, c_mask, i - cbase);
+    } else {  // read-ahead past the chunk: straight from the list
+      const size_t e = lbase + t0 + warp + size_t(kQuAttnWarps) * i;
+      page = P.ulist[e];
+      phys = P.uphys[e];
+      m = P.umask[e];
+    }
+  };
+  load_chunk(0);
+
+  // entry i into stage s: its page's 16 K rows then 16 V rows (rows past a
   // partial page's tokens are zero-filled)
-  auto gather = [&](int t, int s) {
-    const int page = ul[t];
+  auto gather = [&](int i, int s) {
+    int page, phys;
+    uint32_t m;
+    entry(i, page, phys, m);
+    if (unsigned(phys) >= unsigned(P.num_pages)) phys = 0;  // reported when the list was built
     const int valid = page == n_full ? tail : kQuPage;
-    const size_t base = ((size_t(qu_phys(P, b, page)) * P.Hkv + kvh) * kQuPage) * kQuD;
+    const size_t base = ((size_t(phys) * P.Hkv + kvh) * kQuPage) * kQuD;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int c = lane + 32 * i;
+    for (int k = 0; k < 16; ++k) {
+      const int c = lane + 32 * k;
       const int row = c >> 4, u = c & 15;
       const int r16 = row & 15;
       const __nv_bfloat16* src = (row < 16 ? P.k_pool : P.v_pool) + base + size_t(r16) * kQuD + u * 8;
@@ -382,23 +410,28 @@ __global__ void __launch_bounds__(kQuAttnWarps * 32) qu_attn_kernel(const QuPara
   auto commit = []() { asm volatile("cp.async.commit_group;" ::: "memory"); };
 
   // every iteration commits one group (empty past the end), so the current
-  // page's group is always the third most recent
-  int t = t0 + warp;
+  // entry's group is always the third most recent
 #pragma unroll
   for (int k = 0; k < kQuAttnStages - 1; ++k) {
-    if (t + k * kQuAttnWarps < t1) gather(t + k * kQuAttnWarps, k);
+    if (k < nw) gather(k, k);
     commit();
   }
   int s = 0;
 #pragma unroll 1
-  for (; t < t1; t += kQuAttnWarps) {
-    const int tn = t + (kQuAttnStages - 1) * kQuAttnWarps;
-    if (tn < t1) gather(tn, s == 0 ? kQuAttnStages - 1 : s - 1);
+  for (int i = 0; i < nw; ++i) {
+    if (i - cbase == 32) {  // the chunk is used up (the read-ahead went straight to the list)
+      cbase += 32;
+      load_chunk(cbase);
+    }
+    const int in = i + kQuAttnStages - 1;
+    if (in < nw) gather(in, s == 0 ? kQuAttnStages - 1 : s - 1);
     commit();
     asm volatile("cp.async.wait_group %0;" ::"n"(kQuAttnStages - 1) : "memory");
     __syncwarp();
-    const int page = ul[t];
-    const bool on = head_ok && ((um[t] >> g) & 1u);
+    int page, phys;
+    uint32_t m;
+    entry(i, page, phys, m);
+    const bool on = head_ok && ((m >> g) & 1u);
     float x0, x1, x2, x3;
     attend_tile(wbuf + s * 8192, wbuf + s * 8192 + 4096, qa, page == n_full ? tail : kQuPage, P.scale_log2, st,
                 x0, x1, x2, x3, on);
@@ -441,7 +474,7 @@ using namespace kvsel_host;
 
 namespace {
 struct QuWs {
-  size_t cnt, bounds, sel, mask, ulist, umask, ucount, part, total;
+  size_t cnt, bounds, sel, mask, ulist, uphys, umask, ucount, part, total;
 };
 QuWs qu_ws_layout(int batch, int Hq, int Hkv, int max_pages, int budget, bool own_bounds, bool own_sel) {
   QuWs w;
@@ -456,6 +489,7 @@ QuWs qu_ws_layout(int batch, int Hq, int Hkv, int max_pages, int budget, bool ow
   w.sel = own_sel ? take(size_t(batch) * Hq * budget * 4) : 0;
   w.mask = take(size_t(batch) * Hkv * max_pages * 4);
   w.ulist = take(size_t(batch) * Hkv * max_pages * 4);
+  w.uphys = take(size_t(batch) * Hkv * max_pages * 4);
   w.umask = take(size_t(batch) * Hkv * max_pages * 4);
   w.ucount = take(size_t(batch) * Hkv * 4);
   w.part = take(size_t(batch) * Hkv * kTileMaxSplits * kPartFloats * 4);
@@ -557,6 +591,7 @@ extern "C" kvsel_status kvsel_quest_decode(const kvsel_paged_kv* kv, const int32
   P.sel = pages_out ? pages_out : reinterpret_cast<int32_t*>(ws + L.sel);
   P.mask = reinterpret_cast<uint32_t*>(ws + L.mask);
   P.ulist = reinterpret_cast<int32_t*>(ws + L.ulist);
+  P.uphys = reinterpret_cast<int32_t*>(ws + L.uphys);
   P.umask = reinterpret_cast<uint32_t*>(ws + L.umask);
   P.ucount = reinterpret_cast<int32_t*>(ws + L.ucount);
   P.topk_cnt = reinterpret_cast<unsigned*>(ws + L.cnt);

@@ -178,6 +178,15 @@ def test_heads_choose_their_own_pages():
         assert p in pages[0, h].tolist()
 
 
+def test_long_page_lists_per_warp():
+    # one kv head with a 10000-page budget over 12.5K pages: each attention warp
+    # walks more than one 32-entry chunk of the page list
+    wl = workloads.sparse_decode(seed=45, B=1, S0=200003, steps=1, Hq=1, Hkv=1)
+    st = QuestState(wl, budget=10000)
+    st.step(0)
+    _check(st, 0, 1)
+
+
 @pytest.mark.slow
 def test_full_size_70b_128k_sampled():
     """Batch 4 x 128K, 64 q / 8 kv heads, 128 pages (2048 tokens) per head: sampled heads."""
