@@ -50,6 +50,11 @@ class BpOptions(ctypes.Structure):
                 ("step", ctypes.c_int64), ("history_tokens", ctypes.c_int64), ("threshold", ctypes.c_float)]
 
 
+class BlockSignal(ctypes.Structure):
+    _fields_ = [("topk_blocks", ctypes.c_int), ("step", ctypes.c_int32), ("block_score", ctypes.c_void_p),
+                ("block_step", ctypes.c_void_p), ("topk_out", ctypes.c_void_p), ("mass_out", ctypes.c_void_p)]
+
+
 class SnapOptions(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("keep_count", ctypes.c_void_p), ("seed_out", ctypes.c_void_p),
                 ("seed_layer_stride", ctypes.c_int64), ("seed_head_stride", ctypes.c_int64)]
@@ -85,6 +90,9 @@ _SIGS = {
     "kvsel_snapkv_select_workspace": (_sz, [_PKV, _i, _i, _i, _i]),
     "kvsel_snapkv_select": (_i, [_PKV, _vp, _i, _i, _i, _vp, _i, _f, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "kvsel_snapkv_select_ex_workspace": (_sz, [_PKV, _i, _i, _i, _i, _i]),
+    "kvsel_decode_attn_ex_workspace": (_sz, [_PKV, _i, _i, _i, _i]),
+    "kvsel_decode_attn_ex": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _f, _vp, _i, _vp, _vp, _i, _i,
+                                  ctypes.POINTER(BlockSignal), _vp, _sz, _vp, _sz, _vp]),
     "kvsel_quest_page_meta": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp]),
     "kvsel_quest_decode_workspace": (_sz, [_PKV, _i, _i, _i, _i, _i]),
     "kvsel_quest_decode": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _f, _vp, _i, _vp, _vp, _vp, _sz,
@@ -199,13 +207,26 @@ def kvsel_decode_attn_workspace(kv: PagedKV, batch: int, max_len: int, with_prob
     return int(lib().kvsel_decode_attn_workspace(ctypes.byref(kv), batch, max_len, int(with_probs)))
 
 
+def kvsel_decode_attn_ex_workspace(kv: PagedKV, batch: int, max_len: int, with_probs: bool,
+                                   with_signal: bool) -> int:
+    return int(lib().kvsel_decode_attn_ex_workspace(ctypes.byref(kv), batch, max_len, int(with_probs),
+                                                    int(with_signal)))
+
+
 def kvsel_decode_attn(kv: PagedKV, block_table, seq_lens, q, out, workspace, *, k_new=None,
                       v_new=None, pos_map=None, next_pos=None, scale=None, probs=None,
-                      h2o_cum=None, max_len=None, num_ctas=0, h2o_link=None, stream=None):
+                      h2o_cum=None, max_len=None, num_ctas=0, h2o_link=None, block_score=None,
+                      block_step=None, signal_topk=512, signal_step=0, signal_topk_out=None,
+                      signal_mass_out=None, stream=None):
     """Append (optional) + decode attention + probabilities + H2O score update.
 
     h2o_link: the workspace of the kvsel_h2o_evict calls that follow (same
     batch); the step then hands them its heavy-hitter candidates.
+    block_score / block_step (per physical block, fp32 / int32): given, the
+    same launch also emits the step's top-k block signal (signal_topk blocks
+    per sequence; optional outputs signal_topk_out [batch][signal_topk] and
+    signal_mass_out [batch][ceil(max_len / 16)]); the workspace must then be
+    sized by kvsel_decode_attn_ex_workspace(..., with_signal=True).
     """
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
@@ -230,11 +251,20 @@ def kvsel_decode_attn(kv: PagedKV, block_table, seq_lens, q, out, workspace, *, 
     if scale is None:
         scale = kv.head_dim ** -0.5
     odt = KVSEL_F32 if out.dtype == torch.float32 else KVSEL_BF16
-    _check(lib().kvsel_decode_attn(
+    sig = None
+    if block_score is not None or block_step is not None:
+        _need(block_score, torch.float32, "block_score")
+        _need(block_step, torch.int32, "block_step")
+        _need(signal_topk_out, torch.int32, "signal_topk_out", True)
+        _need(signal_mass_out, torch.float32, "signal_mass_out", True)
+        sig = BlockSignal(int(signal_topk), int(signal_step), block_score.data_ptr(), block_step.data_ptr(),
+                          signal_topk_out.data_ptr() if signal_topk_out is not None else None,
+                          signal_mass_out.data_ptr() if signal_mass_out is not None else None)
+    _check(lib().kvsel_decode_attn_ex(
         ctypes.byref(kv), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), batch, _ptr(q),
         _ptr(k_new), _ptr(v_new), _ptr(pos_map), _ptr(next_pos), float(scale), _ptr(out), odt,
-        _ptr(probs), _ptr(h2o_cum), int(max_len), int(num_ctas), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(h2o_link),
+        _ptr(probs), _ptr(h2o_cum), int(max_len), int(num_ctas), ctypes.byref(sig) if sig is not None else None,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(h2o_link),
         0 if h2o_link is None else h2o_link.numel() * h2o_link.element_size(), _stream(stream)))
 
 

@@ -84,7 +84,8 @@ struct SmemLayout {
   static constexpr size_t seqPref = seqS + size_t(kMaxBatch) * 4;                        // [kMaxBatch+1] i64
   static constexpr size_t stats = seqPref + size_t(kMaxBatch + 1) * 8;                   // [8][2] f32
   static constexpr size_t owners = stats + kMaxG * 2 * 4;                                // [kMaxOwners+1] i32
-  static constexpr size_t total = owners + (kMaxOwners + 1) * 4;
+  static constexpr size_t sig = owners + (kMaxOwners + 1) * 4;                           // i32: run the block signal
+  static constexpr size_t total = sig + 16;
 };
 constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 
@@ -111,6 +112,15 @@ struct StepParams {
   unsigned* pair_k;     // [B*Hkv] owners whose K pass is done: their (m, l) are written
   unsigned* pair_v;     // [B*Hkv] owners whose V pass is done: their O is written
   unsigned* pair_done;  // [B*Hkv] owners past both waits (the last resets all three)
+  // per-step top-k block signal (all null / 0 when off)
+  float* bmass;         // [B*Hkv][bpages]: each page's attention mass from one kv head's group
+  float* bsum;          // [B][bpages]: summed over the kv heads (the caller's mass_out, else workspace)
+  uint32_t* bkeys;      // [B][bpages]: their order keys
+  unsigned* seq_done;   // [B]: pairs finished (the last runs the sequence's top-k)
+  float* sig_score;     // [num_pages]
+  int32_t* sig_step;    // [num_pages]
+  int32_t* sig_topk;    // [B][sig_k] or null
+  int sig_k, sig_stepv, bpages;
   int* status;
   int B, max_pages, Hq, Hkv, G, num_pages, max_len, out_f32;
   int vec2;        // logit and score rows are 8-byte aligned: key pairs move as float2
@@ -277,6 +287,188 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// ---------------------------------------------------------------------------
+// Per-step top-k block signal of one sequence, run by the CTA that finishes
+// the sequence's last (sequence, kv head) pair, all kThreads threads:
+//   mass[p]  = the page's attention mass summed over the kv heads (fixed order)
+//   chosen   = the sig_k pages of largest mass, ties to the lower page (every
+//              page when there are no more), in ascending order: a radix select
+//              of the k-th key (four 8-bit digits, most significant first) and
+//              an ordered emission by block scans
+//   for each chosen page: score[phys] += mass, step[phys] = the step.
+// `sm` is shared scratch of sm_words >= 320 words (the ring, free by then);
+// the page keys live there too when they fit.
+__device__ __forceinline__ uint32_t sig_block_scan(uint32_t v, uint32_t* wt, uint32_t& total) {
+  constexpr int kW = kThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wt[warp] = x;
+  __syncthreads();
+  uint32_t before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) {
+    const uint32_t t = wt[w];
+    if (w < warp) before += t;
+    total += t;
+  }
+  __syncthreads();
+  return before + x - v;
+}
+
+__device__ __noinline__ void block_signal(const StepParams& P, int b, int S, uint32_t* sm, int sm_words) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = (S + kPage - 1) / kPage;
+  const int k = min(P.sig_k, n);
+  float* msum = P.bsum + size_t(b) * P.bpages;
+  uint32_t* hist = sm;        // [256]
+  uint32_t* wt = sm + 256;    // [32]
+  uint32_t* bc = sm + 288;    // [2]: digit, remaining
+  // the keys stay in shared memory when they fit (n <= ~16K pages), else in the workspace
+  uint32_t* keys = n <= sm_words - 320 ? sm + 320 : P.bkeys + size_t(b) * P.bpages;
+  {
+    const float* bmb = P.bmass + size_t(b) * P.Hkv * P.bpages;
+    constexpr int kU = 4;  // pages per thread in flight, every kv head's load issued before the sums
+    for (int p0 = tid; p0 < n; p0 += kU * kThreads) {
+      float m[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) m[u] = 0.f;
+#pragma unroll 4
+      for (int h = 0; h < P.Hkv; ++h) {
+        float x[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int p = p0 + u * kThreads;
+          x[u] = p < n ? __ldcg(bmb + size_t(h) * P.bpages + p) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) m[u] += x[u];
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int p = p0 + u * kThreads;
+        if (p < n) {
+          msum[p] = m[u];
+          keys[p] = order_key(m[u]);
+        }
+      }
+    }
+  }
+  __syncthreads();  // the block's own stores, read back below
+  uint32_t prefix = 0u, mask = 0u, remaining = uint32_t(k);
+  if (k < n) {
+#pragma unroll 1
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kThreads) hist[i] = 0u;
+      __syncthreads();
+      for (int p = tid; p < n; p += kThreads) {
+        const uint32_t key = keys[p];
+        if ((key & mask) == prefix) atomicAdd(hist + ((key >> shift) & 255u), 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l owns digits 255 - 8l - j, j = 0..7: counts from the top down
+        uint32_t c[8], tot = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = hist[255 - 8 * lane - j];
+          tot += c[j];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t above = incl - tot;  // keys with a higher digit than this lane's
+        if (above < remaining && remaining <= above + tot) {
+          uint32_t cum = above;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (cum < remaining && remaining <= cum + c[j]) {
+              bc[0] = uint32_t(255 - 8 * lane - j);
+              bc[1] = remaining - cum;
+            }
+            cum += c[j];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= bc[0] << shift;
+      mask |= 0xFFu << shift;
+      remaining = bc[1];
+      __syncthreads();
+    }
+  }
+  // ordered emission: every key above T, then the first `remaining` equal to T
+  const uint32_t T = prefix;
+  const int32_t* bt = P.block_table + size_t(b) * P.max_pages;
+  int32_t* tko = P.sig_topk ? P.sig_topk + size_t(b) * P.sig_k : nullptr;
+  uint32_t out_base = 0u, eq_base = 0u;
+#pragma unroll 1
+  for (int c0 = 0; c0 < n; c0 += kThreads * 8) {
+    uint32_t kk[8];
+    uint32_t neq = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int p = c0 + 8 * tid + j;
+      kk[j] = p < n ? keys[p] : 0u;
+      if (p < n && k < n && kk[j] == T) ++neq;
+    }
+    uint32_t eq_tot;
+    uint32_t eq_rank = eq_base + sig_block_scan(neq, wt, eq_tot);
+    bool take[8];
+    uint32_t ntake = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int p = c0 + 8 * tid + j;
+      bool t = false;
+      if (p < n) {
+        if (k == n || kk[j] > T) t = true;
+        else if (kk[j] == T) t = eq_rank++ < remaining;
+      }
+      take[j] = t;
+      ntake += t ? 1u : 0u;
+    }
+    uint32_t out_tot;
+    uint32_t o = out_base + sig_block_scan(ntake, wt, out_tot);
+    // the taken pages' block-table entries, masses and old scores, all loads issued together
+    int phys[8];
+    float ms[8], old[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int p = c0 + 8 * tid + j;
+      phys[j] = take[j] ? __ldcg(bt + p) : -1;
+      ms[j] = take[j] ? __ldcg(msum + p) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (take[j] && unsigned(phys[j]) >= unsigned(P.num_pages)) {
+        report(P.status, KVSEL_ERR_BAD_INDEX);
+        take[j] = false;
+      }
+      old[j] = take[j] ? __ldcg(P.sig_score + phys[j]) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (!take[j]) continue;
+      if (tko) tko[o] = c0 + 8 * tid + j;
+      P.sig_score[phys[j]] = old[j] + ms[j];
+      P.sig_step[phys[j]] = P.sig_stepv;
+      ++o;
+    }
+    out_base += out_tot;
+    eq_base += eq_tot;
+  }
+  if (tko)
+    for (int i = k + tid; i < P.sig_k; i += kThreads) tko[i] = -1;
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
 decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const StepParams P) {
@@ -291,6 +483,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   long long* sPref = reinterpret_cast<long long*>(smem + SmemLayout::seqPref);
   float* sStat = reinterpret_cast<float*>(smem + SmemLayout::stats);
   int* sOwn = reinterpret_cast<int*>(smem + SmemLayout::owners);  // [kMaxOwners] + count
+  int& sSig = *reinterpret_cast<int*>(smem + SmemLayout::sig);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = gridDim.x, c = blockIdx.x;
@@ -644,7 +837,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         const float p0 = ex2(lg.x - Mg) * Ig, p1 = ex2(lg.y - Mg) * Ig;
         const float p2 = ex2(lg.z - Mg) * Ig, p3 = ex2(lg.w - Mg) * Ig;
         if (prow) store_keys(prow, key0, valid, k0, k2, vec2, make_float4(p0, p1, p2, p3), drop_l2);
-        if (crow) {
+        if (crow || P.bmass) {
           // the group's probability per key, a transposing sum over the 8 head
           // rows: lanes of heads with bit 2 set keep keys k2, k2 + 1, the others
           // k0, k0 + 1; bit 1 then picks one of the two; bit 0 completes the sum
@@ -656,9 +849,17 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           x += __shfl_xor_sync(0xffffffffu, hi2 ? a : bb, 8);
           x += __shfl_xor_sync(0xffffffffu, x, 4);
           const bool on = cown && kc < valid;
-          const float nv = ((append && key0 + kc == S - 1) ? 0.f : cs) + x;  // the appended slot starts from zero
-          if (on) __stcg(crow + key0 + kc, nv);
-          if (hk) cands_stage(wc, on, key0 + kc, nv, hk, lane);
+          if (crow) {
+            const float nv = ((append && key0 + kc == S - 1) ? 0.f : cs) + x;  // the appended slot starts from zero
+            if (on) __stcg(crow + key0 + kc, nv);
+            if (hk) cands_stage(wc, on, key0 + kc, nv, hk, lane);
+          }
+          if (P.bmass) {  // the page's mass from this group: the 16 keys held by the even-head lanes
+            float mass = (csum_lane && kc < valid) ? x : 0.f;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) mass += __shfl_xor_sync(0xffffffffu, mass, off);
+            if (lane == 0) P.bmass[size_t(pair) * P.bpages + key0 / kPage] = mass;
+          }
         }
 
         // O += P V, P as bf16 high part (rows 0..7) + bf16 residual (rows 8..15)
@@ -713,13 +914,16 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (c == 0) {
-    for (int b = 0; b < P.B; ++b)  // sequences without keys: O = 0
-      if (sS[b] == 0)
+    for (int b = 0; b < P.B; ++b)  // sequences without keys: O = 0 (and no block signal)
+      if (sS[b] == 0) {
         for (int idx = tid; idx < P.Hq * kD; idx += kThreads) {
           const size_t oi = size_t(b) * P.Hq * kD + idx;
           if (P.out_f32) static_cast<float*>(P.out)[oi] = 0.f;
           else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(0.f);
         }
+        if (P.sig_topk)
+          for (int i = tid; i < P.sig_k; i += kThreads) P.sig_topk[size_t(b) * P.sig_k + i] = -1;
+      }
   }
 #pragma unroll 1
   for (long long u = u0; u < u1;) {
@@ -731,12 +935,21 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     if (tid == 0) {
       const long long pfirst = sPref[b] + (long long)kvh * np;
       const int no = list_owners(sOwn, pfirst, pfirst + np - 1, U, NC);
+      sSig = 0;
       // every owner's O is written; the last owner past the wait resets the pair's counters
       if (wait_word(P.pair_v + pair, unsigned(no), P.status) &&
           atomicAdd(P.pair_done + pair, 1u) + 1u == unsigned(no)) {
         P.pair_k[pair] = 0u;
         P.pair_v[pair] = 0u;
         P.pair_done[pair] = 0u;
+        if (P.bmass) {  // every owner's page masses are written too: count the pair for its sequence
+          __threadfence();
+          if (atomicAdd(P.seq_done + b, 1u) + 1u == unsigned(Hkv)) {
+            P.seq_done[b] = 0u;
+            __threadfence();
+            sSig = 1;
+          }
+        }
       }
     }
     __syncthreads();
@@ -755,6 +968,11 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(acc);
     }
     __syncthreads();
+    if (sSig) {  // this CTA finished the sequence's last pair: its top-k block signal
+      block_signal(P, b, sS[b], reinterpret_cast<uint32_t*>(smem + SmemLayout::ring),
+                   int((size_t(kStages) * kStageBytes) / 4));
+      __syncthreads();
+    }
     u = seg_end;
   }
   // The last CTA to finish publishes the new lengths: every CTA has read the
@@ -783,7 +1001,7 @@ using namespace kvsel_host;
 namespace {
 
 struct DecodeWs {
-  size_t pair_off, part_off, logit_off, total;
+  size_t pair_off, part_off, logit_off, sig_off, total;
 };
 
 // The finish counter lives in the workspace's status area (byte 64); the
@@ -797,8 +1015,17 @@ DecodeWs decode_ws_layout(int batch, int Hkv, int Hq, int max_len, bool with_pro
   off = align_up(off + (size_t(kMaxCtas) + size_t(batch) * Hkv) * kPartFloats * sizeof(float), 256);
   w.logit_off = off;
   if (!with_probs) off = align_up(off + size_t(batch) * Hq * max_len * sizeof(float), 256);
+  w.sig_off = off;  // block-signal scratch follows (decode_sig_bytes)
   w.total = off;
   return w;
+}
+
+// Block-signal scratch: sequence counters [B], per-group page masses
+// [B*Hkv][bpages], summed masses [B][bpages] and their keys [B][bpages].
+size_t decode_sig_bytes(int batch, int Hkv, int max_len) {
+  const size_t bp = size_t((max_len + kPage - 1) / kPage);
+  return align_up(size_t(batch) * 4, 256) + align_up(size_t(batch) * Hkv * bp * 4, 256) +
+         2 * align_up(size_t(batch) * bp * 4, 256);
 }
 
 int ctas_per_sm() {
@@ -825,6 +1052,13 @@ extern "C" size_t kvsel_decode_attn_workspace(const kvsel_paged_kv* kv, int batc
   return decode_ws_layout(batch, kv->num_kv_heads, kv->num_q_heads, max_len, with_probs != 0).total;
 }
 
+extern "C" size_t kvsel_decode_attn_ex_workspace(const kvsel_paged_kv* kv, int batch, int max_len, int with_probs,
+                                                 int with_signal) {
+  const size_t base = kvsel_decode_attn_workspace(kv, batch, max_len, with_probs);
+  if (!base || !with_signal) return base;
+  return base + decode_sig_bytes(batch, kv->num_kv_heads, max_len);
+}
+
 extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_t* block_table,
                                           int max_pages, int32_t* seq_lens, int batch, const void* q,
                                           const void* k_new, const void* v_new, int32_t* pos_map,
@@ -832,6 +1066,18 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
                                           float* probs, float* h2o_cum, int max_len, int num_ctas,
                                           void* workspace, size_t ws_bytes, void* h2o_link,
                                           size_t h2o_link_bytes, void* stream) {
+  return kvsel_decode_attn_ex(kv, block_table, max_pages, seq_lens, batch, q, k_new, v_new, pos_map, next_pos,
+                              scale, out, out_dtype, probs, h2o_cum, max_len, num_ctas, nullptr, workspace,
+                              ws_bytes, h2o_link, h2o_link_bytes, stream);
+}
+
+extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                             int max_pages, int32_t* seq_lens, int batch, const void* q,
+                                             const void* k_new, const void* v_new, int32_t* pos_map,
+                                             int32_t* next_pos, float scale, void* out, int out_dtype,
+                                             float* probs, float* h2o_cum, int max_len, int num_ctas,
+                                             const kvsel_block_signal* signal, void* workspace, size_t ws_bytes,
+                                             void* h2o_link, size_t h2o_link_bytes, void* stream) {
   const std::string fn = "kvsel_decode_attn: ";
   if (!kv || !kv->k_pool || !kv->v_pool)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "kv pools must be non-NULL");
@@ -861,8 +1107,13 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   if (probs && !aligned(probs, 4)) return fail(KVSEL_ERR_INVALID_ARG, fn + "probs must be 4-byte aligned");
   if (!workspace) return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace is required");
   const DecodeWs L = decode_ws_layout(batch, Hkv, Hq, max_len, probs != nullptr);
-  if (ws_bytes < L.total)
-    return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace too small: need " + std::to_string(L.total));
+  if (signal) {
+    if (signal->topk_blocks < 1 || !signal->block_score || !signal->block_step)
+      return fail(KVSEL_ERR_INVALID_ARG, fn + "block signal: topk_blocks >= 1, block_score and block_step required");
+  }
+  const size_t need = L.total + (signal ? decode_sig_bytes(batch, Hkv, max_len) : 0);
+  if (ws_bytes < need)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace too small: need " + std::to_string(need));
   if (!aligned(workspace, 256))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace must be 256-byte aligned");
   if (h2o_link && (!aligned(h2o_link, 256) || h2o_link_bytes < link_bytes(batch * Hkv)))
@@ -922,6 +1173,29 @@ extern "C" kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_
   P.max_len = max_len;
   P.out_f32 = out_dtype == KVSEL_F32;
   P.vec2 = (max_len % 2 == 0) && aligned(P.logits, 8) && (!h2o_cum || aligned(h2o_cum, 8));
+  P.bpages = (max_len + kPage - 1) / kPage;
+  P.bmass = P.bsum = nullptr;
+  P.bkeys = nullptr;
+  P.seq_done = nullptr;
+  P.sig_score = nullptr;
+  P.sig_step = P.sig_topk = nullptr;
+  P.sig_k = P.sig_stepv = 0;
+  if (signal) {
+    const size_t bp = size_t(P.bpages);
+    size_t off = L.sig_off;
+    P.seq_done = reinterpret_cast<unsigned*>(ws + off);
+    off += align_up(size_t(batch) * 4, 256);
+    P.bmass = reinterpret_cast<float*>(ws + off);
+    off += align_up(size_t(batch) * Hkv * bp * 4, 256);
+    P.bsum = signal->mass_out ? signal->mass_out : reinterpret_cast<float*>(ws + off);
+    off += align_up(size_t(batch) * bp * 4, 256);
+    P.bkeys = reinterpret_cast<uint32_t*>(ws + off);
+    P.sig_score = signal->block_score;
+    P.sig_step = signal->block_step;
+    P.sig_topk = signal->topk_out;
+    P.sig_k = signal->topk_blocks;
+    P.sig_stepv = signal->step;
+  }
   P.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -363,6 +363,35 @@ def cuda_arm(args, rank, world):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     clocks.stop()
+
+    # ---- the same step with the per-step top-512 block signal emitted by the decode launch ----
+    ws_sig = K.workspace(K.kvsel_decode_attn_ex_workspace(kv, B, max_len, probs is not None, True))
+    bscore = torch.zeros(wl.num_pages, device=dev)
+    bstep = torch.full((wl.num_pages,), -1, dtype=torch.int32, device=dev)
+    btop = torch.zeros(B, 512, dtype=torch.int32, device=dev)
+
+    def sig_step(i):
+        t = i % T
+        if t == 0 and i > 0:
+            seq.copy_(seq0)
+        K.kvsel_decode_attn(kv, bt, seq, q_all[t], out, ws_sig, k_new=kn_all[t], v_new=vn_all[t], probs=probs,
+                            h2o_cum=cum, max_len=max_len, h2o_link=ws_ev, block_score=bscore, block_step=bstep,
+                            signal_topk=512, signal_step=i, signal_topk_out=btop)
+        K.kvsel_h2o_evict(kv, bt, seq, cum, ws_ev, budget=wl.budget, n_sink=wl.n_sink,
+                          window=wl.window, compact=False, keep_out=keep)
+    seq.copy_(seq0)
+    for i in range(3):
+        sig_step(i)
+    torch.cuda.synchronize()
+    v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    v0.record(stream)
+    for i in range(3, 3 + 64):
+        sig_step(i)
+    v1.record(stream)
+    torch.cuda.synchronize()
+    sig_ms = v0.elapsed_time(v1) / 64
+    if K.read_status(ws_sig):
+        raise RuntimeError(f"device status after the block-signal steps: {K.read_status(ws_sig)}")
     st0, st1 = K.read_status(ws), K.read_status(ws_ev)
     if st0 or st1:
         raise RuntimeError(f"device status after the timed region: {st0} {st1}")
@@ -397,6 +426,7 @@ def cuda_arm(args, rank, world):
         "e2e": {"value": world * e2e_steps / (e2e_ms / 1e3), "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
+        "variants_ms_per_step": {"with_block_signal_top512": sig_ms},
         "note": line_note,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }

@@ -154,6 +154,56 @@ KVSEL_API kvsel_status kvsel_decode_attn(const kvsel_paged_kv* kv, const int32_t
                                float* probs, float* h2o_cum, int max_len, int num_ctas,
                                void* workspace, size_t ws_bytes, void* h2o_link,
                                size_t h2o_link_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Decode step that also emits the step's top-k block signal ("Sparse
+ * attention x KV-cache offloading: eight questions" §5.1: each block keeps an
+ * fp32 score accumulator and an int32 last-update step, and every decode
+ * step accumulates each request's top-k blocks, k = 512 in the page's
+ * estimate) from the same launch.
+ *
+ * Defines, on top of kvsel_decode_attn: for sequence b (S_b keys after the
+ * append) and block (page) j < ceil(S_b / 16),
+ *   mass[b][j] = the step's attention probability summed over every q head
+ *                and the block's keys
+ *   chosen[b]  = the topk_blocks blocks of largest mass, ties to the lower
+ *                block (every block when there are no more), ascending
+ *   for j in chosen[b], phys = block_table[b][j]:
+ *                block_score[phys] += mass[b][j];  block_step[phys] = step
+ * Other blocks' metadata is left untouched.  A sequence with no keys gets no
+ * signal (its topk_out row is -1).
+ *
+ * signal (host pointer; NULL: exactly kvsel_decode_attn):
+ *   topk_blocks   >= 1.
+ *   step          the value stamped into block_step.
+ *   block_score   fp32 [num_pages], block_step int32 [num_pages]: per
+ *                 physical block, read-modify-written (device pointers).
+ *   topk_out      int32 [batch][topk_blocks] or NULL: chosen[b], -1 padded.
+ *   mass_out      fp32 [batch][ceil(max_len / 16)] or NULL: mass[b][j].
+ * workspace       >= kvsel_decode_attn_ex_workspace(kv, batch, max_len,
+ *                 probs != NULL, signal != NULL) bytes, zeroed before first
+ *                 use.
+ * The signal runs in the kernel's last phase, on the CTA that completes a
+ * sequence's last (sequence, kv head) pair.
+ */
+typedef struct kvsel_block_signal {
+  int topk_blocks;
+  int32_t step;
+  float* block_score;
+  int32_t* block_step;
+  int32_t* topk_out;
+  float* mass_out;
+} kvsel_block_signal;
+KVSEL_API size_t kvsel_decode_attn_ex_workspace(const kvsel_paged_kv* kv, int batch, int max_len,
+                                                int with_probs, int with_signal);
+KVSEL_API kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int32_t* block_table,
+                                            int max_pages, int32_t* seq_lens, int batch, const void* q,
+                                            const void* k_new, const void* v_new, int32_t* pos_map,
+                                            int32_t* next_pos, float scale, void* out, int out_dtype,
+                                            float* probs, float* h2o_cum, int max_len, int num_ctas,
+                                            const kvsel_block_signal* signal, void* workspace,
+                                            size_t ws_bytes, void* h2o_link, size_t h2o_link_bytes,
+                                            void* stream);
 /* Bytes at the start of an H2O evict workspace that kvsel_decode_attn uses as
  * h2o_link (0 for invalid arguments). */
 KVSEL_API size_t kvsel_h2o_link_bytes(int batch, int num_kv_heads);
