@@ -469,6 +469,9 @@ __device__ __noinline__ void block_signal(const StepParams& P, int b, int S, uin
     for (int i = k + tid; i < P.sig_k; i += kThreads) tko[i] = -1;
 }
 
+// kSig: the per-step block signal is on (P.bmass and the rest set); the
+// default instantiation carries none of its code.
+template <bool kSig>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const StepParams P) {
@@ -837,7 +840,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         const float p0 = ex2(lg.x - Mg) * Ig, p1 = ex2(lg.y - Mg) * Ig;
         const float p2 = ex2(lg.z - Mg) * Ig, p3 = ex2(lg.w - Mg) * Ig;
         if (prow) store_keys(prow, key0, valid, k0, k2, vec2, make_float4(p0, p1, p2, p3), drop_l2);
-        if (crow || P.bmass) {
+        if (kSig || crow) {
           // the group's probability per key, a transposing sum over the 8 head
           // rows: lanes of heads with bit 2 set keep keys k2, k2 + 1, the others
           // k0, k0 + 1; bit 1 then picks one of the two; bit 0 completes the sum
@@ -854,7 +857,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             if (on) __stcg(crow + key0 + kc, nv);
             if (hk) cands_stage(wc, on, key0 + kc, nv, hk, lane);
           }
-          if (P.bmass) {  // the page's mass from this group: the 16 keys held by the even-head lanes
+          if (kSig) {  // the page's mass from this group: the 16 keys held by the even-head lanes
             float mass = (csum_lane && kc < valid) ? x : 0.f;
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) mass += __shfl_xor_sync(0xffffffffu, mass, off);
@@ -942,7 +945,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         P.pair_k[pair] = 0u;
         P.pair_v[pair] = 0u;
         P.pair_done[pair] = 0u;
-        if (P.bmass) {  // every owner's page masses are written too: count the pair for its sequence
+        if (kSig) {  // every owner's page masses are written too: count the pair for its sequence
           __threadfence();
           if (atomicAdd(P.seq_done + b, 1u) + 1u == unsigned(Hkv)) {
             P.seq_done[b] = 0u;
@@ -968,7 +971,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(acc);
     }
     __syncthreads();
-    if (sSig) {  // this CTA finished the sequence's last pair: its top-k block signal
+    if (kSig && sSig) {  // this CTA finished the sequence's last pair: its top-k block signal
       block_signal(P, b, sS[b], reinterpret_cast<uint32_t*>(smem + SmemLayout::ring),
                    int((size_t(kStages) * kStageBytes) / 4));
       __syncthreads();
@@ -1028,14 +1031,17 @@ size_t decode_sig_bytes(int batch, int Hkv, int max_len) {
          2 * align_up(size_t(batch) * bp * 4, 256);
 }
 
+// Co-resident CTAs per SM of the kernel instantiation (the launch sizes its
+// grid from it); sets the shared-memory attribute on first use.
+template <bool kSig>
 int ctas_per_sm() {
   static int cached = 0;
   if (cached) return cached;
-  if (cudaFuncSetAttribute(decode_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_step_kernel<kSig>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmemBytes)) != cudaSuccess)
     return 0;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_step_kernel, kThreads, kSmemBytes) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_step_kernel<kSig>, kThreads, kSmemBytes) !=
       cudaSuccess)
     return 0;
   cached = occ;
@@ -1120,7 +1126,7 @@ extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int
     return fail(KVSEL_ERR_INVALID_ARG, fn + "h2o_link must be a 256-byte aligned H2O evict workspace of at least " +
                                            std::to_string(link_bytes(batch * Hkv)) + " bytes");
 
-  const int occ = ctas_per_sm();
+  const int occ = signal ? ctas_per_sm<true>() : ctas_per_sm<false>();
   if (occ < 1) return fail(KVSEL_ERR_CUDA, fn + "cannot configure the decode kernel (occupancy 0)");
   const int resident = sm_count() * occ;
   const int nc = num_ctas == 0 ? std::min(resident, kMaxCtas) : num_ctas;
@@ -1215,7 +1221,8 @@ extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   trace_before("decode_step", st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_step_kernel, tmK, tmV, P);
+  const cudaError_t e = signal ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true>, tmK, tmV, P)
+                               : cudaLaunchKernelEx(&cfg, decode_step_kernel<false>, tmK, tmV, P);
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_decode_attn (launch)");
   return KVSEL_OK;
