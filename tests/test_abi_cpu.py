@@ -191,3 +191,47 @@ def test_snapkv_ex_host_validation(lib):
     assert K.kvsel_snapkv_select_ex_workspace(kv, 2, 4096, 32, False, 5) == 0
     assert (K.kvsel_snapkv_select_workspace(kv, 2, 4096, 32, True) ==
             K.kvsel_snapkv_select_ex_workspace(kv, 2, 4096, 32, True, K.KVSEL_SNAP_GROUP_SUM))
+
+
+def test_decode_block_signal_host_validation(lib):
+    kv = _kv()
+    need = K.kvsel_decode_attn_ex_workspace(kv, 1, 64, True, True)
+    assert need > K.kvsel_decode_attn_workspace(kv, 1, 64, True)
+    assert K.kvsel_decode_attn_ex_workspace(kv, 1, 64, True, False) == K.kvsel_decode_attn_workspace(kv, 1, 64,
+                                                                                                      True)
+
+    def st(sig, ws_bytes=1 << 30):
+        return lib.kvsel_decode_attn_ex(ctypes.byref(kv), 16, 4, 16, 1, 16, None, None, None, None, 0.1, 16, 0,
+                                        16, None, 64, 0, ctypes.byref(sig) if sig is not None else None, 256,
+                                        ws_bytes, None, 0, None)
+    assert st(K.BlockSignal(topk_blocks=0, step=1, block_score=16, block_step=16)) == K.KVSEL_ERR_INVALID_ARG
+    assert b"block signal" in lib.kvsel_last_error_string()
+    assert st(K.BlockSignal(topk_blocks=8, step=1, block_score=None, block_step=16)) == K.KVSEL_ERR_INVALID_ARG
+    # the signal's scratch comes on top of the plain decode's workspace
+    base = K.kvsel_decode_attn_workspace(kv, 1, 64, True)
+    assert st(K.BlockSignal(topk_blocks=8, step=1, block_score=16, block_step=16),
+              ws_bytes=base) == K.KVSEL_ERR_INVALID_ARG
+    assert b"workspace too small" in lib.kvsel_last_error_string()
+
+
+def test_quest_host_validation(lib):
+    kv = _kv(num_pages=64)
+
+    def st(kv_=kv, **over):
+        a = dict(bt=16, max_pages=64, seq=16, B=2, q=16, kn=None, vn=None, meta=16, budget=8, scale=0.1, out=16,
+                 odt=0, pages=None, bounds=None, ws=256, ws_bytes=1 << 30)
+        a.update(over)
+        return lib.kvsel_quest_decode(ctypes.byref(kv_), a["bt"], a["max_pages"], a["seq"], a["B"], a["q"], a["kn"],
+                                      a["vn"], a["meta"], a["budget"], a["scale"], a["out"], a["odt"], a["pages"],
+                                      a["bounds"], a["ws"], a["ws_bytes"], None)
+    assert st(kv_=_kv(num_q_heads=128, num_pages=64)) == K.KVSEL_ERR_UNSUPPORTED   # G = 16
+    assert st(kn=16) == K.KVSEL_ERR_INVALID_ARG                                   # k_new without v_new
+    assert st(budget=0) == K.KVSEL_ERR_INVALID_ARG
+    assert st(meta=None) == K.KVSEL_ERR_INVALID_ARG
+    assert st(meta=8) == K.KVSEL_ERR_INVALID_ARG                                  # misaligned
+    assert st(odt=5) == K.KVSEL_ERR_INVALID_ARG
+    need = K.kvsel_quest_decode_workspace(kv, 2, 64, 8)
+    assert st(ws_bytes=need - 1) == K.KVSEL_ERR_INVALID_ARG
+    # taking the bounds and pages out of the workspace shrinks it by their size
+    assert need - K.kvsel_quest_decode_workspace(kv, 2, 64, 8, True, True) >= 2 * 64 * 64 * 4 + 2 * 64 * 8 * 4
+    assert lib.kvsel_quest_page_meta(ctypes.byref(kv), 16, 64, 16, 2, None, 256, None) == K.KVSEL_ERR_INVALID_ARG
