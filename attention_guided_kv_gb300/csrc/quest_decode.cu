@@ -28,8 +28,10 @@
 //                    tile on the tensor cores (mma.sync: the pages' [min |
 //                    max] rows, 512 bytes each, against the heads' [q- | q+],
 //                    see below).
-//   qu_topk_kernel   (q head, sequence): row_topk of the head's bounds, the
-//                    kept pages marked in the kv head's page mask; the last of
+//   qu_topk_kernel   (q head, sequence): the top pages of the head's bounds
+//                    (a register-resident radix select for rows of up to 16K
+//                    pages, row_topk above), the kept pages marked in the kv
+//                    head's page mask; the last of
 //                    the G heads to finish lists the marked pages in ascending
 //                    order with their head masks (the partial page last, for
 //                    every head) and clears the mask.
@@ -273,6 +275,105 @@ __global__ void __launch_bounds__(kQuBoundThreads) qu_bound_kernel(const QuParam
 }
 
 // ---------------------------------------------------------------------------
+// Top-k of a row of up to kQuSmallRow fp32 bounds by one 1024-thread CTA
+// (k < n): thread t holds positions 16t .. 16t + 15 as order keys in
+// registers; a radix select finds the k-th key T (four 8-bit digits, most
+// significant first; the histogram adds are aggregated per warp with
+// match_any, since the bounds' leading bits are nearly all alike), then an
+// ordered emission keeps every key above T and the first `remaining` equal to
+// it (ties to the lower position), in ascending position order.
+constexpr int kQuSmallPer = 16;
+constexpr int kQuSmallRow = kRkThreads * kQuSmallPer;
+template <class Emit>
+__device__ __forceinline__ void qu_small_topk(const float* row, int n, int k, uint32_t* hist, uint32_t* tmp,
+                                              uint32_t* bc, Emit emit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t kk[kQuSmallPer];
+  const int p0 = tid * kQuSmallPer;
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && p0 + kQuSmallPer <= n) {
+#pragma unroll
+    for (int j = 0; j < kQuSmallPer; j += 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(row + p0 + j));
+      kk[j] = order_key(v.x);
+      kk[j + 1] = order_key(v.y);
+      kk[j + 2] = order_key(v.z);
+      kk[j + 3] = order_key(v.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kQuSmallPer; ++j) kk[j] = p0 + j < n ? order_key(__ldcg(row + p0 + j)) : 0u;
+  }
+  uint32_t prefix = 0u, mask = 0u, remaining = uint32_t(k);
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kRkThreads) hist[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kQuSmallPer; ++j) {
+      const bool live = p0 + j < n && (kk[j] & mask) == prefix;
+      const uint32_t d = live ? (kk[j] >> shift) & 255u : 256u;  // 256: not counted
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      if (live && (peers & rk_lanemask_lt()) == 0u) atomicAdd(hist + d, uint32_t(__popc(peers)));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255 - 8l - j, j = 0..7: counts from the top down
+      uint32_t c[8], tot = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - 8 * lane - j];
+        tot += c[j];
+      }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t above = incl - tot;
+      if (above < remaining && remaining <= above + tot) {
+        uint32_t cum = above;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cum < remaining && remaining <= cum + c[j]) {
+            bc[0] = uint32_t(255 - 8 * lane - j);
+            bc[1] = remaining - cum;
+          }
+          cum += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= bc[0] << shift;
+    mask |= 0xFFu << shift;
+    remaining = bc[1];
+    __syncthreads();
+  }
+  const uint32_t T = prefix;
+  uint32_t neq = 0u;
+#pragma unroll
+  for (int j = 0; j < kQuSmallPer; ++j) neq += (p0 + j < n && kk[j] == T) ? 1u : 0u;
+  uint32_t tot;
+  uint32_t eq_rank = rk_block_excl_scan(neq, tmp, tot);
+  uint32_t ntake = 0u;
+  uint32_t take = 0u;  // bit j: position p0 + j is kept
+#pragma unroll
+  for (int j = 0; j < kQuSmallPer; ++j) {
+    bool t = false;
+    if (p0 + j < n) {
+      if (kk[j] > T) t = true;
+      else if (kk[j] == T) t = eq_rank++ < remaining;
+    }
+    take |= (t ? 1u : 0u) << j;
+    ntake += t ? 1u : 0u;
+  }
+  uint32_t o = rk_block_excl_scan(ntake, tmp, tot);
+#pragma unroll
+  for (int j = 0; j < kQuSmallPer; ++j)
+    if ((take >> j) & 1u) emit(int(o++), p0 + j);
+}
+
+// ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
   extern __shared__ __align__(16) uint8_t tk_smem[];
   RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
@@ -290,6 +391,12 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
       sel[i] = i < n_full ? i : -1;
       if (i < n_full) atomicOr(msk + i, bit);
     }
+  } else if (n_full <= kQuSmallRow) {
+    const float* row = P.bounds + (size_t(b) * P.Hq + h) * P.max_pages;
+    qu_small_topk(row, n_full, k, sm.hist, sm.wtot[0], sm.wtot[1], [&](int i, int p) {
+      sel[i] = p;
+      atomicOr(msk + p, bit);
+    });
   } else {
     const float* row = P.bounds + (size_t(b) * P.Hq + h) * P.max_pages;
     const F32RowKeys src{row, 0, n_full, (reinterpret_cast<uintptr_t>(row) & 15u) == 0};

@@ -187,6 +187,30 @@ def test_long_page_lists_per_warp():
     _check(st, 0, 1)
 
 
+def test_equal_bounds_keep_the_lower_pages():
+    # every full page holds the same 16 keys: all bounds tie exactly
+    wl = workloads.sparse_decode(seed=46, B=2, S0=3000, steps=1, Hq=8, Hkv=2)
+    K4 = wl.K.copy()
+    for b in range(wl.B):
+        for kvh in range(wl.Hkv):
+            page = K4[b, kvh, :16].copy()
+            for p in range(wl.S0 // 16):
+                K4[b, kvh, 16 * p:16 * (p + 1)] = page
+    wl.K = K4                      # the appended token lands in the partial page 187
+    st = QuestState(wl, budget=40)
+    st.step(0)
+    _check(st, 0, 1)
+    assert (st.pages.cpu().numpy() == np.arange(40)).all()
+
+
+def test_rows_longer_than_the_register_select():
+    # 18750 full pages: the per-head selection falls back to the row_topk path
+    wl = workloads.sparse_decode(seed=47, B=1, S0=300003, steps=1, Hq=2, Hkv=1)
+    st = QuestState(wl, budget=100)
+    st.step(0)
+    _check(st, 0, 1)
+
+
 @pytest.mark.slow
 def test_full_size_70b_128k_sampled():
     """Batch 4 x 128K, 64 q / 8 kv heads, 128 pages (2048 tokens) per head: sampled heads."""
