@@ -44,7 +44,7 @@ constexpr int kSnPage = 16;
 constexpr int kSnMaxRows = 256;          // G * W <= 256
 constexpr int kSnMaxChunks = 64;
 constexpr int kSnSelGroups = 8;           // register-resident rows: prefix <= 32768
-constexpr int kSnMaxHalf = 16;            // pool kernel <= 33
+constexpr int kSnMaxHalf = 16;            // max-pool window (pool_kernel) <= 33
 
 struct SnapParams {
   const int32_t* block_table;  // [L][max_pages]
