@@ -235,3 +235,22 @@ def test_quest_host_validation(lib):
     # taking the bounds and pages out of the workspace shrinks it by their size
     assert need - K.kvsel_quest_decode_workspace(kv, 2, 64, 8, True, True) >= 2 * 64 * 64 * 4 + 2 * 64 * 8 * 4
     assert lib.kvsel_quest_page_meta(ctypes.byref(kv), 16, 64, 16, 2, None, 256, None) == K.KVSEL_ERR_INVALID_ARG
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    # the boundary is a C ABI: the header must stand alone in C99 (every struct and enum named)
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    src.write_text('#include "kvsel.h"\n'
+                   'int main(void) {\n'
+                   '  kvsel_block_signal s; kvsel_snap_options o; kvsel_bp_options b; kvsel_paged_kv kv;\n'
+                   '  (void)s; (void)o; (void)b; (void)kv;\n'
+                   '  return (int)KVSEL_SNAP_HEAD_UNION + (int)KVSEL_UPDATE_WINDOW;\n'
+                   '}\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        "-c", str(src), "-o", str(tmp_path / "use.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
