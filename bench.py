@@ -49,6 +49,28 @@ DECODE_STEP_TRAFFIC = 1.142102e9
 TRACE_EVERY = 8   # launch tracing on one timed step in eight: events between kernels cost time
 
 
+def slowest_rank(value: float, world: int, device=None) -> float:
+    """The largest of the ranks' figures (a replica job takes its slowest rank's
+    time); the value itself when running alone."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Units all ranks processed per second over the (slowest rank's) time."""
+    return world * units_per_rank / (ms / 1e3)
+
+
+def replica_seed(base: int, rank: int) -> int:
+    """Each replica draws its own synthetic inputs."""
+    return base + rank
+
+
 def timed_steps(step_fn, first, steps, stream, per_step_launches):
     """Run `steps` steps between two events on `stream`; every TRACE_EVERY-th
     step is bracketed by the library's launch trace (events around each of its
@@ -254,7 +276,7 @@ def cuda_arm(args, rank, world):
     torch.cuda.set_device(dev)
     K.lib()
 
-    wl = workloads.decode_70b(seed=1 + rank, B=args.batch)
+    wl = workloads.decode_70b(seed=replica_seed(1, rank), B=args.batch)
     B, Hq, Hkv, d, S0, T = wl.B, wl.Hq, wl.Hkv, wl.d, wl.S0, wl.steps
     max_len = wl.max_len
 
@@ -313,10 +335,7 @@ def cuda_arm(args, rank, world):
     ms, durs, per_step_launches = timed_steps(dev_step, args.warmup, args.steps, stream, 3)
     barrier()
     t_wall1 = time.time()
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = slowest_rank(ms, world, dev)
     launches = per_step_launches * args.steps
 
     # live step lengths in the timed region (after the append)
@@ -357,11 +376,7 @@ def cuda_arm(args, rank, world):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = slowest_rank(e0.elapsed_time(e1), world, dev)
     clocks.stop()
 
     # ---- the same step with the per-step top-512 block signal emitted by the decode launch ----
@@ -403,7 +418,7 @@ def cuda_arm(args, rank, world):
         line_note = f"batch {args.batch}: profiling case, not the measured workload"
     else:
         line_note = None
-    steps_per_s = world * args.steps / (ms / 1e3)
+    steps_per_s = job_rate(world, args.steps, ms)
     kvb = sum(kv_bytes([S] * B, Hkv, d) for S in S_steps) / len(S_steps)
     eff_kv_gbs = kvb / (ms / args.steps / 1e3) / 1e9
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
@@ -423,7 +438,7 @@ def cuda_arm(args, rank, world):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": DECODE_STEP_TRAFFIC if B == 8 else None,
                      "algorithmic_bytes": dec_bytes},
-        "e2e": {"value": world * e2e_steps / (e2e_ms / 1e3), "unit": "steps/s",
+        "e2e": {"value": job_rate(world, e2e_steps, e2e_ms), "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "variants_ms_per_step": {"with_block_signal_top512": sig_ms},
@@ -830,10 +845,7 @@ def other_workload(args, rank, world):
         torch.cuda.synchronize()
         tw1 = time.time()
         ms = ga.elapsed_time(gb)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = slowest_rank(ms, world, dev)
     per = {}
     for nm, d in durs:
         per.setdefault(nm, []).append(d)
@@ -866,7 +878,7 @@ def other_workload(args, rank, world):
             ho.copy_(o, non_blocking=True)
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1)
+    e2e_ms = slowest_rank(f0.elapsed_time(f1), world, dev)
     variants = None
     if S.get("variant_runs"):
         variants = {}
@@ -954,12 +966,12 @@ def other_workload(args, rank, world):
         ach = S["bytes"].get(dominant, 0) / (kms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dominant, "achieved": ach, "peak": hbm, "peak_kind": peak_kind,
                 "unit": "GB/s", "frac": ach / hbm, "traffic": None}
-    line = {"metric": metric, "value": world * steps / (ms / 1e3), "unit": unit, "n_gpus": world,
+    line = {"metric": metric, "value": job_rate(world, steps, ms), "unit": unit, "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if args.workload != "block_priority" else "f32",
             "data": "synthetic", "config": dict({"workload": cfg_name}, **S["config"]),
             "kernel_ms": kern_ms, "roofline": roof,
-            "e2e": {"value": world * steps / (e2e_ms / 1e3), "unit": unit, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_rate(world, steps, e2e_ms), "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": per_step_launches * steps, "clocks": clocks.summary(tw0, tw1)}
     if eager_ms is not None:
@@ -1006,22 +1018,22 @@ def main():
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    if args.workload != "decode_70b":
-        if args.impl == "reference":
-            if rank == 0:
+    if args.impl == "reference":  # rank 0 alone; the other ranks exit without work
+        if rank == 0:
+            if args.workload != "decode_70b":
                 other_reference(args, world)
-            return
-        other_workload(args, rank, world)
-        return
-    if args.impl == "reference":
-        reference_arm(args, rank, world)
+            else:
+                reference_arm(args, rank, world)
         return
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    cuda_arm(args, rank, world)
+    if args.workload != "decode_70b":
+        other_workload(args, rank, world)
+    else:
+        cuda_arm(args, rank, world)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
