@@ -31,17 +31,17 @@
 //   qu_topk_kernel   (q head, sequence): the top pages of the head's bounds
 //                    (a register-resident radix select for rows of up to 16K
 //                    pages, row_topk above), the kept pages marked in the kv
-//                    head's page mask; the last of
-//                    the G heads to finish lists the marked pages in ascending
-//                    order with their head masks (the partial page last, for
-//                    every head) and clears the mask.
+//                    head's page mask; the last of the G heads to finish
+//                    lists the marked pages in ascending order with their
+//                    physical pages and head masks (the partial page last,
+//                    for every head) and clears the mask.
 //   qu_attn_kernel   (split, kv head, sequence), 4 warps: one 16-key tile per
 //                    listed page (cp.async gather of its K and V rows into the
 //                    swizzled tile, three stages per warp: two pages in
 //                    flight while one is computed), attend_tile with the
-//                    page's head mask;
-//                    the last split of a (sequence, kv head) merges the
-//                    splits into O and the last kv head publishes the length.
+//                    page's head mask; the last split of a (sequence, kv
+//                    head) merges the splits into O and the last kv head
+//                    publishes the length.
 #include "attn_tile.cuh"
 #include "row_topk.cuh"
 
@@ -52,7 +52,7 @@ constexpr int kQuPage = 16;
 constexpr int kQuMaxG = kTileMaxG;
 constexpr int kQuBoundThreads = 256;
 constexpr int kQuBoundPagesPerCta = 256;
-constexpr int kQuTopkGroups = 8;          // rows up to 32K pages stay in registers
+constexpr int kQuTopkGroups = 8;          // row_topk (rows above 16K pages): up to 32K in registers
 constexpr int kQuAttnWarps = 4;
 constexpr int kQuAttnStages = 3;          // per warp
 // the warps' merge scratch reuses the ring once every warp is done with it
