@@ -19,3 +19,20 @@ def kv_bytes(layers: int, kv_heads: int, head_dim: int, tokens: int, elem_bytes:
 def decode_read_seconds(layers, kv_heads, head_dim, tokens, hbm_bytes_per_s, elem_bytes=2):
     """Time to stream the whole KV once at a given HBM bandwidth."""
     return kv_bytes(layers, kv_heads, head_dim, tokens, elem_bytes) / hbm_bytes_per_s
+
+
+# "Sparse attention x KV-cache offloading: eight questions" §5.1 (metadata
+# cost): each KV block keeps an fp32 score accumulator and an int32
+# last-update step, and each decode step writes one fp32 score per top-k
+# block of every request.
+BLOCK_META_BYTES = 4 + 4
+
+
+def block_metadata_bytes(requests: int, blocks_per_request: int) -> int:
+    """Bytes of per-block signal metadata for a whole batch."""
+    return requests * blocks_per_request * BLOCK_META_BYTES
+
+
+def signal_update_bytes(requests: int, topk_blocks: int, score_bytes: int = 4) -> int:
+    """Score bytes one decode step writes for the batch's top-k blocks."""
+    return requests * topk_blocks * score_bytes

@@ -40,3 +40,14 @@ def test_signal_updates_only_the_chosen_physical_blocks():
     assert last.tolist() == [-1, -1, 4, -1, -1, -1, -1, -1, -1, 4]
     acc, last = bs.apply_signal(acc, last, bt, np.array([0, 1]), mass, step=5)
     assert acc[2] == 3.0 and acc[7] == 0.25 and last[9] == 4 and last[2] == 5
+
+
+def test_metadata_sizes_match_the_page(golden):
+    from oracle import costs
+    rows = {r[0]: r[1:] for r in golden("block_metadata_bytes.txt")}
+    req, per, val, unit = rows["metadata"]
+    got = costs.block_metadata_bytes(int(req), int(per))
+    assert got == 256 * 2000 * 8
+    assert abs(got / 1e6 - float(val)) / float(val) < 0.05        # "about 4 MB" (4.1 MB)
+    req, k, val, unit = rows["update"]
+    assert costs.signal_update_bytes(int(req), int(k)) == int(val) * 1024   # 512 KiB exactly
