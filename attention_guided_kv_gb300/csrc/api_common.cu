@@ -1,7 +1,10 @@
 // Host-side plumbing shared by every entry point: the per-thread error
-// string, the workspace status word and the tensor-map encoder.
+// string, the workspace status word, the tensor-map encoder and the launch
+// trace (CUDA events for the bench, NVTX ranges for a timeline profiler).
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -96,7 +99,18 @@ struct TraceState {
 };
 static thread_local TraceState g_trace;
 
+// NVTX ranges around every library launch (named after the kernel) for a
+// timeline profiler, when the environment sets KVSEL_NVTX=1; read once.
+static bool nvtx_on() {
+  static const bool on = [] {
+    const char* v = std::getenv("KVSEL_NVTX");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+
 void trace_before(const char* kernel, cudaStream_t st) {
+  if (nvtx_on()) nvtxRangePushA(kernel);
   TraceState& t = g_trace;
   if (!t.events || t.count >= t.capacity) return;
   t.names.push_back(kernel);
@@ -104,6 +118,7 @@ void trace_before(const char* kernel, cudaStream_t st) {
 }
 
 void trace_after(cudaStream_t st) {
+  if (nvtx_on()) nvtxRangePop();
   TraceState& t = g_trace;
   if (!t.events || t.count >= t.capacity) return;
   cudaEventRecord(static_cast<cudaEvent_t>(t.events[2 * t.count + 1]), st);
