@@ -105,7 +105,7 @@ def peaks():
 
 
 # ---------------------------------------------------------------------------
-# byte model (algorithmic bytes)
+# byte model: algorithmic bytes per launch
 # ---------------------------------------------------------------------------
 def kv_bytes(S_list, Hkv, d=128):
     return sum(S_list) * Hkv * d * 2 * 2

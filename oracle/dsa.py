@@ -66,12 +66,22 @@ def sparse_decode_step(q, K, V, q_idx, w, k_idx, top_k, scale):
 
 
 def quest_page_bound(q: np.ndarray, K: np.ndarray, page: int = 16) -> np.ndarray:
-    """Upper bound of q.k over each full page of K [S][d]: sum_d max(q*kmin, q*kmax)."""
+    """Upper bound of q.k over each full page of K [S][d].
+
+    The sparse-selection section bounds a query's logit against any key of a
+    page by taking, in every dimension, the larger of q_d times the page's
+    smallest and q_d times its largest value of that dimension:
+        bound[p] = sum_d max(q_d * min_t K[t, d], q_d * max_t K[t, d])
+    over the page's tokens t.  Only full pages (S // page of them) get one.
+    """
     S, d = K.shape
-    n = S // page
-    pages = K[:n * page].reshape(n, page, d)
-    kmin, kmax = pages.min(axis=1), pages.max(axis=1)
-    return np.maximum(q[None, :] * kmin, q[None, :] * kmax).sum(axis=1)
+    bounds = np.zeros(S // page)
+    for p in range(S // page):
+        tokens = K[p * page:(p + 1) * page]          # the page's keys, [page][d]
+        lo = tokens.min(axis=0)                      # per-dimension minimum
+        hi = tokens.max(axis=0)                      # per-dimension maximum
+        bounds[p] = np.sum(np.maximum(q * lo, q * hi))
+    return bounds
 
 
 def page_minmax(K: np.ndarray, page: int = 16):
