@@ -79,6 +79,8 @@ _SIGS = {
     "kvsel_h2o_link_bytes": (_sz, [_i, _i]),
     "kvsel_h2o_evict": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                              _sz, _vp]),
+    "kvsel_kv_compact_workspace": (_sz, [_i, _i]),
+    "kvsel_kv_compact": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "kvsel_block_priority_workspace": (_sz, [_i, ctypes.c_int64]),
     "kvsel_block_priority": (_i, [_vp, _vp, _f, _vp, _i, _i, _i, _f, _i, _f, _vp, ctypes.c_int64, _vp,
                                   ctypes.c_int64, _vp, _vp, _sz, _vp]),
@@ -323,6 +325,27 @@ def kvsel_h2o_evict(kv: PagedKV, block_table, seq_lens, h2o_cum, workspace, *, b
         _ptr(h2o_cum), _ptr(pos_map), h2o_cum.shape[-1], int(budget), int(n_sink), int(window),
         int(bool(compact)), _ptr(keep_out), _ptr(freed_pages), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def kvsel_kv_compact_workspace(batch: int, num_kv_heads: int) -> int:
+    return int(lib().kvsel_kv_compact_workspace(batch, num_kv_heads))
+
+
+def kvsel_kv_compact(kv: PagedKV, block_table, seq_lens, keep, workspace, *, keep_count=None, scores=None,
+                     pos_map=None, freed_pages=None, stream=None):
+    """Move each row's kept slots (keep [batch][Hkv][stride], ascending) to the front, in place."""
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(keep, torch.int32, "keep")
+    _need(keep_count, torch.int32, "keep_count", True)
+    _need(scores, torch.float32, "scores", True)
+    _need(pos_map, torch.int32, "pos_map", True)
+    _need(freed_pages, torch.int32, "freed_pages", True)
+    max_len = next((t.shape[-1] for t in (scores, pos_map) if t is not None), 0)
+    _check(lib().kvsel_kv_compact(
+        ctypes.byref(kv), _ptr(block_table), block_table.shape[-1], _ptr(seq_lens), seq_lens.shape[0],
+        _ptr(keep), keep.shape[-1], _ptr(keep_count), _ptr(scores), _ptr(pos_map), int(max_len),
+        _ptr(freed_pages), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:

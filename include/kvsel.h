@@ -275,6 +275,55 @@ KVSEL_API kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block_
                              size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Keep-list compaction of the paged cache: move each row's kept slots to the
+ * front, release the pages past them, shorten the sequence.
+ *
+ * Defines ("From sliding window to attention-guided eviction": the §4.2
+ * pseudocode evicts every slot outside the keep set; §4.3 step 6 continues
+ * generation with only the kept KV): for sequence b with live length
+ * S = seq_lens[b] and kv head g, with keep row r = keep[b][g][0..n):
+ *   K_g[i], V_g[i]  <- K_g[r[i]], V_g[r[i]]     for i < n, in place
+ *   scores[b][g][i] <- scores[b][g][r[i]]       (optional, e.g. the H2O score)
+ *   pos_map[b][g][i]<- pos_map[b][g][r[i]]      (optional)
+ *   block_table[b][p] = -1 for ceil(n/16) <= p < ceil(S/16), those page ids
+ *   listed in freed_pages[b] (-1 padded); seq_lens[b] = n.
+ * After kvsel_snapkv_select[_ex] (group-sum mode) this is the compaction of
+ * the prompt cache: pass the layer block table as [num_layers][max_pages],
+ * seq_lens = S per layer, keep = keep_out with keep_stride = its capacity and
+ * keep_count from the options (positions equal slots in a fresh prompt).  The
+ * seeds kvsel_snapkv_select_ex writes are already in kept order.
+ *
+ * Arguments (device pointers unless noted):
+ *   kv            both pools (read and written in place).
+ *   block_table   int32 [batch][max_pages]; seq_lens int32 [batch] (in/out).
+ *   keep          int32 [batch][num_kv_heads][keep_stride]: each row's kept
+ *                 SLOTS, strictly ascending, each < S.
+ *   keep_count    int32 [batch][num_kv_heads], or NULL: a row's count is then
+ *                 the number of entries before its first negative one.
+ *                 Every kv head of a sequence must keep the same count (one
+ *                 block table serves them all), so the per-head counts of
+ *                 SnapKV's union mode are rejected when they differ.
+ *   scores        fp32 [batch][num_kv_heads][max_len] or NULL.
+ *   pos_map       int32 [batch][num_kv_heads][max_len] or NULL.
+ *   max_len       row length of scores / pos_map (>= S when either is given).
+ *   freed_pages   int32 [batch][max_pages] or NULL.
+ *   workspace     >= kvsel_kv_compact_workspace(batch, num_kv_heads) bytes,
+ *                 status word zeroed.
+ * Device-detected problems (a count or slot out of range, a row not strictly
+ * ascending, counts that differ between kv heads, S beyond the table or
+ * max_len) record KVSEL_ERR_BAD_INDEX and leave that sequence untouched; a
+ * block-table entry outside the pool records it too and skips that row.
+ * Launches: check (one CTA per sequence), move (one per (sequence, kv head)),
+ * truncate (one per sequence).
+ */
+KVSEL_API size_t kvsel_kv_compact_workspace(int batch, int num_kv_heads);
+KVSEL_API kvsel_status kvsel_kv_compact(const kvsel_paged_kv* kv, int32_t* block_table, int max_pages,
+                                        int32_t* seq_lens, int batch, const int32_t* keep, int keep_stride,
+                                        const int32_t* keep_count, float* scores, int32_t* pos_map,
+                                        int max_len, int32_t* freed_pages, void* workspace, size_t ws_bytes,
+                                        void* stream);
+
+/* ---------------------------------------------------------------------------
  * Block offload priority: decay aging, token -> block fold, per-request
  * percentile, global eviction order.
  *

@@ -99,3 +99,46 @@ class DecodeState:
 
     def status(self):
         return K.read_status(self.ws), K.read_status(self.ws_ev)
+
+
+GUARD_BYTES = 256
+GUARD_BYTE = 0xA5
+
+
+class Guards:
+    """Output buffers with guard regions before and after each one.
+
+    Every buffer is carved from a larger allocation whose first and last
+    GUARD_BYTES bytes hold a fixed pattern; ``check()`` asserts that no call
+    wrote outside the buffer it was given (the tail and padding paths of the
+    kernels, without a sanitizer).
+    """
+
+    def __init__(self, dev="cuda"):
+        self.dev = dev
+        self._bufs = []
+
+    def new(self, shape, dtype, fill=0):
+        shape = tuple(int(s) for s in shape)
+        n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+        body = (n + GUARD_BYTES - 1) // GUARD_BYTES * GUARD_BYTES
+        raw = torch.full((2 * GUARD_BYTES + body,), GUARD_BYTE, dtype=torch.uint8, device=self.dev)
+        t = raw[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+        t.fill_(fill)
+        self._bufs.append((raw, n))
+        return t
+
+    def like(self, src, fill=None):
+        t = self.new(src.shape, src.dtype)
+        if fill is None:
+            t.copy_(src)
+        else:
+            t.fill_(fill)
+        return t
+
+    def check(self):
+        for i, (raw, n) in enumerate(self._bufs):
+            head = raw[:GUARD_BYTES]
+            tail = raw[GUARD_BYTES + n:]
+            assert bool((head == GUARD_BYTE).all()), f"guard before buffer {i} was written"
+            assert bool((tail == GUARD_BYTE).all()), f"guard after buffer {i} was written"

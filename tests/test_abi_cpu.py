@@ -237,6 +237,28 @@ def test_quest_host_validation(lib):
     assert lib.kvsel_quest_page_meta(ctypes.byref(kv), 16, 64, 16, 2, None, 256, None) == K.KVSEL_ERR_INVALID_ARG
 
 
+def test_kv_compact_host_validation(lib):
+    def st(kv_=None, **over):
+        a = dict(bt=16, max_pages=64, seq=16, B=2, keep=16, stride=100, count=None, scores=None, pos=None,
+                 max_len=0, freed=None, ws=256, ws_bytes=1 << 20)
+        a.update(over)
+        return lib.kvsel_kv_compact(ctypes.byref(kv_ or _kv()), a["bt"], a["max_pages"], a["seq"], a["B"],
+                                    a["keep"], a["stride"], a["count"], a["scores"], a["pos"], a["max_len"],
+                                    a["freed"], a["ws"], a["ws_bytes"], None)
+    assert st(kv_=_kv(v_pool=None)) == K.KVSEL_ERR_INVALID_ARG
+    assert st(kv_=_kv(k_pool=8)) == K.KVSEL_ERR_INVALID_ARG          # misaligned pool
+    assert st(kv_=_kv(page_size=256)) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(keep=None) == K.KVSEL_ERR_INVALID_ARG
+    assert st(stride=0) == K.KVSEL_ERR_INVALID_ARG
+    assert st(scores=16) == K.KVSEL_ERR_INVALID_ARG                  # scores without max_len
+    assert st(ws=128) == K.KVSEL_ERR_INVALID_ARG                     # misaligned workspace
+    need = K.kvsel_kv_compact_workspace(2, 8)
+    assert need >= 256 + 2 * 4 + 2 * 8 * 4
+    assert st(ws_bytes=need - 1) == K.KVSEL_ERR_INVALID_ARG
+    assert b"workspace too small" in lib.kvsel_last_error_string()
+    assert K.kvsel_kv_compact_workspace(0, 8) == 0
+
+
 def test_header_compiles_as_plain_c(tmp_path):
     # the boundary is a C ABI: the header must stand alone in C99 (every struct and enum named)
     import shutil
