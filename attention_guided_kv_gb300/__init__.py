@@ -68,6 +68,7 @@ _SIGS = {
     "kvsel_last_error_string": (ctypes.c_char_p, []),
     "kvsel_clear_status": (_i, [_vp, _vp]),
     "kvsel_read_status": (_i, [_vp, _vp]),
+    "kvsel_set_wait_limit": (_i, [_vp, ctypes.c_uint, _vp]),
     "kvsel_trace_start": (_i, [ctypes.POINTER(ctypes.c_void_p), _i]),
     "kvsel_trace_stop": (_i, [ctypes.POINTER(ctypes.c_char_p), _i]),
     "kvsel_decode_attn_workspace": (_sz, [_PKV, _i, _i, _i]),
@@ -170,6 +171,11 @@ def clear_status(workspace: torch.Tensor, stream=None):
 def read_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronise and return (and clear) the device status word of a workspace."""
     return int(lib().kvsel_read_status(_ptr(workspace), _stream(stream)))
+
+
+def set_wait_limit(workspace: torch.Tensor, spins: int, stream=None):
+    """Bound the cross-CTA waits of kernels using this workspace (0 = the default of a few seconds)."""
+    _check(lib().kvsel_set_wait_limit(_ptr(workspace), int(spins), _stream(stream)))
 
 
 class LaunchTrace:

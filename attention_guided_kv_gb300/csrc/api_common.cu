@@ -158,6 +158,20 @@ extern "C" kvsel_status kvsel_clear_status(void* workspace, void* stream) {
   return KVSEL_OK;
 }
 
+namespace {
+__global__ void set_wait_limit_kernel(unsigned* word, unsigned spins) { *word = spins; }
+}  // namespace
+
+extern "C" kvsel_status kvsel_set_wait_limit(void* workspace, unsigned spins, void* stream) {
+  if (!workspace || !aligned(workspace, 256))
+    return fail(KVSEL_ERR_INVALID_ARG, "kvsel_set_wait_limit: a 256-byte aligned workspace is required");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  set_wait_limit_kernel<<<1, 1, 0, st>>>(
+      reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + kvsel::kWaitLimitOffset), spins);
+  if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return cuda_fail(e, "kvsel_set_wait_limit");
+  return KVSEL_OK;
+}
+
 extern "C" kvsel_status kvsel_read_status(void* workspace, void* stream) {
   if (!workspace) return fail(KVSEL_ERR_INVALID_ARG, "kvsel_read_status: workspace is NULL");
   cudaStream_t st = static_cast<cudaStream_t>(stream);

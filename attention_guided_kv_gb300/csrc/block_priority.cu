@@ -436,9 +436,16 @@ __global__ void __launch_bounds__(1024) bp_rank_kernel(const BpParams P) {
   }
 }
 
-__device__ __forceinline__ void bp_grid_barrier(unsigned* bar, int* status) {
+// Grid barrier of the cooperative sort: 2^26 sleeps of ~32 ns (a few
+// seconds) unless the workspace sets another limit.  Returns false, in every
+// thread of the CTA, when the wait ran out (KVSEL_ERR_TIMEOUT recorded): the
+// caller must then stop, since the digit offsets it would scatter with may
+// be incomplete.
+__device__ __forceinline__ bool bp_grid_barrier(unsigned* bar, int* status) {
+  __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
+    int ok = 1;
     volatile unsigned* gen = bar + 32;
     const unsigned g = *gen;
     __threadfence();
@@ -447,18 +454,22 @@ __device__ __forceinline__ void bp_grid_barrier(unsigned* bar, int* status) {
       __threadfence();
       atomicAdd(bar + 32, 1u);
     } else {
+      const unsigned limit = spin_limit(status, 1u << 26);
       unsigned spins = 0;
       while (*gen == g) {
         __nanosleep(32);
-        if (++spins > (1u << 26)) {  // a few seconds
+        if (++spins >= limit) {
           report(status, KVSEL_ERR_TIMEOUT);
+          ok = 0;
           break;
         }
       }
     }
     __threadfence();
+    s_ok = ok;
   }
   __syncthreads();
+  return s_ok != 0;
 }
 
 __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams P) {
@@ -519,7 +530,7 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
     __syncthreads();
 #pragma unroll
     for (int d = 0; d < 16; ++d) cnt[d][tid] = wtot[warp][d] + x[d] - v[d];  // exclusive offset inside this CTA
-    bp_grid_barrier(P.bar, P.status);
+    if (!bp_grid_barrier(P.bar, P.status)) return;  // timed out: stop before any scatter
     {
       // start of digit d for this CTA = all keys with a smaller digit + this
       // digit's keys in earlier CTAs; 16 stripes of CTAs x 16 digits in parallel
@@ -560,7 +571,7 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
       ok[pos] = k;
       ov[pos] = iv[e];
     }
-    bp_grid_barrier(P.bar, P.status);
+    if (!bp_grid_barrier(P.bar, P.status)) return;  // timed out: stop before any scatter
   }
   // 8 passes: the sorted keys are back in buffer 0
   long long n_all = P.meta[1];

@@ -27,6 +27,18 @@ __device__ __forceinline__ void report(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Waits on other CTAs (a readiness counter, a grid barrier) spin a bounded
+// number of times, each spin a short sleep.  The bound is the kernel's
+// default (a few seconds) unless the workspace's status block holds a
+// non-zero override at this byte offset (kvsel_set_wait_limit).
+constexpr size_t kWaitLimitOffset = 32;
+__device__ __forceinline__ unsigned spin_limit(const int* status, unsigned dflt) {
+  if (!status) return dflt;
+  const unsigned v =
+      __ldcg(reinterpret_cast<const unsigned*>(reinterpret_cast<const uint8_t*>(status) + kWaitLimitOffset));
+  return v ? v : dflt;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -137,14 +137,18 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-// Bounded spin of one thread until *word == target.  On expiry it records
-// KVSEL_ERR_TIMEOUT and returns false (results are then unspecified, but
-// nothing hangs).
+// Bounded spin of one thread until *word == target: 2^25 sleeps of ~64 ns
+// (a few seconds) unless the workspace sets another limit.  On expiry it
+// records KVSEL_ERR_TIMEOUT and returns false; the caller carries on with
+// whatever the partial slots hold (every index it uses comes from the work
+// split, never from those values), so results are unspecified but every
+// access stays in bounds and nothing hangs.
 __device__ __forceinline__ bool wait_word(const unsigned* word, unsigned target, int* status) {
+  const unsigned limit = spin_limit(status, 1u << 25);
   unsigned spins = 0;
   while (*reinterpret_cast<const volatile unsigned*>(word) != target) {
     __nanosleep(64);
-    if (++spins > (1u << 25)) {  // a few seconds
+    if (++spins >= limit) {
       report(status, KVSEL_ERR_TIMEOUT);
       return false;
     }

@@ -574,6 +574,41 @@ def _setup_snapkv(dev, small=False):
                     ("head_union", run_ex(K.KVSEL_SNAP_HEAD_UNION, False)),
                     ("head_union_with_seeds", run_ex(K.KVSEL_SNAP_HEAD_UNION, True))]
 
+    def compact_after():
+        """Compaction of the kept prompt cache (kvsel_kv_compact on the group-sum keep lists), timed
+        once the selections above are done: it rewrites the pool in place, so every repetition first
+        restores the lengths and the block table (outside the timed events) and then moves the same
+        rows again (same bytes moved)."""
+        vpool = torch.empty_like(kpool)
+        kvc = K.paged_kv(kpool, vpool, wl.Hq)
+        count_g = torch.zeros(wl.L, wl.Hkv, dtype=torch.int32, device=dev)
+        K.kvsel_snapkv_select_ex(kvc, bt, q, keep, ws_u, seq_len=wl.S, keep_k=wl.keep_k,
+                                 pool_kernel=wl.pool_kernel, keep_count=count_g)
+        bt0 = bt.clone()
+        lens = torch.full((wl.L,), wl.S, dtype=torch.int32, device=dev)
+        freed = torch.zeros(wl.L, P, dtype=torch.int32, device=dev)
+        ws_c = K.workspace(K.kvsel_kv_compact_workspace(wl.L, wl.Hkv))
+        times = []
+        for rep in range(6):
+            bt.copy_(bt0)
+            lens.fill_(wl.S)
+            torch.cuda.synchronize()
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            K.kvsel_kv_compact(kvc, bt, lens, keep, ws_c, keep_count=count_g, freed_pages=freed)
+            b2.record()
+            torch.cuda.synchronize()
+            if rep >= 2:
+                times.append(a.elapsed_time(b2) * 1e3)
+        if K.read_status(ws_c):
+            raise RuntimeError("device status after the compaction")
+        bt.copy_(bt0)
+        us = sum(times) / len(times)
+        moved = wl.L * wl.Hkv * (wl.keep_k + wl.W) * 2 * 512   # K and V rows, read and written
+        return {"compact_us": us, "compact_gbs": moved / (us * 1e-6) / 1e9,
+                "compact_note": "kvsel_kv_compact of the 28 x 4 x 2080 kept rows (K and V, read + write "
+                                "1024 B per row), mean of 4 calls after 2 untimed"}
+
     pairs = wl.L * wl.Hkv
     rows = wl.G * wl.W
     qk_flops = 2.0 * rows * wl.S * wl.d * pairs
@@ -583,7 +618,7 @@ def _setup_snapkv(dev, small=False):
     return dict(step=step, run=run, host_in=[("q_obs", q[None])], outs=[keep], ws=[ws, ws_u],
                 bytes={"snap_stats": kbytes, "snap_vote": kbytes}, flops={"snap_stats": qk_flops,
                 "snap_vote": 2.0 * rows * (wl.S - wl.W) * wl.d * pairs}, ex2=ex2, per_step_launches=3,
-                variant_runs=variant_runs, variants_key="variants_us_per_select",
+                variant_runs=variant_runs, variants_key="variants_us_per_select", after=compact_after,
                 config={"layers": wl.L, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "prompt": wl.S,
                         "obs_window": wl.W, "keep": wl.keep_k, "pool_kernel": wl.pool_kernel,
                         "l2": "inputs larger than L2 (940 MB of K per pass)"})
@@ -926,6 +961,7 @@ def other_workload(args, rank, world):
             b2.record(stream)
             torch.cuda.synchronize()
             variants[name] = a.elapsed_time(b2) / 20 * 1e3
+    after = S["after"]() if S.get("after") else None
     clocks.stop()
     for w in S["ws"]:
         st = K.read_status(w)
@@ -979,6 +1015,8 @@ def other_workload(args, rank, world):
         line["config"]["eager_ms_per_step"] = eager_ms / steps
     if variants:
         line[S.get("variants_key", "variants_us_per_pass")] = variants
+    if after:
+        line.update(after)
     if args.small:
         line["note"] = "--small profiling case, not the measured workload"
     if not args.no_cpu_baseline:

@@ -79,6 +79,18 @@ KVSEL_API kvsel_status kvsel_clear_status(void* workspace, void* stream);
  * since it was last cleared, and clear it. */
 KVSEL_API kvsel_status kvsel_read_status(void* workspace, void* stream);
 
+/* Bound the waits on other CTAs of the kernels that use `workspace` (the
+ * decode step's per-pair readiness counters, the block-priority sort's grid
+ * barriers) at `spins` short sleeps (tens of ns each) instead of the default
+ * of a few seconds; 0 restores the default.  Enqueued on `stream`; the value
+ * sits in the workspace's status block and stays until changed or the
+ * workspace is zeroed.  A wait that runs out records KVSEL_ERR_TIMEOUT and
+ * the kernel finishes without hanging: the decode step's results are then
+ * unspecified (every access stays in bounds), the sort stops before its
+ * scatter.  Waits inside one CTA (TMA stages) keep their own fixed bound.
+ * Failure-detection tests use a short limit with a wait that nothing ends. */
+KVSEL_API kvsel_status kvsel_set_wait_limit(void* workspace, unsigned spins, void* stream);
+
 /* Launch tracing for profiling.  While tracing is on for the calling thread,
  * every kernel the library launches from that thread records
  * events[2i] just before and events[2i+1] just after launch i, on the launch

@@ -23,6 +23,49 @@ def rel_l2(x, ref) -> float:
     return float(np.linalg.norm(x - ref) / (n if n > 0 else 1.0))
 
 
+GUARD_BYTES = 256
+GUARD_BYTE = 0xA5
+
+
+class Guards:
+    """Output buffers with guard regions before and after each one.
+
+    Every buffer is carved from a larger allocation whose first and last
+    GUARD_BYTES bytes hold a fixed pattern; ``check()`` asserts that no call
+    wrote outside the buffer it was given (the tail and padding paths of the
+    kernels, without a sanitizer).
+    """
+
+    def __init__(self, dev="cuda"):
+        self.dev = dev
+        self._bufs = []
+
+    def new(self, shape, dtype, fill=0):
+        shape = tuple(int(s) for s in shape)
+        n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+        body = (n + GUARD_BYTES - 1) // GUARD_BYTES * GUARD_BYTES
+        raw = torch.full((2 * GUARD_BYTES + body,), GUARD_BYTE, dtype=torch.uint8, device=self.dev)
+        t = raw[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+        t.fill_(fill)
+        self._bufs.append((raw, n))
+        return t
+
+    def like(self, src, fill=None):
+        t = self.new(src.shape, src.dtype)
+        if fill is None:
+            t.copy_(src)
+        else:
+            t.fill_(fill)
+        return t
+
+    def check(self):
+        for i, (raw, n) in enumerate(self._bufs):
+            head = raw[:GUARD_BYTES]
+            tail = raw[GUARD_BYTES + n:]
+            assert bool((head == GUARD_BYTE).all()), f"guard before buffer {i} was written"
+            assert bool((tail == GUARD_BYTE).all()), f"guard after buffer {i} was written"
+
+
 class DecodeState:
     """Device-side paged cache + bookkeeping for a DecodeWorkload."""
 
@@ -39,21 +82,24 @@ class DecodeState:
         self.bt = torch.from_numpy(self.bt_host).to(dev)
         self.free = list(range(wl.num_pages, npages))
         self.S = np.full(wl.B, wl.S0, dtype=np.int64)
-        self.seq = torch.from_numpy(self.S.astype(np.int32)).to(dev)
-        self.cum = torch.zeros(wl.B, wl.Hkv, wl.max_len, device=dev)
-        self.probs = torch.zeros(wl.B, wl.Hq, wl.max_len, device=dev) if with_probs else None
+        # every buffer the calls write sits between guard regions (checked by status())
+        self.guards = g = Guards(dev)
+        self.bt = g.like(self.bt)
+        self.seq = g.like(torch.from_numpy(self.S.astype(np.int32)).to(dev))
+        self.cum = g.new((wl.B, wl.Hkv, wl.max_len), torch.float32)
+        self.probs = g.new((wl.B, wl.Hq, wl.max_len), torch.float32) if with_probs else None
         if with_pos:
             pos = np.tile(np.arange(wl.max_len, dtype=np.int32), (wl.B, wl.Hkv, 1))
-            self.pos = torch.from_numpy(pos).to(dev)
-            self.next_pos = torch.full((wl.B,), wl.S0, dtype=torch.int32, device=dev)
+            self.pos = g.like(torch.from_numpy(pos).to(dev))
+            self.next_pos = g.like(torch.full((wl.B,), wl.S0, dtype=torch.int32, device=dev))
         else:
             self.pos = self.next_pos = None
-        self.out = torch.zeros(wl.B, wl.Hq, wl.d, device=dev,
-                               dtype=torch.float32 if out_f32 else torch.bfloat16)
-        self.ws = K.workspace(K.kvsel_decode_attn_workspace(self.kv, wl.B, wl.max_len, with_probs))
-        self.ws_ev = K.workspace(K.kvsel_h2o_evict_workspace(self.kv, wl.B, wl.budget))
-        self.keep = torch.full((wl.B, wl.Hkv, wl.budget), -1, dtype=torch.int32, device=dev)
-        self.freed = torch.full((wl.B, self.bt_host.shape[1]), -1, dtype=torch.int32, device=dev)
+        self.out = g.new((wl.B, wl.Hq, wl.d), torch.float32 if out_f32 else torch.bfloat16)
+        self.ws = g.new((max(256, K.kvsel_decode_attn_workspace(self.kv, wl.B, wl.max_len, with_probs)),),
+                        torch.uint8)
+        self.ws_ev = g.new((max(256, K.kvsel_h2o_evict_workspace(self.kv, wl.B, wl.budget)),), torch.uint8)
+        self.keep = g.new((wl.B, wl.Hkv, wl.budget), torch.int32, fill=-1)
+        self.freed = g.new((wl.B, self.bt_host.shape[1]), torch.int32, fill=-1)
 
     def ensure_append_page(self):
         """Give every sequence a page for its next slot (host-side allocator)."""
@@ -98,47 +144,7 @@ class DecodeState:
         return self.ws_ev[off:off + rows * 4].view(torch.int32).cpu().numpy().copy()
 
     def status(self):
-        return K.read_status(self.ws), K.read_status(self.ws_ev)
-
-
-GUARD_BYTES = 256
-GUARD_BYTE = 0xA5
-
-
-class Guards:
-    """Output buffers with guard regions before and after each one.
-
-    Every buffer is carved from a larger allocation whose first and last
-    GUARD_BYTES bytes hold a fixed pattern; ``check()`` asserts that no call
-    wrote outside the buffer it was given (the tail and padding paths of the
-    kernels, without a sanitizer).
-    """
-
-    def __init__(self, dev="cuda"):
-        self.dev = dev
-        self._bufs = []
-
-    def new(self, shape, dtype, fill=0):
-        shape = tuple(int(s) for s in shape)
-        n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
-        body = (n + GUARD_BYTES - 1) // GUARD_BYTES * GUARD_BYTES
-        raw = torch.full((2 * GUARD_BYTES + body,), GUARD_BYTE, dtype=torch.uint8, device=self.dev)
-        t = raw[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
-        t.fill_(fill)
-        self._bufs.append((raw, n))
-        return t
-
-    def like(self, src, fill=None):
-        t = self.new(src.shape, src.dtype)
-        if fill is None:
-            t.copy_(src)
-        else:
-            t.fill_(fill)
-        return t
-
-    def check(self):
-        for i, (raw, n) in enumerate(self._bufs):
-            head = raw[:GUARD_BYTES]
-            tail = raw[GUARD_BYTES + n:]
-            assert bool((head == GUARD_BYTE).all()), f"guard before buffer {i} was written"
-            assert bool((tail == GUARD_BYTE).all()), f"guard after buffer {i} was written"
+        """Device status of both workspaces (read and cleared); asserts the guards are intact."""
+        st = K.read_status(self.ws), K.read_status(self.ws_ev)
+        self.guards.check()
+        return st

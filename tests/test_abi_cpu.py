@@ -237,6 +237,12 @@ def test_quest_host_validation(lib):
     assert lib.kvsel_quest_page_meta(ctypes.byref(kv), 16, 64, 16, 2, None, 256, None) == K.KVSEL_ERR_INVALID_ARG
 
 
+def test_wait_limit_host_validation(lib):
+    assert lib.kvsel_set_wait_limit(None, 100, None) == K.KVSEL_ERR_INVALID_ARG
+    assert lib.kvsel_set_wait_limit(16, 100, None) == K.KVSEL_ERR_INVALID_ARG     # misaligned workspace
+    assert b"aligned" in lib.kvsel_last_error_string()
+
+
 def test_kv_compact_host_validation(lib):
     def st(kv_=None, **over):
         a = dict(bt=16, max_pages=64, seq=16, B=2, keep=16, stride=100, count=None, scores=None, pos=None,

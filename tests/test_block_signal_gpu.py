@@ -26,13 +26,14 @@ class SignalState(DecodeState):
     def __init__(self, wl, k, **kw):
         super().__init__(wl, **kw)
         self.k = k
-        self.ws = K.workspace(K.kvsel_decode_attn_ex_workspace(self.kv, wl.B, wl.max_len, self.probs is not None,
-                                                               True))
+        g = self.guards
+        self.ws = g.new((K.kvsel_decode_attn_ex_workspace(self.kv, wl.B, wl.max_len, self.probs is not None,
+                                                          True),), torch.uint8)
         n_pool = self.kpool.shape[0]
-        self.score = torch.zeros(n_pool, device="cuda")
-        self.last = torch.full((n_pool,), -1, dtype=torch.int32, device="cuda")
-        self.topk = torch.full((wl.B, k), -7, dtype=torch.int32, device="cuda")
-        self.mass = torch.zeros(wl.B, -(-wl.max_len // 16), device="cuda")
+        self.score = g.new((n_pool,), torch.float32)
+        self.last = g.new((n_pool,), torch.int32, fill=-1)
+        self.topk = g.new((wl.B, k), torch.int32, fill=-7)
+        self.mass = g.new((wl.B, -(-wl.max_len // 16)), torch.float32)
 
     def decode_signal(self, step):
         wl = self.wl
@@ -61,6 +62,7 @@ def _run_and_check(st, steps, seqs=None):
         st.decode_signal(t)
         torch.cuda.synchronize()
         assert K.read_status(st.ws) == 0
+        st.guards.check()
         mass = st.mass.cpu().numpy()
         topk = st.topk.cpu().numpy()
         out = st.out.double().cpu().numpy()

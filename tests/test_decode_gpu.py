@@ -68,6 +68,7 @@ def test_group_sizes(Hq, Hkv):
     st = DecodeState(wl)
     st.decode(0)
     torch.cuda.synchronize()
+    assert st.status() == (0, 0)
     _check_step(st, wl)
 
 
@@ -88,6 +89,7 @@ def test_single_token_returns_its_value():
     st = DecodeState(wl)
     st.decode(0)
     torch.cuda.synchronize()
+    assert st.status() == (0, 0)
     v = bf16_bits_to_f64(wl.v_new[0, 0])
     np.testing.assert_allclose(st.out[0].double().cpu().numpy(), np.repeat(v, 2, axis=0), rtol=1e-6)
     np.testing.assert_array_equal(st.probs[0, :, 0].cpu().numpy(), np.ones(16, dtype=np.float32))
@@ -101,6 +103,7 @@ def test_mixed_batch_lengths_without_append():
     st.seq.copy_(torch.from_numpy(lens.astype(np.int32)))
     st.decode(0, append=False)
     torch.cuda.synchronize()
+    assert st.status() == (0, 0)
     for b in range(3):
         S = int(lens[b])
         Kb = bf16_bits_to_f64(wl.K[b])[:, :S]
@@ -117,6 +120,7 @@ def test_bf16_output_and_no_probs_buffer():
     st = DecodeState(wl, with_probs=False, out_f32=False)
     st.decode(0)
     torch.cuda.synchronize()
+    assert st.status() == (0, 0)
     _check_step(st, wl)
 
 
@@ -128,6 +132,7 @@ def test_bad_block_table_entry_is_reported_not_faulted():
     st.decode(0)
     assert K.read_status(st.ws) == K.KVSEL_ERR_BAD_INDEX
     assert K.read_status(st.ws) == 0        # cleared by the read
+    st.guards.check()
 
 
 @pytest.mark.slow

@@ -14,7 +14,7 @@ import torch
 import workloads
 from oracle.attention import bf16_bits_to_f64
 from oracle.h2o import H2OSequence, h2o_keep
-from _harness import DecodeState, bf16, rel_l2
+from _harness import DecodeState, Guards, bf16, rel_l2
 
 import attention_guided_kv_gb300 as K
 
@@ -27,15 +27,17 @@ def _run_select(cum_np, S_list, budget, n_sink, window, max_len, pos=None):
     dev = "cuda"
     kpool = torch.zeros(1, Hkv, 16, 128, dtype=torch.bfloat16, device=dev)
     kv = K.paged_kv(kpool, kpool, Hkv)
-    bt = torch.zeros(B, (max_len + 15) // 16, dtype=torch.int32, device=dev)
-    seq = torch.tensor(S_list, dtype=torch.int32, device=dev)
-    cum = torch.from_numpy(cum_np.astype(np.float32)).to(dev)
-    keep = torch.full((B, Hkv, budget), -7, dtype=torch.int32, device=dev)
-    ws = K.workspace(K.kvsel_h2o_evict_workspace(kv, B, budget))
+    g = Guards()
+    bt = g.new((B, (max_len + 15) // 16), torch.int32)
+    seq = g.like(torch.tensor(S_list, dtype=torch.int32, device=dev))
+    cum = g.like(torch.from_numpy(cum_np.astype(np.float32)).to(dev))
+    keep = g.new((B, Hkv, budget), torch.int32, fill=-7)
+    ws = g.new((K.kvsel_h2o_evict_workspace(kv, B, budget),), torch.uint8)
     K.kvsel_h2o_evict(kv, bt, seq, cum, ws, budget=budget, n_sink=n_sink, window=window,
                       compact=False, keep_out=keep,
-                      pos_map=None if pos is None else torch.from_numpy(pos).to(dev))
+                      pos_map=None if pos is None else g.like(torch.from_numpy(pos).to(dev)))
     assert K.read_status(ws) == 0
+    g.check()
     return keep.cpu().numpy()
 
 
@@ -165,19 +167,23 @@ def test_compaction_moves_rows_exactly():
     assert st.seq.cpu().tolist() == [wl.budget] * wl.B
 
 
-def _run_mode_a(wl, steps, link=False):
-    """Evict-every-step loop on GPU and oracle with teacher forcing at near-ties."""
+def _run_mode_a(wl, steps, link=False, track=None):
+    """Evict-every-step loop on GPU and oracle with teacher forcing at near-ties.
+
+    The GPU steps every sequence of the batch; the oracle follows the
+    sequences in ``track`` (all of them by default)."""
+    track = list(range(wl.B)) if track is None else list(track)
     st = DecodeState(wl, spare_pages=8, link=link)
-    refs = [H2OSequence(bf16_bits_to_f64(wl.K[b]), bf16_bits_to_f64(wl.V[b])) for b in range(wl.B)]
+    refs = {b: H2OSequence(bf16_bits_to_f64(wl.K[b]), bf16_bits_to_f64(wl.V[b])) for b in track}
     swaps = 0
     for t in range(steps):
         st.decode(t)
         torch.cuda.synchronize()
         S = int(st.S[0])
-        probs = st.probs[:, :, :S].double().cpu().numpy()
-        outs = st.out.double().cpu().numpy()
-        cum_gpu = st.cum[:, :, :S].double().cpu().numpy()
-        for b, ref in enumerate(refs):
+        probs = dict(zip(track, st.probs[track, :, :S].double().cpu().numpy()))
+        outs = dict(zip(track, st.out[track].double().cpu().numpy()))
+        cum_gpu = dict(zip(track, st.cum[track, :, :S].double().cpu().numpy()))
+        for b, ref in refs.items():
             ref.append(bf16_bits_to_f64(wl.k_new[t, b]), bf16_bits_to_f64(wl.v_new[t, b]))
             o, p = ref.attend(bf16_bits_to_f64(wl.q[t, b]), wl.scale)
             assert ref.S == S
@@ -190,7 +196,7 @@ def _run_mode_a(wl, steps, link=False):
         if S <= wl.budget:
             continue
         kept_pos = st.keep.cpu().numpy()
-        for b, ref in enumerate(refs):
+        for b, ref in refs.items():
             want = ref.select(wl.budget, wl.n_sink, wl.window)
             want_pos = np.stack([ref.pos[h, want[h]] for h in range(wl.Hkv)])
             if not np.array_equal(kept_pos[b], want_pos):
@@ -205,8 +211,11 @@ def _run_mode_a(wl, steps, link=False):
                     for p in diff:
                         assert abs(ref.cum[h, slot[p]] - kth) <= 1e-5 * kth, (t, b, h, p)
                     swaps += 1
-                gpu_slots = np.stack([[{int(p): i for i, p in enumerate(ref.pos[h])}[int(x)]
-                                       for x in kept_pos[b, h]] for h in range(wl.Hkv)])
+                gpu_slots = []
+                for h in range(wl.Hkv):
+                    slot = {int(p): i for i, p in enumerate(ref.pos[h])}
+                    gpu_slots.append([slot[int(x)] for x in kept_pos[b, h]])
+                gpu_slots = np.array(gpu_slots, dtype=np.int64)
                 ref.apply_keep(gpu_slots)
             else:
                 ref.apply_keep(want)
@@ -217,6 +226,16 @@ def test_small_config_evict_every_step_end_to_end():
     wl = workloads.decode_small()
     swaps = _run_mode_a(wl, wl.steps)
     assert swaps <= 4
+
+
+@pytest.mark.slow
+def test_70b_shape_evict_every_step_end_to_end():
+    """The 70B layer shape evicting every step: batch 8 x 32K, budget 6553 = 4 sinks + 1024
+    window + 5525 heavy hitters, all 128 steps with the decode -> select hand-off; the oracle
+    follows sequences 0 and 5 step by step (outputs, probabilities, scores, keep-sets)."""
+    wl = workloads.decode_70b()
+    swaps = _run_mode_a(wl, wl.steps, link=True, track=[0, 5])
+    assert swaps <= 32, swaps
 
 
 @pytest.mark.parametrize("link", [False, True])
