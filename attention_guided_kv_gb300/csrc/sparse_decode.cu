@@ -11,25 +11,38 @@
 //   o[b, h] = softmax over s in sel_b of scale * q[b, h] . K_{h/G}[s], times V
 // One selected set per (sequence, step), shared by every q head.
 //
-// Kernels (four launches on the caller's stream):
-//   sd_index_kernel      128 tokens per CTA; the indexer dot products run on
-//                        mma.sync (16 tokens x 16 dims x 8 heads per MMA, the
-//                        dims permuted per lane so every lane reads 8-byte runs
-//                        of a key row); also writes the appended token's K, V
-//                        and indexer key.
-//   sd_topk_chunk_kernel exact top-k (row_topk) of every 16K-position chunk
-//                        of a row, many CTAs per row: the candidates (key and
-//                        position, in position order)
-//   sd_topk_final_kernel exact top-k of each row over its chunk candidates;
-//                        kept positions come out ascending.  (With top_k >=
-//                        16K a single sd_topk_kernel per row replaces both.)
-//   sd_attn_kernel       (splits, kv head, sequence): each warp gathers 16
-//                        selected rows of K and V with cp.async into the
-//                        swizzled tile layout (double-buffered; the pages were
-//                        resolved by the top-k stage) and runs the shared
-//                        mma.sync tile; the 4 warps merge per CTA; the last
-//                        split of a (sequence, kv head) merges the splits
-//                        into O and the last kv head publishes the length
+// Kernels (three launches on the caller's stream, chained by programmatic
+// launch so each one's launch overlaps its predecessor's tail):
+//   sd_index_kernel   (CTA range of 16-token tiles, sequence): streams the
+//                     sequence's indexer keys with 16-byte loads, four tiles
+//                     in flight per warp; the dot products run on mma.sync
+//                     (16 tokens x 16 dims x 8 heads per MMA, the dims
+//                     permuted per lane so that a lane's 16-byte run of a key
+//                     row feeds two k-steps); writes the scores and adds their
+//                     top 12 key bits to a per-row histogram (a shared-memory
+//                     histogram per CTA, flushed once); also writes the
+//                     appended token's K, V and indexer key.
+//   sd_select_kernel  (slices, sequence), 1024 threads: every CTA finds, from
+//                     the histogram, the bin holding the k-th largest score
+//                     and appends the positions of its slice scoring in or
+//                     above that bin to a candidate list (a few thousand at
+//                     the 128K shape); the last CTA of the row selects the
+//                     exact top_k among the candidates (radix select on the
+//                     keys, bitmaps over the positions for the tie rule and
+//                     the ascending order), resolves each selected position's
+//                     page, and resets the row's histogram and counters.
+//                     Lists too long for shared memory fall back to the
+//                     whole-row select (row_topk) in the same CTA.
+//   sd_attn_kernel    (splits, kv head, sequence), the splits of a (sequence,
+//                     kv head) one thread-block cluster: each warp gathers 16
+//                     selected rows of K and V at a time with cp.async into
+//                     the swizzled tile layout (three tiles in flight; the
+//                     pool rows, resolved by the select, loaded four tiles at
+//                     a time and shared by shuffles) and runs the shared
+//                     mma.sync tile; the 4 warps merge per CTA into shared
+//                     memory, the cluster's CTAs merge the splits through
+//                     distributed shared memory (each writes a slice of O),
+//                     and the last kv head of a sequence publishes its length
 #include "attn_tile.cuh"
 #include "row_topk.cuh"
 
@@ -39,15 +52,26 @@ constexpr int kSdD = 128;
 constexpr int kSdPage = 16;
 constexpr int kSdDi = 64;
 constexpr int kSdMaxHi = 8;
-constexpr int kSdTopkGroups = 8;         // rows up to 32K stay in registers; longer rows are swept
-constexpr int kSdChunk = 16384;          // positions per first-stage top-k chunk (top_k < kSdChunk)
+constexpr int kSdTopkGroups = 8;         // whole-row fallback: rows up to 32K stay in registers
 constexpr int kSdMaxLen = 1 << 28;
-constexpr int kSdMaxSplits = kTileMaxSplits;
 constexpr int kSdMaxG = kTileMaxG;
 constexpr int kSdPartFloats = kPartFloats;
 constexpr int kSdAttnWarps = 4;
-constexpr size_t kSdAttnSmem = size_t(kSdAttnWarps) * 2 * 8192 + 1024 +
-                               size_t(kSdAttnWarps) * kSdMaxG * (kSdD + 2) * 4;
+constexpr int kSdAttnStages = 3;         // gathered tiles in flight per warp
+constexpr int kSdMaxClusterSplits = 8;   // splits of a (sequence, kv head): one portable cluster
+// the warps' rings; the CTA's merge scratch reuses them once every tile is consumed
+constexpr size_t kSdAttnRing = size_t(kSdAttnWarps) * kSdAttnStages * 8192;
+static_assert(kSdAttnRing >= size_t(kSdAttnWarps) * kSdMaxG * (kSdD + 2) * 4, "merge scratch fits in the rings");
+constexpr size_t kSdAttnSmem = kSdAttnRing + 1024;
+constexpr int kSdIdxWarps = 8;           // indexer CTA: 8 warps
+constexpr int kSdIdxBatch = 4;           // tiles of 16 tokens a warp loads before computing
+constexpr int kSdHistBits = 12;          // histogram of the top 12 bits of a score's order key
+constexpr int kSdHistBins = 1 << kSdHistBits;
+constexpr int kSdSelThreads = 1024;
+constexpr int kSdCandCap = 8192;         // candidates per row the final select holds (8 per thread)
+constexpr int kSdSelSlice = 16 * kSdSelThreads;  // positions a select CTA scans (16 per thread)
+constexpr int kSdSliceCap = 2048;        // candidates a slice may hand over (more: whole-row select)
+constexpr int kSdMaxSlices = kSdSelThreads;  // slices the final select reads in one pass (rows to 16M)
 
 struct SdParams {
   const int32_t* block_table;
@@ -62,18 +86,22 @@ struct SdParams {
   __nv_bfloat16* idx_k;            // [B][max_len][64]
   const __nv_bfloat16* idx_k_new;  // [B][64] or null
   float* scores;                   // [B][max_len] (workspace or the caller's buffer)
-  uint32_t* cand_key;              // [B][nchunks][top_k]: first-stage candidates (two-stage only)
-  int32_t* cand_pos;               // [B][nchunks][top_k]
+  uint32_t* hist;                  // [B][kSdHistBins]: score counts by top key bits (zero between calls)
+  uint32_t* subhist;               // [B][kSdHistBins]: the threshold bin's counts by the next 12 bits (zero)
+  unsigned* cand_cnt;              // [B][slices]: candidates each select slice found
+  unsigned* row_done;              // [B]: select CTAs finished (zero between calls)
+  uint32_t* cand_key;              // [B][slices][kSdSliceCap], each slice in position order
+  int32_t* cand_pos;               // [B][slices][kSdSliceCap]
+  int32_t* cand_row;               // [B][slices][kSdSliceCap]: the candidate's pool row for kv head 0
   int32_t* sel;                    // [B][top_k]
-  int32_t* sel_page;               // [B][top_k]: physical page of each selected position
-  unsigned* merge_cnt;             // [B][Hkv]: splits done (the last one merges)
+  int32_t* sel_row;                // [B][top_k]: pool row of each selected position for kv head 0
   unsigned* seq_cnt;               // [B]: kv heads merged (the last one publishes the length)
   int32_t* nsel;                   // [B]
   int32_t* topk_out;               // [B][top_k] or null
-  float* part;                     // [B][Hkv][splits][kSdPartFloats]
   void* out;
   int* status;
-  int B, max_pages, Hq, Hkv, G, Hi, num_pages, max_len, top_k, nchunks, splits, appended, out_f32;
+  int B, max_pages, Hq, Hkv, G, Hi, num_pages, max_len, top_k, idx_ctas, slices, splits, appended, out_f32;
+  int scores_vec;                  // score rows are 16-byte aligned (float4 reads)
   float scale_log2;
 };
 
@@ -94,16 +122,28 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) sd_index_kernel(const SdParams P) {
-  const int b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// Indexer.  Lane (g, q) of a warp holds, for a tile of 16 tokens, rows g and
+// g + 8 as two 16-byte runs each: dims 8q..8q+7 and 32+8q..32+8q+7.  MMA
+// k-step t takes the half (t & 1) of run (t >> 1) as its logical k's
+// {2q, 2q+1 | 2q+8, 2q+9}; the indexer query (the B operand) is read with the
+// same permutation, so each product pairs the same physical dims.
+__global__ void __launch_bounds__(kSdIdxWarps * 32) sd_index_kernel(const SdParams P) {
+  __shared__ uint32_t s_hist[kSdHistBins];
+  // launched early when the previous kernel allows it (the previous step's attention does, once its
+  // gathers are done): nothing is read or written before that kernel has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the select waits for this grid
+  const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int S;
   if (!sd_len_ok(P, b, S)) {
-    if (blockIdx.x == 0 && tid == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
+    if (c == 0 && tid == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
     return;
   }
   const int S_old = S - P.appended;
-  if (P.appended && blockIdx.x == 0) {
-    // the new token's K, V (every kv head) and indexer key
+  const int tiles = (S + 15) / 16;
+  const int t0 = int((long long)tiles * c / P.idx_ctas), t1 = int((long long)tiles * (c + 1) / P.idx_ctas);
+  if (P.appended && S_old / 16 >= t0 && S_old / 16 < t1) {
+    // this CTA covers the appended token: its K, V (every kv head) and indexer key
     const int phys = P.block_table[size_t(b) * P.max_pages + S_old / kSdPage];
     if (unsigned(phys) < unsigned(P.num_pages)) {
       for (int i = tid; i < P.Hkv * 32; i += blockDim.x) {
@@ -121,238 +161,534 @@ __global__ void __launch_bounds__(128) sd_index_kernel(const SdParams P) {
       reinterpret_cast<uint4*>(P.idx_k + (size_t(b) * P.max_len + S_old) * kSdDi)[tid] =
           reinterpret_cast<const uint4*>(P.idx_k_new + size_t(b) * kSdDi)[tid];
   }
+  for (int i = tid; i < kSdHistBins; i += blockDim.x) s_hist[i] = 0u;
   const int g = lane >> 2, qd = lane & 3;
-  // B fragments: indexer head g (zero past Hi), dims permuted per k-step t:
-  // logical k {2q, 2q+1, 2q+8, 2q+9} <-> physical dims 16t + 4q + {0, 1, 2, 3}
+  // B fragments: indexer head g (zero past Hi), dims permuted as described above
   uint32_t bq[4][2];
   const bool h_ok = g < P.Hi;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     uint2 v = make_uint2(0u, 0u);
-    if (h_ok) v = *reinterpret_cast<const uint2*>(P.idx_q + (size_t(b) * P.Hi + g) * kSdDi + 16 * t + 4 * qd);
+    if (h_ok)
+      v = *reinterpret_cast<const uint2*>(P.idx_q + (size_t(b) * P.Hi + g) * kSdDi + 8 * (qd + 4 * (t >> 1)) +
+                                          4 * (t & 1));
     bq[t][0] = v.x;
     bq[t][1] = v.y;
   }
   const float w0 = 2 * qd < P.Hi ? P.idx_w[b * P.Hi + 2 * qd] : 0.f;
   const float w1 = 2 * qd + 1 < P.Hi ? P.idx_w[b * P.Hi + 2 * qd + 1] : 0.f;
   float* srow = P.scores + size_t(b) * P.max_len;
+  const __nv_bfloat16* kbase = P.idx_k + size_t(b) * P.max_len * kSdDi;
+  const __nv_bfloat16* knew = P.appended ? P.idx_k_new + size_t(b) * kSdDi : nullptr;
+  __syncthreads();  // histogram cleared
+#pragma unroll 1
+  for (int tb = t0 + warp; tb < t1; tb += kSdIdxWarps * kSdIdxBatch) {
+    uint4 ra[kSdIdxBatch][2], rb[kSdIdxBatch][2];
 #pragma unroll
-  for (int grp = 0; grp < 2; ++grp) {
-    const int tok0 = blockIdx.x * 128 + warp * 32 + grp * 16;
-    if (tok0 >= S) break;
-    const int ta = tok0 + g, tb = tok0 + g + 8;
-    auto krow = [&](int s) -> const __nv_bfloat16* {
-      return (P.appended && s == S_old) ? P.idx_k_new + size_t(b) * kSdDi
-                                        : P.idx_k + (size_t(b) * P.max_len + s) * kSdDi;
-    };
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < kSdIdxBatch; ++j) {
+      const int tile = tb + j * kSdIdxWarps;
+      const int ta = tile * 16 + g, tbk = ta + 8;
+      const bool oka = tile < t1 && ta < S, okb = tile < t1 && tbk < S;
+      const __nv_bfloat16* pa = (knew && ta == S_old) ? knew : kbase + size_t(ta) * kSdDi;
+      const __nv_bfloat16* pb = (knew && tbk == S_old) ? knew : kbase + size_t(tbk) * kSdDi;
+      ra[j][0] = oka ? __ldcs(reinterpret_cast<const uint4*>(pa + 8 * qd)) : make_uint4(0u, 0u, 0u, 0u);
+      ra[j][1] = oka ? __ldcs(reinterpret_cast<const uint4*>(pa + 32 + 8 * qd)) : make_uint4(0u, 0u, 0u, 0u);
+      rb[j][0] = okb ? __ldcs(reinterpret_cast<const uint4*>(pb + 8 * qd)) : make_uint4(0u, 0u, 0u, 0u);
+      rb[j][1] = okb ? __ldcs(reinterpret_cast<const uint4*>(pb + 32 + 8 * qd)) : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      uint2 va = make_uint2(0u, 0u), vb = make_uint2(0u, 0u);
-      if (ta < S) va = *reinterpret_cast<const uint2*>(krow(ta) + 16 * t + 4 * qd);
-      if (tb < S) vb = *reinterpret_cast<const uint2*>(krow(tb) + 16 * t + 4 * qd);
-      mma_bf16_16816(c, va.x, vb.x, va.y, vb.y, bq[t][0], bq[t][1]);
+    for (int j = 0; j < kSdIdxBatch; ++j) {
+      const int tile = tb + j * kSdIdxWarps;
+      if (tile >= t1) break;  // warp-uniform
+      float cc[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_bf16_16816(cc, ra[j][0].x, rb[j][0].x, ra[j][0].y, rb[j][0].y, bq[0][0], bq[0][1]);
+      mma_bf16_16816(cc, ra[j][0].z, rb[j][0].z, ra[j][0].w, rb[j][0].w, bq[1][0], bq[1][1]);
+      mma_bf16_16816(cc, ra[j][1].x, rb[j][1].x, ra[j][1].y, rb[j][1].y, bq[2][0], bq[2][1]);
+      mma_bf16_16816(cc, ra[j][1].z, rb[j][1].z, ra[j][1].w, rb[j][1].w, bq[3][0], bq[3][1]);
+      float ia = w0 * fmaxf(cc[0], 0.f) + w1 * fmaxf(cc[1], 0.f);
+      float ib = w0 * fmaxf(cc[2], 0.f) + w1 * fmaxf(cc[3], 0.f);
+      ia += __shfl_xor_sync(0xffffffffu, ia, 1);
+      ia += __shfl_xor_sync(0xffffffffu, ia, 2);
+      ib += __shfl_xor_sync(0xffffffffu, ib, 1);
+      ib += __shfl_xor_sync(0xffffffffu, ib, 2);
+      const int ta = tile * 16 + g, tbk = ta + 8;
+      if (qd == 0) {
+        if (ta < S) {
+          srow[ta] = ia;
+          atomicAdd(&s_hist[order_key(ia) >> (32 - kSdHistBits)], 1u);
+        }
+        if (tbk < S) {
+          srow[tbk] = ib;
+          atomicAdd(&s_hist[order_key(ib) >> (32 - kSdHistBits)], 1u);
+        }
+      }
     }
-    float ia = w0 * fmaxf(c[0], 0.f) + w1 * fmaxf(c[1], 0.f);
-    float ib = w0 * fmaxf(c[2], 0.f) + w1 * fmaxf(c[3], 0.f);
-    ia += __shfl_xor_sync(0xffffffffu, ia, 1);
-    ia += __shfl_xor_sync(0xffffffffu, ia, 2);
-    ib += __shfl_xor_sync(0xffffffffu, ib, 1);
-    ib += __shfl_xor_sync(0xffffffffu, ib, 2);
-    if (qd == 0) {
-      if (ta < S) srow[ta] = ia;
-      if (tb < S) srow[tb] = ib;
-    }
+  }
+  __syncthreads();
+  uint32_t* ghist = P.hist + size_t(b) * kSdHistBins;
+  for (int i = tid; i < kSdHistBins; i += blockDim.x) {
+    const uint32_t h = s_hist[i];
+    if (h) atomicAdd(ghist + i, h);
   }
 }
 
 // ---------------------------------------------------------------------------
-// First stage (top_k < kSdChunk): the top_k of every chunk of kSdChunk
-// positions (the whole chunk when it is shorter), keys and positions in
-// position order.  Every chunk but a row's last holds exactly top_k
-// candidates, so a row's candidates are contiguous.
-__global__ void __launch_bounds__(kRkThreads) sd_topk_chunk_kernel(const SdParams P) {
-  extern __shared__ __align__(16) uint8_t tk_smem[];
-  RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
+// Selection.
+static_assert(kRkUpMax >= kSdSelSlice && kRkUpMax >= kSdCandCap, "slice keys and candidates fit in ukey");
+static_assert(kSdCandCap <= 256 * 32, "the kept positions are staged in lhist");
+struct SdSelSmem {
+  RowTopkSmem rk;                      // ukey: the slice's keys, then the row's candidate keys; lhist:
+                                       // radix select of the last bits; all of it: the whole-row fallback
+  int32_t cpos[kSdCandCap];            // the row's candidates in position order: positions
+  int32_t crow[kSdCandCap];            // and pool rows for kv head 0
+  uint32_t pref[kSdMaxSlices + 1];     // candidate offset of each slice
+  uint32_t fin[256];                   // keys of the final sub-bin (their last 8 bits decide)
+  int bstar, last, sub, ovf;
+  uint32_t above, sub_above, nfin, m, T, need_eq;
+};
+
+// The bin holding the kk-th largest of 4096 counts, scanned from the top: thread t holds the
+// counts of bins 4095-4t .. 4092-4t in h[0..3].  Writes the bin and the count above it to *bin /
+// *above (left alone if the counts hold fewer than kk).  1024 threads.
+__device__ __forceinline__ void sd_find_bin(const uint32_t (&h)[4], uint32_t kk, uint32_t* scan_tmp, int* bin,
+                                            uint32_t* above_out) {
+  const int tid = threadIdx.x;
+  const uint32_t v = h[0] + h[1] + h[2] + h[3];
+  uint32_t total;
+  const uint32_t above = rk_block_excl_scan(v, scan_tmp, total);
+  if (above < kk && kk <= above + v) {
+    uint32_t run = above;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (run + h[e] >= kk) {
+        *bin = kSdHistBins - 1 - 4 * tid - e;
+        *above_out = run;
+        break;
+      }
+      run += h[e];
+    }
+  }
+  __syncthreads();
+}
+__device__ __forceinline__ void sd_load_bins(const uint32_t* hist, uint32_t (&h)[4]) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) h[e] = __ldcg(hist + (kSdHistBins - 1 - 4 * int(threadIdx.x) - e));
+}
+
+// Per row: every CTA scans a slice of 16K positions, finds from the indexer's
+// histogram the bin of the k-th largest score, writes the slice's positions
+// in or above that bin (in position order, with their pool rows) to the
+// slice's own candidate run, and counts the threshold bin's keys by their
+// next 12 bits.  The row's last CTA then knows the sub-bin of the k-th key;
+// only the few keys of that sub-bin need their last 8 bits.  It reads the
+// candidate runs back in position order, so one block scan gives every kept
+// position its place in the ascending output.
+__global__ void __launch_bounds__(kSdSelThreads) sd_select_kernel(const SdParams P) {
+  extern __shared__ __align__(16) uint8_t sel_smem_raw[];
+  SdSelSmem& sm = *reinterpret_cast<SdSelSmem*>(sel_smem_raw);
   const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  asm volatile("griddepcontrol.wait;" ::: "memory");               // scores and histogram are complete
+  // The attention may launch once every CTA of this grid has exited or reached the trigger below,
+  // which only each row's final CTA does: by then the slice CTAs have left their SMs, so the
+  // attention's clusters (eight CTAs in one GPC each) all find room.
   int S;
   if (!sd_len_ok(P, b, S)) return;
-  const int p0 = c * kSdChunk;
-  const int n = max(0, min(kSdChunk, S - p0));
-  if (n == 0 || S <= P.top_k) return;
-  const int kc = min(P.top_k, n);
-  const float* srow = P.scores + size_t(b) * P.max_len + p0;
-  uint32_t* ckey = P.cand_key + (size_t(b) * P.nchunks + c) * P.top_k;
-  int32_t* cpos = P.cand_pos + (size_t(b) * P.nchunks + c) * P.top_k;
-  auto put = [&](int i, int rel) {
-    ckey[i] = order_key(__ldcg(srow + rel));
-    cpos[i] = p0 + rel;
+  const int k = min(P.top_k, S);
+  int32_t* sel = P.sel + size_t(b) * P.top_k;
+  int32_t* tko = P.topk_out ? P.topk_out + size_t(b) * P.top_k : nullptr;
+  int32_t* srow_out = P.sel_row + size_t(b) * P.top_k;
+  const int32_t* bt = P.block_table + size_t(b) * P.max_pages;
+  uint32_t* ghist = P.hist + size_t(b) * kSdHistBins;
+  uint32_t* gsub = P.subhist + size_t(b) * kSdHistBins;
+  // a position's pool row for kv head 0 (every kv head adds kvh * 16), given its page's entry
+  auto pool_row = [&](int pos, int phys) {
+    if (unsigned(phys) >= unsigned(P.num_pages)) {
+      report(P.status, KVSEL_ERR_BAD_INDEX);
+      phys = 0;
+    }
+    return phys * P.Hkv * kSdPage + (pos & (kSdPage - 1));
   };
-  if (kc == n) {
-    for (int i = tid; i < n; i += kRkThreads) put(i, i);
+  auto put = [&](int i, int pos) {
+    sel[i] = pos;
+    srow_out[i] = pool_row(pos, bt[pos / kSdPage]);
+    if (tko) tko[i] = pos;
+  };
+  auto finish_row = [&]() {  // the row's histograms and counter back to zero, the count out
+    for (int i = tid; i < kSdHistBins; i += kSdSelThreads) {
+      ghist[i] = 0u;
+      gsub[i] = 0u;
+    }
+    if (tko)
+      for (int i = k + tid; i < P.top_k; i += kSdSelThreads) tko[i] = -1;
+    if (tid == 0) {
+      P.nsel[b] = k;
+      P.row_done[b] = 0u;
+    }
+  };
+  if (k == S) {  // every position is selected: one CTA of the row writes them
+    if (c != 0) return;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int i = tid; i < S; i += kSdSelThreads) put(i, i);
+    finish_row();
     return;
   }
-  const F32RowKeys src{srow, 0, n, (reinterpret_cast<uintptr_t>(srow) & 15u) == 0};
-  row_topk<kSdTopkGroups>(src, kc, 0u, sm, put);
-}
-
-// Second stage: the top_k of a row over its chunk candidates, ascending.
-__global__ void __launch_bounds__(kRkThreads) sd_topk_final_kernel(const SdParams P) {
-  extern __shared__ __align__(16) uint8_t tk_smem[];
-  RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
-  const int b = blockIdx.x, tid = threadIdx.x;
-  int S;
-  if (!sd_len_ok(P, b, S)) return;
-  const int k = min(P.top_k, S);
-  int32_t* sel = P.sel + size_t(b) * P.top_k;
-  int32_t* tko = P.topk_out ? P.topk_out + size_t(b) * P.top_k : nullptr;
-  int32_t* spage = P.sel_page + size_t(b) * P.top_k;
-  const int32_t* bt = P.block_table + size_t(b) * P.max_pages;
-  auto put = [&](int i, int pos) {
-    sel[i] = pos;
-    spage[i] = bt[pos / kSdPage];  // resolved once here for every kv head's gather
-    if (tko) tko[i] = pos;
-  };
-  if (k == S) {
-    for (int i = tid; i < S; i += kRkThreads) put(i, i);
-  } else {
-    const int nch = (S + kSdChunk - 1) / kSdChunk;
-    const int m = (nch - 1) * P.top_k + min(P.top_k, S - (nch - 1) * kSdChunk);
-    const uint32_t* ck = P.cand_key + size_t(b) * P.nchunks * P.top_k;
-    const int32_t* cp = P.cand_pos + size_t(b) * P.nchunks * P.top_k;
-    const U32RowKeys src{ck, 0, m, (reinterpret_cast<uintptr_t>(ck) & 15u) == 0};
-    row_topk<kSdTopkGroups>(src, k, 0u, sm, [&](int i, int rel) { put(i, __ldcg(cp + rel)); });
+  // this CTA's slice: 16 consecutive positions per thread -- one page -- with the histogram bins,
+  // the scores and the page's block-table entry all loaded before anything is used; the keys are
+  // kept in shared memory (key 0 past the length)
+  const int pt = c * kSdSelSlice + 16 * tid;
+  uint4* mykeys = reinterpret_cast<uint4*>(sm.rk.ukey + 16 * tid);
+  uint32_t h[4];
+  sd_load_bins(ghist, h);
+  const int phys0 = pt < S ? bt[pt / kSdPage] : 0;
+  {
+    const float* srow = P.scores + size_t(b) * P.max_len;
+    if (P.scores_vec && pt + 15 < S) {
+      float4 v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = __ldcg(reinterpret_cast<const float4*>(srow + pt) + e);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        mykeys[e] = make_uint4(order_key(v[e].x), order_key(v[e].y), order_key(v[e].z), order_key(v[e].w));
+    } else {
+      uint32_t kk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) kk[e] = pt + e < S ? order_key(__ldcg(srow + pt + e)) : 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mykeys[e] = make_uint4(kk[4 * e], kk[4 * e + 1], kk[4 * e + 2], kk[4 * e + 3]);
+    }
   }
-  if (tko)
-    for (int i = k + tid; i < P.top_k; i += kRkThreads) tko[i] = -1;
-  if (tid == 0) P.nsel[b] = k;
-}
-
-// ---------------------------------------------------------------------------
-// Single stage (top_k >= kSdChunk): top-k positions of every row by indexer score (ties to the lower position),
-// ascending; every position when S <= top_k.  Also the -1-padded copy for the
-// caller.
-__global__ void __launch_bounds__(kRkThreads) sd_topk_kernel(const SdParams P) {
-  extern __shared__ __align__(16) uint8_t tk_smem[];
-  RowTopkSmem& sm = *reinterpret_cast<RowTopkSmem*>(tk_smem);
-  const int b = blockIdx.x, tid = threadIdx.x;
-  int S;
-  if (!sd_len_ok(P, b, S)) return;
-  const int k = min(P.top_k, S);
-  int32_t* sel = P.sel + size_t(b) * P.top_k;
-  int32_t* tko = P.topk_out ? P.topk_out + size_t(b) * P.top_k : nullptr;
-  int32_t* spage = P.sel_page + size_t(b) * P.top_k;
-  const int32_t* bt = P.block_table + size_t(b) * P.max_pages;
-  auto put = [&](int i, int pos) {
-    sel[i] = pos;
-    spage[i] = bt[pos / kSdPage];  // resolved once here for every kv head's gather
-    if (tko) tko[i] = pos;
-  };
-  if (k == S) {
-    for (int i = tid; i < S; i += kRkThreads) put(i, i);
+  // the bin holding the k-th largest score (bin 0, every position a candidate, if the counts are short)
+  if (tid == 0) {
+    sm.bstar = 0;
+    sm.above = 0u;
+  }
+  sd_find_bin(h, uint32_t(k), sm.rk.wtot[0], &sm.bstar, &sm.above);
+  const uint32_t lo_key = uint32_t(sm.bstar) << (32 - kSdHistBits);
+  const uint32_t bin_hi = (uint32_t(sm.bstar) + 1u) << (32 - kSdHistBits);  // 0 for the top bin
+  // candidates (in or above the bin) to this slice's run, in position order; the bin's own keys
+  // counted by their next 12 bits
+  {
+    uint32_t mine = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = mykeys[q];
+      const uint32_t kq[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool cand = kq[e] >= lo_key && kq[e] != 0u;  // key 0: past the length
+        mine += cand ? 1u : 0u;
+        if (cand && (bin_hi == 0u || kq[e] < bin_hi)) atomicAdd(gsub + ((kq[e] >> 8) & (kSdHistBins - 1)), 1u);
+      }
+    }
+    uint32_t total;
+    uint32_t at = rk_block_excl_scan(mine, sm.rk.wtot[0], total);
+    const size_t run = (size_t(b) * P.slices + c) * kSdSliceCap;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = mykeys[q];
+      const uint32_t kq[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (kq[e] >= lo_key && kq[e] != 0u) {
+          if (at < uint32_t(kSdSliceCap)) {
+            const int pos = pt + 4 * q + e;
+            P.cand_key[run + at] = kq[e];
+            P.cand_pos[run + at] = pos;
+            P.cand_row[run + at] = pool_row(pos, phys0);
+          }
+          ++at;
+        }
+    }
+    if (tid == 0) P.cand_cnt[size_t(b) * P.slices + c] = total;
+  }
+  // the last CTA of the row to finish selects
+  __syncthreads();
+  if (tid == 0) {  // release this CTA's candidates; the last arrival acquires everyone's
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(prev) : "l"(P.row_done + b) : "memory");
+    sm.last = prev + 1u == gridDim.x;
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // slice offsets and the total (overflow: a slice with more than its capacity), and the sub-bin
+  // holding the (k - above)-th best key of the bin; both sets of counts loaded together
+  {
+    const bool in = tid < P.slices && P.slices <= kSdMaxSlices;
+    const uint32_t n = in ? __ldcg(P.cand_cnt + size_t(b) * P.slices + tid) : 0u;
+    uint32_t hs[4];
+    sd_load_bins(gsub, hs);
+    if (tid == 0) {
+      sm.ovf = P.slices > kSdMaxSlices;
+      sm.sub = 0;
+      sm.sub_above = 0u;
+      sm.nfin = 0u;
+    }
+    __syncthreads();
+    if (n > uint32_t(kSdSliceCap)) sm.ovf = 1;
+    uint32_t total;
+    const uint32_t off = rk_block_excl_scan(n, sm.rk.wtot[0], total);
+    if (in) sm.pref[tid] = off;
+    if (tid == 0) {
+      sm.pref[min(P.slices, kSdMaxSlices)] = total;
+      sm.m = total;
+    }
+    sd_find_bin(hs, uint32_t(k) - sm.above, sm.rk.wtot[0], &sm.sub, &sm.sub_above);
+  }
+  const uint32_t kt = uint32_t(k) - sm.above;  // 1 <= kt <= the bin's count
+  const uint32_t m = sm.m;
+  if (!sm.ovf && m >= uint32_t(k) && m <= uint32_t(kSdCandCap)) {
+    // thread t takes the candidates [t*m/1024, (t+1)*m/1024) in position order: keys to shared
+    // memory, the keys of the final sub-bin (they decide by their last 8 bits) to a short list
+    constexpr int kPer = kSdCandCap / kSdSelThreads;
+    const uint32_t i0 = uint32_t((uint64_t(tid) * m) / kSdSelThreads);
+    const uint32_t i1 = uint32_t((uint64_t(tid + 1) * m) / kSdSelThreads);
+    const uint32_t p24 = (lo_key >> 8) | uint32_t(sm.sub);
+    {
+      uint32_t kk[kPer];
+      int pp[kPer], rr[kPer];
+      int sl = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {  // key, position and pool row, all loads issued together
+        const uint32_t i = i0 + j;
+        kk[j] = 0u;
+        pp[j] = rr[j] = 0;
+        if (i < i1) {
+          while (sm.pref[sl + 1] <= i) ++sl;  // slices holding no candidate are stepped over
+          const size_t src = (size_t(b) * P.slices + sl) * kSdSliceCap + (i - sm.pref[sl]);
+          kk[j] = __ldcg(P.cand_key + src);
+          pp[j] = __ldcg(P.cand_pos + src);
+          rr[j] = __ldcg(P.cand_row + src);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        if (i0 + j >= i1) break;
+        sm.rk.ukey[i0 + j] = kk[j];
+        sm.cpos[i0 + j] = pp[j];
+        sm.crow[i0 + j] = rr[j];
+        if ((kk[j] >> 8) == p24) {
+          const uint32_t at = atomicAdd(&sm.nfin, 1u);
+          if (at < 256u) sm.fin[at] = kk[j];
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t nf = sm.nfin;
+    const uint32_t kf = kt - sm.sub_above;  // 1 <= kf <= nf
+    if (nf <= 256u) {  // ranked directly
+      if (uint32_t(tid) < nf) {
+        const uint32_t f = sm.fin[tid];
+        uint32_t gt = 0, eq = 0;
+        for (uint32_t x = 0; x < nf; ++x) {
+          gt += sm.fin[x] > f;
+          eq += sm.fin[x] == f;
+        }
+        if (gt < kf && kf <= gt + eq) {  // every thread holding this key writes the same values
+          sm.T = f;
+          sm.need_eq = kf - gt;
+        }
+      }
+    } else {
+      uint32_t T, need_eq;
+      rk_radix(
+          [&](auto&& f) {
+            for (int j = 0; j < kPer; ++j) {
+              const uint32_t i = i0 + j;
+              const uint32_t key = i < i1 ? sm.rk.ukey[i] : 0u;
+              const bool live = i < i1 && (key >> 8) == p24;
+              f(live ? key : 0u, live);
+            }
+          },
+          7, p24 << 8, kf, sm.rk, T, need_eq);
+      if (tid == 0) {
+        sm.T = T;
+        sm.need_eq = need_eq;
+      }
+    }
+    __syncthreads();
+    const uint32_t T = sm.T, need_eq = sm.need_eq;
+    // kept: every key above T, and the first need_eq keys equal to it in position order
+    uint32_t ng = 0, ne = 0;
+    for (uint32_t i = i0; i < i1; ++i) {
+      const uint32_t key = sm.rk.ukey[i];
+      ng += key > T ? 1u : 0u;
+      ne += key == T ? 1u : 0u;
+    }
+    uint32_t tot;
+    const uint32_t ex = rk_block_excl_scan(ng | (ne << 16), sm.rk.wtot[0], tot);
+    uint32_t g_before = ex & 0xFFFFu, e_before = ex >> 16;
+    for (uint32_t i = i0; i < i1; ++i) {
+      const uint32_t key = sm.rk.ukey[i];
+      const bool gt = key > T, eq = key == T;
+      if (gt || (eq && e_before < need_eq)) {
+        const uint32_t o = g_before + min(e_before, need_eq);
+        if (o < uint32_t(k)) {
+          sel[o] = sm.cpos[i];
+          srow_out[o] = sm.crow[i];
+          if (tko) tko[o] = sm.cpos[i];
+        }
+      }
+      g_before += gt;
+      e_before += eq;
+    }
   } else {
+    // more candidates than fit (or a very long row): exact top-k over the whole row
     const float* srow = P.scores + size_t(b) * P.max_len;
     const F32RowKeys src{srow, 0, S, (reinterpret_cast<uintptr_t>(srow) & 15u) == 0};
-    row_topk<kSdTopkGroups>(src, k, 0u, sm, put);
+    row_topk<kSdTopkGroups>(src, k, lo_key, sm.rk, put);
   }
-  if (tko)
-    for (int i = k + tid; i < P.top_k; i += kRkThreads) tko[i] = -1;
-  if (tid == 0) P.nsel[b] = k;
+  __syncthreads();
+  finish_row();
 }
 
 // ---------------------------------------------------------------------------
+// Thread-block cluster helpers: the splits of one (sequence, kv head) form a
+// cluster and merge their partial results through distributed shared memory.
+__device__ __forceinline__ void sd_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared variable in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t sd_cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float sd_cluster_ld(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  float* wo = reinterpret_cast<float*>(smem + kSdAttnWarps * 2 * 8192);  // [4][8][130]
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  __shared__ __align__(16) float s_part[kSdPartFloats];  // this split's (M, L, O) of the pair
+  __shared__ float s_f[kSdMaxClusterSplits][kSdMaxG];    // each split's max per head, then its merge weight
+  __shared__ float s_l[kSdMaxClusterSplits][kSdMaxG];    // each split's sum per head
+  float* wo = reinterpret_cast<float*>(smem);  // [4][8][130] merge scratch, over the rings once they are idle
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;  // split = the CTA's rank in its cluster
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int S;
-  if (!sd_len_ok(P, b, S)) return;
-  const int nsel = P.nsel[b];
-  const int tiles = (nsel + 15) / 16;
-  const int t0 = int((long long)split * tiles / P.splits), t1 = int((long long)(split + 1) * tiles / P.splits);
   const int G = P.G, g = lane >> 2, qd = lane & 3;
   const bool head_ok = g < G;
-  const int32_t* sel = P.sel + size_t(b) * P.top_k;
-  const int32_t* spg = P.sel_page + size_t(b) * P.top_k;
-  const uint32_t wbuf = smem_u32(smem + warp * 2 * 8192);
-
+  // the q rows and the length are inputs: read while the select finishes (the select writes neither)
   uint32_t qa[8][2];
   load_q_frags(P.q + (size_t(b) * P.Hq + kvh * G + (head_ok ? g : 0)) * kSdD, head_ok, qd, qa);
+  int S;
+  if (!sd_len_ok(P, b, S)) return;  // the whole cluster (one sequence) leaves together
+  const int nsel = min(P.top_k, S);
+  const int tiles = (nsel + 15) / 16;
+  const int t0 = int((long long)split * tiles / P.splits), t1 = int((long long)(split + 1) * tiles / P.splits);
+  const int32_t* srow = P.sel_row + size_t(b) * P.top_k;
+  const uint32_t wbuf = smem_u32(smem + warp * kSdAttnStages * 8192);
+  const int tw0 = t0 + warp;  // this warp's tiles: tw0, tw0 + 4, ... (ordinal j = 0, 1, ...)
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the selection is complete
+
   TileState st;
   st.init();
 
-  // gather tile t into stage s: 16 rows of K then 16 of V, 16 x 16-byte units each
-  auto gather = [&](int t, int s) {
+  // Pool rows of this warp's tiles j0 .. j0+3, two per lane (lane l: tile j0 + l/16 and
+  // j0 + 2 + l/16, key l % 16), all loads issued together; -1 past the selection.
+  int ro[2];
+  auto load_rows = [&](int j0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int tt = tw0 + (j0 + 2 * h + (lane >> 4)) * kSdAttnWarps;
+      const int tok = tt * 16 + (lane & 15);
+      ro[h] = (tt < t1 && tok < nsel) ? __ldcg(srow + tok) : -1;
+    }
+  };
+  // gather tile ordinal j into stage s: 16 rows of K then 16 of V, 16 x 16-byte units each; the
+  // rows' pool positions come from the lanes that loaded them, by shuffles
+  auto gather = [&](int j, int s) {
+    if ((j & 3) == 0) load_rows(j);
+    const int jj = j & 3;
+    const int mine = (jj >> 1) ? ro[1] : ro[0];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int c = lane + 32 * i;
       const int row = c >> 4, u = c & 15;  // row 0..31: K rows 0..15, then V rows
       const int r16 = row & 15;
-      const int tok = t * 16 + r16;
-      const bool valid = tok < nsel;
-      const int posi = valid ? sel[tok] : 0;
-      int phys = valid ? spg[tok] : 0;
-      if (valid && unsigned(phys) >= unsigned(P.num_pages)) {
-        report(P.status, KVSEL_ERR_BAD_INDEX);
-        phys = 0;
-      }
-      const __nv_bfloat16* pool = row < 16 ? P.k_pool : P.v_pool;
-      const __nv_bfloat16* src =
-          pool + ((size_t(phys) * P.Hkv + kvh) * kSdPage + (posi % kSdPage)) * kSdD + u * 8;
+      const int r = __shfl_sync(0xffffffffu, mine, (jj & 1) * 16 + r16);
+      const bool valid = r >= 0;
+      const size_t prow = size_t(valid ? r : 0) + size_t(kvh) * kSdPage;
+      const __nv_bfloat16* src = (row < 16 ? P.k_pool : P.v_pool) + prow * kSdD + u * 8;
       const uint32_t dst = wbuf + s * 8192 + (row < 16 ? 0 : 4096) + tile_unit_off(r16, u);
       cp_async16(dst, src, valid);
     }
     cp_async_commit();
   };
 
-  int t = t0 + warp;
-  if (t < t1) gather(t, 0);
-  int s = 0;
+  // the first kSdAttnStages tiles gathered at once, then one more each time one is consumed (one
+  // commit group per tile slot, empty past the end, so the wait below always leaves the newer
+  // kSdAttnStages - 1 groups in flight)
+#pragma unroll
+  for (int j = 0; j < kSdAttnStages; ++j) {
+    if (tw0 + j * kSdAttnWarps < t1) gather(j, j);
+    else cp_async_commit();
+  }
+  int s = 0, j = 0;
 #pragma unroll 1
-  for (; t < t1; t += kSdAttnWarps) {
-    const int tn = t + kSdAttnWarps;
-    if (tn < t1) {
-      gather(tn, s ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+  for (int t = tw0; t < t1; t += kSdAttnWarps, ++j) {
+    cp_async_wait<kSdAttnStages - 1>();
     __syncwarp();
     float x0, x1, x2, x3;
     const int valid = min(16, nsel - t * 16);
     attend_tile(wbuf + s * 8192, wbuf + s * 8192 + 4096, qa, valid, P.scale_log2, st, x0, x1, x2, x3);
     __syncwarp();
-    s ^= 1;
+    if (t + kSdAttnStages * kSdAttnWarps < t1) gather(j + kSdAttnStages, s);
+    else cp_async_commit();
+    s = s + 1 == kSdAttnStages ? 0 : s + 1;
   }
-  float* slot = P.part + ((size_t(b) * P.Hkv + kvh) * P.splits + split) * kSdPartFloats;
-  merge_warps_to_slot<kSdAttnWarps>(st, wo, slot, G);
-  // The last split of (sequence, kv head) to finish merges all of them into O;
-  // the last kv head of a sequence to be merged publishes its length.
-  __shared__ int s_last;
+  cp_async_wait<0>();
+  // the next step's indexer may launch now: it waits for this grid before touching anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __syncthreads();  // every warp is done with its ring: the merge scratch may overwrite it
+  merge_warps_to_slot<kSdAttnWarps>(st, wo, s_part, G);
+  sd_cluster_sync();  // every split's partial is in its shared memory
+  // merge weights: every split's (max, sum) per head fetched at once, then combined per head
+  const int ns = P.splits;
+  if (tid < ns * G) {
+    const int sp = tid / G, gg = tid % G;
+    s_f[sp][gg] = sd_cluster_ld(sd_cluster_addr(&s_part[gg], sp));
+    s_l[sp][gg] = sd_cluster_ld(sd_cluster_addr(&s_part[kSdMaxG + gg], sp));
+  }
   __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const unsigned done = atomicAdd(P.merge_cnt + size_t(b) * P.Hkv + kvh, 1u) + 1u;
-    s_last = done == unsigned(P.splits);
-    if (s_last) {
-      P.merge_cnt[size_t(b) * P.Hkv + kvh] = 0u;  // every split has arrived: ready for the next call
-      __threadfence();
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, s_f[sp][tid]);
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int sp = 0; sp < ns; ++sp)
+        if (s_f[sp][tid] != -INFINITY) L += s_l[sp][tid] * exp2f(s_f[sp][tid] - M);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int sp = 0; sp < ns; ++sp) {
+      const float ms = s_f[sp][tid];
+      s_f[sp][tid] = (M != -INFINITY && ms != -INFINITY) ? exp2f(ms - M) * inv : 0.f;
     }
   }
   __syncthreads();
-  if (s_last) {
-    merge_split_slots(P.part + (size_t(b) * P.Hkv + kvh) * P.splits * kSdPartFloats, P.splits, G, P.out,
-                      P.out_f32 != 0, size_t(b) * P.Hq + size_t(kvh) * G, reinterpret_cast<float*>(smem));
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      if (atomicAdd(P.seq_cnt + b, 1u) + 1u == unsigned(P.Hkv)) {
-        P.seq_cnt[b] = 0u;
-        P.seq_lens[b] = S;  // every CTA of this sequence has read the old length
-      }
+  // this split's share of the pair's G x 128 outputs
+  const int E = G * kSdD;
+  const int e1 = (split + 1) * E / ns;
+  for (int idx = split * E / ns + tid; idx < e1; idx += kSdAttnWarps * 32) {
+    const int gg = idx / kSdD, dd = idx % kSdD;
+    float acc = 0.f;
+    for (int sp = 0; sp < ns; ++sp)
+      acc += s_f[sp][gg] * sd_cluster_ld(sd_cluster_addr(&s_part[2 * kSdMaxG + gg * kSdD + dd], sp));
+    const size_t oi = (size_t(b) * P.Hq + size_t(kvh) * G + gg) * kSdD + dd;
+    if (P.out_f32) static_cast<float*>(P.out)[oi] = acc;
+    else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(acc);
+  }
+  sd_cluster_sync();  // no CTA leaves while another still reads its partial
+  // the last (sequence, kv head) cluster of a sequence publishes its length: every CTA of the
+  // sequence has read the old one by then
+  if (split == 0 && tid == 0) {
+    __threadfence();
+    if (atomicAdd(P.seq_cnt + b, 1u) + 1u == unsigned(P.Hkv)) {
+      P.seq_cnt[b] = 0u;
+      P.seq_lens[b] = S;
     }
   }
 }
@@ -364,12 +700,10 @@ using namespace kvsel_host;
 
 namespace {
 struct SdWs {
-  size_t scores, ckey, cpos, sel, spage, nsel, cnt, part, total;
-  int nchunks;  // 0: single-stage top-k
+  size_t scores, hist, cnt, ckey, cpos, crow, sel, srow, nsel, total;
 };
-SdWs sd_ws_layout(int batch, int Hkv, int max_len, int top_k, bool own_scores) {
+SdWs sd_ws_layout(int batch, int max_len, int top_k, bool own_scores) {
   SdWs w;
-  w.nchunks = top_k < kSdChunk ? (max_len + kSdChunk - 1) / kSdChunk : 0;
   size_t off = kStatusBytes;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -377,13 +711,15 @@ SdWs sd_ws_layout(int batch, int Hkv, int max_len, int top_k, bool own_scores) {
     return o;
   };
   w.scores = own_scores ? take(size_t(batch) * max_len * 4) : 0;
-  w.ckey = take(size_t(batch) * w.nchunks * top_k * 4);
-  w.cpos = take(size_t(batch) * w.nchunks * top_k * 4);
+  const size_t slices = size_t((max_len + kSdSelSlice - 1) / kSdSelSlice);
+  w.hist = take(size_t(batch) * kSdHistBins * 4 * 2);        // the indexer's histogram, then the sub-bins
+  w.cnt = take(size_t(batch) * (slices + 2) * 4);            // per-slice candidates, CTAs done, kv heads merged
+  w.ckey = take(size_t(batch) * slices * kSdSliceCap * 4);
+  w.cpos = take(size_t(batch) * slices * kSdSliceCap * 4);
+  w.crow = take(size_t(batch) * slices * kSdSliceCap * 4);
   w.sel = take(size_t(batch) * top_k * 4);
-  w.spage = take(size_t(batch) * top_k * 4);
-  w.cnt = take((size_t(batch) * Hkv + batch) * 4);
+  w.srow = take(size_t(batch) * top_k * 4);
   w.nsel = take(size_t(batch) * 4);
-  w.part = take(size_t(batch) * Hkv * kSdMaxSplits * kSdPartFloats * 4);
   w.total = off;
   return w;
 }
@@ -392,7 +728,7 @@ SdWs sd_ws_layout(int batch, int Hkv, int max_len, int top_k, bool own_scores) {
 extern "C" size_t kvsel_sparse_decode_workspace(const kvsel_paged_kv* kv, int batch, int max_len,
                                                 int top_k, int with_scores_out) {
   if (!kv || batch < 1 || max_len < 1 || top_k < 1 || kv->num_kv_heads < 1) return 0;
-  return sd_ws_layout(batch, kv->num_kv_heads, max_len, top_k, with_scores_out == 0).total;
+  return sd_ws_layout(batch, max_len, top_k, with_scores_out == 0).total;
 }
 
 extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int32_t* block_table,
@@ -422,8 +758,10 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
     return fail(KVSEL_ERR_INVALID_ARG, fn + "k_new, v_new and idx_k_new must all be given or all NULL");
   if (out_dtype != KVSEL_BF16 && out_dtype != KVSEL_F32)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "out_dtype must be KVSEL_BF16 or KVSEL_F32");
-  const SdWs L = sd_ws_layout(batch, Hkv, max_len, top_k, scores_out == nullptr);
+  const SdWs L = sd_ws_layout(batch, max_len, top_k, scores_out == nullptr);
   if (max_len > kSdMaxLen) return fail(KVSEL_ERR_UNSUPPORTED, fn + "max_len must be <= 2^28");
+  if ((long long)kv->num_pages * Hkv * kSdPage >= (1LL << 31))
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "num_pages * num_kv_heads * 16 must be below 2^31");
   if (!aligned(kv->k_pool, 16) || !aligned(kv->v_pool, 16) || !aligned(q, 16) || !aligned(idx_k, 16) ||
       !aligned(idx_q, 8) || (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(idx_k_new, 16))))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "pools, q, k_new, v_new, idx_k, idx_k_new must be 16-byte aligned");
@@ -433,10 +771,13 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
     return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace too small: need " + std::to_string(L.total));
 
   const int sms = sm_count();
+  // indexer: two CTAs per SM over the whole batch, each a contiguous run of one row's tiles
+  const int idx_ctas = std::max(1, (2 * sms + batch - 1) / batch);
+  // attention: one wave at two CTAs per SM
   const int tiles_max = (std::min(top_k, max_len) + 15) / 16;
-  int splits = std::max(1, (sms * 4) / (batch * Hkv));
-  splits = std::min(splits, std::max(1, (tiles_max + 7) / 8));
-  splits = std::min(splits, kSdMaxSplits);
+  int splits = std::max(1, (2 * sms) / (batch * Hkv));
+  splits = std::min(splits, std::max(1, (tiles_max + 3) / 4));
+  splits = std::min(splits, kSdMaxClusterSplits);
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   SdParams P;
@@ -452,16 +793,20 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   P.idx_k = static_cast<__nv_bfloat16*>(idx_k);
   P.idx_k_new = static_cast<const __nv_bfloat16*>(idx_k_new);
   P.scores = scores_out ? scores_out : reinterpret_cast<float*>(ws + L.scores);
+  const int slices = (max_len + kSdSelSlice - 1) / kSdSelSlice;
+  P.hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  P.subhist = P.hist + size_t(batch) * kSdHistBins;
+  P.cand_cnt = reinterpret_cast<unsigned*>(ws + L.cnt);
+  P.row_done = P.cand_cnt + size_t(batch) * slices;
+  P.seq_cnt = P.row_done + batch;
+  P.slices = slices;
   P.cand_key = reinterpret_cast<uint32_t*>(ws + L.ckey);
   P.cand_pos = reinterpret_cast<int32_t*>(ws + L.cpos);
-  P.nchunks = L.nchunks;
+  P.cand_row = reinterpret_cast<int32_t*>(ws + L.crow);
   P.sel = reinterpret_cast<int32_t*>(ws + L.sel);
-  P.sel_page = reinterpret_cast<int32_t*>(ws + L.spage);
-  P.merge_cnt = reinterpret_cast<unsigned*>(ws + L.cnt);
-  P.seq_cnt = P.merge_cnt + size_t(batch) * Hkv;
+  P.sel_row = reinterpret_cast<int32_t*>(ws + L.srow);
   P.nsel = reinterpret_cast<int32_t*>(ws + L.nsel);
   P.topk_out = topk_out;
-  P.part = reinterpret_cast<float*>(ws + L.part);
   P.out = out;
   P.status = reinterpret_cast<int*>(ws);
   P.B = batch;
@@ -473,6 +818,8 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   P.num_pages = kv->num_pages;
   P.max_len = max_len;
   P.top_k = top_k;
+  P.idx_ctas = idx_ctas;
+  P.scores_vec = (max_len % 4 == 0) && aligned(P.scores, 16);
   P.splits = splits;
   P.appended = k_new ? 1 : 0;
   P.out_f32 = out_dtype == KVSEL_F32;
@@ -481,27 +828,36 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   {
     cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(sd_attn_kernel), int(kSdAttnSmem));
-    for (const void* f : {reinterpret_cast<const void*>(sd_topk_kernel),
-                          reinterpret_cast<const void*>(sd_topk_chunk_kernel),
-                          reinterpret_cast<const void*>(sd_topk_final_kernel)})
-      if (e0 == cudaSuccess) e0 = smem_limit_once(f, int(sizeof(RowTopkSmem)));
+    if (e0 == cudaSuccess)
+      e0 = smem_limit_once(reinterpret_cast<const void*>(sd_select_kernel), int(sizeof(SdSelSmem)));
     if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_sparse_decode (attribute)");
   }
   cudaError_t e;
-#define KVSEL_SD_LAUNCH(name, kernel, grid, block, smem)                 \
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // the attention's splits of a pair: one cluster
+  attr[1].val.clusterDim.x = unsigned(splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.stream = st;
+  // Every kernel may launch while its predecessor runs (programmatic launch) and waits for it
+  // before reading its results; each predecessor lets the next one in as early as that is useful.
+#define KVSEL_SD_LAUNCH(name, kernel, grid, block, smem, nattr)          \
+  cfg.gridDim = grid;                                                    \
+  cfg.blockDim = dim3(block);                                            \
+  cfg.dynamicSmemBytes = smem;                                           \
+  cfg.attrs = nattr ? attr : nullptr;                                    \
+  cfg.numAttrs = nattr;                                                  \
   trace_before(name, st);                                                \
-  kernel<<<grid, block, smem, st>>>(P);                                  \
-  e = cudaGetLastError();                                                \
+  e = cudaLaunchKernelEx(&cfg, kernel, P);                               \
   trace_after(st);                                                       \
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_sparse_decode (" name ")");
-  KVSEL_SD_LAUNCH("sd_index", sd_index_kernel, dim3((max_len + 127) / 128, batch), 128, 0)
-  if (L.nchunks > 0) {
-    KVSEL_SD_LAUNCH("sd_topk_chunk", sd_topk_chunk_kernel, dim3(L.nchunks, batch), kRkThreads, sizeof(RowTopkSmem))
-    KVSEL_SD_LAUNCH("sd_topk_final", sd_topk_final_kernel, dim3(batch), kRkThreads, sizeof(RowTopkSmem))
-  } else {
-    KVSEL_SD_LAUNCH("sd_topk", sd_topk_kernel, dim3(batch), kRkThreads, sizeof(RowTopkSmem))
-  }
-  KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem)
+  KVSEL_SD_LAUNCH("sd_index", sd_index_kernel, dim3(idx_ctas, batch), kSdIdxWarps * 32, 0, 1)
+  KVSEL_SD_LAUNCH("sd_select", sd_select_kernel, dim3(slices, batch),
+                  kSdSelThreads, sizeof(SdSelSmem), 1)
+  KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem, 2)
 #undef KVSEL_SD_LAUNCH
   return KVSEL_OK;
 }

@@ -16,7 +16,7 @@ import torch
 
 import workloads
 from oracle import block_priority as BP
-from _harness import rel_l2
+from _harness import Guards, rel_l2
 
 import attention_guided_kv_gb300 as K
 
@@ -29,18 +29,20 @@ def _run(tok, offsets, bs, agg, norm, frac, inc=None, decay=1.0, top_p=0.1):
     R = len(offsets) - 1
     nblk = sum(int(-(-int(offsets[r + 1] - offsets[r]) // bs)) for r in range(R))
     maxb = max(nblk, 1)
-    t_tok = torch.from_numpy(np.asarray(tok, dtype=np.float32)).to(dev)
+    g = Guards()
+    t_tok = g.like(torch.from_numpy(np.asarray(tok, dtype=np.float32)).to(dev))
     t_inc = None if inc is None else torch.from_numpy(np.asarray(inc, dtype=np.float32)).to(dev)
     t_off = torch.from_numpy(np.asarray(offsets, dtype=np.int64)).to(dev)
-    bso = torch.full((maxb,), float("nan"), device=dev)
+    bso = g.new((maxb,), torch.float32, fill=float("nan"))
     cap = max(1, math.ceil(frac * maxb))
-    order = torch.full((cap,), -7, dtype=torch.int64, device=dev)
-    n_out = torch.zeros(2, dtype=torch.int64, device=dev)
-    ws = K.workspace(K.kvsel_block_priority_workspace(R, maxb))
+    order = g.new((cap,), torch.int64, fill=-7)
+    n_out = g.new((2,), torch.int64)
+    ws = g.new((K.kvsel_block_priority_workspace(R, maxb),), torch.uint8)
     K.kvsel_block_priority(t_tok, t_off, order, n_out, ws, block_size=bs, agg=agg, norm=norm,
                            evict_frac=frac, increment=t_inc, decay=decay, top_p=top_p,
                            block_score_out=bso, max_total_blocks=maxb)
     assert K.read_status(ws) == 0
+    g.check()
     n_ev, N = n_out.cpu().tolist()
     assert N == nblk
     return t_tok.cpu().numpy(), bso.cpu().numpy()[:nblk], order.cpu().numpy()[:n_ev], n_ev
@@ -174,13 +176,15 @@ def _run_ex(tok_dev, off, bs, agg, norm, frac, **kw):
     R = len(off) - 1
     nblk = sum(int(-(-int(off[r + 1] - off[r]) // bs)) for r in range(R))
     t_off = torch.from_numpy(np.asarray(off, dtype=np.int64)).to(dev)
-    bso = torch.full((nblk,), float("nan"), device=dev)
-    order = torch.full((max(1, math.ceil(frac * nblk)),), -7, dtype=torch.int64, device=dev)
-    n_out = torch.zeros(2, dtype=torch.int64, device=dev)
-    ws = K.workspace(K.kvsel_block_priority_workspace(R, nblk))
+    g = Guards()
+    bso = g.new((nblk,), torch.float32, fill=float("nan"))
+    order = g.new((max(1, math.ceil(frac * nblk)),), torch.int64, fill=-7)
+    n_out = g.new((2,), torch.int64)
+    ws = g.new((K.kvsel_block_priority_workspace(R, nblk),), torch.uint8)
     K.kvsel_block_priority(tok_dev, t_off, order, n_out, ws, block_size=bs, agg=agg, norm=norm,
                            evict_frac=frac, block_score_out=bso, max_total_blocks=nblk, **kw)
     assert K.read_status(ws) == 0
+    g.check()
     n_ev, N = n_out.cpu().tolist()
     assert N == nblk
     return bso.cpu().numpy(), order.cpu().numpy()[:n_ev]

@@ -18,7 +18,7 @@ import torch
 import workloads
 from oracle import dsa
 from oracle.attention import bf16_bits_to_f64, decode_attention
-from _harness import bf16, rel_l2
+from _harness import Guards, bf16, rel_l2
 
 import attention_guided_kv_gb300 as K
 
@@ -36,13 +36,15 @@ class QuestState:
         self.kpool = bf16(workloads.paged_pool(wl.K, wl.block_table, wl.num_pages))
         self.vpool = bf16(workloads.paged_pool(wl.V, wl.block_table, wl.num_pages))
         self.kv = K.paged_kv(self.kpool, self.vpool, wl.Hq)
-        self.bt = torch.from_numpy(wl.block_table).to(dev)
-        self.seq = torch.full((wl.B,), wl.S0, dtype=torch.int32, device=dev)
-        self.meta = torch.zeros(wl.num_pages, wl.Hkv, 2, wl.d, dtype=torch.bfloat16, device=dev)
-        self.out = torch.zeros(wl.B, wl.Hq, wl.d, device=dev, dtype=torch.float32 if out_f32 else torch.bfloat16)
-        self.pages = torch.full((wl.B, wl.Hq, budget), -7, dtype=torch.int32, device=dev)
-        self.bounds = torch.zeros(wl.B, wl.Hq, wl.max_pages, device=dev)
-        self.ws = K.workspace(K.kvsel_quest_decode_workspace(self.kv, wl.B, wl.max_pages, budget, True, True))
+        self.guards = g = Guards()
+        self.bt = g.like(torch.from_numpy(wl.block_table).to(dev))
+        self.seq = g.like(torch.full((wl.B,), wl.S0, dtype=torch.int32, device=dev))
+        self.meta = g.new((wl.num_pages, wl.Hkv, 2, wl.d), torch.bfloat16)
+        self.out = g.new((wl.B, wl.Hq, wl.d), torch.float32 if out_f32 else torch.bfloat16)
+        self.pages = g.new((wl.B, wl.Hq, budget), torch.int32, fill=-7)
+        self.bounds = g.new((wl.B, wl.Hq, wl.max_pages), torch.float32)
+        self.ws = g.new((K.kvsel_quest_decode_workspace(self.kv, wl.B, wl.max_pages, budget, True, True),),
+                        torch.uint8)
         K.kvsel_quest_page_meta(self.kv, self.bt, self.seq, self.meta, self.ws)
 
     def step(self, t, append=True):
@@ -53,6 +55,7 @@ class QuestState:
                              bounds_out=self.bounds)
         torch.cuda.synchronize()
         assert K.read_status(self.ws) == 0
+        self.guards.check()
 
 
 def _logical(wl, b, appended):

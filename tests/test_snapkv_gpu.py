@@ -12,7 +12,7 @@ import torch
 import workloads
 from oracle import snapkv
 from oracle.attention import bf16_bits_to_f64
-from _harness import bf16, rel_l2
+from _harness import Guards, bf16, rel_l2
 
 import attention_guided_kv_gb300 as K
 
@@ -39,9 +39,10 @@ class SnapState:
         self.bt = torch.from_numpy(bts).cuda()
         self.q = bf16(q)
         L = len(layers)
-        self.keep = torch.full((L, wl.Hkv, wl.keep_k + wl.W), -7, dtype=torch.int32, device="cuda")
-        self.vote = torch.zeros(L, wl.Hkv, max(wl.S - wl.W, 1), device="cuda")
-        self.ws = K.workspace(K.kvsel_snapkv_select_workspace(self.kv, L, wl.S, wl.W, True))
+        self.guards = g = Guards()
+        self.keep = g.new((L, wl.Hkv, wl.keep_k + wl.W), torch.int32, fill=-7)
+        self.vote = g.new((L, wl.Hkv, max(wl.S - wl.W, 1)), torch.float32)
+        self.ws = g.new((K.kvsel_snapkv_select_workspace(self.kv, L, wl.S, wl.W, True),), torch.uint8)
 
     def run(self):
         wl = self.wl
@@ -49,6 +50,7 @@ class SnapState:
                               keep_k=wl.keep_k, pool_kernel=wl.pool_kernel, vote_out=self.vote)
         torch.cuda.synchronize()
         assert K.read_status(self.ws) == 0
+        self.guards.check()
 
 
 def _check(st, layer_ids=None, kv_heads=None):
@@ -125,17 +127,19 @@ def _run_ex(st, mode, head_pad=5, layer_pad=3):
     cap = G * wl.keep_k + wl.W
     hs = cap + head_pad
     ls = wl.Hkv * hs + layer_pad
-    seed = torch.full((L * ls,), float("nan"), device="cuda")
-    keep = torch.full((L, wl.Hkv, cap), -7, dtype=torch.int32, device="cuda")
-    count = torch.full((L, wl.Hkv), -7, dtype=torch.int32, device="cuda")
+    g = Guards()
+    seed = g.new((L * ls,), torch.float32, fill=float("nan"))
+    keep = g.new((L, wl.Hkv, cap), torch.int32, fill=-7)
+    count = g.new((L, wl.Hkv), torch.int32, fill=-7)
     vrows = wl.Hq if mode == K.KVSEL_SNAP_HEAD_UNION else wl.Hkv
-    vote = torch.zeros(L, vrows, max(wl.S - wl.W, 1), device="cuda")
-    ws = K.workspace(K.kvsel_snapkv_select_ex_workspace(st.kv, L, wl.S, wl.W, True, mode))
+    vote = g.new((L, vrows, max(wl.S - wl.W, 1)), torch.float32)
+    ws = g.new((K.kvsel_snapkv_select_ex_workspace(st.kv, L, wl.S, wl.W, True, mode),), torch.uint8)
     K.kvsel_snapkv_select_ex(st.kv, st.bt, st.q, keep, ws, seq_len=wl.S, keep_k=wl.keep_k, mode=mode,
                              pool_kernel=wl.pool_kernel, vote_out=vote, keep_count=count, seed_out=seed,
                              seed_layer_stride=ls, seed_head_stride=hs)
     torch.cuda.synchronize()
     assert K.read_status(ws) == 0
+    g.check()
     seed = seed.cpu().numpy()
     rows = np.stack([np.stack([seed[l * ls + h * hs:l * ls + h * hs + cap] for h in range(wl.Hkv)])
                      for l in range(L)])

@@ -13,7 +13,7 @@ import torch
 import workloads
 from oracle import dsa
 from oracle.attention import bf16_bits_to_f64, decode_attention
-from _harness import bf16, rel_l2
+from _harness import Guards, bf16, rel_l2
 
 import attention_guided_kv_gb300 as K
 
@@ -33,11 +33,13 @@ class SparseState:
         idx = np.zeros((wl.B, wl.max_len, wl.Di), dtype=np.uint16)
         idx[:, :wl.S0] = wl.k_idx
         self.idx_k = bf16(idx)
-        self.out = torch.zeros(wl.B, wl.Hq, wl.d, device=dev,
-                               dtype=torch.float32 if out_f32 else torch.bfloat16)
-        self.topk = torch.zeros(wl.B, wl.top_k, dtype=torch.int32, device=dev)
-        self.scores = torch.zeros(wl.B, wl.max_len, device=dev)
-        self.ws = K.workspace(K.kvsel_sparse_decode_workspace(self.kv, wl.B, wl.max_len, wl.top_k, True))
+        self.guards = g = Guards()
+        self.seq = g.like(self.seq)
+        self.bt = g.like(self.bt)
+        self.out = g.new((wl.B, wl.Hq, wl.d), torch.float32 if out_f32 else torch.bfloat16)
+        self.topk = g.new((wl.B, wl.top_k), torch.int32, fill=-7)
+        self.scores = g.new((wl.B, wl.max_len), torch.float32)
+        self.ws = g.new((K.kvsel_sparse_decode_workspace(self.kv, wl.B, wl.max_len, wl.top_k, True),), torch.uint8)
 
     def step(self, t, append=True):
         wl = self.wl
@@ -64,6 +66,7 @@ def _logical(wl, b, t_done):
 def _check(st, t, heads=None):
     wl = st.wl
     torch.cuda.synchronize()
+    st.guards.check()
     S = int(st.seq[0])
     scores = st.scores.cpu().numpy()
     topk = st.topk.cpu().numpy()
