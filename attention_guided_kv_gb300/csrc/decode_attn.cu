@@ -84,8 +84,9 @@ struct SmemLayout {
   static constexpr size_t seqPref = seqS + size_t(kMaxBatch) * 4;                        // [kMaxBatch+1] i64
   static constexpr size_t stats = seqPref + size_t(kMaxBatch + 1) * 8;                   // [8][2] f32
   static constexpr size_t owners = stats + kMaxG * 2 * 4;                                // [kMaxOwners+1] i32
-  static constexpr size_t sig = owners + (kMaxOwners + 1) * 4;                           // i32: run the block signal
-  static constexpr size_t total = sig + 16;
+  static constexpr size_t sig = owners + (kMaxOwners + 1) * 4;                           // i32: segment completed its pair
+  static constexpr size_t sigseqs = sig + 16;                                            // [kMaxBatch/32] u32 bitmap
+  static constexpr size_t total = sigseqs + kMaxBatch / 8;
 };
 constexpr size_t kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
 
@@ -111,7 +112,8 @@ struct StepParams {
   unsigned* fin;   // CTAs finished (status area); the last one publishes the lengths
   unsigned* pair_k;     // [B*Hkv] owners whose K pass is done: their (m, l) are written
   unsigned* pair_v;     // [B*Hkv] owners whose V pass is done: their O is written
-  unsigned* pair_done;  // [B*Hkv] owners past both waits (the last resets all three)
+  unsigned* pair_done;  // [B*Hkv] (unused)
+  float* oacc;          // [B][Hq][128] fp32: the owners' normalised partial O, summed (zero between calls)
   // per-step top-k block signal (all null / 0 when off)
   float* bmass;         // [B*Hkv][bpages]: each page's attention mass from one kv head's group
   float* bsum;          // [B][bpages]: summed over the kv heads (the caller's mass_out, else workspace)
@@ -490,7 +492,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   long long* sPref = reinterpret_cast<long long*>(smem + SmemLayout::seqPref);
   float* sStat = reinterpret_cast<float*>(smem + SmemLayout::stats);
   int* sOwn = reinterpret_cast<int*>(smem + SmemLayout::owners);  // [kMaxOwners] + count
-  int& sSig = *reinterpret_cast<int*>(smem + SmemLayout::sig);
+  int& sLastPair = *reinterpret_cast<int*>(smem + SmemLayout::sig);  // this segment completed its pair
+  uint32_t* sSigSeqs = reinterpret_cast<uint32_t*>(smem + SmemLayout::sigseqs);  // [kMaxBatch / 32]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = gridDim.x, c = blockIdx.x;
@@ -516,6 +519,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     }
     sPref[P.B] = bad ? -1 : acc;
   }
+  for (int i = tid; i < kMaxBatch / 32; i += kThreads) sSigSeqs[i] = 0u;
   if (tid == 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -896,7 +900,9 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       }
       if (hk) cands_flush(wc, P, pair, lane);
 
-      // ---- the segment's O (already normalised): the 4 warps' sum into the partial slot ----
+      // ---- the segment's O (already normalised): the 4 warps' sum, added into the pair's fp32
+      // accumulator; the pair's last owner to get here writes O and clears the accumulator, so
+      // no owner waits for the others ----
       if (head_ok) {
         float* dst = wo + (warp * kMaxG + g) * kD;
 #pragma unroll
@@ -905,14 +911,38 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
               make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
       }
       consumer_sync();
-      {
-        float* slot = P.part + size_t(c + pair) * kPartFloats + 2 * kMaxG;
-        for (int idx = tid; idx < G * kD; idx += kConsumerWarps * 32)
-          slot[idx] = ((wo[idx] + wo[kMaxG * kD + idx]) + wo[2 * kMaxG * kD + idx]) + wo[3 * kMaxG * kD + idx];
-        __threadfence();
+      float* oacc = P.oacc + (size_t(b) * P.Hq + kvh * G) * kD;
+      for (int idx = tid; idx < G * kD; idx += kConsumerWarps * 32)
+        atomicAdd(oacc + idx, ((wo[idx] + wo[kMaxG * kD + idx]) + wo[2 * kMaxG * kD + idx]) + wo[3 * kMaxG * kD + idx]);
+      __threadfence();
+      consumer_sync();
+      if (tid == 0) {
+        const int no = sOwn[kMaxOwners];  // this segment's owners (listed at its start)
+        const int last = atomicAdd(P.pair_v + pair, 1u) + 1u == unsigned(no);
+        if (last) {
+          __threadfence();
+          P.pair_k[pair] = 0u;
+          P.pair_v[pair] = 0u;
+          if (kSig) {  // every owner's page masses are written too: count the pair for its sequence
+            if (atomicAdd(P.seq_done + b, 1u) + 1u == unsigned(Hkv)) {
+              P.seq_done[b] = 0u;
+              __threadfence();
+              atomicOr(sSigSeqs + (b >> 5), 1u << (b & 31));  // run after the V pass (it needs the ring)
+            }
+          }
+        }
+        sLastPair = last;
       }
       consumer_sync();
-      if (tid == 0) atomicAdd(P.pair_v + pair, 1u);
+      if (sLastPair) {
+        for (int idx = tid; idx < G * kD; idx += kConsumerWarps * 32) {
+          const float v = __ldcg(oacc + idx);
+          __stcg(oacc + idx, 0.f);
+          const size_t oi = (size_t(b) * P.Hq + kvh * G) * kD + idx;
+          if (P.out_f32) static_cast<float*>(P.out)[oi] = v;
+          else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(v);
+        }
+      }
       u = seg_end;
     }
   }
@@ -932,55 +962,18 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           for (int i = tid; i < P.sig_k; i += kThreads) P.sig_topk[size_t(b) * P.sig_k + i] = -1;
       }
   }
-#pragma unroll 1
-  for (long long u = u0; u < u1;) {
-    int b, kvh, pg;
-    loc.locate(u, b, kvh, pg);
-    const int np = loc.pages(b);
-    const long long seg_end = min(u1, u + (np - pg));
-    const int pair = b * Hkv + kvh;
-    if (tid == 0) {
-      const long long pfirst = sPref[b] + (long long)kvh * np;
-      const int no = list_owners(sOwn, pfirst, pfirst + np - 1, U, NC);
-      sSig = 0;
-      // every owner's O is written; the last owner past the wait resets the pair's counters
-      if (wait_word(P.pair_v + pair, unsigned(no), P.status) &&
-          atomicAdd(P.pair_done + pair, 1u) + 1u == unsigned(no)) {
-        P.pair_k[pair] = 0u;
-        P.pair_v[pair] = 0u;
-        P.pair_done[pair] = 0u;
-        if (kSig) {  // every owner's page masses are written too: count the pair for its sequence
-          __threadfence();
-          if (atomicAdd(P.seq_done + b, 1u) + 1u == unsigned(Hkv)) {
-            P.seq_done[b] = 0u;
-            __threadfence();
-            sSig = 1;
-          }
-        }
+  if (kSig) {  // the block signal of every sequence whose last pair this CTA completed
+    __syncthreads();
+    for (int w = 0; w < (P.B + 31) / 32; ++w) {
+      uint32_t bits = sSigSeqs[w];
+      while (bits) {
+        const int b = w * 32 + __ffs(bits) - 1;
+        bits &= bits - 1;
+        block_signal(P, b, sS[b], reinterpret_cast<uint32_t*>(smem + SmemLayout::ring),
+                     int((size_t(kStages) * kStageBytes) / 4));
+        __syncthreads();
       }
     }
-    __syncthreads();
-    const int nown = sOwn[kMaxOwners];
-    int kme = 0;
-    while (kme < nown - 1 && sOwn[kme] != c) ++kme;
-    const int E = G * kD;
-    const int e1 = (kme + 1) * E / nown;
-    for (int idx = kme * E / nown + tid; idx < e1; idx += kThreads) {
-      float acc = 0.f;
-#pragma unroll 4
-      for (int k = 0; k < nown; ++k)
-        acc += __ldcg(P.part + size_t(sOwn[k] + pair) * kPartFloats + 2 * kMaxG + idx);
-      const size_t oi = (size_t(b) * P.Hq + kvh * G) * kD + idx;
-      if (P.out_f32) static_cast<float*>(P.out)[oi] = acc;
-      else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(acc);
-    }
-    __syncthreads();
-    if (kSig && sSig) {  // this CTA finished the sequence's last pair: its top-k block signal
-      block_signal(P, b, sS[b], reinterpret_cast<uint32_t*>(smem + SmemLayout::ring),
-                   int((size_t(kStages) * kStageBytes) / 4));
-      __syncthreads();
-    }
-    u = seg_end;
   }
   // The last CTA to finish publishes the new lengths: every CTA has read the
   // old ones by then.
@@ -1008,16 +1001,20 @@ using namespace kvsel_host;
 namespace {
 
 struct DecodeWs {
-  size_t pair_off, part_off, logit_off, sig_off, total;
+  size_t pair_off, oacc_off, part_off, logit_off, sig_off, total;
 };
 
 // The finish counter lives in the workspace's status area (byte 64); the
-// three per-pair readiness counters follow it.
+// three per-pair readiness counters follow it, then the fp32 O accumulator.
+// Everything before part_off must be zero when a call starts; each call leaves
+// it so.
 DecodeWs decode_ws_layout(int batch, int Hkv, int Hq, int max_len, bool with_probs) {
   DecodeWs w;
   size_t off = kStatusBytes;
   w.pair_off = off;
   off = align_up(off + size_t(batch) * Hkv * 3 * sizeof(unsigned), 256);
+  w.oacc_off = off;
+  off = align_up(off + size_t(batch) * Hq * kD * sizeof(float), 256);
   w.part_off = off;
   off = align_up(off + (size_t(kMaxCtas) + size_t(batch) * Hkv) * kPartFloats * sizeof(float), 256);
   w.logit_off = off;
@@ -1173,6 +1170,7 @@ extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int
   P.pair_k = reinterpret_cast<unsigned*>(ws + L.pair_off);
   P.pair_v = P.pair_k + size_t(batch) * Hkv;
   P.pair_done = P.pair_v + size_t(batch) * Hkv;
+  P.oacc = reinterpret_cast<float*>(ws + L.oacc_off);
   P.status = reinterpret_cast<int*>(ws);
   P.B = batch;
   P.max_pages = max_pages;
