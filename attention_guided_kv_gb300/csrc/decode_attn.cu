@@ -38,15 +38,16 @@
 //     selection), and
 //     accumulates O += P V with P split into a bf16 high part (A rows 0..7)
 //     and its bf16 residual (rows 8..15), so P keeps ~16 mantissa bits at no
-//     extra MMA cost.  The segment's O, already normalised, goes to the slot.
+//     extra MMA cost.  The segment's O, already normalised, is added into
+//     the pair's fp32 accumulator; the owner that adds last writes O and
+//     clears the accumulator, so no owner waits for another at the end.
 // The normalisation work therefore overlaps the V stream instead of trailing
-// the kernel.  Last, once every owner's V pass is done, each owner writes its
-// share of O = the sum of the pair's partial O.  The last CTA to finish
-// publishes the new lengths.
+// the kernel.
 //
 // The CTA that owns the page of a sequence's appended slot writes k_new /
 // v_new into the pool (and the slot's original position) before its
 // producer starts, fencing the generic-proxy stores against the TMA reads.
+// Once every CTA is past that point, the last one publishes the new lengths.
 #include <mutex>
 
 #include "common.cuh"
@@ -109,7 +110,7 @@ struct StepParams {
   int32_t* link_pos;
   void* out;
   float* part;     // [slots][kPartFloats]
-  unsigned* fin;   // CTAs finished (status area); the last one publishes the lengths
+  unsigned* fin;   // CTAs past the append (status area); the last one publishes the lengths
   unsigned* pair_k;     // [B*Hkv] owners whose K pass is done: their (m, l) are written
   unsigned* pair_v;     // [B*Hkv] owners whose V pass is done: their O is written
   unsigned* pair_done;  // [B*Hkv] (unused)
@@ -565,6 +566,21 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     fence_proxy_async_global();
   }
   __syncthreads();
+  // Every CTA has read the old lengths and positions (and appended) once all
+  // have counted themselves here: the last one publishes the new ones, long
+  // before a kernel launched after this one can start.  (A preceding H2O
+  // select reads the lengths before it lets this launch start.)
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(P.fin, 1u) + 1u == unsigned(NC)) {
+      *P.fin = 0u;
+      for (int b = 0; b < P.B; ++b) {
+        P.seq_lens[b] = sS[b];
+        if (append && P.next_pos) P.next_pos[b] += 1;
+      }
+      __threadfence();
+    }
+  }
 
   const int n = int(u1 - u0);       // pages of the range
   const int nsk = (n + 1) >> 1;     // stages per pass
@@ -947,7 +963,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     }
   }
 
-  // ================= O = the sum of the pair's partial O =================
+  // ================= zero-length sequences, block signals =================
   __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (c == 0) {
@@ -973,19 +989,6 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                      int((size_t(kStages) * kStageBytes) / 4));
         __syncthreads();
       }
-    }
-  }
-  // The last CTA to finish publishes the new lengths: every CTA has read the
-  // old ones by then.
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(P.fin, 1u) + 1u == unsigned(NC)) {
-      *P.fin = 0u;
-      for (int b = 0; b < P.B; ++b) {
-        P.seq_lens[b] = sS[b];
-        if (append && P.next_pos) P.next_pos[b] += 1;
-      }
-      __threadfence();
     }
   }
 }

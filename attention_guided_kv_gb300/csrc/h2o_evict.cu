@@ -194,14 +194,13 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
   __shared__ int s_first;
   __shared__ uint32_t s_cnt;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the scores come from the previous kernel
-  // A decode step launched after this kernel may start now: it touches the
-  // scores, the candidate lists and the thresholds only after waiting for
-  // this kernel to finish.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x;
   const int S = P.seq_lens[b];
+  // A decode step launched after this kernel may start now: it publishes new
+  // lengths early (read above), and touches the scores, the candidate lists
+  // and the thresholds only after waiting for this kernel to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const size_t rowi = size_t(b) * P.Hkv + kvh;
   const float* row = P.cum + rowi * P.max_len;
   const int32_t* prow = P.pos_map ? P.pos_map + rowi * P.max_len : nullptr;
