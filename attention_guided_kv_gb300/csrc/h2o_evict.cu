@@ -68,6 +68,53 @@ __device__ __forceinline__ uint32_t lowest_bits(uint32_t x, uint32_t n) {
   return r;
 }
 
+// Radix select of the k-th largest of the live keys ukey[0..cnt) (key 0: not a
+// candidate; keys whose bits above `top` differ from `prefix` are ignored)
+// with 11-bit digits from bit `top` down, so a 32-bit spread takes three
+// passes.  A candidate list is small, so one shared histogram of 2048 bins
+// takes the increments directly; two histograms alternate, each pass clearing
+// the next one's.  The bins are scanned from the top down, two per thread.
+// Returns T and need_eq (how many keys equal to T are kept).
+__device__ __forceinline__ void list_radix(const uint32_t* ukey, uint32_t cnt, int top, uint32_t prefix, uint32_t k,
+                                           RowTopkSmem& rk, uint32_t& T, uint32_t& need_eq) {
+  static_assert(sizeof(RowTopkSmem::lhist) >= 2 * 2048 * sizeof(uint32_t), "two histograms of 2048 bins");
+  static_assert(kSelThreads * 2 == 2048, "two bins per thread");
+  const int tid = threadIdx.x;
+  uint32_t* H = &rk.lhist[0][0];
+  uint32_t mask = top >= 31 ? 0u : ~((2u << top) - 1u);
+  prefix &= mask;
+  uint32_t krem = k;
+  for (int i = tid; i < 2048; i += kSelThreads) H[i] = 0u;
+  __syncthreads();
+#pragma unroll 1
+  for (int hi = top, pass = 0; hi >= 0; hi -= 11, ++pass) {
+    uint32_t* h = H + (pass & 1) * 2048;
+    uint32_t* hn = H + ((pass + 1) & 1) * 2048;
+    const int shift = hi >= 10 ? hi - 10 : 0;
+    const uint32_t dmask = (2u << (hi - shift)) - 1u;
+    for (uint32_t i = tid; i < cnt; i += kSelThreads) {
+      const uint32_t u = ukey[i];
+      if (u != 0u && (u & mask) == prefix) atomicAdd(&h[(u >> shift) & dmask], 1u);
+    }
+    for (int i = tid; i < 2048; i += kSelThreads) hn[i] = 0u;
+    __syncthreads();
+    const uint32_t c0 = h[2047 - 2 * tid], c1 = h[2046 - 2 * tid];
+    uint32_t tot;
+    const uint32_t ex = rk_block_excl_scan(c0 + c1, rk.wtot[0], tot);
+    if (ex < krem && krem <= ex + c0 + c1) {  // this thread's bins hold the krem-th largest
+      const bool first = krem <= ex + c0;
+      rk.digit = first ? 2047u - 2u * tid : 2046u - 2u * tid;
+      rk.above = first ? ex : ex + c0;
+    }
+    __syncthreads();
+    krem -= rk.above;
+    prefix |= rk.digit << shift;
+    mask |= dmask << shift;
+  }
+  T = prefix;
+  need_eq = krem;
+}
+
 // Top-k of the middle slots [lo, hi) from the candidate list that the decode
 // step collected (every slot whose score is >= the row's last threshold).
 // Usable when the list is fresh and holds at least k slots of [lo, hi): the
@@ -144,15 +191,7 @@ __device__ __forceinline__ bool select_from_list(const SelectParams& P, size_t r
     T = lo_key;
     need_eq = uint32_t(k);
   } else {
-    const uint32_t c_r = (cnt + 31u) & ~31u;
-    rk_radix(
-        [&](auto&& f) {
-          for (uint32_t i = tid; i < c_r; i += kSelThreads) {
-            const bool live = i < cnt;
-            f(live ? sm.rk.ukey[i] : 0u, live);
-          }
-        },
-        31 - __clz(lo_key ^ hi_key), lo_key, uint32_t(k), sm.rk, T, need_eq);
+    list_radix(sm.rk.ukey, cnt, 31 - __clz(lo_key ^ hi_key), lo_key, uint32_t(k), sm.rk, T, need_eq);
   }
   for (uint32_t i = tid; i < cnt; i += kSelThreads) {
     const uint32_t u = sm.rk.ukey[i];
@@ -192,16 +231,19 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
   extern __shared__ __align__(16) uint8_t sel_smem[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_smem);
   __shared__ int s_first;
-  __shared__ uint32_t s_cnt;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the scores come from the previous kernel
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x;
+  const size_t rowi = size_t(b) * P.Hkv + kvh;
+  // the length, the decode step's candidate count and the row's last
+  // threshold, in one round trip
   const int S = P.seq_lens[b];
+  const uint32_t cnt = __ldcg(P.link.count + rowi);
+  const uint32_t hk = __ldcg(P.link.hint + rowi);
   // A decode step launched after this kernel may start now: it publishes new
   // lengths early (read above), and touches the scores, the candidate lists
   // and the thresholds only after waiting for this kernel to finish.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const size_t rowi = size_t(b) * P.Hkv + kvh;
   const float* row = P.cum + rowi * P.max_len;
   const int32_t* prow = P.pos_map ? P.pos_map + rowi * P.max_len : nullptr;
   int32_t* keep = P.keep_slots + rowi * P.budget;
@@ -211,9 +253,6 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
     if (tid == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
     return;
   }
-  if (tid == 0) s_cnt = P.link.count[rowi];
-  __syncthreads();
-  const uint32_t cnt = s_cnt;
   if (S <= P.budget) {
     for (int i = tid; i < P.budget; i += kSelThreads) {
       const int slot = i < S ? i : -1;
@@ -241,7 +280,6 @@ __global__ void __launch_bounds__(kSelThreads) h2o_select_kernel(const SelectPar
   for (int i = tid; i < P.window; i += kSelThreads) put(P.budget - P.window + i, S - P.window + i);
   if (k > 0) {
     const int lo = P.n_sink, hi = S - P.window;
-    const uint32_t hk = P.link.hint[rowi];
     uint32_t T = 0;
     bool done = false;
     if (hk != 0u && cnt >= uint32_t(k) && cnt <= uint32_t(kLinkCap) && hi - lo <= 32 * kListWords)
