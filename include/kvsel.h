@@ -232,11 +232,13 @@ KVSEL_API size_t kvsel_h2o_link_bytes(int batch, int num_kv_heads);
  *    the device current); make that first call before any stream capture.
  *  - Calls that need more scratch than 8 MiB are rejected with
  *    KVSEL_ERR_INVALID_ARG: about (1024 + batch * num_kv_heads) * 4160 bytes
- *    + batch * num_kv_heads * 12 bytes, plus batch * num_q_heads * max_len * 4
- *    bytes when probs is not given (the kernel keeps its logits there).
+ *    + batch * num_kv_heads * 12 bytes + batch * num_q_heads * 512 bytes (an
+ *    fp32 O accumulator), plus batch * num_q_heads * max_len * 4 bytes when
+ *    probs is not given (the kernel keeps its logits there).
  *  - Every call uses the same array, so calls that overlap on the GPU (other
  *    streams, other threads) race and corrupt each other; serialise them.
- *    Each call clears the array's status word and counters first.
+ *    Each call clears the array's status word, counters and O accumulator
+ *    first.
  *  - Device-side problems (a block-table entry outside the pool) are not
  *    reported back: there is no workspace to read them from.
  * Nothing here calls cudaMalloc, cudaFree or any allocating library routine. */
