@@ -23,6 +23,14 @@ namespace kvsel {
 // ---------------------------------------------------------------------------
 constexpr size_t kStatusBytes = 256;
 
+// Pool pages hold 16, 32, 64, 128 or 256 tokens; kernels address them in
+// 16-token tiles.  Returns log2(page_size / 16), or -1 for any other size.
+__host__ __device__ inline int page_shift_of(int page_size) {
+  for (int s = 0; s <= 4; ++s)
+    if (page_size == (16 << s)) return s;
+  return -1;
+}
+
 __device__ __forceinline__ void report(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }

@@ -126,6 +126,7 @@ struct StepParams {
   int sig_k, sig_stepv, bpages;
   int* status;
   int B, max_pages, Hq, Hkv, G, num_pages, max_len, out_f32;
+  int page_shift;  // log2(page_size / 16): a pool page holds 1 << page_shift 16-token tiles
   int vec2;        // logit and score rows are 8-byte aligned: key pairs move as float2
   float scale_log2;
 };
@@ -515,7 +516,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       sPref[b] = acc;
       const int S = sS[b];
       const int np = (S + kPage - 1) / kPage;
-      if (S < (append ? 1 : 0) || S > P.max_len || np > P.max_pages) bad = 1;
+      if (S < (append ? 1 : 0) || S > P.max_len || np > (P.max_pages << P.page_shift)) bad = 1;
       acc += (long long)Hkv * np;
     }
     sPref[P.B] = bad ? -1 : acc;
@@ -549,9 +550,10 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       for (int kvh = 0; kvh < Hkv; ++kvh) {
         const long long ua = sPref[b] + (long long)kvh * np + S_old / kPage;
         if (ua < u0 || ua >= u1) continue;
-        const int phys = __ldcg(P.block_table + size_t(b) * P.max_pages + S_old / kPage);
+        const int phys = __ldcg(P.block_table + size_t(b) * P.max_pages + (S_old >> (4 + P.page_shift)));
         if (unsigned(phys) < unsigned(P.num_pages)) {
-          const size_t row = (size_t(phys) * Hkv + kvh) * kPage + (S_old % kPage);
+          const int psz = kPage << P.page_shift;
+          const size_t row = (size_t(phys) * Hkv + kvh) * psz + (S_old & (psz - 1));
           const int t = tid & 15;
           const __nv_bfloat16* src = (tid < 16 ? P.k_new : P.v_new) + (size_t(b) * Hkv + kvh) * kD;
           __nv_bfloat16* dst = (tid < 16 ? P.k_pool : P.v_pool) + row * kD;
@@ -612,12 +614,13 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         if (i >= n) return -1;
         int b, kvh, pg;
         loc.locate(u0 + i, b, kvh, pg);
-        int phys = __ldcg(P.block_table + size_t(b) * P.max_pages + pg);
+        int phys = __ldcg(P.block_table + size_t(b) * P.max_pages + (pg >> P.page_shift));
         if (unsigned(phys) >= unsigned(P.num_pages)) {
           report(P.status, KVSEL_ERR_BAD_INDEX);
           phys = 0;
         }
-        return (phys * Hkv + kvh) * kPage;
+        // the 16-token tile pg of a page of 16 << page_shift rows
+        return ((phys * Hkv + kvh) << P.page_shift | (pg & ((1 << P.page_shift) - 1))) * kPage;
       };
       bool stop = false;
 #pragma unroll 1
@@ -1091,14 +1094,18 @@ extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int
   const std::string fn = "kvsel_decode_attn: ";
   if (!kv || !kv->k_pool || !kv->v_pool)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "kv pools must be non-NULL");
-  if (kv->head_dim != kD || kv->page_size != kPage)
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16 are implemented");
+  if (kv->head_dim != kD || page_shift_of(kv->page_size) < 0)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16, 32, 64, 128 or 256 are implemented");
+  if (signal && kv->page_size != kPage)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "the block signal is implemented for page_size 16 only");
   if (kv->num_kv_heads < 1 || kv->num_q_heads < 1 || kv->num_q_heads % kv->num_kv_heads != 0)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "num_q_heads must be a positive multiple of num_kv_heads");
   const int Hkv = kv->num_kv_heads, Hq = kv->num_q_heads, G = Hq / Hkv;
   if (G > kMaxG) return fail(KVSEL_ERR_UNSUPPORTED, fn + "at most 8 q heads per kv head are implemented");
-  if (kv->num_pages < 1 || (long long)kv->num_pages * Hkv * kPage >= (1LL << 31))
-    return fail(KVSEL_ERR_INVALID_ARG, fn + "num_pages * num_kv_heads * 16 must be in [1, 2^31)");
+  if (kv->num_pages < 1 || (long long)kv->num_pages * Hkv * kv->page_size >= (1LL << 31))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "num_pages * num_kv_heads * page_size must be in [1, 2^31)");
+  if ((long long)max_pages << page_shift_of(kv->page_size) >= (1LL << 31))
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "max_pages * page_size / 16 must be below 2^31");
   if (!block_table || !seq_lens || !q || !out || batch < 1 || max_pages < 1 || max_len < 1)
     return fail(KVSEL_ERR_INVALID_ARG,
                 fn + "block_table, seq_lens, q, out are required; batch, max_pages, max_len >= 1");
@@ -1139,7 +1146,7 @@ extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int
                 fn + "num_ctas exceeds the co-resident CTA count " + std::to_string(resident));
 
   CUtensorMap tmK, tmV;
-  const uint64_t rows = uint64_t(kv->num_pages) * Hkv * kPage;
+  const uint64_t rows = uint64_t(kv->num_pages) * Hkv * kv->page_size;
   if (!encode_bf16_row_pages(&tmK, kv->k_pool, rows, kPage) ||
       !encode_bf16_row_pages(&tmV, kv->v_pool, rows, kPage))
     return fail(KVSEL_ERR_CUDA, fn + "tensor-map encode failed");
@@ -1177,6 +1184,7 @@ extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int
   P.status = reinterpret_cast<int*>(ws);
   P.B = batch;
   P.max_pages = max_pages;
+  P.page_shift = page_shift_of(kv->page_size);
   P.Hq = Hq;
   P.Hkv = Hkv;
   P.G = G;

@@ -28,7 +28,7 @@
 namespace kvsel {
 
 constexpr int kHD = 128;
-constexpr int kPg = 16;
+constexpr int kPg = 16;  // the smallest page; pools may use 16 << page_shift tokens per page
 constexpr int kSelThreads = 1024;
 constexpr int kChunk = 64;
 constexpr int kSelGroups = 8;  // register-resident rows: up to 32 x 8 x 128 candidates
@@ -313,14 +313,18 @@ struct CompactParams {
   int32_t* pos_map;
   int* status;
   int Hkv, max_len, max_pages, num_pages, budget;
+  int page_shift;  // log2(page_size / 16)
 };
 
-__device__ __forceinline__ size_t pool_row(const int32_t* bt, int slot, int Hkv, int kvh,
+// Pool row of a sequence's slot: page block_table[slot / page_size], row
+// slot % page_size of the kv head's part of that page.
+__device__ __forceinline__ size_t pool_row(const int32_t* bt, int slot, int Hkv, int kvh, int page_shift,
                                            int num_pages, int* status, bool& ok) {
-  const int phys = bt[slot / kPg];
+  const int lg = 4 + page_shift;
+  const int phys = bt[slot >> lg];
   ok = unsigned(phys) < unsigned(num_pages);
   if (!ok) report(status, KVSEL_ERR_BAD_INDEX);
-  return (size_t(phys) * Hkv + kvh) * kPg + (slot % kPg);
+  return ((size_t(phys) * Hkv + kvh) << lg) + (slot & ((1 << lg) - 1));
 }
 
 __global__ void __launch_bounds__(256) h2o_compact_kernel(const CompactParams P) {
@@ -334,7 +338,7 @@ __global__ void __launch_bounds__(256) h2o_compact_kernel(const CompactParams P)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the truncation waits for this kernel
   const int S = P.seq_lens[b];
   if (S <= P.budget) return;
-  if (S > P.max_len || S > P.max_pages * kPg) {
+  if (S > P.max_len || (long long)S > ((long long)P.max_pages << (4 + P.page_shift))) {
     if (tid == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
     return;
   }
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(256) h2o_compact_kernel(const CompactParams P)
     const int cnt = min(kChunk, n_keep - c0);
     for (int t = tok; t < cnt; t += 16) {
       bool ok;
-      const size_t r = pool_row(bt, keep[c0 + t], P.Hkv, kvh, P.num_pages, P.status, ok);
+      const size_t r = pool_row(bt, keep[c0 + t], P.Hkv, kvh, P.page_shift, P.num_pages, P.status, ok);
       sk[t][t16] = ok ? reinterpret_cast<const uint4*>(P.k_pool + r * kHD)[t16] : make_uint4(0, 0, 0, 0);
       sv[t][t16] = ok ? reinterpret_cast<const uint4*>(P.v_pool + r * kHD)[t16] : make_uint4(0, 0, 0, 0);
     }
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(256) h2o_compact_kernel(const CompactParams P)
     __syncthreads();
     for (int t = tok; t < cnt; t += 16) {
       bool ok;
-      const size_t r = pool_row(bt, c0 + t, P.Hkv, kvh, P.num_pages, P.status, ok);
+      const size_t r = pool_row(bt, c0 + t, P.Hkv, kvh, P.page_shift, P.num_pages, P.status, ok);
       if (ok) {
         reinterpret_cast<uint4*>(P.k_pool + r * kHD)[t16] = sk[t][t16];
         reinterpret_cast<uint4*>(P.v_pool + r * kHD)[t16] = sv[t][t16];
@@ -381,6 +385,7 @@ struct TruncateParams {
   int32_t* block_table;
   int32_t* freed;
   int max_pages, budget, max_len;
+  int page_shift;
 };
 
 __global__ void __launch_bounds__(256) h2o_truncate_kernel(const TruncateParams P) {
@@ -392,8 +397,9 @@ __global__ void __launch_bounds__(256) h2o_truncate_kernel(const TruncateParams 
   const int S = P.seq_lens[b];
   if (S > P.max_len) return;
   const int n_keep = S > P.budget ? P.budget : S;
-  const int old_pages = min(P.max_pages, (S + kPg - 1) / kPg);
-  const int new_pages = (n_keep + kPg - 1) / kPg;
+  const int psz = kPg << P.page_shift;
+  const int old_pages = min(P.max_pages, (S + psz - 1) / psz);
+  const int new_pages = (n_keep + psz - 1) / psz;
   int32_t* bt = P.block_table + size_t(b) * P.max_pages;
   int32_t* fr = P.freed ? P.freed + size_t(b) * P.max_pages : nullptr;
   for (int p = threadIdx.x; p < P.max_pages; p += blockDim.x) {
@@ -443,8 +449,8 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   const std::string fn = "kvsel_h2o_evict: ";
   if (!kv || kv->num_kv_heads < 1)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "kv descriptor is required");
-  if (kv->page_size != kPg || kv->head_dim != kHD)
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16 are implemented");
+  if (page_shift_of(kv->page_size) < 0 || kv->head_dim != kHD)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16, 32, 64, 128 or 256 are implemented");
   if (!block_table || !seq_lens || !h2o_cum || batch < 1 || max_pages < 1 || max_len < 1)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "block_table, seq_lens, h2o_cum required; batch, max_pages, max_len >= 1");
   if (budget < 1 || n_sink < 0 || window < 0 || (long long)n_sink + window > budget)
@@ -509,6 +515,7 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   C.max_pages = max_pages;
   C.num_pages = kv->num_pages;
   C.budget = budget;
+  C.page_shift = page_shift_of(kv->page_size);
   trace_before("h2o_compact", st);
   cfg.gridDim = dim3(kv->num_kv_heads, batch);
   cfg.blockDim = dim3(256);
@@ -524,6 +531,7 @@ extern "C" kvsel_status kvsel_h2o_evict(const kvsel_paged_kv* kv, int32_t* block
   T.max_pages = max_pages;
   T.budget = budget;
   T.max_len = max_len;
+  T.page_shift = C.page_shift;
   trace_before("h2o_truncate", st);
   cfg.gridDim = dim3(batch);
   cfg.blockDim = dim3(256);

@@ -25,7 +25,7 @@
 namespace kvsel {
 
 constexpr int kKcHD = 128;
-constexpr int kKcPg = 16;
+constexpr int kKcPg = 16;         // the smallest page; pools may use 16 << page_shift tokens per page
 constexpr int kKcChunk = 128;     // slots per chunk: 128 x 512 B of K and V held in registers
 constexpr int kKcThreads = 512;
 constexpr int kKcCheckThreads = 256;
@@ -44,6 +44,7 @@ struct KcParams {
   int32_t* first_move;        // workspace [batch][Hkv]
   int* status;
   int Hkv, keep_stride, max_len, max_pages, num_pages;
+  int page_shift;             // log2(page_size / 16)
 };
 
 __global__ void __launch_bounds__(kKcCheckThreads) kc_check_kernel(const KcParams P) {
@@ -52,7 +53,8 @@ __global__ void __launch_bounds__(kKcCheckThreads) kc_check_kernel(const KcParam
   __shared__ int s_n, s_bad, s_first;
   const int b = blockIdx.x, tid = threadIdx.x;
   const int S = P.seq_lens[b];
-  bool bad = S < 0 || S > P.max_pages * kKcPg || ((P.scores || P.pos_map) && S > P.max_len);
+  bool bad = S < 0 || (long long)S > ((long long)P.max_pages << (4 + P.page_shift)) ||
+             ((P.scores || P.pos_map) && S > P.max_len);
   int n_all = -1;
   for (int g = 0; g < P.Hkv && !bad; ++g) {
     const size_t rowi = size_t(b) * P.Hkv + g;
@@ -100,13 +102,15 @@ __global__ void __launch_bounds__(kKcCheckThreads) kc_check_kernel(const KcParam
   }
 }
 
-// Pool row of slot `slot` of kv head `kvh` through the sequence's block table.
-__device__ __forceinline__ size_t kc_pool_row(const int32_t* bt, int slot, int Hkv, int kvh, int num_pages,
-                                              int* status, bool& ok) {
-  const int phys = bt[slot / kKcPg];
+// Pool row of slot `slot` of kv head `kvh` through the sequence's block table:
+// page block_table[slot / page_size], row slot % page_size of the head's part.
+__device__ __forceinline__ size_t kc_pool_row(const int32_t* bt, int slot, int Hkv, int kvh, int page_shift,
+                                              int num_pages, int* status, bool& ok) {
+  const int lg = 4 + page_shift;
+  const int phys = bt[slot >> lg];
   ok = unsigned(phys) < unsigned(num_pages);
   if (!ok) report(status, KVSEL_ERR_BAD_INDEX);
-  return (size_t(phys) * Hkv + kvh) * kKcPg + (slot % kKcPg);
+  return ((size_t(phys) * Hkv + kvh) << lg) + (slot & ((1 << lg) - 1));
 }
 
 constexpr int kKcRowsPerThread = kKcChunk / (kKcThreads / 16);
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(kKcThreads) kc_move_kernel(const KcParams P) {
       rk[j] = rv[j] = make_uint4(0, 0, 0, 0);
       if (t < cnt) {
         bool ok;
-        const size_t r = kc_pool_row(bt, s_src[t], P.Hkv, kvh, P.num_pages, P.status, ok);
+        const size_t r = kc_pool_row(bt, s_src[t], P.Hkv, kvh, P.page_shift, P.num_pages, P.status, ok);
         if (ok) {
           rk[j] = __ldcs(reinterpret_cast<const uint4*>(P.k_pool + r * kKcHD) + part);
           rv[j] = __ldcs(reinterpret_cast<const uint4*>(P.v_pool + r * kKcHD) + part);
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(kKcThreads) kc_move_kernel(const KcParams P) {
       const int t = r0 + j * (kKcThreads / 16);
       if (t < cnt) {
         bool ok;
-        const size_t r = kc_pool_row(bt, c0 + t, P.Hkv, kvh, P.num_pages, P.status, ok);
+        const size_t r = kc_pool_row(bt, c0 + t, P.Hkv, kvh, P.page_shift, P.num_pages, P.status, ok);
         if (ok) {
           reinterpret_cast<uint4*>(P.k_pool + r * kKcHD)[part] = rk[j];
           reinterpret_cast<uint4*>(P.v_pool + r * kKcHD)[part] = rv[j];
@@ -179,8 +183,9 @@ __global__ void __launch_bounds__(kKcCheckThreads) kc_truncate_kernel(const KcPa
   const int n = P.n_keep[b];
   if (n < 0) return;
   const int S = P.seq_lens[b];
-  const int old_pages = (S + kKcPg - 1) / kKcPg;  // <= max_pages (checked)
-  const int new_pages = (n + kKcPg - 1) / kKcPg;
+  const int psz = kKcPg << P.page_shift;
+  const int old_pages = (S + psz - 1) / psz;  // <= max_pages (checked)
+  const int new_pages = (n + psz - 1) / psz;
   int32_t* bt = P.block_table + size_t(b) * P.max_pages;
   if (P.freed) {
     int32_t* fr = P.freed + size_t(b) * P.max_pages;
@@ -223,8 +228,8 @@ extern "C" kvsel_status kvsel_kv_compact(const kvsel_paged_kv* kv, int32_t* bloc
   const std::string fn = "kvsel_kv_compact: ";
   if (!kv || kv->num_kv_heads < 1 || !kv->k_pool || !kv->v_pool || kv->num_pages < 1)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "kv descriptor with both pools is required");
-  if (kv->page_size != kKcPg || kv->head_dim != kKcHD)
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16 are implemented");
+  if (page_shift_of(kv->page_size) < 0 || kv->head_dim != kKcHD)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16, 32, 64, 128 or 256 are implemented");
   if (!aligned(kv->k_pool, 16) || !aligned(kv->v_pool, 16))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "pools must be 16-byte aligned");
   if (!block_table || !seq_lens || !keep || batch < 1 || max_pages < 1 || keep_stride < 1)
@@ -257,6 +262,7 @@ extern "C" kvsel_status kvsel_kv_compact(const kvsel_paged_kv* kv, int32_t* bloc
   P.max_len = max_len;
   P.max_pages = max_pages;
   P.num_pages = kv->num_pages;
+  P.page_shift = page_shift_of(kv->page_size);
 
   trace_before("kc_check", st);
   kc_check_kernel<<<batch, kKcCheckThreads, 0, st>>>(P);

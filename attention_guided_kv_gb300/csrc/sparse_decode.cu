@@ -49,7 +49,7 @@
 namespace kvsel {
 
 constexpr int kSdD = 128;
-constexpr int kSdPage = 16;
+constexpr int kSdPage = 16;  // the smallest page; pools may use 16 << page_shift tokens per page
 constexpr int kSdDi = 64;
 constexpr int kSdMaxHi = 8;
 constexpr int kSdTopkGroups = 8;         // whole-row fallback: rows up to 32K stay in registers
@@ -102,12 +102,13 @@ struct SdParams {
   int* status;
   int B, max_pages, Hq, Hkv, G, Hi, num_pages, max_len, top_k, idx_ctas, slices, splits, appended, out_f32;
   int scores_vec;                  // score rows are 16-byte aligned (float4 reads)
+  int page_shift;                  // log2(page_size / 16)
   float scale_log2;
 };
 
 __device__ __forceinline__ bool sd_len_ok(const SdParams& P, int b, int& S) {
   S = P.seq_lens[b] + P.appended;
-  return S >= 0 && S <= P.max_len && (S + kSdPage - 1) / kSdPage <= P.max_pages;
+  return S >= 0 && S <= P.max_len && (((long long)S + (kSdPage << P.page_shift) - 1) >> (4 + P.page_shift)) <= P.max_pages;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -144,12 +145,13 @@ __global__ void __launch_bounds__(kSdIdxWarps * 32) sd_index_kernel(const SdPara
   const int t0 = int((long long)tiles * c / P.idx_ctas), t1 = int((long long)tiles * (c + 1) / P.idx_ctas);
   if (P.appended && S_old / 16 >= t0 && S_old / 16 < t1) {
     // this CTA covers the appended token: its K, V (every kv head) and indexer key
-    const int phys = P.block_table[size_t(b) * P.max_pages + S_old / kSdPage];
+    const int phys = P.block_table[size_t(b) * P.max_pages + (S_old >> (4 + P.page_shift))];
     if (unsigned(phys) < unsigned(P.num_pages)) {
       for (int i = tid; i < P.Hkv * 32; i += blockDim.x) {
         const int kvh = i >> 5, t = i & 15;
         const bool isv = (i & 31) >= 16;
-        const size_t row = (size_t(phys) * P.Hkv + kvh) * kSdPage + (S_old % kSdPage);
+        const size_t row = ((size_t(phys) * P.Hkv + kvh) << (4 + P.page_shift)) +
+                           (S_old & ((kSdPage << P.page_shift) - 1));
         const uint4* src = reinterpret_cast<const uint4*>((isv ? P.v_new : P.k_new) +
                                                           (size_t(b) * P.Hkv + kvh) * kSdD);
         reinterpret_cast<uint4*>((isv ? P.v_pool : P.k_pool) + row * kSdD)[t] = src[t];
@@ -300,17 +302,18 @@ __global__ void __launch_bounds__(kSdSelThreads) sd_select_kernel(const SdParams
   const int32_t* bt = P.block_table + size_t(b) * P.max_pages;
   uint32_t* ghist = P.hist + size_t(b) * kSdHistBins;
   uint32_t* gsub = P.subhist + size_t(b) * kSdHistBins;
-  // a position's pool row for kv head 0 (every kv head adds kvh * 16), given its page's entry
+  // a position's pool row for kv head 0 (every kv head adds kvh * page_size), given its page's entry
+  const int lg = 4 + P.page_shift;
   auto pool_row = [&](int pos, int phys) {
     if (unsigned(phys) >= unsigned(P.num_pages)) {
       report(P.status, KVSEL_ERR_BAD_INDEX);
       phys = 0;
     }
-    return phys * P.Hkv * kSdPage + (pos & (kSdPage - 1));
+    return ((phys * P.Hkv) << lg) + (pos & ((1 << lg) - 1));
   };
   auto put = [&](int i, int pos) {
     sel[i] = pos;
-    srow_out[i] = pool_row(pos, bt[pos / kSdPage]);
+    srow_out[i] = pool_row(pos, bt[pos >> lg]);
     if (tko) tko[i] = pos;
   };
   auto finish_row = [&]() {  // the row's histograms and counter back to zero, the count out
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(kSdSelThreads) sd_select_kernel(const SdParams
   uint4* mykeys = reinterpret_cast<uint4*>(sm.rk.ukey + 16 * tid);
   uint32_t h[4];
   sd_load_bins(ghist, h);
-  const int phys0 = pt < S ? bt[pt / kSdPage] : 0;
+  const int phys0 = pt < S ? bt[pt >> lg] : 0;  // the 16 positions lie in one page
   {
     const float* srow = P.scores + size_t(b) * P.max_len;
     if (P.scores_vec && pt + 15 < S) {
@@ -612,7 +615,7 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
       const int r16 = row & 15;
       const int r = __shfl_sync(0xffffffffu, mine, (jj & 1) * 16 + r16);
       const bool valid = r >= 0;
-      const size_t prow = size_t(valid ? r : 0) + size_t(kvh) * kSdPage;
+      const size_t prow = size_t(valid ? r : 0) + (size_t(kvh) << (4 + P.page_shift));
       const __nv_bfloat16* src = (row < 16 ? P.k_pool : P.v_pool) + prow * kSdD + u * 8;
       const uint32_t dst = wbuf + s * 8192 + (row < 16 ? 0 : 4096) + tile_unit_off(r16, u);
       cp_async16(dst, src, valid);
@@ -742,8 +745,8 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   const std::string fn = "kvsel_sparse_decode: ";
   if (!kv || !kv->k_pool || !kv->v_pool)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "kv pools must be non-NULL");
-  if (kv->head_dim != kSdD || kv->page_size != kSdPage)
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16 are implemented");
+  if (kv->head_dim != kSdD || page_shift_of(kv->page_size) < 0)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16, 32, 64, 128 or 256 are implemented");
   if (kv->num_kv_heads < 1 || kv->num_q_heads < 1 || kv->num_q_heads % kv->num_kv_heads != 0)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "num_q_heads must be a positive multiple of num_kv_heads");
   const int Hkv = kv->num_kv_heads, Hq = kv->num_q_heads, G = Hq / Hkv;
@@ -760,8 +763,8 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
     return fail(KVSEL_ERR_INVALID_ARG, fn + "out_dtype must be KVSEL_BF16 or KVSEL_F32");
   const SdWs L = sd_ws_layout(batch, max_len, top_k, scores_out == nullptr);
   if (max_len > kSdMaxLen) return fail(KVSEL_ERR_UNSUPPORTED, fn + "max_len must be <= 2^28");
-  if ((long long)kv->num_pages * Hkv * kSdPage >= (1LL << 31))
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "num_pages * num_kv_heads * 16 must be below 2^31");
+  if ((long long)kv->num_pages * Hkv * kv->page_size >= (1LL << 31))
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "num_pages * num_kv_heads * page_size must be below 2^31");
   if (!aligned(kv->k_pool, 16) || !aligned(kv->v_pool, 16) || !aligned(q, 16) || !aligned(idx_k, 16) ||
       !aligned(idx_q, 8) || (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(idx_k_new, 16))))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "pools, q, k_new, v_new, idx_k, idx_k_new must be 16-byte aligned");
@@ -793,6 +796,7 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   P.idx_k = static_cast<__nv_bfloat16*>(idx_k);
   P.idx_k_new = static_cast<const __nv_bfloat16*>(idx_k_new);
   P.scores = scores_out ? scores_out : reinterpret_cast<float*>(ws + L.scores);
+  P.page_shift = page_shift_of(kv->page_size);
   const int slices = (max_len + kSdSelSlice - 1) / kSdSelSlice;
   P.hist = reinterpret_cast<uint32_t*>(ws + L.hist);
   P.subhist = P.hist + size_t(batch) * kSdHistBins;

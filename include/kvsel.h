@@ -24,12 +24,16 @@
  *  - No C++ exception crosses this interface.
  *
  * Paged KV layout (the paged cache of "From sliding window to
- * attention-guided eviction" §5, blocks of 16 tokens): K and V pools are
- * separate bf16 arrays [num_pages][num_kv_heads][page_size][head_dim]; a
+ * attention-guided eviction" §5, blocks of 16 or 256 tokens): K and V pools
+ * are separate bf16 arrays [num_pages][num_kv_heads][page_size][head_dim]; a
  * sequence owns the pages listed in its row of an int32 block table
  * [batch][max_pages]; token slot t of sequence b lives in page
  * block_table[b][t / page_size], row t % page_size.  Supported here:
- * head_dim = 128, page_size = 16, num_q_heads / num_kv_heads <= 8.
+ * head_dim = 128, num_q_heads / num_kv_heads <= 8, and page_size 16, 32,
+ * 64, 128 or 256 for the decode step, the H2O evict, the keep-list
+ * compaction and the sparse decode (the kernels address a page in 16-token
+ * tiles); SnapKV, Quest and the decode step's block signal take page_size
+ * 16 only (else KVSEL_ERR_UNSUPPORTED).
  */
 #ifndef KVSEL_H
 #define KVSEL_H
@@ -65,7 +69,7 @@ typedef struct kvsel_paged_kv {
   int32_t num_kv_heads;
   int32_t num_q_heads;   /* q head h reads kv head h / (num_q_heads/num_kv_heads) */
   int32_t head_dim;      /* 128                                                 */
-  int32_t page_size;     /* 16                                                  */
+  int32_t page_size;     /* 16, 32, 64, 128 or 256 (see above for which calls)  */
 } kvsel_paged_kv;
 
 /* Human-readable reason for the last non-OK status returned on this thread. */

@@ -75,8 +75,8 @@ class DecodeState:
         self.link = link
         self.dev = dev
         npages = wl.num_pages + spare_pages
-        self.kpool = bf16(workloads.paged_pool(wl.K, wl.block_table, npages), dev)
-        self.vpool = bf16(workloads.paged_pool(wl.V, wl.block_table, npages), dev)
+        self.kpool = bf16(workloads.paged_pool(wl.K, wl.block_table, npages, wl.page), dev)
+        self.vpool = bf16(workloads.paged_pool(wl.V, wl.block_table, npages, wl.page), dev)
         self.kv = K.paged_kv(self.kpool, self.vpool, wl.Hq)
         self.bt_host = wl.block_table.copy()
         self.bt = torch.from_numpy(self.bt_host).to(dev)
@@ -105,7 +105,7 @@ class DecodeState:
         """Give every sequence a page for its next slot (host-side allocator)."""
         changed = False
         for b in range(self.wl.B):
-            p = int(self.S[b]) // 16
+            p = int(self.S[b]) // self.wl.page
             if self.bt_host[b, p] < 0:
                 self.bt_host[b, p] = self.free.pop()
                 changed = True

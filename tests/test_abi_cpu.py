@@ -83,7 +83,8 @@ def _decode_status(lib, kv, **over):
 def test_decode_host_validation(lib):
     assert _decode_status(lib, _kv(k_pool=None)) == K.KVSEL_ERR_INVALID_ARG
     assert _decode_status(lib, _kv(head_dim=64)) == K.KVSEL_ERR_UNSUPPORTED
-    assert _decode_status(lib, _kv(page_size=32)) == K.KVSEL_ERR_UNSUPPORTED
+    for bad_page in (8, 24, 48, 512):                           # 16, 32, 64, 128, 256 are accepted
+        assert _decode_status(lib, _kv(page_size=bad_page)) == K.KVSEL_ERR_UNSUPPORTED
     assert _decode_status(lib, _kv(num_q_heads=160, num_kv_heads=8)) == K.KVSEL_ERR_UNSUPPORTED
     assert _decode_status(lib, _kv(num_q_heads=12)) == K.KVSEL_ERR_INVALID_ARG
     assert _decode_status(lib, _kv(), k_new=16) == K.KVSEL_ERR_INVALID_ARG
@@ -253,7 +254,8 @@ def test_kv_compact_host_validation(lib):
                                     a["freed"], a["ws"], a["ws_bytes"], None)
     assert st(kv_=_kv(v_pool=None)) == K.KVSEL_ERR_INVALID_ARG
     assert st(kv_=_kv(k_pool=8)) == K.KVSEL_ERR_INVALID_ARG          # misaligned pool
-    assert st(kv_=_kv(page_size=256)) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(kv_=_kv(page_size=512)) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(kv_=_kv(page_size=48)) == K.KVSEL_ERR_UNSUPPORTED
     assert st(keep=None) == K.KVSEL_ERR_INVALID_ARG
     assert st(stride=0) == K.KVSEL_ERR_INVALID_ARG
     assert st(scores=16) == K.KVSEL_ERR_INVALID_ARG                  # scores without max_len

@@ -83,6 +83,40 @@ def test_ragged_lengths_and_page_tails(S0):
     _check_step(st, wl)
 
 
+@pytest.mark.parametrize("page", [32, 256])
+@pytest.mark.parametrize("S0", [0, 255, 256, 1000])
+def test_larger_pages(page, S0):
+    """Pool pages of 32 or 256 tokens (PagedAttention's blocks are 16 or 256): the append lands in
+    the right row of a big page, ragged tails, permuted pages, a split that cuts pages."""
+    wl = workloads.decode_custom(seed=60 + S0, B=2, Hq=32, Hkv=4, d=128, S0=S0, steps=1, budget=8,
+                                 n_sink=0, window=8, permute_pages=True, page=page)
+    st = DecodeState(wl)
+    st.decode(0, num_ctas=5)
+    torch.cuda.synchronize()
+    assert st.status() == (0, 0)
+    _check_step(st, wl)
+    assert st.seq.cpu().tolist() == [S0 + 1] * wl.B
+
+
+def test_256_token_pages_across_a_page_boundary():
+    """Several steps whose appends cross from one 256-token page into the next, 70B head groups."""
+    wl = workloads.decode_custom(seed=71, B=2, Hq=64, Hkv=8, d=128, S0=8190, steps=4, budget=8,
+                                 n_sink=0, window=8, permute_pages=True, page=256)
+    st = DecodeState(wl)
+    for t in range(wl.steps):
+        st.decode(t)
+        torch.cuda.synchronize()
+        assert st.status() == (0, 0)
+    S = wl.S0 + wl.steps
+    for b in range(wl.B):
+        Kb = np.concatenate([bf16_bits_to_f64(wl.K[b]), bf16_bits_to_f64(wl.k_new[:, b]).transpose(1, 0, 2)], axis=1)
+        Vb = np.concatenate([bf16_bits_to_f64(wl.V[b]), bf16_bits_to_f64(wl.v_new[:, b]).transpose(1, 0, 2)], axis=1)
+        assert Kb.shape[1] == S
+        o, p = decode_attention(bf16_bits_to_f64(wl.q[wl.steps - 1, b]), Kb, Vb, wl.scale)
+        assert rel_l2(st.out[b].double().cpu().numpy(), o) < TOL
+        assert rel_l2(st.probs[b, :, :S].double().cpu().numpy(), p) < TOL
+
+
 def test_single_token_returns_its_value():
     wl = workloads.decode_custom(seed=3, B=1, Hq=16, Hkv=8, d=128, S0=0, steps=1, budget=8,
                                  n_sink=0, window=8)

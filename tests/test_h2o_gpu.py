@@ -129,9 +129,11 @@ def test_all_equal_scores_keep_lowest_candidates():
     assert got[0, 0].tolist() == list(range(14)) + list(range(44, 50))
 
 
-def test_compaction_moves_rows_exactly():
+@pytest.mark.parametrize("page", [16, 64, 256])
+def test_compaction_moves_rows_exactly(page):
     wl = workloads.decode_custom(seed=12, B=2, Hq=16, Hkv=8, d=128, S0=700, steps=1, budget=300,
-                                 n_sink=4, window=40, permute_pages=True)
+                                 n_sink=4, window=40, permute_pages=True, page=page)
+    P = wl.page
     st = DecodeState(wl, spare_pages=4)
     rng = np.random.default_rng(3)
     cum = rng.random((wl.B, wl.Hkv, wl.max_len), dtype=np.float32)
@@ -152,13 +154,13 @@ def test_compaction_moves_rows_exactly():
             keep = h2o_keep(cum[b, h], wl.S0, wl.budget, wl.n_sink, wl.window)
             assert keep_out[b, h].tolist() == pos_before[b, h, keep].tolist()
             for i, src in enumerate(keep):
-                ps, pd = bt_before[b, src // 16], st.bt_host[b, i // 16]
-                assert np.array_equal(kn[pd, h, i % 16], k_before[ps, h, src % 16])
-                assert np.array_equal(vn[pd, h, i % 16], v_before[ps, h, src % 16])
+                ps, pd = bt_before[b, src // P], st.bt_host[b, i // P]
+                assert np.array_equal(kn[pd, h, i % P], k_before[ps, h, src % P])
+                assert np.array_equal(vn[pd, h, i % P], v_before[ps, h, src % P])
             np.testing.assert_array_equal(cn[b, h, :wl.budget], cum[b, h, keep])
             np.testing.assert_array_equal(pn[b, h, :wl.budget], pos_before[b, h, keep])
-    new_pages = (wl.budget + 15) // 16
-    old_pages = (wl.S0 + 15) // 16
+    new_pages = (wl.budget + P - 1) // P
+    old_pages = (wl.S0 + P - 1) // P
     assert (st.bt_host[:, new_pages:old_pages] == -1).all()
     fr = st.freed.cpu().numpy()
     for b in range(wl.B):
@@ -238,10 +240,10 @@ def test_70b_shape_evict_every_step_end_to_end():
     assert swaps <= 32, swaps
 
 
-@pytest.mark.parametrize("link", [False, True])
-def test_custom_config_evict_every_step_permuted_pages(link):
+@pytest.mark.parametrize("link,page", [(False, 16), (True, 16), (True, 256), (False, 32)])
+def test_custom_config_evict_every_step_permuted_pages(link, page):
     wl = workloads.decode_custom(seed=77, B=3, Hq=64, Hkv=8, d=128, S0=500, steps=12, budget=200,
-                                 n_sink=4, window=33, permute_pages=True)
+                                 n_sink=4, window=33, permute_pages=True, page=page)
     _run_mode_a(wl, wl.steps, link=link)
 
 

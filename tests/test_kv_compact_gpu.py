@@ -27,24 +27,25 @@ PAGE = 16
 class PagedBatch:
     """A paged cache of random bf16 rows with permuted pages and spare pages."""
 
-    def __init__(self, seed, S_list, Hkv, spare=3, max_len=None):
+    def __init__(self, seed, S_list, Hkv, spare=3, max_len=None, page=PAGE):
         rng = np.random.default_rng(seed)
         self.rng = rng
+        self.page = P = page
         self.S = list(S_list)
         self.B, self.Hkv = len(S_list), Hkv
         self.max_len = max_len or max(max(S_list), 1)
-        self.max_pages = (self.max_len + PAGE - 1) // PAGE
-        used = sum((s + PAGE - 1) // PAGE for s in S_list)
+        self.max_pages = (self.max_len + P - 1) // P
+        used = sum((s + P - 1) // P for s in S_list)
         self.num_pages = used + spare
         ids = rng.permutation(self.num_pages).astype(np.int32)
         self.bt = np.full((self.B, self.max_pages), -1, dtype=np.int32)
         o = 0
         for b, s in enumerate(S_list):
-            n = (s + PAGE - 1) // PAGE
+            n = (s + P - 1) // P
             self.bt[b, :n] = ids[o:o + n]
             o += n
-        self.kbits = rng.integers(0, 1 << 16, (self.num_pages, Hkv, PAGE, 128), dtype=np.uint16)
-        self.vbits = rng.integers(0, 1 << 16, (self.num_pages, Hkv, PAGE, 128), dtype=np.uint16)
+        self.kbits = rng.integers(0, 1 << 16, (self.num_pages, Hkv, P, 128), dtype=np.uint16)
+        self.vbits = rng.integers(0, 1 << 16, (self.num_pages, Hkv, P, 128), dtype=np.uint16)
         self.scores = rng.random((self.B, Hkv, self.max_len), dtype=np.float32)
         self.pos = rng.integers(0, 1 << 30, (self.B, Hkv, self.max_len), dtype=np.int32)
 
@@ -52,7 +53,7 @@ class PagedBatch:
         bt = self.bt if bt is None else bt
         out = np.zeros((self.Hkv, S, 128), dtype=np.uint16)
         for t in range(S):
-            out[:, t] = pool[bt[b, t // PAGE], :, t % PAGE]
+            out[:, t] = pool[bt[b, t // self.page], :, t % self.page]
         return out
 
     def upload(self, g):
@@ -87,7 +88,8 @@ def _check_sequence(pb, b, keep_rows, kn, vn, bt_new, scores_new, pos_new, freed
     np.testing.assert_array_equal(got_v, ref.V)
     np.testing.assert_array_equal(scores_new[b, :, :n].astype(np.float64), ref.cum)
     np.testing.assert_array_equal(pos_new[b, :, :n].astype(np.int64), ref.pos)
-    old_p, new_p = (pb.S[b] + PAGE - 1) // PAGE, (n + PAGE - 1) // PAGE
+    P = pb.page
+    old_p, new_p = (pb.S[b] + P - 1) // P, (n + P - 1) // P
     np.testing.assert_array_equal(bt_new[b, :new_p], pb.bt[b, :new_p])
     assert (bt_new[b, new_p:old_p] == -1).all()
     np.testing.assert_array_equal(bt_new[b, old_p:], pb.bt[b, old_p:])
@@ -106,14 +108,14 @@ def _random_rows(rng, S, n, Hkv, structured):
     return [r.astype(np.int32) for r in rows]
 
 
-@pytest.mark.parametrize("with_count", [True, False])
-def test_random_keep_lists_move_bytes_exactly(with_count):
+@pytest.mark.parametrize("with_count,page", [(True, 16), (False, 16), (True, 256), (False, 64)])
+def test_random_keep_lists_move_bytes_exactly(with_count, page):
     # ragged tails, a whole page kept exactly, an empty keep, a 3-chunk row,
-    # identity rows (nothing moves) and a zero-length sequence
+    # identity rows (nothing moves) and a zero-length sequence; pages of 16 to 256 tokens
     S_list = [700, 33, 1000, 5, 16, 0, 611]
     n_list = [300, 17, 999, 0, 16, 0, 611]
     Hkv = 4
-    pb = PagedBatch(11 + with_count, S_list, Hkv)
+    pb = PagedBatch(11 + with_count, S_list, Hkv, page=page)
     stride = max(n_list) + 5
     keep = np.full((pb.B, Hkv, stride), -1, dtype=np.int32)
     counts = np.zeros((pb.B, Hkv), dtype=np.int32)

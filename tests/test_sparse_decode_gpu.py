@@ -25,8 +25,8 @@ class SparseState:
     def __init__(self, wl, out_f32=True):
         self.wl = wl
         dev = "cuda"
-        self.kpool = bf16(workloads.paged_pool(wl.K, wl.block_table, wl.num_pages))
-        self.vpool = bf16(workloads.paged_pool(wl.V, wl.block_table, wl.num_pages))
+        self.kpool = bf16(workloads.paged_pool(wl.K, wl.block_table, wl.num_pages, wl.page))
+        self.vpool = bf16(workloads.paged_pool(wl.V, wl.block_table, wl.num_pages, wl.page))
         self.kv = K.paged_kv(self.kpool, self.vpool, wl.Hq)
         self.bt = torch.from_numpy(wl.block_table).to(dev)
         self.seq = torch.full((wl.B,), wl.S0, dtype=torch.int32, device=dev)
@@ -98,6 +98,19 @@ def test_three_steps_multi_chunk():
         st.step(t)
         _check(st, t)
     assert st.seq.cpu().tolist() == [40003, 40003]
+    assert K.read_status(st.ws) == 0
+
+
+@pytest.mark.parametrize("page", [64, 256])
+def test_larger_pages_across_a_page_boundary(page):
+    """Pool pages of 64 or 256 tokens: appends crossing into a new page, the selected rows resolved
+    through the bigger pages (every kv head's row at its own offset in the page)."""
+    wl = workloads.sparse_decode(seed=24, B=2, S0=20478, steps=3, top_k=700, page=page)
+    st = SparseState(wl)
+    for t in range(3):
+        st.step(t)
+        _check(st, t)
+    assert st.seq.cpu().tolist() == [20481, 20481]
     assert K.read_status(st.ws) == 0
 
 

@@ -55,19 +55,19 @@ def _unit(v: np.ndarray) -> np.ndarray:
     return v / np.linalg.norm(v)
 
 
-def paged_pool(logical: np.ndarray, block_table: np.ndarray, num_pages: int) -> np.ndarray:
-    """Scatter logical ``[B][Hkv][S][d]`` rows into a ``[pages][Hkv][16][d]`` pool.
+def paged_pool(logical: np.ndarray, block_table: np.ndarray, num_pages: int, page: int = PAGE) -> np.ndarray:
+    """Scatter logical ``[B][Hkv][S][d]`` rows into a ``[pages][Hkv][page][d]`` pool.
 
-    Token ``t`` of sequence ``b`` goes to page ``block_table[b][t // 16]``,
-    row ``t % 16``.  Unused pool rows are zero.
+    Token ``t`` of sequence ``b`` goes to page ``block_table[b][t // page]``,
+    row ``t % page``.  Unused pool rows are zero.
     """
     B, Hkv, S, d = logical.shape
-    pool = np.zeros((num_pages, Hkv, PAGE, d), dtype=logical.dtype)
-    npg = (S + PAGE - 1) // PAGE
+    pool = np.zeros((num_pages, Hkv, page, d), dtype=logical.dtype)
+    npg = (S + page - 1) // page
     for b in range(B):
-        full = np.zeros((Hkv, npg * PAGE, d), dtype=logical.dtype)
+        full = np.zeros((Hkv, npg * page, d), dtype=logical.dtype)
         full[:, :S] = logical[b]
-        pages = full.reshape(Hkv, npg, PAGE, d).transpose(1, 0, 2, 3)
+        pages = full.reshape(Hkv, npg, page, d).transpose(1, 0, 2, 3)
         pool[block_table[b, :npg]] = pages
     return pool
 
@@ -98,6 +98,7 @@ class DecodeWorkload:
     v_new: np.ndarray
     seed: int = 0
     extra: dict = field(default_factory=dict)
+    page: int = PAGE                 # tokens per pool page
 
     @property
     def G(self) -> int:
@@ -109,10 +110,10 @@ class DecodeWorkload:
 
 
 def _decode_workload(name, seed, B, Hq, Hkv, d, S0, steps, budget, n_sink, window,
-                     permute_pages, plant_sink):
+                     permute_pages, plant_sink, page=PAGE):
     rng = np.random.default_rng(seed)
     max_len = S0 + steps
-    max_pages = (max_len + PAGE - 1) // PAGE
+    max_pages = (max_len + page - 1) // page
     num_pages = B * max_pages
     if permute_pages:
         block_table = rng.permutation(num_pages).astype(np.int32).reshape(B, max_pages)
@@ -140,7 +141,7 @@ def _decode_workload(name, seed, B, Hq, Hkv, d, S0, steps, budget, n_sink, windo
         Kf[b] = None
     return DecodeWorkload(name, B, Hq, Hkv, d, S0, steps, budget, n_sink, window,
                           max_len, max_pages, num_pages, block_table, K, V, q,
-                          k_new, v_new, seed)
+                          k_new, v_new, seed, page=page)
 
 
 def decode_small(seed: int = 0, S0: int = 1600, steps: int = 64) -> DecodeWorkload:
@@ -162,9 +163,9 @@ def decode_70b(seed: int = 1, B: int = 8, S0: int = 32768, steps: int = 128) -> 
 
 
 def decode_custom(seed, B, Hq, Hkv, d, S0, steps, budget, n_sink, window,
-                  permute_pages=True, plant_sink=False, name="decode_custom"):
+                  permute_pages=True, plant_sink=False, name="decode_custom", page=PAGE):
     return _decode_workload(name, seed, B, Hq, Hkv, d, S0, steps, budget, n_sink,
-                            window, permute_pages, plant_sink)
+                            window, permute_pages, plant_sink, page)
 
 
 # ----------------------------------------------------------------------------
@@ -325,6 +326,7 @@ class SparseDecodeWorkload:
     w_idx: np.ndarray         # fp32 [steps][B][Hi]
     k_idx_new: np.ndarray     # bf16 bits [steps][B][Di]
     seed: int
+    page: int = PAGE          # tokens per pool page
 
     @property
     def G(self) -> int:
@@ -337,10 +339,10 @@ class SparseDecodeWorkload:
 
 def sparse_decode(seed: int = 4, B: int = 4, S0: int = 131072, steps: int = 64,
                   Hq: int = 64, Hkv: int = 8, d: int = 128, Hi: int = 4, Di: int = 64,
-                  top_k: int = 2048) -> SparseDecodeWorkload:
+                  top_k: int = 2048, page: int = PAGE) -> SparseDecodeWorkload:
     rng = np.random.default_rng(seed)
     max_len = S0 + steps
-    max_pages = (max_len + PAGE - 1) // PAGE
+    max_pages = (max_len + page - 1) // page
     num_pages = B * max_pages
     bt = rng.permutation(num_pages).astype(np.int32).reshape(B, max_pages)
     K = np.empty((B, Hkv, S0, d), dtype=np.uint16)
@@ -357,4 +359,4 @@ def sparse_decode(seed: int = 4, B: int = 4, S0: int = 131072, steps: int = 64,
     k_idx_new = normal_bf16(rng, (steps, B, Di))
     return SparseDecodeWorkload("sparse_decode_70b", B, Hq, Hkv, d, S0, steps, Hi, Di, top_k,
                                 max_len, max_pages, num_pages, bt, K, V, k_idx, q, k_new,
-                                v_new, q_idx, w_idx, k_idx_new, seed)
+                                v_new, q_idx, w_idx, k_idx_new, seed, page=page)
