@@ -21,8 +21,9 @@
 // stages; warps 0..3 take the ring's stages round-robin.  (A producer's
 // issue loop costs a fixed few hundred cycles per stage, so one-page stages
 // or a single producer warp could not keep up with HBM.)
-//   * K pass: S = Q K^T with mma.sync m16n8k16 (A = the group's q rows, at
-//     most 8 real; B = 16 keys via ldmatrix); the scaled log2-domain logits
+//   * K pass: S = Q K^T with mma.sync m16n8k16 (A = the group's q rows, up
+//     to 16: head g in row g, head g + 8 in row g + 8; B = 16 keys via
+//     ldmatrix); the scaled log2-domain logits
 //     are stored to the probability buffer, marked evict-last so they are
 //     still in L2 for the V pass, and each lane keeps a running (max, sum of
 //     exp2) of its keys.  At a segment end the CTA writes the segment's
@@ -36,9 +37,10 @@
 //     p = exp2(s - M) / L, writes them (evict-first), adds the group's sum
 //     into the H2O score (collecting the H2O candidates of the next
 //     selection), and
-//     accumulates O += P V with P split into a bf16 high part (A rows 0..7)
-//     and its bf16 residual (rows 8..15), so P keeps ~16 mantissa bits at no
-//     extra MMA cost.  The segment's O, already normalised, is added into
+//     accumulates O += P V with P split into a bf16 high part and its bf16
+//     residual, so P keeps ~16 mantissa bits: with up to 8 heads the high
+//     parts fill A rows 0..7 and the residuals rows 8..15 (no extra MMA);
+//     with more, a second MMA adds the residuals.  The segment's O, already normalised, is added into
 //     the pair's fp32 accumulator; the owner that adds last writes O and
 //     clears the accumulator, so no owner waits for another at the end.
 // The normalisation work therefore overlaps the V stream instead of trailing
@@ -63,7 +65,8 @@ constexpr int kProducerWarps = 2;  // alternate stages: the issue loop's fixed c
 constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kPageBytes = 4096;   // 16 rows x 128 bf16, as two 2 KB swizzled halves
 constexpr int kStageBytes = 2 * kPageBytes;
-constexpr int kMaxG = 8;
+constexpr int kMaxG = 16;   // q heads per kv head: rows g and g + 8 of the MMA tiles
+constexpr int kRowG = 8;    // q heads whose O one merge round moves (the A tile's first 8 rows)
 constexpr int kMaxCtas = 1024;
 // Consumer warp w takes the stages t with t % kConsumerWarps == w, so with a
 // ring depth that is a multiple of the warp count a stage is always used by
@@ -71,19 +74,19 @@ constexpr int kMaxCtas = 1024;
 static_assert(kStages % kConsumerWarps == 0, "ring depth must be a multiple of the consumer warps");
 static_assert(kStages % kProducerWarps == 0, "a ring slot must always have the same producer");
 constexpr int kMaxBatch = 1024;
-constexpr int kPartFloats = kMaxG * (kD + 2);  // one partial slot: m[8], l[8], O[8][128]
+constexpr int kPartFloats = 2 * kMaxG;  // one partial slot: m[16], l[16] of an owner's segment
 constexpr int kMaxOwners = kMaxCtas;           // CTAs sharing one (sequence, kv head) pair
 constexpr int kWarpCands = 256;                // H2O candidates a consumer warp stages
 
 struct SmemLayout {
   static constexpr size_t ring = 0;
-  static constexpr size_t merge_o = ring + size_t(kStages) * kStageBytes;                // [4][8][128] f32
-  static constexpr size_t merge_ml = merge_o + size_t(kConsumerWarps) * kMaxG * kD * 4;  // [4][8][2] f32
+  static constexpr size_t merge_o = ring + size_t(kStages) * kStageBytes;                // [4][8][128] f32 (8 heads a round)
+  static constexpr size_t merge_ml = merge_o + size_t(kConsumerWarps) * kRowG * kD * 4;  // [4][16][2] f32
   static constexpr size_t cands = merge_ml + size_t(kConsumerWarps) * kMaxG * 2 * 4;    // [4][256] u32 + i32
   static constexpr size_t bars = cands + size_t(kConsumerWarps) * kWarpCands * 8;        // 2 x kStages u64
   static constexpr size_t seqS = bars + 2 * kStages * 8;                                 // [kMaxBatch] i32
   static constexpr size_t seqPref = seqS + size_t(kMaxBatch) * 4;                        // [kMaxBatch+1] i64
-  static constexpr size_t stats = seqPref + size_t(kMaxBatch + 1) * 8;                   // [8][2] f32
+  static constexpr size_t stats = seqPref + size_t(kMaxBatch + 1) * 8;                   // [16][2] f32
   static constexpr size_t owners = stats + kMaxG * 2 * 4;                                // [kMaxOwners+1] i32
   static constexpr size_t sig = owners + (kMaxOwners + 1) * 4;                           // i32: segment completed its pair
   static constexpr size_t sigseqs = sig + 16;                                            // [kMaxBatch/32] u32 bitmap
@@ -478,8 +481,9 @@ __device__ __noinline__ void block_signal(const StepParams& P, int b, int S, uin
 }
 
 // kSig: the per-step block signal is on (P.bmass and the rest set); the
-// default instantiation carries none of its code.
-template <bool kSig>
+// default instantiation carries none of its code.  kWide: more than 8 q
+// heads per kv head (up to 16).
+template <bool kSig, bool kWide>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const StepParams P) {
@@ -588,6 +592,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
   const int nsk = (n + 1) >> 1;     // stages per pass
   const int g = lane >> 2, qd = lane & 3;
   const bool head_ok = g < G;
+  const bool head_ok2 = kWide && g + kRowG < G;  // rows 8..15 carry head g + 8
   const bool vec2 = P.vec2 != 0;
   const int k0 = 2 * qd, k2 = 8 + 2 * qd;  // this lane's keys in a page: k0, k0+1, k2, k2+1
 
@@ -674,18 +679,25 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       const long long seg_end = min(u1, u + (np - pg));
       const int pair = b * Hkv + kvh;
 
-      uint32_t qa[8][2];
+      // A rows: head g in rows 0..7; with more than 8 heads, head g + 8 in rows 8..15
+      uint32_t qa[8][2], qb[8][2];
       {
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
             P.q + (size_t(b) * P.Hq + kvh * G + (head_ok ? g : 0)) * kD);
+        const uint32_t* qrow2 = reinterpret_cast<const uint32_t*>(
+            P.q + (size_t(b) * P.Hq + kvh * G + (head_ok2 ? g + kRowG : 0)) * kD);
 #pragma unroll
         for (int kt = 0; kt < 8; ++kt) {
           qa[kt][0] = head_ok ? qrow[(16 * kt + 2 * qd) >> 1] : 0u;
           qa[kt][1] = head_ok ? qrow[(16 * kt + 8 + 2 * qd) >> 1] : 0u;
+          qb[kt][0] = head_ok2 ? qrow2[(16 * kt + 2 * qd) >> 1] : 0u;
+          qb[kt][1] = head_ok2 ? qrow2[(16 * kt + 8 + 2 * qd) >> 1] : 0u;
         }
       }
       float* lrow = head_ok ? P.logits + (size_t(b) * P.Hq + kvh * G + g) * P.max_len : nullptr;
-      float m_l = -INFINITY, l_l = 0.f;  // this lane's keys of the segment
+      float* lrow2 = head_ok2 ? P.logits + (size_t(b) * P.Hq + kvh * G + g + kRowG) * P.max_len : nullptr;
+      float m_l = -INFINITY, l_l = 0.f;    // this lane's keys of the segment, head g
+      float m_l2 = -INFINITY, l_l2 = 0.f;  // head g + 8
 
       const int i_begin = int(u - u0), i_end = int(seg_end - u0);
 #pragma unroll 1
@@ -703,8 +715,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           const int uu = 2 * kt + (mi & 1);
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kb + tile_off(key, uu), b0, b1, b2, b3);
-          mma_bf16_16816(s0, qa[kt][0], 0u, qa[kt][1], 0u, b0, b1);
-          mma_bf16_16816(s1, qa[kt][0], 0u, qa[kt][1], 0u, b2, b3);
+          mma_bf16_16816(s0, qa[kt][0], qb[kt][0], qa[kt][1], qb[kt][1], b0, b1);
+          mma_bf16_16816(s1, qa[kt][0], qb[kt][0], qa[kt][1], qb[kt][1], b2, b3);
         }
         __syncwarp();
         if ((i & 1) || i + 1 == n)  // the stage's last page: its K rows are in registers now
@@ -712,19 +724,25 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 
         const int key0 = (pg + (i - i_begin)) * kPage;
         const int valid = S - key0;  // >= 1
-        float4 x;
-        x.x = k0 < valid ? s0[0] * P.scale_log2 : -INFINITY;
-        x.y = k0 + 1 < valid ? s0[1] * P.scale_log2 : -INFINITY;
-        x.z = k2 < valid ? s1[0] * P.scale_log2 : -INFINITY;
-        x.w = k2 + 1 < valid ? s1[1] * P.scale_log2 : -INFINITY;
-        if (lrow) store_keys(lrow, key0, valid, k0, k2, vec2, x, keep_l2);  // read back by the V pass
-        const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
-        if (mx != -INFINITY) {
-          const float m_new = fmaxf(m_l, mx);
-          l_l = l_l * ex2(m_l - m_new) + ((ex2(x.x - m_new) + ex2(x.y - m_new)) +
-                                          (ex2(x.z - m_new) + ex2(x.w - m_new)));
-          m_l = m_new;
-        }
+        // one head's four logits of the page: stored (read back by the V pass) and folded
+        // into the lane's running (max, sum of exp2)
+        auto fold = [&](float a, float bq, float cq, float dq, float* row, float& m, float& l) {
+          float4 x;
+          x.x = k0 < valid ? a * P.scale_log2 : -INFINITY;
+          x.y = k0 + 1 < valid ? bq * P.scale_log2 : -INFINITY;
+          x.z = k2 < valid ? cq * P.scale_log2 : -INFINITY;
+          x.w = k2 + 1 < valid ? dq * P.scale_log2 : -INFINITY;
+          if (row) store_keys(row, key0, valid, k0, k2, vec2, x, keep_l2);
+          const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+          if (mx != -INFINITY) {
+            const float m_new = fmaxf(m, mx);
+            l = l * ex2(m - m_new) + ((ex2(x.x - m_new) + ex2(x.y - m_new)) +
+                                      (ex2(x.z - m_new) + ex2(x.w - m_new)));
+            m = m_new;
+          }
+        };
+        fold(s0[0], s0[1], s1[0], s1[1], lrow, m_l, l_l);
+        if (kWide) fold(s0[2], s0[3], s1[2], s1[3], lrow2, m_l2, l_l2);
       }
 
       // ---- the segment's (m, l) per head: over the head's 4 lanes, then the 4 warps ----
@@ -733,10 +751,19 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         const float mo = __shfl_xor_sync(0xffffffffu, m_l, off);
         const float lo = __shfl_xor_sync(0xffffffffu, l_l, off);
         ml_merge(m_l, l_l, mo, lo);
+        if (kWide) {
+          const float mo2 = __shfl_xor_sync(0xffffffffu, m_l2, off);
+          const float lo2 = __shfl_xor_sync(0xffffffffu, l_l2, off);
+          ml_merge(m_l2, l_l2, mo2, lo2);
+        }
       }
       if (qd == 0 && head_ok) {
         wml[(warp * kMaxG + g) * 2 + 0] = m_l;
         wml[(warp * kMaxG + g) * 2 + 1] = l_l;
+      }
+      if (qd == 0 && head_ok2) {
+        wml[(warp * kMaxG + g + kRowG) * 2 + 0] = m_l2;
+        wml[(warp * kMaxG + g + kRowG) * 2 + 1] = l_l2;
       }
       consumer_sync();
       if (tid < G) {
@@ -792,6 +819,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       const size_t hrow = (size_t(b) * P.Hq + kvh * G + g) * P.max_len;
       const float* lrow = head_ok ? P.logits + hrow : nullptr;
       float* prow = (head_ok && P.probs) ? P.probs + hrow : nullptr;
+      const float* lrow2 = head_ok2 ? P.logits + hrow + size_t(kRowG) * P.max_len : nullptr;  // head g + 8
+      float* prow2 = (head_ok2 && P.probs) ? P.probs + hrow + size_t(kRowG) * P.max_len : nullptr;
       float* crow = P.cum ? P.cum + (size_t(b) * Hkv + kvh) * P.max_len : nullptr;
       const bool cown = crow != nullptr && csum_lane;
       // the row's last H2O threshold: collect the slots at or above it (0: no list)
@@ -799,21 +828,23 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 
       const int i_begin = int(u - u0), i_end = int(seg_end - u0);
       // the stored logits and old score of one of this warp's pages
-      auto fetch = [&](int ii, float4& lg, float& cs) {
+      auto fetch = [&](int ii, float4& lg, float4& lg2, float& cs) {
         lg = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        lg2 = lg;
         cs = 0.f;
         if (ii < i_end) {
           const int key0 = (pg + (ii - i_begin)) * kPage;
           const int valid = S - key0;
           if (lrow) lg = load_keys(lrow, key0, valid, k0, k2, vec2, -INFINITY);
+          if (kWide && lrow2) lg2 = load_keys(lrow2, key0, valid, k0, k2, vec2, -INFINITY);
           if (cown && kc < valid) cs = __ldcg(crow + key0 + kc);
         }
       };
       int i = first_page(i_begin, nsk);
-      float4 lgA, lgB;
+      float4 lgA, lgB, lgA2, lgB2;
       float csA, csB;
-      fetch(i, lgA, csA);  // two pages ahead: issued before the wait below
-      fetch(next_page(i), lgB, csB);
+      fetch(i, lgA, lgA2, csA);  // two pages ahead: issued before the wait below
+      fetch(next_page(i), lgB, lgB2, csB);
       if (tid == 0) {
         const long long pfirst = sPref[b] + (long long)kvh * np;
         const int no = list_owners(sOwn, pfirst, pfirst + np - 1, U, NC);
@@ -842,6 +873,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       consumer_sync();
       const float Mg = head_ok ? sStat[g * 2] : 0.f;
       const float Ig = head_ok ? sStat[g * 2 + 1] : 0.f;
+      const float Mg2 = head_ok2 ? sStat[(g + kRowG) * 2] : 0.f;
+      const float Ig2 = head_ok2 ? sStat[(g + kRowG) * 2 + 1] : 0.f;
 
       float o[16][4];
 #pragma unroll
@@ -849,11 +882,12 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 
 #pragma unroll 1
       for (; i < i_end && alive; i = next_page(i)) {
-        const float4 lg = lgA;
+        const float4 lg = lgA, lg2 = lgA2;
         const float cs = csA;
         lgA = lgB;
+        lgA2 = lgB2;
         csA = csB;
-        fetch(next_page(next_page(i)), lgB, csB);
+        fetch(next_page(next_page(i)), lgB, lgB2, csB);
         const int t = nsk + (i >> 1), s = t % kStages;
         if (!mbar_wait(smem_u32(&full[s]), (t / kStages) & 1, P.status)) {
           alive = false;
@@ -867,14 +901,24 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         const float p0 = ex2(lg.x - Mg) * Ig, p1 = ex2(lg.y - Mg) * Ig;
         const float p2 = ex2(lg.z - Mg) * Ig, p3 = ex2(lg.w - Mg) * Ig;
         if (prow) store_keys(prow, key0, valid, k0, k2, vec2, make_float4(p0, p1, p2, p3), drop_l2);
+        float p4 = 0.f, p5 = 0.f, p6 = 0.f, p7 = 0.f;  // head g + 8
+        if (kWide) {
+          p4 = ex2(lg2.x - Mg2) * Ig2;
+          p5 = ex2(lg2.y - Mg2) * Ig2;
+          p6 = ex2(lg2.z - Mg2) * Ig2;
+          p7 = ex2(lg2.w - Mg2) * Ig2;
+          if (prow2) store_keys(prow2, key0, valid, k0, k2, vec2, make_float4(p4, p5, p6, p7), drop_l2);
+        }
         if (kSig || crow) {
-          // the group's probability per key, a transposing sum over the 8 head
-          // rows: lanes of heads with bit 2 set keep keys k2, k2 + 1, the others
-          // k0, k0 + 1; bit 1 then picks one of the two; bit 0 completes the sum
+          // the group's probability per key (heads g and g + 8 first added in
+          // the lane), a transposing sum over the 8 head rows: lanes of heads
+          // with bit 2 set keep keys k2, k2 + 1, the others k0, k0 + 1; bit 1
+          // then picks one of the two; bit 0 completes the sum
+          const float q0 = p0 + p4, q1 = p1 + p5, q2 = p2 + p6, q3 = p3 + p7;
           const bool hi4 = (g & 4) != 0, hi2 = (g & 2) != 0;
-          float a = hi4 ? p2 : p0, bb = hi4 ? p3 : p1;
-          a += __shfl_xor_sync(0xffffffffu, hi4 ? p0 : p2, 16);
-          bb += __shfl_xor_sync(0xffffffffu, hi4 ? p1 : p3, 16);
+          float a = hi4 ? q2 : q0, bb = hi4 ? q3 : q1;
+          a += __shfl_xor_sync(0xffffffffu, hi4 ? q0 : q2, 16);
+          bb += __shfl_xor_sync(0xffffffffu, hi4 ? q1 : q3, 16);
           float x = hi2 ? bb : a;
           x += __shfl_xor_sync(0xffffffffu, hi2 ? a : bb, 8);
           x += __shfl_xor_sync(0xffffffffu, x, 4);
@@ -892,11 +936,21 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
           }
         }
 
-        // O += P V, P as bf16 high part (rows 0..7) + bf16 residual (rows 8..15)
+        // O += P V with P as a bf16 high part plus its bf16 residual.  Up to 8 heads: the
+        // high parts in rows 0..7, the residuals in rows 8..15, one MMA.  More than 8: heads
+        // g and g + 8 in rows g and g + 8, one MMA for the high parts and one for the residuals
+        // into the same accumulators.
         const uint32_t hi01 = pack_bf16x2(p0, p1);
         const uint32_t hi23 = pack_bf16x2(p2, p3);
         const uint32_t lo01 = pack_bf16x2(p0 - bf16lo_to_f32(hi01), p1 - bf16hi_to_f32(hi01));
         const uint32_t lo23 = pack_bf16x2(p2 - bf16lo_to_f32(hi23), p3 - bf16hi_to_f32(hi23));
+        uint32_t hi45 = 0u, hi67 = 0u, lo45 = 0u, lo67 = 0u;
+        if (kWide) {
+          hi45 = pack_bf16x2(p4, p5);
+          hi67 = pack_bf16x2(p6, p7);
+          lo45 = pack_bf16x2(p4 - bf16lo_to_f32(hi45), p5 - bf16hi_to_f32(hi45));
+          lo67 = pack_bf16x2(p6 - bf16lo_to_f32(hi67), p7 - bf16hi_to_f32(hi67));
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int key = (mi & 1) * 8 + r8;
@@ -909,8 +963,15 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             b2 = keep_keys(b2, 2 * qd, valid);
             b3 = keep_keys(b3, 8 + 2 * qd, valid);
           }
-          mma_bf16_16816(o[2 * j], hi01, lo01, hi23, lo23, b0, b1);
-          mma_bf16_16816(o[2 * j + 1], hi01, lo01, hi23, lo23, b2, b3);
+          if (kWide) {
+            mma_bf16_16816(o[2 * j], hi01, hi45, hi23, hi67, b0, b1);
+            mma_bf16_16816(o[2 * j + 1], hi01, hi45, hi23, hi67, b2, b3);
+            mma_bf16_16816(o[2 * j], lo01, lo45, lo23, lo67, b0, b1);
+            mma_bf16_16816(o[2 * j + 1], lo01, lo45, lo23, lo67, b2, b3);
+          } else {
+            mma_bf16_16816(o[2 * j], hi01, lo01, hi23, lo23, b0, b1);
+            mma_bf16_16816(o[2 * j + 1], hi01, lo01, hi23, lo23, b2, b3);
+          }
         }
         __syncwarp();
         if ((i & 1) || i + 1 == n)
@@ -922,17 +983,26 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       // ---- the segment's O (already normalised): the 4 warps' sum, added into the pair's fp32
       // accumulator; the pair's last owner to get here writes O and clears the accumulator, so
       // no owner waits for the others ----
-      if (head_ok) {
-        float* dst = wo + (warp * kMaxG + g) * kD;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt)
-          *reinterpret_cast<float2*>(dst + 8 * nt + 2 * qd) =
-              make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
-      }
-      consumer_sync();
+      // (eight heads a round through the shared buffer: heads 0..7, then 8..15 when the group
+      // is wider)
       float* oacc = P.oacc + (size_t(b) * P.Hq + kvh * G) * kD;
-      for (int idx = tid; idx < G * kD; idx += kConsumerWarps * 32)
-        atomicAdd(oacc + idx, ((wo[idx] + wo[kMaxG * kD + idx]) + wo[2 * kMaxG * kD + idx]) + wo[3 * kMaxG * kD + idx]);
+#pragma unroll 1
+      for (int half = 0; half < (kWide ? 2 : 1); ++half) {
+        const int gh = half * kRowG, hn = min(kRowG, G - gh);  // this round's first head, heads
+        if (g < hn) {
+          float* dst = wo + (warp * kRowG + g) * kD;
+#pragma unroll
+          for (int nt = 0; nt < 16; ++nt)
+            *reinterpret_cast<float2*>(dst + 8 * nt + 2 * qd) =
+                kWide ? (half ? make_float2(o[nt][2], o[nt][3]) : make_float2(o[nt][0], o[nt][1]))
+                      : make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
+        }
+        consumer_sync();
+        for (int idx = tid; idx < hn * kD; idx += kConsumerWarps * 32)
+          atomicAdd(oacc + gh * kD + idx,
+                    ((wo[idx] + wo[kRowG * kD + idx]) + wo[2 * kRowG * kD + idx]) + wo[3 * kRowG * kD + idx]);
+        if (kWide && half == 0) consumer_sync();  // the next round overwrites the buffer
+      }
       __threadfence();
       consumer_sync();
       if (tid == 0) {
@@ -1040,15 +1110,15 @@ size_t decode_sig_bytes(int batch, int Hkv, int max_len) {
 
 // Co-resident CTAs per SM of the kernel instantiation (the launch sizes its
 // grid from it); sets the shared-memory attribute on first use.
-template <bool kSig>
+template <bool kSig, bool kWide>
 int ctas_per_sm() {
   static int cached = 0;
   if (cached) return cached;
-  if (cudaFuncSetAttribute(decode_step_kernel<kSig>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_step_kernel<kSig, kWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmemBytes)) != cudaSuccess)
     return 0;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_step_kernel<kSig>, kThreads, kSmemBytes) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_step_kernel<kSig, kWide>, kThreads, kSmemBytes) !=
       cudaSuccess)
     return 0;
   cached = occ;
@@ -1101,7 +1171,7 @@ extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int
   if (kv->num_kv_heads < 1 || kv->num_q_heads < 1 || kv->num_q_heads % kv->num_kv_heads != 0)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "num_q_heads must be a positive multiple of num_kv_heads");
   const int Hkv = kv->num_kv_heads, Hq = kv->num_q_heads, G = Hq / Hkv;
-  if (G > kMaxG) return fail(KVSEL_ERR_UNSUPPORTED, fn + "at most 8 q heads per kv head are implemented");
+  if (G > kMaxG) return fail(KVSEL_ERR_UNSUPPORTED, fn + "at most 16 q heads per kv head are implemented");
   if (kv->num_pages < 1 || (long long)kv->num_pages * Hkv * kv->page_size >= (1LL << 31))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "num_pages * num_kv_heads * page_size must be in [1, 2^31)");
   if ((long long)max_pages << page_shift_of(kv->page_size) >= (1LL << 31))
@@ -1137,7 +1207,9 @@ extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int
     return fail(KVSEL_ERR_INVALID_ARG, fn + "h2o_link must be a 256-byte aligned H2O evict workspace of at least " +
                                            std::to_string(link_bytes(batch * Hkv)) + " bytes");
 
-  const int occ = signal ? ctas_per_sm<true>() : ctas_per_sm<false>();
+  const bool wide = G > kRowG;
+  const int occ = signal ? (wide ? ctas_per_sm<true, true>() : ctas_per_sm<true, false>())
+                         : (wide ? ctas_per_sm<false, true>() : ctas_per_sm<false, false>());
   if (occ < 1) return fail(KVSEL_ERR_CUDA, fn + "cannot configure the decode kernel (occupancy 0)");
   const int resident = sm_count() * occ;
   const int nc = num_ctas == 0 ? std::min(resident, kMaxCtas) : num_ctas;
@@ -1234,8 +1306,11 @@ extern "C" kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   trace_before("decode_step", st);
-  const cudaError_t e = signal ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true>, tmK, tmV, P)
-                               : cudaLaunchKernelEx(&cfg, decode_step_kernel<false>, tmK, tmV, P);
+  const cudaError_t e =
+      signal ? (wide ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true, true>, tmK, tmV, P)
+                     : cudaLaunchKernelEx(&cfg, decode_step_kernel<true, false>, tmK, tmV, P))
+             : (wide ? cudaLaunchKernelEx(&cfg, decode_step_kernel<false, true>, tmK, tmV, P)
+                     : cudaLaunchKernelEx(&cfg, decode_step_kernel<false, false>, tmK, tmV, P));
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_decode_attn (launch)");
   return KVSEL_OK;

@@ -29,7 +29,8 @@
  * sequence owns the pages listed in its row of an int32 block table
  * [batch][max_pages]; token slot t of sequence b lives in page
  * block_table[b][t / page_size], row t % page_size.  Supported here:
- * head_dim = 128, num_q_heads / num_kv_heads <= 8, and page_size 16, 32,
+ * head_dim = 128; num_q_heads / num_kv_heads <= 16 for the decode step
+ * (and its block signal), <= 8 elsewhere; and page_size 16, 32,
  * 64, 128 or 256 for the decode step, the H2O evict, the keep-list
  * compaction and the sparse decode (the kernels address a page in 16-token
  * tiles); SnapKV, Quest and the decode step's block signal take page_size
@@ -235,7 +236,7 @@ KVSEL_API size_t kvsel_h2o_link_bytes(int batch, int num_kv_heads);
  *  - The first call on a device looks up that array's device address (with
  *    the device current); make that first call before any stream capture.
  *  - Calls that need more scratch than 8 MiB are rejected with
- *    KVSEL_ERR_INVALID_ARG: about (1024 + batch * num_kv_heads) * 4160 bytes
+ *    KVSEL_ERR_INVALID_ARG: about (1024 + batch * num_kv_heads) * 64 bytes
  *    + batch * num_kv_heads * 12 bytes + batch * num_q_heads * 512 bytes (an
  *    fp32 O accumulator), plus batch * num_q_heads * max_len * 4 bytes when
  *    probs is not given (the kernel keeps its logits there).

@@ -94,6 +94,14 @@ def test_ragged_steps_group_of_four():
     _run_and_check(st, 3)
 
 
+def test_group_of_sixteen():
+    """16 q heads per kv head: each block's mass sums all 16 heads' probabilities."""
+    wl = workloads.decode_custom(seed=63, B=2, Hq=64, Hkv=4, d=128, S0=1500, steps=2, budget=1024, n_sink=4,
+                                 window=64)
+    st = SignalState(wl, k=40, spare_pages=8)
+    _run_and_check(st, 2)
+
+
 def test_every_block_when_k_covers_the_sequence():
     wl = workloads.decode_custom(seed=62, B=2, Hq=8, Hkv=8, d=128, S0=500, steps=2, budget=256, n_sink=4,
                                  window=64)

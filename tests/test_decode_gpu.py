@@ -61,8 +61,10 @@ def test_work_split_invariance(ctas):
     _check_step(st, wl)
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 8), (16, 4), (64, 8), (12, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 8), (16, 4), (64, 8), (12, 2),
+                                    (128, 8), (24, 2), (36, 4), (16, 1)])
 def test_group_sizes(Hq, Hkv):
+    """1 to 16 q heads per kv head (16: e.g. 128 q / 8 kv heads; 9 and 12: ragged upper rows)."""
     wl = workloads.decode_custom(seed=40 + Hq, B=2, Hq=Hq, Hkv=Hkv, d=128, S0=257, steps=1,
                                  budget=128, n_sink=4, window=16, permute_pages=True)
     st = DecodeState(wl)
@@ -146,6 +148,16 @@ def test_mixed_batch_lengths_without_append():
         assert rel_l2(st.out[b].double().cpu().numpy(), o) < TOL
         assert rel_l2(st.probs[b, :, :S].double().cpu().numpy(), p) < TOL
     assert st.seq.cpu().tolist() == lens.tolist()
+
+
+def test_group_of_16_bf16_output_no_probs_and_a_split_cutting_pages():
+    wl = workloads.decode_custom(seed=19, B=3, Hq=128, Hkv=8, d=128, S0=3001, steps=1, budget=8,
+                                 n_sink=0, window=8, permute_pages=True, page=64)
+    st = DecodeState(wl, with_probs=False, out_f32=False)
+    st.decode(0, num_ctas=37)
+    torch.cuda.synchronize()
+    assert st.status() == (0, 0)
+    _check_step(st, wl)
 
 
 def test_bf16_output_and_no_probs_buffer():

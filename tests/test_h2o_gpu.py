@@ -247,6 +247,13 @@ def test_custom_config_evict_every_step_permuted_pages(link, page):
     _run_mode_a(wl, wl.steps, link=link)
 
 
+def test_group_of_16_evict_every_step():
+    """16 q heads per kv head: the H2O score sums all 16 heads' probabilities of a key."""
+    wl = workloads.decode_custom(seed=78, B=2, Hq=64, Hkv=4, d=128, S0=400, steps=6, budget=150,
+                                 n_sink=4, window=20, permute_pages=True)
+    _run_mode_a(wl, wl.steps, link=True)
+
+
 def test_decode_hands_candidates_to_select():
     """With the hand-off, the select keeps exactly the top-k of the GPU's own
     scores (compacting on every other step), and each list is used once."""
