@@ -7,11 +7,13 @@
 // probability, and the H2O running score cum[kv head][key] += the sum of the
 // group's probabilities.
 //
-// Layout of the work.  A "unit" is one 16-token page of one (sequence, kv
-// head) pair; the units of the whole batch are numbered pair-major and cut
-// into gridDim.x equal contiguous ranges, one per CTA (stream-K style: every
-// CTA gets the same number of pages whatever the lengths, so a single wave of
-// co-resident CTAs finishes together).  A CTA's range covers one or a few
+// Layout of the work.  A "unit" is one 16-token tile of one (sequence, kv
+// head) pair: a whole page of a 16-token pool, or one of the 2..16 tiles of
+// a larger page (pools of 32..256-token pages).  The units of the whole
+// batch are numbered pair-major and cut into gridDim.x equal contiguous
+// ranges, one per CTA (stream-K style: every CTA gets the same number of
+// tiles whatever the lengths, so a single wave of co-resident CTAs finishes
+// together).  A CTA's range covers one or a few
 // pairs; each covered piece of a pair is a "segment".
 //
 // Each CTA (6 warps) streams its range twice, K pages first, then V pages:
