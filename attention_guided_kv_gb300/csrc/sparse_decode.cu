@@ -64,11 +64,14 @@ constexpr size_t kSdAttnRing = size_t(kSdAttnWarps) * kSdAttnStages * 8192;
 static_assert(kSdAttnRing >= size_t(kSdAttnWarps) * kSdMaxG * (kSdD + 2) * 4, "merge scratch fits in the rings");
 constexpr size_t kSdAttnSmem = kSdAttnRing + 1024;
 constexpr int kSdIdxWarps = 8;           // indexer CTA: 8 warps
-constexpr int kSdIdxBatch = 4;           // tiles of 16 tokens a warp loads before computing
+constexpr int kSdIdxRing = 4;            // tiles of 16 keys in a warp's copy ring (3 in flight)
+constexpr int kSdIdxTileBytes = 16 * 128; // 16 keys x 64 bf16
+constexpr size_t kSdIdxSmem = size_t(1 << 12) * 4 + size_t(kSdIdxWarps) * kSdIdxRing * kSdIdxTileBytes;
 constexpr int kSdHistBits = 12;          // histogram of the top 12 bits of a score's order key
 constexpr int kSdHistBins = 1 << kSdHistBits;
 constexpr int kSdSelThreads = 1024;
-constexpr int kSdCandCap = 8192;         // candidates per row the final select holds (8 per thread)
+constexpr int kSdCandCap = 12288;        // candidates per row the final select holds (12 per thread): a
+                                         // row whose scores are all <= 0 ties thousands of keys at 0
 constexpr int kSdSelSlice = 16 * kSdSelThreads;  // positions a select CTA scans (16 per thread)
 constexpr int kSdSliceCap = 2048;        // candidates a slice may hand over (more: whole-row select)
 constexpr int kSdMaxSlices = kSdSelThreads;  // slices the final select reads in one pass (rows to 16M)
@@ -128,8 +131,27 @@ __device__ __forceinline__ void cp_async_wait() {
 // k-step t takes the half (t & 1) of run (t >> 1) as its logical k's
 // {2q, 2q+1 | 2q+8, 2q+9}; the indexer query (the B operand) is read with the
 // same permutation, so each product pairs the same physical dims.
+// One warp's copy of a 16-key tile (16 rows of 128 B) into a ring slot, 16-byte chunk c of row r
+// stored at chunk c ^ (r & 7), so that the fragment reads below hit eight different bank groups;
+// rows at or past the length are zero-filled.
+__device__ __forceinline__ void sd_idx_tile_copy(uint32_t slot, const __nv_bfloat16* tile, int rows, int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = lane + 32 * i, r = q >> 3, ch = q & 7;
+    const bool ok = r < rows;
+    cp_async16(slot + r * 128 + ((ch ^ (r & 7)) << 4), tile + (ok ? r * kSdDi + ch * 8 : 0), ok);
+  }
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 __global__ void __launch_bounds__(kSdIdxWarps * 32) sd_index_kernel(const SdParams P) {
-  __shared__ uint32_t s_hist[kSdHistBins];
+  extern __shared__ __align__(128) uint8_t idx_smem[];
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(idx_smem);  // [kSdHistBins]
   // launched early when the previous kernel allows it (the previous step's attention does, once its
   // gathers are done): nothing is read or written before that kernel has finished
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -144,7 +166,8 @@ __global__ void __launch_bounds__(kSdIdxWarps * 32) sd_index_kernel(const SdPara
   const int tiles = (S + 15) / 16;
   const int t0 = int((long long)tiles * c / P.idx_ctas), t1 = int((long long)tiles * (c + 1) / P.idx_ctas);
   if (P.appended && S_old / 16 >= t0 && S_old / 16 < t1) {
-    // this CTA covers the appended token: its K, V (every kv head) and indexer key
+    // this CTA covers the appended token: its K, V (every kv head) and indexer key (which this
+    // CTA's own copies below read back from L2)
     const int phys = P.block_table[size_t(b) * P.max_pages + (S_old >> (4 + P.page_shift))];
     if (unsigned(phys) < unsigned(P.num_pages)) {
       for (int i = tid; i < P.Hkv * 32; i += blockDim.x) {
@@ -159,9 +182,11 @@ __global__ void __launch_bounds__(kSdIdxWarps * 32) sd_index_kernel(const SdPara
     } else if (tid == 0) {
       report(P.status, KVSEL_ERR_BAD_INDEX);
     }
-    if (tid < 8)
+    if (tid < 8) {
       reinterpret_cast<uint4*>(P.idx_k + (size_t(b) * P.max_len + S_old) * kSdDi)[tid] =
           reinterpret_cast<const uint4*>(P.idx_k_new + size_t(b) * kSdDi)[tid];
+      __threadfence();  // in L2 before the barrier below: the copies read L2
+    }
   }
   for (int i = tid; i < kSdHistBins; i += blockDim.x) s_hist[i] = 0u;
   const int g = lane >> 2, qd = lane & 3;
@@ -181,51 +206,57 @@ __global__ void __launch_bounds__(kSdIdxWarps * 32) sd_index_kernel(const SdPara
   const float w1 = 2 * qd + 1 < P.Hi ? P.idx_w[b * P.Hi + 2 * qd + 1] : 0.f;
   float* srow = P.scores + size_t(b) * P.max_len;
   const __nv_bfloat16* kbase = P.idx_k + size_t(b) * P.max_len * kSdDi;
-  const __nv_bfloat16* knew = P.appended ? P.idx_k_new + size_t(b) * kSdDi : nullptr;
-  __syncthreads();  // histogram cleared
-#pragma unroll 1
-  for (int tb = t0 + warp; tb < t1; tb += kSdIdxWarps * kSdIdxBatch) {
-    uint4 ra[kSdIdxBatch][2], rb[kSdIdxBatch][2];
-#pragma unroll
-    for (int j = 0; j < kSdIdxBatch; ++j) {
-      const int tile = tb + j * kSdIdxWarps;
-      const int ta = tile * 16 + g, tbk = ta + 8;
-      const bool oka = tile < t1 && ta < S, okb = tile < t1 && tbk < S;
-      const __nv_bfloat16* pa = (knew && ta == S_old) ? knew : kbase + size_t(ta) * kSdDi;
-      const __nv_bfloat16* pb = (knew && tbk == S_old) ? knew : kbase + size_t(tbk) * kSdDi;
-      ra[j][0] = oka ? __ldcs(reinterpret_cast<const uint4*>(pa + 8 * qd)) : make_uint4(0u, 0u, 0u, 0u);
-      ra[j][1] = oka ? __ldcs(reinterpret_cast<const uint4*>(pa + 32 + 8 * qd)) : make_uint4(0u, 0u, 0u, 0u);
-      rb[j][0] = okb ? __ldcs(reinterpret_cast<const uint4*>(pb + 8 * qd)) : make_uint4(0u, 0u, 0u, 0u);
-      rb[j][1] = okb ? __ldcs(reinterpret_cast<const uint4*>(pb + 32 + 8 * qd)) : make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();  // histogram cleared, the appended key in L2
+  // warp w takes the CTA's tiles t0 + w, t0 + w + 8, ...; kSdIdxRing - 1 of them always in flight
+  const int nj = t1 - t0 > warp ? (t1 - t0 - warp + kSdIdxWarps - 1) / kSdIdxWarps : 0;
+  const uint32_t ring = smem_u32(idx_smem + size_t(kSdHistBins) * 4 + size_t(warp) * kSdIdxRing * kSdIdxTileBytes);
+  auto issue = [&](int j) {  // tile j of this warp into its slot (an empty group past the end)
+    if (j < nj) {
+      const int tile = t0 + warp + j * kSdIdxWarps;
+      sd_idx_tile_copy(ring + (j % kSdIdxRing) * kSdIdxTileBytes, kbase + size_t(tile) * 16 * kSdDi,
+                       min(16, S - tile * 16), lane);
     }
+    cp_async_commit();
+  };
 #pragma unroll
-    for (int j = 0; j < kSdIdxBatch; ++j) {
-      const int tile = tb + j * kSdIdxWarps;
-      if (tile >= t1) break;  // warp-uniform
-      float cc[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_bf16_16816(cc, ra[j][0].x, rb[j][0].x, ra[j][0].y, rb[j][0].y, bq[0][0], bq[0][1]);
-      mma_bf16_16816(cc, ra[j][0].z, rb[j][0].z, ra[j][0].w, rb[j][0].w, bq[1][0], bq[1][1]);
-      mma_bf16_16816(cc, ra[j][1].x, rb[j][1].x, ra[j][1].y, rb[j][1].y, bq[2][0], bq[2][1]);
-      mma_bf16_16816(cc, ra[j][1].z, rb[j][1].z, ra[j][1].w, rb[j][1].w, bq[3][0], bq[3][1]);
-      float ia = w0 * fmaxf(cc[0], 0.f) + w1 * fmaxf(cc[1], 0.f);
-      float ib = w0 * fmaxf(cc[2], 0.f) + w1 * fmaxf(cc[3], 0.f);
-      ia += __shfl_xor_sync(0xffffffffu, ia, 1);
-      ia += __shfl_xor_sync(0xffffffffu, ia, 2);
-      ib += __shfl_xor_sync(0xffffffffu, ib, 1);
-      ib += __shfl_xor_sync(0xffffffffu, ib, 2);
-      const int ta = tile * 16 + g, tbk = ta + 8;
-      if (qd == 0) {
-        if (ta < S) {
-          srow[ta] = ia;
-          atomicAdd(&s_hist[order_key(ia) >> (32 - kSdHistBits)], 1u);
-        }
-        if (tbk < S) {
-          srow[tbk] = ib;
-          atomicAdd(&s_hist[order_key(ib) >> (32 - kSdHistBits)], 1u);
-        }
+  for (int j = 0; j < kSdIdxRing - 1; ++j) issue(j);
+#pragma unroll 1
+  for (int j = 0; j < nj; ++j) {
+    issue(j + kSdIdxRing - 1);          // into the slot read last iteration
+    cp_async_wait<kSdIdxRing - 1>();    // tile j has landed
+    __syncwarp();
+    // rows g and g + 8, chunks qd and 4 + qd (swizzled: (g + 8) & 7 == g)
+    const uint32_t sb = ring + (j % kSdIdxRing) * kSdIdxTileBytes;
+    const uint4 ra0 = lds128(sb + g * 128 + ((qd ^ g) << 4));
+    const uint4 ra1 = lds128(sb + g * 128 + (((4 + qd) ^ g) << 4));
+    const uint4 rb0 = lds128(sb + (g + 8) * 128 + ((qd ^ g) << 4));
+    const uint4 rb1 = lds128(sb + (g + 8) * 128 + (((4 + qd) ^ g) << 4));
+    __syncwarp();                       // every lane has read the slot before it is refilled
+    const int tile = t0 + warp + j * kSdIdxWarps;
+    float cc[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_bf16_16816(cc, ra0.x, rb0.x, ra0.y, rb0.y, bq[0][0], bq[0][1]);
+    mma_bf16_16816(cc, ra0.z, rb0.z, ra0.w, rb0.w, bq[1][0], bq[1][1]);
+    mma_bf16_16816(cc, ra1.x, rb1.x, ra1.y, rb1.y, bq[2][0], bq[2][1]);
+    mma_bf16_16816(cc, ra1.z, rb1.z, ra1.w, rb1.w, bq[3][0], bq[3][1]);
+    float ia = w0 * fmaxf(cc[0], 0.f) + w1 * fmaxf(cc[1], 0.f);
+    float ib = w0 * fmaxf(cc[2], 0.f) + w1 * fmaxf(cc[3], 0.f);
+    ia += __shfl_xor_sync(0xffffffffu, ia, 1);
+    ia += __shfl_xor_sync(0xffffffffu, ia, 2);
+    ib += __shfl_xor_sync(0xffffffffu, ib, 1);
+    ib += __shfl_xor_sync(0xffffffffu, ib, 2);
+    const int ta = tile * 16 + g, tbk = ta + 8;
+    if (qd == 0) {
+      if (ta < S) {
+        srow[ta] = ia;
+        atomicAdd(&s_hist[order_key(ia) >> (32 - kSdHistBits)], 1u);
+      }
+      if (tbk < S) {
+        srow[tbk] = ib;
+        atomicAdd(&s_hist[order_key(ib) >> (32 - kSdHistBits)], 1u);
       }
     }
   }
+  cp_async_wait<0>();
   __syncthreads();
   uint32_t* ghist = P.hist + size_t(b) * kSdHistBins;
   for (int i = tid; i < kSdHistBins; i += blockDim.x) {
@@ -237,7 +268,6 @@ __global__ void __launch_bounds__(kSdIdxWarps * 32) sd_index_kernel(const SdPara
 // ---------------------------------------------------------------------------
 // Selection.
 static_assert(kRkUpMax >= kSdSelSlice && kRkUpMax >= kSdCandCap, "slice keys and candidates fit in ukey");
-static_assert(kSdCandCap <= 256 * 32, "the kept positions are staged in lhist");
 struct SdSelSmem {
   RowTopkSmem rk;                      // ukey: the slice's keys, then the row's candidate keys; lhist:
                                        // radix select of the last bits; all of it: the whole-row fallback
@@ -832,6 +862,7 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   {
     cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(sd_attn_kernel), int(kSdAttnSmem));
+    if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(sd_index_kernel), int(kSdIdxSmem));
     if (e0 == cudaSuccess)
       e0 = smem_limit_once(reinterpret_cast<const void*>(sd_select_kernel), int(sizeof(SdSelSmem)));
     if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_sparse_decode (attribute)");
@@ -858,7 +889,7 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   e = cudaLaunchKernelEx(&cfg, kernel, P);                               \
   trace_after(st);                                                       \
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_sparse_decode (" name ")");
-  KVSEL_SD_LAUNCH("sd_index", sd_index_kernel, dim3(idx_ctas, batch), kSdIdxWarps * 32, 0, 1)
+  KVSEL_SD_LAUNCH("sd_index", sd_index_kernel, dim3(idx_ctas, batch), kSdIdxWarps * 32, kSdIdxSmem, 1)
   KVSEL_SD_LAUNCH("sd_select", sd_select_kernel, dim3(slices, batch),
                   kSdSelThreads, sizeof(SdSelSmem), 1)
   KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem, 2)

@@ -114,6 +114,18 @@ def test_larger_pages_across_a_page_boundary(page):
     assert K.read_status(st.ws) == 0
 
 
+@pytest.mark.parametrize("S0", [140000, 250000])
+def test_scores_all_at_most_zero_tie_thousands_at_zero(S0):
+    """Every indexer weight negative: every score is <= 0 and thousands of keys tie at exactly 0
+    (10.2K at 140K keys: the final select's candidate list; 14.2K at 250K: past its capacity,
+    the whole-row select).  Ties go to the lower positions."""
+    wl = workloads.sparse_decode(seed=25, B=1, S0=S0, steps=1, Hq=16, Hkv=2, top_k=2048)
+    wl.w_idx = -np.abs(wl.w_idx)
+    st = SparseState(wl)
+    st.step(0)
+    _check(st, 0)
+
+
 def test_short_context_selects_all_and_matches_dense():
     wl = workloads.sparse_decode(seed=15, B=3, S0=300, steps=1, top_k=2048)
     st = SparseState(wl)
