@@ -49,7 +49,7 @@ namespace kvsel {
 
 constexpr int kQuD = 128;
 constexpr int kQuPage = 16;
-constexpr int kQuMaxG = kTileMaxG;
+constexpr int kQuMaxG = 8;  // q heads per kv head (the page bounds take the group's rows 0..7)
 constexpr int kQuBoundThreads = 256;
 constexpr int kQuBoundPagesPerCta = 256;
 constexpr int kQuTopkGroups = 8;          // row_topk (rows above 16K pages): up to 32K in registers

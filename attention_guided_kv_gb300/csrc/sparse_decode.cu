@@ -593,6 +593,8 @@ __device__ __forceinline__ float sd_cluster_ld(uint32_t addr) {
   return v;
 }
 
+// kWide: 9..16 q heads per kv head (attend_tile_wide)
+template <bool kWide>
 __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -600,14 +602,15 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
   __shared__ __align__(16) float s_part[kSdPartFloats];  // this split's (M, L, O) of the pair
   __shared__ float s_f[kSdMaxClusterSplits][kSdMaxG];    // each split's max per head, then its merge weight
   __shared__ float s_l[kSdMaxClusterSplits][kSdMaxG];    // each split's sum per head
-  float* wo = reinterpret_cast<float*>(smem);  // [4][8][130] merge scratch, over the rings once they are idle
+  float* wo = reinterpret_cast<float*>(smem);  // [4][16][130] merge scratch, over the rings once they are idle
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;  // split = the CTA's rank in its cluster
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = P.G, g = lane >> 2, qd = lane & 3;
-  const bool head_ok = g < G;
+  const bool head_ok = g < G, head_ok2 = kWide && g + 8 < G;
   // the q rows and the length are inputs: read while the select finishes (the select writes neither)
-  uint32_t qa[8][2];
+  uint32_t qa[8][2], qb[8][2];
   load_q_frags(P.q + (size_t(b) * P.Hq + kvh * G + (head_ok ? g : 0)) * kSdD, head_ok, qd, qa);
+  if (kWide) load_q_frags(P.q + (size_t(b) * P.Hq + kvh * G + (head_ok2 ? g + 8 : 0)) * kSdD, head_ok2, qd, qb);
   int S;
   if (!sd_len_ok(P, b, S)) return;  // the whole cluster (one sequence) leaves together
   const int nsel = min(P.top_k, S);
@@ -666,9 +669,13 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
   for (int t = tw0; t < t1; t += kSdAttnWarps, ++j) {
     cp_async_wait<kSdAttnStages - 1>();
     __syncwarp();
-    float x0, x1, x2, x3;
     const int valid = min(16, nsel - t * 16);
-    attend_tile(wbuf + s * 8192, wbuf + s * 8192 + 4096, qa, valid, P.scale_log2, st, x0, x1, x2, x3);
+    if (kWide) {
+      attend_tile_wide(wbuf + s * 8192, wbuf + s * 8192 + 4096, qa, qb, valid, P.scale_log2, st, head_ok, head_ok2);
+    } else {
+      float x0, x1, x2, x3;
+      attend_tile(wbuf + s * 8192, wbuf + s * 8192 + 4096, qa, valid, P.scale_log2, st, x0, x1, x2, x3);
+    }
     __syncwarp();
     if (t + kSdAttnStages * kSdAttnWarps < t1) gather(j + kSdAttnStages, s);
     else cp_async_commit();
@@ -678,7 +685,7 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
   // the next step's indexer may launch now: it waits for this grid before touching anything
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();  // every warp is done with its ring: the merge scratch may overwrite it
-  merge_warps_to_slot<kSdAttnWarps>(st, wo, s_part, G);
+  merge_warps_to_slot<kSdAttnWarps, kWide>(st, wo, s_part, G);
   sd_cluster_sync();  // every split's partial is in its shared memory
   // merge weights: every split's (max, sum) per head fetched at once, then combined per head
   const int ns = P.splits;
@@ -780,7 +787,7 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   if (kv->num_kv_heads < 1 || kv->num_q_heads < 1 || kv->num_q_heads % kv->num_kv_heads != 0)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "num_q_heads must be a positive multiple of num_kv_heads");
   const int Hkv = kv->num_kv_heads, Hq = kv->num_q_heads, G = Hq / Hkv;
-  if (G > kSdMaxG) return fail(KVSEL_ERR_UNSUPPORTED, fn + "at most 8 q heads per kv head");
+  if (G > kSdMaxG) return fail(KVSEL_ERR_UNSUPPORTED, fn + "at most 16 q heads per kv head");
   if (idx_dim != kSdDi || num_idx_heads < 1 || num_idx_heads > kSdMaxHi)
     return fail(KVSEL_ERR_UNSUPPORTED, fn + "indexer: 1..8 heads of dimension 64 are implemented");
   if (!block_table || !seq_lens || !q || !out || !idx_q || !idx_w || !idx_k || batch < 1 ||
@@ -861,7 +868,8 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   {
-    cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(sd_attn_kernel), int(kSdAttnSmem));
+    cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(sd_attn_kernel<false>), int(kSdAttnSmem));
+    if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(sd_attn_kernel<true>), int(kSdAttnSmem));
     if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(sd_index_kernel), int(kSdIdxSmem));
     if (e0 == cudaSuccess)
       e0 = smem_limit_once(reinterpret_cast<const void*>(sd_select_kernel), int(sizeof(SdSelSmem)));
@@ -892,7 +900,11 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   KVSEL_SD_LAUNCH("sd_index", sd_index_kernel, dim3(idx_ctas, batch), kSdIdxWarps * 32, kSdIdxSmem, 1)
   KVSEL_SD_LAUNCH("sd_select", sd_select_kernel, dim3(slices, batch),
                   kSdSelThreads, sizeof(SdSelSmem), 1)
-  KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem, 2)
+  if (G > 8) {
+    KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel<true>, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem, 2)
+  } else {
+    KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel<false>, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem, 2)
+  }
 #undef KVSEL_SD_LAUNCH
   return KVSEL_OK;
 }

@@ -30,7 +30,8 @@
  * [batch][max_pages]; token slot t of sequence b lives in page
  * block_table[b][t / page_size], row t % page_size.  Supported here:
  * head_dim = 128; num_q_heads / num_kv_heads <= 16 for the decode step
- * (and its block signal), <= 8 elsewhere; and page_size 16, 32,
+ * (and its block signal) and the sparse decode, <= 8 for SnapKV and Quest;
+ * and page_size 16, 32,
  * 64, 128 or 256 for the decode step, the H2O evict, the keep-list
  * compaction and the sparse decode (the kernels address a page in 16-token
  * tiles); SnapKV, Quest and the decode step's block signal take page_size

@@ -159,7 +159,7 @@ def test_sparse_decode_host_validation(lib):
     assert st(top_k=0) == K.KVSEL_ERR_INVALID_ARG
     assert st(max_len=(1 << 28) + 1) == K.KVSEL_ERR_UNSUPPORTED
     assert st(ws_bytes=100) == K.KVSEL_ERR_INVALID_ARG
-    assert st(kv=_kv(num_q_heads=128)) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(kv=_kv(num_q_heads=136)) == K.KVSEL_ERR_UNSUPPORTED     # 17 q heads per kv head
 
 
 def test_snapkv_ex_host_validation(lib):

@@ -159,7 +159,7 @@ def test_large_top_k_single_stage():
     _check(st, 0)
 
 
-@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("G", [1, 4, 8, 12, 16])
 def test_group_sizes_and_bf16_output(G):
     wl = workloads.sparse_decode(seed=17 + G, B=2, S0=5000, steps=1, Hq=8 * G, Hkv=8, top_k=1000)
     st = SparseState(wl, out_f32=False)
