@@ -78,6 +78,7 @@ _SIGS = {
                                        _vp, _vp, _i, _i, _vp]),
     "kvsel_h2o_evict_workspace": (_sz, [_PKV, _i, _i]),
     "kvsel_h2o_link_bytes": (_sz, [_i, _i]),
+    "kvsel_h2o_link_reset": (_i, [_vp, _i, _i, _vp]),
     "kvsel_h2o_evict": (_i, [_PKV, _vp, _i, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                              _sz, _vp]),
     "kvsel_kv_compact_workspace": (_sz, [_i, _i]),
@@ -311,6 +312,11 @@ def kvsel_decode_attn_noalloc(kv: PagedKV, block_table, seq_lens, q, out, *, k_n
 # ----------------------------------------------------------------------------
 # H2O select / evict
 # ----------------------------------------------------------------------------
+def kvsel_h2o_link_reset(workspace, batch: int, num_kv_heads: int, stream=None):
+    """Clear the decode -> select hand-off in an H2O evict workspace (after an outside write to h2o_cum)."""
+    _check(lib().kvsel_h2o_link_reset(_ptr(workspace), int(batch), int(num_kv_heads), _stream(stream)))
+
+
 def kvsel_h2o_evict_workspace(kv: PagedKV, batch: int, budget: int) -> int:
     return int(lib().kvsel_h2o_evict_workspace(ctypes.byref(kv), batch, budget))
 

@@ -431,6 +431,18 @@ EvictWs evict_ws_layout(int batch, int Hkv, int budget) {
 }
 }  // namespace
 
+extern "C" kvsel_status kvsel_h2o_link_reset(void* workspace, int batch, int num_kv_heads, void* stream) {
+  const std::string fn = "kvsel_h2o_link_reset: ";
+  if (!workspace || !aligned(workspace, 256) || batch < 1 || num_kv_heads < 1)
+    return fail(KVSEL_ERR_INVALID_ARG, fn + "a 256-byte aligned workspace, batch >= 1 and num_kv_heads >= 1 are required");
+  // the thresholds and the candidate counts (adjacent): no threshold, no list
+  const H2OLink L = link_layout(workspace, batch * num_kv_heads);
+  const size_t bytes = reinterpret_cast<uint8_t*>(L.key) - reinterpret_cast<uint8_t*>(L.hint);
+  cudaError_t e = cudaMemsetAsync(L.hint, 0, bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kvsel_h2o_link_reset");
+  return KVSEL_OK;
+}
+
 extern "C" size_t kvsel_h2o_link_bytes(int batch, int num_kv_heads) {
   if (batch < 1 || num_kv_heads < 1) return 0;
   return link_bytes(batch * num_kv_heads);

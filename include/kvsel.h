@@ -226,6 +226,20 @@ KVSEL_API kvsel_status kvsel_decode_attn_ex(const kvsel_paged_kv* kv, const int3
  * h2o_link (0 for invalid arguments). */
 KVSEL_API size_t kvsel_h2o_link_bytes(int batch, int num_kv_heads);
 
+/* Invalidate the decode -> select hand-off kept in an H2O evict workspace
+ * (async on `stream`): every row's candidate list and last threshold are
+ * cleared, so the next kvsel_h2o_evict ranks each row's full scores and the
+ * decode step after it collects candidates again from the new thresholds.
+ * Call it after writing h2o_cum by other means (seeding it from
+ * kvsel_snapkv_select_ex's seed_out, adding a prefill seed, restoring a
+ * checkpoint): a list built before such a write does not hold a slot that
+ * the write lifted above the row's threshold.
+ *   workspace  the H2O evict workspace (256-byte aligned), for batch x
+ *              num_kv_heads rows.
+ * Returns KVSEL_ERR_INVALID_ARG for a NULL or misaligned workspace or
+ * non-positive sizes. */
+KVSEL_API kvsel_status kvsel_h2o_link_reset(void* workspace, int batch, int num_kv_heads, void* stream);
+
 /* Allocation-free kvsel_decode_attn.  The pages have no counterpart: this is
  * for callers that cannot allocate device memory (a runtime without a device
  * allocator, a plug-in whose host owns all allocations, code that must not

@@ -254,6 +254,44 @@ def test_group_of_16_evict_every_step():
     _run_mode_a(wl, wl.steps, link=True)
 
 
+def test_link_reset_after_an_outside_score_write():
+    """A caller lifts unlisted slots far above every score (a prefill seed, say) between a decode
+    step and the select; after kvsel_h2o_link_reset the select keeps them: the exact top-k."""
+    wl = workloads.decode_custom(seed=79, B=2, Hq=16, Hkv=4, d=128, S0=3000, steps=2, budget=500,
+                                 n_sink=4, window=32, permute_pages=True)
+    st = DecodeState(wl, spare_pages=8, link=True)
+    st.decode(0)
+    st.evict(compact=False)       # thresholds for the next decode's lists
+    st.decode(1)
+    torch.cuda.synchronize()
+    assert (st.link_counts() > 0).all()
+    cum = st.cum.cpu().numpy().copy()
+    S = int(st.S[0])
+    keep_before = st.keep.cpu().numpy().copy()
+    pos0 = st.pos.cpu().numpy()
+    lifted = []
+    for b in range(wl.B):
+        for h in range(wl.Hkv):
+            kept = set(keep_before[b, h].tolist())
+            j = next(x for x in range(wl.n_sink, S - wl.window) if int(pos0[b, h, x]) not in kept)
+            cum[b, h, j] = cum[b, h, :S].max() * 4.0 + 1.0
+            lifted.append((b, h, j))
+    st.cum.copy_(torch.from_numpy(cum))
+    K.kvsel_h2o_link_reset(st.ws_ev, wl.B, wl.Hkv)
+    assert (st.link_counts() == 0).all()
+    st.evict(compact=False)
+    torch.cuda.synchronize()
+    assert st.status() == (0, 0)
+    keep = st.keep.cpu().numpy()
+    pos = st.pos.cpu().numpy()
+    for b in range(wl.B):
+        for h in range(wl.Hkv):
+            want = h2o_keep(cum[b, h].astype(np.float32), S, wl.budget, wl.n_sink, wl.window)
+            np.testing.assert_array_equal(keep[b, h, :len(want)], pos[b, h, want])
+    for b, h, j in lifted:
+        assert pos[b, h, j] in keep[b, h]
+
+
 def test_decode_hands_candidates_to_select():
     """With the hand-off, the select keeps exactly the top-k of the GPU's own
     scores (compacting on every other step), and each list is used once."""

@@ -6,14 +6,17 @@ runs the same decode kernel on the library's built-in scratch array instead
 of a caller-provided workspace.  This test drives two identical caches, one
 through each entry point, for two decode steps in a row (so the second call
 runs on scratch the first one left behind) and compares outputs,
-probabilities, H2O scores and lengths.  It sits in a file of its own that is
-collected last.
+probabilities, H2O scores and lengths, and checks the outputs and
+probabilities against the fp64 oracle as well.  It sits in a file of its own
+that is collected last.
 """
 
+import numpy as np
 import pytest
 import torch
 
 import workloads
+from oracle.attention import bf16_bits_to_f64, decode_attention
 from _harness import DecodeState, bf16, rel_l2
 
 import attention_guided_kv_gb300 as K
@@ -48,6 +51,15 @@ def test_noalloc_matches_workspace_entry_point_two_calls():
                       ref.cum[:, :, :S].double().cpu().numpy()) < TOL
         assert alt.seq.cpu().tolist() == ref.seq.cpu().tolist() == [S] * wl.B
         assert alt.pos.cpu().tolist() == ref.pos.cpu().tolist()
+        # and against the oracle directly: O and probabilities of every sequence at this step
+        for b in range(wl.B):
+            Kb = np.concatenate([bf16_bits_to_f64(wl.K[b]),
+                                 bf16_bits_to_f64(wl.k_new[:step + 1, b]).transpose(1, 0, 2)], axis=1)
+            Vb = np.concatenate([bf16_bits_to_f64(wl.V[b]),
+                                 bf16_bits_to_f64(wl.v_new[:step + 1, b]).transpose(1, 0, 2)], axis=1)
+            o, p = decode_attention(bf16_bits_to_f64(wl.q[step, b]), Kb, Vb, wl.scale)
+            assert rel_l2(alt.out[b].double().cpu().numpy(), o) < TOL
+            assert rel_l2(alt.probs[b, :, :S].double().cpu().numpy(), p) < TOL
     assert K.read_status(ref.ws) == 0
 
 
