@@ -6,7 +6,8 @@
 // sequence b (S_b keys once the new token is appended) and q head h of kv
 // head h / G:
 //   bound[b, h, p] = sum_d max(q_d * kmin[p]_d, q_d * kmax[p]_d)   for every
-//                    full page p < S_b / 16
+//                    full page p < S_b / 16 (a Quest page is 16 tokens: one
+//                    16-row tile of a pool page of 16 to 256 tokens)
 //   pages[b, h]    = the budget_pages largest bounds, ties to the lower page
 //                    (every full page when there are no more), ascending
 //   o[b, h]        = softmax(scale * q . k) V over the tokens of pages[b, h]
@@ -20,12 +21,13 @@
 // Kernels:
 //   qu_meta_kernel   builds the per-page min / max of a prompt's keys: one
 //                    warp per (page, kv head), a partial page over its valid
-//                    tokens.
+//                    tokens.  A page's pair sits beside its pool tile: pool
+//                    page p, kv head h, tile j -> meta[p][h][j].
 //   qu_bound_kernel  (page chunk, kv head, sequence), 8 warps: the CTA whose
 //                    chunk holds the new token's page appends it (K and V
 //                    rows, and the page's min / max) before its own bounds;
-//                    then the bounds of 16 full pages x 8 heads per warp
-//                    tile on the tensor cores (mma.sync: the pages' [min |
+//                    then the bounds of 16 full pages x 8 heads (two such
+//                    columns for 9..16 heads) per warp tile on the tensor cores (mma.sync: the pages' [min |
 //                    max] rows, 512 bytes each, against the heads' [q- | q+],
 //                    see below).
 //   qu_topk_kernel   (q head, sequence): the top pages of the head's bounds
@@ -33,13 +35,13 @@
 //                    pages, row_topk above), the kept pages marked in the kv
 //                    head's page mask; the last of the G heads to finish
 //                    lists the marked pages in ascending order with their
-//                    physical pages and head masks (the partial page last,
+//                    pool tiles and head masks (the partial page last,
 //                    for every head) and clears the mask.
 //   qu_attn_kernel   (split, kv head, sequence), 4 warps: one 16-key tile per
 //                    listed page (cp.async gather of its K and V rows into the
 //                    swizzled tile, three stages per warp: two pages in
-//                    flight while one is computed), attend_tile with the
-//                    page's head mask; the last split of a (sequence, kv
+//                    flight while one is computed), attend_tile (9..16
+//                    heads: attend_tile_wide) with the page's head mask; the last split of a (sequence, kv
 //                    head) merges the splits into O and the last kv head
 //                    publishes the length.
 #include "attn_tile.cuh"
@@ -48,8 +50,8 @@
 namespace kvsel {
 
 constexpr int kQuD = 128;
-constexpr int kQuPage = 16;
-constexpr int kQuMaxG = 8;  // q heads per kv head (the page bounds take the group's rows 0..7)
+constexpr int kQuPage = 16;  // tokens per Quest page: one 16-row tile of a pool page of 16..256 tokens
+constexpr int kQuMaxG = 16;  // q heads per kv head (bounds: one or two 8-head MMA columns)
 constexpr int kQuBoundThreads = 256;
 constexpr int kQuBoundPagesPerCta = 256;
 constexpr int kQuTopkGroups = 8;          // row_topk (rows above 16K pages): up to 32K in registers
@@ -68,13 +70,13 @@ struct QuParams {
   const __nv_bfloat16* v_new;
   __nv_bfloat16* k_pool;
   __nv_bfloat16* v_pool;
-  __nv_bfloat16* meta;           // [num_pages][Hkv][2][128]: min row, max row
-  float* bounds;                 // [B][Hq][max_pages]
+  __nv_bfloat16* meta;           // [num_pages][Hkv][pool page / 16][2][128]: min row, max row
+  float* bounds;                 // [B][Hq][max_qp]
   int32_t* sel;                  // [B][Hq][budget]
-  uint32_t* mask;                // [B][Hkv][max_pages]: heads that chose each page (zero between calls)
-  int32_t* ulist;                // [B][Hkv][max_pages]: listed pages, ascending
-  int32_t* uphys;                // [B][Hkv][max_pages]: their physical pages
-  uint32_t* umask;               // [B][Hkv][max_pages]: their head masks
+  uint32_t* mask;                // [B][Hkv][max_qp]: heads that chose each page (zero between calls)
+  int32_t* ulist;                // [B][Hkv][max_qp]: listed pages, ascending
+  int32_t* uphys;                // [B][Hkv][max_qp]: their pool tiles (qu_tile)
+  uint32_t* umask;               // [B][Hkv][max_qp]: their head masks
   int32_t* ucount;               // [B][Hkv]
   unsigned* topk_cnt;            // [B][Hkv]: heads done (the last one lists)
   unsigned* merge_cnt;           // [B][Hkv]: splits done (the last one merges)
@@ -83,21 +85,30 @@ struct QuParams {
   void* out;
   int* status;
   int B, max_pages, Hq, Hkv, G, num_pages, budget, chunks, splits, appended, out_f32;
+  int page_shift;                // log2(pool page / 16)
+  int max_qp;                    // Quest pages per block-table row: max_pages << page_shift
   float scale_log2;
 };
 
 __device__ __forceinline__ bool qu_len_ok(const QuParams& P, int b, int& S) {
   S = P.seq_lens[b] + P.appended;
-  return S >= 0 && (S + kQuPage - 1) / kQuPage <= P.max_pages;
+  return S >= 0 && (S + kQuPage - 1) / kQuPage <= P.max_qp;
 }
 
-__device__ __forceinline__ int qu_phys(const QuParams& P, int b, int page) {
-  int phys = P.block_table[size_t(b) * P.max_pages + page];
-  if (unsigned(phys) >= unsigned(P.num_pages)) {
-    report(P.status, KVSEL_ERR_BAD_INDEX);
+// Pool tile of Quest page t of sequence b, kv head kvh: the 16 rows from row
+// 16 * tile of the pool and the min / max pair at meta + tile * 256.  A bad
+// block-table entry is reported and read as page 0.
+__device__ __forceinline__ int qu_tile_of(const int32_t* block_table, int max_pages, int num_pages, int Hkv,
+                                          int page_shift, int* status, int b, int kvh, int t) {
+  int phys = block_table[size_t(b) * max_pages + (t >> page_shift)];
+  if (unsigned(phys) >= unsigned(num_pages)) {
+    report(status, KVSEL_ERR_BAD_INDEX);
     phys = 0;
   }
-  return phys;
+  return ((phys * Hkv + kvh) << page_shift) | (t & ((1 << page_shift) - 1));
+}
+__device__ __forceinline__ int qu_tile(const QuParams& P, int b, int kvh, int t) {
+  return qu_tile_of(P.block_table, P.max_pages, P.num_pages, P.Hkv, P.page_shift, P.status, b, kvh, t);
 }
 
 __device__ __forceinline__ void qu_cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -111,32 +122,32 @@ __device__ __forceinline__ float bf16_at(uint4 v, int i) {
 }
 
 // ---------------------------------------------------------------------------
-// Page min / max of a prompt: grid (ceil(max_pages / 4), Hkv, B), 4 warps, one
-// page each; lane l owns dimensions 4l .. 4l + 3.
+// Page min / max of a prompt: grid (ceil(max_qp / 4), Hkv, B), 4 warps, one
+// Quest page each; lane l owns dimensions 4l .. 4l + 3.
 struct QuMetaParams {
   const int32_t* block_table;
   const int32_t* seq_lens;
   const __nv_bfloat16* k_pool;
   __nv_bfloat16* meta;
   int* status;
-  int max_pages, Hkv, num_pages;
+  int max_pages, Hkv, num_pages, page_shift, max_qp;
 };
 __global__ void __launch_bounds__(128) qu_meta_kernel(const QuMetaParams P) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int page = blockIdx.x * 4 + warp, kvh = blockIdx.y, b = blockIdx.z;
   const int S = P.seq_lens[b];
-  if (S < 0 || (S + kQuPage - 1) / kQuPage > P.max_pages) {
+  if (S < 0 || (S + kQuPage - 1) / kQuPage > P.max_qp) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
     return;
   }
   if (page * kQuPage >= S) return;
   const int n = min(kQuPage, S - page * kQuPage);
-  int phys = P.block_table[size_t(b) * P.max_pages + page];
-  if (unsigned(phys) >= unsigned(P.num_pages)) {
+  if (unsigned(P.block_table[size_t(b) * P.max_pages + (page >> P.page_shift)]) >= unsigned(P.num_pages)) {
     if (lane == 0) report(P.status, KVSEL_ERR_BAD_INDEX);
     return;
   }
-  const __nv_bfloat16* rows = P.k_pool + (size_t(phys) * P.Hkv + kvh) * kQuPage * kQuD;
+  const int tile = qu_tile_of(P.block_table, P.max_pages, P.num_pages, P.Hkv, P.page_shift, P.status, b, kvh, page);
+  const __nv_bfloat16* rows = P.k_pool + size_t(tile) * kQuPage * kQuD;
   float mn[4], mx[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -154,13 +165,15 @@ __global__ void __launch_bounds__(128) qu_meta_kernel(const QuMetaParams P) {
     }
   }
   // min / max of bf16 values are bf16 values: the conversion back is exact
-  __nv_bfloat16* m = P.meta + (size_t(phys) * P.Hkv + kvh) * 2 * kQuD;
+  __nv_bfloat16* m = P.meta + size_t(tile) * 2 * kQuD;
   *reinterpret_cast<uint2*>(m + 4 * lane) = make_uint2(pack_bf16x2(mn[0], mn[1]), pack_bf16x2(mn[2], mn[3]));
   *reinterpret_cast<uint2*>(m + kQuD + 4 * lane) =
       make_uint2(pack_bf16x2(mx[0], mx[1]), pack_bf16x2(mx[2], mx[3]));
 }
 
 // ---------------------------------------------------------------------------
+// kWide: 9..16 q heads per kv head, heads 8.. in a second N = 8 column of MMAs
+template <bool kWide>
 __global__ void __launch_bounds__(kQuBoundThreads) qu_bound_kernel(const QuParams P) {
   const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   int S;
@@ -175,15 +188,15 @@ __global__ void __launch_bounds__(kQuBoundThreads) qu_bound_kernel(const QuParam
   const int pa = S_old / kQuPage;
   if (P.appended && pa >= p0 && pa < p1) {
     // the new token: K and V rows, then the page's min / max (first token: itself)
-    const int phys = qu_phys(P, b, pa);
-    const size_t row = (size_t(phys) * P.Hkv + kvh) * kQuPage + (S_old % kQuPage);
+    const int tile = qu_tile(P, b, kvh, pa);
+    const size_t row = size_t(tile) * kQuPage + (S_old % kQuPage);
     const __nv_bfloat16* kn = P.k_new + (size_t(b) * P.Hkv + kvh) * kQuD;
     const __nv_bfloat16* vn = P.v_new + (size_t(b) * P.Hkv + kvh) * kQuD;
     if (tid < 16) reinterpret_cast<uint4*>(P.k_pool + row * kQuD)[tid] = reinterpret_cast<const uint4*>(kn)[tid];
     else if (tid < 32) reinterpret_cast<uint4*>(P.v_pool + row * kQuD)[tid - 16] = reinterpret_cast<const uint4*>(vn)[tid - 16];
     else if (tid < 48) {
       const int u = tid - 32;  // 8 dimensions
-      __nv_bfloat16* m = P.meta + (size_t(phys) * P.Hkv + kvh) * 2 * kQuD;
+      __nv_bfloat16* m = P.meta + size_t(tile) * 2 * kQuD;
       const uint4 x = reinterpret_cast<const uint4*>(kn)[u];
       uint4 lo = x, hi = x;
       if (S_old % kQuPage != 0) {
@@ -209,11 +222,14 @@ __global__ void __launch_bounds__(kQuBoundThreads) qu_bound_kernel(const QuParam
   // k-step 2u + v takes entries 32u + 8c + 4v + {0, 1} as logical k {2c, 2c + 1} and
   // + {2, 3} as {2c + 8, 2c + 9}, on A and B alike.
   const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, cq = lane & 3;
-  uint32_t bfr[16][2];
-  {
+  constexpr int kCols = kWide ? 2 : 1;  // 8-head columns: heads 8 j .. 8 j + 7
+  uint32_t bfr[kCols][16][2];
+#pragma unroll
+  for (int j = 0; j < kCols; ++j) {
+    const int hq = 8 * j + gq;
     uint4 qraw[4] = {};
-    if (gq < G) {
-      const uint4* qrow = reinterpret_cast<const uint4*>(P.q + (size_t(b) * P.Hq + size_t(kvh) * G + gq) * kQuD);
+    if (hq < G) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(P.q + (size_t(b) * P.Hq + size_t(kvh) * G + hq) * kQuD);
 #pragma unroll
       for (int u = 0; u < 4; ++u) qraw[u] = qrow[4 * u + cq];  // dims 32u + 8c .. + 7
     }
@@ -234,42 +250,48 @@ __global__ void __launch_bounds__(kQuBoundThreads) qu_bound_kernel(const QuParam
         }
         w[i] = r;
       }
-      bfr[2 * u][0] = w[0];
-      bfr[2 * u][1] = w[1];
-      bfr[2 * u + 1][0] = w[2];
-      bfr[2 * u + 1][1] = w[3];
+      bfr[j][2 * u][0] = w[0];
+      bfr[j][2 * u][1] = w[1];
+      bfr[j][2 * u + 1][0] = w[2];
+      bfr[j][2 * u + 1][1] = w[3];
     }
   }
   __syncthreads();  // orders the append's min / max before the reads below
   const int pe = min(p1, n_full);
-  float* bnd = P.bounds + (size_t(b) * P.Hq + size_t(kvh) * G) * P.max_pages;
+  float* bnd = P.bounds + (size_t(b) * P.Hq + size_t(kvh) * G) * P.max_qp;
   constexpr int kWarps = kQuBoundThreads / 32;
 #pragma unroll 1
   for (int tp = p0 + warp * 16; tp < pe; tp += kWarps * 16) {
     const int pg0 = tp + gq, pg1 = tp + gq + 8;
-    const uint4* r0 = pg0 < pe ? reinterpret_cast<const uint4*>(P.meta + (size_t(qu_phys(P, b, pg0)) * P.Hkv + kvh) * 2 * kQuD) : nullptr;
-    const uint4* r1 = pg1 < pe ? reinterpret_cast<const uint4*>(P.meta + (size_t(qu_phys(P, b, pg1)) * P.Hkv + kvh) * 2 * kQuD) : nullptr;
+    const uint4* r0 = pg0 < pe ? reinterpret_cast<const uint4*>(P.meta + size_t(qu_tile(P, b, kvh, pg0)) * 2 * kQuD) : nullptr;
+    const uint4* r1 = pg1 < pe ? reinterpret_cast<const uint4*>(P.meta + size_t(qu_tile(P, b, kvh, pg1)) * 2 * kQuD) : nullptr;
     uint4 x0[8], x1[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       x0[u] = r0 ? __ldcg(r0 + 4 * u + cq) : make_uint4(0u, 0u, 0u, 0u);
       x1[u] = r1 ? __ldcg(r1 + 4 * u + cq) : make_uint4(0u, 0u, 0u, 0u);
     }
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    float c[kCols][4] = {};
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      mma_bf16_16816(c, x0[u].x, x1[u].x, x0[u].y, x1[u].y, bfr[2 * u][0], bfr[2 * u][1]);
-      mma_bf16_16816(c, x0[u].z, x1[u].z, x0[u].w, x1[u].w, bfr[2 * u + 1][0], bfr[2 * u + 1][1]);
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) {
+        mma_bf16_16816(c[j], x0[u].x, x1[u].x, x0[u].y, x1[u].y, bfr[j][2 * u][0], bfr[j][2 * u][1]);
+        mma_bf16_16816(c[j], x0[u].z, x1[u].z, x0[u].w, x1[u].w, bfr[j][2 * u + 1][0], bfr[j][2 * u + 1][1]);
+      }
     }
-    // c: pages (gq, gq + 8) x heads (2 cq, 2 cq + 1)
-    const int h0 = 2 * cq, h1 = 2 * cq + 1;
-    if (pg0 < pe) {
-      if (h0 < G) bnd[size_t(h0) * P.max_pages + pg0] = c[0];
-      if (h1 < G) bnd[size_t(h1) * P.max_pages + pg0] = c[1];
-    }
-    if (pg1 < pe) {
-      if (h0 < G) bnd[size_t(h0) * P.max_pages + pg1] = c[2];
-      if (h1 < G) bnd[size_t(h1) * P.max_pages + pg1] = c[3];
+    // c[j]: pages (gq, gq + 8) x heads (8 j + 2 cq, 8 j + 2 cq + 1)
+#pragma unroll
+    for (int j = 0; j < kCols; ++j) {
+      const int h0 = 8 * j + 2 * cq, h1 = h0 + 1;
+      if (pg0 < pe) {
+        if (h0 < G) bnd[size_t(h0) * P.max_qp + pg0] = c[j][0];
+        if (h1 < G) bnd[size_t(h1) * P.max_qp + pg0] = c[j][1];
+      }
+      if (pg1 < pe) {
+        if (h0 < G) bnd[size_t(h0) * P.max_qp + pg1] = c[j][2];
+        if (h1 < G) bnd[size_t(h1) * P.max_qp + pg1] = c[j][3];
+      }
     }
   }
 }
@@ -384,7 +406,7 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
   if (!qu_len_ok(P, b, S)) return;
   const int n_full = S / kQuPage, k = P.budget;
   int32_t* sel = P.sel + (size_t(b) * P.Hq + h) * k;
-  uint32_t* msk = P.mask + (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  uint32_t* msk = P.mask + (size_t(b) * P.Hkv + kvh) * P.max_qp;
   const uint32_t bit = 1u << g;
   if (n_full <= k) {
     for (int i = tid; i < k; i += kRkThreads) {
@@ -392,13 +414,13 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
       if (i < n_full) atomicOr(msk + i, bit);
     }
   } else if (n_full <= kQuSmallRow) {
-    const float* row = P.bounds + (size_t(b) * P.Hq + h) * P.max_pages;
+    const float* row = P.bounds + (size_t(b) * P.Hq + h) * P.max_qp;
     qu_small_topk(row, n_full, k, sm.hist, sm.wtot[0], sm.wtot[1], [&](int i, int p) {
       sel[i] = p;
       atomicOr(msk + p, bit);
     });
   } else {
-    const float* row = P.bounds + (size_t(b) * P.Hq + h) * P.max_pages;
+    const float* row = P.bounds + (size_t(b) * P.Hq + h) * P.max_qp;
     const F32RowKeys src{row, 0, n_full, (reinterpret_cast<uintptr_t>(row) & 15u) == 0};
     row_topk<kQuTopkGroups>(src, k, 0u, sm, [&](int i, int p) {
       sel[i] = p;
@@ -418,9 +440,9 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
   __syncthreads();
   if (!s_last) return;
   // list the marked pages in ascending order (block scan per round of 1024)
-  int32_t* ul = P.ulist + (size_t(b) * P.Hkv + kvh) * P.max_pages;
-  int32_t* uph = P.uphys + (size_t(b) * P.Hkv + kvh) * P.max_pages;
-  uint32_t* um = P.umask + (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  int32_t* ul = P.ulist + (size_t(b) * P.Hkv + kvh) * P.max_qp;
+  int32_t* uph = P.uphys + (size_t(b) * P.Hkv + kvh) * P.max_qp;
+  uint32_t* um = P.umask + (size_t(b) * P.Hkv + kvh) * P.max_qp;
   uint32_t total_all = 0;
   for (int r0 = 0; r0 < n_full; r0 += kRkThreads) {
     const int i = r0 + tid;
@@ -429,7 +451,7 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
     const uint32_t off = rk_block_excl_scan(m != 0u ? 1u : 0u, sm.wtot[0], tot);
     if (m != 0u) {
       ul[total_all + off] = i;
-      uph[total_all + off] = qu_phys(P, b, i);
+      uph[total_all + off] = qu_tile(P, b, kvh, i);
       um[total_all + off] = m;
       msk[i] = 0u;
     }
@@ -439,7 +461,7 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
     int n = int(total_all);
     if (S % kQuPage != 0) {  // the partial page, for every head
       ul[n] = n_full;
-      uph[n] = qu_phys(P, b, n_full);
+      uph[n] = qu_tile(P, b, kvh, n_full);
       um[n] = (G >= 32) ? 0xFFFFFFFFu : ((1u << G) - 1u);
       ++n;
     }
@@ -448,6 +470,8 @@ __global__ void __launch_bounds__(kRkThreads) qu_topk_kernel(const QuParams P) {
 }
 
 // ---------------------------------------------------------------------------
+// kWide: 9..16 q heads per kv head (attend_tile_wide: head g + 8 in MMA rows 8..15)
+template <bool kWide>
 __global__ void __launch_bounds__(kQuAttnWarps * 32) qu_attn_kernel(const QuParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -461,36 +485,38 @@ __global__ void __launch_bounds__(kQuAttnWarps * 32) qu_attn_kernel(const QuPara
   const int n_full = S / kQuPage, tail = S % kQuPage;
   const int t0 = int((long long)split * n / P.splits), t1 = int((long long)(split + 1) * n / P.splits);
   const int G = P.G, g = lane >> 2, qd = lane & 3;
-  const bool head_ok = g < G;
-  const size_t lbase = (size_t(b) * P.Hkv + kvh) * P.max_pages;
+  const bool head_ok = g < G, head_ok2 = kWide && g + 8 < G;
+  const size_t lbase = (size_t(b) * P.Hkv + kvh) * P.max_qp;
   const uint32_t wbuf = smem_u32(smem + warp * kQuAttnStages * 8192);
+  const int num_tiles = (P.num_pages * P.Hkv) << P.page_shift;
 
-  uint32_t qa[8][2];
+  uint32_t qa[8][2], qb[8][2];
   load_q_frags(P.q + (size_t(b) * P.Hq + kvh * G + (head_ok ? g : 0)) * kQuD, head_ok, qd, qa);
+  if (kWide) load_q_frags(P.q + (size_t(b) * P.Hq + kvh * G + (head_ok2 ? g + 8 : 0)) * kQuD, head_ok2, qd, qb);
   TileState st;
   st.init();
 
   // this warp's list entries are t0 + warp + 4 i; lane j holds entry cbase + j of
-  // the current chunk of 32 (page, physical page, head mask), read ahead in one go
+  // the current chunk of 32 (page, pool tile, head mask), read ahead in one go
   const int nw = t0 + warp < t1 ? (t1 - t0 - warp + kQuAttnWarps - 1) / kQuAttnWarps : 0;
-  int cbase = 0, c_page = 0, c_phys = 0;
+  int cbase = 0, c_page = 0, c_tile = 0;
   uint32_t c_mask = 0u;
   auto load_chunk = [&](int base) {
     const int e = t0 + warp + kQuAttnWarps * (base + lane);
     const bool ok = base + lane < nw;
     c_page = ok ? P.ulist[lbase + e] : 0;
-    c_phys = ok ? P.uphys[lbase + e] : 0;
+    c_tile = ok ? P.uphys[lbase + e] : 0;
     c_mask = ok ? P.umask[lbase + e] : 0u;
   };
-  auto entry = [&](int i, int& page, int& phys, uint32_t& m) {  // called by the whole warp
+  auto entry = [&](int i, int& page, int& tile, uint32_t& m) {  // called by the whole warp
     if (i - cbase < 32) {
       page = __shfl_sync(0xffffffffu, c_page, i - cbase);
-      phys = __shfl_sync(0xffffffffu, c_phys, i - cbase);
+      tile = __shfl_sync(0xffffffffu, c_tile, i - cbase);
       m = __shfl_sync(0xffffffffu, c_mask, i - cbase);
     } else {  // read-ahead past the chunk: straight from the list
       const size_t e = lbase + t0 + warp + size_t(kQuAttnWarps) * i;
       page = P.ulist[e];
-      phys = P.uphys[e];
+      tile = P.uphys[e];
       m = P.umask[e];
     }
   };
@@ -499,12 +525,12 @@ __global__ void __launch_bounds__(kQuAttnWarps * 32) qu_attn_kernel(const QuPara
   // entry i into stage s: its page's 16 K rows then 16 V rows (rows past a
   // partial page's tokens are zero-filled)
   auto gather = [&](int i, int s) {
-    int page, phys;
+    int page, tile;
     uint32_t m;
-    entry(i, page, phys, m);
-    if (unsigned(phys) >= unsigned(P.num_pages)) phys = 0;  // reported when the list was built
+    entry(i, page, tile, m);
+    if (unsigned(tile) >= unsigned(num_tiles)) tile = 0;  // a bad entry was reported when the list was built
     const int valid = page == n_full ? tail : kQuPage;
-    const size_t base = ((size_t(phys) * P.Hkv + kvh) * kQuPage) * kQuD;
+    const size_t base = size_t(tile) * kQuPage * kQuD;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       const int c = lane + 32 * k;
@@ -535,20 +561,25 @@ __global__ void __launch_bounds__(kQuAttnWarps * 32) qu_attn_kernel(const QuPara
     commit();
     asm volatile("cp.async.wait_group %0;" ::"n"(kQuAttnStages - 1) : "memory");
     __syncwarp();
-    int page, phys;
+    int page, tile;
     uint32_t m;
-    entry(i, page, phys, m);
+    entry(i, page, tile, m);
     const bool on = head_ok && ((m >> g) & 1u);
-    float x0, x1, x2, x3;
-    attend_tile(wbuf + s * 8192, wbuf + s * 8192 + 4096, qa, page == n_full ? tail : kQuPage, P.scale_log2, st,
-                x0, x1, x2, x3, on);
+    const int valid = page == n_full ? tail : kQuPage;
+    if (kWide) {
+      const bool on2 = head_ok2 && ((m >> (g + 8)) & 1u);
+      attend_tile_wide(wbuf + s * 8192, wbuf + s * 8192 + 4096, qa, qb, valid, P.scale_log2, st, on, on2);
+    } else {
+      float x0, x1, x2, x3;
+      attend_tile(wbuf + s * 8192, wbuf + s * 8192 + 4096, qa, valid, P.scale_log2, st, x0, x1, x2, x3, on);
+    }
     __syncwarp();
     s = s + 1 == kQuAttnStages ? 0 : s + 1;
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();  // every warp is done with the ring: it becomes the merge scratch
   float* slot = P.part + ((size_t(b) * P.Hkv + kvh) * P.splits + split) * kPartFloats;
-  merge_warps_to_slot<kQuAttnWarps>(st, wo, slot, G);
+  merge_warps_to_slot<kQuAttnWarps, kWide>(st, wo, slot, G);
   __syncthreads();
   if (tid == 0) {
     __threadfence();
@@ -583,7 +614,7 @@ namespace {
 struct QuWs {
   size_t cnt, bounds, sel, mask, ulist, uphys, umask, ucount, part, total;
 };
-QuWs qu_ws_layout(int batch, int Hq, int Hkv, int max_pages, int budget, bool own_bounds, bool own_sel) {
+QuWs qu_ws_layout(int batch, int Hq, int Hkv, int max_qp, int budget, bool own_bounds, bool own_sel) {
   QuWs w;
   size_t off = kStatusBytes;
   auto take = [&](size_t bytes) {
@@ -592,12 +623,12 @@ QuWs qu_ws_layout(int batch, int Hq, int Hkv, int max_pages, int budget, bool ow
     return o;
   };
   w.cnt = take((size_t(batch) * Hkv * 2 + batch) * 4);
-  w.bounds = own_bounds ? take(size_t(batch) * Hq * max_pages * 4) : 0;
+  w.bounds = own_bounds ? take(size_t(batch) * Hq * max_qp * 4) : 0;
   w.sel = own_sel ? take(size_t(batch) * Hq * budget * 4) : 0;
-  w.mask = take(size_t(batch) * Hkv * max_pages * 4);
-  w.ulist = take(size_t(batch) * Hkv * max_pages * 4);
-  w.uphys = take(size_t(batch) * Hkv * max_pages * 4);
-  w.umask = take(size_t(batch) * Hkv * max_pages * 4);
+  w.mask = take(size_t(batch) * Hkv * max_qp * 4);
+  w.ulist = take(size_t(batch) * Hkv * max_qp * 4);
+  w.uphys = take(size_t(batch) * Hkv * max_qp * 4);
+  w.umask = take(size_t(batch) * Hkv * max_qp * 4);
   w.ucount = take(size_t(batch) * Hkv * 4);
   w.part = take(size_t(batch) * Hkv * kTileMaxSplits * kPartFloats * 4);
   w.total = off;
@@ -612,10 +643,13 @@ extern "C" kvsel_status kvsel_quest_page_meta(const kvsel_paged_kv* kv, const in
   if (!kv || !kv->k_pool || !block_table || !seq_lens || !page_meta || !status_word || batch < 1 || max_pages < 1)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "kv, block_table, seq_lens, page_meta, status_word required; "
                                             "batch, max_pages >= 1");
-  if (kv->head_dim != kQuD || kv->page_size != kQuPage)
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16 are implemented");
+  if (kv->head_dim != kQuD || page_shift_of(kv->page_size) < 0)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "head_dim 128 and page_size 16, 32, 64, 128 or 256 are implemented");
   if (kv->num_kv_heads < 1 || kv->num_pages < 1 || batch > 65535 || kv->num_kv_heads > 65535)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "num_kv_heads and num_pages >= 1; batch, num_kv_heads <= 65535");
+  if ((long long)max_pages * kv->page_size >= (1LL << 31) ||
+      (long long)kv->num_pages * kv->num_kv_heads * kv->page_size >= (1LL << 31))
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "max_pages * page_size and num_pages * num_kv_heads * page_size < 2^31");
   if (!aligned(kv->k_pool, 16) || !aligned(page_meta, 16) || !aligned(status_word, 4))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "K pool and page_meta must be 16-byte aligned");
   QuMetaParams P;
@@ -627,9 +661,11 @@ extern "C" kvsel_status kvsel_quest_page_meta(const kvsel_paged_kv* kv, const in
   P.max_pages = max_pages;
   P.Hkv = kv->num_kv_heads;
   P.num_pages = kv->num_pages;
+  P.page_shift = page_shift_of(kv->page_size);
+  P.max_qp = max_pages << P.page_shift;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   trace_before("qu_meta", st);
-  qu_meta_kernel<<<dim3((max_pages + 3) / 4, P.Hkv, batch), 128, 0, st>>>(P);
+  qu_meta_kernel<<<dim3((P.max_qp + 3) / 4, P.Hkv, batch), 128, 0, st>>>(P);
   const cudaError_t e = cudaGetLastError();
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_quest_page_meta (launch)");
@@ -639,10 +675,11 @@ extern "C" kvsel_status kvsel_quest_page_meta(const kvsel_paged_kv* kv, const in
 extern "C" size_t kvsel_quest_decode_workspace(const kvsel_paged_kv* kv, int batch, int max_pages, int budget_pages,
                                                int with_bounds_out, int with_pages_out) {
   if (!kv || batch < 1 || max_pages < 1 || budget_pages < 1 || kv->num_kv_heads < 1 ||
-      kv->num_q_heads % kv->num_kv_heads != 0)
+      kv->num_q_heads % kv->num_kv_heads != 0 || page_shift_of(kv->page_size) < 0 ||
+      (long long)max_pages * kv->page_size >= (1LL << 31))
     return 0;
-  return qu_ws_layout(batch, kv->num_q_heads, kv->num_kv_heads, max_pages, budget_pages, with_bounds_out == 0,
-                      with_pages_out == 0).total;
+  return qu_ws_layout(batch, kv->num_q_heads, kv->num_kv_heads, max_pages << page_shift_of(kv->page_size),
+                      budget_pages, with_bounds_out == 0, with_pages_out == 0).total;
 }
 
 extern "C" kvsel_status kvsel_quest_decode(const kvsel_paged_kv* kv, const int32_t* block_table, int max_pages,
@@ -652,12 +689,12 @@ extern "C" kvsel_status kvsel_quest_decode(const kvsel_paged_kv* kv, const int32
                                            void* workspace, size_t ws_bytes, void* stream) {
   const std::string fn = "kvsel_quest_decode: ";
   if (!kv || !kv->k_pool || !kv->v_pool) return fail(KVSEL_ERR_INVALID_ARG, fn + "kv pools must be non-NULL");
-  if (kv->head_dim != kQuD || kv->page_size != kQuPage)
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "only head_dim 128 and page_size 16 are implemented");
+  if (kv->head_dim != kQuD || page_shift_of(kv->page_size) < 0)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "head_dim 128 and page_size 16, 32, 64, 128 or 256 are implemented");
   if (kv->num_kv_heads < 1 || kv->num_q_heads < 1 || kv->num_q_heads % kv->num_kv_heads != 0)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "num_q_heads must be a positive multiple of num_kv_heads");
   const int Hkv = kv->num_kv_heads, Hq = kv->num_q_heads, G = Hq / Hkv;
-  if (G > kQuMaxG) return fail(KVSEL_ERR_UNSUPPORTED, fn + "at most 8 q heads per kv head");
+  if (G > kQuMaxG) return fail(KVSEL_ERR_UNSUPPORTED, fn + "at most 16 q heads per kv head");
   if (!block_table || !seq_lens || !q || !out || !page_meta || batch < 1 || max_pages < 1 || budget_pages < 1)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "block_table, seq_lens, q, out, page_meta are required; batch, "
                                             "max_pages, budget_pages >= 1");
@@ -665,24 +702,26 @@ extern "C" kvsel_status kvsel_quest_decode(const kvsel_paged_kv* kv, const int32
     return fail(KVSEL_ERR_INVALID_ARG, fn + "k_new and v_new must both be given or both NULL");
   if (out_dtype != KVSEL_BF16 && out_dtype != KVSEL_F32)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "out_dtype must be KVSEL_BF16 or KVSEL_F32");
-  if (batch > 65535 || Hq > 65535 || (long long)max_pages * kQuPage >= (1LL << 31) ||
-      (long long)kv->num_pages * Hkv * kQuPage >= (1LL << 31) || kv->num_pages < 1)
-    return fail(KVSEL_ERR_UNSUPPORTED, fn + "batch, num_q_heads <= 65535; max_pages * 16 and num_pages * "
-                                            "num_kv_heads * 16 < 2^31");
+  if (batch > 65535 || Hq > 65535 || (long long)max_pages * kv->page_size >= (1LL << 31) ||
+      (long long)kv->num_pages * Hkv * kv->page_size >= (1LL << 31) || kv->num_pages < 1)
+    return fail(KVSEL_ERR_UNSUPPORTED, fn + "batch, num_q_heads <= 65535; max_pages * page_size and num_pages * "
+                                            "num_kv_heads * page_size < 2^31");
   if (!aligned(kv->k_pool, 16) || !aligned(kv->v_pool, 16) || !aligned(q, 16) || !aligned(page_meta, 16) ||
       (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))))
     return fail(KVSEL_ERR_INVALID_ARG, fn + "pools, q, k_new, v_new and page_meta must be 16-byte aligned");
-  const QuWs L = qu_ws_layout(batch, Hq, Hkv, max_pages, budget_pages, bounds_out == nullptr, pages_out == nullptr);
+  const int page_shift = page_shift_of(kv->page_size);
+  const int max_qp = max_pages << page_shift;  // Quest pages (16 tokens) per block-table row
+  const QuWs L = qu_ws_layout(batch, Hq, Hkv, max_qp, budget_pages, bounds_out == nullptr, pages_out == nullptr);
   if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total)
     return fail(KVSEL_ERR_INVALID_ARG, fn + "workspace missing, misaligned or smaller than " +
                                            std::to_string(L.total));
 
   const int sms = sm_count();
-  const int list_max = std::min(max_pages, G * budget_pages + 1);
+  const int list_max = std::min(max_qp, G * budget_pages + 1);
   int splits = std::max(1, (sms * 2) / (batch * Hkv));  // one wave at two CTAs per SM
   splits = std::min(splits, std::max(1, (list_max + 7) / 8));
   splits = std::min(splits, kTileMaxSplits);
-  const int chunks = std::max(1, std::min(65535, (max_pages + kQuBoundPagesPerCta - 1) / kQuBoundPagesPerCta));
+  const int chunks = std::max(1, std::min(65535, (max_qp + kQuBoundPagesPerCta - 1) / kQuBoundPagesPerCta));
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   QuParams P;
@@ -709,6 +748,8 @@ extern "C" kvsel_status kvsel_quest_decode(const kvsel_paged_kv* kv, const int32
   P.status = reinterpret_cast<int*>(ws);
   P.B = batch;
   P.max_pages = max_pages;
+  P.page_shift = page_shift;
+  P.max_qp = max_qp;
   P.Hq = Hq;
   P.Hkv = Hkv;
   P.G = G;
@@ -722,7 +763,8 @@ extern "C" kvsel_status kvsel_quest_decode(const kvsel_paged_kv* kv, const int32
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   {
-    cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(qu_attn_kernel), int(kQuAttnSmem));
+    cudaError_t e0 = smem_limit_once(reinterpret_cast<const void*>(qu_attn_kernel<false>), int(kQuAttnSmem));
+    if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(qu_attn_kernel<true>), int(kQuAttnSmem));
     if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(qu_topk_kernel), int(sizeof(RowTopkSmem)));
     if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_quest_decode (attribute)");
   }
@@ -733,9 +775,17 @@ extern "C" kvsel_status kvsel_quest_decode(const kvsel_paged_kv* kv, const int32
   e = cudaGetLastError();                                                \
   trace_after(st);                                                       \
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_quest_decode (" name ")");
-  KVSEL_QU_LAUNCH("qu_bound", qu_bound_kernel, dim3(chunks, Hkv, batch), kQuBoundThreads, 0)
+  if (G > 8) {
+    KVSEL_QU_LAUNCH("qu_bound", qu_bound_kernel<true>, dim3(chunks, Hkv, batch), kQuBoundThreads, 0)
+  } else {
+    KVSEL_QU_LAUNCH("qu_bound", qu_bound_kernel<false>, dim3(chunks, Hkv, batch), kQuBoundThreads, 0)
+  }
   KVSEL_QU_LAUNCH("qu_topk", qu_topk_kernel, dim3(Hq, batch), kRkThreads, sizeof(RowTopkSmem))
-  KVSEL_QU_LAUNCH("qu_attn", qu_attn_kernel, dim3(splits, Hkv, batch), kQuAttnWarps * 32, kQuAttnSmem)
+  if (G > 8) {
+    KVSEL_QU_LAUNCH("qu_attn", qu_attn_kernel<true>, dim3(splits, Hkv, batch), kQuAttnWarps * 32, kQuAttnSmem)
+  } else {
+    KVSEL_QU_LAUNCH("qu_attn", qu_attn_kernel<false>, dim3(splits, Hkv, batch), kQuAttnWarps * 32, kQuAttnSmem)
+  }
 #undef KVSEL_QU_LAUNCH
   return KVSEL_OK;
 }

@@ -791,7 +791,7 @@ def _setup_sparse_decode(dev, small=False):
 
     # Quest page selection on the same cache: top_k / 16 pages (2048 tokens) per q head
     budget_pages = wl.top_k // 16
-    meta = torch.zeros(wl.num_pages, wl.Hkv, 2, wl.d, dtype=torch.bfloat16, device=dev)
+    meta = torch.zeros(wl.num_pages, wl.Hkv, wl.page // 16, 2, wl.d, dtype=torch.bfloat16, device=dev)
     seq_q = seq0.clone()
     ws_q = K.workspace(K.kvsel_quest_decode_workspace(kv, wl.B, wl.max_pages, budget_pages))
     K.kvsel_quest_page_meta(kv, bt, seq_q, meta, ws_q)

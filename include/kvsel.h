@@ -30,12 +30,11 @@
  * [batch][max_pages]; token slot t of sequence b lives in page
  * block_table[b][t / page_size], row t % page_size.  Supported here:
  * head_dim = 128; num_q_heads / num_kv_heads <= 16 for the decode step
- * (and its block signal) and the sparse decode, <= 8 for SnapKV and Quest;
- * and page_size 16, 32,
- * 64, 128 or 256 for the decode step, the H2O evict, the keep-list
- * compaction and the sparse decode (the kernels address a page in 16-token
- * tiles); SnapKV, Quest and the decode step's block signal take page_size
- * 16 only (else KVSEL_ERR_UNSUPPORTED).
+ * (and its block signal), the sparse decode and Quest, <= 8 for SnapKV;
+ * and page_size 16, 32, 64, 128 or 256 for the decode step, the H2O evict,
+ * the keep-list compaction, the sparse decode and Quest (the kernels
+ * address a page in 16-token tiles); SnapKV and the decode step's block
+ * signal take page_size 16 only (else KVSEL_ERR_UNSUPPORTED).
  */
 #ifndef KVSEL_H
 #define KVSEL_H
@@ -591,7 +590,8 @@ KVSEL_API kvsel_status kvsel_snapkv_select_ex(const kvsel_paged_kv* kv, const in
  * elementwise min and max of its keys, and the best-bounded pages are kept).
  *
  * Defines, for sequence b (S_b keys once the new token is appended) and q
- * head h (kv head h / G):
+ * head h (kv head h / G), with Quest pages of 16 tokens whatever the pool's
+ * page_size (a pool page of P tokens holds P / 16 of them):
  *   bound[b][h][p] = sum_d max(q_d * kmin[p]_d, q_d * kmax[p]_d), for every
  *                    full page p < S_b / 16 (kmin / kmax over its 16 keys)
  *   pages[b][h]    = the budget_pages largest bounds, ties to the lower page
@@ -600,9 +600,10 @@ KVSEL_API kvsel_status kvsel_snapkv_select_ex(const kvsel_paged_kv* kv, const in
  *                    and those of the trailing partial page (always kept)
  * Each q head chooses alone.
  *
- * Page metadata (both calls): page_meta bf16 [num_pages][num_kv_heads][2][128]
- * indexed by PHYSICAL page: the min row, then the max row, of the page's keys
- * (its valid keys for a partial page).  kvsel_quest_page_meta fills it for
+ * Page metadata (both calls): page_meta bf16
+ * [num_pages][num_kv_heads][page_size / 16][2][128] indexed by PHYSICAL pool
+ * page, then the Quest page within it: the min row, then the max row, of that
+ * Quest page's keys (its valid keys for a partial page).  kvsel_quest_page_meta fills it for
  * every page 0..ceil(seq_lens[b] / 16) - 1 of each sequence (after a prefill);
  * kvsel_quest_decode keeps it current as it appends.
  *
@@ -616,17 +617,19 @@ KVSEL_API kvsel_status kvsel_snapkv_select_ex(const kvsel_paged_kv* kv, const in
  *                 kvsel_decode_attn (k_new / v_new both given or both NULL;
  *                 seq_lens += 1 when appending, published at the end).
  *   page_meta     as above; updated for the appended token's page.
- *   budget_pages  >= 1 full pages per q head (budget / 16 tokens).
+ *   budget_pages  >= 1 full Quest pages per q head (budget / 16 tokens).
  *   out           [batch][num_q_heads][128], bf16 or fp32 (out_dtype).
- *   pages_out     int32 [batch][num_q_heads][budget_pages] or NULL: pages[b][h],
- *                 -1 padded.
- *   bounds_out    fp32 [batch][num_q_heads][max_pages] or NULL: bound[b][h][p]
- *                 for p < S_b / 16 (the rest untouched).
+ *   pages_out     int32 [batch][num_q_heads][budget_pages] or NULL: pages[b][h]
+ *                 (Quest page indices), -1 padded.
+ *   bounds_out    fp32 [batch][num_q_heads][max_pages * page_size / 16] or
+ *                 NULL: bound[b][h][p] for p < S_b / 16 (the rest untouched).
  *   workspace     >= kvsel_quest_decode_workspace(kv, batch, max_pages,
  *                 budget_pages, bounds_out != NULL, pages_out != NULL) bytes,
  *                 zeroed before its first use (it carries counters and page
  *                 masks that every call leaves at zero).
- * Limits: head_dim 128, page_size 16, G <= 8 (else UNSUPPORTED).
+ * Limits: head_dim 128, page_size 16, 32, 64, 128 or 256, G <= 16 (else
+ * UNSUPPORTED); max_pages * page_size and num_pages * num_kv_heads *
+ * page_size < 2^31.
  * Launches: bounds (+ append), per-head top-k (+ the kv head's page list),
  * attention over the listed pages.
  */

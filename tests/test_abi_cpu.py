@@ -225,7 +225,16 @@ def test_quest_host_validation(lib):
         return lib.kvsel_quest_decode(ctypes.byref(kv_), a["bt"], a["max_pages"], a["seq"], a["B"], a["q"], a["kn"],
                                       a["vn"], a["meta"], a["budget"], a["scale"], a["out"], a["odt"], a["pages"],
                                       a["bounds"], a["ws"], a["ws_bytes"], None)
-    assert st(kv_=_kv(num_q_heads=128, num_pages=64)) == K.KVSEL_ERR_UNSUPPORTED   # G = 16
+    assert st(kv_=_kv(num_q_heads=136, num_pages=64)) == K.KVSEL_ERR_UNSUPPORTED   # G = 17
+    assert st(kv_=_kv(page_size=512, num_pages=64)) == K.KVSEL_ERR_UNSUPPORTED
+    assert st(kv_=_kv(page_size=48, num_pages=64)) == K.KVSEL_ERR_UNSUPPORTED
+    assert lib.kvsel_quest_page_meta(ctypes.byref(_kv(page_size=512)), 16, 64, 16, 2, 16, 256,
+                                     None) == K.KVSEL_ERR_UNSUPPORTED
+    # 256-token pool pages hold 16 Quest pages each: per-page buffers grow 16-fold with max_pages fixed
+    w16 = K.kvsel_quest_decode_workspace(kv, 2, 64, 8, True, True)
+    w256 = K.kvsel_quest_decode_workspace(_kv(page_size=256, num_pages=64), 2, 64, 8, True, True)
+    assert w256 - w16 >= 15 * 4 * (2 * 8 * 64 * 4)
+    assert K.kvsel_quest_decode_workspace(_kv(page_size=48, num_pages=64), 2, 64, 8) == 0
     assert st(kn=16) == K.KVSEL_ERR_INVALID_ARG                                   # k_new without v_new
     assert st(budget=0) == K.KVSEL_ERR_INVALID_ARG
     assert st(meta=None) == K.KVSEL_ERR_INVALID_ARG

@@ -33,16 +33,17 @@ class QuestState:
         self.wl = wl
         self.budget = budget
         dev = "cuda"
-        self.kpool = bf16(workloads.paged_pool(wl.K, wl.block_table, wl.num_pages))
-        self.vpool = bf16(workloads.paged_pool(wl.V, wl.block_table, wl.num_pages))
+        self.kpool = bf16(workloads.paged_pool(wl.K, wl.block_table, wl.num_pages, page=wl.page))
+        self.vpool = bf16(workloads.paged_pool(wl.V, wl.block_table, wl.num_pages, page=wl.page))
         self.kv = K.paged_kv(self.kpool, self.vpool, wl.Hq)
+        tiles = wl.page // PAGE       # Quest pages per pool page
         self.guards = g = Guards()
         self.bt = g.like(torch.from_numpy(wl.block_table).to(dev))
         self.seq = g.like(torch.full((wl.B,), wl.S0, dtype=torch.int32, device=dev))
-        self.meta = g.new((wl.num_pages, wl.Hkv, 2, wl.d), torch.bfloat16)
+        self.meta = g.new((wl.num_pages, wl.Hkv, tiles, 2, wl.d), torch.bfloat16)
         self.out = g.new((wl.B, wl.Hq, wl.d), torch.float32 if out_f32 else torch.bfloat16)
         self.pages = g.new((wl.B, wl.Hq, budget), torch.int32, fill=-7)
-        self.bounds = g.new((wl.B, wl.Hq, wl.max_pages), torch.float32)
+        self.bounds = g.new((wl.B, wl.Hq, wl.max_pages * tiles), torch.float32)
         self.ws = g.new((K.kvsel_quest_decode_workspace(self.kv, wl.B, wl.max_pages, budget, True, True),),
                         torch.uint8)
         K.kvsel_quest_page_meta(self.kv, self.bt, self.seq, self.meta, self.ws)
@@ -76,9 +77,9 @@ def _check_meta(st, appended):
         for kvh in range(wl.Hkv):
             kmin, kmax = dsa.page_minmax(Kb[kvh], PAGE)
             for p in range(-(-S // PAGE)):
-                phys = wl.block_table[b, p]
-                np.testing.assert_array_equal(meta[phys, kvh, 0], kmin[p])
-                np.testing.assert_array_equal(meta[phys, kvh, 1], kmax[p])
+                phys, j = wl.block_table[b, p * PAGE // wl.page], (p * PAGE % wl.page) // PAGE
+                np.testing.assert_array_equal(meta[phys, kvh, j, 0], kmin[p])
+                np.testing.assert_array_equal(meta[phys, kvh, j, 1], kmax[p])
 
 
 def _check(st, t, appended, heads=None):
@@ -128,6 +129,42 @@ def test_steps_across_a_page_boundary():
     assert st.seq.cpu().tolist() == [2034, 2034]
 
 
+@pytest.mark.parametrize("page,S0", [(256, 2555), (64, 1000), (32, 5)])
+def test_pool_pages_of_32_to_256_tokens(page, S0):
+    """Quest pages stay 16 tokens inside larger pool pages: appends cross Quest-page and (at 256:
+    the sixth append is token 2560) pool-page boundaries; meta, bounds, pages and output as at
+    page 16."""
+    wl = workloads.sparse_decode(seed=60 + page, B=2, S0=S0, steps=8, Hq=16, Hkv=2, page=page)
+    st = QuestState(wl, budget=12)
+    torch.cuda.synchronize()
+    _check_meta(st, 0)
+    for t in range(wl.steps):
+        st.step(t)
+        _check(st, t, t + 1)
+    _check_meta(st, wl.steps)
+    assert st.seq.cpu().tolist() == [S0 + wl.steps] * wl.B
+
+
+def test_sixteen_heads_choose_their_own_pages_at_page_256():
+    # a planted page per q head of a 16-head group: heads 8..15 run in the wide tile's second half
+    wl = workloads.sparse_decode(seed=48, B=1, S0=4000, steps=1, Hq=16, Hkv=1, page=256)
+    Kf = bf16_bits_to_f64(wl.K[0]).astype(np.float32)
+    qf = bf16_bits_to_f64(wl.q[0, 0]).astype(np.float32)
+    planted = {}
+    for h in range(wl.Hq):
+        p = 7 + 15 * h
+        u = qf[h] / np.linalg.norm(qf[h])
+        Kf[0, p * PAGE:(p + 1) * PAGE] += 6.0 * u
+        planted[h] = p
+    wl.K = workloads.f32_to_bf16_bits(Kf)[None]
+    st = QuestState(wl, budget=3)
+    st.step(0)
+    _check(st, 0, 1)
+    pages = st.pages.cpu().numpy()
+    for h, p in planted.items():
+        assert p in pages[0, h].tolist()
+
+
 def test_without_append_and_with_every_page_in_budget():
     wl = workloads.sparse_decode(seed=42, B=3, S0=300, steps=1, Hq=16, Hkv=4)
     st = QuestState(wl, budget=32)
@@ -152,7 +189,7 @@ def test_short_contexts(S0):
     _check_meta(st, 2)
 
 
-@pytest.mark.parametrize("G,budget", [(1, 3), (8, 20), (5, 64)])
+@pytest.mark.parametrize("G,budget", [(1, 3), (8, 20), (5, 64), (12, 40), (16, 20)])
 def test_group_sizes_budgets_and_bf16_output(G, budget):
     wl = workloads.sparse_decode(seed=50 + G, B=2, S0=6000 + G, steps=1, Hq=4 * G, Hkv=4)
     st = QuestState(wl, budget=budget, out_f32=False)
