@@ -22,7 +22,17 @@
 //                     top 12 key bits to a per-row histogram (a shared-memory
 //                     histogram per CTA, flushed once); also writes the
 //                     appended token's K, V and indexer key.
-//   sd_select_kernel  (slices, sequence), 1024 threads: every CTA finds, from
+//   sd_select_cluster_kernel  (8 CTAs, sequence), one 8-CTA cluster of 1024
+//                     threads per row, rows up to 256K positions: each CTA
+//                     holds a chunk of the row's scores in shared memory,
+//                     takes the k-th key's top 12 bits from the histogram,
+//                     compacts its candidates (keys in or above that bin) in
+//                     one sweep, and resolves the other 20 bits in two radix
+//                     passes whose counts the cluster sums through
+//                     distributed shared memory; every CTA then writes its
+//                     own kept positions, in ascending order, at offsets
+//                     from the cluster's kept counts.
+//   sd_select_kernel  (slices, sequence), longer rows, 1024 threads: every CTA finds, from
 //                     the histogram, the bin holding the k-th largest score
 //                     and appends the positions of its slice scoring in or
 //                     above that bin to a candidate list (a few thousand at
@@ -593,6 +603,287 @@ __device__ __forceinline__ float sd_cluster_ld(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t sd_cluster_ld_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Select for rows of up to kSdCsMaxLen positions, one thread-block cluster of
+// kSdCsCtas CTAs per row.  CTA r copies a contiguous chunk of the row's
+// scores into its shared memory (warp w: R rounds of 128 consecutive
+// positions, 16 bytes a lane) and takes from the indexer's histogram the
+// 12-bit bin of the k-th largest key.  One sweep over the chunk then
+// compacts, per warp and in position order, the candidates -- keys in or
+// above that bin, a few hundred per CTA -- into the warp's own part of the
+// buffer; every later step reads the candidates only.  The cluster resolves the k-th key T in two 10-bit radix passes: every CTA adds
+// its counts (aggregated per warp) into a histogram in each CTA of the
+// cluster through distributed shared memory, and after a cluster barrier each
+// CTA finds the same digit in its own copy.  Each CTA counts its kept candidates (above T, and equal to it), pushes
+// the totals into every CTA of the cluster, and after a last barrier writes
+// its kept positions, in ascending order, straight to the output.  One round
+// trip to global memory (the scores, the histogram and the block-table
+// entries, issued together) and four cluster barriers, the first while the
+// scores are in flight, against the slice
+// select's hand-off of candidates through global memory to one final CTA.
+constexpr int kSdCsCtas = 8;
+constexpr int kSdCsMaxRounds = 8;                                     // 128-position rounds per warp
+constexpr int kSdCsChunkMax = 32 * 128 * kSdCsMaxRounds;              // positions per CTA
+constexpr int kSdCsMaxLen = kSdCsCtas * kSdCsChunkMax;                // 262144
+constexpr int kSdCsDigit = 10;                                        // two passes below the 12-bit bin
+constexpr int kSdCsBins = 1 << kSdCsDigit;
+static_assert(kSdCsBins == kSdSelThreads, "one radix bin per thread");
+static_assert(kSdHistBits + 2 * kSdCsDigit == 32, "the bin and two digits make the whole key");
+static_assert(kSdCsChunkMax <= 65536, "chunk positions fit 16 bits");
+struct SdCsSmem {
+  uint32_t key[kSdCsChunkMax];          // the chunk's scores (raw bits), then each warp's candidate keys
+  uint16_t cpos[kSdCsChunkMax];         // the candidates' chunk positions
+  int32_t pg[kSdCsChunkMax / 16 + 1];   // block-table entries of the chunk's pages
+  uint32_t tot[2][kSdCsBins];           // the two passes' counts over the cluster, added by every CTA
+  uint32_t wtot[32];                    // block-scan scratch
+  uint32_t wg[32], we[32];              // per-warp kept counts (above / equal to T), then prefixes
+  uint32_t allcnt[kSdCsCtas][2];        // every CTA's kept counts, stored here by that CTA
+  uint32_t found_d, found_k;
+  int bstar;
+  uint32_t above;
+};
+
+__device__ __forceinline__ void sd_cluster_st_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sd_cluster_add_u32(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Counts one key per lane into the histogram `hist` of every CTA of the cluster: lanes with the
+// same digit add once (a row of equal scores sends thousands of keys to one bin).  Called by the
+// whole warp.
+__device__ __forceinline__ void sd_warp_count(uint32_t* hist, bool live, uint32_t digit) {
+  if (__ballot_sync(0xffffffffu, live)) {
+    const uint32_t d = live ? digit : 0xFFFFFFFFu;
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    if (live && int(threadIdx.x & 31) == __ffs(peers) - 1) {
+      const uint32_t n = uint32_t(__popc(peers));
+#pragma unroll
+      for (int q = 0; q < kSdCsCtas; ++q) sd_cluster_add_u32(sd_cluster_addr(&hist[d], uint32_t(q)), n);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSdSelThreads) sd_select_cluster_kernel(const SdParams P) {
+  extern __shared__ __align__(16) uint8_t cs_smem_raw[];
+  SdCsSmem& sm = *reinterpret_cast<SdCsSmem*>(cs_smem_raw);
+  const int r = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // scores and histogram are complete
+  // Every early return below is taken by the whole cluster (it depends on the row only), so no
+  // CTA is left waiting at a cluster barrier.
+  int S;
+  if (!sd_len_ok(P, b, S)) return;
+  const int k = min(P.top_k, S);
+  int32_t* sel = P.sel + size_t(b) * P.top_k;
+  int32_t* tko = P.topk_out ? P.topk_out + size_t(b) * P.top_k : nullptr;
+  int32_t* srow_out = P.sel_row + size_t(b) * P.top_k;
+  const int32_t* bt = P.block_table + size_t(b) * P.max_pages;
+  uint32_t* ghist = P.hist + size_t(b) * kSdHistBins;
+  const int lg = 4 + P.page_shift;
+  auto pool_row = [&](int pos, int phys) {  // the position's pool row for kv head 0
+    if (unsigned(phys) >= unsigned(P.num_pages)) {
+      report(P.status, KVSEL_ERR_BAD_INDEX);
+      phys = 0;
+    }
+    return ((phys * P.Hkv) << lg) + (pos & ((1 << lg) - 1));
+  };
+  if (k == S) {  // every position is selected: CTA 0 writes them
+    if (r != 0) return;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int i = tid; i < S; i += kSdSelThreads) {
+      sel[i] = i;
+      srow_out[i] = pool_row(i, bt[i >> lg]);
+      if (tko) tko[i] = i;
+    }
+    for (int i = tid; i < kSdHistBins; i += kSdSelThreads) ghist[i] = 0u;
+    if (tko)
+      for (int i = k + tid; i < P.top_k; i += kSdSelThreads) tko[i] = -1;
+    if (tid == 0) P.nsel[b] = k;
+    return;
+  }
+  // chunk: R rounds of 128 positions per warp, 32 warps; positions [c0, c0 + lim) are live
+  const int R = (S + kSdCsCtas * 32 * 128 - 1) / (kSdCsCtas * 32 * 128);  // <= kSdCsMaxRounds (host)
+  const int W = 128 * R, C = 32 * W, c0 = r * C;
+  const int lim = max(0, min(C, S - c0));
+  const float* srow = P.scores + size_t(b) * P.max_len;
+  {
+    const uint32_t base = smem_u32(sm.key);
+    for (int i = 0; i < R; ++i) {
+      const int rel = warp * W + i * 128 + 4 * lane;
+      if (P.scores_vec) {  // the row is 16-byte aligned and a multiple of 4 long: 16 bytes a lane
+        cp_async16(base + rel * 4, rel < lim ? srow + c0 + rel : srow, rel < lim);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          cp_async4(base + (rel + e) * 4, rel + e < lim ? srow + c0 + rel + e : srow, rel + e < lim);
+      }
+    }
+    cp_async_commit();
+  }
+  const int pfirst = c0 >> lg;
+  const int npg = lim > 0 ? ((c0 + lim - 1) >> lg) - pfirst + 1 : 0;  // <= C / 16 + 1
+  for (int i = tid; i < npg; i += kSdSelThreads) sm.pg[i] = bt[pfirst + i];
+  uint32_t h[4];
+  sd_load_bins(ghist, h);
+  // the cluster totals this CTA receives start at zero before any CTA adds to them (the barrier
+  // waits while the copies above are in flight)
+  sm.tot[0][tid] = 0u;
+  sm.tot[1][tid] = 0u;
+  if (tid == 0) {
+    sm.bstar = 0;
+    sm.above = 0u;
+  }
+  sd_cluster_sync();
+  sd_find_bin(h, uint32_t(k), sm.wtot, &sm.bstar, &sm.above);
+  const uint32_t bstar = uint32_t(sm.bstar);
+  uint32_t kt = uint32_t(k) - sm.above;  // the k-th key's rank among the keys of its bin
+  cp_async_wait<0>();
+  __syncthreads();  // scores, page entries and cleared histograms visible to the CTA
+
+  // the sweep: each warp's candidates compacted in place, in position order (lane l takes
+  // positions 32 e + l of each 128-position round, so a ballot per e gives every candidate its
+  // place)
+  constexpr int kLoShift = 32 - kSdHistBits;  // 20: bits below the bin
+  const uint32_t lo_key = bstar << kLoShift;
+  uint32_t* wkey = sm.key + warp * W;
+  uint16_t* wpos = sm.cpos + warp * W;
+  const unsigned below = (1u << lane) - 1u;
+  uint32_t nw = 0;  // the warp's candidates so far
+  for (int i = 0; i < R; ++i) {
+    const int rel0 = warp * W + i * 128 + lane;
+    uint32_t kq[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) kq[e] = order_key(__uint_as_float(sm.key[rel0 + 32 * e]));
+    __syncwarp();  // the round is read before anyone overwrites it (writes stay below its end)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool cand = rel0 + 32 * e < lim && kq[e] >= lo_key;
+      const unsigned m = __ballot_sync(0xffffffffu, cand);
+      if (cand) {
+        const uint32_t at = nw + __popc(m & below);
+        wkey[at] = kq[e];
+        wpos[at] = uint16_t(rel0 + 32 * e);
+      }
+      nw += __popc(m);
+    }
+  }
+  __syncwarp();
+  const uint32_t nw_pad = (nw + 31u) & ~31u;
+
+  uint32_t prefix = bstar;
+  int shift = kLoShift;  // bits of the key below the prefix
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int dshift = shift - kSdCsDigit;
+    uint32_t* hh = sm.tot[pass];
+    for (uint32_t j = lane; j < nw_pad; j += 32) {
+      const uint32_t key = j < nw ? wkey[j] : 0u;
+      sd_warp_count(hh, j < nw && (key >> shift) == prefix, (key >> dshift) & (kSdCsBins - 1));
+    }
+    sd_cluster_sync();  // every CTA's counts of this pass have arrived
+    if (pass == 0 && tid < kSdHistBins / kSdCsCtas)  // every CTA has read the histogram: clear its share
+      ghist[r * (kSdHistBins / kSdCsCtas) + tid] = 0u;
+    // thread t: digit 1023 - t; the digit holding the kt-th key, from the top
+    const int d = kSdCsBins - 1 - tid;
+    const uint32_t v = hh[d];
+    if (tid == 0) {
+      sm.found_d = 0u;
+      sm.found_k = 1u;
+    }
+    uint32_t total;
+    const uint32_t above = rk_block_excl_scan(v, sm.wtot, total);
+    if (above < kt && kt <= above + v) {
+      sm.found_d = uint32_t(d);
+      sm.found_k = kt - above;
+    }
+    __syncthreads();
+    prefix = (prefix << kSdCsDigit) | sm.found_d;
+    kt = sm.found_k;
+    shift = dshift;
+  }
+  const uint32_t T = prefix, need_eq = kt;  // kept: every key above T and the first need_eq equal to it
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // kept candidates per warp, the warps' prefixes, the CTA's totals to every CTA of the cluster
+  {
+    uint32_t ng = 0, ne = 0;
+    for (uint32_t j = lane; j < nw; j += 32) {
+      const uint32_t key = wkey[j];
+      ng += key > T ? 1u : 0u;
+      ne += key == T ? 1u : 0u;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      ng += __shfl_xor_sync(0xffffffffu, ng, o);
+      ne += __shfl_xor_sync(0xffffffffu, ne, o);
+    }
+    if (lane == 0) {
+      sm.wg[warp] = ng;
+      sm.we[warp] = ne;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t g0 = sm.wg[lane], e0 = sm.we[lane];
+      uint32_t gi = g0, ei = e0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t yg = __shfl_up_sync(0xffffffffu, gi, o), ye = __shfl_up_sync(0xffffffffu, ei, o);
+        if (lane >= o) {
+          gi += yg;
+          ei += ye;
+        }
+      }
+      sm.wg[lane] = gi - g0;
+      sm.we[lane] = ei - e0;
+      const uint32_t G = __shfl_sync(0xffffffffu, gi, 31), E = __shfl_sync(0xffffffffu, ei, 31);
+      if (lane < kSdCsCtas) {  // lane q stores this CTA's totals into CTA q
+        sd_cluster_st_u32(sd_cluster_addr(&sm.allcnt[r][0], uint32_t(lane)), G);
+        sd_cluster_st_u32(sd_cluster_addr(&sm.allcnt[r][1], uint32_t(lane)), E);
+      }
+    }
+  }
+  sd_cluster_sync();  // every CTA's totals are here; no distributed shared memory access follows
+  uint32_t before_g = 0, before_e = 0;
+  for (int q = 0; q < r; ++q) {
+    before_g += sm.allcnt[q][0];
+    before_e += sm.allcnt[q][1];
+  }
+  // emission in position order: a kept key at position p goes to (keys above T before p) +
+  // min(keys equal to T before p, need_eq)
+  {
+    uint32_t g_run = before_g + sm.wg[warp], e_run = before_e + sm.we[warp];
+    for (uint32_t j0 = 0; j0 < nw_pad; j0 += 32) {
+      const uint32_t j = j0 + lane;
+      const uint32_t key = j < nw ? wkey[j] : 0u;
+      const bool gt = j < nw && key > T, eq = j < nw && key == T;
+      const unsigned mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
+      const uint32_t gb = g_run + __popc(mg & below), eb = e_run + __popc(me & below);
+      if (gt || (eq && eb < need_eq)) {
+        const uint32_t o = gb + min(eb, need_eq);
+        if (o < uint32_t(k)) {
+          const int pos = c0 + int(wpos[j]);
+          sel[o] = pos;
+          srow_out[o] = pool_row(pos, sm.pg[(pos >> lg) - pfirst]);
+          if (tko) tko[o] = pos;
+        }
+      }
+      g_run += __popc(mg);
+      e_run += __popc(me);
+    }
+  }
+  if (r == 0 && tid == 0) P.nsel[b] = k;
+}
+
 // kWide: 9..16 q heads per kv head (attend_tile_wide)
 template <bool kWide>
 __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdParams P) {
@@ -714,9 +1005,14 @@ __global__ void __launch_bounds__(kSdAttnWarps * 32) sd_attn_kernel(const SdPara
   const int e1 = (split + 1) * E / ns;
   for (int idx = split * E / ns + tid; idx < e1; idx += kSdAttnWarps * 32) {
     const int gg = idx / kSdD, dd = idx % kSdD;
+    float pv[kSdMaxClusterSplits];  // every split's value issued before any is used
+#pragma unroll
+    for (int sp = 0; sp < kSdMaxClusterSplits; ++sp)
+      pv[sp] = sp < ns ? sd_cluster_ld(sd_cluster_addr(&s_part[2 * kSdMaxG + gg * kSdD + dd], uint32_t(sp))) : 0.f;
     float acc = 0.f;
-    for (int sp = 0; sp < ns; ++sp)
-      acc += s_f[sp][gg] * sd_cluster_ld(sd_cluster_addr(&s_part[2 * kSdMaxG + gg * kSdD + dd], sp));
+#pragma unroll
+    for (int sp = 0; sp < kSdMaxClusterSplits; ++sp)
+      if (sp < ns) acc += s_f[sp][gg] * pv[sp];
     const size_t oi = (size_t(b) * P.Hq + size_t(kvh) * G + gg) * kSdD + dd;
     if (P.out_f32) static_cast<float*>(P.out)[oi] = acc;
     else static_cast<__nv_bfloat16*>(P.out)[oi] = __float2bfloat16_rn(acc);
@@ -873,6 +1169,8 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
     if (e0 == cudaSuccess) e0 = smem_limit_once(reinterpret_cast<const void*>(sd_index_kernel), int(kSdIdxSmem));
     if (e0 == cudaSuccess)
       e0 = smem_limit_once(reinterpret_cast<const void*>(sd_select_kernel), int(sizeof(SdSelSmem)));
+    if (e0 == cudaSuccess)
+      e0 = smem_limit_once(reinterpret_cast<const void*>(sd_select_cluster_kernel), int(sizeof(SdCsSmem)));
     if (e0 != cudaSuccess) return cuda_fail(e0, "kvsel_sparse_decode (attribute)");
   }
   cudaError_t e;
@@ -880,8 +1178,8 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;  // the attention's splits of a pair: one cluster
-  attr[1].val.clusterDim.x = unsigned(splits);
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // set per launch below
+  attr[1].val.clusterDim.x = 1;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.stream = st;
@@ -898,8 +1196,14 @@ extern "C" kvsel_status kvsel_sparse_decode(const kvsel_paged_kv* kv, const int3
   trace_after(st);                                                       \
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_sparse_decode (" name ")");
   KVSEL_SD_LAUNCH("sd_index", sd_index_kernel, dim3(idx_ctas, batch), kSdIdxWarps * 32, kSdIdxSmem, 1)
-  KVSEL_SD_LAUNCH("sd_select", sd_select_kernel, dim3(slices, batch),
-                  kSdSelThreads, sizeof(SdSelSmem), 1)
+  if (max_len <= kSdCsMaxLen) {  // a row's select: one cluster of kSdCsCtas CTAs
+    attr[1].val.clusterDim.x = unsigned(kSdCsCtas);
+    KVSEL_SD_LAUNCH("sd_select", sd_select_cluster_kernel, dim3(kSdCsCtas, batch), kSdSelThreads,
+                    sizeof(SdCsSmem), 2)
+  } else {  // longer rows: slices of 16K positions hand their candidates to the row's last CTA
+    KVSEL_SD_LAUNCH("sd_select", sd_select_kernel, dim3(slices, batch), kSdSelThreads, sizeof(SdSelSmem), 1)
+  }
+  attr[1].val.clusterDim.x = unsigned(splits);  // the attention's splits of a pair: one cluster
   if (G > 8) {
     KVSEL_SD_LAUNCH("sd_attn", sd_attn_kernel<true>, dim3(splits, Hkv, batch), kSdAttnWarps * 32, kSdAttnSmem, 2)
   } else {

@@ -117,13 +117,38 @@ def test_larger_pages_across_a_page_boundary(page):
 @pytest.mark.parametrize("S0", [140000, 250000])
 def test_scores_all_at_most_zero_tie_thousands_at_zero(S0):
     """Every indexer weight negative: every score is <= 0 and thousands of keys tie at exactly 0
-    (10.2K at 140K keys: the final select's candidate list; 14.2K at 250K: past its capacity,
-    the whole-row select).  Ties go to the lower positions."""
+    (10.2K at 140K keys, 14.2K at 250K), all in one radix bin of the cluster select.  Ties go to
+    the lower positions."""
     wl = workloads.sparse_decode(seed=25, B=1, S0=S0, steps=1, Hq=16, Hkv=2, top_k=2048)
     wl.w_idx = -np.abs(wl.w_idx)
     st = SparseState(wl)
     st.step(0)
     _check(st, 0)
+
+
+def test_aligned_score_rows_across_the_select_cluster():
+    """Rows whose length is a multiple of 4 (16-byte score copies in the cluster select), chunks
+    of 2 rounds per warp, the last CTA of the cluster partly and the rest of the chunk empty."""
+    wl = workloads.sparse_decode(seed=26, B=2, S0=65533, steps=3, top_k=2048)
+    assert wl.max_len % 4 == 0
+    st = SparseState(wl)
+    for t in range(3):
+        st.step(t)
+        _check(st, t)
+    assert K.read_status(st.ws) == 0
+
+
+@pytest.mark.parametrize("negative", [False, True])
+def test_rows_longer_than_the_select_cluster(negative):
+    """270K positions: past the cluster select's 256K, the slice select with its final CTA (and,
+    with every score <= 0, its whole-row fallback)."""
+    wl = workloads.sparse_decode(seed=27, B=1, S0=270000, steps=1, Hq=8, Hkv=1, top_k=2048)
+    if negative:
+        wl.w_idx = -np.abs(wl.w_idx)
+    st = SparseState(wl)
+    st.step(0)
+    _check(st, 0)
+    assert K.read_status(st.ws) == 0
 
 
 def test_short_context_selects_all_and_matches_dense():
