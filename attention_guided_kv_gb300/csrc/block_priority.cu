@@ -317,10 +317,14 @@ __device__ __forceinline__ void bp_rank_sort(unsigned long long* sk, int npow, i
 // column, one scan over (digit, warp) turns the columns into offsets, and the
 // keys are scattered.  Equal scores keep block order, the specified tie-break.
 constexpr int kRankRadixMax = 8192;
+// A warp's histogram column is a row of 257 words: the leaders of one warp (different digits)
+// then hit different banks, and the scan below, which walks (digit, warp) order 8 counts per
+// thread, reads 32 distinct banks per instruction.
+constexpr int kRankHistPitch = 257;
 struct RankRadixSmem {
   uint32_t key[2][kRankRadixMax];
   uint16_t idx[2][kRankRadixMax];
-  uint32_t hist[256 * 32];  // [digit][warp]
+  uint32_t hist[32 * kRankHistPitch];  // [warp][digit], padded: see kRankHistPitch
   uint32_t wsum[32];
 };
 __device__ __forceinline__ void bp_rank_radix(RankRadixSmem& sm, int n, long long b0, int r, const BpParams& P) {
@@ -338,7 +342,7 @@ __device__ __forceinline__ void bp_rank_radix(RankRadixSmem& sm, int n, long lon
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 8 * pass;
-    for (int j = tid; j < 256 * 32; j += 1024) sm.hist[j] = 0u;
+    for (int j = tid; j < 32 * kRankHistPitch; j += 1024) sm.hist[j] = 0u;
     __syncthreads();
     uint32_t pos[8];
 #pragma unroll
@@ -348,17 +352,19 @@ __device__ __forceinline__ void bp_rank_radix(RankRadixSmem& sm, int n, long lon
       const int leader = __ffs(peers) - 1;
       uint32_t old = 0;
       if (lane == leader) {
-        old = sm.hist[d * 32 + warp];
-        sm.hist[d * 32 + warp] = old + __popc(peers);
+        old = sm.hist[warp * kRankHistPitch + d];
+        sm.hist[warp * kRankHistPitch + d] = old + __popc(peers);
       }
       pos[e] = __shfl_sync(0xffffffffu, old, leader) + __popc(peers & lt);
     }
     __syncthreads();
     {  // exclusive scan of the 8192 counts in (digit, warp) order: 8 per thread
+      // count q = tid * 8 + j is digit q / 32 of warp q % 32
+      auto at = [&](int q) -> uint32_t& { return sm.hist[(q & 31) * kRankHistPitch + (q >> 5)]; };
       uint32_t c[8], run = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c[j] = sm.hist[tid * 8 + j];
+        c[j] = at(tid * 8 + j);
         run += c[j];
       }
       uint32_t incl = run;
@@ -383,7 +389,7 @@ __device__ __forceinline__ void bp_rank_radix(RankRadixSmem& sm, int n, long lon
       uint32_t base = sm.wsum[warp] + incl - run;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        sm.hist[tid * 8 + j] = base;
+        at(tid * 8 + j) = base;
         base += c[j];
       }
     }
@@ -392,7 +398,7 @@ __device__ __forceinline__ void bp_rank_radix(RankRadixSmem& sm, int n, long lon
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const uint32_t d = (k[e] >> shift) & 255u;
-      const uint32_t dst = sm.hist[d * 32 + warp] + pos[e];
+      const uint32_t dst = sm.hist[warp * kRankHistPitch + d] + pos[e];
       sm.key[ob][dst] = k[e];
       sm.idx[ob][dst] = v[e];
     }
