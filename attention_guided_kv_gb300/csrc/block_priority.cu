@@ -51,7 +51,7 @@ struct BpParams {
   uint32_t* key[2];          // workspace [max_blocks] x 2
   int64_t* val[2];           // workspace [max_blocks] x 2
   int64_t* meta;             // workspace [3]: N (or -1), evict count, evictable (all-cold) blocks
-  unsigned* hist;            // workspace [kBpMaxSortCtas][16]
+  unsigned* hist;            // workspace [2][kBpMaxSortCtas][16]
   unsigned* bar;             // grid-barrier words
   int* status;
   int64_t max_blocks, order_cap;
@@ -483,6 +483,7 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
   __shared__ unsigned base[16];
   __shared__ unsigned sTot[kBpSortThreads / 16][16], sBefore[kBpSortThreads / 16][16];
   __shared__ unsigned wtot[kBpSortThreads / 32][16];
+  __shared__ int s_same;
   const long long N = P.meta[0];
   if (N < 0) return;  // same for every CTA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -491,13 +492,17 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
   const long long per = (c1 - c0 + kBpSortThreads - 1) / kBpSortThreads;
   const long long t0 = min(c1, c0 + per * tid), t1 = min(c1, t0 + per);
 
+  int cur = 0;  // the buffer holding the keys sorted so far
 #pragma unroll 1
   for (int pass = 0; pass < 8; ++pass) {
     const int shift = 4 * pass;
-    const uint32_t* ik = P.key[pass & 1];
-    const int64_t* iv = P.val[pass & 1];
-    uint32_t* ok = P.key[(pass + 1) & 1];
-    int64_t* ov = P.val[(pass + 1) & 1];
+    const uint32_t* ik = P.key[cur];
+    const int64_t* iv = P.val[cur];
+    uint32_t* ok = P.key[cur ^ 1];
+    int64_t* ov = P.val[cur ^ 1];
+    // the CTAs' digit counts alternate between two halves: a pass whose scatter is skipped has no
+    // second barrier, so a CTA may write the next pass's counts while another still reads these
+    unsigned* phist = P.hist + (pass & 1) * (kBpMaxSortCtas * 16);
     // this thread's digit counts (its keys are a contiguous run of the input)
     unsigned v[16];
 #pragma unroll
@@ -531,7 +536,7 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
         wtot[w][tid] = run;
         run += t;
       }
-      P.hist[c * 16 + tid] = run;  // this CTA's count of digit tid
+      phist[c * 16 + tid] = run;  // this CTA's count of digit tid
     }
     __syncthreads();
 #pragma unroll
@@ -543,7 +548,7 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
       const int d = tid & 15, stripe = tid >> 4;
       unsigned tot = 0, before = 0;
       for (int cc = stripe; cc < NC; cc += kBpSortThreads / 16) {
-        const unsigned h = __ldcg(P.hist + cc * 16 + d);
+        const unsigned h = __ldcg(phist + cc * 16 + d);
         tot += h;
         if (cc < c) before += h;
       }
@@ -561,15 +566,18 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
       }
       __syncthreads();
       if (tid == 0) {
-        unsigned run = 0;
+        unsigned run = 0, widest = 0;
         for (int dd = 0; dd < 16; ++dd) {
           const unsigned t = sTot[0][dd];
           base[dd] += run;
           run += t;
+          widest = max(widest, t);
         }
+        s_same = widest == run;  // one digit holds every key: the stable scatter would not move one
       }
     }
     __syncthreads();
+    if (s_same) continue;  // the same in every CTA: no scatter, no barrier, the keys stay where they are
     for (long long e = t0; e < t1; ++e) {
       const uint32_t k = ik[e];
       const unsigned d = (k >> shift) & 15u;
@@ -578,8 +586,8 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
       ov[pos] = iv[e];
     }
     if (!bp_grid_barrier(P.bar, P.status)) return;  // timed out: stop before any scatter
+    cur ^= 1;
   }
-  // 8 passes: the sorted keys are back in buffer 0
   long long n_all = P.meta[1];
   if (P.agg == kAggAllCold) {  // only the evictable blocks (they sort first)
     n_all = min(n_all, (long long)P.meta[2]);
@@ -587,7 +595,7 @@ __global__ void __launch_bounds__(kBpSortThreads) bp_sort_kernel(const BpParams 
   }
   const long long n_ev = min(n_all, (long long)P.order_cap);
   for (long long i = (long long)c * kBpSortThreads + tid; i < n_ev; i += (long long)NC * kBpSortThreads)
-    P.order_out[i] = __ldcg(P.val[0] + i);
+    P.order_out[i] = __ldcg(P.val[cur] + i);
 }
 
 }  // namespace kvsel
@@ -614,7 +622,7 @@ BpWs bp_ws_layout(int R, long long max_blocks) {
   w.val0 = take(size_t(max_blocks) * 8);
   w.val1 = take(size_t(max_blocks) * 8);
   w.meta = take(24);
-  w.hist = take(size_t(kBpMaxSortCtas) * 16 * 4);
+  w.hist = take(size_t(2) * kBpMaxSortCtas * 16 * 4);
   w.total = off;
   return w;
 }
