@@ -128,7 +128,111 @@ __global__ void __launch_bounds__(1024) bp_prefix_kernel(const BpParams P) {
   }
 }
 
-__global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
+// One token's score update (decay, max over steps or the sliding-window sum), written back.
+__device__ __forceinline__ float bp_update_token(const BpParams& P, float* hslot, long long t) {
+  float s = P.tok[t];
+  if (P.inc) {
+    const float in = P.inc[t];
+    if (P.update == kUpdMax) {
+      s = fmaxf(s, in);
+    } else if (P.update == kUpdWindow) {  // the increment leaving the window is replaced
+      float* h = hslot + t;
+      s = s + (in - *h);
+      *h = in;
+    } else {
+      s = fmaf(P.decay, s, in);
+    }
+    P.tok[t] = s;
+  }
+  return s;
+}
+
+// The block's outputs (lane-independent): score, its copy out, the all-cold count, the sort key.
+__device__ __forceinline__ void bp_block_out(const BpParams& P, long long g, int r, float result) {
+  P.bscore[g] = result;
+  if (P.bscore_out) P.bscore_out[g] = result;
+  const bool hot_block = P.agg == kAggAllCold && result >= P.threshold;  // never evicted
+  if (P.agg == kAggAllCold && !hot_block) atomicAdd(reinterpret_cast<unsigned long long*>(P.meta + 2), 1ull);
+  if (P.norm == 0) {  // no normalisation: sort directly on the block score
+    P.key[0][g] = hot_block ? 0xFFFFFFFFu : order_key(result);
+    P.val[0][g] = ((long long)r << 32) | (g - P.blk_off[r]);
+  }
+}
+
+// Blocks of up to 32 tokens: one lane per block.  A warp takes 32 consecutive blocks, whose tokens
+// are one contiguous run of the CSR array (requests lie back to back): the warp loads, updates and
+// writes that run back coalesced through its shared-memory buffer, then each lane folds its own
+// block from there (a warp per block would have at most one block's 64..128 bytes in flight).
+// The mean sums the block in token order, the top-p mean takes the maximum k times.
+constexpr int kBpFoldThreads = 256;
+__device__ __forceinline__ void bp_fold_lanes(const BpParams& P, long long N, float* hslot) {
+  __shared__ float sbuf[kBpFoldThreads / 32][32 * 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* buf = sbuf[warp];
+  const long long wstride = (long long)gridDim.x * (blockDim.x >> 5) * 32;
+  for (long long g0 = ((long long)blockIdx.x * (blockDim.x >> 5) + warp) * 32; g0 < N; g0 += wstride) {
+    const long long g = g0 + lane;
+    const bool live = g < N;
+    int r = 0, n = 0;
+    long long t0 = 0;
+    if (live) {
+      r = bp_request_of(P.blk_off, P.R, g);
+      t0 = P.off[r] + (g - P.blk_off[r]) * P.bs;
+      n = int(min((long long)P.bs, P.off[r + 1] - t0));
+    }
+    const unsigned act = __ballot_sync(0xffffffffu, live);
+    const int last = 31 - __clz(act);
+    const long long T0 = __shfl_sync(0xffffffffu, t0, 0);
+    const long long T1 = __shfl_sync(0xffffffffu, t0 + n, last);
+    for (long long x = lane; x < T1 - T0; x += 32) buf[x] = bp_update_token(P, hslot, T0 + x);
+    __syncwarp();
+    float v[32];
+    float sum = 0.f, mx = -INFINITY;
+    int hot = 0;
+    const int rel = int(t0 - T0);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      v[t] = -INFINITY;
+      if (t < n) {
+        const float s = buf[rel + t];
+        v[t] = s;
+        sum += s;
+        mx = fmaxf(mx, s);
+        hot += s >= P.threshold ? 1 : 0;
+      }
+    }
+    float result;
+    if (P.agg == kAggMax || P.agg == kAggAllCold) {
+      result = mx;
+    } else if (P.agg == kAggFracHot) {
+      result = __fdiv_rn(float(hot), float(n));
+    } else if (P.agg == kAggMean) {
+      result = __fdiv_rn(sum, float(n));
+    } else {
+      const int k = max(1, int(ceilf(__fmul_rn(P.top_p, float(n)))));
+      float acc = 0.f;
+      for (int it = 0; it < k; ++it) {  // the largest remaining, the lowest token on ties
+        float m = -INFINITY;
+        int at = 0;
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (v[t] > m) {
+            m = v[t];
+            at = t;
+          }
+        acc += m;
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (t == at) v[t] = -INFINITY;
+      }
+      result = __fdiv_rn(acc, float(k));
+    }
+    if (live) bp_block_out(P, g, r, result);
+    __syncwarp();  // every lane has read the buffer before the next group refills it
+  }
+}
+
+__global__ void __launch_bounds__(kBpFoldThreads) bp_fold_kernel(const BpParams P) {
   const long long N = P.meta[0];
   if (N <= 0) return;
   const int lane = threadIdx.x & 31;
@@ -136,6 +240,10 @@ __global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
   constexpr int kPer = kBpMaxBlockSize / 32;
   // sliding-window update: this step's slot of the history ring
   float* const hslot = P.update == kUpdWindow ? P.whist + (P.step % P.window) * P.hist_tokens : nullptr;
+  if (P.bs <= 32) {
+    bp_fold_lanes(P, N, hslot);
+    return;
+  }
   for (long long g = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < N; g += warps) {
     const int r = bp_request_of(P.blk_off, P.R, g);
     const long long t0 = P.off[r] + (g - P.blk_off[r]) * P.bs;
@@ -147,20 +255,7 @@ __global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
       const int t = lane + 32 * e;
       v[e] = -INFINITY;
       if (t < n) {
-        float s = P.tok[t0 + t];
-        if (P.inc) {
-          const float in = P.inc[t0 + t];
-          if (P.update == kUpdMax) {
-            s = fmaxf(s, in);
-          } else if (P.update == kUpdWindow) {  // the increment leaving the window is replaced
-            float* h = hslot + t0 + t;
-            s = s + (in - *h);
-            *h = in;
-          } else {
-            s = fmaf(P.decay, s, in);
-          }
-          P.tok[t0 + t] = s;
-        }
+        const float s = bp_update_token(P, hslot, t0 + t);
         v[e] = s;
         sum += s;
         mx = fmaxf(mx, s);
@@ -216,16 +311,7 @@ __global__ void __launch_bounds__(256) bp_fold_kernel(const BpParams P) {
       }
       result = __fdiv_rn(acc, float(k));
     }
-    if (lane == 0) {
-      P.bscore[g] = result;
-      if (P.bscore_out) P.bscore_out[g] = result;
-      const bool hot_block = P.agg == kAggAllCold && result >= P.threshold;  // never evicted
-      if (P.agg == kAggAllCold && !hot_block) atomicAdd(reinterpret_cast<unsigned long long*>(P.meta + 2), 1ull);
-      if (P.norm == 0) {  // no normalisation: sort directly on the block score
-        P.key[0][g] = hot_block ? 0xFFFFFFFFu : order_key(result);
-        P.val[0][g] = ((long long)r << 32) | (g - P.blk_off[r]);
-      }
-    }
+    if (lane == 0) bp_block_out(P, g, r, result);
   }
 }
 
@@ -734,7 +820,7 @@ extern "C" kvsel_status kvsel_block_priority_ex(float* token_scores, const float
 
   const int sms = sm_count();
   trace_before("bp_fold", st);
-  bp_fold_kernel<<<sms * 8, 256, 0, st>>>(P);
+  bp_fold_kernel<<<sms * 8, kBpFoldThreads, 0, st>>>(P);
   e = cudaGetLastError();
   trace_after(st);
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_block_priority (fold launch)");
