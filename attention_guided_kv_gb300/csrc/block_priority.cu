@@ -163,7 +163,8 @@ __device__ __forceinline__ void bp_block_out(const BpParams& P, long long g, int
 // are one contiguous run of the CSR array (requests lie back to back): the warp loads, updates and
 // writes that run back coalesced through its shared-memory buffer, then each lane folds its own
 // block from there (a warp per block would have at most one block's 64..128 bytes in flight).
-// The mean sums the block in token order, the top-p mean takes the maximum k times.
+// The mean sums the block's scores in the lane's (rotated) visiting order, the top-p mean takes the
+// maximum k times.
 constexpr int kBpFoldThreads = 256;
 __device__ __forceinline__ void bp_fold_lanes(const BpParams& P, long long N, float* hslot) {
   __shared__ float sbuf[kBpFoldThreads / 32][32 * 32];
@@ -190,11 +191,16 @@ __device__ __forceinline__ void bp_fold_lanes(const BpParams& P, long long N, fl
     float sum = 0.f, mx = -INFINITY;
     int hot = 0;
     const int rel = int(t0 - T0);
+    // each lane visits its block's tokens rotated by its lane index, so that lanes whose blocks
+    // start a multiple of 32 words apart read different banks (the fold does not depend on order)
+    const int rot = n > 0 ? lane % n : 0;
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
       v[t] = -INFINITY;
       if (t < n) {
-        const float s = buf[rel + t];
+        int q = t + rot;
+        if (q >= n) q -= n;
+        const float s = buf[rel + q];
         v[t] = s;
         sum += s;
         mx = fmaxf(mx, s);
