@@ -480,6 +480,11 @@ KVSEL_API kvsel_status kvsel_block_priority_ex(float* token_scores, const float*
  *   scores_out    fp32 [batch][max_len] or NULL: I (entries >= S_b untouched).
  *   workspace     >= kvsel_sparse_decode_workspace(kv, batch, max_len, top_k,
  *                 scores_out != NULL) bytes, status word zeroed.
+ * Launches: the indexer; the top-k (one 8-CTA thread-block cluster of 1024
+ * threads per sequence when max_len <= 262144, 16K-position slices and a
+ * final CTA per sequence above that); the attention (the splits of a
+ * (sequence, kv head) one cluster).  Each may start while its predecessor
+ * finishes and waits for it before reading its results.
  */
 KVSEL_API size_t kvsel_sparse_decode_workspace(const kvsel_paged_kv* kv, int batch, int max_len,
                                                int top_k, int with_scores_out);
