@@ -151,6 +151,37 @@ def test_rows_longer_than_the_select_cluster(negative):
     assert K.read_status(st.ws) == 0
 
 
+def test_mixed_lengths_in_one_batch():
+    """Rows of different lengths in one call: below, at and just above top_k (the select-all path
+    and the cluster select side by side), a short row and long ones; each row checked against the
+    oracle on its own prefix."""
+    wl = workloads.sparse_decode(seed=28, B=6, S0=9000, steps=1, Hq=16, Hkv=2, top_k=2048)
+    lens = np.array([9000, 2046, 2047, 2048, 100, 5000])
+    st = SparseState(wl)
+    st.seq.copy_(torch.from_numpy(lens.astype(np.int32)))
+    st.step(0)
+    torch.cuda.synchronize()
+    st.guards.check()
+    assert st.seq.cpu().tolist() == (lens + 1).tolist()
+    scores = st.scores.cpu().numpy()
+    topk = st.topk.cpu().numpy()
+    out = st.out.double().cpu().numpy()
+    for b in range(wl.B):
+        n0 = int(lens[b])
+        S = n0 + 1
+        Kb = np.concatenate([bf16_bits_to_f64(wl.K[b][:, :n0]), bf16_bits_to_f64(wl.k_new[0, b])[:, None]], axis=1)
+        Vb = np.concatenate([bf16_bits_to_f64(wl.V[b][:, :n0]), bf16_bits_to_f64(wl.v_new[0, b])[:, None]], axis=1)
+        ki = np.concatenate([bf16_bits_to_f64(wl.k_idx[b][:n0]), bf16_bits_to_f64(wl.k_idx_new[0, b])[None]], axis=0)
+        I = dsa.indexer_scores(bf16_bits_to_f64(wl.q_idx[0, b]), wl.w_idx[0, b].astype(np.float64), ki)
+        assert rel_l2(scores[b, :S], I) < TOL
+        sel = dsa.select_topk(scores[b, :S].astype(np.float32), wl.top_k)
+        np.testing.assert_array_equal(topk[b, :len(sel)], sel)
+        assert (topk[b, len(sel):] == -1).all()
+        o = dsa.masked_attention(bf16_bits_to_f64(wl.q[0, b]), Kb, Vb, sel, wl.scale)
+        assert rel_l2(out[b], o) < TOL
+    assert K.read_status(st.ws) == 0
+
+
 def test_short_context_selects_all_and_matches_dense():
     wl = workloads.sparse_decode(seed=15, B=3, S0=300, steps=1, top_k=2048)
     st = SparseState(wl)
