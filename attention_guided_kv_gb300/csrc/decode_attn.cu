@@ -990,7 +990,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
       float* oacc = P.oacc + (size_t(b) * P.Hq + kvh * G) * kD;
 #pragma unroll 1
       for (int half = 0; half < (kWide ? 2 : 1); ++half) {
-        const int gh = half * kRowG, hn = min(kRowG, G - gh);  // this round's first head, heads
+        const int gh = half * kRowG, hn = min(kRowG, G - gh);  // this merge pass's first head, heads
         if (g < hn) {
           float* dst = wo + (warp * kRowG + g) * kD;
 #pragma unroll
