@@ -42,9 +42,9 @@ PAGE = 16
 
 
 
-# DRAM bytes (read + write) of one decode_step launch at batch 8 x 32K, from one ncu full-set
+# DRAM bytes (read + write) of one decode_step launch at batch 8 x 32K, from one ncu DRAM-counter
 # capture of this kernel (summarised under profiles/); set to None whenever the kernel changes.
-DECODE_STEP_TRAFFIC = 1.142554e9
+DECODE_STEP_TRAFFIC = 1.141956e9
 
 TRACE_EVERY = 8   # launch tracing on one timed step in eight: events between kernels cost time
 
