@@ -247,6 +247,15 @@ def test_quest_host_validation(lib):
     assert lib.kvsel_quest_page_meta(ctypes.byref(kv), 16, 64, 16, 2, None, 256, None) == K.KVSEL_ERR_INVALID_ARG
 
 
+def test_link_reset_host_validation(lib):
+    # every check happens on the host, before anything is enqueued
+    assert lib.kvsel_h2o_link_reset(None, 2, 8, None) == K.KVSEL_ERR_INVALID_ARG
+    assert lib.kvsel_h2o_link_reset(256 + 16, 2, 8, None) == K.KVSEL_ERR_INVALID_ARG    # misaligned
+    assert b"256-byte aligned" in lib.kvsel_last_error_string()
+    assert lib.kvsel_h2o_link_reset(256, 0, 8, None) == K.KVSEL_ERR_INVALID_ARG
+    assert lib.kvsel_h2o_link_reset(256, 2, 0, None) == K.KVSEL_ERR_INVALID_ARG
+
+
 def test_wait_limit_host_validation(lib):
     assert lib.kvsel_set_wait_limit(None, 100, None) == K.KVSEL_ERR_INVALID_ARG
     assert lib.kvsel_set_wait_limit(16, 100, None) == K.KVSEL_ERR_INVALID_ARG     # misaligned workspace
