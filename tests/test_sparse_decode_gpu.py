@@ -223,6 +223,18 @@ def test_group_sizes_and_bf16_output(G):
     _check(st, 0)
 
 
+def test_sixteen_heads_on_256_token_pages():
+    """Both widenings at once: 16 q heads per kv head (heads g + 8 in the wide tile's rows 8..15)
+    gathering rows out of 256-token pool pages, across an append that opens a new page."""
+    wl = workloads.sparse_decode(seed=29, B=2, S0=4094, steps=3, Hq=32, Hkv=2, top_k=700, page=256)
+    st = SparseState(wl)
+    for t in range(3):
+        st.step(t)
+        _check(st, t)
+    assert st.seq.cpu().tolist() == [4097, 4097]
+    assert K.read_status(st.ws) == 0
+
+
 @pytest.mark.slow
 def test_full_size_70b_128k_sampled():
     """Batch 4 x 128K, 70B shape, indexer 4 x 64, top-2048: sampled heads vs the oracle."""
