@@ -429,7 +429,10 @@ def cuda_arm(args, rank, world):
         e2e_step(i, j)
         ev_dec[j % ring].record(stream)
         if j + 1 < e2e_steps:             # step j+1's q, k_new, v_new
-            cs_up.wait_event(ev_dec[j % ring])
+            # into the buffer decode j-1 read (done once that decode is), so the copy runs during
+            # decode j and is in place before select j, which the stream holds until it is
+            if j >= 1:
+                cs_up.wait_event(ev_dec[(j - 1) % ring])
             with torch.cuda.stream(cs_up):
                 d_in[(j + 1) % 2].copy_(h_in[(i + 1) % T], non_blocking=True)
             ev_up[(j + 1) % ring].record(cs_up)
