@@ -485,6 +485,9 @@ KVSEL_API kvsel_status kvsel_block_priority_ex(float* token_scores, const float*
  * final CTA per sequence above that); the attention (the splits of a
  * (sequence, kv head) one cluster).  Each may start while its predecessor
  * finishes and waits for it before reading its results.
+ * CUDA graphs: do not capture this call.  Captured with its input and output
+ * copies and replayed, these launches have ended in an illegal memory access
+ * whose cause is not known; called on a stream, they have not.
  */
 KVSEL_API size_t kvsel_sparse_decode_workspace(const kvsel_paged_kv* kv, int batch, int max_len,
                                                int top_k, int with_scores_out);
