@@ -742,6 +742,55 @@ def _setup_block_priority(dev, small=False):
                         "l2": "~9 MB of token scores per pass (fits in L2): latency-bound"})
 
 
+class _Rt:
+    """The CUDA runtime that torch has loaded, called through ctypes for a loop's per-step copies
+    and event operations: torch's Python wrappers cost several microseconds of host time a call,
+    more than a short step leaves.  `ok` is False where the library cannot be found."""
+
+    def __init__(self, dev):
+        import ctypes
+        self.lib = None
+        for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+            try:
+                self.lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        self.ok = self.lib is not None
+        if not self.ok:
+            return
+        vp = ctypes.c_void_p
+        L = self.lib
+        L.cudaSetDevice.argtypes = [ctypes.c_int]
+        L.cudaMemcpyAsync.argtypes = [vp, vp, ctypes.c_size_t, ctypes.c_int, vp]
+        L.cudaEventRecord.argtypes = [vp, vp]
+        L.cudaStreamWaitEvent.argtypes = [vp, vp, ctypes.c_uint]
+        L.cudaEventCreateWithFlags.argtypes = [ctypes.POINTER(vp), ctypes.c_uint]
+        L.cudaEventDestroy.argtypes = [vp]
+        for f in (L.cudaSetDevice, L.cudaMemcpyAsync, L.cudaEventRecord, L.cudaStreamWaitEvent,
+                  L.cudaEventCreateWithFlags, L.cudaEventDestroy):
+            f.restype = ctypes.c_int
+        self.check(L.cudaSetDevice(dev.index or 0), "cudaSetDevice")
+
+    @staticmethod
+    def check(code, what):
+        if code != 0:
+            raise RuntimeError(f"{what}: CUDA error {code}")
+
+    def events(self, n):
+        import ctypes
+        out = []
+        for _ in range(n):
+            h = ctypes.c_void_p()
+            self.check(self.lib.cudaEventCreateWithFlags(ctypes.byref(h), 2), "cudaEventCreateWithFlags")  # no timing
+            out.append(h)
+        return out
+
+    def destroy(self, evs):
+        for h in evs:
+            self.check(self.lib.cudaEventDestroy(h), "cudaEventDestroy")
+
+
 def _setup_sparse_decode(dev, small=False):
     import numpy as np
     import torch
@@ -807,12 +856,132 @@ def _setup_sparse_decode(dev, small=False):
         K.kvsel_quest_decode(kv, bt, seq_q, q[t], meta, out_q, ws_q, budget_pages=budget_pages, k_new=kn[t],
                              v_new=vn[t])
 
+    # ---- end to end: one packed upload of a step's six inputs, one packed download of its O and
+    # top-k positions, on two side streams.  Inputs are double-buffered and results
+    # triple-buffered on the device; the events that order them sit between steps (the three
+    # launches of a step come from one call).  Argument lists are marshalled once per buffer.
+    def al(n):
+        return (n + 255) // 256 * 256
+    parts = [("q", q), ("q_idx", qi), ("w_idx", wi), ("k_new", kn), ("v_new", vn), ("k_idx_new", kin)]
+    offs, in_bytes = {}, 0
+    for nm, t in parts:
+        offs[nm] = in_bytes
+        in_bytes += al(t[0].numel() * t.element_size())
+    h_in = torch.zeros((wl.steps, in_bytes), dtype=torch.uint8, pin_memory=True)
+    for nm, t in parts:
+        nb = t[0].numel() * t.element_size()
+        h_in[:, offs[nm]:offs[nm] + nb].copy_(t.reshape(wl.steps, -1).view(torch.uint8).cpu())
+    out_bytes = out.numel() * out.element_size()
+    topk_off = al(out_bytes)
+    res_bytes = topk_off + topk.numel() * 4
+    h_res = torch.empty((res_bytes,), dtype=torch.uint8, pin_memory=True)
+    d_in = [torch.empty((in_bytes,), dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_res = [torch.empty((res_bytes,), dtype=torch.uint8, device=dev) for _ in range(3)]
+    e2e_args = {}
+    for bi in range(2):
+        a = d_in[bi].data_ptr()
+        pv = {nm: ctypes.c_void_p(a + o) for nm, o in offs.items()}
+        for ro in range(3):
+            r0 = d_res[ro].data_ptr()
+            e2e_args[bi, ro] = (fixed["kv"], fixed["bt"], fixed["mp"], fixed["seq"], fixed["B"], pv["q"],
+                                pv["k_new"], pv["v_new"], pv["q_idx"], pv["w_idx"], fixed["idx_k"], pv["k_idx_new"],
+                                wl.Hi, wl.Di, wl.max_len, wl.top_k, float(wl.scale), ctypes.c_void_p(r0),
+                                K.KVSEL_BF16, ctypes.c_void_p(r0 + topk_off), None, fixed["ws"], fixed["wsb"],
+                                ctypes.c_void_p(Sc.cuda_stream))
+
+    rt = _Rt(dev)
+
+    def e2e_rt(base, n, cs_up, cs_down, ring):  # the loop below, its copies and events through ctypes
+        L, vp = rt.lib, ctypes.c_void_p
+        evs = rt.events(3 * ring)
+        ev_step, ev_up, ev_down = evs[:ring], evs[ring:2 * ring], evs[2 * ring:]
+        sC, sU, sD = vp(Sc.cuda_stream), vp(cs_up.cuda_stream), vp(cs_down.cuda_stream)
+        hin0, hres = h_in.data_ptr(), vp(h_res.data_ptr())
+        din = [vp(t.data_ptr()) for t in d_in]
+        dres = [vp(t.data_ptr()) for t in d_res]
+        rec, wait, cp = L.cudaEventRecord, L.cudaStreamWaitEvent, L.cudaMemcpyAsync
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(Sc)
+        cs_up.wait_event(e0)
+        err = cp(din[0], vp(hin0 + (base % wl.steps) * in_bytes), in_bytes, 1, sU)
+        err |= rec(ev_up[0], sU) | wait(sC, ev_up[0], 0)
+        for j in range(n):
+            i = base + j
+            if i % wl.steps == 0 and i > 0:
+                seq.copy_(seq0)             # replay the 64-step window from 128K again
+            code = call(*e2e_args[j % 2, j % 3])
+            if code != K.KVSEL_OK:
+                raise RuntimeError(f"kvsel_sparse_decode: status {code}")
+            err |= rec(ev_step[j % ring], sC)
+            if j + 1 < n:                   # step j+1's inputs, into the buffer step j-1 read
+                if j >= 1:
+                    err |= wait(sU, ev_step[(j - 1) % ring], 0)
+                err |= cp(din[(j + 1) % 2], vp(hin0 + ((i + 1) % wl.steps) * in_bytes), in_bytes, 1, sU)
+                err |= rec(ev_up[(j + 1) % ring], sU) | wait(sC, ev_up[(j + 1) % ring], 0)
+            err |= wait(sD, ev_step[j % ring], 0)   # step j's O and top-k down
+            err |= cp(hres, dres[j % 3], res_bytes, 2, sD) | rec(ev_down[j % ring], sD)
+            if j >= 2:
+                err |= wait(sC, ev_down[(j - 2) % ring], 0)  # result buffer (j + 1) % 3 is free again
+            if err:
+                raise RuntimeError(f"end-to-end loop: CUDA error {err} at step {j}")
+        err = wait(sC, ev_down[(n - 1) % ring], 0)
+        e1.record(Sc)
+        torch.cuda.synchronize()
+        rt.check(err, "cudaStreamWaitEvent")
+        rt.destroy(evs)
+        return e0.elapsed_time(e1), in_bytes, res_bytes
+
+    def e2e(base, n):
+        cs_up, cs_down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ring = 4
+        if rt.ok:
+            return e2e_rt(base, n, cs_up, cs_down, ring)
+        ev_step = [torch.cuda.Event() for _ in range(ring)]
+        ev_up = [torch.cuda.Event() for _ in range(ring)]
+        ev_down = [torch.cuda.Event() for _ in range(ring)]
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(Sc)
+        cs_up.wait_event(e0)
+        with torch.cuda.stream(cs_up):
+            d_in[0].copy_(h_in[base % wl.steps], non_blocking=True)
+        ev_up[0].record(cs_up)
+        Sc.wait_event(ev_up[0])
+        for j in range(n):
+            i = base + j
+            if i % wl.steps == 0 and i > 0:
+                seq.copy_(seq0)             # replay the 64-step window from 128K again
+            code = call(*e2e_args[j % 2, j % 3])
+            if code != K.KVSEL_OK:
+                raise RuntimeError(f"kvsel_sparse_decode: status {code}")
+            ev_step[j % ring].record(Sc)
+            if j + 1 < n:                   # step j+1's inputs, into the buffer step j-1 read
+                if j >= 1:
+                    cs_up.wait_event(ev_step[(j - 1) % ring])
+                with torch.cuda.stream(cs_up):
+                    d_in[(j + 1) % 2].copy_(h_in[(i + 1) % wl.steps], non_blocking=True)
+                ev_up[(j + 1) % ring].record(cs_up)
+                Sc.wait_event(ev_up[(j + 1) % ring])
+            cs_down.wait_event(ev_step[j % ring])   # step j's O and top-k down
+            with torch.cuda.stream(cs_down):
+                h_res.copy_(d_res[j % 3], non_blocking=True)
+            ev_down[j % ring].record(cs_down)
+            if j >= 2:
+                Sc.wait_event(ev_down[(j - 2) % ring])  # result buffer (j + 1) % 3 is free again
+        Sc.wait_event(ev_down[(n - 1) % ring])
+        e1.record(Sc)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), in_bytes, res_bytes
+
     S = wl.S0 + wl.steps // 2
     byts = {"sd_index": wl.B * S * (wl.Di * 2 + 4), "sd_attn": wl.B * wl.top_k * wl.Hkv * 512,
             "sd_select": wl.B * S * 4}
     host_in = [("q", q), ("q_idx", qi), ("w_idx", wi), ("k_new", kn), ("v_new", vn), ("k_idx_new", kin)]
     return dict(step=step, run=run, host_in=host_in, outs=[out, topk], ws=[ws, ws_q], bytes=byts, flops={},
-                per_step_launches=3, steps_cycle=wl.steps, e2e_graph=False,
+                per_step_launches=3, steps_cycle=wl.steps, e2e_graph=False, e2e=e2e,
+                e2e_launch=("C ABI called eagerly, copies overlapped on side streams"
+                            + ("; copies and events through the CUDA runtime" if rt.ok else "")),
                 variant_runs=[(f"quest_{budget_pages}_pages_per_head", quest)], variants_key="variants_us_per_step",
                 config={"batch": wl.B, "context": wl.S0, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
                         "indexer": f"{wl.Hi} x {wl.Di}", "top_k": wl.top_k,
@@ -1010,7 +1179,10 @@ def other_workload(args, rank, world):
     # and runs its steps eagerly.
     cap = cyc or 64
     e2e_graph = None
-    if S.get("e2e_graph", True) and not args.no_graph:
+    e2e_own = None
+    if S.get("e2e") is not None:  # the workload's own loop (packed copies overlapped with the steps)
+        e2e_own = S["e2e"](base, steps)
+    elif S.get("e2e_graph", True) and not args.no_graph:
         gr = torch.cuda.CUDAGraph()
         torch.cuda.synchronize()
         with torch.cuda.graph(gr):
@@ -1021,7 +1193,10 @@ def other_workload(args, rank, world):
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    if e2e_graph is not None:
+    if e2e_own is not None:
+        e2e_n = steps
+        e2e_ms, h2d, d2h = e2e_own
+    elif e2e_graph is not None:
         reps = max(1, steps // cap)
         for _ in range(reps):
             e2e_graph.replay()
@@ -1031,7 +1206,10 @@ def other_workload(args, rank, world):
         e2e_n = steps
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = slowest_rank(f0.elapsed_time(f1), world, dev)
+    if e2e_own is not None:
+        e2e_ms = slowest_rank(e2e_ms, world, dev)
+    else:
+        e2e_ms = slowest_rank(f0.elapsed_time(f1), world, dev)
     variants = None
     if S.get("variant_runs"):
         variants = {}
@@ -1127,7 +1305,8 @@ def other_workload(args, rank, world):
             "kernel_ms": kern_ms, "roofline": roof,
             "e2e": {"value": job_rate(world, e2e_n, e2e_ms), "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_n,
-                    "launch": (f"CUDA graph of {cap} steps (copies and launches), replayed"
+                    "launch": (S["e2e_launch"] if e2e_own is not None else
+                               f"CUDA graph of {cap} steps (copies and launches), replayed"
                                if e2e_graph is not None else "eager")},
             "gpu_launches": per_step_launches * steps, "clocks": clocks.summary(tw0, tw1)}
     if eager_ms is not None:
