@@ -22,8 +22,9 @@
 //                     block's tokens (written back) and the fold.
 //   bp_rank_kernel    one CTA per request (percentile only): stable radix sort
 //                     of the request's scores with block indices (up to 8192
-//                     blocks; a register bitonic sort above that); the rank
-//                     gives the percentile key of each block.
+//                     blocks; a register bitonic sort up to 16384; above that
+//                     the same radix sort through global memory, 8192 keys a
+//                     tile); the rank gives the percentile key of each block.
 //   bp_sort_kernel    cooperative: stable LSD radix sort of the N 32-bit keys
 //                     (4-bit digits, 8 passes, two bounded grid barriers per
 //                     pass; the 16 digit offsets of a CTA are scanned at once).  The input is in (request, block) order and the
@@ -35,7 +36,8 @@
 namespace kvsel {
 
 constexpr int kBpMaxBlockSize = 256;          // tokens per block: the pages' 16..256
-constexpr int kBpMaxReqBlocks = 16384;        // blocks per request (shared-memory rank sort)
+constexpr int kBpMaxReqBlocks = 1 << 30;      // blocks per request: a block index fits the order code
+constexpr int kBpSharedRankMax = 16384;       // blocks per request ranked in shared memory
 constexpr int kBpSortThreads = 256;
 constexpr int kBpMaxSortCtas = 256;
 
@@ -512,6 +514,152 @@ __device__ __forceinline__ void bp_rank_radix(RankRadixSmem& sm, int n, long lon
   }
 }
 
+// Requests above kBpSharedRankMax blocks: the same stable LSD radix sort (8-bit digits, 4
+// passes), its keys and block indices ping-ponging through the request's own segments of the
+// workspace key / value arrays (the global sort only uses them afterwards).  A pass first counts
+// every digit over the request, then visits the request in tiles of 8192 keys in order; inside a
+// tile the keys are ranked among equal digits exactly as in bp_rank_radix, and a key goes to its
+// digit's next free slot plus its rank among that digit's keys in the tile.  Tiles in order and
+// ranks in index order keep the sort stable.
+struct RankGlobalSmem {
+  uint32_t hist[32 * kRankHistPitch];  // [warp][digit], padded; slot 256 takes the tail's empty lanes
+  uint32_t wsum[32];
+  uint32_t run[256];                   // the next output slot of each digit
+  uint32_t tstart[257];                // the tile's first slot of each digit; [256]: its keys
+};
+__device__ __forceinline__ void bp_rank_global(RankGlobalSmem& sm, int n, long long b0, int r, const BpParams& P) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+  uint32_t* kb[2] = {P.key[0] + b0, P.key[1] + b0};
+  int64_t* vb[2] = {P.val[0] + b0, P.val[1] + b0};
+  const int tiles = (n + kRankRadixMax - 1) / kRankRadixMax;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 8 * pass;
+    const int dstb = (pass & 1) ^ 1, srcb = pass & 1;  // pass 0 reads the scores: 1, 0, 1, 0
+    auto key_at = [&](int i) -> uint32_t { return pass == 0 ? order_key(P.bscore[b0 + i]) : kb[srcb][i]; };
+    auto val_at = [&](int i) -> uint32_t { return pass == 0 ? uint32_t(i) : uint32_t(vb[srcb][i]); };
+    // every digit's count over the request, then each digit's first slot
+    if (tid < 256) sm.run[tid] = 0u;
+    __syncthreads();
+    for (int i0 = warp * 32; i0 < n; i0 += 1024) {  // lanes with the same digit add once
+      const int i = i0 + lane;
+      const uint32_t d = i < n ? (key_at(i) >> shift) & 255u : 256u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      if (d < 256u && lane == __ffs(peers) - 1) atomicAdd(&sm.run[d], uint32_t(__popc(peers)));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t c[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sm.run[lane * 8 + j];
+        tot += c[j];
+      }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t base = incl - tot;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sm.run[lane * 8 + j] = base;
+        base += c[j];
+      }
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int t = 0; t < tiles; ++t) {
+      const int t0 = t * kRankRadixMax;
+      for (int j = tid; j < 32 * kRankHistPitch; j += 1024) sm.hist[j] = 0u;
+      __syncthreads();
+      uint32_t k[8], v[8], pos[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = t0 + warp * 256 + e * 32 + lane;
+        const bool ok = i < n;
+        k[e] = ok ? key_at(i) : 0u;
+        v[e] = ok ? val_at(i) : 0u;
+        const uint32_t d = ok ? (k[e] >> shift) & 255u : 256u;  // past the end: the unused slot 256
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        const int leader = __ffs(peers) - 1;
+        uint32_t old = 0;
+        if (lane == leader) {
+          old = sm.hist[warp * kRankHistPitch + d];
+          sm.hist[warp * kRankHistPitch + d] = old + __popc(peers);
+        }
+        pos[e] = __shfl_sync(0xffffffffu, old, leader) + __popc(peers & lt);
+      }
+      __syncthreads();
+      {  // exclusive scan of the tile's 8192 counts in (digit, warp) order: 8 per thread
+        auto at = [&](int q) -> uint32_t& { return sm.hist[(q & 31) * kRankHistPitch + (q >> 5)]; };
+        uint32_t c[8], run = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = at(tid * 8 + j);
+          run += c[j];
+        }
+        uint32_t incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane == 31) sm.wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+          const uint32_t tw = sm.wsum[lane];
+          uint32_t x = tw;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+          }
+          sm.wsum[lane] = x - tw;
+        }
+        __syncthreads();
+        uint32_t base = sm.wsum[warp] + incl - run;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          at(tid * 8 + j) = base;
+          base += c[j];
+        }
+      }
+      __syncthreads();
+      if (tid < 256) sm.tstart[tid] = sm.hist[tid];  // warp 0's column: where digit tid starts in the tile
+      if (tid == 0) sm.tstart[256] = uint32_t(min(kRankRadixMax, n - t0));
+      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = t0 + warp * 256 + e * 32 + lane;
+        if (i < n) {
+          const uint32_t d = (k[e] >> shift) & 255u;
+          const uint32_t dst = sm.run[d] + sm.hist[warp * kRankHistPitch + d] + pos[e] - sm.tstart[d];
+          kb[dstb][dst] = k[e];
+          vb[dstb][dst] = v[e];
+        }
+      }
+      __syncthreads();
+      if (tid < 256) sm.run[tid] += sm.tstart[tid + 1] - sm.tstart[tid];  // the digit's keys in this tile
+      __syncthreads();
+    }
+  }
+  // buffer 0 holds the blocks in rank order: their indices move to key buffer 1 before buffer 0
+  // is overwritten with the percentile keys
+  for (int i = tid; i < n; i += 1024) kb[1][i] = uint32_t(vb[0][i]);
+  __syncthreads();
+  for (int i = tid; i < n; i += 1024) {
+    const unsigned blk = kb[1][i];
+    const float pct = __fdiv_rn(__ll2float_rn(2LL * i + 1), __ll2float_rn(2LL * n));  // correctly rounded
+    const bool hot_block = P.agg == kAggAllCold && P.bscore[b0 + blk] >= P.threshold;
+    P.key[0][b0 + blk] = hot_block ? 0xFFFFFFFFu : __float_as_uint(pct);
+    P.val[0][b0 + blk] = ((long long)r << 32) | blk;
+  }
+}
+
 __global__ void __launch_bounds__(1024) bp_rank_kernel(const BpParams P) {
   extern __shared__ unsigned long long skeys[];
   if (P.meta[0] <= 0) return;
@@ -521,6 +669,10 @@ __global__ void __launch_bounds__(1024) bp_rank_kernel(const BpParams P) {
   if (n == 0) return;
   if (n <= kRankRadixMax) {
     bp_rank_radix(*reinterpret_cast<RankRadixSmem*>(skeys), n, b0, r, P);
+    return;
+  }
+  if (n > kBpSharedRankMax) {
+    bp_rank_global(*reinterpret_cast<RankGlobalSmem*>(skeys), n, b0, r, P);
     return;
   }
   int npow = 1;
@@ -832,7 +984,8 @@ extern "C" kvsel_status kvsel_block_priority_ex(float* token_scores, const float
   if (e != cudaSuccess) return cuda_fail(e, "kvsel_block_priority (fold launch)");
 
   if (norm == KVSEL_NORM_PERCENTILE) {
-    const size_t smem = std::max(size_t(kBpMaxReqBlocks) * 8, sizeof(RankRadixSmem));
+    const size_t smem =
+        std::max(std::max(size_t(kBpSharedRankMax) * 8, sizeof(RankRadixSmem)), sizeof(RankGlobalSmem));
     static bool attr_set = false;
     if (!attr_set) {
       e = cudaFuncSetAttribute(bp_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));

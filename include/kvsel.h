@@ -378,7 +378,11 @@ KVSEL_API kvsel_status kvsel_kv_compact(const kvsel_paged_kv* kv, int32_t* block
  *   token_scores  fp32 [total tokens], requests laid out back to back (CSR).
  *   increment     fp32, same layout, or NULL (no update).
  *   req_offsets   int64 [num_requests + 1] token offsets, non-decreasing.
- *   block_size    1..256 tokens; at most 16384 blocks per request.
+ *   block_size    1..256 tokens; at most 2^30 blocks per request.  With the
+ *                 percentile, requests of up to 16384 blocks are ranked in
+ *                 shared memory, larger ones by one CTA sorting the request
+ *                 through the workspace (about 12 us per 8192 blocks and
+ *                 digit pass, four passes: meant for token-level blocks).
  *   agg           KVSEL_AGG_MAX / _MEAN / _TOPP;  norm  KVSEL_NORM_*.
  *   block_score_out  fp32 [max_total_blocks] or NULL: block scores in
  *                 (request, block) order.
@@ -388,7 +392,7 @@ KVSEL_API kvsel_status kvsel_kv_compact(const kvsel_paged_kv* kv, int32_t* block
  *   n_out         int64 [2]: the evict count and N (-1 if the lengths were
  *                 rejected on the device).
  * Device-detected problems: N > max_total_blocks or a negative length ->
- * KVSEL_ERR_BAD_INDEX; more than 16384 blocks in one request ->
+ * KVSEL_ERR_BAD_INDEX; more than 2^30 blocks in one request ->
  * KVSEL_ERR_UNSUPPORTED; in both cases nothing else is computed.
  */
 typedef enum kvsel_block_agg {

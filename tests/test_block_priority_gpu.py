@@ -96,10 +96,11 @@ def test_max_aggregation_order_is_exact_end_to_end(norm):
     np.testing.assert_array_equal(order, want)
 
 
-@pytest.mark.parametrize("nblocks", [8192, 8193, 12500, 16384])
+@pytest.mark.parametrize("nblocks", [8192, 8193, 12500, 16384, 16385, 24576, 40000])
 def test_percentile_ranks_at_and_above_8192_blocks(nblocks):
-    """Requests of up to 8192 blocks are ranked by the shared-memory radix sort,
-    larger ones by the register bitonic sort: both must give the oracle's order."""
+    """Requests of up to 8192 blocks are ranked by the shared-memory radix sort, up to 16384 by
+    the register bitonic sort and above that by the radix sort through the workspace (whole
+    tiles, a ragged last tile): all must give the oracle's order."""
     rng = np.random.default_rng(nblocks)
     lens = np.array([nblocks * 16 - 7, 300, nblocks * 16], dtype=np.int64)
     off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
@@ -229,5 +230,20 @@ def test_threshold_policies_exact(agg, norm, bs):
     thr = 0.75
     blk, order = _run_ex(torch.from_numpy(tok).cuda(), off, bs, agg, norm, 0.4, threshold=thr)
     blocks, _, want = BP.priority_pass(tok.astype(np.float64), off, bs, agg, 0.1, norm, 0.4, threshold=thr)
+    np.testing.assert_array_equal(blk, np.concatenate(blocks).astype(np.float32))
+    np.testing.assert_array_equal(order, want)
+
+
+@pytest.mark.parametrize("agg", [BP.AGG_MAX, K.KVSEL_AGG_ALL_COLD])
+def test_token_level_blocks_of_long_requests(agg):
+    """Block size 1 turns every token into a block: requests of 100K and 70K tokens rank through
+    the workspace sort (13 and 9 tiles), with thousands of tied scores, next to short ones."""
+    rng = np.random.default_rng(17 + agg)
+    lens = np.array([100000, 5, 70001, 0, 3000], dtype=np.int64)
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    tok = (rng.integers(0, 300, int(off[-1])) * 0.125).astype(np.float32)   # exact in fp32, tied
+    kw = {"threshold": 30.0} if agg == K.KVSEL_AGG_ALL_COLD else {}
+    blk, order = _run_ex(torch.from_numpy(tok).cuda(), off, 1, agg, BP.NORM_PERCENTILE, 0.3, **kw)
+    blocks, _, want = BP.priority_pass(tok.astype(np.float64), off, 1, agg, 0.1, BP.NORM_PERCENTILE, 0.3, **kw)
     np.testing.assert_array_equal(blk, np.concatenate(blocks).astype(np.float32))
     np.testing.assert_array_equal(order, want)
