@@ -330,18 +330,24 @@ def cuda_arm(args, rank, world):
         if world > 1:
             dist.barrier()
 
-    # warm-up
-    for i in range(args.warmup):
-        dev_step(i)
-    torch.cuda.synchronize()
-    st0, st1 = K.read_status(ws), K.read_status(ws_ev)
-    if st0 or st1:
-        raise RuntimeError(f"device status after warm-up: {st0} {st1}")
-
+    # the clock sampler starts (and settles) before the warm-up, so that the warm-up steps run
+    # right before the timed ones with no idle gap between them
     gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
     clocks = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid)
     clocks.start()
     time.sleep(0.3)
+
+    # warm-up
+    try:
+        for i in range(args.warmup):
+            dev_step(i)
+        torch.cuda.synchronize()
+        st0, st1 = K.read_status(ws), K.read_status(ws_ev)
+        if st0 or st1:
+            raise RuntimeError(f"device status after warm-up: {st0} {st1}")
+    except BaseException:
+        clocks.stop()
+        raise
 
     # ---- timed region (device-resident inputs) ----
     barrier()
@@ -1106,17 +1112,22 @@ def other_workload(args, rank, world):
     S = SETUPS[args.workload](dev, small=args.small)
     stream = torch.cuda.current_stream()
     steps = args.steps
-    for i in range(args.warmup):
-        S["step"](i)
-    torch.cuda.synchronize()
-    for w in S["ws"]:
-        st = K.read_status(w)
-        if st:
-            raise RuntimeError(f"device status after warm-up: {st}")
+    # the clock sampler starts (and settles) before the warm-up: no idle gap before the timed steps
     gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
     clocks = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid)
     clocks.start()
     time.sleep(0.3)
+    try:
+        for i in range(args.warmup):
+            S["step"](i)
+        torch.cuda.synchronize()
+        for w in S["ws"]:
+            st = K.read_status(w)
+            if st:
+                raise RuntimeError(f"device status after warm-up: {st}")
+    except BaseException:
+        clocks.stop()
+        raise
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
