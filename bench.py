@@ -906,6 +906,15 @@ def _setup_sparse_decode(dev, small=False):
         din = [vp(t.data_ptr()) for t in d_in]
         dres = [vp(t.data_ptr()) for t in d_res]
         rec, wait, cp = L.cudaEventRecord, L.cudaStreamWaitEvent, L.cudaMemcpyAsync
+        try:
+            return e2e_rt_loop(base, n, cs_up, ring, ev_step, ev_up, ev_down, sC, sU, sD, hin0, hres, din, dres,
+                               rec, wait, cp)
+        finally:
+            torch.cuda.synchronize()
+            rt.destroy(evs)
+
+    def e2e_rt_loop(base, n, cs_up, ring, ev_step, ev_up, ev_down, sC, sU, sD, hin0, hres, din, dres, rec, wait, cp):
+        vp = ctypes.c_void_p
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(Sc)
@@ -935,7 +944,6 @@ def _setup_sparse_decode(dev, small=False):
         e1.record(Sc)
         torch.cuda.synchronize()
         rt.check(err, "cudaStreamWaitEvent")
-        rt.destroy(evs)
         return e0.elapsed_time(e1), in_bytes, res_bytes
 
     def e2e(base, n):
