@@ -516,6 +516,8 @@ def cuda_arm(args, rank, world):
         "config": {"workload": CONFIG_NAME, "batch": B, "context": S0, "q_heads": Hq, "kv_heads": Hkv,
                    "head_dim": d, "page": PAGE, "budget": wl.budget, "probs_written": probs is not None,
                    "l2": "inputs larger than L2 (1.07 GB of K/V per step vs 129 MB L2)",
+                   "h2o_scores": ("start at zero and accumulate over the replayed 128-step window; the "
+                                  "first tens of steps hand the select longer candidate lists"),
                    "parallelism": f"replicas x{world}"},
         "effective_kv_gbs": eff_kv_gbs,
         "effective_kv_frac_of_peak": eff_kv_gbs / hbm,
