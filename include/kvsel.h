@@ -21,6 +21,11 @@
  *    window, a workspace that is too small) return immediately with no
  *    launch, and kvsel_last_error_string() describes them.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *  - CUDA graphs: calls of kvsel_decode_attn, kvsel_h2o_evict,
+ *    kvsel_snapkv_select and kvsel_block_priority (with their input and
+ *    output copies) have been captured and replayed; kvsel_sparse_decode
+ *    must not be captured (see its notes); the other entry points have not
+ *    been tried in a graph.
  *  - No C++ exception crosses this interface.
  *
  * Paged KV layout (the paged cache of "From sliding window to
