@@ -23,7 +23,8 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
  *  - CUDA graphs: calls of kvsel_decode_attn, kvsel_h2o_evict,
  *    kvsel_snapkv_select and kvsel_block_priority (with their input and
- *    output copies) have been captured and replayed; kvsel_sparse_decode
+ *    output copies) have been captured and replayed, the first two with
+ *    results identical to the same calls made eagerly; kvsel_sparse_decode
  *    must not be captured (see its notes); the other entry points have not
  *    been tried in a graph.
  *  - No C++ exception crosses this interface.
